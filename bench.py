@@ -1,0 +1,395 @@
+#!/usr/bin/env python
+"""MoE-layer throughput at the Qwen3-30B-A3B shape on GB300, through the C ABI.
+
+One step = one pass of the whole sparse MoE block (router GEMM, softmax / top-k /
+renormalisation, expert histogram + scan + stable permutation, grouped SwiGLU
+experts, weighted un-permute) over one batch of seeded synthetic tokens, as one
+``moe_forward`` call captured in a CUDA graph.  Weights are random-init with the
+model's shapes (no checkpoint); inputs are resident in HBM when timing starts.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle (plain C
+loops in double) on the same workload instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode8|...] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/sec at Qwen3-30B-A3B shape; achieved HBM GB/s vs roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+DESCR = {
+    "tiny": "tiny MoE block fp32: T=16 H=64 E=8 k=2 I=32",
+    "decode8": "Qwen3-30B-A3B MoE layer decode, bf16: T=8 H=2048 E=128 k=8 I=768, norm_topk",
+    "decode64z": "Qwen3-30B-A3B MoE layer decode, bf16, Zipf(1.1) router bias: T=64 H=2048 E=128 k=8 I=768",
+    "decode48q": "Qwen3-30B-A3B MoE layer decode, 4-bit codebook expert weights: T=48 H=2048 E=128 k=8 I=768",
+    "prefill": "Qwen3-30B-A3B MoE layer prefill, bf16: 4 independent layers x T=4096 H=2048 E=128 k=8 I=768",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode8", choices=sorted(DESCR))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region (every 100 ms)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.idx), "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def src_digest(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def layer_inputs(workload):
+    import synth
+    c = synth.WORKLOADS[workload]
+    return [synth.make_inputs(workload, layer=l) for l in range(c["layers"])]
+
+
+def expert_bytes_per_expert(inp):
+    if inp.w == "q4":
+        return 3 * inp.I * inp.H // 2 + 3 * inp.I * inp.H // inp.q_block * 2
+    return 3 * inp.I * inp.H * (4 if inp.w == "f32" else 2)
+
+
+def cpu_baseline(layers, seconds: float):
+    """The oracle as it stands (single-threaded C, double) on a bounded sample of the workload."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    inp = layers[0]
+    # one step of the sample: the whole batch if it is small, else a slice of tokens
+    toks = np.arange(inp.T, dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.forward_tokens(inp, toks[:1])
+    per_tok = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(1, min(inp.T, seconds / per_tok)))
+    reps, done, t0 = 0, 0, time.perf_counter()
+    while True:
+        oracle.forward_tokens(inp, toks[:n])
+        reps += 1
+        done += n
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"oracle.forward_tokens on {n} of the {inp.T} tokens of layer 0, {reps} repetition(s), "
+                      f"{dt:.1f} s single-threaded"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    layers = layer_inputs(args.workload)
+    import numpy as np
+    import oracle
+    oracle.build()
+    inp = layers[0]
+    toks = np.arange(inp.T, dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.forward_tokens(inp, toks[:1])
+    per_tok = max(time.perf_counter() - t0, 1e-4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(inp.T, budget / per_tok)))
+    for _ in range(args.warmup):
+        oracle.forward_tokens(inp, toks[:n])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward_tokens(inp, toks[:n])
+    dt = time.perf_counter() - t0
+    value = args.steps * n / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "tokens_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} of {inp.T} tokens per step through oracle.forward_tokens (C, double, "
+                                   f"single-threaded)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+    import top_routing_grouped_router_gb300 as moe
+    from top_routing_grouped_router_gb300 import build as moe_build
+    from top_routing_grouped_router_gb300.device import upload, to_device
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    moe_build.build()
+    peaks, peak_kind = load_peaks()
+
+    layers = layer_inputs(args.workload)
+    inp0 = layers[0]
+    T, H, E, k, I = inp0.T, inp0.H, inp0.E, inp0.k, inp0.I
+    # enough weight copies that a replay never finds the previous replay's weights in L2
+    per_copy = sum(expert_bytes_per_expert(l) * E for l in layers)
+    n_copies = 1 if per_copy * 0.3 > 2 * L2_BYTES else 3
+    dl = [[upload(l, dev) for l in layers] for _ in range(n_copies)]
+    for c in range(1, n_copies):  # copies share x / router / bias with copy 0 (the same tokens each step)
+        for l in range(len(layers)):
+            dl[c][l].x, dl[c][l].w_router, dl[c][l].b_router = dl[0][l].x, dl[0][l].w_router, dl[0][l].b_router
+    out_dt = dl[0][0].out_dtype()
+    outs = [torch.empty((T, H), dtype=out_dt, device=dev) for _ in layers]
+    wss = [d.new_workspace() for d in dl[0]]
+    stream = torch.cuda.Stream(device=dev)
+
+    def forward(c, st=None):
+        for l, L in enumerate(dl[c]):
+            moe.moe_forward(L.shape, L.x, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4, outs[l],
+                            workspace=wss[l], stream=st)
+
+    with torch.cuda.stream(stream):
+        for c in range(n_copies):
+            forward(c)
+    torch.cuda.synchronize()
+    graphs = []
+    for c in range(n_copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            forward(c)
+        graphs.append(g)
+
+    # active experts (fixed by the seeded tokens) -> algorithmic bytes of the expert kernel
+    counts = []
+    for l, L in enumerate(dl[0]):
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        moe.moe_route(L.shape, L.x, L.w_router, L.b_router, ids, w, workspace=wss[l])
+        counts.append(torch.bincount(ids.view(-1).long(), minlength=E).cpu().numpy())
+    torch.cuda.synchronize()
+    n_active = [int((c > 0).sum()) for c in counts]
+    act_b = 2 if inp0.act == "bf16" else 4
+    grouped_bytes = sum(na * expert_bytes_per_expert(l) + T * H * act_b + T * k * H * act_b
+                        for na, l in zip(n_active, layers))
+    step_bytes = grouped_bytes + sum(E * H * act_b + T * H * act_b for _ in layers)
+    flops = sum(2 * T * H * E + 2 * T * k * 3 * I * H for _ in layers)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            graphs[i % n_copies].replay()
+        # bring the GPU under load before the timed region so the clock samples mean something
+        t_end = time.perf_counter() + 0.5
+        while time.perf_counter() < t_end:
+            for g in graphs:
+                g.replay()
+            stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % n_copies].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    tokens_per_step = T * len(layers)
+    value = world * tokens_per_step * args.steps / (ms_total / 1e3)
+
+    # the dominant kernel (grouped SwiGLU experts) timed alone with events on its stream
+    kt_steps = min(args.steps, 200)
+    ids_b = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in layers]
+    w_b = [torch.empty((T, k), dtype=torch.float32, device=dev) for _ in layers]
+    cnt_b = [torch.empty(E, dtype=torch.int32, device=dev) for _ in layers]
+    off_b = [torch.empty(E + 1, dtype=torch.int32, device=dev) for _ in layers]
+    ord_b = [torch.empty(T * k, dtype=torch.int32, device=dev) for _ in layers]
+    pos_b = [torch.empty(T * k, dtype=torch.int32, device=dev) for _ in layers]
+    y_b = [torch.empty((T * k, H), dtype=out_dt, device=dev) for _ in layers]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kt_steps)]
+    with torch.cuda.stream(stream):
+        for l, L in enumerate(dl[0]):
+            moe.moe_route(L.shape, L.x, L.w_router, L.b_router, ids_b[l], w_b[l], workspace=wss[l], stream=stream)
+            moe.moe_permute(L.shape, ids_b[l], cnt_b[l], off_b[l], ord_b[l], pos_b[l], wss[l], stream=stream)
+        for i in range(kt_steps + 3):
+            c = i % n_copies
+            if i >= 3:
+                kev[i - 3][0].record(stream)
+            for l, L in enumerate(dl[c]):
+                moe.moe_grouped_swiglu(L.shape, dl[0][l].x, off_b[l], ord_b[l], L.w_gate, L.w_up, L.w_down, L.q4,
+                                       y_b[l], wss[l], stream=stream)
+            if i >= 3:
+                kev[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    k_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+
+    # end to end through the public API: pinned host tokens in, host result out, every step
+    x_host = [to_device(l.x, "cpu", pin=True) for l in layers]
+    out_host = [torch.empty((T, H), dtype=out_dt, pin_memory=True) for _ in layers]
+    e2e_steps = min(args.steps, 500)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e2e_steps):
+            for l in range(len(layers)):
+                dl[0][l].x.copy_(x_host[l], non_blocking=True)
+            graphs[i % n_copies].replay()
+            for l in range(len(layers)):
+                out_host[l].copy_(outs[l], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    bi = sum(x.numel() * x.element_size() for x in x_host)
+    bo = sum(o.numel() * o.element_size() for o in out_host)
+
+    launches = sum(moe.moe_forward_launches(L.shape) for L in dl[0])
+    tensor_bound = args.workload == "prefill"
+    if tensor_bound:
+        peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        achieved = flops / (k_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
+    else:
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        achieved = grouped_bytes / (k_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+    roof["kernel"] = "moe_grouped_swiglu (grouped SwiGLU expert kernels)"
+    roof["kernel_ms"] = k_ms
+    roof["algorithmic_bytes"] = grouped_bytes
+    roof["traffic"] = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        tr = json.load(open(tr_path)).get(args.workload)
+        if tr and tr.get("src_digest") == src_digest(tr["sources"]):
+            roof["traffic"] = tr["dram_bytes_per_launch"]
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if inp0.act == "bf16" else "f32",
+        "data": "synthetic: seeded N(0,1) tokens, N(0,1/fan_in) random-init weights of the model's shapes",
+        "config": {"workload": DESCR[args.workload], "T": T, "H": H, "E": E, "k": k, "I": I,
+                   "layers": len(layers), "weights": inp0.w, "active_experts": n_active,
+                   "l2": f"inputs larger than L2: {n_copies} rotating weight cop{'y' if n_copies == 1 else 'ies'} "
+                         f"({n_copies * per_copy / 1e9:.1f} GB), one moe_forward graph per copy",
+                   "step_hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
+                   "step_tflops": flops / (ms_step / 1e3) / 1e12, "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "e2e": {"value": world * tokens_per_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(layers, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

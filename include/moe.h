@@ -1,0 +1,208 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) sparse Mixture-of-Experts block
+ * (Qwen3-MoE style: router, softmax over the E experts, top-k, renormalised
+ * weights, grouped SwiGLU experts, weighted combine back to token order).
+ *
+ * The op sequence is the one the unsloth commit page 80aaf1121b
+ * ("Qwen3-30B-A3B decode ... CUDA-graph capture", paragraph on the grouped_mm
+ * backend) names for the MoE block: expert histogram (bincount, replaced by a
+ * capture-safe scatter_add_), cumsum, argsort, torch._grouped_mm, index_add_.
+ * Here each op is a hand-written CUDA kernel; the whole block runs without a
+ * host synchronisation, so every call below can be captured in a CUDA graph
+ * (the capture failure that page describes came from a host round trip inside
+ * bincount).
+ *
+ * Notation: T tokens, H hidden size, E experts, k experts per token, I expert
+ * intermediate size, A = T*k assignments.  Assignment a = t*k + j is token t's
+ * j-th choice (j = 0 is the largest router logit).  All arrays are row-major
+ * and C-contiguous.
+ *
+ * Conventions shared by every entry point:
+ *  - Every data pointer is a DEVICE pointer owned by the caller; the library
+ *    never allocates, frees or copies to the host, and never synchronises the
+ *    stream (moe_read_device_error excepted).  Work is enqueued on `stream`
+ *    (NULL = the legacy default stream) in stream order; outputs are ready
+ *    when the stream reaches that point.
+ *  - Device pointers must be 16-byte aligned (MOE_ERR_ALIGN otherwise).
+ *  - Arguments are validated on the host before anything is launched; on any
+ *    error nothing is enqueued and the error code is returned.
+ *  - Calls on different streams are independent if they use different
+ *    workspaces and outputs; two calls in flight must not share a workspace.
+ *  - Inconsistent device data (an expert id outside [0, E) given to
+ *    moe_permute) is not trapped: the kernel records MOE_ERR_DEVICE in the
+ *    workspace's error word, skips the bad element and returns.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *moe_stream_t;
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_NULLPTR = -1,    /* a required pointer is NULL */
+    MOE_ERR_SHAPE = -2,      /* sizes outside the supported range (see moe_shape) */
+    MOE_ERR_DTYPE = -3,      /* unsupported activation / weight dtype combination */
+    MOE_ERR_WORKSPACE = -4,  /* workspace NULL or smaller than moe_workspace_size() */
+    MOE_ERR_ALIGN = -5,      /* a device pointer is not 16-byte aligned */
+    MOE_ERR_LAUNCH = -6,     /* the CUDA runtime rejected a launch */
+    MOE_ERR_DEVICE = -7      /* recorded on the device: inconsistent input data */
+};
+
+enum moe_dtype {
+    MOE_DT_F32 = 0,   /* IEEE fp32 */
+    MOE_DT_BF16 = 1,  /* bfloat16 (stored as 16-bit patterns) */
+    MOE_DT_Q4 = 2     /* 4-bit codebook codes + bf16 block scales (expert weights only) */
+};
+
+/*
+ * Problem sizes and formats.
+ *   1 <= E <= 256, 1 <= k <= min(E, 32), 0 <= T <= 2^18, T*k < 2^30,
+ *   H and I positive multiples of 8.
+ * Supported (act_dtype, w_dtype): (F32, F32), (BF16, BF16), (BF16, Q4).
+ *   act_dtype is the dtype of x, the router weight and the output.
+ *   Q4 needs q_block even, dividing both H and I.
+ * norm_topk != 0 renormalises the k selected softmax probabilities to sum to 1
+ * (Qwen3-30B-A3B's norm_topk_prob); 0 keeps the softmax probabilities.
+ */
+typedef struct {
+    int32_t T, H, E, k, I;
+    int32_t act_dtype;
+    int32_t w_dtype;
+    int32_t norm_topk;
+    int32_t q_block;
+} moe_shape;
+
+/*
+ * 4-bit expert weights.  With w_dtype == MOE_DT_Q4, the w_gate / w_up / w_down
+ * arguments point to packed codes: row-major [E][rows][in/2] bytes where
+ * element 2i of a row sits in the low nibble of byte i and element 2i+1 in the
+ * high nibble ("in" is the input dim: H for gate/up, I for down; rows is I for
+ * gate/up and H for down).  Element value = codebook[code] * scale, with one
+ * bf16 scale per q_block consecutive input-dim elements of a row:
+ * scales are row-major [E][rows][in/q_block] bf16 DEVICE arrays.  The
+ * codebook is given by value (host memory) and travels in the kernel
+ * parameters.
+ */
+typedef struct {
+    const void *gate_scales;
+    const void *up_scales;
+    const void *down_scales;
+    float codebook[16];
+} moe_q4;
+
+/*
+ * Workspace bytes the entry points below need for this shape (host only, no
+ * CUDA call).  The same workspace serves every entry point; it must be
+ * 256-byte aligned.  Its first 256 bytes hold the device error word and must
+ * be zeroed once before first use (moe_read_device_error clears the word
+ * again).  Returns MOE_ERR_NULLPTR / MOE_ERR_SHAPE / MOE_ERR_DTYPE on bad
+ * arguments.
+ */
+MOE_API int moe_workspace_size(const moe_shape *shape, size_t *bytes);
+
+/*
+ * Router GEMM, softmax, top-k and renormalisation (steps A-B).
+ *   x           [T][H]   act dtype
+ *   w_router    [E][H]   act dtype
+ *   b_router    [E] fp32 or NULL (added to the logits before softmax/top-k)
+ *   expert_ids  [T][k]   int32 out: chosen experts, largest logit first;
+ *                         equal fp32 logits: lower expert index first
+ *   weights     [T][k]   fp32 out: softmax probabilities of the chosen experts,
+ *                         divided by their sum when norm_topk
+ *   tie_margin  [T]      fp32 out or NULL: logit of the k-th choice minus the
+ *                         (k+1)-th largest logit (+inf when k == E)
+ *   logits      [T][E]   fp32 out or NULL: router logits (bias included)
+ * Logits accumulate in fp32; softmax is max-subtracted in fp32.
+ */
+MOE_API int moe_route(const moe_shape *shape, const void *x, const void *w_router, const float *b_router,
+              int32_t *expert_ids, float *weights, float *tie_margin, float *logits,
+              void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Expert histogram, exclusive scan and stable permutation (steps C-D).
+ *   expert_ids [A] int32 in
+ *   counts     [E] int32 out: assignments per expert
+ *   offsets    [E+1] int32 out: offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]
+ *   order      [A] int32 out: order[p] = assignment at permuted row p; rows of
+ *              expert e are [offsets[e], offsets[e+1]) in ascending a (stable)
+ *   pos        [A] int32 out: inverse of order
+ * Integer-exact and deterministic.  An id outside [0, E) sets MOE_ERR_DEVICE.
+ */
+MOE_API int moe_permute(const moe_shape *shape, const int32_t *expert_ids, int32_t *counts, int32_t *offsets,
+                int32_t *order, int32_t *pos, void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Grouped SwiGLU experts (steps E-F) over the permuted rows.  For permuted row
+ * p of expert e (offsets[e] <= p < offsets[e+1]) and source token
+ * t = order[p] / k:
+ *   h = SiLU(x[t] . W_gate[e]^T) * (x[t] . W_up[e]^T),  SiLU(z) = z / (1 + e^-z)
+ *   y[p] = h . W_down[e]^T
+ *   x       [T][H] act dtype
+ *   offsets, order: as produced by moe_permute
+ *   w_gate, w_up [E][I][H], w_down [E][H][I]: F32 / BF16 elements, or Q4 codes
+ *   q4      scales + codebook when w_dtype == MOE_DT_Q4, else ignored (may be NULL)
+ *   y       [A][H] out: fp32 when act dtype is F32, bf16 when BF16
+ * Accumulation is fp32; with bf16 activations h is rounded to bf16 before the
+ * down projection.
+ */
+MOE_API int moe_grouped_swiglu(const moe_shape *shape, const void *x, const int32_t *offsets, const int32_t *order,
+                       const void *w_gate, const void *w_up, const void *w_down, const moe_q4 *q4,
+                       void *y, void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Weighted un-permute (step G): out[t] = sum_{j<k} weights[t][j] * y[pos[t*k+j]],
+ * summed in j order in fp32 and rounded once to the act dtype.  No atomics;
+ * bitwise deterministic.
+ *   y [A][H] (dtype as produced by moe_grouped_swiglu), weights [T][k] fp32,
+ *   pos [A] int32, out [T][H] act dtype.
+ */
+MOE_API int moe_unpermute(const moe_shape *shape, const void *y, const float *weights, const int32_t *pos,
+                  void *out, moe_stream_t stream);
+
+/*
+ * The whole block (steps A-G) in one call, intermediates in the workspace.
+ *   out            [T][H] act dtype
+ *   expert_ids_out [T][k] int32 or NULL, weights_out [T][k] fp32 or NULL:
+ *                  optional copies of the routing decision.
+ * Other arguments as in the calls above.
+ */
+MOE_API int moe_forward(const moe_shape *shape, const void *x, const void *w_router, const float *b_router,
+                const void *w_gate, const void *w_up, const void *w_down, const moe_q4 *q4,
+                void *out, int32_t *expert_ids_out, float *weights_out,
+                void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Number of kernel launches one moe_forward call with this shape enqueues
+ * (host only, no CUDA call).  Lets callers account for the kernels they run.
+ */
+MOE_API int moe_forward_launches(const moe_shape *shape, int32_t *launches);
+
+/*
+ * Reads and clears the device error word of a workspace.  Synchronises
+ * `stream` (use outside graph capture).  *code receives MOE_OK or
+ * MOE_ERR_DEVICE.  Returns MOE_OK or MOE_ERR_LAUNCH if the copy failed.
+ */
+MOE_API int moe_read_device_error(void *workspace, int32_t *code, moe_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+MOE_API const char *moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

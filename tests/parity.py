@@ -1,0 +1,149 @@
+"""Helpers of the GPU parity tests: run the CUDA path step by step through the C ABI
+and compare every step with the CPU oracle on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+import top_routing_grouped_router_gb300 as moe
+from top_routing_grouped_router_gb300.device import DeviceLayer, bf16_tensor_bits, upload
+
+# A token whose k-th and (k+1)-th oracle logits differ by less than this is a near tie:
+# its expert choice may legitimately differ between fp32 and double, so it is excluded
+# from the bit-exact comparison and reported.
+NEAR_TIE = 1e-5
+
+
+def tolerance(inp) -> float:
+    """max |out - ref| / max |ref| allowed: 1e-5 for the fp32 block, 1e-2 for bf16 / 4-bit."""
+    return 1e-5 if inp.act == "f32" else 1e-2
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return synth.bf16_bits_to_f32(bf16_tensor_bits(t)).astype(np.float64)
+    return t.detach().cpu().numpy().astype(np.float64)
+
+
+def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
+    scale = float(np.abs(ref).max()) if ref.size else 0.0
+    if scale == 0.0:
+        return float(np.abs(got).max()) if got.size else 0.0
+    return float(np.abs(got - ref).max() / scale)
+
+
+def run_steps(L: DeviceLayer) -> dict:
+    """moe_route -> moe_permute -> moe_grouped_swiglu -> moe_unpermute, then moe_forward; host copies."""
+    s = L.shape
+    T, k, E, H = s.T, s.k, s.E, s.H
+    A = T * k
+    dev = L.x.device
+    ws = L.new_workspace()
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    ids = torch.full((T, k), -1, **i32)
+    w = torch.full((T, k), float("nan"), **f32)
+    margin = torch.empty(T, **f32)
+    logits = torch.empty((T, E), **f32)
+    moe.moe_route(s, L.x, L.w_router, L.b_router, ids, w, margin, logits, ws)
+    counts = torch.full((E,), -1, **i32)
+    offsets = torch.full((E + 1,), -1, **i32)
+    order = torch.full((max(A, 1),), -1, **i32)
+    pos = torch.full((max(A, 1),), -1, **i32)
+    moe.moe_permute(s, ids, counts, offsets, order, pos, ws)
+    y = torch.zeros((max(A, 1), H), dtype=L.out_dtype(), device=dev)
+    moe.moe_grouped_swiglu(s, L.x, offsets, order, L.w_gate, L.w_up, L.w_down, L.q4, y, ws)
+    out = torch.zeros((max(T, 1), H), dtype=L.out_dtype(), device=dev)
+    moe.moe_unpermute(s, y, w, pos, out)
+    ws2 = L.new_workspace()
+    out_f = torch.zeros_like(out)
+    ids_f = torch.full((T, k), -1, **i32)
+    w_f = torch.empty((T, k), **f32)
+    moe.moe_forward(s, L.x, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4, out_f, ids_f, w_f, ws2)
+    torch.cuda.synchronize()
+    err = moe.moe_read_device_error(ws), moe.moe_read_device_error(ws2)
+    return dict(ids=ids.cpu().numpy(), weights=w.cpu().numpy().astype(np.float64),
+                tie_margin=margin.cpu().numpy(), logits=logits.cpu().numpy().astype(np.float64),
+                counts=counts.cpu().numpy(), offsets=offsets.cpu().numpy(), order=order[:A].cpu().numpy(),
+                pos=pos[:A].cpu().numpy(), y=to_f64(y[:A]), out=to_f64(out[:T]), out_forward=to_f64(out_f[:T]),
+                ids_forward=ids_f.cpu().numpy(), weights_forward=w_f.cpu().numpy().astype(np.float64),
+                device_errors=err, y_raw=y, out_raw=out_f)
+
+
+def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
+    if T <= n:
+        return np.arange(T, dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(T, n - 2, replace=False).tolist()) | {0, T - 1}
+    return np.array(sorted(pick), dtype=np.int32)
+
+
+def check_layer(inp, *, full_oracle: bool, n_sample_tokens: int = 16, n_sample_rows: int = 24, report=None):
+    """Every step of the CUDA path against the oracle; returns a summary dict."""
+    L = upload(inp)
+    g = run_steps(L)
+    T, k, E = inp.T, inp.k, inp.E
+    tol = tolerance(inp)
+    assert g["device_errors"] == (0, 0)
+
+    # steps A-B: routing, bit-exact ids except reported near ties
+    o_logits = oracle.router_logits(inp)
+    o_ids, o_w, o_margin = oracle.select_topk(o_logits, k, inp.norm_topk)
+    np.testing.assert_allclose(g["logits"], o_logits, rtol=0, atol=2e-4 * max(1.0, np.abs(o_logits).max()))
+    near = np.where(o_margin < NEAR_TIE)[0]
+    ok = np.setdiff1d(np.arange(T), near)
+    np.testing.assert_array_equal(g["ids"][ok], o_ids[ok])
+    np.testing.assert_allclose(g["weights"][ok], o_w[ok], rtol=0, atol=2e-5)
+    finite = np.isfinite(o_margin[ok])
+    np.testing.assert_allclose(g["tie_margin"][ok][finite], o_margin[ok][finite], rtol=0,
+                               atol=4e-4 * max(1.0, np.abs(o_logits).max()))
+    np.testing.assert_array_equal(g["ids_forward"], g["ids"])
+    np.testing.assert_array_equal(g["weights_forward"], g["weights"])
+
+    # steps C-D on the GPU's own routing decision: integer-exact
+    c, off, order, pos = oracle.permute(g["ids"], E)
+    np.testing.assert_array_equal(g["counts"], c)
+    np.testing.assert_array_equal(g["offsets"], off)
+    np.testing.assert_array_equal(g["order"], order)
+    np.testing.assert_array_equal(g["pos"], pos)
+
+    # steps E-F on the GPU's permutation
+    A = T * k
+    if full_oracle:
+        _, o_y = oracle.grouped_swiglu(inp, off, order)
+        y_err = rel_err(g["y"], o_y)
+    else:
+        rows = sample_tokens(A, n_sample_rows, seed=1) if A else np.zeros(0, np.int32)
+        ref = []
+        for p in rows:
+            e = int(np.searchsorted(off, p, side="right") - 1)
+            t = order[p] // k
+            xrow = synth.bf16_bits_to_f32(inp.x[t]).astype(np.float64) if inp.act == "bf16" else inp.x[t].astype(np.float64)
+            ref.append(oracle.expert_mlp(inp, xrow, e)[1])
+        y_err = rel_err(g["y"][rows], np.array(ref)) if len(rows) else 0.0
+    assert y_err <= tol, f"grouped SwiGLU rel err {y_err}"
+
+    # step G on the GPU's own y, weights and pos
+    if A:
+        o_out_g = oracle.unpermute(g["y"], g["weights"], g["pos"], T, k)
+        g_err = rel_err(g["out"], o_out_g)
+        assert g_err <= (2e-6 if inp.act == "f32" else 4e-3), f"unpermute rel err {g_err}"
+
+    # whole block vs the oracle's own routing, near-tie tokens excluded
+    np.testing.assert_array_equal(g["out_forward"], g["out"])
+    if full_oracle:
+        ref = oracle.forward(inp)
+        toks = ok
+        o_out = ref["out"][toks]
+    else:
+        toks = np.setdiff1d(sample_tokens(T, n_sample_tokens), near)
+        o_out = oracle.forward_tokens(inp, toks)["out"]
+    out_err = rel_err(g["out"][toks], o_out) if len(toks) else 0.0
+    assert out_err <= tol, f"block output rel err {out_err}"
+    summary = dict(name=inp.name, T=T, near_ties=near.tolist(), y_rel_err=y_err, out_rel_err=out_err,
+                   active_experts=int((g["counts"] > 0).sum()))
+    if report is not None:
+        report.append(summary)
+    return summary, g

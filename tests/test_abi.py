@@ -1,0 +1,100 @@
+"""The C-ABI library builds, loads and exports every entry point declared in include/moe.h,
+and rejects bad arguments on the host before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import top_routing_grouped_router_gb300 as moe
+from top_routing_grouped_router_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    moe_build.build()
+    return moe.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(moe.EXPORTED_SYMBOLS) == names
+
+
+def test_status_strings(L):
+    for code in range(0, -8, -1):
+        assert moe.moe_status_string(code).startswith("MOE_")
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode8", "decode64z", "decode48q", "prefill"])
+def test_workspace_size_for_every_workload(L, name):
+    import synth
+    c = synth.WORKLOADS[name]
+    s = moe.make_shape(c["T"], c["H"], c["E"], c["k"], c["I"], c["act"], c["w"])
+    n = moe.moe_workspace_size(s)
+    A = c["T"] * c["k"]
+    assert n >= A * c["H"] * (4 if c["act"] == "f32" else 2)
+    assert n % 256 == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=9, E=8), -2),          # k > E
+    (dict(E=300, k=2), -2),        # E above 256
+    (dict(H=60), -2),              # H not a multiple of 8
+    (dict(I=0), -2),
+    (dict(T=-1), -2),
+    (dict(k=33, E=64), -2),
+    (dict(act="f32", w="bf16"), -3),
+    (dict(act="f32", w="q4"), -3),
+    (dict(w="q4", q_block=48), -2),  # q_block does not divide H=64*...
+])
+def test_shape_validation(L, kw, code):
+    base = dict(T=4, H=128, E=8, k=2, I=64, act="bf16", w="bf16", q_block=64)
+    base.update(kw)
+    s = moe.make_shape(base["T"], base["H"], base["E"], base["k"], base["I"], base["act"], base["w"],
+                       q_block=base["q_block"])
+    n = ctypes.c_size_t(0)
+    assert L.moe_workspace_size(ctypes.byref(s), ctypes.byref(n)) == code
+
+
+def test_null_and_workspace_errors_return_before_launch(L):
+    s = moe.make_shape(4, 128, 8, 2, 64)
+    ws_need = moe.moe_workspace_size(s)
+    fake = 1 << 20  # never dereferenced: every call below fails host-side validation
+    st = None
+    # null shape / null pointers
+    assert L.moe_route(None, fake, fake, None, fake, fake, None, None, fake, ws_need, st) == -1
+    assert L.moe_route(ctypes.byref(s), None, fake, None, fake, fake, None, None, fake, ws_need, st) == -1
+    assert L.moe_forward(ctypes.byref(s), fake, fake, None, None, fake, fake, None, fake, None, None, fake,
+                         ws_need, st) == -1
+    # workspace too small / missing
+    assert L.moe_route(ctypes.byref(s), fake, fake, None, fake, fake, None, None, fake, ws_need - 1, st) == -4
+    assert L.moe_permute(ctypes.byref(s), fake, fake, fake, fake, fake, None, ws_need, st) == -4
+    assert L.moe_grouped_swiglu(ctypes.byref(s), fake, fake, fake, fake, fake, fake, None, fake, fake, 16, st) == -4
+    # misaligned pointers
+    assert L.moe_route(ctypes.byref(s), fake + 2, fake, None, fake, fake, None, None, fake, ws_need, st) == -5
+    assert L.moe_unpermute(ctypes.byref(s), fake + 8, fake, fake, fake, st) == -5
+    assert L.moe_forward(ctypes.byref(s), fake, fake, None, fake, fake, fake, None, fake, None, None, fake + 64,
+                         ws_need, st) == -5
+    # q4 without scales
+    sq = moe.make_shape(4, 128, 8, 2, 64, "bf16", "q4")
+    assert L.moe_grouped_swiglu(ctypes.byref(sq), fake, fake, fake, fake, fake, fake, None, fake, fake,
+                                moe.moe_workspace_size(sq), st) == -1
+    assert L.moe_read_device_error(None, None, st) == -1
+
+
+def test_binding_raises_on_error(L):
+    s = moe.make_shape(4, 128, 8, 9, 64)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_workspace_size(s)
+    assert ei.value.status == -2

@@ -1,0 +1,168 @@
+"""GB300-native sparse Mixture-of-Experts block (Qwen3-MoE style), Python binding.
+
+A thin ctypes binding of the C ABI in ``include/moe.h`` (``libmoe_gb300.so``,
+built in-tree by ``top_routing_grouped_router_gb300.build``).  The functions
+below keep the C names and only marshal arguments: torch CUDA tensors (or raw
+integer device addresses) become pointers, the current torch CUDA stream becomes
+the ``stream`` argument.  Every step of the block runs in the library's CUDA
+kernels; there is no fallback of any kind, and every call raises if the library
+is missing or returns an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = [
+    "MOE_DT_F32", "MOE_DT_BF16", "MOE_DT_Q4", "MoEError", "MoEShape", "MoEQ4", "lib", "library_path",
+    "make_shape", "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
+    "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string", "EXPORTED_SYMBOLS",
+]
+
+MOE_DT_F32, MOE_DT_BF16, MOE_DT_Q4 = 0, 1, 2
+_DT = {"f32": MOE_DT_F32, "bf16": MOE_DT_BF16, "q4": MOE_DT_Q4}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libmoe_gb300.so")
+
+EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
+                    "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {moe_status_string(status)} ({status})")
+        self.status = status
+
+
+class MoEShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("I", ctypes.c_int32), ("act_dtype", ctypes.c_int32), ("w_dtype", ctypes.c_int32),
+                ("norm_topk", ctypes.c_int32), ("q_block", ctypes.c_int32)]
+
+
+class MoEQ4(ctypes.Structure):
+    _fields_ = [("gate_scales", ctypes.c_void_p), ("up_scales", ctypes.c_void_p),
+                ("down_scales", ctypes.c_void_p), ("codebook", ctypes.c_float * 16)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"CUDA library {library_path} is missing: build it with "
+                               f"`python -m top_routing_grouped_router_gb300.build`")
+        L = ctypes.CDLL(library_path)
+        vp, sz, i32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
+        sp = ctypes.POINTER(MoEShape)
+        q4p = ctypes.POINTER(MoEQ4)
+        sig = {
+            "moe_workspace_size": [sp, ctypes.POINTER(ctypes.c_size_t)],
+            "moe_route": [sp, vp, vp, vp, i32p, vp, vp, vp, vp, sz, vp],
+            "moe_permute": [sp, i32p, i32p, i32p, i32p, i32p, vp, sz, vp],
+            "moe_grouped_swiglu": [sp, vp, i32p, i32p, vp, vp, vp, q4p, vp, vp, sz, vp],
+            "moe_unpermute": [sp, vp, vp, i32p, vp, vp],
+            "moe_forward": [sp, vp, vp, vp, vp, vp, vp, q4p, vp, i32p, vp, vp, sz, vp],
+            "moe_read_device_error": [vp, ctypes.POINTER(ctypes.c_int32), vp],
+            "moe_forward_launches": [sp, ctypes.POINTER(ctypes.c_int32)],
+        }
+        for name, argtypes in sig.items():
+            f = getattr(L, name)
+            f.argtypes = argtypes
+            f.restype = ctypes.c_int
+        L.moe_status_string.argtypes = [ctypes.c_int]
+        L.moe_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def make_shape(T, H, E, k, I, act="bf16", w="bf16", norm_topk=True, q_block=64) -> MoEShape:
+    return MoEShape(int(T), int(H), int(E), int(k), int(I), _DT[act] if isinstance(act, str) else int(act),
+                    _DT[w] if isinstance(w, str) else int(w), int(bool(norm_topk)), int(q_block))
+
+
+def _ptr(t):
+    """Device address of a torch tensor, an int address, or None -> NULL."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise MoEError(rc, what)
+
+
+def moe_workspace_size(shape: MoEShape) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(ctypes.byref(shape), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_route(shape, x, w_router, b_router, expert_ids, weights, tie_margin=None, logits=None, workspace=None,
+              stream=None):
+    _check(lib().moe_route(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(b_router), _ptr(expert_ids),
+                           _ptr(weights), _ptr(tie_margin), _ptr(logits), _ptr(workspace), _nbytes(workspace),
+                           _stream(stream)), "moe_route")
+
+
+def moe_permute(shape, expert_ids, counts, offsets, order, pos, workspace, stream=None):
+    _check(lib().moe_permute(ctypes.byref(shape), _ptr(expert_ids), _ptr(counts), _ptr(offsets), _ptr(order),
+                             _ptr(pos), _ptr(workspace), _nbytes(workspace), _stream(stream)), "moe_permute")
+
+
+def moe_grouped_swiglu(shape, x, offsets, order, w_gate, w_up, w_down, q4, y, workspace, stream=None):
+    _check(lib().moe_grouped_swiglu(ctypes.byref(shape), _ptr(x), _ptr(offsets), _ptr(order), _ptr(w_gate),
+                                    _ptr(w_up), _ptr(w_down), ctypes.byref(q4) if q4 is not None else None,
+                                    _ptr(y), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "moe_grouped_swiglu")
+
+
+def moe_unpermute(shape, y, weights, pos, out, stream=None):
+    _check(lib().moe_unpermute(ctypes.byref(shape), _ptr(y), _ptr(weights), _ptr(pos), _ptr(out),
+                               _stream(stream)), "moe_unpermute")
+
+
+def moe_forward(shape, x, w_router, b_router, w_gate, w_up, w_down, q4, out, expert_ids_out=None,
+                weights_out=None, workspace=None, stream=None):
+    _check(lib().moe_forward(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(b_router), _ptr(w_gate),
+                             _ptr(w_up), _ptr(w_down), ctypes.byref(q4) if q4 is not None else None, _ptr(out),
+                             _ptr(expert_ids_out), _ptr(weights_out), _ptr(workspace), _nbytes(workspace),
+                             _stream(stream)), "moe_forward")
+
+
+def moe_forward_launches(shape: MoEShape) -> int:
+    n = ctypes.c_int32(0)
+    _check(lib().moe_forward_launches(ctypes.byref(shape), ctypes.byref(n)), "moe_forward_launches")
+    return n.value
+
+
+def moe_read_device_error(workspace, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(lib().moe_read_device_error(_ptr(workspace), ctypes.byref(code), _stream(stream)),
+           "moe_read_device_error")
+    return code.value

@@ -1,0 +1,249 @@
+// moe_api.cu -- the extern "C" entry points: host-side validation, workspace
+// layout and kernel sequencing.  No entry point allocates, frees, synchronises
+// or copies to the host (moe_read_device_error excepted), so every call can be
+// recorded into a CUDA graph.
+#include "moe_internal.cuh"
+
+#include <limits.h>
+
+namespace moe {
+
+int permute_chunks(int A);
+int select_grouped_path(const moe_shape &s);
+cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
+                                const int32_t *order, const void *wg, const void *wu, const void *wd,
+                                const moe_q4 *q4, const int32_t *active, float *part, void *h, void *y,
+                                int32_t *err, cudaStream_t st);
+size_t grouped_fast_part_bytes(int path, const moe_shape &s);
+int grouped_fast_launches(int path, const moe_shape &s);
+int route_launches(const moe_shape &s);
+int permute_launches(const moe_shape &s);
+int grouped_simple_launches(const moe_shape &s);
+
+namespace {
+size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+size_t act_bytes(const moe_shape &s) { return s.act_dtype == MOE_DT_F32 ? 4 : 2; }
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+}  // namespace
+
+int validate_shape(const moe_shape *s) {
+    if (!s) return MOE_ERR_NULLPTR;
+    if (s->T < 0 || s->H <= 0 || s->E <= 0 || s->I <= 0 || s->k <= 0) return MOE_ERR_SHAPE;
+    if (s->E > kMaxE || s->k > s->E || s->k > kMaxK) return MOE_ERR_SHAPE;
+    if (s->H % 8 || s->I % 8) return MOE_ERR_SHAPE;
+    if (s->T > (1 << 18) || (int64_t)s->T * s->k >= (int64_t(1) << 30)) return MOE_ERR_SHAPE;
+    const bool ok = (s->act_dtype == MOE_DT_F32 && s->w_dtype == MOE_DT_F32) ||
+                    (s->act_dtype == MOE_DT_BF16 && (s->w_dtype == MOE_DT_BF16 || s->w_dtype == MOE_DT_Q4));
+    if (!ok) return MOE_ERR_DTYPE;
+    if (s->w_dtype == MOE_DT_Q4) {
+        if (s->q_block <= 0 || s->q_block % 2 || s->H % s->q_block || s->I % s->q_block) return MOE_ERR_SHAPE;
+    }
+    return MOE_OK;
+}
+
+WsLayout ws_layout(const moe_shape &s) {
+    WsLayout L{};
+    const size_t A = (size_t)s.T * s.k, E = s.E;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += round_up(bytes);
+        return o;
+    };
+    L.err = take(256);
+    L.logits = take((size_t)s.T * E * 4);
+    L.ids = take(A * 4);
+    L.weights = take(A * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.order = take(A * 4);
+    L.pos = take(A * 4);
+    L.active = take((E + 1) * 4);
+    L.hist = take((size_t)permute_chunks((int)A) * E * 4);
+    L.h = take(A * s.I * 4);
+    L.y = take(A * s.H * act_bytes(s));
+    L.part = take(grouped_fast_part_bytes(select_grouped_path(s), s));
+    L.total = off;
+    return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+#define MOE_TRY(expr)                  \
+    do {                               \
+        const int _rc = (expr);        \
+        if (_rc != MOE_OK) return _rc; \
+    } while (0)
+
+namespace {
+
+int check_ws(const moe_shape &s, const void *ws, size_t bytes) {
+    if (!ws) return MOE_ERR_WORKSPACE;
+    if (bytes < ws_layout(s).total) return MOE_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
+int launch_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
+
+template <typename T>
+T *at(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
+
+int check_weights(const moe_shape &s, const void *wg, const void *wu, const void *wd, const moe_q4 *q4) {
+    if (!wg || !wu || !wd) return MOE_ERR_NULLPTR;
+    if (misaligned(wg) || misaligned(wu) || misaligned(wd)) return MOE_ERR_ALIGN;
+    if (s.w_dtype == MOE_DT_Q4) {
+        if (!q4 || !q4->gate_scales || !q4->up_scales || !q4->down_scales) return MOE_ERR_NULLPTR;
+        if (misaligned(q4->gate_scales) || misaligned(q4->up_scales) || misaligned(q4->down_scales))
+            return MOE_ERR_ALIGN;
+    }
+    return MOE_OK;
+}
+
+int do_route(const moe_shape &s, const void *x, const void *wr, const float *b, int32_t *ids, float *w,
+             float *margin, float *logits, void *ws, cudaStream_t st) {
+    const WsLayout L = ws_layout(s);
+    float *lg = logits ? logits : at<float>(ws, L.logits);
+    MOE_TRY(launch_rc(launch_router_logits(s, x, wr, b, lg, st)));
+    return launch_rc(launch_topk(s, lg, ids, w, margin, st));
+}
+
+int do_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t *offsets, int32_t *order,
+               int32_t *pos, void *ws, cudaStream_t st) {
+    const WsLayout L = ws_layout(s);
+    return launch_rc(launch_permute(s, ids, counts, offsets, order, pos, at<int32_t>(ws, L.active),
+                                    at<int32_t>(ws, L.hist), at<int32_t>(ws, L.err), st));
+}
+
+int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order, const void *wg,
+               const void *wu, const void *wd, const moe_q4 *q4, void *y, void *ws, cudaStream_t st) {
+    const WsLayout L = ws_layout(s);
+    const int path = select_grouped_path(s);
+    if (path > 0)
+        return launch_rc(launch_grouped_fast(path, s, x, offsets, order, wg, wu, wd, q4,
+                                             at<int32_t>(ws, L.active), at<float>(ws, L.part), at<void>(ws, L.h),
+                                             y, at<int32_t>(ws, L.err), st));
+    return launch_rc(launch_grouped_simple(s, x, offsets, order, wg, wu, wd, q4, at<void>(ws, L.h), y, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_workspace_size(const moe_shape *shape, size_t *bytes) {
+    if (!bytes) return MOE_ERR_NULLPTR;
+    MOE_TRY(validate_shape(shape));
+    *bytes = ws_layout(*shape).total;
+    return MOE_OK;
+}
+
+int moe_route(const moe_shape *shape, const void *x, const void *w_router, const float *b_router,
+              int32_t *expert_ids, float *weights, float *tie_margin, float *logits, void *workspace,
+              size_t workspace_bytes, moe_stream_t stream) {
+    MOE_TRY(validate_shape(shape));
+    const moe_shape &s = *shape;
+    if (!x || !w_router || !expert_ids || !weights) return MOE_ERR_NULLPTR;
+    MOE_TRY(check_ws(s, workspace, workspace_bytes));
+    if (misaligned(x) || misaligned(w_router)) return MOE_ERR_ALIGN;
+    return do_route(s, x, w_router, b_router, expert_ids, weights, tie_margin, logits, workspace,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_permute(const moe_shape *shape, const int32_t *expert_ids, int32_t *counts, int32_t *offsets,
+                int32_t *order, int32_t *pos, void *workspace, size_t workspace_bytes, moe_stream_t stream) {
+    MOE_TRY(validate_shape(shape));
+    const moe_shape &s = *shape;
+    if (!counts || !offsets || (s.T > 0 && (!expert_ids || !order || !pos))) return MOE_ERR_NULLPTR;
+    MOE_TRY(check_ws(s, workspace, workspace_bytes));
+    return do_permute(s, expert_ids, counts, offsets, order, pos, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_grouped_swiglu(const moe_shape *shape, const void *x, const int32_t *offsets, const int32_t *order,
+                       const void *w_gate, const void *w_up, const void *w_down, const moe_q4 *q4, void *y,
+                       void *workspace, size_t workspace_bytes, moe_stream_t stream) {
+    MOE_TRY(validate_shape(shape));
+    const moe_shape &s = *shape;
+    if (!x || !offsets || !order || !y) return MOE_ERR_NULLPTR;
+    MOE_TRY(check_weights(s, w_gate, w_up, w_down, q4));
+    MOE_TRY(check_ws(s, workspace, workspace_bytes));
+    if (misaligned(x) || misaligned(y)) return MOE_ERR_ALIGN;
+    return do_grouped(s, x, offsets, order, w_gate, w_up, w_down, q4, y, workspace,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_unpermute(const moe_shape *shape, const void *y, const float *weights, const int32_t *pos, void *out,
+                  moe_stream_t stream) {
+    MOE_TRY(validate_shape(shape));
+    const moe_shape &s = *shape;
+    if (!y || !weights || !pos || !out) return MOE_ERR_NULLPTR;
+    if (misaligned(y) || misaligned(out)) return MOE_ERR_ALIGN;
+    return launch_rc(launch_unpermute(s, y, weights, pos, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_forward(const moe_shape *shape, const void *x, const void *w_router, const float *b_router,
+                const void *w_gate, const void *w_up, const void *w_down, const moe_q4 *q4, void *out,
+                int32_t *expert_ids_out, float *weights_out, void *workspace, size_t workspace_bytes,
+                moe_stream_t stream) {
+    MOE_TRY(validate_shape(shape));
+    const moe_shape &s = *shape;
+    if (!x || !w_router || !out) return MOE_ERR_NULLPTR;
+    MOE_TRY(check_weights(s, w_gate, w_up, w_down, q4));
+    MOE_TRY(check_ws(s, workspace, workspace_bytes));
+    if (misaligned(x) || misaligned(w_router) || misaligned(out)) return MOE_ERR_ALIGN;
+    if (s.T == 0) return MOE_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const WsLayout L = ws_layout(s);
+    int32_t *ids = expert_ids_out ? expert_ids_out : at<int32_t>(workspace, L.ids);
+    float *w = weights_out ? weights_out : at<float>(workspace, L.weights);
+    int32_t *offsets = at<int32_t>(workspace, L.offsets), *order = at<int32_t>(workspace, L.order),
+            *pos = at<int32_t>(workspace, L.pos);
+    void *y = at<void>(workspace, L.y);
+    MOE_TRY(do_route(s, x, w_router, b_router, ids, w, nullptr, nullptr, workspace, st));
+    MOE_TRY(do_permute(s, ids, at<int32_t>(workspace, L.counts), offsets, order, pos, workspace, st));
+    MOE_TRY(do_grouped(s, x, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st));
+    return launch_rc(launch_unpermute(s, y, w, pos, out, st));
+}
+
+int moe_forward_launches(const moe_shape *shape, int32_t *launches) {
+    if (!launches) return MOE_ERR_NULLPTR;
+    MOE_TRY(validate_shape(shape));
+    const moe_shape &s = *shape;
+    if (s.T == 0) {
+        *launches = 0;
+        return MOE_OK;
+    }
+    const int path = select_grouped_path(s);
+    *launches = route_launches(s) + permute_launches(s) +
+                (path > 0 ? grouped_fast_launches(path, s) : grouped_simple_launches(s)) + 1;
+    return MOE_OK;
+}
+
+int moe_read_device_error(void *workspace, int32_t *code, moe_stream_t stream) {
+    if (!workspace || !code) return MOE_ERR_NULLPTR;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    int32_t *err = at<int32_t>(workspace, 0);
+    if (cudaMemcpyAsync(&v, err, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_LAUNCH;
+    if (cudaMemsetAsync(err, 0, sizeof v, st) != cudaSuccess) return MOE_ERR_LAUNCH;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_LAUNCH;
+    *code = v;
+    return MOE_OK;
+}
+
+const char *moe_status_string(int status) {
+    switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_NULLPTR: return "MOE_ERR_NULLPTR: a required pointer is NULL";
+    case MOE_ERR_SHAPE: return "MOE_ERR_SHAPE: sizes outside the supported range";
+    case MOE_ERR_DTYPE: return "MOE_ERR_DTYPE: unsupported dtype combination";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing or too small";
+    case MOE_ERR_ALIGN: return "MOE_ERR_ALIGN: device pointer not 16-byte aligned";
+    case MOE_ERR_LAUNCH: return "MOE_ERR_LAUNCH: CUDA launch failed";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: inconsistent device data recorded";
+    default: return "unknown moe status";
+    }
+}
+
+}  // extern "C"

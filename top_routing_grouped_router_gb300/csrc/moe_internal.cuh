@@ -1,0 +1,80 @@
+// moe_internal.cuh -- internal declarations shared by the CUDA translation units
+// of the MoE library (workspace layout, device helpers, launcher prototypes).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 32;
+constexpr size_t kAlign = 256;
+
+// Workspace regions (byte offsets from the workspace base).  Every region is
+// 256-byte aligned.  The first 256 bytes hold the device error word and small
+// counters.
+struct WsLayout {
+    size_t err;        // int32 error word (MOE_OK / MOE_ERR_DEVICE)
+    size_t logits;     // fp32 [T][E]
+    size_t ids;        // int32 [A]
+    size_t weights;    // fp32 [A]
+    size_t counts;     // int32 [E]
+    size_t offsets;    // int32 [E+1]
+    size_t order;      // int32 [A]
+    size_t pos;        // int32 [A]
+    size_t active;     // int32 [1 + E]: number of non-empty experts, then their ids ascending
+    size_t hist;       // int32 [chunks][E]: per-chunk expert histograms (multi-block permute)
+    size_t h;          // [A][I] intermediate SwiGLU activations (fp32 or bf16)
+    size_t y;          // [A][H] expert outputs in permuted order (act dtype)
+    size_t part;       // fp32 split-K partial sums of the weight-streaming path
+    size_t total;
+};
+
+// Assignments handled by one block of the permute kernels.
+constexpr int kPermuteChunk = 1024;
+
+WsLayout ws_layout(const moe_shape &s);
+int validate_shape(const moe_shape *s);
+
+// ---------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// SiLU(g) * u with an fp32 logistic.
+__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// Records the first device-side error in the workspace error word.
+__device__ __forceinline__ void record_error(int32_t *err, int code) { atomicCAS(err, 0, code); }
+
+// ---------------------------------------------------------------- launchers (each returns cudaError_t of the launch)
+
+cudaError_t launch_router_logits(const moe_shape &s, const void *x, const void *wr, const float *bias,
+                                 float *logits, cudaStream_t st);
+cudaError_t launch_topk(const moe_shape &s, const float *logits, int32_t *ids, float *w, float *margin,
+                        cudaStream_t st);
+cudaError_t launch_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t *offsets,
+                           int32_t *order, int32_t *pos, int32_t *active, int32_t *hist, int32_t *err,
+                           cudaStream_t st);
+cudaError_t launch_grouped_simple(const moe_shape &s, const void *x, const int32_t *offsets,
+                                  const int32_t *order, const void *wg, const void *wu, const void *wd,
+                                  const moe_q4 *q4, void *h, void *y, cudaStream_t st);
+cudaError_t launch_unpermute(const moe_shape &s, const void *y, const float *w, const int32_t *pos, void *out,
+                             cudaStream_t st);
+
+}  // namespace moe
