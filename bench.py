@@ -123,6 +123,22 @@ def src_digest(paths):
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time (every rank times the same number of steps)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step: int, steps: int, ms_total: float) -> float:
+    """Whole-job tokens/s: every replica processes its own batch each step (weak scaling)."""
+    return world * tokens_per_step * steps / (ms_total / 1e3)
+
+
 def layer_inputs(workload):
     import synth
     c = synth.WORKLOADS[workload]
@@ -217,7 +233,7 @@ def run_ours(args, rank, world, local):
     T, H, E, k, I = inp0.T, inp0.H, inp0.E, inp0.k, inp0.I
     # enough weight copies that a replay never finds the previous replay's weights in L2
     per_copy = sum(expert_bytes_per_expert(l) * E for l in layers)
-    n_copies = 1 if per_copy * 0.3 > 2 * L2_BYTES else 3
+    n_copies = 1 if per_copy > 32 * L2_BYTES else 3
     dl = [[upload(l, dev) for l in layers] for _ in range(n_copies)]
     for c in range(1, n_copies):  # copies share x / router / bias with copy 0 (the same tokens each step)
         for l in range(len(layers)):
@@ -282,14 +298,10 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    ms_total = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     ms_step = ms_total / args.steps
     tokens_per_step = T * len(layers)
-    value = world * tokens_per_step * args.steps / (ms_total / 1e3)
+    value = job_throughput(world, tokens_per_step, args.steps, ms_total)
 
     # the dominant kernel (grouped SwiGLU experts) timed alone with events on its stream
     kt_steps = min(args.steps, 200)
