@@ -185,6 +185,37 @@ MOE_API int moe_forward(const moe_shape *shape, const void *x, const void *w_rou
                 void *out, int32_t *expert_ids_out, float *weights_out,
                 void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* Size of the library's fixed device scratch array used by moe_forward_static_scratch. */
+#define MOE_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * moe_forward without a caller workspace, for callers that cannot allocate
+ * device memory: code running while another thread captures a CUDA graph in
+ * global mode (cudaMalloc is illegal then), plugins whose host framework owns
+ * the whole device-memory budget, latency-critical paths that cannot afford
+ * cudaMalloc's implicit synchronisation.  The pages have no counterpart: this
+ * is a deployment convenience, not a step of the method.
+ *
+ * Same arguments and results as moe_forward, minus the workspace.  The scratch
+ * is one fixed MOE_STATIC_SCRATCH_BYTES (32 MiB) array in the library's device
+ * image; every GPU that loads the library holds it until the process exits.
+ *   - Allocates nothing and calls no allocating routine.
+ *   - Shapes whose moe_workspace_size() exceeds 32 MiB are rejected with
+ *     MOE_ERR_WORKSPACE before anything is enqueued (the decode shapes fit:
+ *     the Qwen3-30B-A3B layer up to a few hundred tokens).
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call outside any stream
+ *     capture.
+ *   - Every call shares the one array and leaves its contents behind; each call
+ *     clears the error word itself.  Calls whose executions overlap on the GPU
+ *     (different streams, or graphs replayed concurrently) race on the array:
+ *     serialise them.
+ */
+MOE_API int moe_forward_static_scratch(const moe_shape *shape, const void *x, const void *w_router,
+                                       const float *b_router, const void *w_gate, const void *w_up,
+                                       const void *w_down, const moe_q4 *q4, void *out,
+                                       int32_t *expert_ids_out, float *weights_out, moe_stream_t stream);
+
 /*
  * Number of kernel launches one moe_forward call with this shape enqueues
  * (host only, no CUDA call).  Lets callers account for the kernels they run.

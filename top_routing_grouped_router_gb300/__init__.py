@@ -18,6 +18,7 @@ __all__ = [
     "MOE_DT_F32", "MOE_DT_BF16", "MOE_DT_Q4", "MoEError", "MoEShape", "MoEQ4", "lib", "library_path",
     "make_shape", "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string", "EXPORTED_SYMBOLS",
+    "moe_forward_static_scratch",
 ]
 
 MOE_DT_F32, MOE_DT_BF16, MOE_DT_Q4 = 0, 1, 2
@@ -27,7 +28,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libmoe_gb300.so")
 
 EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
-                    "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string")
+                    "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string",
+                    "moe_forward_static_scratch")
 
 
 class MoEError(RuntimeError):
@@ -70,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "moe_forward": [sp, vp, vp, vp, vp, vp, vp, q4p, vp, i32p, vp, vp, sz, vp],
             "moe_read_device_error": [vp, ctypes.POINTER(ctypes.c_int32), vp],
             "moe_forward_launches": [sp, ctypes.POINTER(ctypes.c_int32)],
+            "moe_forward_static_scratch": [sp, vp, vp, vp, vp, vp, vp, q4p, vp, i32p, vp, vp],
         }
         for name, argtypes in sig.items():
             f = getattr(L, name)
@@ -153,6 +156,16 @@ def moe_forward(shape, x, w_router, b_router, w_gate, w_up, w_down, q4, out, exp
                              _ptr(w_up), _ptr(w_down), ctypes.byref(q4) if q4 is not None else None, _ptr(out),
                              _ptr(expert_ids_out), _ptr(weights_out), _ptr(workspace), _nbytes(workspace),
                              _stream(stream)), "moe_forward")
+
+
+def moe_forward_static_scratch(shape, x, w_router, b_router, w_gate, w_up, w_down, q4, out, expert_ids_out=None,
+                               weights_out=None, stream=None):
+    """moe_forward with the library's fixed 32 MiB device scratch instead of a caller workspace."""
+    _check(lib().moe_forward_static_scratch(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(b_router),
+                                            _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                            ctypes.byref(q4) if q4 is not None else None, _ptr(out),
+                                            _ptr(expert_ids_out), _ptr(weights_out), _stream(stream)),
+           "moe_forward_static_scratch")
 
 
 def moe_forward_launches(shape: MoEShape) -> int:
