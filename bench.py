@@ -50,6 +50,7 @@ def parse_args():
     ap.add_argument("--workload", default="decode8", choices=sorted(DESCR))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--copies", type=int, default=0, help="weight copies to rotate (0 = automatic)")
     return ap.parse_args()
 
 
@@ -233,7 +234,7 @@ def run_ours(args, rank, world, local):
     T, H, E, k, I = inp0.T, inp0.H, inp0.E, inp0.k, inp0.I
     # enough weight copies that a replay never finds the previous replay's weights in L2
     per_copy = sum(expert_bytes_per_expert(l) * E for l in layers)
-    n_copies = 1 if per_copy > 32 * L2_BYTES else 3
+    n_copies = args.copies if args.copies > 0 else (1 if per_copy > 32 * L2_BYTES else 3)
     dl = [[upload(l, dev) for l in layers] for _ in range(n_copies)]
     for c in range(1, n_copies):  # copies share x / router / bias with copy 0 (the same tokens each step)
         for l in range(len(layers)):

@@ -56,14 +56,17 @@ __device__ __forceinline__ int expert_of_row(const int32_t *offsets, int E, int 
 template <typename ActT, int WFMT>
 __global__ void __launch_bounds__(kWarps * 32)
 gate_up_simple_kernel(const ActT *__restrict__ x, const int32_t *__restrict__ offsets,
-                      const int32_t *__restrict__ order, int E, int k, int H, int I, WeightRef wg, WeightRef wu,
-                      Codebook cb, float *__restrict__ h, int p0) {
+                      const int32_t *__restrict__ order, int E, int k, int H, int I, int A, WeightRef wg,
+                      WeightRef wu, Codebook cb, float *__restrict__ h, int p0) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i = blockIdx.x * kWarps + warp;
     const int p = p0 + blockIdx.y;
     if (i >= I) return;
     const int e = expert_of_row(offsets, E, p);
-    const int t = __ldg(order + p) / k;
+    const int a = __ldg(order + p);
+    if (e >= E) return;
+    if (a < 0 || a >= A) return;  // inconsistent permutation: leave the row alone
+    const int t = a / k;
     float g = 0.f, u = 0.f;
     for (int c = lane; c < H; c += 32) {
         const float xv = act_at(x, (size_t)t * H + c);
@@ -88,6 +91,7 @@ down_simple_kernel(const float *__restrict__ h, const int32_t *__restrict__ offs
     const int p = p0 + blockIdx.y;
     if (r >= H) return;
     const int e = expert_of_row(offsets, E, p);
+    if (e >= E) return;  // inconsistent offsets: leave the row alone
     float s = 0.f;
     for (int c = lane; c < I; c += 32) s = fmaf(__ldg(h + (size_t)p * I + c), weight_at<WFMT>(wd, cb, e, r, c), s);
     s = warp_sum(s);
@@ -116,7 +120,7 @@ cudaError_t launch_typed(const moe_shape &s, const void *x, const int32_t *offse
         const int rows = min(65535, A - p0);
         dim3 g1((s.I + kWarps - 1) / kWarps, rows);
         gate_up_simple_kernel<ActT, WFMT><<<g1, kWarps * 32, 0, st>>>(static_cast<const ActT *>(x), offsets, order,
-                                                                      s.E, s.k, s.H, s.I, rg, ru, cb,
+                                                                      s.E, s.k, s.H, s.I, A, rg, ru, cb,
                                                                       static_cast<float *>(h), p0);
     }
     for (int p0 = 0; p0 < A; p0 += 65535) {

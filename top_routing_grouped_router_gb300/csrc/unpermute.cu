@@ -39,7 +39,7 @@ __device__ __forceinline__ void store8(uint16_t *p, const float *v) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 unpermute_kernel(const T *__restrict__ y, const float *__restrict__ w, const int32_t *__restrict__ pos,
-                 T *__restrict__ out, int k, int H, int col_blocks) {
+                 T *__restrict__ out, int k, int H, int A, int col_blocks) {
     const int t = blockIdx.x / col_blocks;
     const int c0 = ((blockIdx.x % col_blocks) * kThreads + threadIdx.x) * kCols;
     if (c0 >= H) return;
@@ -48,6 +48,7 @@ unpermute_kernel(const T *__restrict__ y, const float *__restrict__ w, const int
     for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
     for (int j = 0; j < k; ++j) {
         const int p = __ldg(pos + (size_t)t * k + j);
+        if (p < 0 || p >= A) continue;  // inconsistent pos: that slot contributes nothing
         const float wt = __ldg(w + (size_t)t * k + j);
         float v[kCols];
         load8(y + (size_t)p * H + c0, v);
@@ -66,10 +67,10 @@ cudaError_t launch_unpermute(const moe_shape &s, const void *y, const float *w, 
     const unsigned grid = unsigned(cb) * unsigned(s.T);
     if (s.act_dtype == MOE_DT_F32)
         unpermute_kernel<float><<<grid, kThreads, 0, st>>>(static_cast<const float *>(y), w, pos,
-                                                           static_cast<float *>(out), s.k, s.H, cb);
+                                                           static_cast<float *>(out), s.k, s.H, s.T * s.k, cb);
     else
         unpermute_kernel<uint16_t><<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(y), w, pos,
-                                                              static_cast<uint16_t *>(out), s.k, s.H, cb);
+                                                              static_cast<uint16_t *>(out), s.k, s.H, s.T * s.k, cb);
     return cudaGetLastError();
 }
 
