@@ -1,24 +1,29 @@
-// grouped_stream.cu -- grouped SwiGLU experts at decode batch sizes (<= 64 tokens per
-// expert): a persistent, weight-streaming kernel that reads only the active experts'
-// weights, once, through a TMA + mbarrier pipeline.
+// grouped_stream.cu -- grouped SwiGLU experts on the 5th-generation tensor cores:
+// a persistent kernel that streams only the active experts' weights through a TMA +
+// mbarrier pipeline into tcgen05.mma, with fp32 accumulators in tensor memory.
 //
-// Work = tiles.  A gate/up tile is (active expert e, 32 rows of I): the gate and up
-// rows i0..i0+31 against the expert's tokens, K = H streamed in 64-wide slabs.  A
-// down tile is (e, 64 rows of H) against the expert's h rows, K = I.  All gate/up
-// tiles come before all down tiles in one tile sequence that CTAs claim with an
-// atomic counter, so a down tile only ever waits (bounded) on gate/up tiles that
-// running CTAs already own; a per-expert counter (one increment per consumer warp and
-// gate/up tile) says when an expert's h is complete.
+// Orientation ("swap AB"): the weights are the MMA's M side (128 weight rows per
+// tile) and the expert's tokens the N side (up to 128 per tile, padded to 16), so a
+// decode step with 1-64 tokens per expert still fills the 128-row MMA and its cost is
+// the weight stream alone.  Both operands are K-major, loaded by TMA as 64-element
+// (128-byte) slabs with the 128-byte swizzle.
 //
-// Per CTA: one producer warp (one lane issues TMA 2-D loads of the weight slab and of
-// the token rows into a 10-stage ring, 128-byte swizzled) and four consumer warps.
-// Consumer warp w owns one m16 tile.  For gate/up its rows 0-7 are gate rows and rows
-// 8-15 the SAME rows of up, so each thread's mma.sync accumulators hold matching gate
-// and up values and SiLU(g)*u is formed in registers.  Tokens are the mma N dim
-// (8 per n-tile, weights are the "A" operand: swap-AB), fp32 accumulation.
+// Tiles: gate/up tile = (expert e, 128 rows of I, 128-token chunk): two MMAs per
+// k-step, gate into TMEM columns [0, N) and up into [128, 128+N), so one epilogue
+// thread (TMEM lane = weight row) holds g and u of the same row and forms
+// SiLU(g)*u in registers.  Down tile = (e, 128 rows of H, token chunk) over the
+// expert's h rows.  All gate/up tiles precede all down tiles in one list that CTAs
+// claim with an atomic counter; a down tile waits (bounded) until every epilogue warp
+// of every gate/up tile of its expert has published h.
 //
-// The token rows are gathered into permuted order first (x_perm), so every expert's
-// rows are contiguous and one TMA box covers 16 of them.
+// Roles per CTA (one CTA per SM): warp 0 lane 0 issues TMA loads into a 4-stage ring;
+// warp 1 owns the TMEM allocation and lane 0 issues the MMAs (tcgen05.commit frees a
+// stage when its MMAs are done, and hands a finished accumulator to the epilogue);
+// warps 2-5 are the epilogue (warp w reads TMEM lanes 32*(w%4)..+31), with two
+// accumulator buffers so the epilogue of one tile overlaps the MMAs of the next.
+//
+// The token rows are first gathered into permuted order (x_perm) so that every
+// expert's rows are contiguous for TMA; the same prep kernel builds the tile list.
 #include "moe_internal.cuh"
 
 #include <cuda.h>
@@ -27,29 +32,38 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 10;
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (1 + kConsumerWarps) * 32;
-constexpr int kSlab = 64;                 // k elements per stage: one 128-byte swizzle row
-constexpr int kGURows = 32;               // I rows per gate/up tile (x2 matrices)
-constexpr int kDnRows = 64;               // H rows per down tile
-constexpr int kNBox = 16;                 // token rows per activation TMA box
-constexpr int kMaxN = 64;                 // tokens per expert on this path
-constexpr int kNTiles = kMaxN / 8;
-constexpr int kABytes = 8192;             // gate 4 KB + up 4 KB, or down 8 KB
-constexpr int kBBytes = kMaxN * 128;      // up to 64 token rows x 128 B
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 1024 /*barriers + meta*/;
+constexpr int kStages = 4;
+constexpr int kRows = 128;                 // weight rows per tile (MMA M)
+constexpr int kMaxN = 128;                 // tokens per tile (MMA N, multiple of 16)
+constexpr int kSlab = 64;                  // k elements per stage (one 128-byte swizzle row)
+constexpr int kNBox = 16;                  // token rows per activation TMA box
+constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
+constexpr int kBBytes = kMaxN * 128;       // 16 KB per token slab
+constexpr int kStageBytes = 2 * kABytes + kBBytes;
+constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
+constexpr int kBufCols = 256;
+constexpr int kUpCol = 128;                // up accumulator column offset inside a buffer
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kMetaRing = 8;
+constexpr int kCtrlBytes = 1024;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*alignment*/ + kCtrlBytes;
 constexpr long long kSpinLimit = 1ll << 22;
 
+// Tile list entry: bit 31 = down tile, bits 16-23 expert, bits 8-15 row block, bits 0-7 token chunk.
+__host__ __device__ constexpr uint32_t pack_tile(int down, int e, int rb, int nc) {
+    return (uint32_t(down) << 31) | (uint32_t(e) << 16) | (uint32_t(rb) << 8) | uint32_t(nc);
+}
+
 struct Params {
-    const int32_t *offsets;   // [E+1]
-    const int32_t *active;    // [1+E]
+    const int32_t *offsets;     // [E+1]
+    const uint32_t *tiles;      // tile list
+    const int *n_tiles;         // its length
     int *tile_counter;
-    int *done;                // [E] finished gate/up tiles per expert
+    int *done;                  // [E] published gate/up tiles (per epilogue warp)
     int32_t *err;
-    uint16_t *h;              // [A][I] bf16
-    uint16_t *y;              // [A][H] bf16
+    uint16_t *h;                // [A][I] bf16
+    uint16_t *y;                // [A][H] bf16
     int E, H, I, A;
 };
 
@@ -58,19 +72,15 @@ struct Params {
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
 }
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -83,8 +93,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: after kSpinLimit polls record the error, raise the CTA's abort flag
-// (so that every later wait of the CTA gives up at once) and carry on.
+// Bounded wait: after kSpinLimit polls record the error and raise the CTA's abort flag,
+// so that every later wait of the CTA gives up at once and the kernel drains.
 __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, int32_t *err, volatile int *abort) {
     long long n = 0;
     while (!mbar_try_wait(bar, parity)) {
@@ -104,90 +114,139 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128 B, 8-row
+// groups 1024 B apart (stride byte offset), fixed version bits 46-48 = 0b001.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+           (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, M x N.
+__device__ __forceinline__ uint32_t instr_desc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
 }
 
-// Byte offset of 16-byte chunk j of row r in a 128-byte-swizzled tile (rows of 128 B).
-__device__ __forceinline__ uint32_t swz(int r, int j) { return uint32_t(r * 128 + ((j ^ (r & 7)) << 4)); }
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
 
-struct Tile {
-    bool gate_up;
-    int e, rb, off, m;
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct TileInfo {
+    int down, e, rb, r0, m, N;
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, int n_gu, const Params &p) {
-    Tile d;
-    const int gu_per = p.I / kGURows, dn_per = p.H / kDnRows;
-    d.gate_up = t < n_gu;
-    const int r = d.gate_up ? t : t - n_gu;
-    const int per = d.gate_up ? gu_per : dn_per;
-    d.e = __ldg(p.active + 1 + r / per);
-    d.rb = r % per;
-    d.off = __ldg(p.offsets + d.e);
-    d.m = __ldg(p.offsets + d.e + 1) - d.off;
+__device__ __forceinline__ TileInfo read_tile(uint32_t entry, const Params &p, bool &ok) {
+    TileInfo d;
+    d.down = int(entry >> 31);
+    d.e = int((entry >> 16) & 0xFF);
+    d.rb = int((entry >> 8) & 0xFF);
+    const int nc = int(entry & 0xFF);
+    ok = d.e < p.E;
+    const int off = ok ? __ldg(p.offsets + d.e) : 0;
+    const int me = ok ? __ldg(p.offsets + d.e + 1) - off : 0;
+    d.r0 = off + nc * kMaxN;
+    d.m = min(kMaxN, me - nc * kMaxN);
+    ok = ok && off >= 0 && me >= 0 && off + me <= p.A && d.m > 0;
+    if (!ok) {  // inconsistent offsets or tile entry: load in-range rows, store nothing
+        d.m = 0;
+        d.r0 = 0;
+        d.e = min(d.e, p.E - 1);
+    }
+    d.N = d.m > 0 ? (d.m + 15) & ~15 : 16;
     return d;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-stream_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
-                     const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_x,
-                     const __grid_constant__ CUtensorMap tm_h, const Params p) {
+tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
+                 const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_x,
+                 const __grid_constant__ CUtensorMap tm_h, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
-    uint64_t *empty = full + kStages;
-    int *meta = reinterpret_cast<int *>(empty + kStages);  // [kStages][8]: tile, slab, gate_up, e, rb, off, m
-    volatile int *abort = meta + 8 * kStages;
+    uint8_t *ctrl = smem + kStages * kStageBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(ctrl);           // [kStages]
+    uint64_t *empty = full + kStages;                              // [kStages]
+    uint64_t *accf = empty + kStages;                              // [2]
+    uint64_t *acce = accf + 2;                                     // [2]
+    uint64_t *tmf = acce + 2;                                      // [kMetaRing]
+    uint64_t *tme = tmf + kMetaRing;                               // [kMetaRing]
+    uint64_t *drain = tme + kMetaRing;                             // [1]
+    int *smeta = reinterpret_cast<int *>(drain + 1);               // [kStages][4]: down, ks, nslab, N
+    int *tmeta = smeta + 4 * kStages;                              // [kMetaRing][8]
+    volatile int *abort = tmeta + 8 * kMetaRing;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmeta + 8 * kMetaRing + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), kConsumerWarps);
+            mbar_init(smem_u32(&empty[s]), 1);
         }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&accf[b]), 1);
+            mbar_init(smem_u32(&acce[b]), kEpiWarps);
+        }
+        for (int s = 0; s < kMetaRing; ++s) {
+            mbar_init(smem_u32(&tmf[s]), 1);
+            mbar_init(smem_u32(&tme[s]), kEpiWarps);
+        }
+        mbar_init(smem_u32(drain), 1);
         *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "n"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int n_tiles = *p.n_tiles;
 
-    const int n_active = __ldg(p.active);
-    const int n_gu = n_active * (p.I / kGURows);
-    const int n_tiles = n_gu + n_active * (p.H / kDnRows);
-
-    if (warp == 0) {
-        // ------------------------------------------------ producer
-        if (lane != 0) return;
-        int stage = 0;
-        uint32_t phase = 0;
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int stage = 0, slot = 0;
+        uint32_t phase = 0, mphase = 0;
+        int next = atomicAdd(p.tile_counter, 1);
         for (;;) {
-            const int t = atomicAdd(p.tile_counter, 1);
-            if (t >= n_tiles) break;
-            Tile d = decode_tile(t, n_gu, p);
-            if (d.off < 0 || d.m < 0 || d.m > kMaxN || d.off + d.m > p.A) {
-                // inconsistent offsets: record, and compute nothing for this expert
-                record_error(p.err, MOE_ERR_DEVICE);
-                d.m = 0;
-                d.off = 0;
-            }
-            const int nbox = (d.m + kNBox - 1) / kNBox;
-            if (!d.gate_up) {
-                // the expert's h must be complete: every consumer warp of all its gate/up tiles
-                const int need = (p.I / kGURows) * kConsumerWarps;
+            const int t = next;
+            if (t >= n_tiles || *abort) break;
+            next = atomicAdd(p.tile_counter, 1);  // claim ahead: its latency hides behind this tile
+            bool ok;
+            const TileInfo d = read_tile(__ldg(p.tiles + t), p, ok);
+            if (!ok) record_error(p.err, MOE_ERR_DEVICE);
+            if (d.down) {
+                // the expert's h must be complete: every epilogue warp of every gate/up tile
+                const int me = __ldg(p.offsets + d.e + 1) - __ldg(p.offsets + d.e);
+                const int need = (p.I / kRows) * ((me + kMaxN - 1) / kMaxN) * kEpiWarps;
                 long long n = 0;
                 for (;;) {
                     int v;
@@ -202,160 +261,222 @@ stream_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_c
                 }
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
-            const int nslab = (d.gate_up ? p.H : p.I) / kSlab;
-            const uint32_t bytes = kABytes + nbox * kNBox * 128;
+            // hand the tile to the epilogue
+            mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, p.err, abort);
+            int *tm = tmeta + 8 * slot;
+            tm[0] = d.down;
+            tm[1] = d.e;
+            tm[2] = d.rb;
+            tm[3] = d.r0;
+            tm[4] = d.m;
+            tm[5] = d.N;
+            mbar_arrive(smem_u32(&tmf[slot]));
+            if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
+
+            const int nslab = (d.down ? p.I : p.H) / kSlab;
+            const int nbox = d.N / kNBox;
+            const uint32_t bytes = (d.down ? kABytes : 2 * kABytes) + nbox * kNBox * 128;
+            const int wrow = d.e * (d.down ? p.H : p.I) + d.rb * kRows;
             for (int ks = 0; ks < nslab; ++ks) {
                 mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort);
-                int *mt = meta + 8 * stage;
-                mt[0] = t;
-                mt[1] = ks;
-                mt[2] = d.gate_up;
-                mt[3] = d.e;
-                mt[4] = d.rb;
-                mt[5] = d.off;
-                mt[6] = d.m;
+                int *sm = smeta + 4 * stage;
+                sm[0] = d.down;
+                sm[1] = ks;
+                sm[2] = nslab;
+                sm[3] = d.N;
                 const uint32_t fb = smem_u32(&full[stage]);
                 mbar_arrive_expect_tx(fb, bytes);
-                const uint32_t a = smem_u32(smem + stage * kStageBytes);
-                const uint32_t b = a + kABytes;
-                if (d.gate_up) {
-                    const int row = d.e * p.I + d.rb * kGURows;
-                    tma_load_2d(a, &tm_gate, ks * kSlab, row, fb);
-                    tma_load_2d(a + 4096, &tm_up, ks * kSlab, row, fb);
-                    for (int q = 0; q < nbox; ++q) tma_load_2d(b + q * 2048, &tm_x, ks * kSlab, d.off + q * kNBox, fb);
+                const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
+                const uint32_t bb = a0 + 2 * kABytes;
+                if (d.down) {
+                    tma_load_2d(a0, &tm_down, ks * kSlab, wrow, fb);
+                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * 2048, &tm_h, ks * kSlab, d.r0 + q * kNBox, fb);
                 } else {
-                    tma_load_2d(a, &tm_down, ks * kSlab, d.e * p.H + d.rb * kDnRows, fb);
-                    for (int q = 0; q < nbox; ++q) tma_load_2d(b + q * 2048, &tm_h, ks * kSlab, d.off + q * kNBox, fb);
+                    tma_load_2d(a0, &tm_gate, ks * kSlab, wrow, fb);
+                    tma_load_2d(a0 + kABytes, &tm_up, ks * kSlab, wrow, fb);
+                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * 2048, &tm_x, ks * kSlab, d.r0 + q * kNBox, fb);
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
         }
-        // sentinel: tell the consumers there is no more work
+        // sentinels for the MMA issuer and the epilogue
+        mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, p.err, abort);
+        tmeta[8 * slot] = -1;
+        mbar_arrive(smem_u32(&tmf[slot]));
         mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort);
-        meta[8 * stage] = -1;
+        smeta[4 * stage + 1] = -1;
         mbar_arrive(smem_u32(&full[stage]));
-        return;
-    }
-
-    // ---------------------------------------------------- consumers
-    const int cw = warp - 1;
-    const int g = lane >> 2, c = lane & 3;
-    const int mat = lane >> 3, r8 = lane & 7;
-    int stage = 0;
-    uint32_t phase = 0;
-    float acc[kNTiles][4];
-    Tile d{};
-    int nt = 0;
-    for (;;) {
-        mbar_wait(smem_u32(&full[stage]), phase, p.err, abort);
-        const int *mt = meta + 8 * stage;
-        const int t = mt[0];
-        const int ks = mt[1];
-        if (t < 0 || *abort) break;
-        if (ks == 0) {
-            d.gate_up = mt[2] != 0;
-            d.e = mt[3];
-            d.rb = mt[4];
-            d.off = mt[5];
-            d.m = mt[6];
-            nt = (d.m + 7) >> 3;
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int tile_count = 0;
+        for (;;) {
+            mbar_wait(smem_u32(&full[stage]), phase, p.err, abort);
+            const int *sm = smeta + 4 * stage;
+            const int down = sm[0], ks = sm[1], nslab = sm[2], N = sm[3];
+            if (ks < 0 || *abort) break;
+            const int b = tile_count & 1;
+            if (ks == 0) {
+                mbar_wait(smem_u32(&acce[b]), ((tile_count >> 1) & 1) ^ 1, p.err, abort);
+                tc_fence_after();
+            }
+            const uint32_t d = tmem_base + uint32_t(b * kBufCols);
+            const uint32_t idesc = instr_desc(kRows, N);
+            const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
+            const uint32_t bb = a0 + 2 * kABytes;
 #pragma unroll
-            for (int u = 0; u < kNTiles; ++u)
-                acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+            for (int kk = 0; kk < kSlab / 16; ++kk) {
+                const uint32_t acc = (ks | kk) != 0;
+                const uint64_t bdesc = smem_desc(bb + kk * 32);
+                mma_bf16(d, smem_desc(a0 + kk * 32), bdesc, idesc, acc);
+                if (!down) mma_bf16(d + kUpCol, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, acc);
+            }
+            mma_commit(smem_u32(&empty[stage]));  // the stage's smem is free once these MMAs are done
+            if (ks == nslab - 1) {
+                mma_commit(smem_u32(&accf[b]));   // accumulator complete: hand to the epilogue
+                ++tile_count;
+            }
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-        const uint32_t a = smem_u32(smem + stage * kStageBytes);
-        const uint32_t b = a + kABytes;
-        // this lane's ldmatrix row for the A operand
-        uint32_t a_row_base;
-        if (d.gate_up) a_row_base = a + ((mat & 1) ? 4096u : 0u) + uint32_t((8 * cw + r8) * 128);
-        else a_row_base = a + uint32_t((16 * cw + 8 * (mat & 1) + r8) * 128);
+        // every MMA this thread issued has completed before TMEM is released
+        mma_commit(smem_u32(drain));
+        mbar_wait(smem_u32(drain), 0, p.err, abort);
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        const int row = 32 * q + lane;
+        int slot = 0, tile_count = 0;
+        uint32_t mphase = 0;
+        for (;;) {
+            mbar_wait(smem_u32(&tmf[slot]), mphase, p.err, abort);
+            const int *tm = tmeta + 8 * slot;
+            const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], N = tm[5];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tme[slot]));
+            if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
+            if (down < 0 || *abort) break;
+            const int b = tile_count & 1;
+            mbar_wait(smem_u32(&accf[b]), (tile_count >> 1) & 1, p.err, abort);
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(b * kBufCols);
+            const size_t col = (size_t)rb * kRows + row;
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                if (down) {
+                    float v[16];
+                    tmem_ld16(taddr + c0, v);
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            uint32_t af[4];
-            const int j = 2 * s + (mat >> 1);
-            ldsm_x4(a_row_base + uint32_t((j ^ r8) << 4), af[0], af[1], af[2], af[3]);
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < m) p.y[(size_t)(r0 + c0 + j) * p.H + col] = f32_to_bf16_bits(v[j]);
+                } else {
+                    float g[16], u[16];
+                    tmem_ld16(taddr + c0, g);
+                    tmem_ld16(taddr + kUpCol + c0, u);
 #pragma unroll
-            for (int u = 0; u < kNTiles; ++u) {
-                if (u < nt) {
-                    uint32_t b0, b1;
-                    const int jb = 2 * s + (mat & 1);
-                    ldsm_x2(b + swz(8 * u + r8, jb), b0, b1);
-                    mma_bf16(acc[u], af, b0, b1);
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < m) p.h[(size_t)(r0 + c0 + j) * p.I + col] = f32_to_bf16_bits(swiglu(g[j], u[j]));
                 }
             }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
-
-        const int nslab = (d.gate_up ? p.H : p.I) / kSlab;
-        if (ks == nslab - 1) {
-            if (d.gate_up) {
-                const int i = d.rb * kGURows + 8 * cw + g;
-#pragma unroll
-                for (int u = 0; u < kNTiles; ++u) {
-                    if (u < nt) {
-                        const int tok = 8 * u + 2 * c;
-                        if (tok < d.m)
-                            p.h[(size_t)(d.off + tok) * p.I + i] = f32_to_bf16_bits(swiglu(acc[u][0], acc[u][2]));
-                        if (tok + 1 < d.m)
-                            p.h[(size_t)(d.off + tok + 1) * p.I + i] = f32_to_bf16_bits(swiglu(acc[u][1], acc[u][3]));
-                    }
-                }
-                // publish this warp's h stores (they are read back through TMA): one
-                // release increment per consumer warp and tile
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acce[b]));
+            if (!down && e < p.E) {
+                // publish this warp's h rows (read back through TMA by down tiles)
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
                     __threadfence();
-                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done + d.e) : "memory");
-                }
-            } else {
-                const int r = d.rb * kDnRows + 16 * cw + g;
-#pragma unroll
-                for (int u = 0; u < kNTiles; ++u) {
-                    if (u < nt) {
-                        const int tok = 8 * u + 2 * c;
-                        if (tok < d.m) {
-                            p.y[(size_t)(d.off + tok) * p.H + r] = f32_to_bf16_bits(acc[u][0]);
-                            p.y[(size_t)(d.off + tok) * p.H + r + 8] = f32_to_bf16_bits(acc[u][2]);
-                        }
-                        if (tok + 1 < d.m) {
-                            p.y[(size_t)(d.off + tok + 1) * p.H + r] = f32_to_bf16_bits(acc[u][1]);
-                            p.y[(size_t)(d.off + tok + 1) * p.H + r + 8] = f32_to_bf16_bits(acc[u][3]);
-                        }
-                    }
+                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done + e) : "memory");
                 }
             }
+            ++tile_count;
         }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kTmemCols)
+                     : "memory");
     }
 }
 
-// x_perm[p] = x[order[p] / k]; block 0 also rebuilds the active-expert list from the
-// offsets and clears the scheduling counters of the streaming kernel.
-__global__ void __launch_bounds__(256)
-gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order,
-                   const int32_t *__restrict__ offsets, int T, int k, int H, int E, uint16_t *__restrict__ x_perm,
-                   int32_t *active, int *tile_counter, int *done, int32_t *err) {
-    const int pr = blockIdx.x;
-    const int a = __ldg(order + pr);
-    uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
-    if (a < 0 || a >= T * k) {
-        if (threadIdx.x == 0) record_error(err, MOE_ERR_DEVICE);
-        for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
-    } else {
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(a / k) * H);
-        for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+// Block-wide exclusive scan of one int per thread (blockDim.x == 256).
+__device__ int scan256(int v, int *s_warp, int &total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
     }
-    if (pr == 0) {
-        if (threadIdx.x == 0) {
-            int n = 0;
-            for (int e = 0; e < E; ++e)
-                if (offsets[e + 1] > offsets[e]) active[1 + n++] = e;
-            active[0] = n;
-            *tile_counter = 0;
+    if (lane == 31) s_warp[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        const int wv = lane < 8 ? s_warp[lane] : 0;
+        int i2 = wv;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, i2, o);
+            if (lane >= o) i2 += n;
         }
-        for (int e = threadIdx.x; e < E; e += blockDim.x) done[e] = 0;
+        if (lane < 8) s_warp[lane] = i2 - wv;
+        if (lane == 7) s_warp[8] = i2;
+    }
+    __syncthreads();
+    const int excl = s_warp[w] + incl - v;
+    total = s_warp[8];
+    __syncthreads();
+    return excl;
+}
+
+// x_perm[p] = x[order[p] / k].  Block 0 also builds the tile list from the offsets
+// and clears the scheduling counters of the tensor-core kernel.
+__global__ void __launch_bounds__(256)
+prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
+            int T, int k, int H, int I, int E, uint16_t *__restrict__ x_perm, uint32_t *tiles, int max_tiles,
+            int *n_tiles, int *tile_counter, int *done, int32_t *err) {
+    if (blockIdx.x > 0) {
+        const int pr = blockIdx.x - 1;
+        const int a = __ldg(order + pr);
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
+        if (a < 0 || a >= T * k) {
+            if (threadIdx.x == 0) record_error(err, MOE_ERR_DEVICE);
+            for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+        } else {
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(a / k) * H);
+            for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+        }
+        return;
+    }
+    __shared__ int s_warp[9];
+    const int e = threadIdx.x;
+    int me = 0;
+    if (e < E) {
+        me = min(max(offsets[e + 1] - offsets[e], 0), T * k);
+        done[e] = 0;
+    }
+    const int nch = me > 0 ? (me + kMaxN - 1) / kMaxN : 0;
+    const int gu_per = I / kRows, dn_per = H / kRows;
+    int n_gu, n_dn;
+    const int gu_off = scan256(nch * gu_per, s_warp, n_gu);
+    const int dn_off = scan256(nch * dn_per, s_warp, n_dn);
+    for (int c = 0; c < nch; ++c) {
+        for (int r = 0; r < gu_per; ++r) {
+            const int i = gu_off + c * gu_per + r;
+            if (i < max_tiles) tiles[i] = pack_tile(0, e, r, c);
+        }
+        for (int r = 0; r < dn_per; ++r) {
+            const int i = n_gu + dn_off + c * dn_per + r;
+            if (i < max_tiles) tiles[i] = pack_tile(1, e, r, c);
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (n_gu + n_dn > max_tiles) record_error(err, MOE_ERR_DEVICE);  // inconsistent offsets
+        *n_tiles = min(n_gu + n_dn, max_tiles);
+        *tile_counter = 0;
     }
 }
 
@@ -404,44 +525,51 @@ int sm_count() {
     return n[dev];
 }
 
+constexpr int kMaxT = 8192;
+
 size_t xperm_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * s.H * 2 + 255) / 256 * 256; }
+size_t max_tiles(const moe_shape &s) {
+    const size_t chunks = (size_t)s.E + ((size_t)s.T * s.k + kMaxN - 1) / kMaxN;
+    return chunks * (size_t)(s.I / kRows + s.H / kRows);
+}
 
 }  // namespace
 
-// 0 = the per-output-element kernels of grouped_simple.cu; 1 = the weight-streaming kernel.
+// 0 = the per-output-element kernels of grouped_simple.cu; 1 = the tensor-core kernel.
 int select_grouped_path(const moe_shape &s) {
-    if (s.act_dtype == MOE_DT_BF16 && s.w_dtype == MOE_DT_BF16 && s.T >= 1 && s.T <= kMaxN && s.H % kDnRows == 0 &&
-        s.I % kSlab == 0)
+    if (s.act_dtype == MOE_DT_BF16 && s.w_dtype == MOE_DT_BF16 && s.T >= 1 && s.T <= kMaxT && s.H % kRows == 0 &&
+        s.I % kRows == 0 && s.H / kRows <= 256 && s.I / kRows <= 256)
         return 1;
     return 0;
 }
 
 size_t grouped_fast_part_bytes(int path, const moe_shape &s) {
     if (path != 1) return 0;
-    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4;
+    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (max_tiles(s) * 4 + 255) / 256 * 256;
 }
 
 int grouped_fast_launches(int path, const moe_shape &) { return path == 1 ? 2 : 0; }
 
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
-                                const moe_q4 *, const int32_t *active, float *part, void *h, void *y,
-                                int32_t *err, cudaStream_t st) {
+                                const moe_q4 *, const int32_t *, float *part, void *h, void *y, int32_t *err,
+                                cudaStream_t st) {
     if (path != 1) return cudaErrorInvalidValue;
     const int A = s.T * s.k;
-    uint16_t *x_perm = reinterpret_cast<uint16_t *>(part);
-    int *sched = reinterpret_cast<int *>(reinterpret_cast<char *>(part) + xperm_bytes(s));
-    int *tile_counter = sched, *done = sched + 64;
-    int32_t *act = const_cast<int32_t *>(active);
+    char *base = reinterpret_cast<char *>(part);
+    uint16_t *x_perm = reinterpret_cast<uint16_t *>(base);
+    int *sched = reinterpret_cast<int *>(base + xperm_bytes(s));
+    int *tile_counter = sched, *n_tiles = sched + 1, *done = sched + 64;
+    uint32_t *tiles = reinterpret_cast<uint32_t *>(base + xperm_bytes(s) + 256 + (size_t)kMaxE * 4);
 
     CUtensorMap mg, mu, md, mx, mh;
-    if (!make_map(&mg, wg, (uint64_t)s.E * s.I, s.H, kGURows) || !make_map(&mu, wu, (uint64_t)s.E * s.I, s.H, kGURows) ||
-        !make_map(&md, wd, (uint64_t)s.E * s.H, s.I, kDnRows) || !make_map(&mx, x_perm, A, s.H, kNBox) ||
+    if (!make_map(&mg, wg, (uint64_t)s.E * s.I, s.H, kRows) || !make_map(&mu, wu, (uint64_t)s.E * s.I, s.H, kRows) ||
+        !make_map(&md, wd, (uint64_t)s.E * s.H, s.I, kRows) || !make_map(&mx, x_perm, A, s.H, kNBox) ||
         !make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
 
-    gather_rows_kernel<<<A, 256, 0, st>>>(static_cast<const uint16_t *>(x), order, offsets, s.T, s.k, s.H, s.E,
-                                          x_perm, act, tile_counter, done, err);
+    prep_kernel<<<A + 1, 256, 0, st>>>(static_cast<const uint16_t *>(x), order, offsets, s.T, s.k, s.H, s.I, s.E,
+                                       x_perm, tiles, (int)max_tiles(s), n_tiles, tile_counter, done, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -449,13 +577,13 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(stream_swiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(tc_swiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    Params prm{offsets, active, tile_counter, done, err, static_cast<uint16_t *>(h), static_cast<uint16_t *>(y),
-               s.E, s.H, s.I, A};
-    stream_swiglu_kernel<<<sm_count(), kThreads, kSmemBytes, st>>>(mg, mu, md, mx, mh, prm);
+    Params prm{offsets, tiles, n_tiles, tile_counter, done, err, static_cast<uint16_t *>(h),
+               static_cast<uint16_t *>(y), s.E, s.H, s.I, A};
+    tc_swiglu_kernel<<<sm_count(), kThreads, kSmemBytes, st>>>(mg, mu, md, mx, mh, prm);
     return cudaGetLastError();
 }
 
