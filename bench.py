@@ -313,22 +313,35 @@ def run_ours(args, rank, world, local):
     ord_b = [torch.empty(T * k, dtype=torch.int32, device=dev) for _ in layers]
     pos_b = [torch.empty(T * k, dtype=torch.int32, device=dev) for _ in layers]
     y_b = [torch.empty((T * k, H), dtype=out_dt, device=dev) for _ in layers]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kt_steps)]
+    # per entry point: events around each op of the step, ops launched eagerly back to back
+    ops = ("route", "permute", "grouped_swiglu", "unpermute")
+    kev = {o: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(kt_steps)] for o in ops}
+    out_b = [torch.empty((T, H), dtype=out_dt, device=dev) for _ in layers]
+
+    def timed(name, i, fn):
+        if i >= 3:
+            kev[name][i - 3][0].record(stream)
+        fn()
+        if i >= 3:
+            kev[name][i - 3][1].record(stream)
+
     with torch.cuda.stream(stream):
-        for l, L in enumerate(dl[0]):
-            moe.moe_route(L.shape, L.x, L.w_router, L.b_router, ids_b[l], w_b[l], workspace=wss[l], stream=stream)
-            moe.moe_permute(L.shape, ids_b[l], cnt_b[l], off_b[l], ord_b[l], pos_b[l], wss[l], stream=stream)
         for i in range(kt_steps + 3):
             c = i % n_copies
-            if i >= 3:
-                kev[i - 3][0].record(stream)
-            for l, L in enumerate(dl[c]):
-                moe.moe_grouped_swiglu(L.shape, dl[0][l].x, off_b[l], ord_b[l], L.w_gate, L.w_up, L.w_down, L.q4,
-                                       y_b[l], wss[l], stream=stream)
-            if i >= 3:
-                kev[i - 3][1].record(stream)
+            timed("route", i, lambda: [moe.moe_route(L.shape, dl[0][l].x, L.w_router, L.b_router, ids_b[l], w_b[l],
+                                                     workspace=wss[l], stream=stream) for l, L in enumerate(dl[c])])
+            timed("permute", i, lambda: [moe.moe_permute(L.shape, ids_b[l], cnt_b[l], off_b[l], ord_b[l], pos_b[l],
+                                                         wss[l], stream=stream) for l, L in enumerate(dl[c])])
+            timed("grouped_swiglu", i, lambda: [moe.moe_grouped_swiglu(L.shape, dl[0][l].x, off_b[l], ord_b[l],
+                                                                       L.w_gate, L.w_up, L.w_down, L.q4, y_b[l],
+                                                                       wss[l], stream=stream)
+                                                for l, L in enumerate(dl[c])])
+            timed("unpermute", i, lambda: [moe.moe_unpermute(L.shape, y_b[l], w_b[l], pos_b[l], out_b[l],
+                                                             stream=stream) for l, L in enumerate(dl[c])])
     torch.cuda.synchronize()
-    k_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    breakdown = {o: statistics.mean(a.elapsed_time(b) for a, b in kev[o]) * 1e3 for o in ops}
+    k_ms = breakdown["grouped_swiglu"] / 1e3
 
     # end to end through the public API: pinned host tokens in, host result out, every step
     x_host = [to_device(l.x, "cpu", pin=True) for l in layers]
@@ -385,6 +398,7 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": world * tokens_per_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
         "gpu_launches": launches * args.steps,
+        "breakdown_us": {**breakdown, "note": "each entry point timed alone (eager launches, CUDA events)"},
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -107,9 +107,10 @@ typedef struct {
 /*
  * Workspace bytes the entry points below need for this shape (host only, no
  * CUDA call).  The same workspace serves every entry point; it must be
- * 256-byte aligned.  Its first 256 bytes hold the device error word and must
- * be zeroed once before first use (moe_read_device_error clears the word
- * again).  Returns MOE_ERR_NULLPTR / MOE_ERR_SHAPE / MOE_ERR_DTYPE on bad
+ * 256-byte aligned.  Its first 256 bytes hold the device error word and
+ * scheduling counters and must be zeroed once before first use; the kernels
+ * leave the counters at zero again (moe_read_device_error clears the error
+ * word).  Returns MOE_ERR_NULLPTR / MOE_ERR_SHAPE / MOE_ERR_DTYPE on bad
  * arguments.
  */
 MOE_API int moe_workspace_size(const moe_shape *shape, size_t *bytes);

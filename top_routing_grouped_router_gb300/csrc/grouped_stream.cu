@@ -196,7 +196,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     uint64_t *tmf = acce + 2;                                      // [kMetaRing]
     uint64_t *tme = tmf + kMetaRing;                               // [kMetaRing]
     uint64_t *drain = tme + kMetaRing;                             // [1]
-    int *smeta = reinterpret_cast<int *>(drain + 1);               // [kStages][4]: down, ks, nslab, N
+    int *smeta = reinterpret_cast<int *>(drain + 1);               // [kStages][4]: down|two<<1, ks, nstage, N
     int *tmeta = smeta + 4 * kStages;                              // [kMetaRing][8]
     volatile int *abort = tmeta + 8 * kMetaRing;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmeta + 8 * kMetaRing + 4);
@@ -273,22 +273,34 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             mbar_arrive(smem_u32(&tmf[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
 
+            // a down tile with at most 64 tokens takes two k-slabs per stage (weights in
+            // both A regions, token rows in the two halves of B), so every stage carries
+            // 32 KB of weights whatever the tile kind
+            const int two = d.down && d.N <= kMaxN / 2 && (p.I / kSlab) % 2 == 0;
             const int nslab = (d.down ? p.I : p.H) / kSlab;
+            const int nstage = two ? nslab / 2 : nslab;
             const int nbox = d.N / kNBox;
-            const uint32_t bytes = (d.down ? kABytes : 2 * kABytes) + nbox * kNBox * 128;
+            const uint32_t bytes = (d.down && !two ? kABytes : 2 * kABytes) + (two ? 2 : 1) * nbox * kNBox * 128;
             const int wrow = d.e * (d.down ? p.H : p.I) + d.rb * kRows;
-            for (int ks = 0; ks < nslab; ++ks) {
+            for (int ks = 0; ks < nstage; ++ks) {
                 mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort);
                 int *sm = smeta + 4 * stage;
-                sm[0] = d.down;
+                sm[0] = d.down | (two << 1);
                 sm[1] = ks;
-                sm[2] = nslab;
+                sm[2] = nstage;
                 sm[3] = d.N;
                 const uint32_t fb = smem_u32(&full[stage]);
                 mbar_arrive_expect_tx(fb, bytes);
                 const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
                 const uint32_t bb = a0 + 2 * kABytes;
-                if (d.down) {
+                if (two) {
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int k0 = (2 * ks + h2) * kSlab;
+                        tma_load_2d(a0 + h2 * kABytes, &tm_down, k0, wrow, fb);
+                        for (int q = 0; q < nbox; ++q)
+                            tma_load_2d(bb + h2 * (kBBytes / 2) + q * 2048, &tm_h, k0, d.r0 + q * kNBox, fb);
+                    }
+                } else if (d.down) {
                     tma_load_2d(a0, &tm_down, ks * kSlab, wrow, fb);
                     for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * 2048, &tm_h, ks * kSlab, d.r0 + q * kNBox, fb);
                 } else {
@@ -314,7 +326,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         for (;;) {
             mbar_wait(smem_u32(&full[stage]), phase, p.err, abort);
             const int *sm = smeta + 4 * stage;
-            const int down = sm[0], ks = sm[1], nslab = sm[2], N = sm[3];
+            const int down = sm[0] & 1, two = sm[0] >> 1, ks = sm[1], nslab = sm[2], N = sm[3];
             if (ks < 0 || *abort) break;
             const int b = tile_count & 1;
             if (ks == 0) {
@@ -325,12 +337,21 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const uint32_t idesc = instr_desc(kRows, N);
             const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
             const uint32_t bb = a0 + 2 * kABytes;
+            if (two) {
 #pragma unroll
-            for (int kk = 0; kk < kSlab / 16; ++kk) {
-                const uint32_t acc = (ks | kk) != 0;
-                const uint64_t bdesc = smem_desc(bb + kk * 32);
-                mma_bf16(d, smem_desc(a0 + kk * 32), bdesc, idesc, acc);
-                if (!down) mma_bf16(d + kUpCol, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, acc);
+                for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                    for (int kk = 0; kk < kSlab / 16; ++kk)
+                        mma_bf16(d, smem_desc(a0 + h2 * kABytes + kk * 32),
+                                 smem_desc(bb + h2 * (kBBytes / 2) + kk * 32), idesc, (ks | h2 | kk) != 0);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < kSlab / 16; ++kk) {
+                    const uint32_t acc = (ks | kk) != 0;
+                    const uint64_t bdesc = smem_desc(bb + kk * 32);
+                    mma_bf16(d, smem_desc(a0 + kk * 32), bdesc, idesc, acc);
+                    if (!down) mma_bf16(d + kUpCol, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, acc);
+                }
             }
             mma_commit(smem_u32(&empty[stage]));  // the stage's smem is free once these MMAs are done
             if (ks == nslab - 1) {

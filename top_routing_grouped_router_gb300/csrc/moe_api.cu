@@ -106,8 +106,7 @@ int do_route(const moe_shape &s, const void *x, const void *wr, const float *b, 
              float *margin, float *logits, void *ws, cudaStream_t st) {
     const WsLayout L = ws_layout(s);
     float *lg = logits ? logits : at<float>(ws, L.logits);
-    MOE_TRY(launch_rc(launch_router_logits(s, x, wr, b, lg, st)));
-    return launch_rc(launch_topk(s, lg, ids, w, margin, st));
+    return launch_rc(launch_route(s, x, wr, b, lg, ids, w, margin, at<int>(ws, kHdrArrivals), st));
 }
 
 int do_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t *offsets, int32_t *order,
@@ -200,8 +199,15 @@ int moe_forward(const moe_shape *shape, const void *x, const void *w_router, con
     int32_t *offsets = at<int32_t>(workspace, L.offsets), *order = at<int32_t>(workspace, L.order),
             *pos = at<int32_t>(workspace, L.pos);
     void *y = at<void>(workspace, L.y);
-    MOE_TRY(do_route(s, x, w_router, b_router, ids, w, nullptr, nullptr, workspace, st));
-    MOE_TRY(do_permute(s, ids, at<int32_t>(workspace, L.counts), offsets, order, pos, workspace, st));
+    if (route_fuses(s)) {
+        MOE_TRY(launch_rc(launch_route_permute(s, x, w_router, b_router, at<float>(workspace, L.logits), ids, w,
+                                               at<int>(workspace, kHdrArrivals), at<int32_t>(workspace, L.counts),
+                                               offsets, order, pos, at<int32_t>(workspace, L.active),
+                                               at<int32_t>(workspace, L.err), st)));
+    } else {
+        MOE_TRY(do_route(s, x, w_router, b_router, ids, w, nullptr, nullptr, workspace, st));
+        MOE_TRY(do_permute(s, ids, at<int32_t>(workspace, L.counts), offsets, order, pos, workspace, st));
+    }
     MOE_TRY(do_grouped(s, x, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st));
     return launch_rc(launch_unpermute(s, y, w, pos, out, st));
 }
@@ -215,7 +221,7 @@ int moe_forward_launches(const moe_shape *shape, int32_t *launches) {
         return MOE_OK;
     }
     const int path = select_grouped_path(s);
-    *launches = route_launches(s) + permute_launches(s) +
+    *launches = (route_fuses(s) ? 1 : route_launches(s) + permute_launches(s)) +
                 (path > 0 ? grouped_fast_launches(path, s) : grouped_simple_launches(s)) + 1;
     return MOE_OK;
 }

@@ -64,10 +64,17 @@ __device__ __forceinline__ void record_error(int32_t *err, int code) { atomicCAS
 
 // ---------------------------------------------------------------- launchers (each returns cudaError_t of the launch)
 
-cudaError_t launch_router_logits(const moe_shape &s, const void *x, const void *wr, const float *bias,
-                                 float *logits, cudaStream_t st);
-cudaError_t launch_topk(const moe_shape &s, const float *logits, int32_t *ids, float *w, float *margin,
-                        cudaStream_t st);
+// Workspace header: error word at byte 0, router arrival counter at byte 64 (both zero
+// between launches).
+constexpr size_t kHdrArrivals = 64;
+
+bool route_fuses(const moe_shape &s);
+cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
+                         int32_t *ids, float *w, float *margin, int *arrivals, cudaStream_t st);
+cudaError_t launch_route_permute(const moe_shape &s, const void *x, const void *wr, const float *bias,
+                                 float *logits, int32_t *ids, float *w, int *arrivals, int32_t *counts,
+                                 int32_t *offsets, int32_t *order, int32_t *pos, int32_t *active, int32_t *err,
+                                 cudaStream_t st);
 cudaError_t launch_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t *offsets,
                            int32_t *order, int32_t *pos, int32_t *active, int32_t *hist, int32_t *err,
                            cudaStream_t st);

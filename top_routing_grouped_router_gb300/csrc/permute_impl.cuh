@@ -1,0 +1,123 @@
+// permute_impl.cuh -- device building blocks of the expert histogram, exclusive scan and
+// stable permutation (the bincount / scatter_add_, cumsum and argsort steps of the
+// grouped_mm MoE path).  Shared by the permute kernels and by the fused routing kernel,
+// so both produce bit-identical results.
+//
+// Stable rank of an assignment inside an NT-assignment chunk: __match_any_sync groups
+// the lanes of a warp that carry the same expert; the rank among them is the popcount
+// of the lower lanes in the group, and the per-warp group sizes (a shared-memory table
+// [NT/32 warps][E]) give the offset contributed by the lower warps of the chunk.
+// Chunks are processed in ascending order, so rows of one expert end up in ascending
+// assignment order.  Integer-only, deterministic.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+// Exclusive scan of s_val[0..E) (E <= 256) by a block of at least 256 threads; returns the total.
+__device__ __forceinline__ int block_excl_scan(const int *s_val, int *s_excl, int E, int *s_warp) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int v = (tid < E) ? s_val[tid] : 0;
+    int incl = v;
+    if (tid < kMaxE) {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (lane == 31) s_warp[w] = incl;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        const int wv = (tid < kMaxE / 32) ? s_warp[tid] : 0;
+        int i2 = wv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, i2, o);
+            if (tid >= o) i2 += n;
+        }
+        if (tid < kMaxE / 32) s_warp[tid] = i2 - wv;
+        if (tid == kMaxE / 32 - 1) s_warp[kMaxE / 32] = i2;
+    }
+    __syncthreads();
+    if (tid < E) s_excl[tid] = s_warp[w] + incl - v;
+    const int total = s_warp[kMaxE / 32];
+    __syncthreads();
+    return total;
+}
+
+template <int NT>
+struct PermuteSmem {
+    int cnt[kMaxE], base[kMaxE], flag[2 * kMaxE], warp[kMaxE / 32 + 1];
+    int wcnt[NT / 32][kMaxE];
+};
+
+// counts / offsets / active-expert list from the block's histogram s.cnt (s.base = offsets).
+template <int NT>
+__device__ void write_counts(PermuteSmem<NT> &s, int E, int32_t *counts, int32_t *offsets, int32_t *active) {
+    const int tid = threadIdx.x;
+    const int total = block_excl_scan(s.cnt, s.base, E, s.warp);
+    if (tid < E) {
+        counts[tid] = s.cnt[tid];
+        offsets[tid] = s.base[tid];
+        s.flag[tid] = s.cnt[tid] > 0;
+    }
+    if (tid == 0) offsets[E] = total;
+    __syncthreads();
+    int *slot = s.flag + kMaxE;
+    const int n_active = block_excl_scan(s.flag, slot, E, s.warp);
+    if (tid < E && s.flag[tid]) active[1 + slot[tid]] = tid;
+    if (tid == 0) active[0] = n_active;
+}
+
+// Scatter the chunk [a0, a0 + NT) given per-expert bases s.base (advanced in place).
+template <int NT>
+__device__ void scatter_chunk(const int32_t *ids, int a0, int A, int E, PermuteSmem<NT> &s, int32_t *order,
+                              int32_t *pos, int32_t *err) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int a = a0 + tid;
+    int e = (a < A) ? __ldcg(ids + a) : -1;
+    if (a < A && (e < 0 || e >= E)) {
+        record_error(err, MOE_ERR_DEVICE);
+        e = -1;
+    }
+    for (int i = lane; i < E; i += 32) s.wcnt[w][i] = 0;
+    __syncwarp();
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const unsigned lower = peers & ((1u << lane) - 1u);
+    if (e >= 0 && lower == 0) s.wcnt[w][e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+        int before = 0;
+        for (int w2 = 0; w2 < w; ++w2) before += s.wcnt[w2][e];
+        const int p = s.base[e] + before + __popc(lower);
+        order[p] = a;
+        pos[a] = p;
+    }
+    __syncthreads();
+    for (int i = tid; i < E; i += NT) {
+        int sum = 0;
+        for (int w2 = 0; w2 < NT / 32; ++w2) sum += s.wcnt[w2][i];
+        s.base[i] += sum;
+    }
+    __syncthreads();
+}
+
+// The whole permutation of A assignments by one block of NT threads.
+template <int NT>
+__device__ void permute_block(const int32_t *ids, int A, int E, int32_t *counts, int32_t *offsets, int32_t *order,
+                              int32_t *pos, int32_t *active, int32_t *err, PermuteSmem<NT> &s) {
+    const int tid = threadIdx.x;
+    for (int i = tid; i < E; i += NT) s.cnt[i] = 0;
+    __syncthreads();
+    for (int a = tid; a < A; a += NT) {
+        const int e = __ldcg(ids + a);
+        if (e >= 0 && e < E) atomicAdd(&s.cnt[e], 1);
+    }
+    __syncthreads();
+    write_counts(s, E, counts, offsets, active);
+    for (int a0 = 0; a0 < A; a0 += NT) scatter_chunk(ids, a0, A, E, s, order, pos, err);
+}
+
+}  // namespace moe

@@ -1,23 +1,35 @@
-// route.cu -- router GEMM (logits = x . W_r^T + b) and per-token softmax / top-k /
-// renormalisation of the Qwen3-MoE sparse block.
+// route.cu -- router GEMM (logits = x . W_r^T + b), per-token softmax / top-k /
+// renormalisation of the Qwen3-MoE sparse block and, for decode batch sizes, the
+// expert permutation in the same launch.
 //
-// Router GEMM: one warp per (expert, group of 8 tokens); a block's 8 warps share
-// the token group, so the x rows are read from L1 after the first warp.  Each
-// lane streams 16-byte vectors of the expert's router row and accumulates the 8
-// dot products in fp32; a shuffle tree reduces them.
+// Router GEMM: a block owns 4 experts and up to 64 tokens (in groups of 8).  Each of
+// its 256 threads owns 16-byte chunks of the hidden dim: it loads the 4 experts'
+// router-weight chunks once and the 8 tokens' activation chunks, accumulating 32 fp32
+// dot products; a shuffle tree and one pass over the 8 warps' partials in shared
+// memory reduce them.  The arithmetic of a (token, expert) logit does not depend on
+// the grid, so every path below produces bit-identical logits.
 //
 // Top-k: one warp per token.  Lane l holds the logits of experts l, l+32, ...;
 // k rounds of a shuffle arg-max (ties -> lower expert index) pick the experts in
 // descending order, a (k+1)-th round gives the tie margin.  The weights are
 // exp(l_j - l_max) / sum over the chosen experts (norm_topk) or over all experts,
 // which equals softmax followed by renormalisation of the chosen probabilities.
+//
+// With at most 64 tokens, top-k (and, for moe_forward, the permutation of
+// permute_impl.cuh) run in the last router block to finish (an atomic arrival
+// counter in the workspace header, reset by that block), saving two launches.
 #include "moe_internal.cuh"
+#include "permute_impl.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kRouterTokens = 8;   // tokens per warp
-constexpr int kRouterWarps = 8;    // experts per block
+constexpr int kRThreads = 256;
+constexpr int kRWarps = kRThreads / 32;
+constexpr int kEPB = 4;      // experts per block
+constexpr int kTG = 8;       // tokens per accumulation group
+constexpr int kTPB = 64;     // tokens per block
+constexpr int kFuseMaxT = kTPB;
 
 template <typename T> struct Vec;
 template <> struct Vec<float> {
@@ -40,42 +52,65 @@ template <> struct Vec<uint16_t> {
     }
 };
 
+// logits[t][e] for e in [e0, e0+4) and t in [t0, t0+64), t < T.
 template <typename ActT>
-__global__ void __launch_bounds__(kRouterWarps * 32)
-router_logits_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const float *__restrict__ bias,
-                     float *__restrict__ logits, int T, int H, int E) {
+__device__ void router_block(const ActT *__restrict__ x, const ActT *__restrict__ wr, const float *__restrict__ bias,
+                             float *__restrict__ logits, int T, int H, int E, int e0, int t0,
+                             float (*s_part)[kEPB * kTG]) {
     constexpr int V = Vec<ActT>::N;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * kRouterWarps + warp;
-    const int t0 = blockIdx.y * kRouterTokens;
-    if (e >= E) return;
-    const int nt = min(kRouterTokens, T - t0);
-    float acc[kRouterTokens];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int nchunk = H / V;
+    const int ne = min(kEPB, E - e0);
+    const int tend = min(T, t0 + kTPB);
+    for (int tg = t0; tg < tend; tg += kTG) {
+        const int nt = min(kTG, T - tg);
+        float acc[kEPB][kTG];
 #pragma unroll
-    for (int i = 0; i < kRouterTokens; ++i) acc[i] = 0.f;
-    const ActT *wrow = wr + (size_t)e * H;
-    for (int h = lane * V; h < H; h += 32 * V) {
-        float wv[V];
-        Vec<ActT>::load(wrow + h, wv);
+        for (int i = 0; i < kEPB; ++i)
 #pragma unroll
-        for (int tt = 0; tt < kRouterTokens; ++tt) {
-            if (tt < nt) {
-                float xv[V];
-                Vec<ActT>::load(x + (size_t)(t0 + tt) * H + h, xv);
+            for (int j = 0; j < kTG; ++j) acc[i][j] = 0.f;
+        for (int c = tid; c < nchunk; c += kRThreads) {
+            float wv[kEPB][V];
 #pragma unroll
-                for (int v = 0; v < V; ++v) acc[tt] = fmaf(xv[v], wv[v], acc[tt]);
+            for (int ee = 0; ee < kEPB; ++ee) {
+                if (ee < ne) Vec<ActT>::load(wr + (size_t)(e0 + ee) * H + (size_t)c * V, wv[ee]);
+                else
+#pragma unroll
+                    for (int v = 0; v < V; ++v) wv[ee][v] = 0.f;
+            }
+#pragma unroll
+            for (int tt = 0; tt < kTG; ++tt) {
+                if (tt < nt) {
+                    float xv[V];
+                    Vec<ActT>::load(x + (size_t)(tg + tt) * H + (size_t)c * V, xv);
+#pragma unroll
+                    for (int ee = 0; ee < kEPB; ++ee)
+#pragma unroll
+                        for (int v = 0; v < V; ++v) acc[ee][tt] = fmaf(xv[v], wv[ee][v], acc[ee][tt]);
+                }
             }
         }
-    }
-    const float b = bias ? bias[e] : 0.f;
 #pragma unroll
-    for (int tt = 0; tt < kRouterTokens; ++tt) {
-        float s = warp_sum(acc[tt]);
-        if (lane == 0 && tt < nt) logits[(size_t)(t0 + tt) * E + e] = s + b;
+        for (int ee = 0; ee < kEPB; ++ee)
+#pragma unroll
+            for (int tt = 0; tt < kTG; ++tt) {
+                const float s = warp_sum(acc[ee][tt]);
+                if (lane == 0) s_part[w][ee * kTG + tt] = s;
+            }
+        __syncthreads();
+        if (tid < kEPB * kTG) {
+            const int ee = tid / kTG, tt = tid % kTG;
+            if (ee < ne && tt < nt) {
+                float s = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < kRWarps; ++w2) s += s_part[w2][tid];
+                logits[(size_t)(tg + tt) * E + e0 + ee] = s + (bias ? bias[e0 + ee] : 0.f);
+            }
+        }
+        __syncthreads();
     }
 }
 
-constexpr int kTopkWarps = 4;
 constexpr int kMaxPerLane = kMaxE / 32;
 
 // Warp arg-max over (value, index) pairs; equal values -> lower index.
@@ -88,18 +123,16 @@ __device__ __forceinline__ void warp_argmax(float &v, int &i) {
     }
 }
 
-__global__ void __launch_bounds__(kTopkWarps * 32)
-topk_kernel(const float *__restrict__ logits, int T, int E, int k, int norm, int32_t *__restrict__ ids,
-            float *__restrict__ w, float *__restrict__ margin) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kTopkWarps + warp;
-    if (t >= T) return;
+// Softmax / top-k / renormalisation of token t by one warp.
+__device__ void topk_token(const float *logits, int t, int E, int k, int norm, int32_t *ids, float *w,
+                           float *margin) {
+    const int lane = threadIdx.x & 31;
     const float *l = logits + (size_t)t * E;
     float v[kMaxPerLane];
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
         const int e = lane + 32 * i;
-        v[i] = (e < E) ? l[e] : -INFINITY;
+        v[i] = (e < E) ? __ldcg(l + e) : -INFINITY;
     }
     uint32_t taken = 0;
     float lmax = 0.f, my_l = 0.f, last = 0.f;
@@ -142,29 +175,84 @@ topk_kernel(const float *__restrict__ logits, int T, int E, int k, int norm, int
     }
 }
 
-}  // namespace
+struct RouteArgs {
+    float *logits;
+    int T, H, E, k, norm;
+    int32_t *ids;
+    float *w, *margin;
+    int *arrivals;            // workspace counter, zero between launches
+    int fuse;                 // 0: logits only, 1: + top-k, 2: + top-k + permutation
+    int32_t *counts, *offsets, *order, *pos, *active, *err;
+};
 
-cudaError_t launch_router_logits(const moe_shape &s, const void *x, const void *wr, const float *bias,
-                                 float *logits, cudaStream_t st) {
-    if (s.T == 0) return cudaSuccess;
-    dim3 grid((s.E + kRouterWarps - 1) / kRouterWarps, (s.T + kRouterTokens - 1) / kRouterTokens);
+template <typename ActT>
+__global__ void __launch_bounds__(kRThreads)
+route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const float *__restrict__ bias, RouteArgs a) {
+    __shared__ float s_part[kRWarps][kEPB * kTG];
+    __shared__ int s_last;
+    router_block<ActT>(x, wr, bias, a.logits, a.T, a.H, a.E, blockIdx.x * kEPB, blockIdx.y * kTPB, s_part);
+    if (!a.fuse) return;
+    // last block to finish: every logit of the batch is in memory
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(a.arrivals, 1) == int(gridDim.x * gridDim.y) - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int w = threadIdx.x >> 5;
+    for (int t = w; t < a.T; t += kRWarps) topk_token(a.logits, t, a.E, a.k, a.norm, a.ids, a.w, a.margin);
+    if (threadIdx.x == 0) *a.arrivals = 0;
+    if (a.fuse < 2) return;
+    __syncthreads();
+    __shared__ PermuteSmem<kRThreads> ps;
+    permute_block<kRThreads>(a.ids, a.T * a.k, a.E, a.counts, a.offsets, a.order, a.pos, a.active, a.err, ps);
+}
+
+__global__ void __launch_bounds__(128)
+topk_kernel(const float *__restrict__ logits, int T, int E, int k, int norm, int32_t *__restrict__ ids,
+            float *__restrict__ w, float *__restrict__ margin) {
+    const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (t < T) topk_token(logits, t, E, k, norm, ids, w, margin);
+}
+
+cudaError_t launch_route_kernel(const moe_shape &s, const void *x, const void *wr, const float *bias,
+                                const RouteArgs &a, cudaStream_t st) {
+    dim3 grid((s.E + kEPB - 1) / kEPB, (s.T + kTPB - 1) / kTPB);
     if (s.act_dtype == MOE_DT_F32)
-        router_logits_kernel<float><<<grid, kRouterWarps * 32, 0, st>>>(
-            static_cast<const float *>(x), static_cast<const float *>(wr), bias, logits, s.T, s.H, s.E);
+        route_kernel<float><<<grid, kRThreads, 0, st>>>(static_cast<const float *>(x), static_cast<const float *>(wr),
+                                                        bias, a);
     else
-        router_logits_kernel<uint16_t><<<grid, kRouterWarps * 32, 0, st>>>(
-            static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(wr), bias, logits, s.T, s.H, s.E);
+        route_kernel<uint16_t><<<grid, kRThreads, 0, st>>>(static_cast<const uint16_t *>(x),
+                                                           static_cast<const uint16_t *>(wr), bias, a);
     return cudaGetLastError();
 }
 
-int route_launches(const moe_shape &s) { return s.T > 0 ? 2 : 0; }
+}  // namespace
 
-cudaError_t launch_topk(const moe_shape &s, const float *logits, int32_t *ids, float *w, float *margin,
-                        cudaStream_t st) {
+bool route_fuses(const moe_shape &s) { return s.T <= kFuseMaxT; }
+
+int route_launches(const moe_shape &s) { return s.T == 0 ? 0 : (route_fuses(s) ? 1 : 2); }
+
+// moe_route: logits, then top-k (fused into the router launch for small batches).
+cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
+                         int32_t *ids, float *w, float *margin, int *arrivals, cudaStream_t st) {
     if (s.T == 0) return cudaSuccess;
-    topk_kernel<<<(s.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, st>>>(logits, s.T, s.E, s.k,
-                                                                                   s.norm_topk, ids, w, margin);
+    RouteArgs a{logits, s.T, s.H, s.E, s.k, s.norm_topk, ids, w, margin, arrivals, route_fuses(s) ? 1 : 0,
+                nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    cudaError_t e = launch_route_kernel(s, x, wr, bias, a, st);
+    if (e != cudaSuccess || a.fuse) return e;
+    topk_kernel<<<(s.T + 3) / 4, 128, 0, st>>>(logits, s.T, s.E, s.k, s.norm_topk, ids, w, margin);
     return cudaGetLastError();
+}
+
+// moe_forward for small batches: logits, top-k and the permutation in one launch.
+cudaError_t launch_route_permute(const moe_shape &s, const void *x, const void *wr, const float *bias,
+                                 float *logits, int32_t *ids, float *w, int *arrivals, int32_t *counts,
+                                 int32_t *offsets, int32_t *order, int32_t *pos, int32_t *active, int32_t *err,
+                                 cudaStream_t st) {
+    RouteArgs a{logits, s.T, s.H, s.E, s.k, s.norm_topk, ids, w, nullptr, arrivals, 2,
+                counts, offsets, order, pos, active, err};
+    return launch_route_kernel(s, x, wr, bias, a, st);
 }
 
 }  // namespace moe
