@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 gate_up_simple_kernel(const ActT *__restrict__ x, const int32_t *__restrict__ offsets,
                       const int32_t *__restrict__ order, int E, int k, int H, int I, int A, WeightRef wg,
                       WeightRef wu, Codebook cb, float *__restrict__ h, int p0) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i = blockIdx.x * kWarps + warp;
     const int p = p0 + blockIdx.y;
@@ -86,6 +88,8 @@ template <typename OutT, int WFMT>
 __global__ void __launch_bounds__(kWarps * 32)
 down_simple_kernel(const float *__restrict__ h, const int32_t *__restrict__ offsets, int E, int H, int I,
                    WeightRef wd, Codebook cb, OutT *__restrict__ y, int p0) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * kWarps + warp;
     const int p = p0 + blockIdx.y;
@@ -119,15 +123,18 @@ cudaError_t launch_typed(const moe_shape &s, const void *x, const int32_t *offse
     for (int p0 = 0; p0 < A; p0 += 65535) {
         const int rows = min(65535, A - p0);
         dim3 g1((s.I + kWarps - 1) / kWarps, rows);
-        gate_up_simple_kernel<ActT, WFMT><<<g1, kWarps * 32, 0, st>>>(static_cast<const ActT *>(x), offsets, order,
-                                                                      s.E, s.k, s.H, s.I, A, rg, ru, cb,
-                                                                      static_cast<float *>(h), p0);
+        const cudaError_t e = launch_pdl(gate_up_simple_kernel<ActT, WFMT>, g1, dim3(kWarps * 32), 0, st,
+                                         static_cast<const ActT *>(x), offsets, order, s.E, s.k, s.H, s.I, A, rg, ru,
+                                         cb, static_cast<float *>(h), p0);
+        if (e != cudaSuccess) return e;
     }
     for (int p0 = 0; p0 < A; p0 += 65535) {
         const int rows = min(65535, A - p0);
         dim3 g2((s.H + kWarps - 1) / kWarps, rows);
-        down_simple_kernel<ActT, WFMT><<<g2, kWarps * 32, 0, st>>>(static_cast<const float *>(h), offsets, s.E,
-                                                                   s.H, s.I, rd, cb, static_cast<ActT *>(y), p0);
+        const cudaError_t e = launch_pdl(down_simple_kernel<ActT, WFMT>, g2, dim3(kWarps * 32), 0, st,
+                                         static_cast<const float *>(h), offsets, s.E, s.H, s.I, rd, cb,
+                                         static_cast<ActT *>(y), p0);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

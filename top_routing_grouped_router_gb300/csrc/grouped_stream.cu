@@ -228,6 +228,9 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // everything above overlaps the previous kernel; from here on its outputs are read
+    griddep_launch_dependents();
+    griddep_wait();
     const uint32_t tmem_base = *tmem_slot;
     const int n_tiles = *p.n_tiles;
 
@@ -459,6 +462,8 @@ __global__ void __launch_bounds__(256)
 prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
             int T, int k, int H, int I, int E, uint16_t *__restrict__ x_perm, uint32_t *tiles, int max_tiles,
             int *n_tiles, int *tile_counter, int *done, int32_t *err) {
+    griddep_launch_dependents();
+    griddep_wait();
     if (blockIdx.x > 0) {
         const int pr = blockIdx.x - 1;
         const int a = __ldg(order + pr);
@@ -589,9 +594,9 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
         !make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
 
-    prep_kernel<<<A + 1, 256, 0, st>>>(static_cast<const uint16_t *>(x), order, offsets, s.T, s.k, s.H, s.I, s.E,
-                                       x_perm, tiles, (int)max_tiles(s), n_tiles, tile_counter, done, err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
+                               offsets, s.T, s.k, s.H, s.I, s.E, x_perm, tiles, (int)max_tiles(s), n_tiles,
+                               tile_counter, done, err);
     if (e != cudaSuccess) return e;
 
     static bool attr_set[64] = {};
@@ -604,8 +609,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     }
     Params prm{offsets, tiles, n_tiles, tile_counter, done, err, static_cast<uint16_t *>(h),
                static_cast<uint16_t *>(y), s.E, s.H, s.I, A};
-    tc_swiglu_kernel<<<sm_count(), kThreads, kSmemBytes, st>>>(mg, mu, md, mx, mh, prm);
-    return cudaGetLastError();
+    return launch_pdl(tc_swiglu_kernel, dim3(sm_count()), dim3(kThreads), kSmemBytes, st, mg, mu, md, mx, mh, prm);
 }
 
 }  // namespace moe

@@ -59,13 +59,39 @@ __device__ __forceinline__ float warp_sum(float v) {
 // SiLU(g) * u with an fp32 logistic.
 __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+// Programmatic dependent launch: let the next kernel of the stream be scheduled now,
+// and wait until the previous kernel has completed and its writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with programmatic stream serialization, so that the kernel's launch and
+// prologue overlap the previous kernel (every kernel calls griddep_wait before it
+// touches memory the previous kernel may use).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Records the first device-side error in the workspace error word.
 __device__ __forceinline__ void record_error(int32_t *err, int code) { atomicCAS(err, 0, code); }
 
 // ---------------------------------------------------------------- launchers (each returns cudaError_t of the launch)
 
-// Workspace header: error word at byte 0, router arrival counter at byte 64 (both zero
-// between launches).
+// Workspace header: error word at byte 0, router arrival counters at bytes 64..127
+// (all zero between launches).
 constexpr size_t kHdrArrivals = 64;
 
 bool route_fuses(const moe_shape &s);

@@ -20,12 +20,16 @@ __global__ void __launch_bounds__(kThreads)
 permute_small_kernel(const int32_t *__restrict__ ids, int A, int E, int32_t *counts, int32_t *offsets,
                      int32_t *order, int32_t *pos, int32_t *active, int32_t *err) {
     __shared__ PermuteSmem<kThreads> s;
+    griddep_launch_dependents();
+    griddep_wait();
     permute_block<kThreads>(ids, A, E, counts, offsets, order, pos, active, err, s);
 }
 
 __global__ void __launch_bounds__(kThreads)
 permute_hist_kernel(const int32_t *__restrict__ ids, int A, int E, int32_t *hist) {
     __shared__ int s_cnt[kMaxE];
+    griddep_launch_dependents();
+    griddep_wait();
     const int tid = threadIdx.x;
     for (int i = tid; i < E; i += kThreads) s_cnt[i] = 0;
     __syncthreads();
@@ -42,6 +46,8 @@ permute_hist_kernel(const int32_t *__restrict__ ids, int A, int E, int32_t *hist
 __global__ void __launch_bounds__(kThreads)
 permute_scan_kernel(int nchunks, int E, int32_t *hist, int32_t *counts, int32_t *offsets, int32_t *active) {
     __shared__ PermuteSmem<32> s;  // the per-warp table is not used here
+    griddep_launch_dependents();
+    griddep_wait();
     const int tid = threadIdx.x;
     if (tid < E) {
         int run = 0;
@@ -61,6 +67,8 @@ __global__ void __launch_bounds__(kThreads)
 permute_scatter_kernel(const int32_t *__restrict__ ids, int A, int E, const int32_t *hist, int32_t *order,
                        int32_t *pos, int32_t *err) {
     __shared__ PermuteSmem<kThreads> s;
+    griddep_launch_dependents();
+    griddep_wait();
     for (int i = threadIdx.x; i < E; i += kThreads) s.base[i] = hist[(size_t)blockIdx.x * E + i];
     __syncthreads();
     scatter_chunk<kThreads>(ids, blockIdx.x * kThreads, A, E, s, order, pos, err);
@@ -78,14 +86,17 @@ cudaError_t launch_permute(const moe_shape &s, const int32_t *ids, int32_t *coun
     static_assert(kThreads == kPermuteChunk, "one assignment per thread per chunk");
     const int A = s.T * s.k;
     if (A <= kSmallA) {
-        permute_small_kernel<<<1, kThreads, 0, st>>>(ids, A, s.E, counts, offsets, order, pos, active, err);
-        return cudaGetLastError();
+        return launch_pdl(permute_small_kernel, dim3(1), dim3(kThreads), 0, st, ids, A, s.E, counts, offsets, order,
+                          pos, active, err);
     }
     const int nch = permute_chunks(A);
-    permute_hist_kernel<<<nch, kThreads, 0, st>>>(ids, A, s.E, hist);
-    permute_scan_kernel<<<1, kThreads, 0, st>>>(nch, s.E, hist, counts, offsets, active);
-    permute_scatter_kernel<<<nch, kThreads, 0, st>>>(ids, A, s.E, hist, order, pos, err);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(permute_hist_kernel, dim3(nch), dim3(kThreads), 0, st, ids, A, s.E, hist);
+    if (e == cudaSuccess)
+        e = launch_pdl(permute_scan_kernel, dim3(1), dim3(kThreads), 0, st, nch, s.E, hist, counts, offsets, active);
+    if (e == cudaSuccess)
+        e = launch_pdl(permute_scatter_kernel, dim3(nch), dim3(kThreads), 0, st, ids, A, s.E,
+                       (const int32_t *)hist, order, pos, err);
+    return e;
 }
 
 }  // namespace moe

@@ -2,7 +2,7 @@
 // renormalisation of the Qwen3-MoE sparse block and, for decode batch sizes, the
 // expert permutation in the same launch.
 //
-// Router GEMM: a block owns 4 experts and up to 64 tokens (in groups of 8).  Each of
+// Router GEMM: a block owns 4 experts and 8 tokens.  Each of
 // its 256 threads owns 16-byte chunks of the hidden dim: it loads the 4 experts'
 // router-weight chunks once and the 8 tokens' activation chunks, accumulating 32 fp32
 // dot products; a shuffle tree and one pass over the 8 warps' partials in shared
@@ -15,9 +15,10 @@
 // exp(l_j - l_max) / sum over the chosen experts (norm_topk) or over all experts,
 // which equals softmax followed by renormalisation of the chosen probabilities.
 //
-// With at most 64 tokens, top-k (and, for moe_forward, the permutation of
-// permute_impl.cuh) run in the last router block to finish (an atomic arrival
-// counter in the workspace header, reset by that block), saving two launches.
+// With at most 64 tokens, top-k runs in the last expert block of each 8-token group to
+// finish, and (for moe_forward) the permutation of permute_impl.cuh in the last token
+// group to finish -- atomic arrival counters in the workspace header, reset by the
+// blocks that consume them -- saving two launches.
 #include "moe_internal.cuh"
 #include "permute_impl.cuh"
 
@@ -28,8 +29,9 @@ constexpr int kRThreads = 256;
 constexpr int kRWarps = kRThreads / 32;
 constexpr int kEPB = 4;      // experts per block
 constexpr int kTG = 8;       // tokens per accumulation group
-constexpr int kTPB = 64;     // tokens per block
-constexpr int kFuseMaxT = kTPB;
+constexpr int kTPB = 8;      // tokens per block
+constexpr int kFuseMaxT = 64;
+constexpr int kMaxGroups = kFuseMaxT / kTPB;
 
 template <typename T> struct Vec;
 template <> struct Vec<float> {
@@ -52,7 +54,7 @@ template <> struct Vec<uint16_t> {
     }
 };
 
-// logits[t][e] for e in [e0, e0+4) and t in [t0, t0+64), t < T.
+// logits[t][e] for e in [e0, e0+4) and t in [t0, t0+8), t < T.
 template <typename ActT>
 __device__ void router_block(const ActT *__restrict__ x, const ActT *__restrict__ wr, const float *__restrict__ bias,
                              float *__restrict__ logits, int T, int H, int E, int e0, int t0,
@@ -180,7 +182,7 @@ struct RouteArgs {
     int T, H, E, k, norm;
     int32_t *ids;
     float *w, *margin;
-    int *arrivals;            // workspace counter, zero between launches
+    int *arrivals;            // workspace counters [1 + kMaxGroups], zero between launches
     int fuse;                 // 0: logits only, 1: + top-k, 2: + top-k + permutation
     int32_t *counts, *offsets, *order, *pos, *active, *err;
 };
@@ -190,20 +192,32 @@ __global__ void __launch_bounds__(kRThreads)
 route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const float *__restrict__ bias, RouteArgs a) {
     __shared__ float s_part[kRWarps][kEPB * kTG];
     __shared__ int s_last;
+    griddep_launch_dependents();
+    griddep_wait();  // the previous kernel in the stream may still read this workspace
     router_block<ActT>(x, wr, bias, a.logits, a.T, a.H, a.E, blockIdx.x * kEPB, blockIdx.y * kTPB, s_part);
     if (!a.fuse) return;
-    // last block to finish: every logit of the batch is in memory
+    // the last expert block of this token group to finish sees all its logits: top-k,
+    // one warp per token
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(a.arrivals, 1) == int(gridDim.x * gridDim.y) - 1;
+    int *group_arrivals = a.arrivals + 1 + blockIdx.y;
+    if (threadIdx.x == 0) s_last = atomicAdd(group_arrivals, 1) == int(gridDim.x) - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
     const int w = threadIdx.x >> 5;
-    for (int t = w; t < a.T; t += kRWarps) topk_token(a.logits, t, a.E, a.k, a.norm, a.ids, a.w, a.margin);
-    if (threadIdx.x == 0) *a.arrivals = 0;
+    const int t = blockIdx.y * kTPB + w;
+    if (w < kTPB && t < a.T) topk_token(a.logits, t, a.E, a.k, a.norm, a.ids, a.w, a.margin);
+    if (threadIdx.x == 0) *group_arrivals = 0;
     if (a.fuse < 2) return;
+    // the last token group to finish permutes the whole batch
+    __threadfence();
     __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(a.arrivals, 1) == int(gridDim.y) - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x == 0) *a.arrivals = 0;
     __shared__ PermuteSmem<kRThreads> ps;
     permute_block<kRThreads>(a.ids, a.T * a.k, a.E, a.counts, a.offsets, a.order, a.pos, a.active, a.err, ps);
 }
@@ -211,6 +225,8 @@ route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const floa
 __global__ void __launch_bounds__(128)
 topk_kernel(const float *__restrict__ logits, int T, int E, int k, int norm, int32_t *__restrict__ ids,
             float *__restrict__ w, float *__restrict__ margin) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (t < T) topk_token(logits, t, E, k, norm, ids, w, margin);
 }
@@ -219,12 +235,10 @@ cudaError_t launch_route_kernel(const moe_shape &s, const void *x, const void *w
                                 const RouteArgs &a, cudaStream_t st) {
     dim3 grid((s.E + kEPB - 1) / kEPB, (s.T + kTPB - 1) / kTPB);
     if (s.act_dtype == MOE_DT_F32)
-        route_kernel<float><<<grid, kRThreads, 0, st>>>(static_cast<const float *>(x), static_cast<const float *>(wr),
-                                                        bias, a);
-    else
-        route_kernel<uint16_t><<<grid, kRThreads, 0, st>>>(static_cast<const uint16_t *>(x),
-                                                           static_cast<const uint16_t *>(wr), bias, a);
-    return cudaGetLastError();
+        return launch_pdl(route_kernel<float>, grid, dim3(kRThreads), 0, st, static_cast<const float *>(x),
+                          static_cast<const float *>(wr), bias, a);
+    return launch_pdl(route_kernel<uint16_t>, grid, dim3(kRThreads), 0, st, static_cast<const uint16_t *>(x),
+                      static_cast<const uint16_t *>(wr), bias, a);
 }
 
 }  // namespace
@@ -241,8 +255,8 @@ cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, cons
                 nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
     cudaError_t e = launch_route_kernel(s, x, wr, bias, a, st);
     if (e != cudaSuccess || a.fuse) return e;
-    topk_kernel<<<(s.T + 3) / 4, 128, 0, st>>>(logits, s.T, s.E, s.k, s.norm_topk, ids, w, margin);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel, dim3((s.T + 3) / 4), dim3(128), 0, st, (const float *)logits, s.T, s.E, s.k,
+                      s.norm_topk, ids, w, margin);
 }
 
 // moe_forward for small batches: logits, top-k and the permutation in one launch.
