@@ -51,6 +51,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--copies", type=int, default=0, help="weight copies to rotate (0 = automatic)")
+    ap.add_argument("--layers", type=int, default=0, help="use only the first N layers (profiling; 0 = all)")
     return ap.parse_args()
 
 
@@ -230,6 +231,8 @@ def run_ours(args, rank, world, local):
     peaks, peak_kind = load_peaks()
 
     layers = layer_inputs(args.workload)
+    if args.layers > 0:
+        layers = layers[:args.layers]
     inp0 = layers[0]
     T, H, E, k, I = inp0.T, inp0.H, inp0.E, inp0.k, inp0.I
     # enough weight copies that a replay never finds the previous replay's weights in L2

@@ -27,6 +27,7 @@
 #include "moe_internal.cuh"
 
 #include <cuda.h>
+#include <algorithm>
 #include <mutex>
 
 namespace moe {
@@ -55,6 +56,10 @@ __host__ __device__ constexpr uint32_t pack_tile(int down, int e, int rb, int nc
     return (uint32_t(down) << 31) | (uint32_t(e) << 16) | (uint32_t(rb) << 8) | uint32_t(nc);
 }
 
+// Tile kinds.  The router GEMM (logits[t][e] = x_t . W_r[e]) reuses the kernel as one
+// 128-expert x 128-token tile per CTA.
+enum : int { kGateUp = 0, kDown = 1, kRouter = 2 };
+
 struct Params {
     const int32_t *offsets;     // [E+1]
     const uint32_t *tiles;      // tile list
@@ -65,6 +70,11 @@ struct Params {
     uint16_t *h;                // [A][I] bf16
     uint16_t *y;                // [A][H] bf16
     int E, H, I, A;
+    // router mode: tiles are (row block of experts, 128-token chunk), one static sweep
+    int router_tiles;           // > 0 selects router mode
+    int T;
+    float *logits;              // [T][E]
+    const float *bias;          // [E] or null
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -232,21 +242,34 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     griddep_launch_dependents();
     griddep_wait();
     const uint32_t tmem_base = *tmem_slot;
-    const int n_tiles = *p.n_tiles;
+    const bool router = p.router_tiles > 0;
+    const int n_tiles = router ? p.router_tiles : *p.n_tiles;
+    const int erb = (p.E + kRows - 1) / kRows;  // expert row blocks in router mode
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         int stage = 0, slot = 0;
         uint32_t phase = 0, mphase = 0;
-        int next = atomicAdd(p.tile_counter, 1);
+        int next = router ? int(blockIdx.x) : atomicAdd(p.tile_counter, 1);
         for (;;) {
             const int t = next;
             if (t >= n_tiles || *abort) break;
-            next = atomicAdd(p.tile_counter, 1);  // claim ahead: its latency hides behind this tile
-            bool ok;
-            const TileInfo d = read_tile(__ldg(p.tiles + t), p, ok);
+            // claim ahead: the atomic's latency hides behind this tile
+            next = router ? t + int(gridDim.x) : atomicAdd(p.tile_counter, 1);
+            bool ok = true;
+            TileInfo d;
+            if (router) {
+                d.down = kRouter;
+                d.e = 0;
+                d.rb = t % erb;
+                d.r0 = (t / erb) * kMaxN;
+                d.m = min(kMaxN, p.T - d.r0);
+                d.N = (d.m + 15) & ~15;
+            } else {
+                d = read_tile(__ldg(p.tiles + t), p, ok);
+            }
             if (!ok) record_error(p.err, MOE_ERR_DEVICE);
-            if (d.down) {
+            if (d.down == kDown) {
                 // the expert's h must be complete: every epilogue warp of every gate/up tile
                 const int me = __ldg(p.offsets + d.e + 1) - __ldg(p.offsets + d.e);
                 const int need = (p.I / kRows) * ((me + kMaxN - 1) / kMaxN) * kEpiWarps;
@@ -276,19 +299,23 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             mbar_arrive(smem_u32(&tmf[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
 
-            // a down tile with at most 64 tokens takes two k-slabs per stage (weights in
-            // both A regions, token rows in the two halves of B), so every stage carries
-            // 32 KB of weights whatever the tile kind
-            const int two = d.down && d.N <= kMaxN / 2 && (p.I / kSlab) % 2 == 0;
-            const int nslab = (d.down ? p.I : p.H) / kSlab;
+            // a one-matrix tile (down, router) with at most 64 tokens takes two k-slabs per
+            // stage (weights in both A regions, token rows in the two halves of B), so every
+            // stage carries 32 KB of weights whatever the tile kind
+            const int kdim = d.down == kDown ? p.I : p.H;
+            const int two = d.down != kGateUp && d.N <= kMaxN / 2 && (kdim / kSlab) % 2 == 0;
+            const int nslab = kdim / kSlab;
             const int nstage = two ? nslab / 2 : nslab;
             const int nbox = d.N / kNBox;
-            const uint32_t bytes = (d.down && !two ? kABytes : 2 * kABytes) + (two ? 2 : 1) * nbox * kNBox * 128;
-            const int wrow = d.e * (d.down ? p.H : p.I) + d.rb * kRows;
+            const uint32_t bytes =
+                (d.down != kGateUp && !two ? kABytes : 2 * kABytes) + (two ? 2 : 1) * nbox * kNBox * 128;
+            const int wrow = d.down == kRouter ? d.rb * kRows : d.e * (d.down ? p.H : p.I) + d.rb * kRows;
+            const CUtensorMap *wmap = d.down == kDown ? &tm_down : &tm_gate;
+            const CUtensorMap *bmap = d.down == kDown ? &tm_h : &tm_x;
             for (int ks = 0; ks < nstage; ++ks) {
                 mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort);
                 int *sm = smeta + 4 * stage;
-                sm[0] = d.down | (two << 1);
+                sm[0] = d.down | (two << 2);
                 sm[1] = ks;
                 sm[2] = nstage;
                 sm[3] = d.N;
@@ -299,13 +326,13 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 if (two) {
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int k0 = (2 * ks + h2) * kSlab;
-                        tma_load_2d(a0 + h2 * kABytes, &tm_down, k0, wrow, fb);
+                        tma_load_2d(a0 + h2 * kABytes, wmap, k0, wrow, fb);
                         for (int q = 0; q < nbox; ++q)
-                            tma_load_2d(bb + h2 * (kBBytes / 2) + q * 2048, &tm_h, k0, d.r0 + q * kNBox, fb);
+                            tma_load_2d(bb + h2 * (kBBytes / 2) + q * 2048, bmap, k0, d.r0 + q * kNBox, fb);
                     }
-                } else if (d.down) {
-                    tma_load_2d(a0, &tm_down, ks * kSlab, wrow, fb);
-                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * 2048, &tm_h, ks * kSlab, d.r0 + q * kNBox, fb);
+                } else if (d.down != kGateUp) {
+                    tma_load_2d(a0, wmap, ks * kSlab, wrow, fb);
+                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * 2048, bmap, ks * kSlab, d.r0 + q * kNBox, fb);
                 } else {
                     tma_load_2d(a0, &tm_gate, ks * kSlab, wrow, fb);
                     tma_load_2d(a0 + kABytes, &tm_up, ks * kSlab, wrow, fb);
@@ -329,7 +356,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         for (;;) {
             mbar_wait(smem_u32(&full[stage]), phase, p.err, abort);
             const int *sm = smeta + 4 * stage;
-            const int down = sm[0] & 1, two = sm[0] >> 1, ks = sm[1], nslab = sm[2], N = sm[3];
+            const int down = (sm[0] & 3) != kGateUp, two = sm[0] >> 2, ks = sm[1], nslab = sm[2], N = sm[3];
             if (ks < 0 || *abort) break;
             const int b = tile_count & 1;
             if (ks == 0) {
@@ -386,7 +413,16 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const uint32_t taddr = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(b * kBufCols);
             const size_t col = (size_t)rb * kRows + row;
             for (int c0 = 0; c0 < N; c0 += 16) {
-                if (down) {
+                if (down == kRouter) {
+                    float v[16];
+                    tmem_ld16(taddr + c0, v);
+                    if (col < (size_t)p.E) {
+                        const float b = p.bias ? p.bias[col] : 0.f;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (c0 + j < m) p.logits[(size_t)(r0 + c0 + j) * p.E + col] = v[j] + b;
+                    }
+                } else if (down) {
                     float v[16];
                     tmem_ld16(taddr + c0, v);
 #pragma unroll
@@ -404,7 +440,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&acce[b]));
-            if (!down && e < p.E) {
+            if (down == kGateUp && e < p.E) {
                 // publish this warp's h rows (read back through TMA by down tiles)
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 __syncwarp();
@@ -559,7 +595,44 @@ size_t max_tiles(const moe_shape &s) {
     return chunks * (size_t)(s.I / kRows + s.H / kRows);
 }
 
+bool set_smem_attr() {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(tc_swiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess)
+            return false;
+        attr_set[dev] = true;
+    }
+    return true;
+}
+
 }  // namespace
+
+// Router GEMM on the tensor cores (bf16 x and W_r, fp32 logits + bias): one tile per CTA.
+bool router_tc_supported(const moe_shape &s) {
+    return s.act_dtype == MOE_DT_BF16 && s.H % kSlab == 0 && s.T >= 1;
+}
+
+cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
+                             int32_t *err, cudaStream_t st) {
+    CUtensorMap mw, mx;
+    if (!make_map(&mw, wr, s.E, s.H, kRows) || !make_map(&mx, x, s.T, s.H, kNBox)) return cudaErrorInvalidValue;
+    if (!set_smem_attr()) return cudaErrorInvalidValue;
+    const int tiles = ((s.E + kRows - 1) / kRows) * ((s.T + kMaxN - 1) / kMaxN);
+    Params prm{};
+    prm.err = err;
+    prm.E = s.E;
+    prm.H = s.H;
+    prm.I = s.I;
+    prm.router_tiles = tiles;
+    prm.T = s.T;
+    prm.logits = logits;
+    prm.bias = bias;
+    return launch_pdl(tc_swiglu_kernel, dim3(std::min(tiles, sm_count())), dim3(kThreads), kSmemBytes, st, mw, mw, mw,
+                      mx, mx, prm);
+}
 
 // 0 = the per-output-element kernels of grouped_simple.cu; 1 = the tensor-core kernel.
 int select_grouped_path(const moe_shape &s) {
@@ -599,16 +672,20 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
                                tile_counter, done, err);
     if (e != cudaSuccess) return e;
 
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(tc_swiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
-    Params prm{offsets, tiles, n_tiles, tile_counter, done, err, static_cast<uint16_t *>(h),
-               static_cast<uint16_t *>(y), s.E, s.H, s.I, A};
+    if (!set_smem_attr()) return cudaErrorInvalidValue;
+    Params prm{};
+    prm.offsets = offsets;
+    prm.tiles = tiles;
+    prm.n_tiles = n_tiles;
+    prm.tile_counter = tile_counter;
+    prm.done = done;
+    prm.err = err;
+    prm.h = static_cast<uint16_t *>(h);
+    prm.y = static_cast<uint16_t *>(y);
+    prm.E = s.E;
+    prm.H = s.H;
+    prm.I = s.I;
+    prm.A = A;
     return launch_pdl(tc_swiglu_kernel, dim3(sm_count()), dim3(kThreads), kSmemBytes, st, mg, mu, md, mx, mh, prm);
 }
 

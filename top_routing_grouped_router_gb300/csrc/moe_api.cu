@@ -106,7 +106,8 @@ int do_route(const moe_shape &s, const void *x, const void *wr, const float *b, 
              float *margin, float *logits, void *ws, cudaStream_t st) {
     const WsLayout L = ws_layout(s);
     float *lg = logits ? logits : at<float>(ws, L.logits);
-    return launch_rc(launch_route(s, x, wr, b, lg, ids, w, margin, at<int>(ws, kHdrArrivals), st));
+    return launch_rc(launch_route(s, x, wr, b, lg, ids, w, margin, at<int>(ws, kHdrArrivals), at<int32_t>(ws, L.err),
+                                  st));
 }
 
 int do_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t *offsets, int32_t *order,

@@ -96,7 +96,10 @@ constexpr size_t kHdrArrivals = 64;
 
 bool route_fuses(const moe_shape &s);
 cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
-                         int32_t *ids, float *w, float *margin, int *arrivals, cudaStream_t st);
+                         int32_t *ids, float *w, float *margin, int *arrivals, int32_t *err, cudaStream_t st);
+bool router_tc_supported(const moe_shape &s);
+cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
+                             int32_t *err, cudaStream_t st);
 cudaError_t launch_route_permute(const moe_shape &s, const void *x, const void *wr, const float *bias,
                                  float *logits, int32_t *ids, float *w, int *arrivals, int32_t *counts,
                                  int32_t *offsets, int32_t *order, int32_t *pos, int32_t *active, int32_t *err,

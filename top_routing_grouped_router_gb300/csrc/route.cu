@@ -249,11 +249,13 @@ int route_launches(const moe_shape &s) { return s.T == 0 ? 0 : (route_fuses(s) ?
 
 // moe_route: logits, then top-k (fused into the router launch for small batches).
 cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
-                         int32_t *ids, float *w, float *margin, int *arrivals, cudaStream_t st) {
+                         int32_t *ids, float *w, float *margin, int *arrivals, int32_t *err, cudaStream_t st) {
     if (s.T == 0) return cudaSuccess;
     RouteArgs a{logits, s.T, s.H, s.E, s.k, s.norm_topk, ids, w, margin, arrivals, route_fuses(s) ? 1 : 0,
                 nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
-    cudaError_t e = launch_route_kernel(s, x, wr, bias, a, st);
+    // large bf16 batches: the router GEMM on the tensor cores, then a top-k launch
+    cudaError_t e = (!a.fuse && router_tc_supported(s)) ? launch_router_tc(s, x, wr, bias, logits, err, st)
+                                                       : launch_route_kernel(s, x, wr, bias, a, st);
     if (e != cudaSuccess || a.fuse) return e;
     return launch_pdl(topk_kernel, dim3((s.T + 3) / 4), dim3(128), 0, st, (const float *)logits, s.T, s.E, s.k,
                       s.norm_topk, ids, w, margin);
