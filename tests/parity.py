@@ -34,6 +34,36 @@ def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
     return float(np.abs(got - ref).max() / scale)
 
 
+def check_selection(g_ids, g_w, g_logits, o_ids, o_w, o_logits, toks):
+    """Routing parity on the tokens `toks` (those without a k-th/(k+1)-th near tie).
+
+    The selected SET of experts is unique there and must match bit-exactly, with the
+    weight of each selected expert within 2e-5.  The slot order is the descending order
+    of the logits; two selected experts whose oracle logits differ by less than NEAR_TIE
+    may come out in either order (fp32 vs double rounding), so the GPU order is checked
+    to follow the GPU's own logits (ties -> lower index) and any order difference from
+    the oracle must be between such near-equal logits.  Returns the (token, slot) pairs
+    whose order differs, for reporting.
+    """
+    np.testing.assert_array_equal(np.sort(g_ids[toks], axis=1), np.sort(o_ids[toks], axis=1))
+    k = g_ids.shape[1]
+    swaps = []
+    for t in toks:
+        gw = dict(zip(g_ids[t].tolist(), g_w[t].tolist()))
+        ow = dict(zip(o_ids[t].tolist(), o_w[t].tolist()))
+        for e in ow:
+            assert abs(gw[e] - ow[e]) <= 2e-5, (t, e, gw[e], ow[e])
+        lg = g_logits[t, g_ids[t]]
+        for j in range(k - 1):
+            assert lg[j] > lg[j + 1] or (lg[j] == lg[j + 1] and g_ids[t, j] < g_ids[t, j + 1]), (t, j)
+        if not np.array_equal(g_ids[t], o_ids[t]):
+            for j in np.nonzero(g_ids[t] != o_ids[t])[0]:
+                a, b = g_ids[t, j], o_ids[t, j]
+                assert abs(o_logits[t, a] - o_logits[t, b]) < NEAR_TIE, (t, j, a, b)
+                swaps.append((int(t), int(j)))
+    return swaps
+
+
 def run_steps(L: DeviceLayer) -> dict:
     """moe_route -> moe_permute -> moe_grouped_swiglu -> moe_unpermute, then moe_forward; host copies."""
     s = L.shape
@@ -94,8 +124,7 @@ def check_layer(inp, *, full_oracle: bool, n_sample_tokens: int = 16, n_sample_r
     np.testing.assert_allclose(g["logits"], o_logits, rtol=0, atol=2e-4 * max(1.0, np.abs(o_logits).max()))
     near = np.where(o_margin < NEAR_TIE)[0]
     ok = np.setdiff1d(np.arange(T), near)
-    np.testing.assert_array_equal(g["ids"][ok], o_ids[ok])
-    np.testing.assert_allclose(g["weights"][ok], o_w[ok], rtol=0, atol=2e-5)
+    order_ties = check_selection(g["ids"], g["weights"], g["logits"], o_ids, o_w, o_logits, ok)
     finite = np.isfinite(o_margin[ok])
     np.testing.assert_allclose(g["tie_margin"][ok][finite], o_margin[ok][finite], rtol=0,
                                atol=4e-4 * max(1.0, np.abs(o_logits).max()))
@@ -142,8 +171,10 @@ def check_layer(inp, *, full_oracle: bool, n_sample_tokens: int = 16, n_sample_r
         o_out = oracle.forward_tokens(inp, toks)["out"]
     out_err = rel_err(g["out"][toks], o_out) if len(toks) else 0.0
     assert out_err <= tol, f"block output rel err {out_err}"
-    summary = dict(name=inp.name, T=T, near_ties=near.tolist(), y_rel_err=y_err, out_rel_err=out_err,
-                   active_experts=int((g["counts"] > 0).sum()))
+    summary = dict(name=inp.name, T=T, near_ties=near.tolist(), order_ties=order_ties, y_rel_err=y_err,
+                   out_rel_err=out_err, active_experts=int((g["counts"] > 0).sum()))
+    if near.size or order_ties:
+        print(f"{inp.name}: near-tie tokens excluded {near.tolist()}, slot-order near ties {order_ties}")
     if report is not None:
         report.append(summary)
     return summary, g

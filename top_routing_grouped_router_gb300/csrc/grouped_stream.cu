@@ -50,6 +50,7 @@ constexpr int kMetaRing = 8;
 constexpr int kCtrlBytes = 1024;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*alignment*/ + kCtrlBytes;
 constexpr long long kSpinLimit = 1ll << 22;
+constexpr int kRouterN = 64;               // tokens per router tile: twice the tiles, two k-slabs per stage
 
 // Tile list entry: bit 31 = down tile, bits 16-23 expert, bits 8-15 row block, bits 0-7 token chunk.
 __host__ __device__ constexpr uint32_t pack_tile(int down, int e, int rb, int nc) {
@@ -262,8 +263,8 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 d.down = kRouter;
                 d.e = 0;
                 d.rb = t % erb;
-                d.r0 = (t / erb) * kMaxN;
-                d.m = min(kMaxN, p.T - d.r0);
+                d.r0 = (t / erb) * kRouterN;
+                d.m = min(kRouterN, p.T - d.r0);
                 d.N = (d.m + 15) & ~15;
             } else {
                 d = read_tile(__ldg(p.tiles + t), p, ok);
@@ -620,7 +621,7 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
     CUtensorMap mw, mx;
     if (!make_map(&mw, wr, s.E, s.H, kRows) || !make_map(&mx, x, s.T, s.H, kNBox)) return cudaErrorInvalidValue;
     if (!set_smem_attr()) return cudaErrorInvalidValue;
-    const int tiles = ((s.E + kRows - 1) / kRows) * ((s.T + kMaxN - 1) / kMaxN);
+    const int tiles = ((s.E + kRows - 1) / kRows) * ((s.T + kRouterN - 1) / kRouterN);
     Params prm{};
     prm.err = err;
     prm.E = s.E;
