@@ -55,10 +55,19 @@ def test_prefill_full_size_layer(layer):
     (700, 256, 128, 8, 128, "bf16", "bf16", False),  # multi-block permute with a ragged last chunk
     (21, 256, 16, 4, 128, "bf16", "q4", False),      # 4-bit, two scale blocks per row
     (5, 128, 8, 8, 64, "bf16", "bf16", False),       # k == E: every expert, infinite margins
+    (40, 256, 2, 2, 128, "bf16", "q4", False),       # 4-bit, 40 tokens per expert (one k-slab per down stage)
+    (64, 384, 8, 2, 256, "bf16", "q4", True),        # 4-bit, skewed load, three row blocks of H
 ])
 def test_reduced_and_ragged_cases(T, H, E, k, I, act, w, zipf):
     inp = synth.make_custom(T, H, E, k, I, act=act, w=w, zipf=zipf, seed=T + E, name=f"custom{T}")
     check_layer(inp, full_oracle=T * k <= 256, n_sample_tokens=16, n_sample_rows=32)
+
+
+def test_q4_non_affine_codebook_uses_generic_kernels():
+    inp = synth.make_custom(12, 256, 8, 2, 128, act="bf16", w="q4", seed=17)
+    rng = np.random.default_rng(4)
+    inp.codebook = np.sort(rng.uniform(-1, 1, 16)).astype(np.float32)
+    check_layer(inp, full_oracle=True)
 
 
 def test_no_renormalisation():

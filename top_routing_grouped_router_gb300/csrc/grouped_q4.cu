@@ -1,0 +1,564 @@
+// grouped_q4.cu -- grouped SwiGLU experts with 4-bit codebook weights at decode batch
+// sizes (<= 64 tokens per expert), on the tensor cores.
+//
+// Weight format: element (e, r, c) of a [rows][in] matrix is codebook[code] * scale,
+// code = nibble c of row r (element 2i low, 2i+1 high nibble of byte i), one bf16
+// scale per 64 consecutive input-dim elements.  This path needs an affine codebook
+// with a half-integer centre, c_j = b * (j - j0) (the uniform 16-entry codebook on
+// [-1, 1] has b = 2/15, j0 = 7.5); others use the generic kernels.
+//
+// Pipeline per CTA (one per SM):
+//  * warp 0 lane 0: TMA loads of the packed codes (128 rows x 32 bytes per matrix and
+//    64-element slab, unswizzled) and of the token rows into an 8-deep "raw" ring;
+//  * warps 6-13 (dequant): turn one slab of codes into bf16 weights in the 128-byte
+//    swizzled layout the MMA reads, in a 3-deep "A" ring.  A nibble pair is placed
+//    in the mantissa of a bf16 pair with one shift + LOP3: bits 0x4300 | (j << 1) are
+//    exactly 128 + 2j, so one bf16x2 subtraction gives the exact integers 2j - 2j0,
+//    and one bf16x2 multiply by s*b/2 gives the weights (one rounding);
+//  * warp 1 lane 0: tcgen05.mma from the A ring and the token rows still in the raw
+//    ring, accumulators in TMEM (gate and up in separate column ranges);
+//  * warps 2-5: epilogue as in the bf16 kernel.
+// The shift + LOP3 pairs nibbles m and m+4 of a 32-bit word, so each 8-element group
+// of a weight row is stored in the order (0,4,1,5,2,6,3,7).  The dot product does not
+// care about the order of k as long as both operands share it: the token rows (x_perm,
+// built here) and the intermediate h (written by the gate/up epilogue) are stored in
+// the same order.
+#include "moe_internal.cuh"
+#include "tc_common.cuh"
+
+#include <algorithm>
+#include <cmath>
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int kRows = 128;                  // weight rows per tile (MMA M)
+constexpr int kMaxN = 64;                   // tokens per tile
+constexpr int kSlab = 64;                   // k elements per slab
+constexpr int kNBox = 16;
+constexpr int kRawStages = 8;
+constexpr int kAStages = 3;
+constexpr int kCodeBytes = kRows * kSlab / 2;  // 4 KB: one matrix slab of codes
+constexpr int kRawBytes = 16384;               // two code slabs (8 KB) + token rows (8 KB)
+constexpr int kRawTok = 8192;                  // offset of the token rows in a raw stage
+constexpr int kABytes = kRows * 128;           // 16 KB bf16 slab
+constexpr int kAStageBytes = 2 * kABytes;
+constexpr int kTmemCols = 512;
+constexpr int kBufCols = 256;
+constexpr int kUpCol = 128;
+constexpr int kEpiWarps = 4;
+constexpr int kDeqWarps = 8;
+constexpr int kDeqThreads = kDeqWarps * 32;
+constexpr int kThreads = (2 + kEpiWarps + kDeqWarps) * 32;
+constexpr int kMetaRing = 8;
+constexpr int kSmemBytes = kRawStages * kRawBytes + kAStages * kAStageBytes + 1024 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory");
+
+enum : int { kGateUp = 0, kDown = 1 };
+
+__host__ __device__ constexpr uint32_t pack_tile(int down, int e, int rb) {
+    return (uint32_t(down) << 31) | (uint32_t(e) << 16) | (uint32_t(rb) << 8);
+}
+
+struct Params {
+    const int32_t *offsets;
+    const uint32_t *tiles;
+    const int *n_tiles;
+    int *tile_counter;
+    int *done;
+    int32_t *err;
+    uint16_t *h;
+    uint16_t *y;
+    const uint16_t *gs, *us, *ds;   // bf16 block scales
+    float half_b;                   // b / 2
+    uint32_t centre2;               // bf16x2 of 128 + 2*j0
+    int E, H, I, A;
+};
+
+// The 8-element group order of the weights: position q holds element kSigma[q].
+__device__ __forceinline__ int sigma_inv(int i) { return ((i & 3) << 1) | (i >> 2); }
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// 32 codes (16 bytes) -> 32 bf16 weights written as four swizzled 16-byte chunks of row
+// `row`, chunks 4*half .. 4*half+3 of the 64-element slab.
+__device__ __forceinline__ void dequant_unit(const uint8_t *codes, uint32_t a_base, int row, int half, uint32_t gamma2,
+                                             uint32_t centre2) {
+    const uint4 cw = *reinterpret_cast<const uint4 *>(codes);
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w = words[i];
+        uint32_t p[4];
+        p[0] = ((w << 1) & 0x001E001Eu) | 0x43004300u;   // elements 0, 4
+        p[1] = ((w >> 3) & 0x001E001Eu) | 0x43004300u;   // 1, 5
+        p[2] = ((w >> 7) & 0x001E001Eu) | 0x43004300u;   // 2, 6
+        p[3] = ((w >> 11) & 0x001E001Eu) | 0x43004300u;  // 3, 7
+#pragma unroll
+        for (int q = 0; q < 4; ++q) p[q] = bf16x2_mul(bf16x2_sub(p[q], centre2), gamma2);
+        const int j = 4 * half + i;
+        const uint32_t addr = a_base + uint32_t(row * 128 + ((j ^ (row & 7)) << 4));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(p[0]), "r"(p[1]), "r"(p[2]),
+                     "r"(p[3])
+                     : "memory");
+    }
+}
+
+__device__ __forceinline__ uint32_t gamma_pair(const uint16_t *scales, size_t idx, float half_b) {
+    const float s = bf16_bits_to_f32(__ldg(scales + idx)) * half_b;
+    const uint32_t g = f32_to_bf16_bits(s);
+    return g | (g << 16);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constant__ CUtensorMap tm_uc,
+                 const __grid_constant__ CUtensorMap tm_dc, const __grid_constant__ CUtensorMap tm_x,
+                 const __grid_constant__ CUtensorMap tm_h, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *raw = smem;
+    uint8_t *aring = smem + kRawStages * kRawBytes;
+    uint8_t *ctrl = aring + kAStages * kAStageBytes;
+    uint64_t *rfull = reinterpret_cast<uint64_t *>(ctrl);   // [kRawStages]
+    uint64_t *rempty = rfull + kRawStages;                  // [kRawStages]
+    uint64_t *afull = rempty + kRawStages;                  // [kAStages]
+    uint64_t *aempty = afull + kAStages;                    // [kAStages]
+    uint64_t *accf = aempty + kAStages;                     // [2]
+    uint64_t *acce = accf + 2;                              // [2]
+    uint64_t *tmf = acce + 2;                               // [kMetaRing]
+    uint64_t *tme = tmf + kMetaRing;                        // [kMetaRing]
+    uint64_t *drain = tme + kMetaRing;                      // [1]
+    int *rmeta = reinterpret_cast<int *>(drain + 1);        // [kRawStages][8]
+    int *tmeta = rmeta + 8 * kRawStages;                    // [kMetaRing][8]
+    volatile int *abort = tmeta + 8 * kMetaRing;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmeta + 8 * kMetaRing + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRawStages; ++s) {
+            mbar_init(smem_u32(&rfull[s]), 1);
+            mbar_init(smem_u32(&rempty[s]), 1);
+        }
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(smem_u32(&afull[s]), kDeqWarps);
+            mbar_init(smem_u32(&aempty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&accf[b]), 1);
+            mbar_init(smem_u32(&acce[b]), kEpiWarps);
+        }
+        for (int s = 0; s < kMetaRing; ++s) {
+            mbar_init(smem_u32(&tmf[s]), 1);
+            mbar_init(smem_u32(&tme[s]), kEpiWarps);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "n"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    griddep_launch_dependents();
+    griddep_wait();
+    const uint32_t tmem_base = *tmem_slot;
+    const int n_tiles = *p.n_tiles;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int r = 0, slot = 0;
+        uint32_t rp = 0, mphase = 0;
+        int next = atomicAdd(p.tile_counter, 1);
+        for (;;) {
+            const int t = next;
+            if (t >= n_tiles || *abort) break;
+            next = atomicAdd(p.tile_counter, 1);
+            const uint32_t entry = __ldg(p.tiles + t);
+            const int down = int(entry >> 31), e0 = int((entry >> 16) & 0xFF), rb = int((entry >> 8) & 0xFF);
+            const int e = min(e0, p.E - 1);
+            const int off = __ldg(p.offsets + e);
+            int m = __ldg(p.offsets + e + 1) - off;
+            if (e0 >= p.E || off < 0 || m <= 0 || m > kMaxN || off + m > p.A) {
+                record_error(p.err, MOE_ERR_DEVICE);
+                m = 0;
+            }
+            const int r0 = m > 0 ? off : 0;
+            const int N = m > 0 ? (m + 15) & ~15 : 16;
+            if (down) {
+                const int need = (p.I / kRows) * kEpiWarps;
+                long long n = 0;
+                for (;;) {
+                    int v;
+                    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p.done + e) : "memory");
+                    if (v >= need || *abort) break;
+                    if (++n > kSpinLimit) {
+                        record_error(p.err, MOE_ERR_DEVICE);
+                        *abort = 1;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, p.err, abort);
+            int *tm = tmeta + 8 * slot;
+            tm[0] = down;
+            tm[1] = e;
+            tm[2] = rb;
+            tm[3] = r0;
+            tm[4] = m;
+            tm[5] = N;
+            mbar_arrive(smem_u32(&tmf[slot]));
+            if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
+
+            const int kdim = down ? p.I : p.H;
+            const int nslab = kdim / kSlab;
+            const int two = down && N <= kMaxN / 2 && nslab % 2 == 0;
+            const int nstage = two ? nslab / 2 : nslab;
+            const int nbox = N / kNBox;
+            const uint32_t bytes = (down && !two ? kCodeBytes : 2 * kCodeBytes) + (two ? 2 : 1) * nbox * kNBox * 128;
+            const int wrow = e * (down ? p.H : p.I) + rb * kRows;
+            for (int ks = 0; ks < nstage; ++ks) {
+                mbar_wait(smem_u32(&rempty[r]), rp ^ 1, p.err, abort);
+                int *mt = rmeta + 8 * r;
+                mt[0] = down | (two << 2);
+                mt[1] = ks;
+                mt[2] = nstage;
+                mt[3] = N;
+                mt[4] = e;
+                mt[5] = rb;
+                const uint32_t fb = smem_u32(&rfull[r]);
+                mbar_arrive_expect_tx(fb, bytes);
+                const uint32_t base = smem_u32(raw + r * kRawBytes);
+                if (!down) {
+                    tma_load_2d(base, &tm_gc, ks * (kSlab / 2), wrow, fb);
+                    tma_load_2d(base + kCodeBytes, &tm_uc, ks * (kSlab / 2), wrow, fb);
+                    for (int q = 0; q < nbox; ++q)
+                        tma_load_2d(base + kRawTok + q * 2048, &tm_x, ks * kSlab, r0 + q * kNBox, fb);
+                } else if (two) {
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int s2 = 2 * ks + h2;
+                        tma_load_2d(base + h2 * kCodeBytes, &tm_dc, s2 * (kSlab / 2), wrow, fb);
+                        for (int q = 0; q < nbox; ++q)
+                            tma_load_2d(base + kRawTok + h2 * 4096 + q * 2048, &tm_h, s2 * kSlab, r0 + q * kNBox, fb);
+                    }
+                } else {
+                    tma_load_2d(base, &tm_dc, ks * (kSlab / 2), wrow, fb);
+                    for (int q = 0; q < nbox; ++q)
+                        tma_load_2d(base + kRawTok + q * 2048, &tm_h, ks * kSlab, r0 + q * kNBox, fb);
+                }
+                if (++r == kRawStages) { r = 0; rp ^= 1; }
+            }
+        }
+        mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, p.err, abort);
+        tmeta[8 * slot] = -1;
+        mbar_arrive(smem_u32(&tmf[slot]));
+        mbar_wait(smem_u32(&rempty[r]), rp ^ 1, p.err, abort);
+        rmeta[8 * r + 1] = -1;
+        mbar_arrive(smem_u32(&rfull[r]));
+    } else if (warp >= 2 + kEpiWarps) {
+        // ------------------------------------------------ dequant
+        const int u = (warp - 2 - kEpiWarps) * 32 + lane;   // 0..255
+        const int row = u >> 1, half = u & 1;
+        int r = 0, a = 0;
+        uint32_t rp = 0, ap = 0;
+        for (;;) {
+            mbar_wait(smem_u32(&rfull[r]), rp, p.err, abort);
+            const int *mt = rmeta + 8 * r;
+            const int kind = mt[0], ks = mt[1], e = mt[4], rb = mt[5];
+            mbar_wait(smem_u32(&aempty[a]), ap ^ 1, p.err, abort);
+            if (ks >= 0 && !*abort) {
+                const int down = kind & 3, two = kind >> 2;
+                const uint8_t *rbase = raw + r * kRawBytes;
+                const uint32_t abase = smem_u32(aring + a * kAStageBytes);
+                if (!down) {
+                    const size_t srow = (size_t)(e * p.I + rb * kRows + row) * (p.H / kSlab) + ks;
+                    dequant_unit(rbase + row * 32 + half * 16, abase, row, half, gamma_pair(p.gs, srow, p.half_b),
+                                 p.centre2);
+                    dequant_unit(rbase + kCodeBytes + row * 32 + half * 16, abase + kABytes, row, half,
+                                 gamma_pair(p.us, srow, p.half_b), p.centre2);
+                } else {
+                    const size_t srow = (size_t)(e * p.H + rb * kRows + row) * (p.I / kSlab);
+                    for (int h2 = 0; h2 < 1 + two; ++h2)
+                        dequant_unit(rbase + h2 * kCodeBytes + row * 32 + half * 16, abase + h2 * kABytes, row, half,
+                                     gamma_pair(p.ds, srow + (two ? 2 * ks + h2 : ks), p.half_b), p.centre2);
+                }
+                // generic-proxy smem writes -> visible to the tensor core
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&afull[a]));
+            if (++r == kRawStages) { r = 0; rp ^= 1; }
+            if (++a == kAStages) { a = 0; ap ^= 1; }
+            if (ks < 0 || *abort) break;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        int r = 0, a = 0, tile_count = 0;
+        uint32_t ap = 0;
+        for (;;) {
+            mbar_wait(smem_u32(&afull[a]), ap, p.err, abort);
+            const int *mt = rmeta + 8 * r;
+            const int kind = mt[0], ks = mt[1], nstage = mt[2], N = mt[3];
+            if (ks < 0 || *abort) break;
+            const int down = kind & 3, two = kind >> 2;
+            const int b = tile_count & 1;
+            if (ks == 0) {
+                mbar_wait(smem_u32(&acce[b]), ((tile_count >> 1) & 1) ^ 1, p.err, abort);
+                tc_fence_after();
+            }
+            tc_fence_after();
+            const uint32_t d = tmem_base + uint32_t(b * kBufCols);
+            const uint32_t idesc = instr_desc(kRows, N);
+            const uint32_t a0 = smem_u32(aring + a * kAStageBytes);
+            const uint32_t bb = smem_u32(raw + r * kRawBytes) + kRawTok;
+            if (!down) {
+#pragma unroll
+                for (int kk = 0; kk < kSlab / 16; ++kk) {
+                    const uint64_t bdesc = smem_desc(bb + kk * 32);
+                    mma_bf16(d, smem_desc(a0 + kk * 32), bdesc, idesc, (ks | kk) != 0);
+                    mma_bf16(d + kUpCol, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, (ks | kk) != 0);
+                }
+            } else {
+                for (int h2 = 0; h2 < 1 + two; ++h2)
+#pragma unroll
+                    for (int kk = 0; kk < kSlab / 16; ++kk)
+                        mma_bf16(d, smem_desc(a0 + h2 * kABytes + kk * 32), smem_desc(bb + h2 * 4096 + kk * 32), idesc,
+                                 (ks | h2 | kk) != 0);
+            }
+            mma_commit(smem_u32(&aempty[a]));
+            mma_commit(smem_u32(&rempty[r]));
+            if (ks == nstage - 1) {
+                mma_commit(smem_u32(&accf[b]));
+                ++tile_count;
+            }
+            if (++r == kRawStages) r = 0;
+            if (++a == kAStages) { a = 0; ap ^= 1; }
+        }
+        mma_commit(smem_u32(drain));
+        mbar_wait(smem_u32(drain), 0, p.err, abort);
+    } else if (warp >= 2 && warp < 2 + kEpiWarps) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        int slot = 0, tile_count = 0;
+        uint32_t mphase = 0;
+        for (;;) {
+            mbar_wait(smem_u32(&tmf[slot]), mphase, p.err, abort);
+            const int *tm = tmeta + 8 * slot;
+            const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], N = tm[5];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tme[slot]));
+            if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
+            if (down < 0 || *abort) break;
+            const int b = tile_count & 1;
+            mbar_wait(smem_u32(&accf[b]), (tile_count >> 1) & 1, p.err, abort);
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(b * kBufCols);
+            const int col = rb * kRows + row;
+            // h is stored in the weights' 8-element group order (see the file comment)
+            const int hcol = (col & ~7) | sigma_inv(col & 7);
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                if (down) {
+                    float v[16];
+                    tmem_ld16(taddr + c0, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < m) p.y[(size_t)(r0 + c0 + j) * p.H + col] = f32_to_bf16_bits(v[j]);
+                } else {
+                    float g[16], uu[16];
+                    tmem_ld16(taddr + c0, g);
+                    tmem_ld16(taddr + kUpCol + c0, uu);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < m)
+                            p.h[(size_t)(r0 + c0 + j) * p.I + hcol] = f32_to_bf16_bits(swiglu(g[j], uu[j]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acce[b]));
+            if (!down) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done + e) : "memory");
+                }
+            }
+            ++tile_count;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// x_perm[p] = x[order[p] / k] with every 8-element group in the weights' order
+// (0,4,1,5,2,6,3,7).  Block 0 builds the tile list (one token chunk per expert) and
+// clears the scheduling counters.
+__global__ void __launch_bounds__(256)
+q4_prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
+               int T, int k, int H, int I, int E, uint16_t *__restrict__ x_perm, uint32_t *tiles, int *n_tiles,
+               int *tile_counter, int *done, int32_t *err) {
+    griddep_launch_dependents();
+    griddep_wait();
+    if (blockIdx.x > 0) {
+        const int pr = blockIdx.x - 1;
+        const int a = __ldg(order + pr);
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
+        const bool bad = a < 0 || a >= T * k;
+        if (bad && threadIdx.x == 0) record_error(err, MOE_ERR_DEVICE);
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(bad ? 0 : a / k) * H);
+        for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
+            const uint4 v = bad ? make_uint4(0, 0, 0, 0) : __ldg(src + i);
+            // elements e0..e7 in (v.x lo, v.x hi, v.y lo, ...): output (e0,e4),(e1,e5),(e2,e6),(e3,e7)
+            uint4 o;
+            o.x = __byte_perm(v.x, v.z, 0x5410);
+            o.y = __byte_perm(v.x, v.z, 0x7632);
+            o.z = __byte_perm(v.y, v.w, 0x5410);
+            o.w = __byte_perm(v.y, v.w, 0x7632);
+            dst[i] = o;
+        }
+        return;
+    }
+    __shared__ int s_n[kMaxE + 1];
+    if (threadIdx.x == 0) {
+        int n = 0;
+        for (int e = 0; e < E; ++e) {
+            s_n[e] = n;
+            if (offsets[e + 1] > offsets[e]) ++n;
+        }
+        s_n[E] = n;
+        *tile_counter = 0;
+    }
+    __syncthreads();
+    const int n_act = s_n[E];
+    const int gu_per = I / kRows, dn_per = H / kRows;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        done[e] = 0;
+        if (offsets[e + 1] > offsets[e]) {
+            const int i = s_n[e];
+            for (int r = 0; r < gu_per; ++r) tiles[i * gu_per + r] = pack_tile(0, e, r);
+            for (int r = 0; r < dn_per; ++r) tiles[n_act * gu_per + i * dn_per + r] = pack_tile(1, e, r);
+        }
+    }
+    if (threadIdx.x == 0) *n_tiles = n_act * (gu_per + dn_per);
+}
+
+size_t xperm_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * s.H * 2 + 255) / 256 * 256; }
+
+bool set_attr() {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(q4_swiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess)
+            return false;
+        attr_set[dev] = true;
+    }
+    return true;
+}
+
+}  // namespace
+
+// The codebook is affine with a half-integer centre: c_j = b (j - j0), 2 j0 an integer
+// in [0, 30], to within 1e-6 of its largest entry.  Returns b and 2 j0.
+bool q4_codebook_affine(const float *cb, float *b_out, int *twice_j0) {
+    const double b = (double(cb[15]) - double(cb[0])) / 15.0;
+    if (!(b > 0)) return false;
+    const double j0 = -double(cb[0]) / b;
+    const long t = std::lround(2.0 * j0);
+    if (t < 0 || t > 30 || std::fabs(2.0 * j0 - double(t)) > 1e-4) return false;
+    double mx = 0;
+    for (int j = 0; j < 16; ++j) mx = std::max(mx, std::fabs(double(cb[j])));
+    for (int j = 0; j < 16; ++j)
+        if (std::fabs(double(cb[j]) - b * (j - 0.5 * double(t))) > 1e-6 * mx) return false;
+    *b_out = float(b);
+    *twice_j0 = int(t);
+    return true;
+}
+
+constexpr int kQ4MaxT = kMaxN;
+
+bool q4_path_supported(const moe_shape &s) {
+    return s.act_dtype == MOE_DT_BF16 && s.w_dtype == MOE_DT_Q4 && s.q_block == kSlab && s.T >= 1 &&
+           s.T <= kQ4MaxT && s.H % kRows == 0 && s.I % kRows == 0 && s.H / kRows <= 256 && s.I / kRows <= 256;
+}
+
+size_t q4_part_bytes(const moe_shape &s) {
+    const size_t tiles = (size_t)s.E * (s.I / kRows + s.H / kRows);
+    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (tiles * 4 + 255) / 256 * 256;
+}
+
+cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
+                      const void *wg, const void *wu, const void *wd, const moe_q4 *q4, float *part, void *h, void *y,
+                      int32_t *err, cudaStream_t st) {
+    float b = 0;
+    int t2 = 0;
+    if (!q4 || !q4_codebook_affine(q4->codebook, &b, &t2)) return cudaErrorInvalidValue;
+    const int A = s.T * s.k;
+    char *base = reinterpret_cast<char *>(part);
+    uint16_t *x_perm = reinterpret_cast<uint16_t *>(base);
+    int *sched = reinterpret_cast<int *>(base + xperm_bytes(s));
+    int *tile_counter = sched, *n_tiles = sched + 1, *done = sched + 64;
+    uint32_t *tiles = reinterpret_cast<uint32_t *>(base + xperm_bytes(s) + 256 + (size_t)kMaxE * 4);
+
+    CUtensorMap mg, mu, md, mx, mh;
+    if (!make_map(&mg, wg, (uint64_t)s.E * s.I, s.H / 2, kRows, kSlab / 2, true) ||
+        !make_map(&mu, wu, (uint64_t)s.E * s.I, s.H / 2, kRows, kSlab / 2, true) ||
+        !make_map(&md, wd, (uint64_t)s.E * s.H, s.I / 2, kRows, kSlab / 2, true) ||
+        !make_map(&mx, x_perm, A, s.H, kNBox) || !make_map(&mh, h, A, s.I, kNBox))
+        return cudaErrorInvalidValue;
+
+    cudaError_t e = launch_pdl(q4_prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
+                               offsets, s.T, s.k, s.H, s.I, s.E, x_perm, tiles, n_tiles, tile_counter, done, err);
+    if (e != cudaSuccess) return e;
+    if (!set_attr()) return cudaErrorInvalidValue;
+    Params prm{};
+    prm.offsets = offsets;
+    prm.tiles = tiles;
+    prm.n_tiles = n_tiles;
+    prm.tile_counter = tile_counter;
+    prm.done = done;
+    prm.err = err;
+    prm.h = static_cast<uint16_t *>(h);
+    prm.y = static_cast<uint16_t *>(y);
+    prm.gs = static_cast<const uint16_t *>(q4->gate_scales);
+    prm.us = static_cast<const uint16_t *>(q4->up_scales);
+    prm.ds = static_cast<const uint16_t *>(q4->down_scales);
+    prm.half_b = 0.5f * b;
+    const float centre = 128.0f + float(t2);
+    uint32_t cbits;
+    memcpy(&cbits, &centre, 4);
+    const uint32_t c16 = cbits >> 16;  // 128 + 2 j0 is exact in bf16
+    prm.centre2 = c16 | (c16 << 16);
+    prm.E = s.E;
+    prm.H = s.H;
+    prm.I = s.I;
+    prm.A = A;
+    return launch_pdl(q4_swiglu_kernel, dim3(sm_count()), dim3(kThreads), kSmemBytes, st, mg, mu, md, mx, mh, prm);
+}
+
+}  // namespace moe

@@ -25,13 +25,14 @@
 // The token rows are first gathered into permuted order (x_perm) so that every
 // expert's rows are contiguous for TMA; the same prep kernel builds the tile list.
 #include "moe_internal.cuh"
+#include "tc_common.cuh"
 
-#include <cuda.h>
 #include <algorithm>
-#include <mutex>
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 constexpr int kStages = 4;
 constexpr int kRows = 128;                 // weight rows per tile (MMA M)
@@ -49,7 +50,6 @@ constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kMetaRing = 8;
 constexpr int kCtrlBytes = 1024;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*alignment*/ + kCtrlBytes;
-constexpr long long kSpinLimit = 1ll << 22;
 constexpr int kRouterN = 64;               // tokens per router tile: twice the tiles, two k-slabs per stage
 
 // Tile list entry: bit 31 = down tile, bits 16-23 expert, bits 8-15 row block, bits 0-7 token chunk.
@@ -77,96 +77,6 @@ struct Params {
     float *logits;              // [T][E]
     const float *bias;          // [E] or null
 };
-
-// ---------------------------------------------------------------- PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: after kSpinLimit polls record the error and raise the CTA's abort flag,
-// so that every later wait of the CTA gives up at once and the kernel drains.
-__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, int32_t *err, volatile int *abort) {
-    long long n = 0;
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort) return;
-        if (++n > kSpinLimit) {
-            record_error(err, MOE_ERR_DEVICE);
-            *abort = 1;
-            return;
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128 B, 8-row
-// groups 1024 B apart (stride byte offset), fixed version bits 46-48 = 0b001.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
-    return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
-           (uint64_t(1) << 46) | (uint64_t(2) << 61);
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, M x N.
-__device__ __forceinline__ uint32_t instr_desc(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 struct TileInfo {
     int down, e, rb, r0, m, N;
@@ -545,49 +455,6 @@ prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, c
 
 // ---------------------------------------------------------------- host side
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return fn;
-}
-
-// 2-D bf16 tensor map over a row-major [rows][cols] matrix; box = 64 cols x box_rows, 128-B swizzle.
-bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {kSlab, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int sm_count() {
-    static int n[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return 148;
-    if (!n[dev]) {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        n[dev] = v > 0 ? v : 148;
-    }
-    return n[dev];
-}
-
 constexpr int kMaxT = 8192;
 
 size_t xperm_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * s.H * 2 + 255) / 256 * 256; }
@@ -619,7 +486,7 @@ bool router_tc_supported(const moe_shape &s) {
 cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
                              int32_t *err, cudaStream_t st) {
     CUtensorMap mw, mx;
-    if (!make_map(&mw, wr, s.E, s.H, kRows) || !make_map(&mx, x, s.T, s.H, kNBox)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&mw, wr, s.E, s.H, kRows) || !tc::make_map(&mx, x, s.T, s.H, kNBox)) return cudaErrorInvalidValue;
     if (!set_smem_attr()) return cudaErrorInvalidValue;
     const int tiles = ((s.E + kRows - 1) / kRows) * ((s.T + kRouterN - 1) / kRouterN);
     Params prm{};
@@ -631,29 +498,34 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
     prm.T = s.T;
     prm.logits = logits;
     prm.bias = bias;
-    return launch_pdl(tc_swiglu_kernel, dim3(std::min(tiles, sm_count())), dim3(kThreads), kSmemBytes, st, mw, mw, mw,
+    return launch_pdl(tc_swiglu_kernel, dim3(std::min(tiles, tc::sm_count())), dim3(kThreads), kSmemBytes, st, mw, mw, mw,
                       mx, mx, prm);
 }
 
-// 0 = the per-output-element kernels of grouped_simple.cu; 1 = the tensor-core kernel.
+// 0 = the per-output-element kernels of grouped_simple.cu; 1 = the bf16 tensor-core
+// kernel; 2 = the 4-bit tensor-core kernel of grouped_q4.cu (which also needs an affine
+// codebook, checked at launch time by the caller).
 int select_grouped_path(const moe_shape &s) {
     if (s.act_dtype == MOE_DT_BF16 && s.w_dtype == MOE_DT_BF16 && s.T >= 1 && s.T <= kMaxT && s.H % kRows == 0 &&
         s.I % kRows == 0 && s.H / kRows <= 256 && s.I / kRows <= 256)
         return 1;
+    if (q4_path_supported(s)) return 2;
     return 0;
 }
 
 size_t grouped_fast_part_bytes(int path, const moe_shape &s) {
+    if (path == 2) return q4_part_bytes(s);
     if (path != 1) return 0;
     return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (max_tiles(s) * 4 + 255) / 256 * 256;
 }
 
-int grouped_fast_launches(int path, const moe_shape &) { return path == 1 ? 2 : 0; }
+int grouped_fast_launches(int path, const moe_shape &) { return path == 1 || path == 2 ? 2 : 0; }
 
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
-                                const moe_q4 *, const int32_t *, float *part, void *h, void *y, int32_t *err,
+                                const moe_q4 *q4, const int32_t *, float *part, void *h, void *y, int32_t *err,
                                 cudaStream_t st) {
+    if (path == 2) return launch_q4(s, x, offsets, order, wg, wu, wd, q4, part, h, y, err, st);
     if (path != 1) return cudaErrorInvalidValue;
     const int A = s.T * s.k;
     char *base = reinterpret_cast<char *>(part);
@@ -663,9 +535,9 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     uint32_t *tiles = reinterpret_cast<uint32_t *>(base + xperm_bytes(s) + 256 + (size_t)kMaxE * 4);
 
     CUtensorMap mg, mu, md, mx, mh;
-    if (!make_map(&mg, wg, (uint64_t)s.E * s.I, s.H, kRows) || !make_map(&mu, wu, (uint64_t)s.E * s.I, s.H, kRows) ||
-        !make_map(&md, wd, (uint64_t)s.E * s.H, s.I, kRows) || !make_map(&mx, x_perm, A, s.H, kNBox) ||
-        !make_map(&mh, h, A, s.I, kNBox))
+    if (!tc::make_map(&mg, wg, (uint64_t)s.E * s.I, s.H, kRows) || !tc::make_map(&mu, wu, (uint64_t)s.E * s.I, s.H, kRows) ||
+        !tc::make_map(&md, wd, (uint64_t)s.E * s.H, s.I, kRows) || !tc::make_map(&mx, x_perm, A, s.H, kNBox) ||
+        !tc::make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
 
     cudaError_t e = launch_pdl(prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
@@ -687,7 +559,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.H = s.H;
     prm.I = s.I;
     prm.A = A;
-    return launch_pdl(tc_swiglu_kernel, dim3(sm_count()), dim3(kThreads), kSmemBytes, st, mg, mu, md, mx, mh, prm);
+    return launch_pdl(tc_swiglu_kernel, dim3(tc::sm_count()), dim3(kThreads), kSmemBytes, st, mg, mu, md, mx, mh, prm);
 }
 
 }  // namespace moe

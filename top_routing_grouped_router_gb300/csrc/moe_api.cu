@@ -120,7 +120,10 @@ int do_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t 
 int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order, const void *wg,
                const void *wu, const void *wd, const moe_q4 *q4, void *y, void *ws, cudaStream_t st) {
     const WsLayout L = ws_layout(s);
-    const int path = select_grouped_path(s);
+    int path = select_grouped_path(s);
+    float cb_b;
+    int cb_t2;
+    if (path == 2 && !q4_codebook_affine(q4->codebook, &cb_b, &cb_t2)) path = 0;  // generic codebook
     if (path > 0)
         return launch_rc(launch_grouped_fast(path, s, x, offsets, order, wg, wu, wd, q4,
                                              at<int32_t>(ws, L.active), at<float>(ws, L.part), at<void>(ws, L.h),
@@ -221,7 +224,7 @@ int moe_forward_launches(const moe_shape *shape, int32_t *launches) {
         *launches = 0;
         return MOE_OK;
     }
-    const int path = select_grouped_path(s);
+    const int path = select_grouped_path(s);  // a non-affine 4-bit codebook takes path 0 (also 2 launches)
     *launches = (route_fuses(s) ? 1 : route_launches(s) + permute_launches(s)) +
                 (path > 0 ? grouped_fast_launches(path, s) : grouped_simple_launches(s)) + 1;
     return MOE_OK;

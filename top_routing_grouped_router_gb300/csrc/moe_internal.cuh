@@ -110,6 +110,12 @@ cudaError_t launch_permute(const moe_shape &s, const int32_t *ids, int32_t *coun
 cudaError_t launch_grouped_simple(const moe_shape &s, const void *x, const int32_t *offsets,
                                   const int32_t *order, const void *wg, const void *wu, const void *wd,
                                   const moe_q4 *q4, void *h, void *y, cudaStream_t st);
+bool q4_codebook_affine(const float *cb, float *b_out, int *twice_j0);
+bool q4_path_supported(const moe_shape &s);
+size_t q4_part_bytes(const moe_shape &s);
+cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
+                      const void *wg, const void *wu, const void *wd, const moe_q4 *q4, float *part, void *h, void *y,
+                      int32_t *err, cudaStream_t st);
 cudaError_t launch_unpermute(const moe_shape &s, const void *y, const float *w, const int32_t *pos, void *out,
                              cudaStream_t st);
 
