@@ -9,9 +9,11 @@
 //
 // Pipeline per CTA (one per SM):
 //  * warp 0 lane 0: TMA loads of the packed codes (128 rows x 32 bytes per matrix and
-//    64-element slab, unswizzled) and of the token rows into an 8-deep "raw" ring;
+//    64-element slab, unswizzled) and of the token rows into an 8-deep "raw" ring, and
+//    a bulk copy of each tile's block scales (contiguous for 128 consecutive rows) into
+//    one of two per-tile scale buffers;
 //  * warps 6-13 (dequant): turn one slab of codes into bf16 weights in the 128-byte
-//    swizzled layout the MMA reads, in a 3-deep "A" ring.  A nibble pair is placed
+//    swizzled layout the MMA reads, in a 2-deep "A" ring.  A nibble pair is placed
 //    in the mantissa of a bf16 pair with one shift + LOP3: bits 0x4300 | (j << 1) are
 //    exactly 128 + 2j, so one bf16x2 subtraction gives the exact integers 2j - 2j0,
 //    and one bf16x2 multiply by s*b/2 gives the weights (one rounding);
@@ -39,7 +41,7 @@ constexpr int kMaxN = 64;                   // tokens per tile
 constexpr int kSlab = 64;                   // k elements per slab
 constexpr int kNBox = 16;
 constexpr int kRawStages = 8;
-constexpr int kAStages = 3;
+constexpr int kAStages = 2;
 constexpr int kCodeBytes = kRows * kSlab / 2;  // 4 KB: one matrix slab of codes
 constexpr int kRawBytes = 16384;               // two code slabs (8 KB) + token rows (8 KB)
 constexpr int kRawTok = 8192;                  // offset of the token rows in a raw stage
@@ -53,7 +55,8 @@ constexpr int kDeqWarps = 8;
 constexpr int kDeqThreads = kDeqWarps * 32;
 constexpr int kThreads = (2 + kEpiWarps + kDeqWarps) * 32;
 constexpr int kMetaRing = 8;
-constexpr int kSmemBytes = kRawStages * kRawBytes + kAStages * kAStageBytes + 1024 + 1024;
+constexpr int kScaleBytes = 2 * 8192;          // one tile's block scales: 2 matrices x 128 rows x <= 32 blocks
+constexpr int kSmemBytes = kRawStages * kRawBytes + kAStages * kAStageBytes + 2 * kScaleBytes + 1024 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 enum : int { kGateUp = 0, kDown = 1 };
@@ -113,9 +116,8 @@ __device__ __forceinline__ void dequant_unit(const uint8_t *codes, uint32_t a_ba
     }
 }
 
-__device__ __forceinline__ uint32_t gamma_pair(const uint16_t *scales, size_t idx, float half_b) {
-    const float s = bf16_bits_to_f32(__ldg(scales + idx)) * half_b;
-    const uint32_t g = f32_to_bf16_bits(s);
+__device__ __forceinline__ uint32_t gamma_pair(uint16_t scale, float half_b) {
+    const uint32_t g = f32_to_bf16_bits(bf16_bits_to_f32(scale) * half_b);
     return g | (g << 16);
 }
 
@@ -127,7 +129,8 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *raw = smem;
     uint8_t *aring = smem + kRawStages * kRawBytes;
-    uint8_t *ctrl = aring + kAStages * kAStageBytes;
+    uint8_t *sbuf = aring + kAStages * kAStageBytes;        // [2][kScaleBytes] per-tile block scales
+    uint8_t *ctrl = sbuf + 2 * kScaleBytes;
     uint64_t *rfull = reinterpret_cast<uint64_t *>(ctrl);   // [kRawStages]
     uint64_t *rempty = rfull + kRawStages;                  // [kRawStages]
     uint64_t *afull = rempty + kRawStages;                  // [kAStages]
@@ -136,7 +139,9 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
     uint64_t *acce = accf + 2;                              // [2]
     uint64_t *tmf = acce + 2;                               // [kMetaRing]
     uint64_t *tme = tmf + kMetaRing;                        // [kMetaRing]
-    uint64_t *drain = tme + kMetaRing;                      // [1]
+    uint64_t *sfull = tme + kMetaRing;                      // [2]
+    uint64_t *sempty = sfull + 2;                           // [2]
+    uint64_t *drain = sempty + 2;                           // [1]
     int *rmeta = reinterpret_cast<int *>(drain + 1);        // [kRawStages][8]
     int *tmeta = rmeta + 8 * kRawStages;                    // [kMetaRing][8]
     volatile int *abort = tmeta + 8 * kMetaRing;
@@ -160,6 +165,10 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             mbar_init(smem_u32(&tmf[s]), 1);
             mbar_init(smem_u32(&tme[s]), kEpiWarps);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&sfull[b]), 1);
+            mbar_init(smem_u32(&sempty[b]), kDeqWarps);
+        }
         mbar_init(smem_u32(drain), 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -180,7 +189,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
-        int r = 0, slot = 0;
+        int r = 0, slot = 0, tiles_done = 0;
         uint32_t rp = 0, mphase = 0;
         int next = atomicAdd(p.tile_counter, 1);
         for (;;) {
@@ -227,6 +236,23 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 
             const int kdim = down ? p.I : p.H;
             const int nslab = kdim / kSlab;
+            {
+                // the tile's block scales: 128 consecutive rows x nslab bf16, contiguous in memory
+                const int sb = tiles_done & 1;
+                mbar_wait(smem_u32(&sempty[sb]), ((tiles_done >> 1) & 1) ^ 1, p.err, abort);
+                const uint32_t sfb = smem_u32(&sfull[sb]);
+                const uint32_t sbytes = uint32_t(kRows * nslab * 2);
+                const size_t row0 = (size_t)e * (down ? p.H : p.I) + (size_t)rb * kRows;
+                const uint32_t dst = smem_u32(sbuf + sb * kScaleBytes);
+                mbar_arrive_expect_tx(sfb, down ? sbytes : 2 * sbytes);
+                if (down) {
+                    bulk_load(dst, p.ds + row0 * nslab, sbytes, sfb);
+                } else {
+                    bulk_load(dst, p.gs + row0 * nslab, sbytes, sfb);
+                    bulk_load(dst + kScaleBytes / 2, p.us + row0 * nslab, sbytes, sfb);
+                }
+                ++tiles_done;
+            }
             const int two = down && N <= kMaxN / 2 && nslab % 2 == 0;
             const int nstage = two ? nslab / 2 : nslab;
             const int nbox = N / kNBox;
@@ -274,34 +300,42 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         // ------------------------------------------------ dequant
         const int u = (warp - 2 - kEpiWarps) * 32 + lane;   // 0..255
         const int row = u >> 1, half = u & 1;
-        int r = 0, a = 0;
+        int r = 0, a = 0, tiles_done = 0;
         uint32_t rp = 0, ap = 0;
         for (;;) {
             mbar_wait(smem_u32(&rfull[r]), rp, p.err, abort);
             const int *mt = rmeta + 8 * r;
-            const int kind = mt[0], ks = mt[1], e = mt[4], rb = mt[5];
+            const int kind = mt[0], ks = mt[1], nstage = mt[2];
             mbar_wait(smem_u32(&aempty[a]), ap ^ 1, p.err, abort);
+            const int sb = tiles_done & 1;
+            if (ks == 0) mbar_wait(smem_u32(&sfull[sb]), (tiles_done >> 1) & 1, p.err, abort);
             if (ks >= 0 && !*abort) {
                 const int down = kind & 3, two = kind >> 2;
                 const uint8_t *rbase = raw + r * kRawBytes;
                 const uint32_t abase = smem_u32(aring + a * kAStageBytes);
+                const uint16_t *sc = reinterpret_cast<const uint16_t *>(sbuf + sb * kScaleBytes);
                 if (!down) {
-                    const size_t srow = (size_t)(e * p.I + rb * kRows + row) * (p.H / kSlab) + ks;
-                    dequant_unit(rbase + row * 32 + half * 16, abase, row, half, gamma_pair(p.gs, srow, p.half_b),
-                                 p.centre2);
+                    const int nblk = p.H / kSlab;
+                    dequant_unit(rbase + row * 32 + half * 16, abase, row, half,
+                                 gamma_pair(sc[row * nblk + ks], p.half_b), p.centre2);
                     dequant_unit(rbase + kCodeBytes + row * 32 + half * 16, abase + kABytes, row, half,
-                                 gamma_pair(p.us, srow, p.half_b), p.centre2);
+                                 gamma_pair(sc[kScaleBytes / 4 + row * nblk + ks], p.half_b), p.centre2);
                 } else {
-                    const size_t srow = (size_t)(e * p.H + rb * kRows + row) * (p.I / kSlab);
+                    const int nblk = p.I / kSlab;
                     for (int h2 = 0; h2 < 1 + two; ++h2)
                         dequant_unit(rbase + h2 * kCodeBytes + row * 32 + half * 16, abase + h2 * kABytes, row, half,
-                                     gamma_pair(p.ds, srow + (two ? 2 * ks + h2 : ks), p.half_b), p.centre2);
+                                     gamma_pair(sc[row * nblk + (two ? 2 * ks + h2 : ks)], p.half_b), p.centre2);
                 }
                 // generic-proxy smem writes -> visible to the tensor core
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&afull[a]));
+            if (ks >= 0 && ks == nstage - 1) {
+                // this tile's scales are no longer needed
+                if (lane == 0) mbar_arrive(smem_u32(&sempty[sb]));
+                ++tiles_done;
+            }
             if (++r == kRawStages) { r = 0; rp ^= 1; }
             if (++a == kAStages) { a = 0; ap ^= 1; }
             if (ks < 0 || *abort) break;
@@ -503,8 +537,9 @@ bool q4_codebook_affine(const float *cb, float *b_out, int *twice_j0) {
 constexpr int kQ4MaxT = kMaxN;
 
 bool q4_path_supported(const moe_shape &s) {
+    // a tile's scales (128 rows x in/64 bf16 per matrix) must fit one 8 KB half of a scale buffer
     return s.act_dtype == MOE_DT_BF16 && s.w_dtype == MOE_DT_Q4 && s.q_block == kSlab && s.T >= 1 &&
-           s.T <= kQ4MaxT && s.H % kRows == 0 && s.I % kRows == 0 && s.H / kRows <= 256 && s.I / kRows <= 256;
+           s.T <= kQ4MaxT && s.H % kRows == 0 && s.I % kRows == 0 && s.H <= 32 * kSlab && s.I <= 32 * kSlab;
 }
 
 size_t q4_part_bytes(const moe_shape &s) {
