@@ -94,9 +94,8 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 
 // 32 codes (16 bytes) -> 32 bf16 weights written as four swizzled 16-byte chunks of row
 // `row`, chunks 4*half .. 4*half+3 of the 64-element slab.
-__device__ __forceinline__ void dequant_unit(const uint8_t *codes, uint32_t a_base, int row, int half, uint32_t gamma2,
+__device__ __forceinline__ void dequant_unit(const uint4 cw, uint32_t a_base, int row, int half, uint32_t gamma2,
                                              uint32_t centre2) {
-    const uint4 cw = *reinterpret_cast<const uint4 *>(codes);
     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -304,28 +303,28 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         uint32_t rp = 0, ap = 0;
         for (;;) {
             mbar_wait(smem_u32(&rfull[r]), rp, p.err, abort);
-            const int *mt = rmeta + 8 * r;
-            const int kind = mt[0], ks = mt[1], nstage = mt[2];
+            const uint32_t mt = smem_u32(rmeta + 8 * r);
+            const int kind = int(lds_u32(mt)), ks = int(lds_u32(mt + 4)), nstage = int(lds_u32(mt + 8));
             mbar_wait(smem_u32(&aempty[a]), ap ^ 1, p.err, abort);
             const int sb = tiles_done & 1;
             if (ks == 0) mbar_wait(smem_u32(&sfull[sb]), (tiles_done >> 1) & 1, p.err, abort);
             if (ks >= 0 && !*abort) {
                 const int down = kind & 3, two = kind >> 2;
-                const uint8_t *rbase = raw + r * kRawBytes;
+                const uint32_t rbase = smem_u32(raw + r * kRawBytes) + uint32_t(row * 32 + half * 16);
                 const uint32_t abase = smem_u32(aring + a * kAStageBytes);
-                const uint16_t *sc = reinterpret_cast<const uint16_t *>(sbuf + sb * kScaleBytes);
-                if (!down) {
-                    const int nblk = p.H / kSlab;
-                    dequant_unit(rbase + row * 32 + half * 16, abase, row, half,
-                                 gamma_pair(sc[row * nblk + ks], p.half_b), p.centre2);
-                    dequant_unit(rbase + kCodeBytes + row * 32 + half * 16, abase + kABytes, row, half,
-                                 gamma_pair(sc[kScaleBytes / 4 + row * nblk + ks], p.half_b), p.centre2);
-                } else {
-                    const int nblk = p.I / kSlab;
-                    for (int h2 = 0; h2 < 1 + two; ++h2)
-                        dequant_unit(rbase + h2 * kCodeBytes + row * 32 + half * 16, abase + h2 * kABytes, row, half,
-                                     gamma_pair(sc[row * nblk + (two ? 2 * ks + h2 : ks)], p.half_b), p.centre2);
-                }
+                const uint32_t sc = smem_u32(sbuf + sb * kScaleBytes);
+                // both units' codes and scales are loaded before any arithmetic
+                const int nblk = (down ? p.I : p.H) / kSlab;
+                const int blk0 = down && two ? 2 * ks : ks;
+                const uint32_t si0 = sc + uint32_t(row * nblk + blk0) * 2;
+                const uint32_t si1 = down ? si0 + 2 : sc + kScaleBytes / 2 + uint32_t(row * nblk + ks) * 2;
+                const bool second = !down || two;
+                const uint4 c0 = lds_v4(rbase);
+                const uint4 c1 = second ? lds_v4(rbase + kCodeBytes) : c0;
+                const uint32_t g0 = gamma_pair(uint16_t(lds_u16(si0)), p.half_b);
+                const uint32_t g1 = second ? gamma_pair(uint16_t(lds_u16(si1)), p.half_b) : g0;
+                dequant_unit(c0, abase, row, half, g0, p.centre2);
+                if (second) dequant_unit(c1, abase + kABytes, row, half, g1, p.centre2);
                 // generic-proxy smem writes -> visible to the tensor core
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }

@@ -9,7 +9,8 @@
 namespace moe {
 namespace tc {
 
-constexpr long long kSpinLimit = 1ll << 22;
+constexpr long long kSpinLimit = 1ll << 22;   // polls of a global flag (with a 64 ns sleep)
+constexpr long long kPollLimit = 1ll << 20;   // mbarrier polls (each suspends up to 2 us)
 
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -24,25 +25,44 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Waits (suspended, up to the hint) for the phase with the given parity to complete.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(2000)
         : "memory");
     return ok != 0;
 }
 
-// Bounded wait: after kSpinLimit polls record the error and raise the CTA's abort flag,
-// so that every later wait of the CTA gives up at once and the kernel drains.
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// Bounded wait: after kPollLimit polls record the error and raise the CTA's abort flag,
+// so that every later wait of the CTA gives up at once and the kernel drains.  The flag
+// is checked every 16 polls.
 __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, int32_t *err, volatile int *abort) {
     long long n = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if (*abort) return;
-        if (++n > kSpinLimit) {
+        ++n;
+        if ((n & 15) == 0 && *abort) return;
+        if (n > kPollLimit) {
             record_error(err, MOE_ERR_DEVICE);
             *abort = 1;
             return;
