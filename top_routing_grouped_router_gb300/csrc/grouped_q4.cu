@@ -9,11 +9,11 @@
 //
 // Pipeline per CTA (one per SM):
 //  * warp 0 lane 0: TMA loads of the packed codes (128 rows x 32 bytes per matrix and
-//    64-element slab, unswizzled) and of the token rows into an 8-deep "raw" ring, and
+//    64-element slab, unswizzled) and of the token rows into a 6-deep "raw" ring, and
 //    a bulk copy of each tile's block scales (contiguous for 128 consecutive rows) into
 //    one of two per-tile scale buffers;
 //  * warps 6-13 (dequant): turn one slab of codes into bf16 weights in the 128-byte
-//    swizzled layout the MMA reads, in a 2-deep "A" ring.  A nibble pair is placed
+//    swizzled layout the MMA reads, in a 3-deep "A" ring.  A nibble pair is placed
 //    in the mantissa of a bf16 pair with one shift + LOP3: bits 0x4300 | (j << 1) are
 //    exactly 128 + 2j, so one bf16x2 subtraction gives the exact integers 2j - 2j0,
 //    and one bf16x2 multiply by s*b/2 gives the weights (one rounding);
@@ -40,8 +40,8 @@ constexpr int kRows = 128;                  // weight rows per tile (MMA M)
 constexpr int kMaxN = 64;                   // tokens per tile
 constexpr int kSlab = 64;                   // k elements per slab
 constexpr int kNBox = 16;
-constexpr int kRawStages = 8;
-constexpr int kAStages = 2;
+constexpr int kRawStages = 6;
+constexpr int kAStages = 3;
 constexpr int kCodeBytes = kRows * kSlab / 2;  // 4 KB: one matrix slab of codes
 constexpr int kRawBytes = 16384;               // two code slabs (8 KB) + token rows (8 KB)
 constexpr int kRawTok = 8192;                  // offset of the token rows in a raw stage

@@ -16,7 +16,7 @@
 // claim with an atomic counter; a down tile waits (bounded) until every epilogue warp
 // of every gate/up tile of its expert has published h.
 //
-// Roles per CTA (one CTA per SM): warp 0 lane 0 issues TMA loads into a 4-stage ring;
+// Roles per CTA (one CTA per SM): warp 0 lane 0 issues TMA loads into a 4-6 stage ring;
 // warp 1 owns the TMEM allocation and lane 0 issues the MMAs (tcgen05.commit frees a
 // stage when its MMAs are done, and hands a finished accumulator to the epilogue);
 // warps 2-5 are the epilogue (warp w reads TMEM lanes 32*(w%4)..+31), with two
@@ -34,14 +34,11 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 4;
 constexpr int kRows = 128;                 // weight rows per tile (MMA M)
 constexpr int kMaxN = 128;                 // tokens per tile (MMA N, multiple of 16)
 constexpr int kSlab = 64;                  // k elements per stage (one 128-byte swizzle row)
 constexpr int kNBox = 16;                  // token rows per activation TMA box
 constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
-constexpr int kBBytes = kMaxN * 128;       // 16 KB per token slab
-constexpr int kStageBytes = 2 * kABytes + kBBytes;
 constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
 constexpr int kBufCols = 256;
 constexpr int kUpCol = 128;                // up accumulator column offset inside a buffer
@@ -49,7 +46,16 @@ constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kMetaRing = 8;
 constexpr int kCtrlBytes = 1024;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*alignment*/ + kCtrlBytes;
+// Pipeline shape: token rows held per stage (BCap, a bound on N) and stage count.  Small
+// batches need little room for token rows, so they get more stages (more weight bytes in
+// flight); the tile list still chunks tokens by kMaxN.
+template <int BCap, int Stages>
+struct Cfg {
+    static constexpr int kBBytes = BCap * 128;
+    static constexpr int kStageBytes = 2 * kABytes + kBBytes;
+    static constexpr int kSmemBytes = Stages * kStageBytes + 1024 /*alignment*/ + kCtrlBytes;
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
 constexpr int kRouterN = 64;               // tokens per router tile: twice the tiles, two k-slabs per stage
 
 // Tile list entry: bit 31 = down tile, bits 16-23 expert, bits 8-15 row block, bits 0-7 token chunk.
@@ -103,10 +109,13 @@ __device__ __forceinline__ TileInfo read_tile(uint32_t entry, const Params &p, b
     return d;
 }
 
+template <int BCap, int kStages>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                  const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_h, const Params p) {
+    constexpr int kBBytes = Cfg<BCap, kStages>::kBBytes;
+    constexpr int kStageBytes = Cfg<BCap, kStages>::kStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ctrl = smem + kStages * kStageBytes;
@@ -214,7 +223,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             // stage (weights in both A regions, token rows in the two halves of B), so every
             // stage carries 32 KB of weights whatever the tile kind
             const int kdim = d.down == kDown ? p.I : p.H;
-            const int two = d.down != kGateUp && d.N <= kMaxN / 2 && (kdim / kSlab) % 2 == 0;
+            const int two = d.down != kGateUp && d.N <= BCap / 2 && (kdim / kSlab) % 2 == 0;
             const int nslab = kdim / kSlab;
             const int nstage = two ? nslab / 2 : nslab;
             const int nbox = d.N / kNBox;
@@ -463,17 +472,26 @@ size_t max_tiles(const moe_shape &s) {
     return chunks * (size_t)(s.I / kRows + s.H / kRows);
 }
 
+template <int BCap, int Stages>
 bool set_smem_attr() {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(tc_swiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(tc_swiglu_kernel<BCap, Stages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg<BCap, Stages>::kSmemBytes) != cudaSuccess)
             return false;
         attr_set[dev] = true;
     }
     return true;
+}
+
+template <int BCap, int Stages>
+cudaError_t launch_tc(dim3 grid, cudaStream_t st, const CUtensorMap &mg, const CUtensorMap &mu, const CUtensorMap &md,
+                      const CUtensorMap &mx, const CUtensorMap &mh, const Params &prm) {
+    if (!set_smem_attr<BCap, Stages>()) return cudaErrorInvalidValue;
+    return launch_pdl(tc_swiglu_kernel<BCap, Stages>, grid, dim3(kThreads), Cfg<BCap, Stages>::kSmemBytes, st, mg, mu,
+                      md, mx, mh, prm);
 }
 
 }  // namespace
@@ -487,7 +505,6 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
                              int32_t *err, cudaStream_t st) {
     CUtensorMap mw, mx;
     if (!tc::make_map(&mw, wr, s.E, s.H, kRows) || !tc::make_map(&mx, x, s.T, s.H, kNBox)) return cudaErrorInvalidValue;
-    if (!set_smem_attr()) return cudaErrorInvalidValue;
     const int tiles = ((s.E + kRows - 1) / kRows) * ((s.T + kRouterN - 1) / kRouterN);
     Params prm{};
     prm.err = err;
@@ -498,8 +515,7 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
     prm.T = s.T;
     prm.logits = logits;
     prm.bias = bias;
-    return launch_pdl(tc_swiglu_kernel, dim3(std::min(tiles, tc::sm_count())), dim3(kThreads), kSmemBytes, st, mw, mw, mw,
-                      mx, mx, prm);
+    return launch_tc<kMaxN, 4>(dim3(std::min(tiles, tc::sm_count())), st, mw, mw, mw, mx, mx, prm);
 }
 
 // 0 = the per-output-element kernels of grouped_simple.cu; 1 = the bf16 tensor-core
@@ -545,7 +561,6 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
                                tile_counter, done, err);
     if (e != cudaSuccess) return e;
 
-    if (!set_smem_attr()) return cudaErrorInvalidValue;
     Params prm{};
     prm.offsets = offsets;
     prm.tiles = tiles;
@@ -559,7 +574,11 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.H = s.H;
     prm.I = s.I;
     prm.A = A;
-    return launch_pdl(tc_swiglu_kernel, dim3(tc::sm_count()), dim3(kThreads), kSmemBytes, st, mg, mu, md, mx, mh, prm);
+    // every expert has at most T tokens: small batches take the deeper pipelines
+    const dim3 grid(tc::sm_count());
+    if (s.T <= 32) return launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, prm);
+    if (s.T <= 64) return launch_tc<64, 5>(grid, st, mg, mu, md, mx, mh, prm);
+    return launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, prm);
 }
 
 }  // namespace moe

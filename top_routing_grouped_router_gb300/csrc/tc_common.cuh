@@ -10,7 +10,7 @@ namespace moe {
 namespace tc {
 
 constexpr long long kSpinLimit = 1ll << 22;   // polls of a global flag (with a 64 ns sleep)
-constexpr long long kPollLimit = 1ll << 20;   // mbarrier polls (each suspends up to 2 us)
+constexpr long long kPollLimit = 1ll << 22;   // mbarrier polls
 
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -25,15 +25,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-// Waits (suspended, up to the hint) for the phase with the given parity to complete.
+// Tests (briefly suspending) whether the phase with the given parity has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "n"(2000)
+        : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
