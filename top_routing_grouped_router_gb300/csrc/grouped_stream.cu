@@ -40,15 +40,17 @@ constexpr int kSlab = 64;                  // k elements per stage (one 128-byte
 constexpr int kNBox = 16;                  // token rows per activation TMA box
 constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
 constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
-constexpr int kBufCols = 256;
-constexpr int kUpCol = 128;                // up accumulator column offset inside a buffer
+// Token chunks: an expert's m tokens are cut into ceil(m / cmax) nearly equal chunks
+// (multiples of 16), cmax = 128 or 256 by pipeline shape.
+__host__ __device__ inline int n_chunks(int me, int cmax) { return me > 0 ? (me + cmax - 1) / cmax : 0; }
+__host__ __device__ inline int chunk_base(int me, int nch) { return nch > 0 ? (((me + nch - 1) / nch) + 15) & ~15 : 0; }
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kMetaRing = 8;
 constexpr int kCtrlBytes = 1024;
 // Pipeline shape: token rows held per stage (BCap, a bound on N) and stage count.  Small
 // batches need little room for token rows, so they get more stages (more weight bytes in
-// flight); the tile list still chunks tokens by kMaxN.
+// flight); large batches take 256-token tiles.
 template <int BCap, int Stages>
 struct Cfg {
     static constexpr int kBBytes = BCap * 128;
@@ -77,6 +79,7 @@ struct Params {
     uint16_t *h;                // [A][I] bf16
     uint16_t *y;                // [A][H] bf16
     int E, H, I, A;
+    int cmax;                   // largest token chunk of the tile list
     // router mode: tiles are (row block of experts, 128-token chunk), one static sweep
     int router_tiles;           // > 0 selects router mode
     int T;
@@ -97,8 +100,9 @@ __device__ __forceinline__ TileInfo read_tile(uint32_t entry, const Params &p, b
     ok = d.e < p.E;
     const int off = ok ? __ldg(p.offsets + d.e) : 0;
     const int me = ok ? __ldg(p.offsets + d.e + 1) - off : 0;
-    d.r0 = off + nc * kMaxN;
-    d.m = min(kMaxN, me - nc * kMaxN);
+    const int base = chunk_base(me, n_chunks(me, p.cmax));
+    d.r0 = off + nc * base;
+    d.m = min(base, me - nc * base);
     ok = ok && off >= 0 && me >= 0 && off + me <= p.A && d.m > 0;
     if (!ok) {  // inconsistent offsets or tile entry: load in-range rows, store nothing
         d.m = 0;
@@ -116,6 +120,10 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                  const __grid_constant__ CUtensorMap tm_h, const Params p) {
     constexpr int kBBytes = Cfg<BCap, kStages>::kBBytes;
     constexpr int kStageBytes = Cfg<BCap, kStages>::kStageBytes;
+    // TMEM: gate accumulators at column 0, up at kUpCol, of one of kNBuf buffers
+    constexpr int kUpCol = BCap > 128 ? 256 : 128;
+    constexpr int kBufCols = 2 * kUpCol;
+    constexpr int kNBuf = kTmemCols / kBufCols;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ctrl = smem + kStages * kStageBytes;
@@ -192,7 +200,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             if (d.down == kDown) {
                 // the expert's h must be complete: every epilogue warp of every gate/up tile
                 const int me = __ldg(p.offsets + d.e + 1) - __ldg(p.offsets + d.e);
-                const int need = (p.I / kRows) * ((me + kMaxN - 1) / kMaxN) * kEpiWarps;
+                const int need = (p.I / kRows) * n_chunks(me, p.cmax) * kEpiWarps;
                 long long n = 0;
                 for (;;) {
                     int v;
@@ -278,9 +286,9 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const int *sm = smeta + 4 * stage;
             const int down = (sm[0] & 3) != kGateUp, two = sm[0] >> 2, ks = sm[1], nslab = sm[2], N = sm[3];
             if (ks < 0 || *abort) break;
-            const int b = tile_count & 1;
+            const int b = tile_count % kNBuf;
             if (ks == 0) {
-                mbar_wait(smem_u32(&acce[b]), ((tile_count >> 1) & 1) ^ 1, p.err, abort);
+                mbar_wait(smem_u32(&acce[b]), ((tile_count / kNBuf) & 1) ^ 1, p.err, abort);
                 tc_fence_after();
             }
             const uint32_t d = tmem_base + uint32_t(b * kBufCols);
@@ -327,8 +335,8 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             if (lane == 0) mbar_arrive(smem_u32(&tme[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
             if (down < 0 || *abort) break;
-            const int b = tile_count & 1;
-            mbar_wait(smem_u32(&accf[b]), (tile_count >> 1) & 1, p.err, abort);
+            const int b = tile_count % kNBuf;
+            mbar_wait(smem_u32(&accf[b]), (tile_count / kNBuf) & 1, p.err, abort);
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(b * kBufCols);
             const size_t col = (size_t)rb * kRows + row;
@@ -416,8 +424,8 @@ __device__ int scan256(int v, int *s_warp, int &total) {
 // and clears the scheduling counters of the tensor-core kernel.
 __global__ void __launch_bounds__(256)
 prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
-            int T, int k, int H, int I, int E, uint16_t *__restrict__ x_perm, uint32_t *tiles, int max_tiles,
-            int *n_tiles, int *tile_counter, int *done, int32_t *err) {
+            int T, int k, int H, int I, int E, int cmax, uint16_t *__restrict__ x_perm, uint32_t *tiles,
+            int max_tiles, int *n_tiles, int *tile_counter, int *done, int32_t *err) {
     griddep_launch_dependents();
     griddep_wait();
     if (blockIdx.x > 0) {
@@ -440,7 +448,7 @@ prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, c
         me = min(max(offsets[e + 1] - offsets[e], 0), T * k);
         done[e] = 0;
     }
-    const int nch = me > 0 ? (me + kMaxN - 1) / kMaxN : 0;
+    const int nch = n_chunks(me, cmax);
     const int gu_per = I / kRows, dn_per = H / kRows;
     int n_gu, n_dn;
     const int gu_off = scan256(nch * gu_per, s_warp, n_gu);
@@ -556,8 +564,10 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
         !tc::make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
 
+    // batches above 64 tokens take 256-token tiles (twice the MMA work per weight byte)
+    const int cmax = s.T > 64 ? 256 : kMaxN;
     cudaError_t e = launch_pdl(prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
-                               offsets, s.T, s.k, s.H, s.I, s.E, x_perm, tiles, (int)max_tiles(s), n_tiles,
+                               offsets, s.T, s.k, s.H, s.I, s.E, cmax, x_perm, tiles, (int)max_tiles(s), n_tiles,
                                tile_counter, done, err);
     if (e != cudaSuccess) return e;
 
@@ -574,11 +584,12 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.H = s.H;
     prm.I = s.I;
     prm.A = A;
-    // every expert has at most T tokens: small batches take the deeper pipelines
+    prm.cmax = cmax;
+    // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (s.T <= 32) return launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, prm);
-    if (s.T <= 64) return launch_tc<64, 5>(grid, st, mg, mu, md, mx, mh, prm);
-    return launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, prm);
+    if (s.T <= 64) return launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, prm);
+    return launch_tc<256, 3>(grid, st, mg, mu, md, mx, mh, prm);
 }
 
 }  // namespace moe
