@@ -50,7 +50,8 @@ constexpr int kMetaRing = 8;
 constexpr int kCtrlBytes = 1024;
 // Pipeline shape: token rows held per stage (BCap, a bound on N) and stage count.  Small
 // batches need little room for token rows, so they get more stages (more weight bytes in
-// flight); large batches take 256-token tiles.
+// flight).  (256-token tiles with a single TMEM buffer and 3 stages measured slower
+// at prefill than 128-token tiles with double buffering and 4 stages.)
 template <int BCap, int Stages>
 struct Cfg {
     static constexpr int kBBytes = BCap * 128;
@@ -564,8 +565,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
         !tc::make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
 
-    // batches above 64 tokens take 256-token tiles (twice the MMA work per weight byte)
-    const int cmax = s.T > 64 ? 256 : kMaxN;
+    const int cmax = kMaxN;
     cudaError_t e = launch_pdl(prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
                                offsets, s.T, s.k, s.H, s.I, s.E, cmax, x_perm, tiles, (int)max_tiles(s), n_tiles,
                                tile_counter, done, err);
@@ -588,8 +588,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (s.T <= 32) return launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, prm);
-    if (s.T <= 64) return launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, prm);
-    return launch_tc<256, 3>(grid, st, mg, mu, md, mx, mh, prm);
+    return launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, prm);
 }
 
 }  // namespace moe
