@@ -107,7 +107,7 @@ typedef struct {
 /*
  * Workspace bytes the entry points below need for this shape (host only, no
  * CUDA call).  The same workspace serves every entry point; it must be
- * 256-byte aligned.  Its first 256 bytes hold the device error word and
+ * 256-byte aligned.  Its first 2048 bytes hold the device error word and
  * scheduling counters and must be zeroed once before first use; the kernels
  * leave the counters at zero again (moe_read_device_error clears the error
  * word).  Returns MOE_ERR_NULLPTR / MOE_ERR_SHAPE / MOE_ERR_DTYPE on bad
@@ -208,7 +208,7 @@ MOE_API int moe_forward(const moe_shape *shape, const void *x, const void *w_rou
  *     (with that device current); make that first call outside any stream
  *     capture.
  *   - Every call shares the one array and leaves its contents behind; each call
- *     clears the error word itself.  Calls whose executions overlap on the GPU
+ *     clears the array's 2 KB header (error word and counters) itself.  Calls whose executions overlap on the GPU
  *     (different streams, or graphs replayed concurrently) race on the array:
  *     serialise them.
  */

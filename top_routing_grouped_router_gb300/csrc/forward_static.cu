@@ -61,8 +61,9 @@ extern "C" int moe_forward_static_scratch(const moe_shape *shape, const void *x,
     void *scratch = nullptr;
     const int ra = scratch_address(&scratch);
     if (ra != MOE_OK) return ra;
-    // the array keeps the previous call's contents: the error word must start at zero
-    if (cudaMemsetAsync(scratch, 0, 256, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // the array keeps the previous call's contents: the header (error word and scheduling
+    // counters) must start at zero
+    if (cudaMemsetAsync(scratch, 0, moe::kHdrBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MOE_ERR_LAUNCH;
     return moe_forward(shape, x, w_router, b_router, w_gate, w_up, w_down, q4, out, expert_ids_out, weights_out,
                        scratch, kStaticScratchBytes, stream);

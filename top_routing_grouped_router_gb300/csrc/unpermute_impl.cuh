@@ -1,0 +1,57 @@
+// unpermute_impl.cuh -- the weighted un-permute of 8 consecutive output columns of one
+// token (the index_add_ step of the grouped_mm MoE path, as a gather): out[t, c..c+7] =
+// sum_{j<k} w[t, j] * y[pos[t*k + j], c..c+7], summed in slot order in fp32 and rounded
+// once.  Shared by the standalone kernel and the tail of the fused tensor-core kernel so
+// that both give bit-identical results.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ void unp_load8(const float *p, float *v) {
+    const float4 a = __ldcg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldcg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void unp_load8(const uint16_t *p, float *v) {
+    const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void unp_store8(float *p, const float *v) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void unp_store8(uint16_t *p, const float *v) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = uint32_t(f32_to_bf16_bits(v[2 * i])) | (uint32_t(f32_to_bf16_bits(v[2 * i + 1])) << 16);
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Columns [c0, c0 + 8) of token t.  A slot whose pos is outside [0, A) contributes nothing.
+template <typename T>
+__device__ __forceinline__ void unpermute8(const T *y, const float *w, const int32_t *pos, T *out, int t, int c0,
+                                           int k, int H, int A) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+        const int p = __ldg(pos + (size_t)t * k + j);
+        if (p < 0 || p >= A) continue;
+        const float wt = __ldg(w + (size_t)t * k + j);
+        float v[8];
+        unp_load8(y + (size_t)p * H + c0, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wt, v[i], acc[i]);
+    }
+    unp_store8(out + (size_t)t * H + c0, acc);
+}
+
+}  // namespace moe
