@@ -23,7 +23,8 @@
 // warps 2-5 are the epilogue (warp w reads TMEM lanes 32*(w%4)..+31), with two
 // accumulator buffers so the epilogue of one tile overlaps the MMAs of the next.
 //
-// Phases of one launch, all in this kernel: (1) the epilogue warps of all CTAs copy the
+// Phases of one launch (batches up to 64 tokens; larger ones gather in a separate
+// launch and un-permute in unpermute.cu): (1) the epilogue warps of all CTAs copy the
 // token rows into permuted order (x_perm, rows claimed with an atomic counter; TMA of
 // token rows waits until all rows are in); (2) the tiles; (3) with an output given, the
 // weighted un-permute of unpermute_impl.cuh once every tile is done (tokens claimed with
@@ -74,8 +75,11 @@ struct Cfg {
 // 128-expert x 64-token tile per CTA.
 enum : int { kGateUp = 0, kDown = 1, kRouter = 2 };
 
-// Scheduling counters in the workspace header (zero between launches).
+// Scheduling counters in the workspace header (zero between launches), one 128-byte line
+// each so that polling one does not slow the atomics on another.
 enum : int { kCtrTile = 0, kCtrRowClaim, kCtrRowsDone, kCtrEpiDone, kCtrOutClaim, kCtrExit, kCtrCount };
+constexpr int kCtrStride = 32;  // ints
+constexpr int kGatherRows = 4;  // rows per gather claim
 
 struct Params {
     const int32_t *offsets;     // [E+1]
@@ -93,6 +97,7 @@ struct Params {
     const int32_t *pos;
     int E, H, I, A, k;
     int cmax;                   // largest token chunk
+    int gathered;               // x_perm already written by a separate gather launch
     // router mode: tiles are (row block of experts, 64-token chunk), one static sweep
     int router_tiles;           // > 0 selects router mode
     int T;
@@ -275,15 +280,15 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             mbar_wait(smem_u32(tables_ready), 0, p.err, abort);
             n_tiles = s_gu[p.E] + s_dn[p.E];
         }
-        bool rows_ready = router;
+        bool rows_ready = router || p.gathered;
         int stage = 0, slot = 0;
         uint32_t phase = 0, mphase = 0;
-        int next = router ? int(blockIdx.x) : atomicAdd(p.ctr + kCtrTile, 1);
+        int next = router ? int(blockIdx.x) : atomicAdd(p.ctr + kCtrTile * kCtrStride, 1);
         for (;;) {
             const int t = next;
             if (t >= n_tiles || *abort) break;
             // claim ahead: the atomic's latency hides behind this tile
-            next = router ? t + int(gridDim.x) : atomicAdd(p.ctr + kCtrTile, 1);
+            next = router ? t + int(gridDim.x) : atomicAdd(p.ctr + kCtrTile * kCtrStride, 1);
             bool ok = true;
             TileInfo d;
             if (router) {
@@ -350,7 +355,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 }
                 if (d.down == kGateUp && !rows_ready) {
                     // token rows come from x_perm, which the CTAs' epilogue warps fill first
-                    wait_counter(p.ctr + kCtrRowsDone, p.A, p.err, abort);
+                    wait_counter(p.ctr + kCtrRowsDone * kCtrStride, p.A, p.err, abort);
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     rows_ready = true;
                 }
@@ -421,31 +426,34 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         // ------------------------------------------------ epilogue warps
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         const int row = 32 * q + lane;
-        if (!router) {
-            // phase 1: token rows into permuted order, claimed row by row across all CTAs
+        if (!router && !p.gathered) {
+            // phase 1: token rows into permuted order, claimed a few rows at a time across
+            // all CTAs
             int copied = 0;
             for (;;) {
-                int pr = 0;
-                if (lane == 0) pr = atomicAdd(p.ctr + kCtrRowClaim, 1);
-                pr = __shfl_sync(0xffffffffu, pr, 0);
-                if (pr >= p.A) break;
-                const int a = __ldg(p.order + pr);
-                uint4 *dst = reinterpret_cast<uint4 *>(p.x_perm + (size_t)pr * p.H);
-                if (a < 0 || a >= p.A) {
-                    if (lane == 0) record_error(p.err, MOE_ERR_DEVICE);
-                    for (int i = lane; i < p.H / 8; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
-                } else {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)(a / p.k) * p.H);
-                    for (int i = lane; i < p.H / 8; i += 32) dst[i] = __ldg(src + i);
+                int c0 = 0;
+                if (lane == 0) c0 = atomicAdd(p.ctr + kCtrRowClaim * kCtrStride, kGatherRows);
+                c0 = __shfl_sync(0xffffffffu, c0, 0);
+                if (c0 >= p.A) break;
+                for (int pr = c0; pr < min(c0 + kGatherRows, p.A); ++pr) {
+                    const int a = __ldg(p.order + pr);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.x_perm + (size_t)pr * p.H);
+                    if (a < 0 || a >= p.A) {
+                        if (lane == 0) record_error(p.err, MOE_ERR_DEVICE);
+                        for (int i = lane; i < p.H / 8; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+                    } else {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)(a / p.k) * p.H);
+                        for (int i = lane; i < p.H / 8; i += 32) dst[i] = __ldg(src + i);
+                    }
+                    ++copied;
                 }
-                ++copied;
             }
             // publish (the rows are read back through TMA)
             asm volatile("fence.proxy.async.global;" ::: "memory");
             __syncwarp();
             if (lane == 0 && copied) {
                 __threadfence();
-                release_add(p.ctr + kCtrRowsDone, copied);
+                release_add(p.ctr + kCtrRowsDone * kCtrStride, copied);
             }
         }
         // phase 2: tile epilogues
@@ -500,20 +508,23 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 if (lane == 0) {
                     __threadfence();
                     if (down == kGateUp) release_add(p.done + e, 1);
-                    release_add(p.ctr + kCtrEpiDone, 1);
+                    release_add(p.ctr + kCtrEpiDone * kCtrStride, 1);
                 }
             }
             ++tile_count;
         }
         // phase 3: weighted un-permute once every tile of every CTA is done
         if (!router && p.out) {
-            wait_counter(p.ctr + kCtrEpiDone, (s_gu[p.E] + s_dn[p.E]) * kEpiWarps, p.err, abort);
             const int tid = (warp - 2) * 32 + lane;  // 0..127
+            // one poller per CTA; the other epilogue threads wait at the named barrier
+            if (tid == 0)
+                wait_counter(p.ctr + kCtrEpiDone * kCtrStride, (s_gu[p.E] + s_dn[p.E]) * kEpiWarps, p.err, abort);
+            asm volatile("bar.sync 1, 128;" ::: "memory");
             const int per_token = p.H / 8;            // 8-column groups of one token row
             const int T = p.A / p.k;
             for (;;) {
                 // the four epilogue warps share one claim per token
-                if (tid == 0) *s_claim = atomicAdd(p.ctr + kCtrOutClaim, 1);
+                if (tid == 0) *s_claim = atomicAdd(p.ctr + kCtrOutClaim * kCtrStride, 1);
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 const int t = *s_claim;
                 asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -534,14 +545,35 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     if (!router && threadIdx.x == 0) {
         // the last CTA out clears the counters for the next launch
         __threadfence();
-        if (atomicAdd(p.ctr + kCtrExit, 1) == int(gridDim.x) - 1) {
+        if (atomicAdd(p.ctr + kCtrExit * kCtrStride, 1) == int(gridDim.x) - 1) {
             __threadfence();
             for (int e = 0; e < p.E; ++e) p.done[e] = 0;
-            for (int c = 0; c < kCtrCount; ++c) p.ctr[c] = 0;
+            for (int c = 0; c < kCtrCount; ++c) p.ctr[c * kCtrStride] = 0;
             __threadfence();
         }
     }
 }
+
+// x_perm[p] = x[order[p] / k], one block per row: the gather for large batches, where a
+// separate fully parallel launch beats claiming rows inside the persistent kernel.
+__global__ void __launch_bounds__(256)
+gather_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, int A, int k, int H,
+              uint16_t *__restrict__ x_perm, int32_t *err) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int pr = blockIdx.x;
+    const int a = __ldg(order + pr);
+    uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
+    if (a < 0 || a >= A) {
+        if (threadIdx.x == 0) record_error(err, MOE_ERR_DEVICE);
+        for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(a / k) * H);
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+}
+
+constexpr int kFuseMaxT = 64;  // batches up to this size gather and un-permute inside the kernel
 
 template <int BCap, int Stages>
 bool set_smem_attr() {
@@ -610,9 +642,9 @@ size_t grouped_fast_part_bytes(int path, const moe_shape &s) {
     return xperm_bytes(s);
 }
 
-int grouped_fast_launches(int path, const moe_shape &) { return path == 1 ? 1 : path == 2 ? 2 : 0; }
+int grouped_fast_launches(int path, const moe_shape &s) { return path == 1 ? (s.T <= kFuseMaxT ? 1 : 2) : path == 2 ? 2 : 0; }
 
-bool grouped_fuses_unpermute(int path) { return path == 1; }
+bool grouped_fuses_unpermute(int path, const moe_shape &s) { return path == 1 && s.T <= kFuseMaxT; }
 
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
@@ -649,6 +681,12 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.A = A;
     prm.k = s.k;
     prm.cmax = kMaxN;
+    if (s.T > kFuseMaxT) {
+        prm.gathered = 1;
+        const cudaError_t e = launch_pdl(gather_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(x),
+                                         order, A, s.k, s.H, x_perm, err);
+        if (e != cudaSuccess) return e;
+    }
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (s.T <= 32) return launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, prm);

@@ -14,7 +14,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
                                 const moe_q4 *q4, float *part, void *h, void *y, int32_t *err, void *hdr,
                                 const float *w, const int32_t *pos, void *out, cudaStream_t st);
-bool grouped_fuses_unpermute(int path);
+bool grouped_fuses_unpermute(int path, const moe_shape &s);
 size_t grouped_fast_part_bytes(int path, const moe_shape &s);
 int grouped_fast_launches(int path, const moe_shape &s);
 int route_launches(const moe_shape &s);
@@ -133,7 +133,7 @@ int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const 
                const float *w = nullptr, const int32_t *pos = nullptr, void *out = nullptr, bool *fused = nullptr) {
     const WsLayout L = ws_layout(s);
     const int path = grouped_path(s, q4);
-    const bool fuse = out && grouped_fuses_unpermute(path);
+    const bool fuse = out && grouped_fuses_unpermute(path, s);
     if (fused) *fused = fuse;
     if (path > 0)
         return launch_rc(launch_grouped_fast(path, s, x, offsets, order, wg, wu, wd, q4, at<float>(ws, L.part),
@@ -239,7 +239,7 @@ int moe_forward_launches(const moe_shape *shape, int32_t *launches) {
     const int path = select_grouped_path(s);  // a non-affine 4-bit codebook takes path 0 (also 2 launches)
     *launches = (route_fuses(s) ? 1 : route_launches(s) + permute_launches(s)) +
                 (path > 0 ? grouped_fast_launches(path, s) : grouped_simple_launches(s)) +
-                (grouped_fuses_unpermute(path) ? 0 : 1);
+                (grouped_fuses_unpermute(path, s) ? 0 : 1);
     return MOE_OK;
 }
 

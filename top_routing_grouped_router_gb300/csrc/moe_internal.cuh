@@ -92,7 +92,8 @@ __device__ __forceinline__ void record_error(int32_t *err, int code) { atomicCAS
 
 // Workspace header (zeroed once by the caller, kept at zero between launches by the
 // kernels): error word at byte 0, router arrival counters at bytes 64..127, grouped-kernel
-// scheduling counters at 128..191, per-expert completion counters at 1024..2047.
+// scheduling counters at 128..895 (one 128-byte line each), per-expert completion counters
+// at 1024..2047.
 constexpr size_t kHdrBytes = 2048;
 constexpr size_t kHdrArrivals = 64;
 constexpr size_t kHdrGrouped = 128;
