@@ -27,8 +27,8 @@
 // launch and un-permute in unpermute.cu): (1) the epilogue warps of all CTAs copy the
 // token rows into permuted order (x_perm, rows claimed with an atomic counter; TMA of
 // token rows waits until all rows are in); (2) the tiles; (3) with an output given, the
-// weighted un-permute of unpermute_impl.cuh once every tile is done (tokens claimed with
-// an atomic counter).  The scheduling counters live in the zeroed workspace header; the
+// weighted un-permute of unpermute_impl.cuh once every down tile is done (tokens claimed
+// with an atomic counter).  The scheduling counters live in the zeroed workspace header; the
 // last CTA to leave clears them for the next launch.  Every cross-CTA wait is bounded.
 #include "moe_internal.cuh"
 #include "tc_common.cuh"
@@ -500,14 +500,19 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&acce[b]));
-            if (down != kRouter) {
-                // publish this warp's rows: h is read back through TMA by down tiles, y by the
-                // un-permute phase
+            if (down == kGateUp) {
+                // publish this warp's h rows (read back through TMA by down tiles)
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
                     __threadfence();
-                    if (down == kGateUp) release_add(p.done + e, 1);
+                    release_add(p.done + e, 1);
+                }
+            } else if (down == kDown && p.out) {
+                // publish this warp's y rows for the fused un-permute
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
                     release_add(p.ctr + kCtrEpiDone * kCtrStride, 1);
                 }
             }
@@ -518,7 +523,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const int tid = (warp - 2) * 32 + lane;  // 0..127
             // one poller per CTA; the other epilogue threads wait at the named barrier
             if (tid == 0)
-                wait_counter(p.ctr + kCtrEpiDone * kCtrStride, (s_gu[p.E] + s_dn[p.E]) * kEpiWarps, p.err, abort);
+                wait_counter(p.ctr + kCtrEpiDone * kCtrStride, s_dn[p.E] * kEpiWarps, p.err, abort);
             asm volatile("bar.sync 1, 128;" ::: "memory");
             const int per_token = p.H / 8;            // 8-column groups of one token row
             const int T = p.A / p.k;
