@@ -8,14 +8,13 @@
 // the weight stream alone.  Both operands are K-major, loaded by TMA as 64-element
 // (128-byte) slabs with the 128-byte swizzle.
 //
-// Tiles: gate/up tile = (expert e, 128 rows of I, token chunk): two MMAs per k-step,
-// gate into TMEM columns [0, N) and up into [128, 128+N), so one epilogue thread (TMEM
-// lane = weight row) holds g and u of the same row and forms SiLU(g)*u in registers.
-// Down tile = (e, 128 rows of H, token chunk) over the expert's h rows.  All gate/up
-// tiles precede all down tiles in one tile sequence that CTAs claim with an atomic
-// counter; a down tile waits (bounded) until every epilogue warp of every gate/up tile of
-// its expert has published h.  Every CTA derives the tile sequence from the expert
-// offsets itself (prefix sums in shared memory), so no tile list is written.
+// Tiles: gate/up tile = (expert e, 128 rows of I, 128-token chunk): two MMAs per
+// k-step, gate into TMEM columns [0, N) and up into [128, 128+N), so one epilogue
+// thread (TMEM lane = weight row) holds g and u of the same row and forms
+// SiLU(g)*u in registers.  Down tile = (e, 128 rows of H, token chunk) over the
+// expert's h rows.  All gate/up tiles precede all down tiles in one list that CTAs
+// claim with an atomic counter; a down tile waits (bounded) until every epilogue warp
+// of every gate/up tile of its expert has published h.
 //
 // Roles per CTA (one CTA per SM): warp 0 lane 0 issues TMA loads into a 4-6 stage ring;
 // warp 1 owns the TMEM allocation and lane 0 issues the MMAs (tcgen05.commit frees a
@@ -23,16 +22,10 @@
 // warps 2-5 are the epilogue (warp w reads TMEM lanes 32*(w%4)..+31), with two
 // accumulator buffers so the epilogue of one tile overlaps the MMAs of the next.
 //
-// Phases of one launch (batches up to 64 tokens; larger ones gather in a separate
-// launch and un-permute in unpermute.cu): (1) the epilogue warps of all CTAs copy the
-// token rows into permuted order (x_perm, rows claimed with an atomic counter; TMA of
-// token rows waits until all rows are in); (2) the tiles; (3) with an output given, the
-// weighted un-permute of unpermute_impl.cuh once every down tile is done (tokens claimed
-// with an atomic counter).  The scheduling counters live in the zeroed workspace header; the
-// last CTA to leave clears them for the next launch.  Every cross-CTA wait is bounded.
+// The token rows are first gathered into permuted order (x_perm) so that every
+// expert's rows are contiguous for TMA; the same prep kernel builds the tile list.
 #include "moe_internal.cuh"
 #include "tc_common.cuh"
-#include "unpermute_impl.cuh"
 
 #include <algorithm>
 
@@ -47,58 +40,51 @@ constexpr int kSlab = 64;                  // k elements per stage (one 128-byte
 constexpr int kNBox = 16;                  // token rows per activation TMA box
 constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
 constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
+// Token chunks: an expert's m tokens are cut into ceil(m / cmax) chunks of cmax tokens,
+// the last one ragged; a single chunk is rounded up to a multiple of 16 (the MMA's N
+// granule).  Full 128-token chunks measured faster than an even split of m.
+__host__ __device__ inline int n_chunks(int me, int cmax) { return me > 0 ? (me + cmax - 1) / cmax : 0; }
+__host__ __device__ inline int chunk_base(int me, int nch, int cmax) {
+    return nch > 1 ? cmax : (nch ? ((me + 15) & ~15) : 0);
+}
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kMetaRing = 8;
 constexpr int kCtrlBytes = 1024;
-constexpr int kTableBytes = 2 * (kMaxE + 1) * 4;
-constexpr int kRouterN = 64;               // tokens per router tile: twice the tiles, two k-slabs per stage
-
-// Token chunks: an expert's m tokens are cut into ceil(m / cmax) nearly equal chunks
-// (multiples of 16).
-__host__ __device__ inline int n_chunks(int me, int cmax) { return me > 0 ? (me + cmax - 1) / cmax : 0; }
-__host__ __device__ inline int chunk_base(int me, int nch) { return nch > 0 ? (((me + nch - 1) / nch) + 15) & ~15 : 0; }
-
 // Pipeline shape: token rows held per stage (BCap, a bound on N) and stage count.  Small
 // batches need little room for token rows, so they get more stages (more weight bytes in
-// flight).  (256-token tiles with a single TMEM buffer and 3 stages measured slower at
-// prefill than 128-token tiles with double buffering and 4 stages.)
+// flight).  (256-token tiles with a single TMEM buffer and 3 stages measured slower
+// at prefill than 128-token tiles with double buffering and 4 stages.)
 template <int BCap, int Stages>
 struct Cfg {
     static constexpr int kBBytes = BCap * 128;
     static constexpr int kStageBytes = 2 * kABytes + kBBytes;
-    static constexpr int kSmemBytes = Stages * kStageBytes + 1024 /*alignment*/ + kCtrlBytes + kTableBytes;
+    static constexpr int kSmemBytes = Stages * kStageBytes + 1024 /*alignment*/ + kCtrlBytes;
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
+constexpr int kRouterN = 64;               // tokens per router tile: twice the tiles, two k-slabs per stage
+
+// Tile list entry: bit 31 = down tile, bits 16-23 expert, bits 8-15 row block, bits 0-7 token chunk.
+__host__ __device__ constexpr uint32_t pack_tile(int down, int e, int rb, int nc) {
+    return (uint32_t(down) << 31) | (uint32_t(e) << 16) | (uint32_t(rb) << 8) | uint32_t(nc);
+}
 
 // Tile kinds.  The router GEMM (logits[t][e] = x_t . W_r[e]) reuses the kernel as one
-// 128-expert x 64-token tile per CTA.
+// 128-expert x 128-token tile per CTA.
 enum : int { kGateUp = 0, kDown = 1, kRouter = 2 };
-
-// Scheduling counters in the workspace header (zero between launches), one 128-byte line
-// each so that polling one does not slow the atomics on another.
-enum : int { kCtrTile = 0, kCtrRowClaim, kCtrRowsDone, kCtrEpiDone, kCtrOutClaim, kCtrExit, kCtrCount };
-constexpr int kCtrStride = 32;  // ints
-constexpr int kGatherRows = 4;  // rows per gather claim
 
 struct Params {
     const int32_t *offsets;     // [E+1]
-    const int32_t *order;       // [A]
-    const uint16_t *x;          // [T][H] tokens
-    uint16_t *x_perm;           // [A][H] tokens in permuted order (written here)
-    int *ctr;                   // kCtrCount scheduling counters
+    const uint32_t *tiles;      // tile list
+    const int *n_tiles;         // its length
+    int *tile_counter;
     int *done;                  // [E] published gate/up tiles (per epilogue warp)
     int32_t *err;
     uint16_t *h;                // [A][I] bf16
     uint16_t *y;                // [A][H] bf16
-    // fused un-permute (moe_forward): out[t] = sum_j w[t][j] * y[pos[t*k+j]]; out null = none
-    uint16_t *out;
-    const float *w;
-    const int32_t *pos;
-    int E, H, I, A, k;
-    int cmax;                   // largest token chunk
-    int gathered;               // x_perm already written by a separate gather launch
-    // router mode: tiles are (row block of experts, 64-token chunk), one static sweep
+    int E, H, I, A;
+    int cmax;                   // largest token chunk of the tile list
+    // router mode: tiles are (row block of experts, 128-token chunk), one static sweep
     int router_tiles;           // > 0 selects router mode
     int T;
     float *logits;              // [T][E]
@@ -109,61 +95,26 @@ struct TileInfo {
     int down, e, rb, r0, m, N;
 };
 
-// Largest e with tab[e] <= t, for a nondecreasing tab[0..E].
-__device__ __forceinline__ int find_expert(const int *tab, int E, int t) {
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tab[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
-
-// Tile t of the sequence: gate/up tiles of experts 0..E-1 (chunk-major, row block fastest),
-// then their down tiles.  gu/dn: exclusive prefix sums of the tiles per expert.
-__device__ TileInfo decode_tile(int t, const int *gu, const int *dn, const Params &p, bool &ok) {
+__device__ __forceinline__ TileInfo read_tile(uint32_t entry, const Params &p, bool &ok) {
     TileInfo d;
-    const int n_gu = gu[p.E];
-    d.down = t >= n_gu;
-    const int *tab = d.down ? dn : gu;
-    const int r = d.down ? t - n_gu : t;
-    const int per = (d.down ? p.H : p.I) / kRows;
-    d.e = find_expert(tab, p.E, r);
-    const int q = r - tab[d.e];
-    const int nc = q / per;
-    d.rb = q % per;
-    const int off = __ldg(p.offsets + d.e);
-    const int me = __ldg(p.offsets + d.e + 1) - off;
-    const int base = chunk_base(me, n_chunks(me, p.cmax));
+    d.down = int(entry >> 31);
+    d.e = int((entry >> 16) & 0xFF);
+    d.rb = int((entry >> 8) & 0xFF);
+    const int nc = int(entry & 0xFF);
+    ok = d.e < p.E;
+    const int off = ok ? __ldg(p.offsets + d.e) : 0;
+    const int me = ok ? __ldg(p.offsets + d.e + 1) - off : 0;
+    const int base = chunk_base(me, n_chunks(me, p.cmax), p.cmax);
     d.r0 = off + nc * base;
     d.m = min(base, me - nc * base);
-    ok = off >= 0 && me >= 0 && off + me <= p.A && d.m > 0;
-    if (!ok) {  // inconsistent offsets: load in-range rows, store nothing
+    ok = ok && off >= 0 && me >= 0 && off + me <= p.A && d.m > 0;
+    if (!ok) {  // inconsistent offsets or tile entry: load in-range rows, store nothing
         d.m = 0;
         d.r0 = 0;
+        d.e = min(d.e, p.E - 1);
     }
     d.N = d.m > 0 ? (d.m + 15) & ~15 : 16;
     return d;
-}
-
-// Bounded wait until *addr >= target (acquire); records the error and raises abort on timeout.
-__device__ __forceinline__ void wait_counter(const int *addr, int target, int32_t *err, volatile int *abort) {
-    long long n = 0;
-    for (;;) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
-        if (v >= target || *abort) return;
-        if (++n > kSpinLimit) {
-            record_error(err, MOE_ERR_DEVICE);
-            *abort = 1;
-            return;
-        }
-        __nanosleep(64);
-    }
-}
-
-__device__ __forceinline__ void release_add(int *addr, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
 }
 
 template <int BCap, int kStages>
@@ -187,17 +138,12 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     uint64_t *tmf = acce + 2;                                      // [kMetaRing]
     uint64_t *tme = tmf + kMetaRing;                               // [kMetaRing]
     uint64_t *drain = tme + kMetaRing;                             // [1]
-    uint64_t *tables_ready = drain + 1;                            // [1]
-    int *smeta = reinterpret_cast<int *>(tables_ready + 1);        // [kStages][4]: kind|two<<2, ks, nstage, N
+    int *smeta = reinterpret_cast<int *>(drain + 1);               // [kStages][4]: down|two<<1, ks, nstage, N
     int *tmeta = smeta + 4 * kStages;                              // [kMetaRing][8]
     volatile int *abort = tmeta + 8 * kMetaRing;
-    int *s_claim = tmeta + 8 * kMetaRing + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmeta + 8 * kMetaRing + 4);
-    int *s_gu = reinterpret_cast<int *>(ctrl + kCtrlBytes);       // [kMaxE + 1] gate/up tile prefix
-    int *s_dn = s_gu + kMaxE + 1;                                  // [kMaxE + 1] down tile prefix
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool router = p.router_tiles > 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
@@ -212,7 +158,6 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             mbar_init(smem_u32(&tme[s]), kEpiWarps);
         }
         mbar_init(smem_u32(drain), 1);
-        mbar_init(smem_u32(tables_ready), 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -229,66 +174,20 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     griddep_launch_dependents();
     griddep_wait();
     const uint32_t tmem_base = *tmem_slot;
+    const bool router = p.router_tiles > 0;
+    const int n_tiles = router ? p.router_tiles : *p.n_tiles;
     const int erb = (p.E + kRows - 1) / kRows;  // expert row blocks in router mode
-
-    if (warp == 2 && !router) {
-        // tile sequence: per expert ceil(m / cmax) chunks x row blocks, exclusive prefix sums
-        constexpr int kPer = kMaxE / 32;
-        const int gper = p.I / kRows, dper = p.H / kRows;
-        int gsum[kPer], dsum[kPer];
-        int gl = 0, dl = 0;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            const int e = lane * kPer + i;
-            int me = 0;
-            if (e < p.E) me = min(max(__ldg(p.offsets + e + 1) - __ldg(p.offsets + e), 0), p.A);
-            const int nch = n_chunks(me, p.cmax);
-            gsum[i] = gl;
-            dsum[i] = dl;
-            gl += nch * gper;
-            dl += nch * dper;
-        }
-        int gi = gl, di = dl;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int a = __shfl_up_sync(0xffffffffu, gi, o), b = __shfl_up_sync(0xffffffffu, di, o);
-            if (lane >= o) { gi += a; di += b; }
-        }
-        const int gex = gi - gl, dex = di - dl;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            const int e = lane * kPer + i;
-            if (e <= p.E) {
-                s_gu[e] = gex + gsum[i];
-                s_dn[e] = dex + dsum[i];
-            }
-        }
-        if (lane == 31 && p.E == kMaxE) {
-            s_gu[kMaxE] = gi;
-            s_dn[kMaxE] = di;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(tables_ready));
-    }
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
-        int n_tiles;
-        if (router) {
-            n_tiles = p.router_tiles;
-        } else {
-            mbar_wait(smem_u32(tables_ready), 0, p.err, abort);
-            n_tiles = s_gu[p.E] + s_dn[p.E];
-        }
-        bool rows_ready = router || p.gathered;
         int stage = 0, slot = 0;
         uint32_t phase = 0, mphase = 0;
-        int next = router ? int(blockIdx.x) : atomicAdd(p.ctr + kCtrTile * kCtrStride, 1);
+        int next = router ? int(blockIdx.x) : atomicAdd(p.tile_counter, 1);
         for (;;) {
             const int t = next;
             if (t >= n_tiles || *abort) break;
             // claim ahead: the atomic's latency hides behind this tile
-            next = router ? t + int(gridDim.x) : atomicAdd(p.ctr + kCtrTile * kCtrStride, 1);
+            next = router ? t + int(gridDim.x) : atomicAdd(p.tile_counter, 1);
             bool ok = true;
             TileInfo d;
             if (router) {
@@ -299,13 +198,25 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 d.m = min(kRouterN, p.T - d.r0);
                 d.N = (d.m + 15) & ~15;
             } else {
-                d = decode_tile(t, s_gu, s_dn, p, ok);
+                d = read_tile(__ldg(p.tiles + t), p, ok);
             }
             if (!ok) record_error(p.err, MOE_ERR_DEVICE);
             if (d.down == kDown) {
                 // the expert's h must be complete: every epilogue warp of every gate/up tile
                 const int me = __ldg(p.offsets + d.e + 1) - __ldg(p.offsets + d.e);
-                wait_counter(p.done + d.e, (p.I / kRows) * n_chunks(me, p.cmax) * kEpiWarps, p.err, abort);
+                const int need = (p.I / kRows) * n_chunks(me, p.cmax) * kEpiWarps;
+                long long n = 0;
+                for (;;) {
+                    int v;
+                    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p.done + d.e) : "memory");
+                    if (v >= need || *abort) break;
+                    if (++n > kSpinLimit) {
+                        record_error(p.err, MOE_ERR_DEVICE);
+                        *abort = 1;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             // hand the tile to the epilogue
@@ -320,7 +231,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             mbar_arrive(smem_u32(&tmf[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
 
-            // a one-matrix tile (down, router) with at most BCap/2 tokens takes two k-slabs per
+            // a one-matrix tile (down, router) with at most 64 tokens takes two k-slabs per
             // stage (weights in both A regions, token rows in the two halves of B), so every
             // stage carries 32 KB of weights whatever the tile kind
             const int kdim = d.down == kDown ? p.I : p.H;
@@ -344,28 +255,20 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 mbar_arrive_expect_tx(fb, bytes);
                 const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
                 const uint32_t bb = a0 + 2 * kABytes;
-                // weights first: they do not depend on the gather
                 if (two) {
-                    for (int h2 = 0; h2 < 2; ++h2) tma_load_2d(a0 + h2 * kABytes, wmap, (2 * ks + h2) * kSlab, wrow, fb);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int k0 = (2 * ks + h2) * kSlab;
+                        tma_load_2d(a0 + h2 * kABytes, wmap, k0, wrow, fb);
+                        for (int q = 0; q < nbox; ++q)
+                            tma_load_2d(bb + h2 * (kBBytes / 2) + q * 2048, bmap, k0, d.r0 + q * kNBox, fb);
+                    }
                 } else if (d.down != kGateUp) {
                     tma_load_2d(a0, wmap, ks * kSlab, wrow, fb);
+                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * 2048, bmap, ks * kSlab, d.r0 + q * kNBox, fb);
                 } else {
                     tma_load_2d(a0, &tm_gate, ks * kSlab, wrow, fb);
                     tma_load_2d(a0 + kABytes, &tm_up, ks * kSlab, wrow, fb);
-                }
-                if (d.down == kGateUp && !rows_ready) {
-                    // token rows come from x_perm, which the CTAs' epilogue warps fill first
-                    wait_counter(p.ctr + kCtrRowsDone * kCtrStride, p.A, p.err, abort);
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    rows_ready = true;
-                }
-                if (two) {
-                    for (int h2 = 0; h2 < 2; ++h2)
-                        for (int q = 0; q < nbox; ++q)
-                            tma_load_2d(bb + h2 * (kBBytes / 2) + q * 2048, bmap, (2 * ks + h2) * kSlab,
-                                        d.r0 + q * kNBox, fb);
-                } else {
-                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * 2048, bmap, ks * kSlab, d.r0 + q * kNBox, fb);
+                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * 2048, &tm_x, ks * kSlab, d.r0 + q * kNBox, fb);
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
@@ -423,40 +326,9 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         mma_commit(smem_u32(drain));
         mbar_wait(smem_u32(drain), 0, p.err, abort);
     } else if (warp >= 2) {
-        // ------------------------------------------------ epilogue warps
+        // ------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         const int row = 32 * q + lane;
-        if (!router && !p.gathered) {
-            // phase 1: token rows into permuted order, claimed a few rows at a time across
-            // all CTAs
-            int copied = 0;
-            for (;;) {
-                int c0 = 0;
-                if (lane == 0) c0 = atomicAdd(p.ctr + kCtrRowClaim * kCtrStride, kGatherRows);
-                c0 = __shfl_sync(0xffffffffu, c0, 0);
-                if (c0 >= p.A) break;
-                for (int pr = c0; pr < min(c0 + kGatherRows, p.A); ++pr) {
-                    const int a = __ldg(p.order + pr);
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.x_perm + (size_t)pr * p.H);
-                    if (a < 0 || a >= p.A) {
-                        if (lane == 0) record_error(p.err, MOE_ERR_DEVICE);
-                        for (int i = lane; i < p.H / 8; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
-                    } else {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)(a / p.k) * p.H);
-                        for (int i = lane; i < p.H / 8; i += 32) dst[i] = __ldg(src + i);
-                    }
-                    ++copied;
-                }
-            }
-            // publish (the rows are read back through TMA)
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            __syncwarp();
-            if (lane == 0 && copied) {
-                __threadfence();
-                release_add(p.ctr + kCtrRowsDone * kCtrStride, copied);
-            }
-        }
-        // phase 2: tile epilogues
         int slot = 0, tile_count = 0;
         uint32_t mphase = 0;
         for (;;) {
@@ -477,10 +349,10 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     float v[16];
                     tmem_ld16(taddr + c0, v);
                     if (col < (size_t)p.E) {
-                        const float bv = p.bias ? p.bias[col] : 0.f;
+                        const float b = p.bias ? p.bias[col] : 0.f;
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (c0 + j < m) p.logits[(size_t)(r0 + c0 + j) * p.E + col] = v[j] + bv;
+                            if (c0 + j < m) p.logits[(size_t)(r0 + c0 + j) * p.E + col] = v[j] + b;
                     }
                 } else if (down) {
                     float v[16];
@@ -500,42 +372,16 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&acce[b]));
-            if (down == kGateUp) {
+            if (down == kGateUp && e < p.E) {
                 // publish this warp's h rows (read back through TMA by down tiles)
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
                     __threadfence();
-                    release_add(p.done + e, 1);
-                }
-            } else if (down == kDown && p.out) {
-                // publish this warp's y rows for the fused un-permute
-                __syncwarp();
-                if (lane == 0) {
-                    __threadfence();
-                    release_add(p.ctr + kCtrEpiDone * kCtrStride, 1);
+                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done + e) : "memory");
                 }
             }
             ++tile_count;
-        }
-        // phase 3: weighted un-permute once every tile of every CTA is done
-        if (!router && p.out) {
-            const int tid = (warp - 2) * 32 + lane;  // 0..127
-            // one poller per CTA; the other epilogue threads wait at the named barrier
-            if (tid == 0)
-                wait_counter(p.ctr + kCtrEpiDone * kCtrStride, s_dn[p.E] * kEpiWarps, p.err, abort);
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            const int per_token = p.H / 8;            // 8-column groups of one token row
-            const int T = p.A / p.k;
-            for (;;) {
-                // the four epilogue warps share one claim per token
-                if (tid == 0) *s_claim = atomicAdd(p.ctr + kCtrOutClaim * kCtrStride, 1);
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                const int t = *s_claim;
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (t >= T) break;
-                for (int g = tid; g < per_token; g += 128) unpermute8(p.y, p.w, p.pos, p.out, t, g * 8, p.k, p.H, p.A);
-            }
         }
     }
 
@@ -547,38 +393,96 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kTmemCols)
                      : "memory");
     }
-    if (!router && threadIdx.x == 0) {
-        // the last CTA out clears the counters for the next launch
-        __threadfence();
-        if (atomicAdd(p.ctr + kCtrExit * kCtrStride, 1) == int(gridDim.x) - 1) {
-            __threadfence();
-            for (int e = 0; e < p.E; ++e) p.done[e] = 0;
-            for (int c = 0; c < kCtrCount; ++c) p.ctr[c * kCtrStride] = 0;
-            __threadfence();
-        }
-    }
 }
 
-// x_perm[p] = x[order[p] / k], one block per row: the gather for large batches, where a
-// separate fully parallel launch beats claiming rows inside the persistent kernel.
+// Block-wide exclusive scan of one int per thread (blockDim.x == 256).
+__device__ int scan256(int v, int *s_warp, int &total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        const int wv = lane < 8 ? s_warp[lane] : 0;
+        int i2 = wv;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, i2, o);
+            if (lane >= o) i2 += n;
+        }
+        if (lane < 8) s_warp[lane] = i2 - wv;
+        if (lane == 7) s_warp[8] = i2;
+    }
+    __syncthreads();
+    const int excl = s_warp[w] + incl - v;
+    total = s_warp[8];
+    __syncthreads();
+    return excl;
+}
+
+// x_perm[p] = x[order[p] / k].  Block 0 also builds the tile list from the offsets
+// and clears the scheduling counters of the tensor-core kernel.
 __global__ void __launch_bounds__(256)
-gather_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, int A, int k, int H,
-              uint16_t *__restrict__ x_perm, int32_t *err) {
+prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
+            int T, int k, int H, int I, int E, int cmax, uint16_t *__restrict__ x_perm, uint32_t *tiles,
+            int max_tiles, int *n_tiles, int *tile_counter, int *done, int32_t *err) {
     griddep_launch_dependents();
     griddep_wait();
-    const int pr = blockIdx.x;
-    const int a = __ldg(order + pr);
-    uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
-    if (a < 0 || a >= A) {
-        if (threadIdx.x == 0) record_error(err, MOE_ERR_DEVICE);
-        for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+    if (blockIdx.x > 0) {
+        const int pr = blockIdx.x - 1;
+        const int a = __ldg(order + pr);
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
+        if (a < 0 || a >= T * k) {
+            if (threadIdx.x == 0) record_error(err, MOE_ERR_DEVICE);
+            for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+        } else {
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(a / k) * H);
+            for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+        }
         return;
     }
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(a / k) * H);
-    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+    __shared__ int s_warp[9];
+    const int e = threadIdx.x;
+    int me = 0;
+    if (e < E) {
+        me = min(max(offsets[e + 1] - offsets[e], 0), T * k);
+        done[e] = 0;
+    }
+    const int nch = n_chunks(me, cmax);
+    const int gu_per = I / kRows, dn_per = H / kRows;
+    int n_gu, n_dn;
+    const int gu_off = scan256(nch * gu_per, s_warp, n_gu);
+    const int dn_off = scan256(nch * dn_per, s_warp, n_dn);
+    for (int c = 0; c < nch; ++c) {
+        for (int r = 0; r < gu_per; ++r) {
+            const int i = gu_off + c * gu_per + r;
+            if (i < max_tiles) tiles[i] = pack_tile(0, e, r, c);
+        }
+        for (int r = 0; r < dn_per; ++r) {
+            const int i = n_gu + dn_off + c * dn_per + r;
+            if (i < max_tiles) tiles[i] = pack_tile(1, e, r, c);
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (n_gu + n_dn > max_tiles) record_error(err, MOE_ERR_DEVICE);  // inconsistent offsets
+        *n_tiles = min(n_gu + n_dn, max_tiles);
+        *tile_counter = 0;
+    }
 }
 
-constexpr int kFuseMaxT = 64;  // batches up to this size gather and un-permute inside the kernel
+// ---------------------------------------------------------------- host side
+
+constexpr int kMaxT = 8192;
+
+size_t xperm_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * s.H * 2 + 255) / 256 * 256; }
+size_t max_tiles(const moe_shape &s) {
+    const size_t chunks = (size_t)s.E + ((size_t)s.T * s.k + kMaxN - 1) / kMaxN;
+    return chunks * (size_t)(s.I / kRows + s.H / kRows);
+}
 
 template <int BCap, int Stages>
 bool set_smem_attr() {
@@ -601,10 +505,6 @@ cudaError_t launch_tc(dim3 grid, cudaStream_t st, const CUtensorMap &mg, const C
     return launch_pdl(tc_swiglu_kernel<BCap, Stages>, grid, dim3(kThreads), Cfg<BCap, Stages>::kSmemBytes, st, mg, mu,
                       md, mx, mh, prm);
 }
-
-constexpr int kMaxT = 8192;
-
-size_t xperm_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * s.H * 2 + 255) / 256 * 256; }
 
 }  // namespace
 
@@ -644,54 +544,50 @@ int select_grouped_path(const moe_shape &s) {
 size_t grouped_fast_part_bytes(int path, const moe_shape &s) {
     if (path == 2) return q4_part_bytes(s);
     if (path != 1) return 0;
-    return xperm_bytes(s);
+    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (max_tiles(s) * 4 + 255) / 256 * 256;
 }
 
-int grouped_fast_launches(int path, const moe_shape &s) { return path == 1 ? (s.T <= kFuseMaxT ? 1 : 2) : path == 2 ? 2 : 0; }
-
-bool grouped_fuses_unpermute(int path, const moe_shape &s) { return path == 1 && s.T <= kFuseMaxT; }
+int grouped_fast_launches(int path, const moe_shape &) { return path == 1 || path == 2 ? 2 : 0; }
 
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
-                                const moe_q4 *q4, float *part, void *h, void *y, int32_t *err, void *hdr,
-                                const float *w, const int32_t *pos, void *out, cudaStream_t st) {
+                                const moe_q4 *q4, const int32_t *, float *part, void *h, void *y, int32_t *err,
+                                cudaStream_t st) {
     if (path == 2) return launch_q4(s, x, offsets, order, wg, wu, wd, q4, part, h, y, err, st);
     if (path != 1) return cudaErrorInvalidValue;
     const int A = s.T * s.k;
-    uint16_t *x_perm = reinterpret_cast<uint16_t *>(part);
+    char *base = reinterpret_cast<char *>(part);
+    uint16_t *x_perm = reinterpret_cast<uint16_t *>(base);
+    int *sched = reinterpret_cast<int *>(base + xperm_bytes(s));
+    int *tile_counter = sched, *n_tiles = sched + 1, *done = sched + 64;
+    uint32_t *tiles = reinterpret_cast<uint32_t *>(base + xperm_bytes(s) + 256 + (size_t)kMaxE * 4);
 
     CUtensorMap mg, mu, md, mx, mh;
-    if (!tc::make_map(&mg, wg, (uint64_t)s.E * s.I, s.H, kRows) ||
-        !tc::make_map(&mu, wu, (uint64_t)s.E * s.I, s.H, kRows) ||
+    if (!tc::make_map(&mg, wg, (uint64_t)s.E * s.I, s.H, kRows) || !tc::make_map(&mu, wu, (uint64_t)s.E * s.I, s.H, kRows) ||
         !tc::make_map(&md, wd, (uint64_t)s.E * s.H, s.I, kRows) || !tc::make_map(&mx, x_perm, A, s.H, kNBox) ||
         !tc::make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
 
+    const int cmax = kMaxN;
+    cudaError_t e = launch_pdl(prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
+                               offsets, s.T, s.k, s.H, s.I, s.E, cmax, x_perm, tiles, (int)max_tiles(s), n_tiles,
+                               tile_counter, done, err);
+    if (e != cudaSuccess) return e;
+
     Params prm{};
     prm.offsets = offsets;
-    prm.order = order;
-    prm.x = static_cast<const uint16_t *>(x);
-    prm.x_perm = x_perm;
-    prm.ctr = reinterpret_cast<int *>(static_cast<char *>(hdr) + kHdrGrouped);
-    prm.done = reinterpret_cast<int *>(static_cast<char *>(hdr) + kHdrDone);
+    prm.tiles = tiles;
+    prm.n_tiles = n_tiles;
+    prm.tile_counter = tile_counter;
+    prm.done = done;
     prm.err = err;
     prm.h = static_cast<uint16_t *>(h);
     prm.y = static_cast<uint16_t *>(y);
-    prm.out = static_cast<uint16_t *>(out);
-    prm.w = w;
-    prm.pos = pos;
     prm.E = s.E;
     prm.H = s.H;
     prm.I = s.I;
     prm.A = A;
-    prm.k = s.k;
-    prm.cmax = kMaxN;
-    if (s.T > kFuseMaxT) {
-        prm.gathered = 1;
-        const cudaError_t e = launch_pdl(gather_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(x),
-                                         order, A, s.k, s.H, x_perm, err);
-        if (e != cudaSuccess) return e;
-    }
+    prm.cmax = cmax;
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (s.T <= 32) return launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, prm);

@@ -12,9 +12,8 @@ int permute_chunks(int A);
 int select_grouped_path(const moe_shape &s);
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
-                                const moe_q4 *q4, float *part, void *h, void *y, int32_t *err, void *hdr,
-                                const float *w, const int32_t *pos, void *out, cudaStream_t st);
-bool grouped_fuses_unpermute(int path, const moe_shape &s);
+                                const moe_q4 *q4, const int32_t *active, float *part, void *h, void *y,
+                                int32_t *err, cudaStream_t st);
 size_t grouped_fast_part_bytes(int path, const moe_shape &s);
 int grouped_fast_launches(int path, const moe_shape &s);
 int route_launches(const moe_shape &s);
@@ -118,27 +117,17 @@ int do_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t 
                                     at<int32_t>(ws, L.hist), at<int32_t>(ws, L.err), st));
 }
 
-int grouped_path(const moe_shape &s, const moe_q4 *q4) {
+int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order, const void *wg,
+               const void *wu, const void *wd, const moe_q4 *q4, void *y, void *ws, cudaStream_t st) {
+    const WsLayout L = ws_layout(s);
     int path = select_grouped_path(s);
     float cb_b;
     int cb_t2;
     if (path == 2 && !q4_codebook_affine(q4->codebook, &cb_b, &cb_t2)) path = 0;  // generic codebook
-    return path;
-}
-
-// Steps E-F; with `out` given and the tensor-core path, step G is done by the same kernel
-// (returns through *fused whether it was).
-int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order, const void *wg,
-               const void *wu, const void *wd, const moe_q4 *q4, void *y, void *ws, cudaStream_t st,
-               const float *w = nullptr, const int32_t *pos = nullptr, void *out = nullptr, bool *fused = nullptr) {
-    const WsLayout L = ws_layout(s);
-    const int path = grouped_path(s, q4);
-    const bool fuse = out && grouped_fuses_unpermute(path, s);
-    if (fused) *fused = fuse;
     if (path > 0)
-        return launch_rc(launch_grouped_fast(path, s, x, offsets, order, wg, wu, wd, q4, at<float>(ws, L.part),
-                                             at<void>(ws, L.h), y, at<int32_t>(ws, L.err), ws, fuse ? w : nullptr,
-                                             fuse ? pos : nullptr, fuse ? out : nullptr, st));
+        return launch_rc(launch_grouped_fast(path, s, x, offsets, order, wg, wu, wd, q4,
+                                             at<int32_t>(ws, L.active), at<float>(ws, L.part), at<void>(ws, L.h),
+                                             y, at<int32_t>(ws, L.err), st));
     return launch_rc(launch_grouped_simple(s, x, offsets, order, wg, wu, wd, q4, at<void>(ws, L.h), y, st));
 }
 
@@ -223,9 +212,8 @@ int moe_forward(const moe_shape *shape, const void *x, const void *w_router, con
         MOE_TRY(do_route(s, x, w_router, b_router, ids, w, nullptr, nullptr, workspace, st));
         MOE_TRY(do_permute(s, ids, at<int32_t>(workspace, L.counts), offsets, order, pos, workspace, st));
     }
-    bool fused = false;
-    MOE_TRY(do_grouped(s, x, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st, w, pos, out, &fused));
-    return fused ? MOE_OK : launch_rc(launch_unpermute(s, y, w, pos, out, st));
+    MOE_TRY(do_grouped(s, x, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st));
+    return launch_rc(launch_unpermute(s, y, w, pos, out, st));
 }
 
 int moe_forward_launches(const moe_shape *shape, int32_t *launches) {
@@ -238,8 +226,7 @@ int moe_forward_launches(const moe_shape *shape, int32_t *launches) {
     }
     const int path = select_grouped_path(s);  // a non-affine 4-bit codebook takes path 0 (also 2 launches)
     *launches = (route_fuses(s) ? 1 : route_launches(s) + permute_launches(s)) +
-                (path > 0 ? grouped_fast_launches(path, s) : grouped_simple_launches(s)) +
-                (grouped_fuses_unpermute(path, s) ? 0 : 1);
+                (path > 0 ? grouped_fast_launches(path, s) : grouped_simple_launches(s)) + 1;
     return MOE_OK;
 }
 

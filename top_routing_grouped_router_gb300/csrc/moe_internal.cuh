@@ -91,13 +91,10 @@ __device__ __forceinline__ void record_error(int32_t *err, int code) { atomicCAS
 // ---------------------------------------------------------------- launchers (each returns cudaError_t of the launch)
 
 // Workspace header (zeroed once by the caller, kept at zero between launches by the
-// kernels): error word at byte 0, router arrival counters at bytes 64..127, grouped-kernel
-// scheduling counters at 128..895 (one 128-byte line each), per-expert completion counters
-// at 1024..2047.
+// kernels): error word at byte 0, router arrival counters at bytes 64..127, the rest of
+// the 2 KB reserved.
 constexpr size_t kHdrBytes = 2048;
 constexpr size_t kHdrArrivals = 64;
-constexpr size_t kHdrGrouped = 128;
-constexpr size_t kHdrDone = 1024;
 
 bool route_fuses(const moe_shape &s);
 cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,

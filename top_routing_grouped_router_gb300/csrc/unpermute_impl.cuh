@@ -1,8 +1,7 @@
 // unpermute_impl.cuh -- the weighted un-permute of 8 consecutive output columns of one
 // token (the index_add_ step of the grouped_mm MoE path, as a gather): out[t, c..c+7] =
 // sum_{j<k} w[t, j] * y[pos[t*k + j], c..c+7], summed in slot order in fp32 and rounded
-// once.  Shared by the standalone kernel and the tail of the fused tensor-core kernel so
-// that both give bit-identical results.
+// once.
 #pragma once
 
 #include "moe_internal.cuh"
