@@ -57,6 +57,8 @@ def test_prefill_full_size_layer(layer):
     (5, 128, 8, 8, 64, "bf16", "bf16", False),       # k == E: every expert, infinite margins
     (40, 256, 2, 2, 128, "bf16", "q4", False),       # 4-bit, 40 tokens per expert (one k-slab per down stage)
     (64, 384, 8, 2, 256, "bf16", "q4", True),        # 4-bit, skewed load, three row blocks of H
+    (600, 512, 16, 4, 256, "bf16", "bf16", False),   # large batch: several token chunks per expert
+    (1030, 512, 8, 2, 384, "bf16", "bf16", True),    # large batch, skewed load: ragged chunks
 ])
 def test_reduced_and_ragged_cases(T, H, E, k, I, act, w, zipf):
     inp = synth.make_custom(T, H, E, k, I, act=act, w=w, zipf=zipf, seed=T + E, name=f"custom{T}")
@@ -87,6 +89,15 @@ def test_all_tokens_to_the_same_experts():
     s, g = check_layer(inp, full_oracle=False, n_sample_tokens=12, n_sample_rows=24)
     assert sorted(np.nonzero(g["counts"])[0].tolist()) == [3, 17, 22, 30]
     assert (g["counts"][[3, 17, 22, 30]] == 40).all()
+
+
+def test_two_experts_take_every_token_of_a_large_batch():
+    inp = synth.make_custom(777, 256, 16, 2, 128, act="bf16", w="bf16", seed=9)
+    bias = np.zeros(16, np.float32)
+    bias[[2, 11]] = 40.0
+    inp.b_router = bias
+    s, g = check_layer(inp, full_oracle=False, n_sample_tokens=12, n_sample_rows=32)
+    assert (g["counts"][[2, 11]] == 777).all()
 
 
 def test_zero_tokens():

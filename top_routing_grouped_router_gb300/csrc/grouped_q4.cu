@@ -208,18 +208,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const int N = m > 0 ? (m + 15) & ~15 : 16;
             if (down) {
                 const int need = (p.I / kRows) * kEpiWarps;
-                long long n = 0;
-                for (;;) {
-                    int v;
-                    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p.done + e) : "memory");
-                    if (v >= need || *abort) break;
-                    if (++n > kSpinLimit) {
-                        record_error(p.err, MOE_ERR_DEVICE);
-                        *abort = 1;
-                        break;
-                    }
-                    __nanosleep(64);
-                }
+                wait_count(p.done + e, need, p.err, abort);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, p.err, abort);

@@ -11,8 +11,10 @@
 // Tiles: gate/up tile = (expert e, 128 rows of I, 128-token chunk): two MMAs per
 // k-step, gate into TMEM columns [0, N) and up into [128, 128+N), so one epilogue
 // thread (TMEM lane = weight row) holds g and u of the same row and forms
-// SiLU(g)*u in registers.  Down tile = (e, 128 rows of H, token chunk) over the
-// expert's h rows.  All gate/up tiles precede all down tiles in one list that CTAs
+// SiLU(g)*u in registers.  Down tile = (e, 128 rows of H, token chunk of up to 256:
+// an expert's tokens split evenly) over the expert's h rows; its token rows take the
+// stage's second and third 16 KB regions, so a down stage carries as many MMA cycles as
+// a gate/up stage.  All gate/up tiles precede all down tiles in one list that CTAs
 // claim with an atomic counter; a down tile waits (bounded) until every epilogue warp
 // of every gate/up tile of its expert has published h.
 //
@@ -25,6 +27,7 @@
 // The token rows are first gathered into permuted order (x_perm) so that every
 // expert's rows are contiguous for TMA; the same prep kernel builds the tile list.
 #include "moe_internal.cuh"
+#include "grouped_tiles.cuh"
 #include "tc_common.cuh"
 
 #include <algorithm>
@@ -35,18 +38,12 @@ namespace {
 using namespace tc;
 
 constexpr int kRows = 128;                 // weight rows per tile (MMA M)
-constexpr int kMaxN = 128;                 // tokens per tile (MMA N, multiple of 16)
+constexpr int kMaxN = 128;                 // tokens per gate/up tile (MMA N, multiple of 16)
+constexpr int kMaxDownN = 256;             // tokens per down tile
 constexpr int kSlab = 64;                  // k elements per stage (one 128-byte swizzle row)
 constexpr int kNBox = 16;                  // token rows per activation TMA box
 constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
 constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
-// Token chunks: an expert's m tokens are cut into ceil(m / cmax) chunks of cmax tokens,
-// the last one ragged; a single chunk is rounded up to a multiple of 16 (the MMA's N
-// granule).  Full 128-token chunks measured faster than an even split of m.
-__host__ __device__ inline int n_chunks(int me, int cmax) { return me > 0 ? (me + cmax - 1) / cmax : 0; }
-__host__ __device__ inline int chunk_base(int me, int nch, int cmax) {
-    return nch > 1 ? cmax : (nch ? ((me + 15) & ~15) : 0);
-}
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kMetaRing = 8;
@@ -64,11 +61,6 @@ struct Cfg {
 };
 constexpr int kRouterN = 64;               // tokens per router tile: twice the tiles, two k-slabs per stage
 
-// Tile list entry: bit 31 = down tile, bits 16-23 expert, bits 8-15 row block, bits 0-7 token chunk.
-__host__ __device__ constexpr uint32_t pack_tile(int down, int e, int rb, int nc) {
-    return (uint32_t(down) << 31) | (uint32_t(e) << 16) | (uint32_t(rb) << 8) | uint32_t(nc);
-}
-
 // Tile kinds.  The router GEMM (logits[t][e] = x_t . W_r[e]) reuses the kernel as one
 // 128-expert x 128-token tile per CTA.
 enum : int { kGateUp = 0, kDown = 1, kRouter = 2 };
@@ -83,7 +75,8 @@ struct Params {
     uint16_t *h;                // [A][I] bf16
     uint16_t *y;                // [A][H] bf16
     int E, H, I, A;
-    int cmax;                   // largest token chunk of the tile list
+    int cmax;                   // token chunk of the gate/up tiles (fixed chunks)
+    int dmax;                   // token chunk bound of the down tiles (even chunks)
     // router mode: tiles are (row block of experts, 128-token chunk), one static sweep
     int router_tiles;           // > 0 selects router mode
     int T;
@@ -104,7 +97,7 @@ __device__ __forceinline__ TileInfo read_tile(uint32_t entry, const Params &p, b
     ok = d.e < p.E;
     const int off = ok ? __ldg(p.offsets + d.e) : 0;
     const int me = ok ? __ldg(p.offsets + d.e + 1) - off : 0;
-    const int base = chunk_base(me, n_chunks(me, p.cmax), p.cmax);
+    const int base = d.down == kDown ? chunk_base(me, p.dmax, true) : chunk_base(me, p.cmax, false);
     d.r0 = off + nc * base;
     d.m = min(base, me - nc * base);
     ok = ok && off >= 0 && me >= 0 && off + me <= p.A && d.m > 0;
@@ -201,22 +194,16 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 d = read_tile(__ldg(p.tiles + t), p, ok);
             }
             if (!ok) record_error(p.err, MOE_ERR_DEVICE);
+            if (d.down != kGateUp && d.N * 128 > kABytes + kBBytes) {  // cannot happen: chunks fit the stage
+                record_error(p.err, MOE_ERR_DEVICE);
+                d.N = (kABytes + kBBytes) / 128;
+                d.m = min(d.m, d.N);
+            }
             if (d.down == kDown) {
                 // the expert's h must be complete: every epilogue warp of every gate/up tile
                 const int me = __ldg(p.offsets + d.e + 1) - __ldg(p.offsets + d.e);
-                const int need = (p.I / kRows) * n_chunks(me, p.cmax) * kEpiWarps;
-                long long n = 0;
-                for (;;) {
-                    int v;
-                    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p.done + d.e) : "memory");
-                    if (v >= need || *abort) break;
-                    if (++n > kSpinLimit) {
-                        record_error(p.err, MOE_ERR_DEVICE);
-                        *abort = 1;
-                        break;
-                    }
-                    __nanosleep(64);
-                }
+                const int need = (p.I / kRows) * n_chunks(me, p.cmax, false) * kEpiWarps;
+                wait_count(p.done + d.e, need, p.err, abort);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             // hand the tile to the epilogue
@@ -263,8 +250,10 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                             tma_load_2d(bb + h2 * (kBBytes / 2) + q * 2048, bmap, k0, d.r0 + q * kNBox, fb);
                     }
                 } else if (d.down != kGateUp) {
+                    // one weight slab; the token rows fill the rest of the stage (up to 256)
                     tma_load_2d(a0, wmap, ks * kSlab, wrow, fb);
-                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * 2048, bmap, ks * kSlab, d.r0 + q * kNBox, fb);
+                    for (int q = 0; q < nbox; ++q)
+                        tma_load_2d(a0 + kABytes + q * 2048, bmap, ks * kSlab, d.r0 + q * kNBox, fb);
                 } else {
                     tma_load_2d(a0, &tm_gate, ks * kSlab, wrow, fb);
                     tma_load_2d(a0 + kABytes, &tm_up, ks * kSlab, wrow, fb);
@@ -310,7 +299,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
 #pragma unroll
                 for (int kk = 0; kk < kSlab / 16; ++kk) {
                     const uint32_t acc = (ks | kk) != 0;
-                    const uint64_t bdesc = smem_desc(bb + kk * 32);
+                    const uint64_t bdesc = smem_desc((down ? a0 + kABytes : bb) + kk * 32);
                     mma_bf16(d, smem_desc(a0 + kk * 32), bdesc, idesc, acc);
                     if (!down) mma_bf16(d + kUpCol, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, acc);
                 }
@@ -392,85 +381,6 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kTmemCols)
                      : "memory");
-    }
-}
-
-// Block-wide exclusive scan of one int per thread (blockDim.x == 256).
-__device__ int scan256(int v, int *s_warp, int &total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-    }
-    if (lane == 31) s_warp[w] = incl;
-    __syncthreads();
-    if (w == 0) {
-        const int wv = lane < 8 ? s_warp[lane] : 0;
-        int i2 = wv;
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, i2, o);
-            if (lane >= o) i2 += n;
-        }
-        if (lane < 8) s_warp[lane] = i2 - wv;
-        if (lane == 7) s_warp[8] = i2;
-    }
-    __syncthreads();
-    const int excl = s_warp[w] + incl - v;
-    total = s_warp[8];
-    __syncthreads();
-    return excl;
-}
-
-// x_perm[p] = x[order[p] / k].  Block 0 also builds the tile list from the offsets
-// and clears the scheduling counters of the tensor-core kernel.
-__global__ void __launch_bounds__(256)
-prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
-            int T, int k, int H, int I, int E, int cmax, uint16_t *__restrict__ x_perm, uint32_t *tiles,
-            int max_tiles, int *n_tiles, int *tile_counter, int *done, int32_t *err) {
-    griddep_launch_dependents();
-    griddep_wait();
-    if (blockIdx.x > 0) {
-        const int pr = blockIdx.x - 1;
-        const int a = __ldg(order + pr);
-        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
-        if (a < 0 || a >= T * k) {
-            if (threadIdx.x == 0) record_error(err, MOE_ERR_DEVICE);
-            for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
-        } else {
-            const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(a / k) * H);
-            for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
-        }
-        return;
-    }
-    __shared__ int s_warp[9];
-    const int e = threadIdx.x;
-    int me = 0;
-    if (e < E) {
-        me = min(max(offsets[e + 1] - offsets[e], 0), T * k);
-        done[e] = 0;
-    }
-    const int nch = n_chunks(me, cmax);
-    const int gu_per = I / kRows, dn_per = H / kRows;
-    int n_gu, n_dn;
-    const int gu_off = scan256(nch * gu_per, s_warp, n_gu);
-    const int dn_off = scan256(nch * dn_per, s_warp, n_dn);
-    for (int c = 0; c < nch; ++c) {
-        for (int r = 0; r < gu_per; ++r) {
-            const int i = gu_off + c * gu_per + r;
-            if (i < max_tiles) tiles[i] = pack_tile(0, e, r, c);
-        }
-        for (int r = 0; r < dn_per; ++r) {
-            const int i = n_gu + dn_off + c * dn_per + r;
-            if (i < max_tiles) tiles[i] = pack_tile(1, e, r, c);
-        }
-    }
-    if (threadIdx.x == 0) {
-        if (n_gu + n_dn > max_tiles) record_error(err, MOE_ERR_DEVICE);  // inconsistent offsets
-        *n_tiles = min(n_gu + n_dn, max_tiles);
-        *tile_counter = 0;
     }
 }
 
@@ -569,9 +479,10 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
         return cudaErrorInvalidValue;
 
     const int cmax = kMaxN;
+    const int dmax = kMaxDownN;
+    const TileListArgs ta{cmax, 0, dmax, 1, s.I / kRows, s.H / kRows, (int)max_tiles(s)};
     cudaError_t e = launch_pdl(prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
-                               offsets, s.T, s.k, s.H, s.I, s.E, cmax, x_perm, tiles, (int)max_tiles(s), n_tiles,
-                               tile_counter, done, err);
+                               offsets, s.T, s.k, s.H, s.E, ta, x_perm, tiles, n_tiles, tile_counter, done, err);
     if (e != cudaSuccess) return e;
 
     Params prm{};
@@ -588,6 +499,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.I = s.I;
     prm.A = A;
     prm.cmax = cmax;
+    prm.dmax = dmax;
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (s.T <= 32) return launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, prm);

@@ -1,0 +1,123 @@
+// grouped_tiles.cuh -- the tile list of the bf16 tensor-core kernels and the prep kernel
+// that builds it: an expert's tokens (the segment [offsets[e], offsets[e+1]) of the
+// expert-sorted assignments) are cut into token chunks, and every (expert, chunk) pair
+// yields gate/up tiles (row blocks of I) followed, after all gate/up tiles, by down tiles
+// (row blocks of H); gate/up and down tiles may cut the tokens into chunks of different
+// sizes.  The same kernel gathers the token rows into permuted order
+// (x_perm[p] = x[order[p] / k]) so that every expert's rows are contiguous for TMA.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+// Token chunks of an expert with `me` tokens, at most `cmax` tokens each (cmax a multiple
+// of 16).  Fixed policy: chunks of cmax tokens, the last one ragged.  Even policy:
+// ceil(me / cmax) chunks of nearly equal size (multiples of 16 except the last).  A lone
+// chunk is rounded up to a multiple of 16 (the MMA's N granule) in both.
+__host__ __device__ inline int chunk_base(int me, int cmax, bool even) {
+    if (me <= 0) return 0;
+    const int n = (me + cmax - 1) / cmax;
+    if (n == 1) return (me + 15) & ~15;
+    return even ? ((((me + n - 1) / n) + 15) & ~15) : cmax;
+}
+__host__ __device__ inline int n_chunks(int me, int cmax, bool even) {
+    const int b = chunk_base(me, cmax, even);
+    return b > 0 ? (me + b - 1) / b : 0;
+}
+
+// Tile list entry: bit 31 = down tile, bits 16-23 expert, bits 8-15 row block, bits 0-7 token chunk.
+__host__ __device__ constexpr uint32_t pack_tile(int down, int e, int rb, int nc) {
+    return (uint32_t(down) << 31) | (uint32_t(e) << 16) | (uint32_t(rb) << 8) | uint32_t(nc);
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x == 256).
+__device__ inline int scan256(int v, int *s_warp, int &total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        const int wv = lane < 8 ? s_warp[lane] : 0;
+        int i2 = wv;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, i2, o);
+            if (lane >= o) i2 += n;
+        }
+        if (lane < 8) s_warp[lane] = i2 - wv;
+        if (lane == 7) s_warp[8] = i2;
+    }
+    __syncthreads();
+    const int excl = s_warp[w] + incl - v;
+    total = s_warp[8];
+    __syncthreads();
+    return excl;
+}
+
+struct TileListArgs {
+    int gu_cmax, gu_even;  // token chunks of the gate/up tiles: bound and policy (see chunk_base)
+    int dn_cmax, dn_even;  // token chunks of the down tiles
+    int gu_per;            // gate/up tiles per chunk (row blocks of I)
+    int dn_per;            // down tiles per chunk (row blocks of H)
+    int max_tiles;         // capacity of `tiles`
+};
+
+// Block 0: the tile list from the offsets, its length, a zeroed claim counter and zeroed
+// per-expert completion counters.  Blocks 1..A: x_perm row blockIdx.x - 1.
+__global__ void __launch_bounds__(256)
+prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
+            int T, int k, int H, int E, TileListArgs ta, uint16_t *__restrict__ x_perm, uint32_t *tiles,
+            int *n_tiles, int *tile_counter, int *done, int32_t *err) {
+    griddep_launch_dependents();
+    griddep_wait();
+    if (blockIdx.x > 0) {
+        const int pr = blockIdx.x - 1;
+        const int a = __ldg(order + pr);
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
+        if (a < 0 || a >= T * k) {
+            if (threadIdx.x == 0) record_error(err, MOE_ERR_DEVICE);
+            for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+        } else {
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(a / k) * H);
+            for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+        }
+        return;
+    }
+    __shared__ int s_warp[9];
+    const int e = threadIdx.x;
+    int me = 0;
+    if (e < E) {
+        me = min(max(offsets[e + 1] - offsets[e], 0), T * k);
+        done[e] = 0;
+    }
+    const int nch_gu = n_chunks(me, ta.gu_cmax, ta.gu_even != 0);
+    const int nch_dn = n_chunks(me, ta.dn_cmax, ta.dn_even != 0);
+    int n_gu, n_dn;
+    const int gu_off = scan256(nch_gu * ta.gu_per, s_warp, n_gu);
+    const int dn_off = scan256(nch_dn * ta.dn_per, s_warp, n_dn);
+    for (int c = 0; c < nch_gu; ++c)
+        for (int r = 0; r < ta.gu_per; ++r) {
+            const int i = gu_off + c * ta.gu_per + r;
+            if (i < ta.max_tiles) tiles[i] = pack_tile(0, e, r, c);
+        }
+    for (int c = 0; c < nch_dn; ++c)
+        for (int r = 0; r < ta.dn_per; ++r) {
+            const int i = n_gu + dn_off + c * ta.dn_per + r;
+            if (i < ta.max_tiles) tiles[i] = pack_tile(1, e, r, c);
+        }
+    if (threadIdx.x == 0) {
+        if (n_gu + n_dn > ta.max_tiles) record_error(err, MOE_ERR_DEVICE);  // inconsistent offsets
+        *n_tiles = min(n_gu + n_dn, ta.max_tiles);
+        *tile_counter = 0;
+    }
+}
+
+}  // namespace
+}  // namespace moe

@@ -9,8 +9,17 @@
 namespace moe {
 namespace tc {
 
-constexpr long long kSpinLimit = 1ll << 22;   // polls of a global flag (with a 64 ns sleep)
-constexpr long long kPollLimit = 1ll << 22;   // mbarrier polls
+// Every wait of the tensor-core kernels gives up after kWaitNs of wall time (read from
+// %globaltimer): it then records MOE_ERR_DEVICE, raises the CTA's abort flag and returns,
+// so that a lost arrival ends the kernel with an error instead of a hang.  Healthy waits
+// last microseconds; the limit only has to be far above any legitimate stall.
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -54,19 +63,40 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     return v;
 }
 
-// Bounded wait: after kPollLimit polls record the error and raise the CTA's abort flag,
-// so that every later wait of the CTA gives up at once and the kernel drains.  The flag
-// is checked every 16 polls.
+// Bounded wait: after kWaitNs record the error and raise the CTA's abort flag, so that
+// every later wait of the CTA gives up at once and the kernel drains.  The flag and the
+// clock are checked every 16 polls.
 __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, int32_t *err, volatile int *abort) {
-    long long n = 0;
-    while (!mbar_try_wait(bar, parity)) {
-        ++n;
-        if ((n & 15) == 0 && *abort) return;
-        if (n > kPollLimit) {
+    if (mbar_try_wait(bar, parity)) return;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((n & 15) == 0) {
+            if (*abort) return;
+            if (globaltimer_ns() - t0 > kWaitNs) {
+                record_error(err, MOE_ERR_DEVICE);
+                *abort = 1;
+                return;
+            }
+        }
+    }
+}
+
+// Bounded wait until the global counter *p reaches `need` (acquire); same limit.
+__device__ __forceinline__ void wait_count(const int *p, int need, int32_t *err, volatile int *abort) {
+    unsigned long long t0 = 0;
+    for (uint32_t n = 0;; ++n) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= need || *abort) return;
+        if (n == 0) {
+            t0 = globaltimer_ns();
+        } else if (globaltimer_ns() - t0 > kWaitNs) {
             record_error(err, MOE_ERR_DEVICE);
             *abort = 1;
             return;
         }
+        __nanosleep(64);
     }
 }
 
