@@ -230,6 +230,68 @@ MOE_API int moe_forward_launches(const moe_shape *shape, int32_t *launches);
  */
 MOE_API int moe_read_device_error(void *workspace, int32_t *code, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Bucketed CUDA-graph decode (the capture pattern of the unsloth commit page
+ * 80aaf1121b, paragraph on FlexMoEInference.capture_decode_cudagraph): one
+ * graph of moe_forward per batch-size bucket [1, 2, 4, 8] + 16, 32, ... up to
+ * the first multiple of 16 >= max_bs, static input / output buffers and one
+ * device arena shared by every bucket.
+ *
+ * A step with T live tokens replays the smallest bucket B >= T: the static
+ * input rows [T, B) are zeroed, the T live rows copied in, the graph replayed
+ * and the first T output rows (and expert ids) copied out.  Padded rows are
+ * routed like any token and their results discarded, so the live rows equal
+ * those of moe_forward on the zero-padded batch of B tokens.
+ */
+typedef struct moe_graphs moe_graphs;
+
+/*
+ * The bucket list for max_bs (host only): writes n <= cap sizes to buckets.
+ * MOE_ERR_SHAPE if max_bs is outside [1, 2^18] or the list needs more than cap
+ * (or 64) entries.
+ */
+MOE_API int moe_graph_buckets(int max_bs, int32_t *buckets, int cap, int32_t *n);
+
+/*
+ * Device arena bytes a graph set for this shape and max_bs needs (host only):
+ * static x, out and expert ids for the largest bucket and one workspace that
+ * every bucket's moe_workspace_size() fits in.  shape->T is ignored.
+ */
+MOE_API int moe_graphs_arena_size(const moe_shape *shape, int max_bs, size_t *bytes);
+
+/*
+ * Captures the bucket graphs on `stream` (a non-default stream; thread-local
+ * capture mode) after one eager moe_forward per bucket (outside capture).
+ *   arena          caller-owned device memory of moe_graphs_arena_size() bytes,
+ *                  256-byte aligned; the graphs own it until moe_graphs_destroy.
+ *   weights, q4    captured by address (their contents may change between
+ *                  replays, their addresses may not); the 4-bit codebook values
+ *                  are captured by value.
+ *   *graphs        receives a host handle (heap memory of the library).
+ * Returns MOE_ERR_WORKSPACE if arena_bytes is too small, the moe_forward
+ * validation errors for the bucket shapes, MOE_ERR_LAUNCH if a capture or
+ * instantiation fails (nothing is kept then).
+ */
+MOE_API int moe_graphs_create(const moe_shape *shape, int max_bs, const void *w_router, const float *b_router,
+                              const void *w_gate, const void *w_up, const void *w_down, const moe_q4 *q4,
+                              void *arena, size_t arena_bytes, moe_stream_t stream, moe_graphs **graphs);
+
+/* The bucket a step of T tokens replays (host only); MOE_ERR_SHAPE if none. */
+MOE_API int moe_graphs_bucket(const moe_graphs *graphs, int T, int32_t *bucket);
+
+/*
+ * One decode step of T tokens (1 <= T <= largest bucket), enqueued on `stream`.
+ *   x    [T][H] activations, device or host memory (cudaMemcpyDefault).
+ *   out  [T][H] output, device or host memory.
+ *   expert_ids_out [T][k] int32 or NULL.
+ * Steps on different streams must be serialised: the graphs share one arena.
+ */
+MOE_API int moe_graphs_run(moe_graphs *graphs, int T, const void *x, void *out, int32_t *expert_ids_out,
+                           moe_stream_t stream);
+
+/* Frees the graph executables and the handle (not the arena). */
+MOE_API int moe_graphs_destroy(moe_graphs *graphs);
+
 /* Static, human-readable name of a status code. */
 MOE_API const char *moe_status_string(int status);
 

@@ -98,3 +98,25 @@ def test_binding_raises_on_error(L):
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_workspace_size(s)
     assert ei.value.status == -2
+
+
+def test_graph_buckets_follow_the_capture_pattern():
+    # [1, 2, 4, 8] + 16, 32, ... up to the first multiple of 16 covering max_bs
+    assert moe.moe_graph_buckets(1) == [1]
+    assert moe.moe_graph_buckets(5) == [1, 2, 4, 8]
+    assert moe.moe_graph_buckets(8) == [1, 2, 4, 8]
+    assert moe.moe_graph_buckets(64) == [1, 2, 4, 8, 16, 32, 48, 64]
+    assert moe.moe_graph_buckets(40) == [1, 2, 4, 8, 16, 32, 48]
+    with pytest.raises(moe.MoEError):
+        moe.moe_graph_buckets(0)
+    with pytest.raises(moe.MoEError):
+        moe.moe_graph_buckets(100000)  # more buckets than the table holds
+
+
+def test_graph_arena_covers_every_bucket_workspace():
+    shape = moe.make_shape(1, 2048, 128, 8, 768)
+    arena = moe.moe_graphs_arena_size(shape, 64)
+    ws64 = moe.moe_workspace_size(moe.make_shape(64, 2048, 128, 8, 768))
+    static = 2 * 64 * 2048 * 2 + 64 * 8 * 4
+    assert arena >= ws64 + static
+    assert arena <= ws64 + static + 4 * 256

@@ -18,7 +18,7 @@ __all__ = [
     "MOE_DT_F32", "MOE_DT_BF16", "MOE_DT_Q4", "MoEError", "MoEShape", "MoEQ4", "lib", "library_path",
     "make_shape", "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string", "EXPORTED_SYMBOLS",
-    "moe_forward_static_scratch",
+    "moe_forward_static_scratch", "moe_graph_buckets", "moe_graphs_arena_size", "DecodeGraphs",
 ]
 
 MOE_DT_F32, MOE_DT_BF16, MOE_DT_Q4 = 0, 1, 2
@@ -29,7 +29,8 @@ library_path = os.path.join(_HERE, "libmoe_gb300.so")
 
 EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
                     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string",
-                    "moe_forward_static_scratch")
+                    "moe_forward_static_scratch", "moe_graph_buckets", "moe_graphs_arena_size", "moe_graphs_create",
+                    "moe_graphs_bucket", "moe_graphs_run", "moe_graphs_destroy")
 
 
 class MoEError(RuntimeError):
@@ -73,6 +74,12 @@ def lib() -> ctypes.CDLL:
             "moe_read_device_error": [vp, ctypes.POINTER(ctypes.c_int32), vp],
             "moe_forward_launches": [sp, ctypes.POINTER(ctypes.c_int32)],
             "moe_forward_static_scratch": [sp, vp, vp, vp, vp, vp, vp, q4p, vp, i32p, vp, vp],
+            "moe_graph_buckets": [ctypes.c_int, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)],
+            "moe_graphs_arena_size": [sp, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
+            "moe_graphs_create": [sp, ctypes.c_int, vp, vp, vp, vp, vp, q4p, vp, sz, vp, ctypes.POINTER(vp)],
+            "moe_graphs_bucket": [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)],
+            "moe_graphs_run": [vp, ctypes.c_int, vp, vp, i32p, vp],
+            "moe_graphs_destroy": [vp],
         }
         for name, argtypes in sig.items():
             f = getattr(L, name)
@@ -179,3 +186,66 @@ def moe_read_device_error(workspace, stream=None) -> int:
     _check(lib().moe_read_device_error(_ptr(workspace), ctypes.byref(code), _stream(stream)),
            "moe_read_device_error")
     return code.value
+
+
+def moe_graph_buckets(max_bs: int) -> list:
+    """Batch-size buckets of the decode graphs for max_bs (host only)."""
+    buf = (ctypes.c_int32 * 64)()
+    n = ctypes.c_int32(0)
+    _check(lib().moe_graph_buckets(int(max_bs), ctypes.cast(buf, ctypes.c_void_p), 64, ctypes.byref(n)),
+           "moe_graph_buckets")
+    return list(buf[:n.value])
+
+
+def moe_graphs_arena_size(shape: MoEShape, max_bs: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_graphs_arena_size(ctypes.byref(shape), int(max_bs), ctypes.byref(n)), "moe_graphs_arena_size")
+    return n.value
+
+
+class DecodeGraphs:
+    """Bucketed CUDA-graph decode around moe_forward (moe_graphs_* of the C ABI).
+
+    The arena (a device uint8 tensor of moe_graphs_arena_size bytes) is allocated here and
+    kept alive with the graphs; the weights are captured by address and must outlive them.
+    """
+
+    def __init__(self, shape: MoEShape, max_bs: int, w_router, b_router, w_gate, w_up, w_down, q4=None,
+                 device=None, stream=None):
+        import torch
+        self.shape = shape
+        if device is None:
+            device = w_router.device if hasattr(w_router, "device") else torch.device("cuda")
+        self.arena = torch.zeros(moe_graphs_arena_size(shape, max_bs), dtype=torch.uint8, device=device)
+        self._keep = (w_router, b_router, w_gate, w_up, w_down, q4)
+        self._stream = stream if stream is not None else torch.cuda.Stream(device=self.arena.device)
+        h = ctypes.c_void_p(0)
+        _check(lib().moe_graphs_create(ctypes.byref(shape), int(max_bs), _ptr(w_router), _ptr(b_router),
+                                       _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                       ctypes.byref(q4) if q4 is not None else None, _ptr(self.arena),
+                                       self.arena.numel(), _stream(self._stream), ctypes.byref(h)),
+               "moe_graphs_create")
+        self._h = h
+        self.buckets = moe_graph_buckets(max_bs)
+
+    def bucket(self, T: int) -> int:
+        b = ctypes.c_int32(0)
+        _check(lib().moe_graphs_bucket(self._h, int(T), ctypes.byref(b)), "moe_graphs_bucket")
+        return b.value
+
+    def run(self, T: int, x, out, expert_ids_out=None, stream=None):
+        """One decode step of T tokens: x [T][H] in, out [T][H] out (device or host tensors)."""
+        st = self._stream if stream is None else stream
+        _check(lib().moe_graphs_run(self._h, int(T), _ptr(x), _ptr(out), _ptr(expert_ids_out), _stream(st)),
+               "moe_graphs_run")
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().moe_graphs_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
