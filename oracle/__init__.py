@@ -66,6 +66,9 @@ def lib() -> ctypes.CDLL:
             getattr(_lib, name).restype = ctypes.c_int
         _lib.orc_weight_at.restype = ctypes.c_double
         _lib.orc_weight_at.argtypes = [ctypes.POINTER(_Matrix), ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+        _lib.orc_rmsnorm.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_double, ctypes.c_void_p]
+        _lib.orc_round_bf16.argtypes = [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
     return _lib
 
 
@@ -223,3 +226,55 @@ def weight_at(inp, which: str, e: int, r: int, c: int) -> float:
     g, u, d, keep = _mats(inp)
     m = {"gate": g, "up": u, "down": d}[which]
     return lib().orc_weight_at(ctypes.byref(m), e, r, c)
+
+
+def rmsnorm(hs: np.ndarray, gamma: np.ndarray, eps: float, act: str) -> np.ndarray:
+    """Pre-router RMSNorm in double: hs [T, H] and gamma [H] in storage form (fp32, or bf16 bits)."""
+    hs = np.ascontiguousarray(hs)
+    gamma = np.ascontiguousarray(gamma)
+    T, H = hs.shape
+    xn = np.empty((T, H), dtype=np.float64)
+    _check(lib().orc_rmsnorm(T, H, _DT[act], _p(hs), _p(gamma), float(eps), _p(xn)), "rmsnorm")
+    return xn
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """bf16 bits of doubles, rounded to nearest even directly from double."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    bits = np.empty(v.shape, dtype=np.uint16)
+    _check(lib().orc_round_bf16(v.size, _p(v), _p(bits)), "round_bf16")
+    return bits
+
+
+def _prenormed(inp, gamma, eps):
+    import dataclasses
+    xn = rmsnorm(inp.x, gamma, eps, inp.act)
+    x_act = round_bf16(xn) if inp.act == "bf16" else xn.astype(np.float32)
+    return xn, x_act, dataclasses.replace(inp, x=x_act)
+
+
+def _widen(inp, rows):
+    if inp.act == "bf16":
+        return (np.ascontiguousarray(rows).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.asarray(rows, dtype=np.float64)
+
+
+def forward_prenorm(inp, gamma: np.ndarray, eps: float, residual: bool = True) -> dict:
+    """The block on pre-normed inputs: xn = RMSNorm(x) * gamma rounded to the activation dtype
+    (the experts' and the router's input), out = MoE(xn) (+ x when residual)."""
+    xn, x_act, inp2 = _prenormed(inp, gamma, eps)
+    r = forward(inp2)
+    if residual:
+        r["out"] = r["out"] + _widen(inp, inp.x)
+    r["xn"], r["xn_act"] = xn, x_act
+    return r
+
+
+def forward_prenorm_tokens(inp, gamma: np.ndarray, eps: float, tokens: Sequence[int], residual: bool = True) -> dict:
+    """forward_prenorm for a sample of tokens."""
+    xn, x_act, inp2 = _prenormed(inp, gamma, eps)
+    r = forward_tokens(inp2, tokens)
+    if residual:
+        r["out"] = r["out"] + _widen(inp, inp.x[np.asarray(tokens)])
+    r["xn"], r["xn_act"] = xn, x_act
+    return r

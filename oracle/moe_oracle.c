@@ -339,3 +339,57 @@ double orc_weight_at(const orc_matrix *m, int64_t e, int64_t r, int64_t c)
 {
     return weight_at(m, e, r, c);
 }
+
+/*
+ * Pre-router RMSNorm of the Qwen3 decoder layer, the "layernorm" that the unsloth
+ * commit page a1bc5cbd73 (compile_walker paragraph) says Inductor fuses with the
+ * residual and router pointwise ops.  The pages give no formula; this is the plain
+ * RMSNorm definition:
+ *   xn[t,h] = hs[t,h] / sqrt(mean_h' hs[t,h']^2 + eps) * gamma[h]
+ * in double, hs and gamma widened exactly from the activation dtype.
+ */
+int orc_rmsnorm(int T, int H, int act_dtype, const void *hs, const void *gamma, double eps, double *xn)
+{
+    if (T < 0 || H <= 0 || !xn || (T > 0 && (!hs || !gamma)) || eps < 0) return -1;
+    for (int t = 0; t < T; ++t) {
+        double ss = 0.0;
+        for (int h = 0; h < H; ++h) {
+            const double v = act_at(act_dtype, hs, (int64_t)t * H + h);
+            ss += v * v;
+        }
+        const double rms = sqrt(ss / H + eps);
+        for (int h = 0; h < H; ++h) {
+            const double v = act_at(act_dtype, hs, (int64_t)t * H + h);
+            xn[(int64_t)t * H + h] = rms > 0.0 ? v / rms * act_at(act_dtype, gamma, h) : 0.0;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Rounds doubles to bf16 (8 significant bits, round to nearest, ties to even)
+ * directly from double, so no intermediate float rounding can move a tie.
+ * Values must lie in the normal bf16 range or be zero.
+ */
+int orc_round_bf16(int64_t n, const double *v, uint16_t *bits)
+{
+    if (n < 0 || (n > 0 && (!v || !bits))) return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const double d = v[i];
+        if (d == 0.0) {
+            bits[i] = signbit(d) ? 0x8000u : 0u;
+            continue;
+        }
+        int e = 0;
+        const double m = frexp(fabs(d), &e);     /* |d| = m * 2^e, m in [0.5, 1) */
+        const double q = ldexp(m, 8);            /* [128, 256): 8 significant bits before the point */
+        double r = floor(q);
+        const double frac = q - r;
+        if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+        const float f = (float)ldexp(r, e - 8);  /* exact: r has at most 9 bits and is a power of 2 when 256 */
+        uint32_t u;
+        memcpy(&u, &f, sizeof u);
+        bits[i] = (uint16_t)((u >> 16) | (d < 0 ? 0x8000u : 0u));
+    }
+    return 0;
+}

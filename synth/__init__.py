@@ -231,3 +231,10 @@ def make_inputs(name: str, *, seed: Optional[int] = None, layer: int = 0, T: Opt
     assert 0 <= layer < c["layers"]
     return make_custom(T if T is not None else c["T"], c["H"], c["E"], c["k"], c["I"], c["act"], c["w"],
                        zipf=c["zipf"], seed=c["seed"] if seed is None else seed, layer=layer, name=name)
+
+
+def make_norm_weight(H: int, act: str = "bf16", seed: int = 0, layer: int = 0) -> np.ndarray:
+    """Synthetic RMSNorm weight gamma [H]: 1 + 0.1 N(0, 1), in the activation's storage form
+    (bf16 bits, or fp32).  Seeded like every other tensor; no model checkpoint exists here."""
+    g = (1.0 + 0.1 * _rng(seed, layer, 901).standard_normal(H)).astype(np.float32)
+    return bf16_bits(g) if act == "bf16" else g

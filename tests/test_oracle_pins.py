@@ -317,3 +317,58 @@ def test_bf16_widening_is_exact():
                           x=x, w_router=synth.bf16_bits(np.array([[3.140625]], np.float32)), b_router=None,
                           w_gate=z[None], w_up=z[None], w_down=z[None])
     assert oracle.router_logits(inp)[0, 0] == 3.140625
+
+
+# ---------------------------------------------------------------- pre-router RMSNorm
+
+def test_rmsnorm_worked_example(golden_dir):
+    d = json.load(open(os.path.join(golden_dir, "worked_rmsnorm.json")))
+    hs = np.array(d["hs"], dtype=np.float32)
+    for r, gamma in enumerate(d["gamma_rows"]):
+        xn = oracle.rmsnorm(hs[r:r + 1], np.array(gamma, dtype=np.float32), d["eps"], "f32")
+        np.testing.assert_allclose(xn[0], d["expect"][r], rtol=1e-15, atol=0)
+
+
+def test_rmsnorm_is_scale_invariant_and_unit_rms():
+    rng = np.random.default_rng(5)
+    hs = rng.standard_normal((3, 96)).astype(np.float32)
+    gamma = np.ones(96, dtype=np.float32)
+    a = oracle.rmsnorm(hs, gamma, 0.0, "f32")
+    b = oracle.rmsnorm((hs * np.float32(4.0)).astype(np.float32), gamma, 0.0, "f32")  # exact power-of-2 scale
+    np.testing.assert_allclose(a, b, rtol=1e-15, atol=0)
+    np.testing.assert_allclose((a ** 2).mean(axis=1), 1.0, rtol=1e-13)
+    # gamma scales each column; a zero row stays zero with eps > 0
+    g2 = rng.uniform(0.5, 1.5, 96).astype(np.float32)
+    np.testing.assert_allclose(oracle.rmsnorm(hs, g2, 0.0, "f32"), a * g2.astype(np.float64), rtol=1e-14)
+    z = oracle.rmsnorm(np.zeros((1, 96), np.float32), g2, 1e-6, "f32")
+    assert np.all(z == 0)
+    # eps enters under the root: a row of ones with eps = 3 gives 1 / sqrt(1 + 3) = 0.5
+    np.testing.assert_allclose(oracle.rmsnorm(np.ones((1, 8), np.float32), np.ones(8, np.float32), 3.0, "f32"), 0.5,
+                               rtol=1e-15)
+
+
+def test_round_bf16_is_nearest_even_from_double():
+    v = np.array([1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -8 + 2 ** -30, -1.5, 0.0, 3.0 * 2 ** -20, 1 - 2 ** -10])
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: even mantissa -> 1; 1 + 3*2^-8 -> 1 + 2^-6 (even);
+    # just above a half rounds up; 1 - 2^-10 rounds up to 1
+    assert oracle.round_bf16(v).tolist() == [0x3F80, 0x3F80, 0x3F82, 0x3F81, 0xBFC0, 0x0000, 0x3640, 0x3F80]
+    # away from ties it agrees with fp32 rounding followed by bf16 rounding
+    w = np.random.default_rng(6).standard_normal(1000)
+    np.testing.assert_array_equal(oracle.round_bf16(w), synth.bf16_bits(w.astype(np.float32)))
+
+
+def test_prenorm_block_with_one_hidden_unit_has_a_closed_form():
+    # H = 1: RMSNorm(h) * gamma = sign(h) * gamma (eps = 0), so with one expert (E = k = 1,
+    # weight 1) and I = 1, out = h + SiLU(a x) * (b x) * c with x = sign(h) * gamma
+    inp = synth.MoEInputs(name="h1", T=2, H=1, E=1, k=1, I=1, act="f32", w="f32", norm_topk=True, q_block=64,
+                          x=np.array([[-0.75], [2.5]], np.float32), w_router=np.array([[1.0]], np.float32),
+                          b_router=None, w_gate=np.array([[[0.625]]], np.float32), w_up=np.array([[[1.5]]], np.float32),
+                          w_down=np.array([[[-2.0]]], np.float32))
+    gamma = np.array([1.25], np.float32)
+    r = oracle.forward_prenorm(inp, gamma, 0.0, residual=True)
+    for t, h in enumerate([-0.75, 2.5]):
+        x = math.copysign(1.25, h)
+        expect = h + (0.625 * x / (1 + math.exp(-0.625 * x))) * (1.5 * x) * (-2.0)
+        assert abs(r["out"][t, 0] - expect) < 1e-12
+    r0 = oracle.forward_prenorm(inp, gamma, 0.0, residual=False)
+    np.testing.assert_allclose(r["out"] - r0["out"], inp.x.astype(np.float64), rtol=0, atol=1e-15)
