@@ -186,6 +186,29 @@ MOE_API int moe_forward(const moe_shape *shape, const void *x, const void *w_rou
                 void *out, int32_t *expert_ids_out, float *weights_out,
                 void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/*
+ * The MoE block with the pre-router RMSNorm and the residual add of the Qwen3
+ * decoder layer fused in: the "layernorm + residual + router pointwise ops"
+ * that the unsloth commit page a1bc5cbd73 (compile_walker paragraph) reports
+ * Inductor fusing for about 2x decode throughput.
+ *   xn  = RMSNorm(hs) * gamma = (hs / sqrt(mean_h hs^2 + eps)) * gamma, in fp32,
+ *         rounded once to the activation dtype; the router and the experts
+ *         read xn
+ *   out = hs + MoE(xn) when add_residual, else MoE(xn)
+ * For T <= 64 the norm runs inside the router launch (the expert-block-0
+ * column of the router grid writes xn); larger batches take one extra launch.
+ *   hs [T][H], gamma [H]: activation dtype.  eps: finite, >= 0 (else
+ *                  MOE_ERR_SHAPE).
+ *   x_norm_out     [T][H] activation dtype, or NULL: where xn is written (the
+ *                  workspace otherwise).
+ * Other arguments, the workspace size and the errors are those of moe_forward.
+ */
+MOE_API int moe_forward_rmsnorm(const moe_shape *shape, const void *hs, const void *gamma, float eps,
+                                int add_residual, const void *w_router, const float *b_router, const void *w_gate,
+                                const void *w_up, const void *w_down, const moe_q4 *q4, void *out,
+                                void *x_norm_out, int32_t *expert_ids_out, float *weights_out, void *workspace,
+                                size_t workspace_bytes, moe_stream_t stream);
+
 /* Size of the library's fixed device scratch array used by moe_forward_static_scratch. */
 #define MOE_STATIC_SCRATCH_BYTES (32u << 20)
 

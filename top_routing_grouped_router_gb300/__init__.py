@@ -18,7 +18,8 @@ __all__ = [
     "MOE_DT_F32", "MOE_DT_BF16", "MOE_DT_Q4", "MoEError", "MoEShape", "MoEQ4", "lib", "library_path",
     "make_shape", "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string", "EXPORTED_SYMBOLS",
-    "moe_forward_static_scratch", "moe_graph_buckets", "moe_graphs_arena_size", "DecodeGraphs",
+    "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_graph_buckets", "moe_graphs_arena_size",
+    "DecodeGraphs",
 ]
 
 MOE_DT_F32, MOE_DT_BF16, MOE_DT_Q4 = 0, 1, 2
@@ -29,7 +30,7 @@ library_path = os.path.join(_HERE, "libmoe_gb300.so")
 
 EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
                     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string",
-                    "moe_forward_static_scratch", "moe_graph_buckets", "moe_graphs_arena_size", "moe_graphs_create",
+                    "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_graph_buckets", "moe_graphs_arena_size", "moe_graphs_create",
                     "moe_graphs_bucket", "moe_graphs_run", "moe_graphs_destroy")
 
 
@@ -74,6 +75,8 @@ def lib() -> ctypes.CDLL:
             "moe_read_device_error": [vp, ctypes.POINTER(ctypes.c_int32), vp],
             "moe_forward_launches": [sp, ctypes.POINTER(ctypes.c_int32)],
             "moe_forward_static_scratch": [sp, vp, vp, vp, vp, vp, vp, q4p, vp, i32p, vp, vp],
+            "moe_forward_rmsnorm": [sp, vp, vp, ctypes.c_float, ctypes.c_int, vp, vp, vp, vp, vp, q4p, vp, vp, i32p,
+                                    vp, vp, sz, vp],
             "moe_graph_buckets": [ctypes.c_int, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)],
             "moe_graphs_arena_size": [sp, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
             "moe_graphs_create": [sp, ctypes.c_int, vp, vp, vp, vp, vp, q4p, vp, sz, vp, ctypes.POINTER(vp)],
@@ -173,6 +176,16 @@ def moe_forward_static_scratch(shape, x, w_router, b_router, w_gate, w_up, w_dow
                                             ctypes.byref(q4) if q4 is not None else None, _ptr(out),
                                             _ptr(expert_ids_out), _ptr(weights_out), _stream(stream)),
            "moe_forward_static_scratch")
+
+
+def moe_forward_rmsnorm(shape, hs, gamma, eps, w_router, b_router, w_gate, w_up, w_down, q4, out, add_residual=True,
+                        x_norm_out=None, expert_ids_out=None, weights_out=None, workspace=None, stream=None):
+    """out = hs + MoE(RMSNorm(hs) * gamma) (the residual only with add_residual)."""
+    _check(lib().moe_forward_rmsnorm(ctypes.byref(shape), _ptr(hs), _ptr(gamma), float(eps), int(bool(add_residual)),
+                                     _ptr(w_router), _ptr(b_router), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                     ctypes.byref(q4) if q4 is not None else None, _ptr(out), _ptr(x_norm_out),
+                                     _ptr(expert_ids_out), _ptr(weights_out), _ptr(workspace), _nbytes(workspace),
+                                     _stream(stream)), "moe_forward_rmsnorm")
 
 
 def moe_forward_launches(shape: MoEShape) -> int:

@@ -5,6 +5,7 @@
 #include "moe_internal.cuh"
 
 #include <limits.h>
+#include <cmath>
 
 namespace moe {
 
@@ -51,6 +52,7 @@ WsLayout ws_layout(const moe_shape &s) {
         return o;
     };
     L.err = take(kHdrBytes);
+    L.xn = take((size_t)s.T * s.H * act_bytes(s));
     L.logits = take((size_t)s.T * E * 4);
     L.ids = take(A * 4);
     L.weights = take(A * 4);
@@ -185,6 +187,43 @@ int moe_unpermute(const moe_shape *shape, const void *y, const float *weights, c
     return launch_rc(launch_unpermute(s, y, weights, pos, out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+// moe_forward and moe_forward_rmsnorm.  With gamma, the router and the experts read
+// xn = RMSNorm(x) * gamma (written to xn_dst) and `resid` is added in the un-permute.
+int forward_impl(const moe_shape &s, const void *x, const void *w_router, const float *b_router, const void *w_gate,
+                 const void *w_up, const void *w_down, const moe_q4 *q4, void *out, int32_t *expert_ids_out,
+                 float *weights_out, void *workspace, cudaStream_t st, const void *gamma, float eps, void *xn_dst,
+                 const void *resid) {
+    const WsLayout L = ws_layout(s);
+    int32_t *ids = expert_ids_out ? expert_ids_out : at<int32_t>(workspace, L.ids);
+    float *w = weights_out ? weights_out : at<float>(workspace, L.weights);
+    int32_t *offsets = at<int32_t>(workspace, L.offsets), *order = at<int32_t>(workspace, L.order),
+            *pos = at<int32_t>(workspace, L.pos);
+    void *y = at<void>(workspace, L.y);
+    const void *xe = gamma ? xn_dst : x;  // the experts' input
+    if (route_fuses(s)) {
+        MOE_TRY(launch_rc(launch_route_permute(s, x, w_router, b_router, at<float>(workspace, L.logits), ids, w,
+                                               at<int>(workspace, kHdrArrivals), at<int32_t>(workspace, L.counts),
+                                               offsets, order, pos, at<int32_t>(workspace, L.active),
+                                               at<int32_t>(workspace, L.err), st, gamma, eps, xn_dst)));
+    } else {
+        if (gamma) MOE_TRY(launch_rc(launch_rmsnorm(s, x, gamma, eps, xn_dst, st)));
+        MOE_TRY(do_route(s, xe, w_router, b_router, ids, w, nullptr, nullptr, workspace, st));
+        MOE_TRY(do_permute(s, ids, at<int32_t>(workspace, L.counts), offsets, order, pos, workspace, st));
+    }
+    MOE_TRY(do_grouped(s, xe, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st));
+    return launch_rc(launch_unpermute(s, y, w, pos, out, st, resid));
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
 int moe_forward(const moe_shape *shape, const void *x, const void *w_router, const float *b_router,
                 const void *w_gate, const void *w_up, const void *w_down, const moe_q4 *q4, void *out,
                 int32_t *expert_ids_out, float *weights_out, void *workspace, size_t workspace_bytes,
@@ -196,24 +235,28 @@ int moe_forward(const moe_shape *shape, const void *x, const void *w_router, con
     MOE_TRY(check_ws(s, workspace, workspace_bytes));
     if (misaligned(x) || misaligned(w_router) || misaligned(out)) return MOE_ERR_ALIGN;
     if (s.T == 0) return MOE_OK;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const WsLayout L = ws_layout(s);
-    int32_t *ids = expert_ids_out ? expert_ids_out : at<int32_t>(workspace, L.ids);
-    float *w = weights_out ? weights_out : at<float>(workspace, L.weights);
-    int32_t *offsets = at<int32_t>(workspace, L.offsets), *order = at<int32_t>(workspace, L.order),
-            *pos = at<int32_t>(workspace, L.pos);
-    void *y = at<void>(workspace, L.y);
-    if (route_fuses(s)) {
-        MOE_TRY(launch_rc(launch_route_permute(s, x, w_router, b_router, at<float>(workspace, L.logits), ids, w,
-                                               at<int>(workspace, kHdrArrivals), at<int32_t>(workspace, L.counts),
-                                               offsets, order, pos, at<int32_t>(workspace, L.active),
-                                               at<int32_t>(workspace, L.err), st)));
-    } else {
-        MOE_TRY(do_route(s, x, w_router, b_router, ids, w, nullptr, nullptr, workspace, st));
-        MOE_TRY(do_permute(s, ids, at<int32_t>(workspace, L.counts), offsets, order, pos, workspace, st));
-    }
-    MOE_TRY(do_grouped(s, x, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st));
-    return launch_rc(launch_unpermute(s, y, w, pos, out, st));
+    return forward_impl(s, x, w_router, b_router, w_gate, w_up, w_down, q4, out, expert_ids_out, weights_out,
+                        workspace, reinterpret_cast<cudaStream_t>(stream), nullptr, 0.f, nullptr, nullptr);
+}
+
+int moe_forward_rmsnorm(const moe_shape *shape, const void *hs, const void *gamma, float eps, int add_residual,
+                        const void *w_router, const float *b_router, const void *w_gate, const void *w_up,
+                        const void *w_down, const moe_q4 *q4, void *out, void *x_norm_out, int32_t *expert_ids_out,
+                        float *weights_out, void *workspace, size_t workspace_bytes, moe_stream_t stream) {
+    MOE_TRY(validate_shape(shape));
+    const moe_shape &s = *shape;
+    if (!hs || !gamma || !w_router || !out) return MOE_ERR_NULLPTR;
+    if (!(eps >= 0.f) || !(eps < INFINITY)) return MOE_ERR_SHAPE;
+    MOE_TRY(check_weights(s, w_gate, w_up, w_down, q4));
+    MOE_TRY(check_ws(s, workspace, workspace_bytes));
+    if (misaligned(hs) || misaligned(gamma) || misaligned(w_router) || misaligned(out) ||
+        (x_norm_out && misaligned(x_norm_out)))
+        return MOE_ERR_ALIGN;
+    if (s.T == 0) return MOE_OK;
+    void *xn = x_norm_out ? x_norm_out : at<void>(workspace, ws_layout(s).xn);
+    return forward_impl(s, hs, w_router, b_router, w_gate, w_up, w_down, q4, out, expert_ids_out, weights_out,
+                        workspace, reinterpret_cast<cudaStream_t>(stream), gamma, eps, xn,
+                        add_residual ? hs : nullptr);
 }
 
 int moe_forward_launches(const moe_shape *shape, int32_t *launches) {

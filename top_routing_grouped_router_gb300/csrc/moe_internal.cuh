@@ -19,7 +19,8 @@ constexpr size_t kAlign = 256;
 // 256-byte aligned.  The first 256 bytes hold the device error word and small
 // counters.
 struct WsLayout {
-    size_t err;        // int32 error word (MOE_OK / MOE_ERR_DEVICE)
+    size_t err;        // int32 error word (MOE_OK / MOE_ERR_DEVICE) in the 2 KB header
+    size_t xn;         // [T][H] pre-router RMSNorm output (act dtype), moe_forward_rmsnorm
     size_t logits;     // fp32 [T][E]
     size_t ids;        // int32 [A]
     size_t weights;    // fp32 [A]
@@ -31,7 +32,7 @@ struct WsLayout {
     size_t hist;       // int32 [chunks][E]: per-chunk expert histograms (multi-block permute)
     size_t h;          // [A][I] intermediate SwiGLU activations (fp32 or bf16)
     size_t y;          // [A][H] expert outputs in permuted order (act dtype)
-    size_t part;       // fp32 split-K partial sums of the weight-streaming path
+    size_t part;       // tensor-core paths: gathered token rows, counters, tile list
     size_t total;
 };
 
@@ -105,7 +106,9 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
 cudaError_t launch_route_permute(const moe_shape &s, const void *x, const void *wr, const float *bias,
                                  float *logits, int32_t *ids, float *w, int *arrivals, int32_t *counts,
                                  int32_t *offsets, int32_t *order, int32_t *pos, int32_t *active, int32_t *err,
-                                 cudaStream_t st);
+                                 cudaStream_t st, const void *gamma = nullptr, float eps = 0.f, void *xn = nullptr);
+cudaError_t launch_rmsnorm(const moe_shape &s, const void *x, const void *gamma, float eps, void *xn,
+                           cudaStream_t st);
 cudaError_t launch_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t *offsets,
                            int32_t *order, int32_t *pos, int32_t *active, int32_t *hist, int32_t *err,
                            cudaStream_t st);
@@ -119,6 +122,6 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
                       const void *wg, const void *wu, const void *wd, const moe_q4 *q4, float *part, void *h, void *y,
                       int32_t *err, cudaStream_t st);
 cudaError_t launch_unpermute(const moe_shape &s, const void *y, const float *w, const int32_t *pos, void *out,
-                             cudaStream_t st);
+                             cudaStream_t st, const void *resid = nullptr);
 
 }  // namespace moe

@@ -40,6 +40,10 @@ template <> struct Vec<float> {
         float4 v = __ldg(reinterpret_cast<const float4 *>(p));
         out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
     }
+    __device__ static void store(float *p, const float *v) {
+        *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __device__ static float round(float v) { return v; }
 };
 template <> struct Vec<uint16_t> {
     static constexpr int N = 8;
@@ -52,20 +56,76 @@ template <> struct Vec<uint16_t> {
             out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
         }
     }
+    // v already bf16-representable (see round)
+    __device__ static void store(uint16_t *p, const float *v) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = (__float_as_uint(v[2 * i]) >> 16) | (__float_as_uint(v[2 * i + 1]) & 0xffff0000u);
+        *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __device__ static float round(float v) { return __uint_as_float(uint32_t(f32_to_bf16_bits(v)) << 16); }
 };
+
+// Pre-router RMSNorm (Qwen3 decoder, post-attention norm): xn = (hs / rms) * gamma with
+// rms = sqrt(mean(hs^2) + eps), computed in fp32 and rounded once to the activation dtype;
+// the router and the experts read xn.
+struct NormArgs {
+    const void *gamma;   // [H] activation dtype, or null: no norm (x is read as is)
+    float eps;
+    void *xn;            // [T][H] activation dtype, written by the expert-block-0 column
+};
+
+// Sum of squares of the 8 tokens [tg, tg + nt) of this block's group, into s_rs as
+// 1 / rms... kept as rms (the division happens per element).
+template <typename ActT>
+__device__ void group_rms(const ActT *__restrict__ x, int H, float eps, int tg, int nt, float (*s_part)[kEPB * kTG],
+                          float *s_rms) {
+    constexpr int V = Vec<ActT>::N;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    float ss[kTG];
+#pragma unroll
+    for (int j = 0; j < kTG; ++j) ss[j] = 0.f;
+    for (int c = tid; c < H / V; c += kRThreads) {
+#pragma unroll
+        for (int tt = 0; tt < kTG; ++tt)
+            if (tt < nt) {
+                float xv[V];
+                Vec<ActT>::load(x + (size_t)(tg + tt) * H + (size_t)c * V, xv);
+#pragma unroll
+                for (int v = 0; v < V; ++v) ss[tt] = fmaf(xv[v], xv[v], ss[tt]);
+            }
+    }
+#pragma unroll
+    for (int tt = 0; tt < kTG; ++tt) {
+        const float r = warp_sum(ss[tt]);
+        if (lane == 0) s_part[w][tt] = r;
+    }
+    __syncthreads();
+    if (tid < kTG) {
+        float r = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kRWarps; ++w2) r += s_part[w2][tid];
+        s_rms[tid] = sqrtf(r / float(H) + eps);
+    }
+    __syncthreads();
+}
 
 // logits[t][e] for e in [e0, e0+4) and t in [t0, t0+8), t < T.
 template <typename ActT>
 __device__ void router_block(const ActT *__restrict__ x, const ActT *__restrict__ wr, const float *__restrict__ bias,
                              float *__restrict__ logits, int T, int H, int E, int e0, int t0,
-                             float (*s_part)[kEPB * kTG]) {
+                             float (*s_part)[kEPB * kTG], const NormArgs &nm, float *s_rms) {
     constexpr int V = Vec<ActT>::N;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int nchunk = H / V;
     const int ne = min(kEPB, E - e0);
     const int tend = min(T, t0 + kTPB);
+    const ActT *gamma = static_cast<const ActT *>(nm.gamma);
+    ActT *xn = e0 == 0 ? static_cast<ActT *>(nm.xn) : nullptr;
     for (int tg = t0; tg < tend; tg += kTG) {
         const int nt = min(kTG, T - tg);
+        if (gamma) group_rms<ActT>(x, H, nm.eps, tg, nt, s_part, s_rms);
         float acc[kEPB][kTG];
 #pragma unroll
         for (int i = 0; i < kEPB; ++i)
@@ -80,11 +140,19 @@ __device__ void router_block(const ActT *__restrict__ x, const ActT *__restrict_
 #pragma unroll
                     for (int v = 0; v < V; ++v) wv[ee][v] = 0.f;
             }
+            float gv[V];
+            if (gamma) Vec<ActT>::load(gamma + (size_t)c * V, gv);
 #pragma unroll
             for (int tt = 0; tt < kTG; ++tt) {
                 if (tt < nt) {
                     float xv[V];
                     Vec<ActT>::load(x + (size_t)(tg + tt) * H + (size_t)c * V, xv);
+                    if (gamma) {
+                        const float rms = s_rms[tt];
+#pragma unroll
+                        for (int v = 0; v < V; ++v) xv[v] = Vec<ActT>::round(__fdiv_rn(xv[v], rms) * gv[v]);
+                        if (xn) Vec<ActT>::store(xn + (size_t)(tg + tt) * H + (size_t)c * V, xv);
+                    }
 #pragma unroll
                     for (int ee = 0; ee < kEPB; ++ee)
 #pragma unroll
@@ -185,16 +253,19 @@ struct RouteArgs {
     int *arrivals;            // workspace counters [1 + kMaxGroups], zero between launches
     int fuse;                 // 0: logits only, 1: + top-k, 2: + top-k + permutation
     int32_t *counts, *offsets, *order, *pos, *active, *err;
+    NormArgs norm_in;         // optional pre-router RMSNorm of x
 };
 
 template <typename ActT>
 __global__ void __launch_bounds__(kRThreads)
 route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const float *__restrict__ bias, RouteArgs a) {
     __shared__ float s_part[kRWarps][kEPB * kTG];
+    __shared__ float s_rms[kTG];
     __shared__ int s_last;
     griddep_launch_dependents();
     griddep_wait();  // the previous kernel in the stream may still read this workspace
-    router_block<ActT>(x, wr, bias, a.logits, a.T, a.H, a.E, blockIdx.x * kEPB, blockIdx.y * kTPB, s_part);
+    router_block<ActT>(x, wr, bias, a.logits, a.T, a.H, a.E, blockIdx.x * kEPB, blockIdx.y * kTPB, s_part, a.norm_in,
+                       s_rms);
     if (!a.fuse) return;
     // the last expert block of this token group to finish sees all its logits: top-k,
     // one warp per token
@@ -231,6 +302,40 @@ topk_kernel(const float *__restrict__ logits, int T, int E, int k, int norm, int
     if (t < T) topk_token(logits, t, E, k, norm, ids, w, margin);
 }
 
+// Pre-router RMSNorm for batches routed without the fused kernel: one block per token.
+template <typename ActT>
+__global__ void __launch_bounds__(kRThreads)
+rmsnorm_kernel(const ActT *__restrict__ x, const ActT *__restrict__ gamma, float eps, int H, ActT *__restrict__ xn) {
+    constexpr int V = Vec<ActT>::N;
+    __shared__ float s_part[kRWarps];
+    griddep_launch_dependents();
+    griddep_wait();
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const ActT *row = x + (size_t)t * H;
+    float ss = 0.f;
+    for (int c = tid; c < H / V; c += kRThreads) {
+        float xv[V];
+        Vec<ActT>::load(row + (size_t)c * V, xv);
+#pragma unroll
+        for (int v = 0; v < V; ++v) ss = fmaf(xv[v], xv[v], ss);
+    }
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) s_part[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < kRWarps; ++w2) tot += s_part[w2];
+    const float rms = sqrtf(tot / float(H) + eps);
+    for (int c = tid; c < H / V; c += kRThreads) {
+        float xv[V], gv[V];
+        Vec<ActT>::load(row + (size_t)c * V, xv);
+        Vec<ActT>::load(gamma + (size_t)c * V, gv);
+#pragma unroll
+        for (int v = 0; v < V; ++v) xv[v] = Vec<ActT>::round(__fdiv_rn(xv[v], rms) * gv[v]);
+        Vec<ActT>::store(xn + (size_t)t * H + (size_t)c * V, xv);
+    }
+}
+
 cudaError_t launch_route_kernel(const moe_shape &s, const void *x, const void *wr, const float *bias,
                                 const RouteArgs &a, cudaStream_t st) {
     dim3 grid((s.E + kEPB - 1) / kEPB, (s.T + kTPB - 1) / kTPB);
@@ -252,7 +357,7 @@ cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, cons
                          int32_t *ids, float *w, float *margin, int *arrivals, int32_t *err, cudaStream_t st) {
     if (s.T == 0) return cudaSuccess;
     RouteArgs a{logits, s.T, s.H, s.E, s.k, s.norm_topk, ids, w, margin, arrivals, route_fuses(s) ? 1 : 0,
-                nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+                nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, NormArgs{nullptr, 0.f, nullptr}};
     // large bf16 batches: the router GEMM on the tensor cores, then a top-k launch
     cudaError_t e = (!a.fuse && router_tc_supported(s)) ? launch_router_tc(s, x, wr, bias, logits, err, st)
                                                        : launch_route_kernel(s, x, wr, bias, a, st);
@@ -265,10 +370,21 @@ cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, cons
 cudaError_t launch_route_permute(const moe_shape &s, const void *x, const void *wr, const float *bias,
                                  float *logits, int32_t *ids, float *w, int *arrivals, int32_t *counts,
                                  int32_t *offsets, int32_t *order, int32_t *pos, int32_t *active, int32_t *err,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, const void *gamma, float eps, void *xn) {
     RouteArgs a{logits, s.T, s.H, s.E, s.k, s.norm_topk, ids, w, nullptr, arrivals, 2,
-                counts, offsets, order, pos, active, err};
+                counts, offsets, order, pos, active, err, NormArgs{gamma, eps, xn}};
     return launch_route_kernel(s, x, wr, bias, a, st);
+}
+
+// xn = RMSNorm(x) * gamma for every token (the unfused pre-router norm).
+cudaError_t launch_rmsnorm(const moe_shape &s, const void *x, const void *gamma, float eps, void *xn,
+                           cudaStream_t st) {
+    if (s.T == 0) return cudaSuccess;
+    if (s.act_dtype == MOE_DT_F32)
+        return launch_pdl(rmsnorm_kernel<float>, dim3(s.T), dim3(kRThreads), 0, st, static_cast<const float *>(x),
+                          static_cast<const float *>(gamma), eps, s.H, static_cast<float *>(xn));
+    return launch_pdl(rmsnorm_kernel<uint16_t>, dim3(s.T), dim3(kRThreads), 0, st, static_cast<const uint16_t *>(x),
+                      static_cast<const uint16_t *>(gamma), eps, s.H, static_cast<uint16_t *>(xn));
 }
 
 }  // namespace moe

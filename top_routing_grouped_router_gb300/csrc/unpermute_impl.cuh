@@ -35,9 +35,11 @@ __device__ __forceinline__ void unp_store8(uint16_t *p, const float *v) {
 }
 
 // Columns [c0, c0 + 8) of token t.  A slot whose pos is outside [0, A) contributes nothing.
+// With a residual stream `resid` ([T][H], may be null) the sum is added to it before the
+// single rounding: out = resid + sum_j w_j y_j.
 template <typename T>
 __device__ __forceinline__ void unpermute8(const T *y, const float *w, const int32_t *pos, T *out, int t, int c0,
-                                           int k, int H, int A) {
+                                           int k, int H, int A, const T *resid = nullptr) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -49,6 +51,12 @@ __device__ __forceinline__ void unpermute8(const T *y, const float *w, const int
         unp_load8(y + (size_t)p * H + c0, v);
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = fmaf(wt, v[i], acc[i]);
+    }
+    if (resid) {
+        float r[8];
+        unp_load8(resid + (size_t)t * H + c0, r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = r[i] + acc[i];
     }
     unp_store8(out + (size_t)t * H + c0, acc);
 }
