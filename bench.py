@@ -38,6 +38,7 @@ DESCR = {
     "decode64z": "Qwen3-30B-A3B MoE layer decode, bf16, Zipf(1.1) router bias: T=64 H=2048 E=128 k=8 I=768",
     "decode48q": "Qwen3-30B-A3B MoE layer decode, 4-bit codebook expert weights: T=48 H=2048 E=128 k=8 I=768",
     "prefill": "Qwen3-30B-A3B MoE layer prefill, bf16: 4 independent layers x T=4096 H=2048 E=128 k=8 I=768",
+    "prefill4q": "Qwen3-30B-A3B MoE layer prefill, 4-bit codebook expert weights: T=4096 H=2048 E=128 k=8 I=768",
 }
 
 
@@ -52,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--copies", type=int, default=0, help="weight copies to rotate (0 = automatic)")
     ap.add_argument("--layers", type=int, default=0, help="use only the first N layers (profiling; 0 = all)")
+    ap.add_argument("--entry", choices=["forward", "rmsnorm"], default="forward",
+                    help="moe_forward, or moe_forward_rmsnorm (pre-router RMSNorm and residual fused in)")
     return ap.parse_args()
 
 
@@ -219,6 +222,7 @@ def run_ours(args, rank, world, local):
     import top_routing_grouped_router_gb300 as moe
     from top_routing_grouped_router_gb300 import build as moe_build
     from top_routing_grouped_router_gb300.device import upload, to_device
+    import synth
 
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA GPU")
@@ -247,10 +251,16 @@ def run_ours(args, rank, world, local):
     wss = [d.new_workspace() for d in dl[0]]
     stream = torch.cuda.Stream(device=dev)
 
+    gammas = [to_device(synth.make_norm_weight(l.H, l.act, seed=l.T, layer=i), dev) for i, l in enumerate(layers)]
+
     def forward(c, st=None):
         for l, L in enumerate(dl[c]):
-            moe.moe_forward(L.shape, L.x, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4, outs[l],
-                            workspace=wss[l], stream=st)
+            if args.entry == "rmsnorm":
+                moe.moe_forward_rmsnorm(L.shape, L.x, gammas[l], 1e-6, L.w_router, L.b_router, L.w_gate, L.w_up,
+                                        L.w_down, L.q4, outs[l], workspace=wss[l], stream=st)
+            else:
+                moe.moe_forward(L.shape, L.x, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4, outs[l],
+                                workspace=wss[l], stream=st)
 
     with torch.cuda.stream(stream):
         for c in range(n_copies):
@@ -366,7 +376,7 @@ def run_ours(args, rank, world, local):
     bo = sum(o.numel() * o.element_size() for o in out_host)
 
     launches = sum(moe.moe_forward_launches(L.shape) for L in dl[0])
-    tensor_bound = args.workload == "prefill"
+    tensor_bound = args.workload.startswith("prefill")
     if tensor_bound:
         peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
         achieved = flops / (k_ms / 1e3) / 1e12
@@ -391,7 +401,8 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if inp0.act == "bf16" else "f32",
         "data": "synthetic: seeded N(0,1) tokens, N(0,1/fan_in) random-init weights of the model's shapes",
-        "config": {"workload": DESCR[args.workload], "T": T, "H": H, "E": E, "k": k, "I": I,
+        "config": {"workload": DESCR[args.workload], "entry": f"moe_{args.entry}" if args.entry == "forward" else
+                   "moe_forward_rmsnorm (pre-router RMSNorm + residual fused)", "T": T, "H": H, "E": E, "k": k, "I": I,
                    "layers": len(layers), "weights": inp0.w, "active_experts": n_active,
                    "l2": f"inputs larger than L2: {n_copies} rotating weight cop{'y' if n_copies == 1 else 'ies'} "
                          f"({n_copies * per_copy / 1e9:.1f} GB), one moe_forward graph per copy",

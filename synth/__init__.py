@@ -48,6 +48,7 @@ WORKLOADS = {
     "decode64z": dict(T=64,   H=2048, E=128, k=8, I=768, act="bf16", w="bf16", zipf=True,  layers=1, seed=2),
     "decode48q": dict(T=48,   H=2048, E=128, k=8, I=768, act="bf16", w="q4",   zipf=False, layers=1, seed=3),
     "prefill":   dict(T=4096, H=2048, E=128, k=8, I=768, act="bf16", w="bf16", zipf=False, layers=4, seed=4),
+    "prefill4q": dict(T=4096, H=2048, E=128, k=8, I=768, act="bf16", w="q4",   zipf=False, layers=1, seed=5),
 }
 
 _TENSOR_IDS = {"x": 1, "w_router": 2, "gate": 3, "up": 4, "down": 5, "perm": 6}

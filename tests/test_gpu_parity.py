@@ -41,6 +41,11 @@ def test_decode48_q4_full_size():
     check_layer(synth.make_inputs("decode48q"), full_oracle=False, n_sample_tokens=12, n_sample_rows=24)
 
 
+def test_prefill_q4_full_size():
+    s, g = check_layer(synth.make_inputs("prefill4q"), full_oracle=False, n_sample_tokens=10, n_sample_rows=16)
+    assert g["counts"].sum() == 4096 * 8
+
+
 @pytest.mark.parametrize("layer", [0, 1, 2, 3])
 def test_prefill_full_size_layer(layer):
     s, g = check_layer(synth.make_inputs("prefill", layer=layer), full_oracle=False, n_sample_tokens=12,
@@ -59,6 +64,8 @@ def test_prefill_full_size_layer(layer):
     (64, 384, 8, 2, 256, "bf16", "q4", True),        # 4-bit, skewed load, three row blocks of H
     (600, 512, 16, 4, 256, "bf16", "bf16", False),   # large batch: several token chunks per expert
     (1030, 512, 8, 2, 384, "bf16", "bf16", True),    # large batch, skewed load: ragged chunks
+    (200, 256, 16, 4, 128, "bf16", "q4", False),     # 4-bit large batch: several 128-token chunks per expert
+    (300, 512, 8, 2, 256, "bf16", "q4", True),       # 4-bit large batch, skewed load
 ])
 def test_reduced_and_ragged_cases(T, H, E, k, I, act, w, zipf):
     inp = synth.make_custom(T, H, E, k, I, act=act, w=w, zipf=zipf, seed=T + E, name=f"custom{T}")

@@ -1,5 +1,6 @@
-// grouped_q4.cu -- grouped SwiGLU experts with 4-bit codebook weights at decode batch
-// sizes (<= 64 tokens per expert), on the tensor cores.
+// grouped_q4.cu -- grouped SwiGLU experts with 4-bit codebook weights on the tensor
+// cores, for decode batches (an expert's tokens in one tile of <= 64) and large batches
+// (an expert's tokens in chunks of 128).
 //
 // Weight format: element (e, r, c) of a [rows][in] matrix is codebook[code] * scale,
 // code = nibble c of row r (element 2i low, 2i+1 high nibble of byte i), one bf16
@@ -9,7 +10,8 @@
 //
 // Pipeline per CTA (one per SM):
 //  * warp 0 lane 0: TMA loads of the packed codes (128 rows x 32 bytes per matrix and
-//    64-element slab, unswizzled) and of the token rows into a 6-deep "raw" ring, and
+//    64-element slab, unswizzled) and of the token rows into a "raw" ring (6 stages
+//    with room for 64 token rows, or 4 with room for 128), and
 //    a bulk copy of each tile's block scales (contiguous for 128 consecutive rows) into
 //    one of two per-tile scale buffers;
 //  * warps 6-13 (dequant): turn one slab of codes into bf16 weights in the 128-byte
@@ -25,6 +27,7 @@
 // care about the order of k as long as both operands share it: the token rows (x_perm,
 // built here) and the intermediate h (written by the gate/up epilogue) are stored in
 // the same order.
+#include "grouped_tiles.cuh"
 #include "moe_internal.cuh"
 #include "tc_common.cuh"
 
@@ -37,14 +40,11 @@ namespace {
 using namespace tc;
 
 constexpr int kRows = 128;                  // weight rows per tile (MMA M)
-constexpr int kMaxN = 64;                   // tokens per tile
 constexpr int kSlab = 64;                   // k elements per slab
 constexpr int kNBox = 16;
-constexpr int kRawStages = 6;
 constexpr int kAStages = 3;
 constexpr int kCodeBytes = kRows * kSlab / 2;  // 4 KB: one matrix slab of codes
-constexpr int kRawBytes = 16384;               // two code slabs (8 KB) + token rows (8 KB)
-constexpr int kRawTok = 8192;                  // offset of the token rows in a raw stage
+constexpr int kRawTok = 8192;                  // offset of the token rows in a raw stage (after two code slabs)
 constexpr int kABytes = kRows * 128;           // 16 KB bf16 slab
 constexpr int kAStageBytes = 2 * kABytes;
 constexpr int kTmemCols = 512;
@@ -56,14 +56,17 @@ constexpr int kDeqThreads = kDeqWarps * 32;
 constexpr int kThreads = (2 + kEpiWarps + kDeqWarps) * 32;
 constexpr int kMetaRing = 8;
 constexpr int kScaleBytes = 2 * 8192;          // one tile's block scales: 2 matrices x 128 rows x <= 32 blocks
-constexpr int kSmemBytes = kRawStages * kRawBytes + kAStages * kAStageBytes + 2 * kScaleBytes + 1024 + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory");
+// Ring shape: token rows per tile (MaxN) and raw stages.
+template <int MaxN, int RawStages>
+struct QCfg {
+    static constexpr int kRawBytes = kRawTok + MaxN * 128;
+    static constexpr int kSmemBytes = RawStages * kRawBytes + kAStages * kAStageBytes + 2 * kScaleBytes + 1024 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+constexpr int kDecodeMaxN = 64;   // decode: an expert's tokens fit one tile
+constexpr int kChunkN = 128;      // large batches: token chunks of 128
 
 enum : int { kGateUp = 0, kDown = 1 };
-
-__host__ __device__ constexpr uint32_t pack_tile(int down, int e, int rb) {
-    return (uint32_t(down) << 31) | (uint32_t(e) << 16) | (uint32_t(rb) << 8);
-}
 
 struct Params {
     const int32_t *offsets;
@@ -78,6 +81,7 @@ struct Params {
     float half_b;                   // b / 2
     uint32_t centre2;               // bf16x2 of 128 + 2*j0
     int E, H, I, A;
+    int cmax;                       // token chunk (fixed chunks of cmax, see chunk_base)
 };
 
 // The 8-element group order of the weights: position q holds element kSigma[q].
@@ -120,10 +124,13 @@ __device__ __forceinline__ uint32_t gamma_pair(uint16_t scale, float half_b) {
     return g | (g << 16);
 }
 
+template <int MaxN, int kRawStages>
 __global__ void __launch_bounds__(kThreads, 1)
 q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constant__ CUtensorMap tm_uc,
                  const __grid_constant__ CUtensorMap tm_dc, const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_h, const Params p) {
+    constexpr int kRawBytes = QCfg<MaxN, kRawStages>::kRawBytes;
+    constexpr int kHalfTok = (MaxN / 2) * 128;  // second token half of a two-slab down stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *raw = smem;
@@ -197,17 +204,20 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             next = atomicAdd(p.tile_counter, 1);
             const uint32_t entry = __ldg(p.tiles + t);
             const int down = int(entry >> 31), e0 = int((entry >> 16) & 0xFF), rb = int((entry >> 8) & 0xFF);
+            const int nc = int(entry & 0xFF);
             const int e = min(e0, p.E - 1);
             const int off = __ldg(p.offsets + e);
-            int m = __ldg(p.offsets + e + 1) - off;
-            if (e0 >= p.E || off < 0 || m <= 0 || m > kMaxN || off + m > p.A) {
+            const int me = __ldg(p.offsets + e + 1) - off;
+            const int base = chunk_base(me, p.cmax, false);
+            int m = min(base, me - nc * base);
+            if (e0 >= p.E || off < 0 || me <= 0 || off + me > p.A || m <= 0 || m > MaxN) {
                 record_error(p.err, MOE_ERR_DEVICE);
                 m = 0;
             }
-            const int r0 = m > 0 ? off : 0;
+            const int r0 = m > 0 ? off + nc * base : 0;
             const int N = m > 0 ? (m + 15) & ~15 : 16;
             if (down) {
-                const int need = (p.I / kRows) * kEpiWarps;
+                const int need = (p.I / kRows) * n_chunks(me, p.cmax, false) * kEpiWarps;
                 wait_count(p.done + e, need, p.err, abort);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
@@ -241,7 +251,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 }
                 ++tiles_done;
             }
-            const int two = down && N <= kMaxN / 2 && nslab % 2 == 0;
+            const int two = down && N <= MaxN / 2 && nslab % 2 == 0;
             const int nstage = two ? nslab / 2 : nslab;
             const int nbox = N / kNBox;
             const uint32_t bytes = (down && !two ? kCodeBytes : 2 * kCodeBytes) + (two ? 2 : 1) * nbox * kNBox * 128;
@@ -268,7 +278,8 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                         const int s2 = 2 * ks + h2;
                         tma_load_2d(base + h2 * kCodeBytes, &tm_dc, s2 * (kSlab / 2), wrow, fb);
                         for (int q = 0; q < nbox; ++q)
-                            tma_load_2d(base + kRawTok + h2 * 4096 + q * 2048, &tm_h, s2 * kSlab, r0 + q * kNBox, fb);
+                            tma_load_2d(base + kRawTok + h2 * kHalfTok + q * 2048, &tm_h, s2 * kSlab, r0 + q * kNBox,
+                                        fb);
                     }
                 } else {
                     tma_load_2d(base, &tm_dc, ks * (kSlab / 2), wrow, fb);
@@ -359,7 +370,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 for (int h2 = 0; h2 < 1 + two; ++h2)
 #pragma unroll
                     for (int kk = 0; kk < kSlab / 16; ++kk)
-                        mma_bf16(d, smem_desc(a0 + h2 * kABytes + kk * 32), smem_desc(bb + h2 * 4096 + kk * 32), idesc,
+                        mma_bf16(d, smem_desc(a0 + h2 * kABytes + kk * 32), smem_desc(bb + h2 * kHalfTok + kk * 32), idesc,
                                  (ks | h2 | kk) != 0);
             }
             mma_commit(smem_u32(&aempty[a]));
@@ -437,12 +448,12 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 }
 
 // x_perm[p] = x[order[p] / k] with every 8-element group in the weights' order
-// (0,4,1,5,2,6,3,7).  Block 0 builds the tile list (one token chunk per expert) and
-// clears the scheduling counters.
+// (0,4,1,5,2,6,3,7).  Block 0 builds the tile list (an expert's tokens in fixed chunks of
+// cmax; all gate/up tiles before all down tiles) and clears the scheduling counters.
 __global__ void __launch_bounds__(256)
 q4_prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
-               int T, int k, int H, int I, int E, uint16_t *__restrict__ x_perm, uint32_t *tiles, int *n_tiles,
-               int *tile_counter, int *done, int32_t *err) {
+               int T, int k, int H, int I, int E, int cmax, int max_tiles, uint16_t *__restrict__ x_perm,
+               uint32_t *tiles, int *n_tiles, int *tile_counter, int *done, int32_t *err) {
     griddep_launch_dependents();
     griddep_wait();
     if (blockIdx.x > 0) {
@@ -464,43 +475,54 @@ q4_prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order
         }
         return;
     }
-    __shared__ int s_n[kMaxE + 1];
-    if (threadIdx.x == 0) {
-        int n = 0;
-        for (int e = 0; e < E; ++e) {
-            s_n[e] = n;
-            if (offsets[e + 1] > offsets[e]) ++n;
+    __shared__ int s_warp[9];
+    const int e = threadIdx.x;
+    int me = 0;
+    if (e < E) {
+        me = min(max(offsets[e + 1] - offsets[e], 0), T * k);
+        done[e] = 0;
+    }
+    const int nch = n_chunks(me, cmax, false);
+    const int gu_per = I / kRows, dn_per = H / kRows;
+    int n_gu, n_dn;
+    const int gu_off = scan256(nch * gu_per, s_warp, n_gu);
+    const int dn_off = scan256(nch * dn_per, s_warp, n_dn);
+    for (int c = 0; c < nch; ++c) {
+        for (int r = 0; r < gu_per; ++r) {
+            const int i = gu_off + c * gu_per + r;
+            if (i < max_tiles) tiles[i] = pack_tile(0, e, r, c);
         }
-        s_n[E] = n;
+        for (int r = 0; r < dn_per; ++r) {
+            const int i = n_gu + dn_off + c * dn_per + r;
+            if (i < max_tiles) tiles[i] = pack_tile(1, e, r, c);
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (n_gu + n_dn > max_tiles) record_error(err, MOE_ERR_DEVICE);  // inconsistent offsets
+        *n_tiles = min(n_gu + n_dn, max_tiles);
         *tile_counter = 0;
     }
-    __syncthreads();
-    const int n_act = s_n[E];
-    const int gu_per = I / kRows, dn_per = H / kRows;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        done[e] = 0;
-        if (offsets[e + 1] > offsets[e]) {
-            const int i = s_n[e];
-            for (int r = 0; r < gu_per; ++r) tiles[i * gu_per + r] = pack_tile(0, e, r);
-            for (int r = 0; r < dn_per; ++r) tiles[n_act * gu_per + i * dn_per + r] = pack_tile(1, e, r);
-        }
-    }
-    if (threadIdx.x == 0) *n_tiles = n_act * (gu_per + dn_per);
 }
 
 size_t xperm_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * s.H * 2 + 255) / 256 * 256; }
 
+template <int MaxN, int RawStages>
 bool set_attr() {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(q4_swiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(q4_swiglu_kernel<MaxN, RawStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 QCfg<MaxN, RawStages>::kSmemBytes) != cudaSuccess)
             return false;
         attr_set[dev] = true;
     }
     return true;
+}
+
+size_t q4_max_tiles(const moe_shape &s) {
+    const size_t chunks = (size_t)s.E + ((size_t)s.T * s.k + kDecodeMaxN - 1) / kDecodeMaxN;
+    return chunks * (size_t)(s.I / kRows + s.H / kRows);
 }
 
 }  // namespace
@@ -522,7 +544,7 @@ bool q4_codebook_affine(const float *cb, float *b_out, int *twice_j0) {
     return true;
 }
 
-constexpr int kQ4MaxT = kMaxN;
+constexpr int kQ4MaxT = 8192;  // token chunk index fits the tile entry's 8 bits
 
 bool q4_path_supported(const moe_shape &s) {
     // a tile's scales (128 rows x in/64 bf16 per matrix) must fit one 8 KB half of a scale buffer
@@ -531,8 +553,7 @@ bool q4_path_supported(const moe_shape &s) {
 }
 
 size_t q4_part_bytes(const moe_shape &s) {
-    const size_t tiles = (size_t)s.E * (s.I / kRows + s.H / kRows);
-    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (tiles * 4 + 255) / 256 * 256;
+    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (q4_max_tiles(s) * 4 + 255) / 256 * 256;
 }
 
 cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
@@ -555,10 +576,13 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
         !make_map(&mx, x_perm, A, s.H, kNBox) || !make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
 
+    const bool decode = s.T <= kDecodeMaxN;
+    const int cmax = decode ? kDecodeMaxN : kChunkN;
     cudaError_t e = launch_pdl(q4_prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
-                               offsets, s.T, s.k, s.H, s.I, s.E, x_perm, tiles, n_tiles, tile_counter, done, err);
+                               offsets, s.T, s.k, s.H, s.I, s.E, cmax, (int)q4_max_tiles(s), x_perm, tiles, n_tiles,
+                               tile_counter, done, err);
     if (e != cudaSuccess) return e;
-    if (!set_attr()) return cudaErrorInvalidValue;
+    if (!(decode ? set_attr<kDecodeMaxN, 6>() : set_attr<kChunkN, 4>())) return cudaErrorInvalidValue;
     Params prm{};
     prm.offsets = offsets;
     prm.tiles = tiles;
@@ -581,7 +605,12 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     prm.H = s.H;
     prm.I = s.I;
     prm.A = A;
-    return launch_pdl(q4_swiglu_kernel, dim3(sm_count()), dim3(kThreads), kSmemBytes, st, mg, mu, md, mx, mh, prm);
+    prm.cmax = cmax;
+    if (decode)
+        return launch_pdl(q4_swiglu_kernel<kDecodeMaxN, 6>, dim3(sm_count()), dim3(kThreads),
+                          QCfg<kDecodeMaxN, 6>::kSmemBytes, st, mg, mu, md, mx, mh, prm);
+    return launch_pdl(q4_swiglu_kernel<kChunkN, 4>, dim3(sm_count()), dim3(kThreads), QCfg<kChunkN, 4>::kSmemBytes, st,
+                      mg, mu, md, mx, mh, prm);
 }
 
 }  // namespace moe
