@@ -31,6 +31,19 @@ _LIB = os.path.join(_HERE, "libmoe_oracle.so")
 _DT = {"f32": 0, "bf16": 1, "q4": 2}
 
 
+class _Lora(ctypes.Structure):
+    _fields_ = [
+        ("rank", ctypes.c_int32),
+        ("scale", ctypes.c_double),
+        ("a_gate", ctypes.c_void_p),
+        ("b_gate", ctypes.c_void_p),
+        ("a_up", ctypes.c_void_p),
+        ("b_up", ctypes.c_void_p),
+        ("a_down", ctypes.c_void_p),
+        ("b_down", ctypes.c_void_p),
+    ]
+
+
 class _Matrix(ctypes.Structure):
     _fields_ = [
         ("dtype", ctypes.c_int32),
@@ -277,4 +290,32 @@ def forward_prenorm_tokens(inp, gamma: np.ndarray, eps: float, tokens: Sequence[
     if residual:
         r["out"] = r["out"] + _widen(inp, inp.x[np.asarray(tokens)])
     r["xn"], r["xn_act"] = xn, x_act
+    return r
+
+
+def _lora_struct(lora: dict, keep: list) -> _Lora:
+    arrs = {n: np.ascontiguousarray(lora[n], dtype=np.float32) for n in
+            ("a_gate", "b_gate", "a_up", "b_up", "a_down", "b_down")}
+    keep.append(arrs)
+    return _Lora(int(lora["rank"]), float(lora["scale"]), *[_p(arrs[n]) for n in
+                                                            ("a_gate", "b_gate", "a_up", "b_up", "a_down", "b_down")])
+
+
+def forward_lora(inp, lora: dict, tokens: Optional[Sequence[int]] = None) -> dict:
+    """The block with LoRA adapters on the three expert projections (fp32 adapters, all math in
+    double): z = x . W^T + scale * (x . A^T) . B^T for gate, up and down.  ``lora`` holds rank,
+    scale and a_gate [E][r][H], b_gate [E][I][r], a_up, b_up (same), a_down [E][r][I],
+    b_down [E][H][r].  Evaluates ``tokens`` (default: all), each on its own."""
+    g, u, d, keep = _mats(inp)
+    L = _lora_struct(lora, keep)
+    toks = np.ascontiguousarray(np.arange(inp.T, dtype=np.int32) if tokens is None
+                                else np.asarray(tokens, dtype=np.int32))
+    n, k = toks.size, inp.k
+    r = dict(tokens=toks, ids=np.empty((n, k), np.int32), weights=np.empty((n, k)), tie_margin=np.empty(n),
+             out=np.empty((n, inp.H)))
+    x, wr, b = np.ascontiguousarray(inp.x), np.ascontiguousarray(inp.w_router), _bias(inp)
+    _check(lib().orc_forward_tokens_lora(
+        n, _p(toks), inp.H, inp.E, k, inp.I, int(inp.norm_topk), _DT[inp.act], _p(x), _p(wr), _p(b),
+        ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), ctypes.byref(L),
+        _p(r["ids"]), _p(r["weights"]), _p(r["tie_margin"]), _p(r["out"])), "forward_tokens_lora")
     return r

@@ -183,29 +183,83 @@ int orc_permute(int A, int E, const int32_t *ids, int32_t *counts, int32_t *offs
     return 0;
 }
 
-/* Steps E and F for one activation row and one expert. h may be NULL. */
-int orc_expert_mlp(int H, int I, const double *xrow, int e, const orc_matrix *w_gate,
-                   const orc_matrix *w_up, const orc_matrix *w_down, double *h, double *y)
+/*
+ * LoRA adapters on the experts: rank r, fp32, one (A, B) pair per expert and
+ * projection, adding scale * B A to the projection's weight:
+ *   W'_P[e] = W_P[e] + scale * B_P[e] A_P[e],  A_P [E][r][in], B_P [E][out][r],
+ * i.e. z = x . W_P[e]^T + scale * (x . A_P[e]^T) . B_P[e]^T.  The unsloth commit page
+ * 4f2bfe7f69 benchmarks the model with a rank-16 LoRA on 4-bit weights and names
+ * "4bit forward, fp32 LoRA injection" as the inference form; it gives no placement,
+ * so the adapters sit on the three expert projections (gate, up, down).
+ */
+typedef struct {
+    int32_t rank;
+    double scale;
+    const float *a_gate, *b_gate, *a_up, *b_up, *a_down, *b_down;
+} orc_lora;
+
+/* scale * sum_q B[e][row][q] * v[q] */
+static double lora_out(const orc_lora *l, const float *B, int e, int64_t rows, int64_t row, const double *v)
+{
+    double s = 0.0;
+    for (int q = 0; q < l->rank; ++q) s += (double)B[((int64_t)e * rows + row) * l->rank + q] * v[q];
+    return l->scale * s;
+}
+
+/* v[q] = sum_c A[e][q][c] * x[c] */
+static void lora_in(const orc_lora *l, const float *A, int e, int64_t cols, const double *x, double *v)
+{
+    for (int q = 0; q < l->rank; ++q) {
+        double s = 0.0;
+        for (int64_t c = 0; c < cols; ++c) s += (double)A[((int64_t)e * l->rank + q) * cols + c] * x[c];
+        v[q] = s;
+    }
+}
+
+/* Steps E and F for one activation row and one expert, with optional adapters. */
+static int expert_mlp(int H, int I, const double *xrow, int e, const orc_matrix *w_gate, const orc_matrix *w_up,
+                      const orc_matrix *w_down, const orc_lora *lora, double *h, double *y)
 {
     if (H <= 0 || I <= 0 || !xrow || !y || e < 0) return -1;
     if (check_matrix(w_gate, I, H) || check_matrix(w_up, I, H) || check_matrix(w_down, H, I)) return -1;
+    if (lora && (lora->rank < 1 || lora->rank > 64 || !lora->a_gate || !lora->b_gate || !lora->a_up ||
+                 !lora->b_up || !lora->a_down || !lora->b_down))
+        return -1;
     double *hh = h ? h : (double *)malloc(sizeof(double) * (size_t)I);
     if (!hh) return -2;
+    double xg[64], xu[64], hd[64];
+    if (lora) {
+        lora_in(lora, lora->a_gate, e, H, xrow, xg);
+        lora_in(lora, lora->a_up, e, H, xrow, xu);
+    }
     for (int i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
         for (int c = 0; c < H; ++c) {
             g += xrow[c] * weight_at(w_gate, e, i, c);
             u += xrow[c] * weight_at(w_up, e, i, c);
         }
+        if (lora) {
+            g += lora_out(lora, lora->b_gate, e, I, i, xg);
+            u += lora_out(lora, lora->b_up, e, I, i, xu);
+        }
         hh[i] = (g / (1.0 + exp(-g))) * u;
     }
+    if (lora) lora_in(lora, lora->a_down, e, I, hh, hd);
     for (int r = 0; r < H; ++r) {
         double s = 0.0;
         for (int i = 0; i < I; ++i) s += hh[i] * weight_at(w_down, e, r, i);
+        if (lora) s += lora_out(lora, lora->b_down, e, H, r, hd);
         y[r] = s;
     }
     if (!h) free(hh);
     return 0;
+}
+
+/* Steps E and F for one activation row and one expert. h may be NULL. */
+int orc_expert_mlp(int H, int I, const double *xrow, int e, const orc_matrix *w_gate,
+                   const orc_matrix *w_up, const orc_matrix *w_down, double *h, double *y)
+{
+    return expert_mlp(H, I, xrow, e, w_gate, w_up, w_down, NULL, h, y);
 }
 
 static void widen_row(int act_dtype, const void *x, int64_t t, int H, double *row)
@@ -270,10 +324,10 @@ int orc_forward(int T, int H, int E, int k, int I, int norm_topk, int act_dtype,
  * only on token t (its own routing and its own k expert rows), so this is the
  * same definition evaluated for a sample of tokens of a large batch.
  */
-int orc_forward_tokens(int ntok, const int32_t *tokens, int H, int E, int k, int I, int norm_topk,
-                       int act_dtype, const void *x, const void *w_router, const float *bias,
-                       const orc_matrix *w_gate, const orc_matrix *w_up, const orc_matrix *w_down,
-                       int32_t *ids, double *weights, double *tie_margin, double *out)
+static int forward_tokens(int ntok, const int32_t *tokens, int H, int E, int k, int I, int norm_topk,
+                          int act_dtype, const void *x, const void *w_router, const float *bias,
+                          const orc_matrix *w_gate, const orc_matrix *w_up, const orc_matrix *w_down,
+                          const orc_lora *lora, int32_t *ids, double *weights, double *tie_margin, double *out)
 {
     if (ntok < 0 || !tokens || !x || !out || !ids || !weights) return -1;
     double *logit = (double *)malloc(sizeof(double) * (size_t)E);
@@ -292,12 +346,32 @@ int orc_forward_tokens(int ntok, const int32_t *tokens, int H, int E, int k, int
         double *o = out + (int64_t)n * H;
         for (int c = 0; c < H; ++c) o[c] = 0.0;
         for (int j = 0; j < k && rc == 0; ++j) {
-            rc = orc_expert_mlp(H, I, row, ids[(int64_t)n * k + j], w_gate, w_up, w_down, NULL, y);
+            rc = expert_mlp(H, I, row, ids[(int64_t)n * k + j], w_gate, w_up, w_down, lora, NULL, y);
             for (int c = 0; c < H && rc == 0; ++c) o[c] += weights[(int64_t)n * k + j] * y[c];
         }
     }
     free(logit); free(row); free(y);
     return rc;
+}
+
+int orc_forward_tokens(int ntok, const int32_t *tokens, int H, int E, int k, int I, int norm_topk,
+                       int act_dtype, const void *x, const void *w_router, const float *bias,
+                       const orc_matrix *w_gate, const orc_matrix *w_up, const orc_matrix *w_down,
+                       int32_t *ids, double *weights, double *tie_margin, double *out)
+{
+    return forward_tokens(ntok, tokens, H, E, k, I, norm_topk, act_dtype, x, w_router, bias, w_gate, w_up, w_down,
+                          NULL, ids, weights, tie_margin, out);
+}
+
+/* orc_forward_tokens with LoRA adapters on the experts. */
+int orc_forward_tokens_lora(int ntok, const int32_t *tokens, int H, int E, int k, int I, int norm_topk,
+                            int act_dtype, const void *x, const void *w_router, const float *bias,
+                            const orc_matrix *w_gate, const orc_matrix *w_up, const orc_matrix *w_down,
+                            const orc_lora *lora, int32_t *ids, double *weights, double *tie_margin, double *out)
+{
+    if (!lora) return -1;
+    return forward_tokens(ntok, tokens, H, E, k, I, norm_topk, act_dtype, x, w_router, bias, w_gate, w_up, w_down,
+                          lora, ids, weights, tie_margin, out);
 }
 
 /*

@@ -239,3 +239,16 @@ def make_norm_weight(H: int, act: str = "bf16", seed: int = 0, layer: int = 0) -
     (bf16 bits, or fp32).  Seeded like every other tensor; no model checkpoint exists here."""
     g = (1.0 + 0.1 * _rng(seed, layer, 901).standard_normal(H)).astype(np.float32)
     return bf16_bits(g) if act == "bf16" else g
+
+
+def make_lora(E: int, H: int, I: int, rank: int = 16, seed: int = 0, layer: int = 0, alpha: float = 16.0) -> dict:
+    """Synthetic fp32 LoRA adapters for the expert projections (no trained adapters exist here):
+    A ~ N(0, 1/in), B ~ N(0, 0.25/rank), scale = alpha / rank.  Shapes: a_gate, a_up [E][r][H],
+    b_gate, b_up [E][I][r], a_down [E][r][I], b_down [E][H][r]."""
+    def draw(shape, std, tid):
+        return (std * _rng(seed, layer, 950 + tid).standard_normal(shape)).astype(np.float32)
+    bs = 0.5 / np.sqrt(rank)
+    return dict(rank=rank, scale=alpha / rank,
+                a_gate=draw((E, rank, H), 1 / np.sqrt(H), 0), b_gate=draw((E, I, rank), bs, 1),
+                a_up=draw((E, rank, H), 1 / np.sqrt(H), 2), b_up=draw((E, I, rank), bs, 3),
+                a_down=draw((E, rank, I), 1 / np.sqrt(I), 4), b_down=draw((E, H, rank), bs, 5))

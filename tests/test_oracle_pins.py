@@ -372,3 +372,46 @@ def test_prenorm_block_with_one_hidden_unit_has_a_closed_form():
         assert abs(r["out"][t, 0] - expect) < 1e-12
     r0 = oracle.forward_prenorm(inp, gamma, 0.0, residual=False)
     np.testing.assert_allclose(r["out"] - r0["out"], inp.x.astype(np.float64), rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------- LoRA on the experts
+
+def _lora_zero_b(l):
+    z = dict(l)
+    for n in ("b_gate", "b_up", "b_down"):
+        z[n] = np.zeros_like(l[n])
+    return z
+
+
+def test_lora_with_zero_b_is_the_base_block():
+    inp = synth.make_custom(6, 64, 8, 2, 32, act="f32", w="f32", seed=31)
+    lora = _lora_zero_b(synth.make_lora(8, 64, 32, rank=4, seed=1))
+    a = oracle.forward_lora(inp, lora)
+    b = oracle.forward_tokens(inp, np.arange(6))
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["ids"], b["ids"])
+
+
+def test_lora_equals_the_merged_weights():
+    # integer-valued weights and adapters with scale 1/2: W + scale * B A is exact in fp32, so the
+    # oracle on merged weights (a plain numpy matmul builds them) must agree to double rounding;
+    # a transposed A or B, a wrong scale or an adapter on the wrong projection would not
+    rng = np.random.default_rng(7)
+    E, H, I, r, T, k = 4, 16, 8, 3, 5, 2
+    ints = lambda *sh: rng.integers(-2, 3, size=sh).astype(np.float32)
+    inp = synth.MoEInputs(name="lora", T=T, H=H, E=E, k=k, I=I, act="f32", w="f32", norm_topk=True, q_block=64,
+                          x=(ints(T, H) / 4).astype(np.float32), w_router=ints(E, H), b_router=None,
+                          w_gate=ints(E, I, H), w_up=ints(E, I, H), w_down=ints(E, H, I))
+    lora = dict(rank=r, scale=0.5, a_gate=ints(E, r, H), b_gate=ints(E, I, r), a_up=ints(E, r, H),
+                b_up=ints(E, I, r), a_down=ints(E, r, I), b_down=ints(E, H, r))
+    merged = synth.MoEInputs(**{**inp.__dict__})
+    merged.w_gate = (inp.w_gate + 0.5 * np.matmul(lora["b_gate"], lora["a_gate"])).astype(np.float32)
+    merged.w_up = (inp.w_up + 0.5 * np.matmul(lora["b_up"], lora["a_up"])).astype(np.float32)
+    merged.w_down = (inp.w_down + 0.5 * np.matmul(lora["b_down"], lora["a_down"])).astype(np.float32)
+    a = oracle.forward_lora(inp, lora)
+    b = oracle.forward_tokens(merged, np.arange(T))
+    np.testing.assert_array_equal(a["ids"], b["ids"])
+    np.testing.assert_allclose(a["out"], b["out"], rtol=1e-12, atol=1e-12 * np.abs(b["out"]).max())
+    # and the adapters do change the result
+    c = oracle.forward_tokens(inp, np.arange(T))
+    assert np.abs(c["out"] - a["out"]).max() > 1e-3
