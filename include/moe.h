@@ -105,6 +105,24 @@ typedef struct {
 } moe_q4;
 
 /*
+ * LoRA adapters on the experts (moe_forward_lora): rank r in [1, 16], fp32,
+ * one (A, B) pair per expert and projection, so that each projection becomes
+ *   z = x . W^T + scale * (x . A^T) . B^T,
+ * the "fp32 LoRA injection" on top of bf16 or 4-bit expert weights that the
+ * unsloth commit page 4f2bfe7f69 names for its rank-16 LoRA runs.
+ *   a_gate, a_up [E][r][H]     b_gate, b_up [E][I][r]
+ *   a_down       [E][r][I]     b_down       [E][H][r]
+ * Device pointers, row-major, 16-byte aligned.
+ */
+typedef struct {
+    int32_t rank;
+    float scale;   /* lora_alpha / rank */
+    const float *a_gate, *b_gate;
+    const float *a_up, *b_up;
+    const float *a_down, *b_down;
+} moe_lora;
+
+/*
  * Workspace bytes the entry points below need for this shape (host only, no
  * CUDA call).  The same workspace serves every entry point; it must be
  * 256-byte aligned.  Its first 2048 bytes hold the device error word and
@@ -208,6 +226,20 @@ MOE_API int moe_forward_rmsnorm(const moe_shape *shape, const void *hs, const vo
                                 const void *w_up, const void *w_down, const moe_q4 *q4, void *out,
                                 void *x_norm_out, int32_t *expert_ids_out, float *weights_out, void *workspace,
                                 size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_forward with LoRA adapters on the three expert projections (see
+ * moe_lora).  The rank-r products x . A^T and h . A_down^T are computed in fp32
+ * by separate launches; the B side is added in the grouped kernels' epilogues
+ * before SiLU (gate/up) and before y is rounded (down).  Same arguments, results,
+ * workspace and errors as moe_forward, plus MOE_ERR_NULLPTR for a NULL lora or
+ * adapter pointer and MOE_ERR_SHAPE for a rank outside [1, 16] or a non-finite
+ * scale.
+ */
+MOE_API int moe_forward_lora(const moe_shape *shape, const void *x, const void *w_router, const float *b_router,
+                             const void *w_gate, const void *w_up, const void *w_down, const moe_q4 *q4,
+                             const moe_lora *lora, void *out, int32_t *expert_ids_out, float *weights_out,
+                             void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* Size of the library's fixed device scratch array used by moe_forward_static_scratch. */
 #define MOE_STATIC_SCRATCH_BYTES (32u << 20)

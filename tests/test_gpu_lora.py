@@ -1,0 +1,98 @@
+"""GPU parity of moe_forward_lora (LoRA adapters on the expert projections) against the
+oracle, on the bf16 and 4-bit tensor-core paths (decode and large batches) and the
+generic fp32 path; with B = 0 the result must equal moe_forward bit for bit, which also
+checks the split gate/up and down launches the adapters need."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+import top_routing_grouped_router_gb300 as moe  # noqa: E402
+from top_routing_grouped_router_gb300.device import to_device, upload  # noqa: E402
+from parity import NEAR_TIE, rel_err, sample_tokens, to_f64  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from top_routing_grouped_router_gb300 import build
+    build.build()
+    oracle.build()
+
+
+_NAMES = ("a_gate", "b_gate", "a_up", "b_up", "a_down", "b_down")
+
+
+def _dev_lora(lora):
+    t = {n: to_device(np.ascontiguousarray(lora[n], dtype=np.float32), "cuda") for n in _NAMES}
+    return moe.make_lora(lora["rank"], lora["scale"], *[t[n] for n in _NAMES]), t
+
+
+def _run_lora(L, lora_s):
+    ws = L.new_workspace()
+    out = torch.empty((L.shape.T, L.shape.H), dtype=L.out_dtype(), device="cuda")
+    ids = torch.empty((L.shape.T, L.shape.k), dtype=torch.int32, device="cuda")
+    moe.moe_forward_lora(L.shape, L.x, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4, lora_s, out, ids,
+                         workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_error(ws) == 0
+    return out, ids
+
+
+def _check(inp, rank, n_tok):
+    lora = synth.make_lora(inp.E, inp.H, inp.I, rank=rank, seed=inp.T + rank)
+    L = upload(inp)
+    lora_s, keep_alive = _dev_lora(lora)
+    out, ids = _run_lora(L, lora_s)
+    toks = np.arange(inp.T) if n_tok is None else sample_tokens(inp.T, n_tok)
+    ref = oracle.forward_lora(inp, lora, toks)
+    keep = ref["tie_margin"] >= NEAR_TIE
+    g_ids = ids.cpu().numpy()[toks]
+    np.testing.assert_array_equal(np.sort(g_ids[keep], axis=1), np.sort(ref["ids"][keep], axis=1))
+    tol = 1e-5 if inp.act == "f32" else 1e-2
+    err = rel_err(to_f64(out)[toks][keep], ref["out"][keep])
+    assert err <= tol, err
+    # the adapters matter: the base block differs from the LoRA result by more than the tolerance
+    base = oracle.forward_tokens(inp, toks)["out"]
+    assert rel_err(base[keep], ref["out"][keep]) > 5 * tol
+
+    # B = 0: bit-identical to moe_forward (same tiles, same rounding; gate/up and down split)
+    zero = dict(lora)
+    for n in ("b_gate", "b_up", "b_down"):
+        zero[n] = np.zeros_like(lora[n])
+    zs, keep_alive2 = _dev_lora(zero)
+    out0, ids0 = _run_lora(L, zs)
+    ref0 = torch.empty_like(out0)
+    ids_ref = torch.empty_like(ids0)
+    moe.moe_forward(L.shape, L.x, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4, ref0, ids_ref,
+                    workspace=L.new_workspace())
+    torch.cuda.synchronize()
+    assert torch.equal(ids0, ids_ref)
+    assert torch.equal(out0.view(torch.int16) if out0.dtype == torch.bfloat16 else out0,
+                       ref0.view(torch.int16) if ref0.dtype == torch.bfloat16 else ref0)
+
+
+def test_lora_decode_bf16_rank16():
+    _check(synth.make_inputs("decode8"), 16, None)
+
+
+def test_lora_decode_q4_rank16():
+    _check(synth.make_inputs("decode48q"), 16, 12)
+
+
+def test_lora_fp32_generic_path_rank4():
+    _check(synth.make_inputs("tiny"), 4, None)
+
+
+def test_lora_large_batch_bf16_rank8():
+    _check(synth.make_custom(300, 512, 16, 4, 256, seed=41, name="lora300"), 8, 16)
+
+
+def test_lora_large_batch_q4_rank16():
+    _check(synth.make_custom(200, 256, 16, 4, 128, w="q4", seed=43, name="lora200q"), 16, 16)

@@ -18,7 +18,7 @@ __all__ = [
     "MOE_DT_F32", "MOE_DT_BF16", "MOE_DT_Q4", "MoEError", "MoEShape", "MoEQ4", "lib", "library_path",
     "make_shape", "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string", "EXPORTED_SYMBOLS",
-    "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_graph_buckets", "moe_graphs_arena_size",
+    "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_forward_lora", "moe_graph_buckets", "moe_graphs_arena_size",
     "DecodeGraphs",
 ]
 
@@ -30,7 +30,7 @@ library_path = os.path.join(_HERE, "libmoe_gb300.so")
 
 EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
                     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string",
-                    "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_graph_buckets", "moe_graphs_arena_size", "moe_graphs_create",
+                    "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_forward_lora", "moe_graph_buckets", "moe_graphs_arena_size", "moe_graphs_create",
                     "moe_graphs_bucket", "moe_graphs_run", "moe_graphs_destroy")
 
 
@@ -44,6 +44,12 @@ class MoEShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("I", ctypes.c_int32), ("act_dtype", ctypes.c_int32), ("w_dtype", ctypes.c_int32),
                 ("norm_topk", ctypes.c_int32), ("q_block", ctypes.c_int32)]
+
+
+class MoELora(ctypes.Structure):
+    _fields_ = [("rank", ctypes.c_int32), ("scale", ctypes.c_float), ("a_gate", ctypes.c_void_p),
+                ("b_gate", ctypes.c_void_p), ("a_up", ctypes.c_void_p), ("b_up", ctypes.c_void_p),
+                ("a_down", ctypes.c_void_p), ("b_down", ctypes.c_void_p)]
 
 
 class MoEQ4(ctypes.Structure):
@@ -77,6 +83,7 @@ def lib() -> ctypes.CDLL:
             "moe_forward_static_scratch": [sp, vp, vp, vp, vp, vp, vp, q4p, vp, i32p, vp, vp],
             "moe_forward_rmsnorm": [sp, vp, vp, ctypes.c_float, ctypes.c_int, vp, vp, vp, vp, vp, q4p, vp, vp, i32p,
                                     vp, vp, sz, vp],
+            "moe_forward_lora": [sp, vp, vp, vp, vp, vp, vp, q4p, ctypes.POINTER(MoELora), vp, i32p, vp, vp, sz, vp],
             "moe_graph_buckets": [ctypes.c_int, vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)],
             "moe_graphs_arena_size": [sp, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
             "moe_graphs_create": [sp, ctypes.c_int, vp, vp, vp, vp, vp, q4p, vp, sz, vp, ctypes.POINTER(vp)],
@@ -186,6 +193,21 @@ def moe_forward_rmsnorm(shape, hs, gamma, eps, w_router, b_router, w_gate, w_up,
                                      ctypes.byref(q4) if q4 is not None else None, _ptr(out), _ptr(x_norm_out),
                                      _ptr(expert_ids_out), _ptr(weights_out), _ptr(workspace), _nbytes(workspace),
                                      _stream(stream)), "moe_forward_rmsnorm")
+
+
+def make_lora(rank, scale, a_gate, b_gate, a_up, b_up, a_down, b_down) -> MoELora:
+    """The moe_lora struct over device tensors (fp32, row-major; see moe.h for the shapes)."""
+    return MoELora(int(rank), float(scale), _ptr(a_gate), _ptr(b_gate), _ptr(a_up), _ptr(b_up), _ptr(a_down),
+                   _ptr(b_down))
+
+
+def moe_forward_lora(shape, x, w_router, b_router, w_gate, w_up, w_down, q4, lora: MoELora, out, expert_ids_out=None,
+                     weights_out=None, workspace=None, stream=None):
+    """moe_forward with LoRA adapters on the expert projections."""
+    _check(lib().moe_forward_lora(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(b_router), _ptr(w_gate),
+                                  _ptr(w_up), _ptr(w_down), ctypes.byref(q4) if q4 is not None else None,
+                                  ctypes.byref(lora), _ptr(out), _ptr(expert_ids_out), _ptr(weights_out),
+                                  _ptr(workspace), _nbytes(workspace), _stream(stream)), "moe_forward_lora")
 
 
 def moe_forward_launches(shape: MoEShape) -> int:

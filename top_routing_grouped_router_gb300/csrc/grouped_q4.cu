@@ -33,6 +33,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 
 namespace moe {
 namespace {
@@ -71,8 +72,9 @@ enum : int { kGateUp = 0, kDown = 1 };
 struct Params {
     const int32_t *offsets;
     const uint32_t *tiles;
-    const int *n_tiles;
-    int *tile_counter;
+    int *sched;                     // scheduling words (grouped_tiles.cuh)
+    int phase;                      // kPhaseAll / kPhaseGateUp / kPhaseDown
+    LoraDev lora;                   // LoRA B-side terms of the epilogue (rank 0: none)
     int *done;
     int32_t *err;
     uint16_t *h;
@@ -124,7 +126,7 @@ __device__ __forceinline__ uint32_t gamma_pair(uint16_t scale, float half_b) {
     return g | (g << 16);
 }
 
-template <int MaxN, int kRawStages>
+template <int MaxN, int kRawStages, bool kLora>
 __global__ void __launch_bounds__(kThreads, 1)
 q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constant__ CUtensorMap tm_uc,
                  const __grid_constant__ CUtensorMap tm_dc, const __grid_constant__ CUtensorMap tm_x,
@@ -191,17 +193,24 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
     griddep_launch_dependents();
     griddep_wait();
     const uint32_t tmem_base = *tmem_slot;
-    const int n_tiles = *p.n_tiles;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         int r = 0, slot = 0, tiles_done = 0;
         uint32_t rp = 0, mphase = 0;
-        int next = atomicAdd(p.tile_counter, 1);
+        // this launch's tile range [lo, hi) and its claim counter
+        int lo = 0, hi = p.sched[kSchedTiles];
+        int *ctr = p.sched + kSchedClaim;
+        if (p.phase == kPhaseGateUp) hi = p.sched[kSchedGateUp];
+        if (p.phase == kPhaseDown) {
+            lo = p.sched[kSchedGateUp];
+            ctr = p.sched + kSchedClaimDown;
+        }
+        int next = lo + atomicAdd(ctr, 1);
         for (;;) {
             const int t = next;
-            if (t >= n_tiles || *abort) break;
-            next = atomicAdd(p.tile_counter, 1);
+            if (t >= hi || *abort) break;
+            next = lo + atomicAdd(ctr, 1);
             const uint32_t entry = __ldg(p.tiles + t);
             const int down = int(entry >> 31), e0 = int((entry >> 16) & 0xFF), rb = int((entry >> 8) & 0xFF);
             const int nc = int(entry & 0xFF);
@@ -405,21 +414,45 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const int col = rb * kRows + row;
             // h is stored in the weights' 8-element group order (see the file comment)
             const int hcol = (col & ~7) | sigma_inv(col & 7);
+            // LoRA: this row's B vectors (the A-side products xa / ha were computed per token)
+            const LoraDev &lr = p.lora;
+            const bool lora = kLora && lr.rank > 0;
+            float lb0[16], lb1[16];
+            if (lora) {
+                if (down) {
+                    lora_row16(lr.bd, (size_t)e * p.H + col, lr.rank, lb0);
+                } else {
+                    lora_row16(lr.bg, (size_t)e * p.I + col, lr.rank, lb0);
+                    lora_row16(lr.bu, (size_t)e * p.I + col, lr.rank, lb1);
+                }
+            }
             for (int c0 = 0; c0 < N; c0 += 16) {
                 if (down) {
                     float v[16];
                     tmem_ld16(taddr + c0, v);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (c0 + j < m) p.y[(size_t)(r0 + c0 + j) * p.H + col] = f32_to_bf16_bits(v[j]);
+                        if (c0 + j < m) {
+                            const size_t pr = (size_t)(r0 + c0 + j);
+                            float val = v[j];
+                            if (lora) val += lr.scale * lora_dot16(lb0, lr.ha + pr * 16);
+                            p.y[pr * p.H + col] = f32_to_bf16_bits(val);
+                        }
                 } else {
                     float g[16], uu[16];
                     tmem_ld16(taddr + c0, g);
                     tmem_ld16(taddr + kUpCol + c0, uu);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (c0 + j < m)
-                            p.h[(size_t)(r0 + c0 + j) * p.I + hcol] = f32_to_bf16_bits(swiglu(g[j], uu[j]));
+                        if (c0 + j < m) {
+                            const size_t pr = (size_t)(r0 + c0 + j);
+                            float gv = g[j], uv = uu[j];
+                            if (lora) {
+                                gv += lr.scale * lora_dot16(lb0, lr.xa + pr * 32);
+                                uv += lr.scale * lora_dot16(lb1, lr.xa + pr * 32 + 16);
+                            }
+                            p.h[pr * p.I + hcol] = f32_to_bf16_bits(swiglu(gv, uv));
+                        }
                 }
             }
             tc_fence_before();
@@ -453,7 +486,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 __global__ void __launch_bounds__(256)
 q4_prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
                int T, int k, int H, int I, int E, int cmax, int max_tiles, uint16_t *__restrict__ x_perm,
-               uint32_t *tiles, int *n_tiles, int *tile_counter, int *done, int32_t *err) {
+               uint32_t *tiles, int *sched, int *done, int32_t *err) {
     griddep_launch_dependents();
     griddep_wait();
     if (blockIdx.x > 0) {
@@ -499,20 +532,22 @@ q4_prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order
     }
     if (threadIdx.x == 0) {
         if (n_gu + n_dn > max_tiles) record_error(err, MOE_ERR_DEVICE);  // inconsistent offsets
-        *n_tiles = min(n_gu + n_dn, max_tiles);
-        *tile_counter = 0;
+        sched[kSchedClaim] = 0;
+        sched[kSchedTiles] = min(n_gu + n_dn, max_tiles);
+        sched[kSchedGateUp] = min(n_gu, max_tiles);
+        sched[kSchedClaimDown] = 0;
     }
 }
 
 size_t xperm_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * s.H * 2 + 255) / 256 * 256; }
 
-template <int MaxN, int RawStages>
+template <int MaxN, int RawStages, bool Lora>
 bool set_attr() {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(q4_swiglu_kernel<MaxN, RawStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(q4_swiglu_kernel<MaxN, RawStages, Lora>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  QCfg<MaxN, RawStages>::kSmemBytes) != cudaSuccess)
             return false;
         attr_set[dev] = true;
@@ -558,7 +593,7 @@ size_t q4_part_bytes(const moe_shape &s) {
 
 cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
                       const void *wg, const void *wu, const void *wd, const moe_q4 *q4, float *part, void *h, void *y,
-                      int32_t *err, cudaStream_t st) {
+                      int32_t *err, cudaStream_t st, const moe_lora *lora, float *xa, float *ha) {
     float b = 0;
     int t2 = 0;
     if (!q4 || !q4_codebook_affine(q4->codebook, &b, &t2)) return cudaErrorInvalidValue;
@@ -566,7 +601,7 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     char *base = reinterpret_cast<char *>(part);
     uint16_t *x_perm = reinterpret_cast<uint16_t *>(base);
     int *sched = reinterpret_cast<int *>(base + xperm_bytes(s));
-    int *tile_counter = sched, *n_tiles = sched + 1, *done = sched + 64;
+    int *done = sched + 64;
     uint32_t *tiles = reinterpret_cast<uint32_t *>(base + xperm_bytes(s) + 256 + (size_t)kMaxE * 4);
 
     CUtensorMap mg, mu, md, mx, mh;
@@ -579,15 +614,17 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     const bool decode = s.T <= kDecodeMaxN;
     const int cmax = decode ? kDecodeMaxN : kChunkN;
     cudaError_t e = launch_pdl(q4_prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
-                               offsets, s.T, s.k, s.H, s.I, s.E, cmax, (int)q4_max_tiles(s), x_perm, tiles, n_tiles,
-                               tile_counter, done, err);
+                               offsets, s.T, s.k, s.H, s.I, s.E, cmax, (int)q4_max_tiles(s), x_perm, tiles, sched,
+                               done, err);
     if (e != cudaSuccess) return e;
-    if (!(decode ? set_attr<kDecodeMaxN, 6>() : set_attr<kChunkN, 4>())) return cudaErrorInvalidValue;
+    if (!(decode ? set_attr<kDecodeMaxN, 6, false>() && set_attr<kDecodeMaxN, 6, true>()
+                 : set_attr<kChunkN, 4, false>() && set_attr<kChunkN, 4, true>()))
+        return cudaErrorInvalidValue;
     Params prm{};
     prm.offsets = offsets;
     prm.tiles = tiles;
-    prm.n_tiles = n_tiles;
-    prm.tile_counter = tile_counter;
+    prm.sched = sched;
+    prm.phase = kPhaseAll;
     prm.done = done;
     prm.err = err;
     prm.h = static_cast<uint16_t *>(h);
@@ -606,11 +643,23 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     prm.I = s.I;
     prm.A = A;
     prm.cmax = cmax;
-    if (decode)
-        return launch_pdl(q4_swiglu_kernel<kDecodeMaxN, 6>, dim3(sm_count()), dim3(kThreads),
-                          QCfg<kDecodeMaxN, 6>::kSmemBytes, st, mg, mu, md, mx, mh, prm);
-    return launch_pdl(q4_swiglu_kernel<kChunkN, 4>, dim3(sm_count()), dim3(kThreads), QCfg<kChunkN, 4>::kSmemBytes, st,
-                      mg, mu, md, mx, mh, prm);
+    auto run = [&](const Params &pr, auto lora_tag) {
+        constexpr bool L = decltype(lora_tag)::value;
+        if (decode)
+            return launch_pdl(q4_swiglu_kernel<kDecodeMaxN, 6, L>, dim3(sm_count()), dim3(kThreads),
+                              QCfg<kDecodeMaxN, 6>::kSmemBytes, st, mg, mu, md, mx, mh, pr);
+        return launch_pdl(q4_swiglu_kernel<kChunkN, 4, L>, dim3(sm_count()), dim3(kThreads),
+                          QCfg<kChunkN, 4>::kSmemBytes, st, mg, mu, md, mx, mh, pr);
+    };
+    if (!lora) return run(prm, std::false_type{});
+    // with adapters: x . A^T, the gate/up tiles, h . A_down^T (h in the grouped column order), the down tiles
+    prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
+    if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, st)) != cudaSuccess) return e;
+    prm.phase = kPhaseGateUp;
+    if ((e = run(prm, std::true_type{})) != cudaSuccess) return e;
+    if ((e = launch_lora_ha(s, h, false, true, offsets, *lora, ha, st)) != cudaSuccess) return e;
+    prm.phase = kPhaseDown;
+    return run(prm, std::true_type{});
 }
 
 }  // namespace moe

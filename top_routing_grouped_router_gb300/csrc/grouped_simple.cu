@@ -57,7 +57,7 @@ template <typename ActT, int WFMT>
 __global__ void __launch_bounds__(kWarps * 32)
 gate_up_simple_kernel(const ActT *__restrict__ x, const int32_t *__restrict__ offsets,
                       const int32_t *__restrict__ order, int E, int k, int H, int I, int A, WeightRef wg,
-                      WeightRef wu, Codebook cb, float *__restrict__ h, int p0) {
+                      WeightRef wu, Codebook cb, float *__restrict__ h, int p0, LoraDev lr) {
     griddep_launch_dependents();
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -78,6 +78,13 @@ gate_up_simple_kernel(const ActT *__restrict__ x, const int32_t *__restrict__ of
     g = warp_sum(g);
     u = warp_sum(u);
     if (lane == 0) {
+        if (lr.rank) {
+            float b[16];
+            lora_row16(lr.bg, (size_t)e * I + i, lr.rank, b);
+            g += lr.scale * lora_dot16(b, lr.xa + (size_t)p * 32);
+            lora_row16(lr.bu, (size_t)e * I + i, lr.rank, b);
+            u += lr.scale * lora_dot16(b, lr.xa + (size_t)p * 32 + 16);
+        }
         float v = swiglu(g, u);
         if constexpr (sizeof(ActT) == 2) v = bf16_bits_to_f32(f32_to_bf16_bits(v));
         h[(size_t)p * I + i] = v;
@@ -87,7 +94,7 @@ gate_up_simple_kernel(const ActT *__restrict__ x, const int32_t *__restrict__ of
 template <typename OutT, int WFMT>
 __global__ void __launch_bounds__(kWarps * 32)
 down_simple_kernel(const float *__restrict__ h, const int32_t *__restrict__ offsets, int E, int H, int I,
-                   WeightRef wd, Codebook cb, OutT *__restrict__ y, int p0) {
+                   WeightRef wd, Codebook cb, OutT *__restrict__ y, int p0, LoraDev lr) {
     griddep_launch_dependents();
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -100,6 +107,11 @@ down_simple_kernel(const float *__restrict__ h, const int32_t *__restrict__ offs
     for (int c = lane; c < I; c += 32) s = fmaf(__ldg(h + (size_t)p * I + c), weight_at<WFMT>(wd, cb, e, r, c), s);
     s = warp_sum(s);
     if (lane == 0) {
+        if (lr.rank) {
+            float b[16];
+            lora_row16(lr.bd, (size_t)e * H + r, lr.rank, b);
+            s += lr.scale * lora_dot16(b, lr.ha + (size_t)p * 16);
+        }
         if constexpr (sizeof(OutT) == 4) y[(size_t)p * H + r] = s;
         else y[(size_t)p * H + r] = f32_to_bf16_bits(s);
     }
@@ -108,7 +120,13 @@ down_simple_kernel(const float *__restrict__ h, const int32_t *__restrict__ offs
 template <typename ActT, int WFMT>
 cudaError_t launch_typed(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
                          const void *wg, const void *wu, const void *wd, const moe_q4 *q4, void *h, void *y,
-                         cudaStream_t st) {
+                         cudaStream_t st, const moe_lora *lora, float *xa, float *ha) {
+    LoraDev lr{};
+    if (lora) {
+        lr = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
+        const cudaError_t e = launch_lora_xa(s, x, order, offsets, *lora, xa, st);
+        if (e != cudaSuccess) return e;
+    }
     const int A = s.T * s.k;
     Codebook cb{};
     const uint16_t *gs = nullptr, *us = nullptr, *ds = nullptr;
@@ -125,7 +143,11 @@ cudaError_t launch_typed(const moe_shape &s, const void *x, const int32_t *offse
         dim3 g1((s.I + kWarps - 1) / kWarps, rows);
         const cudaError_t e = launch_pdl(gate_up_simple_kernel<ActT, WFMT>, g1, dim3(kWarps * 32), 0, st,
                                          static_cast<const ActT *>(x), offsets, order, s.E, s.k, s.H, s.I, A, rg, ru,
-                                         cb, static_cast<float *>(h), p0);
+                                         cb, static_cast<float *>(h), p0, lr);
+        if (e != cudaSuccess) return e;
+    }
+    if (lora) {
+        const cudaError_t e = launch_lora_ha(s, h, true, false, offsets, *lora, ha, st);
         if (e != cudaSuccess) return e;
     }
     for (int p0 = 0; p0 < A; p0 += 65535) {
@@ -133,7 +155,7 @@ cudaError_t launch_typed(const moe_shape &s, const void *x, const int32_t *offse
         dim3 g2((s.H + kWarps - 1) / kWarps, rows);
         const cudaError_t e = launch_pdl(down_simple_kernel<ActT, WFMT>, g2, dim3(kWarps * 32), 0, st,
                                          static_cast<const float *>(h), offsets, s.E, s.H, s.I, rd, cb,
-                                         static_cast<ActT *>(y), p0);
+                                         static_cast<ActT *>(y), p0, lr);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
@@ -148,12 +170,13 @@ int grouped_simple_launches(const moe_shape &s) {
 
 cudaError_t launch_grouped_simple(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
                                   const void *wg, const void *wu, const void *wd, const moe_q4 *q4, void *h,
-                                  void *y, cudaStream_t st) {
+                                  void *y, cudaStream_t st, const moe_lora *lora, float *xa, float *ha) {
     if (s.T == 0) return cudaSuccess;
-    if (s.act_dtype == MOE_DT_F32) return launch_typed<float, MOE_DT_F32>(s, x, offsets, order, wg, wu, wd, q4, h, y, st);
+    if (s.act_dtype == MOE_DT_F32)
+        return launch_typed<float, MOE_DT_F32>(s, x, offsets, order, wg, wu, wd, q4, h, y, st, lora, xa, ha);
     if (s.w_dtype == MOE_DT_BF16)
-        return launch_typed<uint16_t, MOE_DT_BF16>(s, x, offsets, order, wg, wu, wd, q4, h, y, st);
-    return launch_typed<uint16_t, MOE_DT_Q4>(s, x, offsets, order, wg, wu, wd, q4, h, y, st);
+        return launch_typed<uint16_t, MOE_DT_BF16>(s, x, offsets, order, wg, wu, wd, q4, h, y, st, lora, xa, ha);
+    return launch_typed<uint16_t, MOE_DT_Q4>(s, x, offsets, order, wg, wu, wd, q4, h, y, st, lora, xa, ha);
 }
 
 }  // namespace moe

@@ -68,8 +68,9 @@ enum : int { kGateUp = 0, kDown = 1, kRouter = 2 };
 struct Params {
     const int32_t *offsets;     // [E+1]
     const uint32_t *tiles;      // tile list
-    const int *n_tiles;         // its length
-    int *tile_counter;
+    int *sched;                 // scheduling words (grouped_tiles.cuh)
+    int phase;                  // kPhaseAll / kPhaseGateUp / kPhaseDown
+    LoraDev lora;               // LoRA B-side terms of the epilogue (rank 0: none)
     int *done;                  // [E] published gate/up tiles (per epilogue warp)
     int32_t *err;
     uint16_t *h;                // [A][I] bf16
@@ -110,7 +111,7 @@ __device__ __forceinline__ TileInfo read_tile(uint32_t entry, const Params &p, b
     return d;
 }
 
-template <int BCap, int kStages>
+template <int BCap, int kStages, bool kLora>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                  const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_x,
@@ -168,19 +169,26 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     griddep_wait();
     const uint32_t tmem_base = *tmem_slot;
     const bool router = p.router_tiles > 0;
-    const int n_tiles = router ? p.router_tiles : *p.n_tiles;
     const int erb = (p.E + kRows - 1) / kRows;  // expert row blocks in router mode
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         int stage = 0, slot = 0;
         uint32_t phase = 0, mphase = 0;
-        int next = router ? int(blockIdx.x) : atomicAdd(p.tile_counter, 1);
+        // this launch's tile range [lo, hi) and its claim counter
+        int lo = 0, hi = router ? p.router_tiles : p.sched[kSchedTiles];
+        int *ctr = router ? nullptr : p.sched + kSchedClaim;
+        if (!router && p.phase == kPhaseGateUp) hi = p.sched[kSchedGateUp];
+        if (!router && p.phase == kPhaseDown) {
+            lo = p.sched[kSchedGateUp];
+            ctr = p.sched + kSchedClaimDown;
+        }
+        int next = router ? int(blockIdx.x) : lo + atomicAdd(ctr, 1);
         for (;;) {
             const int t = next;
-            if (t >= n_tiles || *abort) break;
+            if (t >= hi || *abort) break;
             // claim ahead: the atomic's latency hides behind this tile
-            next = router ? t + int(gridDim.x) : atomicAdd(p.tile_counter, 1);
+            next = router ? t + int(gridDim.x) : lo + atomicAdd(ctr, 1);
             bool ok = true;
             TileInfo d;
             if (router) {
@@ -333,6 +341,18 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(b * kBufCols);
             const size_t col = (size_t)rb * kRows + row;
+            // LoRA: this row's B vectors (the A-side products xa / ha were computed per token)
+            const LoraDev &lr = p.lora;
+            const bool lora = kLora && lr.rank > 0 && down != kRouter && e < p.E;
+            float lb0[16], lb1[16];
+            if (lora) {
+                if (down) {
+                    lora_row16(lr.bd, (size_t)e * p.H + col, lr.rank, lb0);
+                } else {
+                    lora_row16(lr.bg, (size_t)e * p.I + col, lr.rank, lb0);
+                    lora_row16(lr.bu, (size_t)e * p.I + col, lr.rank, lb1);
+                }
+            }
             for (int c0 = 0; c0 < N; c0 += 16) {
                 if (down == kRouter) {
                     float v[16];
@@ -348,14 +368,27 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     tmem_ld16(taddr + c0, v);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (c0 + j < m) p.y[(size_t)(r0 + c0 + j) * p.H + col] = f32_to_bf16_bits(v[j]);
+                        if (c0 + j < m) {
+                            const size_t pr = (size_t)(r0 + c0 + j);
+                            float val = v[j];
+                            if (lora) val += lr.scale * lora_dot16(lb0, lr.ha + pr * 16);
+                            p.y[pr * p.H + col] = f32_to_bf16_bits(val);
+                        }
                 } else {
                     float g[16], u[16];
                     tmem_ld16(taddr + c0, g);
                     tmem_ld16(taddr + kUpCol + c0, u);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (c0 + j < m) p.h[(size_t)(r0 + c0 + j) * p.I + col] = f32_to_bf16_bits(swiglu(g[j], u[j]));
+                        if (c0 + j < m) {
+                            const size_t pr = (size_t)(r0 + c0 + j);
+                            float gv = g[j], uv = u[j];
+                            if (lora) {
+                                gv += lr.scale * lora_dot16(lb0, lr.xa + pr * 32);
+                                uv += lr.scale * lora_dot16(lb1, lr.xa + pr * 32 + 16);
+                            }
+                            p.h[pr * p.I + col] = f32_to_bf16_bits(swiglu(gv, uv));
+                        }
                 }
             }
             tc_fence_before();
@@ -394,13 +427,13 @@ size_t max_tiles(const moe_shape &s) {
     return chunks * (size_t)(s.I / kRows + s.H / kRows);
 }
 
-template <int BCap, int Stages>
+template <int BCap, int Stages, bool Lora>
 bool set_smem_attr() {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(tc_swiglu_kernel<BCap, Stages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(tc_swiglu_kernel<BCap, Stages, Lora>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg<BCap, Stages>::kSmemBytes) != cudaSuccess)
             return false;
         attr_set[dev] = true;
@@ -408,12 +441,12 @@ bool set_smem_attr() {
     return true;
 }
 
-template <int BCap, int Stages>
+template <int BCap, int Stages, bool Lora = false>
 cudaError_t launch_tc(dim3 grid, cudaStream_t st, const CUtensorMap &mg, const CUtensorMap &mu, const CUtensorMap &md,
                       const CUtensorMap &mx, const CUtensorMap &mh, const Params &prm) {
-    if (!set_smem_attr<BCap, Stages>()) return cudaErrorInvalidValue;
-    return launch_pdl(tc_swiglu_kernel<BCap, Stages>, grid, dim3(kThreads), Cfg<BCap, Stages>::kSmemBytes, st, mg, mu,
-                      md, mx, mh, prm);
+    if (!set_smem_attr<BCap, Stages, Lora>()) return cudaErrorInvalidValue;
+    return launch_pdl(tc_swiglu_kernel<BCap, Stages, Lora>, grid, dim3(kThreads), Cfg<BCap, Stages>::kSmemBytes, st, mg,
+                      mu, md, mx, mh, prm);
 }
 
 }  // namespace
@@ -459,17 +492,19 @@ size_t grouped_fast_part_bytes(int path, const moe_shape &s) {
 
 int grouped_fast_launches(int path, const moe_shape &) { return path == 1 || path == 2 ? 2 : 0; }
 
+// Without adapters: prep + one launch over all tiles.  With LoRA: prep, x . A^T, the
+// gate/up tiles, h . A_down^T, the down tiles (five launches).
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
                                 const moe_q4 *q4, const int32_t *, float *part, void *h, void *y, int32_t *err,
-                                cudaStream_t st) {
-    if (path == 2) return launch_q4(s, x, offsets, order, wg, wu, wd, q4, part, h, y, err, st);
+                                cudaStream_t st, const moe_lora *lora, float *xa, float *ha) {
+    if (path == 2) return launch_q4(s, x, offsets, order, wg, wu, wd, q4, part, h, y, err, st, lora, xa, ha);
     if (path != 1) return cudaErrorInvalidValue;
     const int A = s.T * s.k;
     char *base = reinterpret_cast<char *>(part);
     uint16_t *x_perm = reinterpret_cast<uint16_t *>(base);
     int *sched = reinterpret_cast<int *>(base + xperm_bytes(s));
-    int *tile_counter = sched, *n_tiles = sched + 1, *done = sched + 64;
+    int *done = sched + 64;
     uint32_t *tiles = reinterpret_cast<uint32_t *>(base + xperm_bytes(s) + 256 + (size_t)kMaxE * 4);
 
     CUtensorMap mg, mu, md, mx, mh;
@@ -482,14 +517,14 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     const int dmax = kMaxDownN;
     const TileListArgs ta{cmax, 0, dmax, 1, s.I / kRows, s.H / kRows, (int)max_tiles(s)};
     cudaError_t e = launch_pdl(prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
-                               offsets, s.T, s.k, s.H, s.E, ta, x_perm, tiles, n_tiles, tile_counter, done, err);
+                               offsets, s.T, s.k, s.H, s.E, ta, x_perm, tiles, sched, done, err);
     if (e != cudaSuccess) return e;
 
     Params prm{};
     prm.offsets = offsets;
     prm.tiles = tiles;
-    prm.n_tiles = n_tiles;
-    prm.tile_counter = tile_counter;
+    prm.sched = sched;
+    prm.phase = kPhaseAll;
     prm.done = done;
     prm.err = err;
     prm.h = static_cast<uint16_t *>(h);
@@ -502,8 +537,20 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.dmax = dmax;
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
-    if (s.T <= 32) return launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, prm);
-    return launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, prm);
+    if (!lora)
+        return s.T <= 32 ? launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, prm)
+                         : launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, prm);
+    auto run = [&](const Params &pr) {
+        return s.T <= 32 ? launch_tc<32, 6, true>(grid, st, mg, mu, md, mx, mh, pr)
+                         : launch_tc<kMaxN, 4, true>(grid, st, mg, mu, md, mx, mh, pr);
+    };
+    prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
+    if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, st)) != cudaSuccess) return e;
+    prm.phase = kPhaseGateUp;
+    if ((e = run(prm)) != cudaSuccess) return e;
+    if ((e = launch_lora_ha(s, h, false, false, offsets, *lora, ha, st)) != cudaSuccess) return e;
+    prm.phase = kPhaseDown;
+    return run(prm);
 }
 
 }  // namespace moe

@@ -69,12 +69,17 @@ struct TileListArgs {
     int max_tiles;         // capacity of `tiles`
 };
 
-// Block 0: the tile list from the offsets, its length, a zeroed claim counter and zeroed
-// per-expert completion counters.  Blocks 1..A: x_perm row blockIdx.x - 1.
+// Scheduling words next to the tile list: [0] claim counter of the gate/up (or all) tiles,
+// [1] number of tiles, [2] number of gate/up tiles (they come first), [3] claim counter
+// of the down tiles when those run in a launch of their own.
+enum : int { kSchedClaim = 0, kSchedTiles = 1, kSchedGateUp = 2, kSchedClaimDown = 3 };
+
+// Block 0: the tile list from the offsets, the scheduling words (zeroed claim counters)
+// and zeroed per-expert completion counters.  Blocks 1..A: x_perm row blockIdx.x - 1.
 __global__ void __launch_bounds__(256)
 prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
             int T, int k, int H, int E, TileListArgs ta, uint16_t *__restrict__ x_perm, uint32_t *tiles,
-            int *n_tiles, int *tile_counter, int *done, int32_t *err) {
+            int *sched, int *done, int32_t *err) {
     griddep_launch_dependents();
     griddep_wait();
     if (blockIdx.x > 0) {
@@ -114,8 +119,10 @@ prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, c
         }
     if (threadIdx.x == 0) {
         if (n_gu + n_dn > ta.max_tiles) record_error(err, MOE_ERR_DEVICE);  // inconsistent offsets
-        *n_tiles = min(n_gu + n_dn, ta.max_tiles);
-        *tile_counter = 0;
+        sched[kSchedClaim] = 0;
+        sched[kSchedTiles] = min(n_gu + n_dn, ta.max_tiles);
+        sched[kSchedGateUp] = min(n_gu, ta.max_tiles);
+        sched[kSchedClaimDown] = 0;
     }
 }
 

@@ -14,7 +14,8 @@ int select_grouped_path(const moe_shape &s);
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
                                 const moe_q4 *q4, const int32_t *active, float *part, void *h, void *y,
-                                int32_t *err, cudaStream_t st);
+                                int32_t *err, cudaStream_t st, const moe_lora *lora = nullptr, float *xa = nullptr,
+                                float *ha = nullptr);
 size_t grouped_fast_part_bytes(int path, const moe_shape &s);
 int grouped_fast_launches(int path, const moe_shape &s);
 int route_launches(const moe_shape &s);
@@ -64,6 +65,8 @@ WsLayout ws_layout(const moe_shape &s) {
     L.hist = take((size_t)permute_chunks((int)A) * E * 4);
     L.h = take(A * s.I * 4);
     L.y = take(A * s.H * act_bytes(s));
+    L.xa = take(A * 32 * 4);
+    L.ha = take(A * 16 * 4);
     L.part = take(grouped_fast_part_bytes(select_grouped_path(s), s));
     L.total = off;
     return L;
@@ -120,8 +123,10 @@ int do_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t 
 }
 
 int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order, const void *wg,
-               const void *wu, const void *wd, const moe_q4 *q4, void *y, void *ws, cudaStream_t st) {
+               const void *wu, const void *wd, const moe_q4 *q4, void *y, void *ws, cudaStream_t st,
+               const moe_lora *lora = nullptr) {
     const WsLayout L = ws_layout(s);
+    float *xa = at<float>(ws, L.xa), *ha = at<float>(ws, L.ha);
     int path = select_grouped_path(s);
     float cb_b;
     int cb_t2;
@@ -129,8 +134,9 @@ int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const 
     if (path > 0)
         return launch_rc(launch_grouped_fast(path, s, x, offsets, order, wg, wu, wd, q4,
                                              at<int32_t>(ws, L.active), at<float>(ws, L.part), at<void>(ws, L.h),
-                                             y, at<int32_t>(ws, L.err), st));
-    return launch_rc(launch_grouped_simple(s, x, offsets, order, wg, wu, wd, q4, at<void>(ws, L.h), y, st));
+                                             y, at<int32_t>(ws, L.err), st, lora, xa, ha));
+    return launch_rc(launch_grouped_simple(s, x, offsets, order, wg, wu, wd, q4, at<void>(ws, L.h), y, st, lora, xa,
+                                           ha));
 }
 
 }  // namespace
@@ -197,7 +203,7 @@ namespace {
 int forward_impl(const moe_shape &s, const void *x, const void *w_router, const float *b_router, const void *w_gate,
                  const void *w_up, const void *w_down, const moe_q4 *q4, void *out, int32_t *expert_ids_out,
                  float *weights_out, void *workspace, cudaStream_t st, const void *gamma, float eps, void *xn_dst,
-                 const void *resid) {
+                 const void *resid, const moe_lora *lora = nullptr) {
     const WsLayout L = ws_layout(s);
     int32_t *ids = expert_ids_out ? expert_ids_out : at<int32_t>(workspace, L.ids);
     float *w = weights_out ? weights_out : at<float>(workspace, L.weights);
@@ -215,7 +221,7 @@ int forward_impl(const moe_shape &s, const void *x, const void *w_router, const 
         MOE_TRY(do_route(s, xe, w_router, b_router, ids, w, nullptr, nullptr, workspace, st));
         MOE_TRY(do_permute(s, ids, at<int32_t>(workspace, L.counts), offsets, order, pos, workspace, st));
     }
-    MOE_TRY(do_grouped(s, xe, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st));
+    MOE_TRY(do_grouped(s, xe, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st, lora));
     return launch_rc(launch_unpermute(s, y, w, pos, out, st, resid));
 }
 
@@ -237,6 +243,27 @@ int moe_forward(const moe_shape *shape, const void *x, const void *w_router, con
     if (s.T == 0) return MOE_OK;
     return forward_impl(s, x, w_router, b_router, w_gate, w_up, w_down, q4, out, expert_ids_out, weights_out,
                         workspace, reinterpret_cast<cudaStream_t>(stream), nullptr, 0.f, nullptr, nullptr);
+}
+
+int moe_forward_lora(const moe_shape *shape, const void *x, const void *w_router, const float *b_router,
+                     const void *w_gate, const void *w_up, const void *w_down, const moe_q4 *q4, const moe_lora *lora,
+                     void *out, int32_t *expert_ids_out, float *weights_out, void *workspace, size_t workspace_bytes,
+                     moe_stream_t stream) {
+    MOE_TRY(validate_shape(shape));
+    const moe_shape &s = *shape;
+    if (!x || !w_router || !out || !lora) return MOE_ERR_NULLPTR;
+    if (!lora->a_gate || !lora->b_gate || !lora->a_up || !lora->b_up || !lora->a_down || !lora->b_down)
+        return MOE_ERR_NULLPTR;
+    if (lora->rank < 1 || lora->rank > 16 || !std::isfinite(lora->scale)) return MOE_ERR_SHAPE;
+    if (misaligned(lora->a_gate) || misaligned(lora->b_gate) || misaligned(lora->a_up) || misaligned(lora->b_up) ||
+        misaligned(lora->a_down) || misaligned(lora->b_down))
+        return MOE_ERR_ALIGN;
+    MOE_TRY(check_weights(s, w_gate, w_up, w_down, q4));
+    MOE_TRY(check_ws(s, workspace, workspace_bytes));
+    if (misaligned(x) || misaligned(w_router) || misaligned(out)) return MOE_ERR_ALIGN;
+    if (s.T == 0) return MOE_OK;
+    return forward_impl(s, x, w_router, b_router, w_gate, w_up, w_down, q4, out, expert_ids_out, weights_out,
+                        workspace, reinterpret_cast<cudaStream_t>(stream), nullptr, 0.f, nullptr, nullptr, lora);
 }
 
 int moe_forward_rmsnorm(const moe_shape *shape, const void *hs, const void *gamma, float eps, int add_residual,

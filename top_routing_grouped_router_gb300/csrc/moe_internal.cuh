@@ -32,6 +32,8 @@ struct WsLayout {
     size_t hist;       // int32 [chunks][E]: per-chunk expert histograms (multi-block permute)
     size_t h;          // [A][I] intermediate SwiGLU activations (fp32 or bf16)
     size_t y;          // [A][H] expert outputs in permuted order (act dtype)
+    size_t xa;         // fp32 [A][32]: LoRA x . A_gate^T | x . A_up^T (moe_forward_lora)
+    size_t ha;         // fp32 [A][16]: LoRA h . A_down^T
     size_t part;       // tensor-core paths: gathered token rows, counters, tile list
     size_t total;
 };
@@ -97,6 +99,43 @@ __device__ __forceinline__ void record_error(int32_t *err, int code) { atomicCAS
 constexpr size_t kHdrBytes = 2048;
 constexpr size_t kHdrArrivals = 64;
 
+// LoRA terms added by the grouped kernels' epilogues (rank 0: none).  xa [A][32] holds
+// x . A_gate^T in columns 0..15 and x . A_up^T in 16..31; ha [A][16] holds h . A_down^T.
+struct LoraDev {
+    const float *bg, *bu, *bd;  // [E][I][rank], [E][I][rank], [E][H][rank]
+    const float *xa, *ha;
+    int rank;
+    float scale;
+};
+
+// scale * sum_q b[q] v[q] over a 16-float rank vector (b zero beyond the rank).
+__device__ __forceinline__ float lora_dot16(const float *b, const float *v) {
+    const float4 *v4 = reinterpret_cast<const float4 *>(v);
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 a = __ldg(v4 + q);
+        s = fmaf(b[4 * q], a.x, s);
+        s = fmaf(b[4 * q + 1], a.y, s);
+        s = fmaf(b[4 * q + 2], a.z, s);
+        s = fmaf(b[4 * q + 3], a.w, s);
+    }
+    return s;
+}
+// One B row (rank floats) into 16 registers, zero-padded.
+__device__ __forceinline__ void lora_row16(const float *B, size_t row, int rank, float *b) {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) b[q] = q < rank ? __ldg(B + row * rank + q) : 0.f;
+}
+
+// Grouped kernels run all tiles (0), only the gate/up tiles (1) or only the down tiles (2).
+enum : int { kPhaseAll = 0, kPhaseGateUp = 1, kPhaseDown = 2 };
+
+cudaError_t launch_lora_xa(const moe_shape &s, const void *x, const int32_t *order, const int32_t *offsets,
+                           const moe_lora &l, float *xa, cudaStream_t st);
+cudaError_t launch_lora_ha(const moe_shape &s, const void *h, bool h_fp32, bool h_grouped, const int32_t *offsets,
+                           const moe_lora &l, float *ha, cudaStream_t st);
+
 bool route_fuses(const moe_shape &s);
 cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
                          int32_t *ids, float *w, float *margin, int *arrivals, int32_t *err, cudaStream_t st);
@@ -114,13 +153,15 @@ cudaError_t launch_permute(const moe_shape &s, const int32_t *ids, int32_t *coun
                            cudaStream_t st);
 cudaError_t launch_grouped_simple(const moe_shape &s, const void *x, const int32_t *offsets,
                                   const int32_t *order, const void *wg, const void *wu, const void *wd,
-                                  const moe_q4 *q4, void *h, void *y, cudaStream_t st);
+                                  const moe_q4 *q4, void *h, void *y, cudaStream_t st,
+                                  const moe_lora *lora = nullptr, float *xa = nullptr, float *ha = nullptr);
 bool q4_codebook_affine(const float *cb, float *b_out, int *twice_j0);
 bool q4_path_supported(const moe_shape &s);
 size_t q4_part_bytes(const moe_shape &s);
 cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
                       const void *wg, const void *wu, const void *wd, const moe_q4 *q4, float *part, void *h, void *y,
-                      int32_t *err, cudaStream_t st);
+                      int32_t *err, cudaStream_t st, const moe_lora *lora = nullptr, float *xa = nullptr,
+                      float *ha = nullptr);
 cudaError_t launch_unpermute(const moe_shape &s, const void *y, const float *w, const int32_t *pos, void *out,
                              cudaStream_t st, const void *resid = nullptr);
 
