@@ -53,8 +53,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--copies", type=int, default=0, help="weight copies to rotate (0 = automatic)")
     ap.add_argument("--layers", type=int, default=0, help="use only the first N layers (profiling; 0 = all)")
-    ap.add_argument("--entry", choices=["forward", "rmsnorm"], default="forward",
-                    help="moe_forward, or moe_forward_rmsnorm (pre-router RMSNorm and residual fused in)")
+    ap.add_argument("--entry", choices=["forward", "rmsnorm", "lora"], default="forward",
+                    help="moe_forward, moe_forward_rmsnorm (pre-router RMSNorm and residual fused in) or "
+                         "moe_forward_lora (synthetic rank-16 fp32 adapters on the expert projections)")
     return ap.parse_args()
 
 
@@ -252,10 +253,21 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream(device=dev)
 
     gammas = [to_device(synth.make_norm_weight(l.H, l.act, seed=l.T, layer=i), dev) for i, l in enumerate(layers)]
+    loras, lora_keep = [], []
+    if args.entry == "lora":
+        names = ("a_gate", "b_gate", "a_up", "b_up", "a_down", "b_down")
+        for i, l in enumerate(layers):
+            ad = synth.make_lora(l.E, l.H, l.I, rank=16, seed=l.T, layer=i)
+            t = [to_device(ad[n], dev) for n in names]
+            lora_keep.append(t)
+            loras.append(moe.make_lora(ad["rank"], ad["scale"], *t))
 
     def forward(c, st=None):
         for l, L in enumerate(dl[c]):
-            if args.entry == "rmsnorm":
+            if args.entry == "lora":
+                moe.moe_forward_lora(L.shape, L.x, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4,
+                                     loras[l], outs[l], workspace=wss[l], stream=st)
+            elif args.entry == "rmsnorm":
                 moe.moe_forward_rmsnorm(L.shape, L.x, gammas[l], 1e-6, L.w_router, L.b_router, L.w_gate, L.w_up,
                                         L.w_down, L.q4, outs[l], workspace=wss[l], stream=st)
             else:
@@ -401,8 +413,9 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if inp0.act == "bf16" else "f32",
         "data": "synthetic: seeded N(0,1) tokens, N(0,1/fan_in) random-init weights of the model's shapes",
-        "config": {"workload": DESCR[args.workload], "entry": f"moe_{args.entry}" if args.entry == "forward" else
-                   "moe_forward_rmsnorm (pre-router RMSNorm + residual fused)", "T": T, "H": H, "E": E, "k": k, "I": I,
+        "config": {"workload": DESCR[args.workload],
+                   "entry": {"forward": "moe_forward", "rmsnorm": "moe_forward_rmsnorm (pre-router RMSNorm + residual)",
+                             "lora": "moe_forward_lora (rank-16 fp32 adapters on the expert projections)"}[args.entry], "T": T, "H": H, "E": E, "k": k, "I": I,
                    "layers": len(layers), "weights": inp0.w, "active_experts": n_active,
                    "l2": f"inputs larger than L2: {n_copies} rotating weight cop{'y' if n_copies == 1 else 'ies'} "
                          f"({n_copies * per_copy / 1e9:.1f} GB), one moe_forward graph per copy",

@@ -593,7 +593,7 @@ size_t q4_part_bytes(const moe_shape &s) {
 
 cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
                       const void *wg, const void *wu, const void *wd, const moe_q4 *q4, float *part, void *h, void *y,
-                      int32_t *err, cudaStream_t st, const moe_lora *lora, float *xa, float *ha) {
+                      int32_t *err, cudaStream_t st, const moe_lora *lora, float *xa, float *ha, float *lpart) {
     float b = 0;
     int t2 = 0;
     if (!q4 || !q4_codebook_affine(q4->codebook, &b, &t2)) return cudaErrorInvalidValue;
@@ -654,10 +654,10 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     if (!lora) return run(prm, std::false_type{});
     // with adapters: x . A^T, the gate/up tiles, h . A_down^T (h in the grouped column order), the down tiles
     prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
-    if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, st)) != cudaSuccess) return e;
+    if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, lpart, st)) != cudaSuccess) return e;
     prm.phase = kPhaseGateUp;
     if ((e = run(prm, std::true_type{})) != cudaSuccess) return e;
-    if ((e = launch_lora_ha(s, h, false, true, offsets, *lora, ha, st)) != cudaSuccess) return e;
+    if ((e = launch_lora_ha(s, h, false, true, offsets, *lora, ha, lpart, st)) != cudaSuccess) return e;
     prm.phase = kPhaseDown;
     return run(prm, std::true_type{});
 }

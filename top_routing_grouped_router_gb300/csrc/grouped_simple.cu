@@ -120,11 +120,11 @@ down_simple_kernel(const float *__restrict__ h, const int32_t *__restrict__ offs
 template <typename ActT, int WFMT>
 cudaError_t launch_typed(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
                          const void *wg, const void *wu, const void *wd, const moe_q4 *q4, void *h, void *y,
-                         cudaStream_t st, const moe_lora *lora, float *xa, float *ha) {
+                         cudaStream_t st, const moe_lora *lora, float *xa, float *ha, float *lpart) {
     LoraDev lr{};
     if (lora) {
         lr = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
-        const cudaError_t e = launch_lora_xa(s, x, order, offsets, *lora, xa, st);
+        const cudaError_t e = launch_lora_xa(s, x, order, offsets, *lora, xa, lpart, st);
         if (e != cudaSuccess) return e;
     }
     const int A = s.T * s.k;
@@ -147,7 +147,7 @@ cudaError_t launch_typed(const moe_shape &s, const void *x, const int32_t *offse
         if (e != cudaSuccess) return e;
     }
     if (lora) {
-        const cudaError_t e = launch_lora_ha(s, h, true, false, offsets, *lora, ha, st);
+        const cudaError_t e = launch_lora_ha(s, h, true, false, offsets, *lora, ha, lpart, st);
         if (e != cudaSuccess) return e;
     }
     for (int p0 = 0; p0 < A; p0 += 65535) {
@@ -170,13 +170,14 @@ int grouped_simple_launches(const moe_shape &s) {
 
 cudaError_t launch_grouped_simple(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
                                   const void *wg, const void *wu, const void *wd, const moe_q4 *q4, void *h,
-                                  void *y, cudaStream_t st, const moe_lora *lora, float *xa, float *ha) {
+                                  void *y, cudaStream_t st, const moe_lora *lora, float *xa, float *ha,
+                                  float *lpart) {
     if (s.T == 0) return cudaSuccess;
     if (s.act_dtype == MOE_DT_F32)
-        return launch_typed<float, MOE_DT_F32>(s, x, offsets, order, wg, wu, wd, q4, h, y, st, lora, xa, ha);
+        return launch_typed<float, MOE_DT_F32>(s, x, offsets, order, wg, wu, wd, q4, h, y, st, lora, xa, ha, lpart);
     if (s.w_dtype == MOE_DT_BF16)
-        return launch_typed<uint16_t, MOE_DT_BF16>(s, x, offsets, order, wg, wu, wd, q4, h, y, st, lora, xa, ha);
-    return launch_typed<uint16_t, MOE_DT_Q4>(s, x, offsets, order, wg, wu, wd, q4, h, y, st, lora, xa, ha);
+        return launch_typed<uint16_t, MOE_DT_BF16>(s, x, offsets, order, wg, wu, wd, q4, h, y, st, lora, xa, ha, lpart);
+    return launch_typed<uint16_t, MOE_DT_Q4>(s, x, offsets, order, wg, wu, wd, q4, h, y, st, lora, xa, ha, lpart);
 }
 
 }  // namespace moe

@@ -497,8 +497,8 @@ int grouped_fast_launches(int path, const moe_shape &) { return path == 1 || pat
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
                                 const moe_q4 *q4, const int32_t *, float *part, void *h, void *y, int32_t *err,
-                                cudaStream_t st, const moe_lora *lora, float *xa, float *ha) {
-    if (path == 2) return launch_q4(s, x, offsets, order, wg, wu, wd, q4, part, h, y, err, st, lora, xa, ha);
+                                cudaStream_t st, const moe_lora *lora, float *xa, float *ha, float *lpart) {
+    if (path == 2) return launch_q4(s, x, offsets, order, wg, wu, wd, q4, part, h, y, err, st, lora, xa, ha, lpart);
     if (path != 1) return cudaErrorInvalidValue;
     const int A = s.T * s.k;
     char *base = reinterpret_cast<char *>(part);
@@ -545,10 +545,10 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
                          : launch_tc<kMaxN, 4, true>(grid, st, mg, mu, md, mx, mh, pr);
     };
     prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
-    if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, st)) != cudaSuccess) return e;
+    if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, lpart, st)) != cudaSuccess) return e;
     prm.phase = kPhaseGateUp;
     if ((e = run(prm)) != cudaSuccess) return e;
-    if ((e = launch_lora_ha(s, h, false, false, offsets, *lora, ha, st)) != cudaSuccess) return e;
+    if ((e = launch_lora_ha(s, h, false, false, offsets, *lora, ha, lpart, st)) != cudaSuccess) return e;
     prm.phase = kPhaseDown;
     return run(prm);
 }

@@ -6,16 +6,22 @@
 // computed here on CUDA cores in fp32:
 //   xa[p][0..r)   = x_t . A_gate[e]^T,  xa[p][16..16+r) = x_t . A_up[e]^T    (t = order[p] / k)
 //   ha[p][0..r)   = h[p] . A_down[e]^T                                      (after the gate/up tiles)
-// A block takes 8 consecutive permuted rows; each warp owns a few rank vectors and keeps
-// one column slice of them in registers while the block's rows (mostly of one expert)
-// stream past, so an expert's A matrices are read once per 8 rows.
+//
+// A block takes 4 consecutive permuted rows and one slice of the input dim; warp w owns
+// rank vectors w, w + 8, ...; each lane covers 8 consecutive columns per step with 16-byte
+// loads, and consecutive rows of the same expert reuse the A values already in registers.
+// Small batches (few rows, mostly of distinct experts) cut the input dim into slices of
+// 256 so that enough blocks stream the adapters in parallel; the slice partial sums are
+// added in a second launch in a fixed order, so the result does not depend on timing.
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kRowsPerBlock = 8;
+constexpr int kRowsPerBlock = 4;
 constexpr int kLWarps = 8;
+constexpr int kSliceCols = 256;      // input columns per block when the dim is split
+constexpr int kSplitMaxRows = 1024;  // split only below this many permuted rows
 
 __device__ __forceinline__ int expert_of_row(const int32_t *offsets, int E, int p) {
     int lo = 0, hi = E;
@@ -26,31 +32,42 @@ __device__ __forceinline__ int expert_of_row(const int32_t *offsets, int E, int 
     return lo;
 }
 
-template <typename T>
-__device__ __forceinline__ float ld_act(const T *p, size_t i) {
-    if constexpr (sizeof(T) == 4) return __ldg(reinterpret_cast<const float *>(p) + i);
-    else return bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t *>(p) + i));
+// 8 consecutive source values from column c (a multiple of 8) of a row.  The 4-bit path
+// stores each 8-element group of h in the order (0,4,1,5,2,6,3,7) (grouped = 1).
+__device__ __forceinline__ void load8(const float *row, int c, int grouped, float *v) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(row + c));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(row + c) + 1);
+    const float t[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = grouped ? t[((i & 3) << 1) | (i >> 2)] : t[i];
+}
+__device__ __forceinline__ void load8(const uint16_t *row, int c, int grouped, float *v) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(row + c));
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    float t[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        t[2 * i] = __uint_as_float(w[i] << 16);
+        t[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+    // stored position q holds element ((q & 1) << 2) | (q >> 1); element i sits at ((i & 3) << 1) | (i >> 2)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = grouped ? t[((i & 3) << 1) | (i >> 2)] : t[i];
 }
 
-// Stored column of logical column c of an h row: the 4-bit path keeps each 8-element group
-// in the order (0,4,1,5,2,6,3,7).
-__device__ __forceinline__ int h_col(int c, int grouped) {
-    return grouped ? (c & ~7) | (((c & 3) << 1) | ((c & 7) >> 2)) : c;
-}
-
-// out[p][v] = src_row(p) . Amat(e, v) for the kNV rank vectors v of a row (vectors whose
-// index within their matrix is >= rank are skipped).  kNV = 32: A_gate (v < 16) and A_up
-// (v >= 16) over x; kNV = 16: A_down over h.
+// out[(p * slices + slice) * kNV + v] = sum over this slice's columns of src_row(p)[c] * Amat(e, v)[c].
 template <typename SrcT, int kNV>
 __global__ void __launch_bounds__(kLWarps * 32)
-lora_a_kernel(const SrcT *__restrict__ src, const int32_t *__restrict__ order, int k, int by_token,
-              int grouped_cols, const int32_t *__restrict__ offsets, int E, int A, int len,
+lora_a_kernel(const SrcT *__restrict__ src, const int32_t *__restrict__ order, int k, int by_token, int grouped,
+              const int32_t *__restrict__ offsets, int E, int A, int len, int slice_cols,
               const float *__restrict__ a0, const float *__restrict__ a1, int rank, float *__restrict__ out) {
     constexpr int kVPW = kNV / kLWarps;  // rank vectors per warp
     griddep_launch_dependents();
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pb = blockIdx.x * kRowsPerBlock;
+    const int slice = blockIdx.y, slices = gridDim.y;
+    const int c_lo = slice * slice_cols, c_hi = min(len, c_lo + slice_cols);
     int rows[kRowsPerBlock], ex[kRowsPerBlock];
 #pragma unroll
     for (int i = 0; i < kRowsPerBlock; ++i) {
@@ -73,8 +90,8 @@ lora_a_kernel(const SrcT *__restrict__ src, const int32_t *__restrict__ order, i
     for (int i = 0; i < kRowsPerBlock; ++i)
 #pragma unroll
         for (int v = 0; v < kVPW; ++v) acc[i][v] = 0.f;
-    for (int c = lane; c < len; c += 32) {
-        float av[kVPW];
+    for (int c = c_lo + lane * 8; c < c_hi; c += 32 * 8) {
+        float av[kVPW][8];
         int ecached = -1;
 #pragma unroll
         for (int i = 0; i < kRowsPerBlock; ++i) {
@@ -83,15 +100,26 @@ lora_a_kernel(const SrcT *__restrict__ src, const int32_t *__restrict__ order, i
                 ecached = ex[i];
 #pragma unroll
                 for (int v = 0; v < kVPW; ++v) {
-                    const int vi = warp * kVPW + v;          // 0..kNV-1
-                    const int q = vi & 15;                    // index within its matrix
+                    const int vi = v * kLWarps + warp;  // 0..kNV-1
+                    const int q = vi & 15;              // index within its matrix
                     const float *am = (kNV == 32 && vi >= 16) ? a1 : a0;
-                    av[v] = q < rank ? __ldg(am + ((size_t)ecached * rank + q) * len + c) : 0.f;
+                    if (q < rank) {
+                        const float4 *ap = reinterpret_cast<const float4 *>(am + ((size_t)ecached * rank + q) * len + c);
+                        const float4 x0 = __ldg(ap), x1 = __ldg(ap + 1);
+                        av[v][0] = x0.x; av[v][1] = x0.y; av[v][2] = x0.z; av[v][3] = x0.w;
+                        av[v][4] = x1.x; av[v][5] = x1.y; av[v][6] = x1.z; av[v][7] = x1.w;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) av[v][j] = 0.f;
+                    }
                 }
             }
-            const float xv = ld_act(src, (size_t)rows[i] * len + h_col(c, grouped_cols));
+            float xv[8];
+            load8(src + (size_t)rows[i] * len, c, grouped, xv);
 #pragma unroll
-            for (int v = 0; v < kVPW; ++v) acc[i][v] = fmaf(xv, av[v], acc[i][v]);
+            for (int v = 0; v < kVPW; ++v)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][v] = fmaf(xv[j], av[v][j], acc[i][v]);
         }
     }
 #pragma unroll
@@ -99,34 +127,66 @@ lora_a_kernel(const SrcT *__restrict__ src, const int32_t *__restrict__ order, i
 #pragma unroll
         for (int v = 0; v < kVPW; ++v) {
             const float s = warp_sum(acc[i][v]);
-            if (lane == 0 && pb + i < A) out[(size_t)(pb + i) * kNV + warp * kVPW + v] = s;
+            if (lane == 0 && pb + i < A) out[((size_t)(pb + i) * slices + slice) * kNV + v * kLWarps + warp] = s;
         }
+}
+
+// out[p][v] = sum_{s < slices} part[p][s][v], in slice order.
+template <int kNV>
+__global__ void __launch_bounds__(256)
+lora_reduce_kernel(const float *__restrict__ part, int A, int slices, float *__restrict__ out) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    if (i >= A * kNV) return;
+    const int p = i / kNV, v = i % kNV;
+    float s = 0.f;
+    for (int sl = 0; sl < slices; ++sl) s += part[((size_t)p * slices + sl) * kNV + v];
+    out[i] = s;
+}
+
+template <typename SrcT, int kNV>
+cudaError_t launch_a(const moe_shape &s, const SrcT *src, const int32_t *order, int by_token, int grouped,
+                     const int32_t *offsets, int len, const float *a0, const float *a1, int rank, float *out,
+                     float *part, cudaStream_t st) {
+    const int A = s.T * s.k;
+    if (A == 0) return cudaSuccess;
+    const int slices = A < kSplitMaxRows ? (len + kSliceCols - 1) / kSliceCols : 1;
+    const dim3 grid((A + kRowsPerBlock - 1) / kRowsPerBlock, slices);
+    const int slice_cols = slices > 1 ? kSliceCols : len;
+    cudaError_t e = launch_pdl(lora_a_kernel<SrcT, kNV>, grid, dim3(kLWarps * 32), 0, st, src, order, s.k, by_token,
+                               grouped, offsets, s.E, A, len, slice_cols, a0, a1, rank, slices > 1 ? part : out);
+    if (e != cudaSuccess || slices == 1) return e;
+    return launch_pdl(lora_reduce_kernel<kNV>, dim3((A * kNV + 255) / 256), dim3(256), 0, st,
+                      static_cast<const float *>(part), A, slices, out);
 }
 
 }  // namespace
 
+// Scratch floats the A-side products need besides xa / ha (slice partial sums).
+size_t lora_part_floats(const moe_shape &s) {
+    const size_t A = (size_t)s.T * s.k;
+    if (A >= (size_t)kSplitMaxRows) return 0;
+    const size_t sx = (s.H + kSliceCols - 1) / kSliceCols, sh = (s.I + kSliceCols - 1) / kSliceCols;
+    return A * (sx > sh ? sx * 32 : sh * 16);
+}
+
 cudaError_t launch_lora_xa(const moe_shape &s, const void *x, const int32_t *order, const int32_t *offsets,
-                           const moe_lora &l, float *xa, cudaStream_t st) {
-    const int A = s.T * s.k;
-    if (A == 0) return cudaSuccess;
-    const dim3 grid((A + kRowsPerBlock - 1) / kRowsPerBlock);
+                           const moe_lora &l, float *xa, float *part, cudaStream_t st) {
     if (s.act_dtype == MOE_DT_F32)
-        return launch_pdl(lora_a_kernel<float, 32>, grid, dim3(kLWarps * 32), 0, st, static_cast<const float *>(x),
-                          order, s.k, 1, 0, offsets, s.E, A, s.H, l.a_gate, l.a_up, l.rank, xa);
-    return launch_pdl(lora_a_kernel<uint16_t, 32>, grid, dim3(kLWarps * 32), 0, st, static_cast<const uint16_t *>(x),
-                      order, s.k, 1, 0, offsets, s.E, A, s.H, l.a_gate, l.a_up, l.rank, xa);
+        return launch_a<float, 32>(s, static_cast<const float *>(x), order, 1, 0, offsets, s.H, l.a_gate, l.a_up,
+                                   l.rank, xa, part, st);
+    return launch_a<uint16_t, 32>(s, static_cast<const uint16_t *>(x), order, 1, 0, offsets, s.H, l.a_gate, l.a_up,
+                                  l.rank, xa, part, st);
 }
 
 cudaError_t launch_lora_ha(const moe_shape &s, const void *h, bool h_fp32, bool h_grouped, const int32_t *offsets,
-                           const moe_lora &l, float *ha, cudaStream_t st) {
-    const int A = s.T * s.k;
-    if (A == 0) return cudaSuccess;
-    const dim3 grid((A + kRowsPerBlock - 1) / kRowsPerBlock);
+                           const moe_lora &l, float *ha, float *part, cudaStream_t st) {
     if (h_fp32)
-        return launch_pdl(lora_a_kernel<float, 16>, grid, dim3(kLWarps * 32), 0, st, static_cast<const float *>(h),
-                          nullptr, s.k, 0, int(h_grouped), offsets, s.E, A, s.I, l.a_down, l.a_down, l.rank, ha);
-    return launch_pdl(lora_a_kernel<uint16_t, 16>, grid, dim3(kLWarps * 32), 0, st, static_cast<const uint16_t *>(h),
-                      nullptr, s.k, 0, int(h_grouped), offsets, s.E, A, s.I, l.a_down, l.a_down, l.rank, ha);
+        return launch_a<float, 16>(s, static_cast<const float *>(h), nullptr, 0, int(h_grouped), offsets, s.I,
+                                   l.a_down, l.a_down, l.rank, ha, part, st);
+    return launch_a<uint16_t, 16>(s, static_cast<const uint16_t *>(h), nullptr, 0, int(h_grouped), offsets, s.I,
+                                  l.a_down, l.a_down, l.rank, ha, part, st);
 }
 
 }  // namespace moe

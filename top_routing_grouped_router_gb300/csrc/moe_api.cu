@@ -15,7 +15,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
                                 const moe_q4 *q4, const int32_t *active, float *part, void *h, void *y,
                                 int32_t *err, cudaStream_t st, const moe_lora *lora = nullptr, float *xa = nullptr,
-                                float *ha = nullptr);
+                                float *ha = nullptr, float *lpart = nullptr);
 size_t grouped_fast_part_bytes(int path, const moe_shape &s);
 int grouped_fast_launches(int path, const moe_shape &s);
 int route_launches(const moe_shape &s);
@@ -67,6 +67,7 @@ WsLayout ws_layout(const moe_shape &s) {
     L.y = take(A * s.H * act_bytes(s));
     L.xa = take(A * 32 * 4);
     L.ha = take(A * 16 * 4);
+    L.lpart = take(lora_part_floats(s) * 4);
     L.part = take(grouped_fast_part_bytes(select_grouped_path(s), s));
     L.total = off;
     return L;
@@ -126,7 +127,7 @@ int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const 
                const void *wu, const void *wd, const moe_q4 *q4, void *y, void *ws, cudaStream_t st,
                const moe_lora *lora = nullptr) {
     const WsLayout L = ws_layout(s);
-    float *xa = at<float>(ws, L.xa), *ha = at<float>(ws, L.ha);
+    float *xa = at<float>(ws, L.xa), *ha = at<float>(ws, L.ha), *lpart = at<float>(ws, L.lpart);
     int path = select_grouped_path(s);
     float cb_b;
     int cb_t2;
@@ -134,9 +135,9 @@ int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const 
     if (path > 0)
         return launch_rc(launch_grouped_fast(path, s, x, offsets, order, wg, wu, wd, q4,
                                              at<int32_t>(ws, L.active), at<float>(ws, L.part), at<void>(ws, L.h),
-                                             y, at<int32_t>(ws, L.err), st, lora, xa, ha));
+                                             y, at<int32_t>(ws, L.err), st, lora, xa, ha, lpart));
     return launch_rc(launch_grouped_simple(s, x, offsets, order, wg, wu, wd, q4, at<void>(ws, L.h), y, st, lora, xa,
-                                           ha));
+                                           ha, lpart));
 }
 
 }  // namespace

@@ -34,6 +34,7 @@ struct WsLayout {
     size_t y;          // [A][H] expert outputs in permuted order (act dtype)
     size_t xa;         // fp32 [A][32]: LoRA x . A_gate^T | x . A_up^T (moe_forward_lora)
     size_t ha;         // fp32 [A][16]: LoRA h . A_down^T
+    size_t lpart;      // fp32 slice partial sums of the LoRA A-side products (small batches)
     size_t part;       // tensor-core paths: gathered token rows, counters, tile list
     size_t total;
 };
@@ -131,10 +132,12 @@ __device__ __forceinline__ void lora_row16(const float *B, size_t row, int rank,
 // Grouped kernels run all tiles (0), only the gate/up tiles (1) or only the down tiles (2).
 enum : int { kPhaseAll = 0, kPhaseGateUp = 1, kPhaseDown = 2 };
 
+// A-side LoRA products (lora.cu); `part` holds lora_part_floats() floats of slice sums.
+size_t lora_part_floats(const moe_shape &s);
 cudaError_t launch_lora_xa(const moe_shape &s, const void *x, const int32_t *order, const int32_t *offsets,
-                           const moe_lora &l, float *xa, cudaStream_t st);
+                           const moe_lora &l, float *xa, float *part, cudaStream_t st);
 cudaError_t launch_lora_ha(const moe_shape &s, const void *h, bool h_fp32, bool h_grouped, const int32_t *offsets,
-                           const moe_lora &l, float *ha, cudaStream_t st);
+                           const moe_lora &l, float *ha, float *part, cudaStream_t st);
 
 bool route_fuses(const moe_shape &s);
 cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
@@ -154,14 +157,15 @@ cudaError_t launch_permute(const moe_shape &s, const int32_t *ids, int32_t *coun
 cudaError_t launch_grouped_simple(const moe_shape &s, const void *x, const int32_t *offsets,
                                   const int32_t *order, const void *wg, const void *wu, const void *wd,
                                   const moe_q4 *q4, void *h, void *y, cudaStream_t st,
-                                  const moe_lora *lora = nullptr, float *xa = nullptr, float *ha = nullptr);
+                                  const moe_lora *lora = nullptr, float *xa = nullptr, float *ha = nullptr,
+                                  float *lpart = nullptr);
 bool q4_codebook_affine(const float *cb, float *b_out, int *twice_j0);
 bool q4_path_supported(const moe_shape &s);
 size_t q4_part_bytes(const moe_shape &s);
 cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
                       const void *wg, const void *wu, const void *wd, const moe_q4 *q4, float *part, void *h, void *y,
                       int32_t *err, cudaStream_t st, const moe_lora *lora = nullptr, float *xa = nullptr,
-                      float *ha = nullptr);
+                      float *ha = nullptr, float *lpart = nullptr);
 cudaError_t launch_unpermute(const moe_shape &s, const void *y, const float *w, const int32_t *pos, void *out,
                              cudaStream_t st, const void *resid = nullptr);
 
