@@ -41,7 +41,10 @@ constexpr int kRows = 128;                 // weight rows per tile (MMA M)
 constexpr int kMaxN = 128;                 // tokens per gate/up tile (MMA N, multiple of 16)
 constexpr int kMaxDownN = 256;             // tokens per down tile
 constexpr int kSlab = 64;                  // k elements per stage (one 128-byte swizzle row)
-constexpr int kNBox = 16;                  // token rows per activation TMA box
+constexpr int kNBox = 16;                  // token rows per activation TMA box (small tiles)
+constexpr int kBigBox = 128;               // token rows per box for large tiles: a TMA instruction
+                                           // costs the producer thread about as much as an MMA does
+                                           // the issuer, so large tiles take few, large boxes
 constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
 constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
 constexpr int kEpiWarps = 4;
@@ -115,7 +118,8 @@ template <int BCap, int kStages, bool kLora>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                  const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_x,
-                 const __grid_constant__ CUtensorMap tm_h, const Params p) {
+                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_xb,
+                 const __grid_constant__ CUtensorMap tm_hb, const Params p) {
     constexpr int kBBytes = Cfg<BCap, kStages>::kBBytes;
     constexpr int kStageBytes = Cfg<BCap, kStages>::kStageBytes;
     // TMEM: gate accumulators at column 0, up at kUpCol, of one of kNBuf buffers
@@ -233,12 +237,16 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const int two = d.down != kGateUp && d.N <= BCap / 2 && (kdim / kSlab) % 2 == 0;
             const int nslab = kdim / kSlab;
             const int nstage = two ? nslab / 2 : nslab;
-            const int nbox = d.N / kNBox;
+            // token rows: 16-row boxes for small tiles, 128-row boxes (rows past the tile are
+            // loaded and ignored) once the tile holds more than half a box
+            const bool big = BCap >= kBigBox && !two && d.down != kRouter && d.N > kBigBox / 2;
+            const int box = big ? kBigBox : kNBox;
+            const int nbox = (d.N + box - 1) / box;
             const uint32_t bytes =
-                (d.down != kGateUp && !two ? kABytes : 2 * kABytes) + (two ? 2 : 1) * nbox * kNBox * 128;
+                (d.down != kGateUp && !two ? kABytes : 2 * kABytes) + (two ? 2 : 1) * nbox * box * 128;
             const int wrow = d.down == kRouter ? d.rb * kRows : d.e * (d.down ? p.H : p.I) + d.rb * kRows;
             const CUtensorMap *wmap = d.down == kDown ? &tm_down : &tm_gate;
-            const CUtensorMap *bmap = d.down == kDown ? &tm_h : &tm_x;
+            const CUtensorMap *bmap = d.down == kDown ? (big ? &tm_hb : &tm_h) : (big ? &tm_xb : &tm_x);
             for (int ks = 0; ks < nstage; ++ks) {
                 mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort);
                 int *sm = smeta + 4 * stage;
@@ -261,11 +269,11 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     // one weight slab; the token rows fill the rest of the stage (up to 256)
                     tma_load_2d(a0, wmap, ks * kSlab, wrow, fb);
                     for (int q = 0; q < nbox; ++q)
-                        tma_load_2d(a0 + kABytes + q * 2048, bmap, ks * kSlab, d.r0 + q * kNBox, fb);
+                        tma_load_2d(a0 + kABytes + q * box * 128, bmap, ks * kSlab, d.r0 + q * box, fb);
                 } else {
                     tma_load_2d(a0, &tm_gate, ks * kSlab, wrow, fb);
                     tma_load_2d(a0 + kABytes, &tm_up, ks * kSlab, wrow, fb);
-                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * 2048, &tm_x, ks * kSlab, d.r0 + q * kNBox, fb);
+                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * box * 128, bmap, ks * kSlab, d.r0 + q * box, fb);
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
@@ -443,10 +451,11 @@ bool set_smem_attr() {
 
 template <int BCap, int Stages, bool Lora = false>
 cudaError_t launch_tc(dim3 grid, cudaStream_t st, const CUtensorMap &mg, const CUtensorMap &mu, const CUtensorMap &md,
-                      const CUtensorMap &mx, const CUtensorMap &mh, const Params &prm) {
+                      const CUtensorMap &mx, const CUtensorMap &mh, const CUtensorMap &mxb, const CUtensorMap &mhb,
+                      const Params &prm) {
     if (!set_smem_attr<BCap, Stages, Lora>()) return cudaErrorInvalidValue;
     return launch_pdl(tc_swiglu_kernel<BCap, Stages, Lora>, grid, dim3(kThreads), Cfg<BCap, Stages>::kSmemBytes, st, mg,
-                      mu, md, mx, mh, prm);
+                      mu, md, mx, mh, mxb, mhb, prm);
 }
 
 }  // namespace
@@ -470,7 +479,7 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
     prm.T = s.T;
     prm.logits = logits;
     prm.bias = bias;
-    return launch_tc<kMaxN, 4>(dim3(std::min(tiles, tc::sm_count())), st, mw, mw, mw, mx, mx, prm);
+    return launch_tc<kMaxN, 4>(dim3(std::min(tiles, tc::sm_count())), st, mw, mw, mw, mx, mx, mx, mx, prm);
 }
 
 // 0 = the per-output-element kernels of grouped_simple.cu; 1 = the bf16 tensor-core
@@ -512,6 +521,9 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
         !tc::make_map(&md, wd, (uint64_t)s.E * s.H, s.I, kRows) || !tc::make_map(&mx, x_perm, A, s.H, kNBox) ||
         !tc::make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
+    CUtensorMap mxb, mhb;
+    if (!tc::make_map(&mxb, x_perm, A, s.H, kBigBox) || !tc::make_map(&mhb, h, A, s.I, kBigBox))
+        return cudaErrorInvalidValue;
 
     const int cmax = kMaxN;
     const int dmax = kMaxDownN;
@@ -538,11 +550,11 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (!lora)
-        return s.T <= 32 ? launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, prm)
-                         : launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, prm);
+        return s.T <= 32 ? launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, mxb, mhb, prm)
+                         : launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, mxb, mhb, prm);
     auto run = [&](const Params &pr) {
-        return s.T <= 32 ? launch_tc<32, 6, true>(grid, st, mg, mu, md, mx, mh, pr)
-                         : launch_tc<kMaxN, 4, true>(grid, st, mg, mu, md, mx, mh, pr);
+        return s.T <= 32 ? launch_tc<32, 6, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, pr)
+                         : launch_tc<kMaxN, 4, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, pr);
     };
     prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
     if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, lpart, st)) != cudaSuccess) return e;

@@ -112,7 +112,7 @@ __device__ void group_rms(const ActT *__restrict__ x, int H, float eps, int tg, 
 }
 
 // logits[t][e] for e in [e0, e0+4) and t in [t0, t0+8), t < T.
-template <typename ActT>
+template <typename ActT, bool kNorm>
 __device__ void router_block(const ActT *__restrict__ x, const ActT *__restrict__ wr, const float *__restrict__ bias,
                              float *__restrict__ logits, int T, int H, int E, int e0, int t0,
                              float (*s_part)[kEPB * kTG], const NormArgs &nm, float *s_rms) {
@@ -121,11 +121,11 @@ __device__ void router_block(const ActT *__restrict__ x, const ActT *__restrict_
     const int nchunk = H / V;
     const int ne = min(kEPB, E - e0);
     const int tend = min(T, t0 + kTPB);
-    const ActT *gamma = static_cast<const ActT *>(nm.gamma);
+    const ActT *gamma = kNorm ? static_cast<const ActT *>(nm.gamma) : nullptr;
     ActT *xn = e0 == 0 ? static_cast<ActT *>(nm.xn) : nullptr;
     for (int tg = t0; tg < tend; tg += kTG) {
         const int nt = min(kTG, T - tg);
-        if (gamma) group_rms<ActT>(x, H, nm.eps, tg, nt, s_part, s_rms);
+        if (kNorm) group_rms<ActT>(x, H, nm.eps, tg, nt, s_part, s_rms);
         float acc[kEPB][kTG];
 #pragma unroll
         for (int i = 0; i < kEPB; ++i)
@@ -141,13 +141,13 @@ __device__ void router_block(const ActT *__restrict__ x, const ActT *__restrict_
                     for (int v = 0; v < V; ++v) wv[ee][v] = 0.f;
             }
             float gv[V];
-            if (gamma) Vec<ActT>::load(gamma + (size_t)c * V, gv);
+            if (kNorm) Vec<ActT>::load(gamma + (size_t)c * V, gv);
 #pragma unroll
             for (int tt = 0; tt < kTG; ++tt) {
                 if (tt < nt) {
                     float xv[V];
                     Vec<ActT>::load(x + (size_t)(tg + tt) * H + (size_t)c * V, xv);
-                    if (gamma) {
+                    if (kNorm) {
                         const float rms = s_rms[tt];
 #pragma unroll
                         for (int v = 0; v < V; ++v) xv[v] = Vec<ActT>::round(__fdiv_rn(xv[v], rms) * gv[v]);
@@ -256,7 +256,7 @@ struct RouteArgs {
     NormArgs norm_in;         // optional pre-router RMSNorm of x
 };
 
-template <typename ActT>
+template <typename ActT, bool kNorm>
 __global__ void __launch_bounds__(kRThreads)
 route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const float *__restrict__ bias, RouteArgs a) {
     __shared__ float s_part[kRWarps][kEPB * kTG];
@@ -264,8 +264,8 @@ route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const floa
     __shared__ int s_last;
     griddep_launch_dependents();
     griddep_wait();  // the previous kernel in the stream may still read this workspace
-    router_block<ActT>(x, wr, bias, a.logits, a.T, a.H, a.E, blockIdx.x * kEPB, blockIdx.y * kTPB, s_part, a.norm_in,
-                       s_rms);
+    router_block<ActT, kNorm>(x, wr, bias, a.logits, a.T, a.H, a.E, blockIdx.x * kEPB, blockIdx.y * kTPB, s_part,
+                              a.norm_in, s_rms);
     if (!a.fuse) return;
     // the last expert block of this token group to finish sees all its logits: top-k,
     // one warp per token
@@ -339,10 +339,14 @@ rmsnorm_kernel(const ActT *__restrict__ x, const ActT *__restrict__ gamma, float
 cudaError_t launch_route_kernel(const moe_shape &s, const void *x, const void *wr, const float *bias,
                                 const RouteArgs &a, cudaStream_t st) {
     dim3 grid((s.E + kEPB - 1) / kEPB, (s.T + kTPB - 1) / kTPB);
-    if (s.act_dtype == MOE_DT_F32)
-        return launch_pdl(route_kernel<float>, grid, dim3(kRThreads), 0, st, static_cast<const float *>(x),
+    const bool norm = a.norm_in.gamma != nullptr;
+    if (s.act_dtype == MOE_DT_F32) {
+        auto k = norm ? route_kernel<float, true> : route_kernel<float, false>;
+        return launch_pdl(k, grid, dim3(kRThreads), 0, st, static_cast<const float *>(x),
                           static_cast<const float *>(wr), bias, a);
-    return launch_pdl(route_kernel<uint16_t>, grid, dim3(kRThreads), 0, st, static_cast<const uint16_t *>(x),
+    }
+    auto k = norm ? route_kernel<uint16_t, true> : route_kernel<uint16_t, false>;
+    return launch_pdl(k, grid, dim3(kRThreads), 0, st, static_cast<const uint16_t *>(x),
                       static_cast<const uint16_t *>(wr), bias, a);
 }
 
