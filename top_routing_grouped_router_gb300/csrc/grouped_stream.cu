@@ -19,10 +19,11 @@
 // of every gate/up tile of its expert has published h.
 //
 // Roles per CTA (one CTA per SM): warp 0 lane 0 issues TMA loads into a 4-6 stage ring;
-// warp 1 owns the TMEM allocation and lane 0 issues the MMAs (tcgen05.commit frees a
-// stage when its MMAs are done, and hands a finished accumulator to the epilogue);
-// warps 2-5 are the epilogue (warp w reads TMEM lanes 32*(w%4)..+31), with two
-// accumulator buffers so the epilogue of one tile overlaps the MMAs of the next.
+// warp 1 owns the TMEM allocation and issues the MMAs, converged, through one elected
+// lane (tcgen05.commit frees a stage when its MMAs are done, and hands a finished
+// accumulator to the epilogue); warps 2-9 are the epilogue (warp w reads TMEM lanes
+// 32*(w%4)..+31, the two warps of a lane quadrant alternating over 32-column groups),
+// with two accumulator buffers so the epilogue of one tile overlaps the MMAs of the next.
 //
 // The token rows are first gathered into permuted order (x_perm) so that every
 // expert's rows are contiguous for TMA; the same prep kernel builds the tile list.
@@ -47,7 +48,7 @@ constexpr int kBigBox = 128;               // token rows per box for large tiles
                                            // the issuer, so large tiles take few, large boxes
 constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
 constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;               // two per TMEM lane quadrant, splitting the columns
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kMetaRing = 8;
 constexpr int kCtrlBytes = 1024;
@@ -70,7 +71,7 @@ enum : int { kGateUp = 0, kDown = 1, kRouter = 2 };
 
 struct Params {
     const int32_t *offsets;     // [E+1]
-    const uint32_t *tiles;      // tile list
+    const uint4 *tiles;         // tile records (grouped_tiles.cuh)
     int *sched;                 // scheduling words (grouped_tiles.cuh)
     int phase;                  // kPhaseAll / kPhaseGateUp / kPhaseDown
     LoraDev lora;               // LoRA B-side terms of the epilogue (rank 0: none)
@@ -89,26 +90,28 @@ struct Params {
 };
 
 struct TileInfo {
-    int down, e, rb, r0, m, N;
+    int down, e, rb, r0, m, N, need;
 };
 
-__device__ __forceinline__ TileInfo read_tile(uint32_t entry, const Params &p, bool &ok) {
+// A tile record checked against the shapes: rows within the permuted range and within
+// what the tile kind holds (cap_gu tokens for gate/up, cap_dn for down).
+__device__ __forceinline__ TileInfo read_tile(uint4 rec, const Params &p, int cap_gu, int cap_dn, bool &ok) {
+    const TileRec r = unpack_rec(rec);
     TileInfo d;
-    d.down = int(entry >> 31);
-    d.e = int((entry >> 16) & 0xFF);
-    d.rb = int((entry >> 8) & 0xFF);
-    const int nc = int(entry & 0xFF);
-    ok = d.e < p.E;
-    const int off = ok ? __ldg(p.offsets + d.e) : 0;
-    const int me = ok ? __ldg(p.offsets + d.e + 1) - off : 0;
-    const int base = d.down == kDown ? chunk_base(me, p.dmax, true) : chunk_base(me, p.cmax, false);
-    d.r0 = off + nc * base;
-    d.m = min(base, me - nc * base);
-    ok = ok && off >= 0 && me >= 0 && off + me <= p.A && d.m > 0;
-    if (!ok) {  // inconsistent offsets or tile entry: load in-range rows, store nothing
+    d.down = r.down;
+    d.e = r.e;
+    d.rb = r.rb;
+    d.r0 = r.r0;
+    d.m = r.m;
+    d.need = r.need;
+    ok = d.e < p.E && d.rb < (d.down ? p.H : p.I) / kRows && d.r0 >= 0 && d.m > 0 && d.m <= p.A - d.r0 &&
+         d.m <= (d.down ? cap_dn : cap_gu);
+    if (!ok) {  // inconsistent record: load in-range rows, store nothing
         d.m = 0;
         d.r0 = 0;
+        d.rb = 0;
         d.e = min(d.e, p.E - 1);
+        d.need = 0;
     }
     d.N = d.m > 0 ? (d.m + 15) & ~15 : 16;
     return d;
@@ -187,11 +190,18 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             lo = p.sched[kSchedGateUp];
             ctr = p.sched + kSchedClaimDown;
         }
+        // the next tile is claimed when this one starts, and its record is loaded a few
+        // stages into this one (when the claim has returned), so neither latency falls
+        // between two tiles; claiming only one ahead keeps the tail balanced when tiles are
+        // long (a decode gate/up tile streams 1 MB of weights)
         int next = router ? int(blockIdx.x) : lo + atomicAdd(ctr, 1);
-        for (;;) {
+        uint4 next_rec = (!router && next < hi) ? __ldg(p.tiles + next) : make_uint4(0, 0, 0, 0);
+        const int cap_dn = min(p.dmax, (kABytes + kBBytes) / 128);
+        bool live = true;
+        while (live) {
             const int t = next;
             if (t >= hi || *abort) break;
-            // claim ahead: the atomic's latency hides behind this tile
+            const uint4 rec = next_rec;
             next = router ? t + int(gridDim.x) : lo + atomicAdd(ctr, 1);
             bool ok = true;
             TileInfo d;
@@ -202,20 +212,14 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 d.r0 = (t / erb) * kRouterN;
                 d.m = min(kRouterN, p.T - d.r0);
                 d.N = (d.m + 15) & ~15;
+                d.need = 0;
             } else {
-                d = read_tile(__ldg(p.tiles + t), p, ok);
+                d = read_tile(rec, p, BCap, cap_dn, ok);
             }
             if (!ok) record_error(p.err, MOE_ERR_DEVICE);
-            if (d.down != kGateUp && d.N * 128 > kABytes + kBBytes) {  // cannot happen: chunks fit the stage
-                record_error(p.err, MOE_ERR_DEVICE);
-                d.N = (kABytes + kBBytes) / 128;
-                d.m = min(d.m, d.N);
-            }
             if (d.down == kDown) {
                 // the expert's h must be complete: every epilogue warp of every gate/up tile
-                const int me = __ldg(p.offsets + d.e + 1) - __ldg(p.offsets + d.e);
-                const int need = (p.I / kRows) * n_chunks(me, p.cmax, false) * kEpiWarps;
-                wait_count(p.done + d.e, need, p.err, abort);
+                wait_count(p.done + d.e, d.need, p.err, abort);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             // hand the tile to the epilogue
@@ -238,8 +242,9 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const int nslab = kdim / kSlab;
             const int nstage = two ? nslab / 2 : nslab;
             // token rows: 16-row boxes for small tiles, 128-row boxes (rows past the tile are
-            // loaded and ignored) once the tile holds more than half a box
-            const bool big = BCap >= kBigBox && !two && d.down != kRouter && d.N > kBigBox / 2;
+            // loaded and ignored) once the tile holds more than half a box and the box fits
+            // its region of the stage
+            const bool big = BCap >= kBigBox && d.down != kRouter && d.N > kBigBox / 2 && (!two || BCap >= 2 * kBigBox);
             const int box = big ? kBigBox : kNBox;
             const int nbox = (d.N + box - 1) / box;
             const uint32_t bytes =
@@ -248,12 +253,19 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const CUtensorMap *wmap = d.down == kDown ? &tm_down : &tm_gate;
             const CUtensorMap *bmap = d.down == kDown ? (big ? &tm_hb : &tm_h) : (big ? &tm_xb : &tm_x);
             for (int ks = 0; ks < nstage; ++ks) {
-                mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort);
-                int *sm = smeta + 4 * stage;
-                sm[0] = d.down | (two << 2);
-                sm[1] = ks;
-                sm[2] = nstage;
-                sm[3] = d.N;
+                if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort)) {
+                    live = false;
+                    break;
+                }
+                if (ks == 0) {  // the tile's shape, read by the MMA issuer at its first stage
+                    int *sm = smeta + 4 * stage;
+                    sm[0] = d.down | (two << 2);
+                    sm[1] = 0;
+                    sm[2] = nstage;
+                    sm[3] = d.N;
+                }
+                if (!router && ks == min(2, nstage - 1))
+                    next_rec = next < hi ? __ldg(p.tiles + next) : make_uint4(0, 0, 0, 0);
                 const uint32_t fb = smem_u32(&full[stage]);
                 mbar_arrive_expect_tx(fb, bytes);
                 const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
@@ -263,7 +275,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                         const int k0 = (2 * ks + h2) * kSlab;
                         tma_load_2d(a0 + h2 * kABytes, wmap, k0, wrow, fb);
                         for (int q = 0; q < nbox; ++q)
-                            tma_load_2d(bb + h2 * (kBBytes / 2) + q * 2048, bmap, k0, d.r0 + q * kNBox, fb);
+                            tma_load_2d(bb + h2 * (kBBytes / 2) + q * box * 128, bmap, k0, d.r0 + q * box, fb);
                     }
                 } else if (d.down != kGateUp) {
                     // one weight slab; the token rows fill the rest of the stage (up to 256)
@@ -285,55 +297,67 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort);
         smeta[4 * stage + 1] = -1;
         mbar_arrive(smem_u32(&full[stage]));
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
+        // The whole warp runs this loop, converged (every branch below is warp-uniform, and
+        // the waits' outcomes are voted), and one elected lane issues each MMA and commit.
+        // The shape of a tile is read once, at its first stage; the stages after it only
+        // wait for their data, so the issue stream is not broken up by shared-memory loads.
         int stage = 0;
         uint32_t phase = 0;
         int tile_count = 0;
         for (;;) {
-            mbar_wait(smem_u32(&full[stage]), phase, p.err, abort);
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, p.err, abort))) break;
             const int *sm = smeta + 4 * stage;
-            const int down = (sm[0] & 3) != kGateUp, two = sm[0] >> 2, ks = sm[1], nslab = sm[2], N = sm[3];
-            if (ks < 0 || *abort) break;
+            const int kind = sm[0], first = sm[1], nstage = sm[2], N = sm[3];
+            if (__any_sync(0xffffffffu, first < 0 || *abort)) break;
+            const int down = (kind & 3) != kGateUp, two = kind >> 2;
             const int b = tile_count % kNBuf;
-            if (ks == 0) {
-                mbar_wait(smem_u32(&acce[b]), ((tile_count / kNBuf) & 1) ^ 1, p.err, abort);
-                tc_fence_after();
-            }
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce[b]), ((tile_count / kNBuf) & 1) ^ 1, p.err, abort)))
+                break;
+            tc_fence_after();
             const uint32_t d = tmem_base + uint32_t(b * kBufCols);
             const uint32_t idesc = instr_desc(kRows, N);
-            const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
-            const uint32_t bb = a0 + 2 * kABytes;
-            if (two) {
+            bool live = true;
+            for (int ks = 0;;) {
+                const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
+                const uint32_t bb = a0 + 2 * kABytes;
+                if (two) {
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2)
+                    for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-                    for (int kk = 0; kk < kSlab / 16; ++kk)
-                        mma_bf16(d, smem_desc(a0 + h2 * kABytes + kk * 32),
-                                 smem_desc(bb + h2 * (kBBytes / 2) + kk * 32), idesc, (ks | h2 | kk) != 0);
-            } else {
+                        for (int kk = 0; kk < kSlab / 16; ++kk)
+                            mma_bf16_warp(d, smem_desc(a0 + h2 * kABytes + kk * 32),
+                                          smem_desc(bb + h2 * (kBBytes / 2) + kk * 32), idesc, (ks | h2 | kk) != 0);
+                } else {
 #pragma unroll
-                for (int kk = 0; kk < kSlab / 16; ++kk) {
-                    const uint32_t acc = (ks | kk) != 0;
-                    const uint64_t bdesc = smem_desc((down ? a0 + kABytes : bb) + kk * 32);
-                    mma_bf16(d, smem_desc(a0 + kk * 32), bdesc, idesc, acc);
-                    if (!down) mma_bf16(d + kUpCol, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, acc);
+                    for (int kk = 0; kk < kSlab / 16; ++kk) {
+                        const uint32_t acc = (ks | kk) != 0;
+                        const uint64_t bdesc = smem_desc((down ? a0 + kABytes : bb) + kk * 32);
+                        mma_bf16_warp(d, smem_desc(a0 + kk * 32), bdesc, idesc, acc);
+                        if (!down) mma_bf16_warp(d + kUpCol, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, acc);
+                    }
+                }
+                mma_commit_warp(smem_u32(&empty[stage]));  // the stage's smem is free once these MMAs are done
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+                if (++ks == nstage) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, p.err, abort))) {
+                    live = false;
+                    break;
                 }
             }
-            mma_commit(smem_u32(&empty[stage]));  // the stage's smem is free once these MMAs are done
-            if (ks == nslab - 1) {
-                mma_commit(smem_u32(&accf[b]));   // accumulator complete: hand to the epilogue
-                ++tile_count;
-            }
-            if (++stage == kStages) { stage = 0; phase ^= 1; }
+            if (!live) break;
+            mma_commit_warp(smem_u32(&accf[b]));  // accumulator complete: hand to the epilogue
+            ++tile_count;
         }
-        // every MMA this thread issued has completed before TMEM is released
-        mma_commit(smem_u32(drain));
+        // every MMA this warp issued has completed before TMEM is released
+        mma_commit_warp(smem_u32(drain));
         mbar_wait(smem_u32(drain), 0, p.err, abort);
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         const int row = 32 * q + lane;
+        const int half = (warp - 2) >> 2;  // which of the quadrant's two warps: alternate 32-column groups
         int slot = 0, tile_count = 0;
         uint32_t mphase = 0;
         for (;;) {
@@ -361,8 +385,10 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     lora_row16(lr.bu, (size_t)e * p.I + col, lr.rank, lb1);
                 }
             }
-            for (int c0 = 0; c0 < N; c0 += 16) {
-                if (down == kRouter) {
+            // TMEM is read 32 columns at a time (gate and up together: one wait per 32
+            // tokens); columns past N are read and ignored (they stay inside the buffer)
+            if (down == kRouter) {
+                for (int c0 = 16 * half; c0 < N; c0 += 32) {
                     float v[16];
                     tmem_ld16(taddr + c0, v);
                     if (col < (size_t)p.E) {
@@ -371,31 +397,34 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                         for (int j = 0; j < 16; ++j)
                             if (c0 + j < m) p.logits[(size_t)(r0 + c0 + j) * p.E + col] = v[j] + b;
                     }
-                } else if (down) {
-                    float v[16];
-                    tmem_ld16(taddr + c0, v);
+                }
+            } else if (down) {
+                for (int c0 = 32 * half; c0 < N; c0 += 64) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + c0, v);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
+                    for (int j = 0; j < 32; ++j)
                         if (c0 + j < m) {
                             const size_t pr = (size_t)(r0 + c0 + j);
-                            float val = v[j];
+                            float val = __uint_as_float(v[j]);
                             if (lora) val += lr.scale * lora_dot16(lb0, lr.ha + pr * 16);
                             p.y[pr * p.H + col] = f32_to_bf16_bits(val);
                         }
-                } else {
-                    float g[16], u[16];
-                    tmem_ld16(taddr + c0, g);
-                    tmem_ld16(taddr + kUpCol + c0, u);
+                }
+            } else {
+                for (int c0 = 32 * half; c0 < N; c0 += 64) {
+                    uint32_t gu[64];
+                    tmem_ld32x2(taddr + c0, taddr + kUpCol + c0, gu);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
+                    for (int j = 0; j < 32; ++j)
                         if (c0 + j < m) {
                             const size_t pr = (size_t)(r0 + c0 + j);
-                            float gv = g[j], uv = u[j];
+                            float gv = __uint_as_float(gu[j]), uv = __uint_as_float(gu[32 + j]);
                             if (lora) {
                                 gv += lr.scale * lora_dot16(lb0, lr.xa + pr * 32);
                                 uv += lr.scale * lora_dot16(lb1, lr.xa + pr * 32 + 16);
                             }
-                            p.h[pr * p.I + col] = f32_to_bf16_bits(swiglu(gv, uv));
+                            p.h[pr * p.I + col] = f32_to_bf16_bits(swiglu_fast(gv, uv));
                         }
                 }
             }
@@ -496,7 +525,7 @@ int select_grouped_path(const moe_shape &s) {
 size_t grouped_fast_part_bytes(int path, const moe_shape &s) {
     if (path == 2) return q4_part_bytes(s);
     if (path != 1) return 0;
-    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (max_tiles(s) * 4 + 255) / 256 * 256;
+    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (max_tiles(s) * 16 + 255) / 256 * 256;
 }
 
 int grouped_fast_launches(int path, const moe_shape &) { return path == 1 || path == 2 ? 2 : 0; }
@@ -514,7 +543,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     uint16_t *x_perm = reinterpret_cast<uint16_t *>(base);
     int *sched = reinterpret_cast<int *>(base + xperm_bytes(s));
     int *done = sched + 64;
-    uint32_t *tiles = reinterpret_cast<uint32_t *>(base + xperm_bytes(s) + 256 + (size_t)kMaxE * 4);
+    uint4 *tiles = reinterpret_cast<uint4 *>(base + xperm_bytes(s) + 256 + (size_t)kMaxE * 4);
 
     CUtensorMap mg, mu, md, mx, mh;
     if (!tc::make_map(&mg, wg, (uint64_t)s.E * s.I, s.H, kRows) || !tc::make_map(&mu, wu, (uint64_t)s.E * s.I, s.H, kRows) ||
@@ -527,7 +556,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
 
     const int cmax = kMaxN;
     const int dmax = kMaxDownN;
-    const TileListArgs ta{cmax, 0, dmax, 1, s.I / kRows, s.H / kRows, (int)max_tiles(s)};
+    const TileListArgs ta{cmax, 0, dmax, 1, s.I / kRows, s.H / kRows, kEpiWarps, (int)max_tiles(s)};
     cudaError_t e = launch_pdl(prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
                                offsets, s.T, s.k, s.H, s.E, ta, x_perm, tiles, sched, done, err);
     if (e != cudaSuccess) return e;

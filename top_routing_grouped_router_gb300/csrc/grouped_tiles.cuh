@@ -3,8 +3,11 @@
 // expert-sorted assignments) are cut into token chunks, and every (expert, chunk) pair
 // yields gate/up tiles (row blocks of I) followed, after all gate/up tiles, by down tiles
 // (row blocks of H); gate/up and down tiles may cut the tokens into chunks of different
-// sizes.  The same kernel gathers the token rows into permuted order
-// (x_perm[p] = x[order[p] / k]) so that every expert's rows are contiguous for TMA.
+// sizes.  Each tile is one 16-byte record holding everything the kernels need (row
+// block, first permuted row, row count, and for a down tile the number of h
+// publications it waits for), so a CTA learns its next tile from a single load.  The
+// same kernel gathers the token rows into permuted order (x_perm[p] = x[order[p] / k])
+// so that every expert's rows are contiguous for TMA.
 #pragma once
 
 #include "moe_internal.cuh"
@@ -27,9 +30,25 @@ __host__ __device__ inline int n_chunks(int me, int cmax, bool even) {
     return b > 0 ? (me + b - 1) / b : 0;
 }
 
-// Tile list entry: bit 31 = down tile, bits 16-23 expert, bits 8-15 row block, bits 0-7 token chunk.
+// Packed tile word: bit 31 = down tile, bits 16-23 expert, bits 8-15 row block, bits 0-7 token chunk.
 __host__ __device__ constexpr uint32_t pack_tile(int down, int e, int rb, int nc) {
     return (uint32_t(down) << 31) | (uint32_t(e) << 16) | (uint32_t(rb) << 8) | uint32_t(nc);
+}
+
+// Tile record of the bf16 kernels: x = packed word, y = first permuted row, z = rows,
+// w = h publications (gate/up epilogue arrivals) a down tile waits for (0 for gate/up).
+struct TileRec {
+    int down, e, rb, r0, m, need;
+};
+__device__ __forceinline__ TileRec unpack_rec(uint4 r) {
+    TileRec t;
+    t.down = int(r.x >> 31);
+    t.e = int((r.x >> 16) & 0xFF);
+    t.rb = int((r.x >> 8) & 0xFF);
+    t.r0 = int(r.y);
+    t.m = int(r.z);
+    t.need = int(r.w);
+    return t;
 }
 
 // Block-wide exclusive scan of one int per thread (blockDim.x == 256).
@@ -66,6 +85,7 @@ struct TileListArgs {
     int dn_cmax, dn_even;  // token chunks of the down tiles
     int gu_per;            // gate/up tiles per chunk (row blocks of I)
     int dn_per;            // down tiles per chunk (row blocks of H)
+    int pub;               // h publications per gate/up tile (epilogue warps that write h)
     int max_tiles;         // capacity of `tiles`
 };
 
@@ -78,7 +98,7 @@ enum : int { kSchedClaim = 0, kSchedTiles = 1, kSchedGateUp = 2, kSchedClaimDown
 // and zeroed per-expert completion counters.  Blocks 1..A: x_perm row blockIdx.x - 1.
 __global__ void __launch_bounds__(256)
 prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
-            int T, int k, int H, int E, TileListArgs ta, uint16_t *__restrict__ x_perm, uint32_t *tiles,
+            int T, int k, int H, int E, TileListArgs ta, uint16_t *__restrict__ x_perm, uint4 *tiles,
             int *sched, int *done, int32_t *err) {
     griddep_launch_dependents();
     griddep_wait();
@@ -97,11 +117,19 @@ prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, c
     }
     __shared__ int s_warp[9];
     const int e = threadIdx.x;
-    int me = 0;
+    const int A = T * k;
+    int me = 0, off = 0;
     if (e < E) {
-        me = min(max(offsets[e + 1] - offsets[e], 0), T * k);
+        off = offsets[e];
+        me = offsets[e + 1] - off;
+        if (off < 0 || me < 0 || off > A || me > A - off) {  // inconsistent offsets: no tiles
+            record_error(err, MOE_ERR_DEVICE);
+            off = me = 0;
+        }
         done[e] = 0;
     }
+    const int bgu = chunk_base(me, ta.gu_cmax, ta.gu_even != 0);
+    const int bdn = chunk_base(me, ta.dn_cmax, ta.dn_even != 0);
     const int nch_gu = n_chunks(me, ta.gu_cmax, ta.gu_even != 0);
     const int nch_dn = n_chunks(me, ta.dn_cmax, ta.dn_even != 0);
     int n_gu, n_dn;
@@ -110,12 +138,15 @@ prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, c
     for (int c = 0; c < nch_gu; ++c)
         for (int r = 0; r < ta.gu_per; ++r) {
             const int i = gu_off + c * ta.gu_per + r;
-            if (i < ta.max_tiles) tiles[i] = pack_tile(0, e, r, c);
+            if (i < ta.max_tiles)
+                tiles[i] = make_uint4(pack_tile(0, e, r, c), uint32_t(off + c * bgu), uint32_t(min(bgu, me - c * bgu)), 0u);
         }
+    const uint32_t need = uint32_t(nch_gu * ta.gu_per * ta.pub);
     for (int c = 0; c < nch_dn; ++c)
         for (int r = 0; r < ta.dn_per; ++r) {
             const int i = n_gu + dn_off + c * ta.dn_per + r;
-            if (i < ta.max_tiles) tiles[i] = pack_tile(1, e, r, c);
+            if (i < ta.max_tiles)
+                tiles[i] = make_uint4(pack_tile(1, e, r, c), uint32_t(off + c * bdn), uint32_t(min(bdn, me - c * bdn)), need);
         }
     if (threadIdx.x == 0) {
         if (n_gu + n_dn > ta.max_tiles) record_error(err, MOE_ERR_DEVICE);  // inconsistent offsets

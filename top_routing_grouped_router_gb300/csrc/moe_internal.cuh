@@ -62,6 +62,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // SiLU(g) * u with an fp32 logistic.
 __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// The same with the hardware exponential and an approximate divide (a few fp32 ulps,
+// far below the bf16 rounding of h): the bf16 tensor-core epilogues, where the SwiGLU's
+// instruction count decides how long an accumulator stays busy.
+__device__ __forceinline__ float swiglu_fast(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 // Programmatic dependent launch: let the next kernel of the stream be scheduled now,
 // and wait until the previous kernel has completed and its writes are visible.
