@@ -8,21 +8,21 @@
 // the weight stream alone.  Both operands are K-major, loaded by TMA as 64-element
 // (128-byte) slabs with the 128-byte swizzle.
 //
-// Tiles: gate/up tile = (expert e, 128 rows of I, 128-token chunk): two MMAs per
-// k-step, gate into TMEM columns [0, N) and up into [128, 128+N), so one epilogue
-// thread (TMEM lane = weight row) holds g and u of the same row and forms
+// Tiles: gate/up tile = (expert e, 128 rows of I, token chunk of up to 128, or up to 256
+// for large batches): two MMAs per k-step, gate and up into two TMEM column ranges, so
+// one epilogue thread (TMEM lane = weight row) holds g and u of the same row and forms
 // SiLU(g)*u in registers.  Down tile = (e, 128 rows of H, token chunk of up to 256:
-// an expert's tokens split evenly) over the expert's h rows; its token rows take the
-// stage's second and third 16 KB regions, so a down stage carries as many MMA cycles as
-// a gate/up stage.  All gate/up tiles precede all down tiles in one list that CTAs
+// an expert's tokens split evenly) over the expert's h rows; its token rows fill the
+// stage's room after the weight slab, so a down stage carries as many MMA cycles as a
+// gate/up stage.  All gate/up tiles precede all down tiles in one list that CTAs
 // claim with an atomic counter; a down tile waits (bounded) until every epilogue warp
 // of every gate/up tile of its expert has published h.
 //
 // Roles per CTA (one CTA per SM): warp 0 lane 0 issues TMA loads into a 4-6 stage ring;
 // warp 1 owns the TMEM allocation and issues the MMAs, converged, through one elected
 // lane (tcgen05.commit frees a stage when its MMAs are done, and hands a finished
-// accumulator to the epilogue); warps 2-9 are the epilogue (warp w reads TMEM lanes
-// 32*(w%4)..+31, the two warps of a lane quadrant alternating over 32-column groups),
+// accumulator to the epilogue); warps 2-17 are the epilogue (warp w reads TMEM lanes
+// 32*(w%4)..+31, the four warps of a lane quadrant alternating over 32-column groups),
 // with two accumulator buffers so the epilogue of one tile overlaps the MMAs of the next.
 //
 // The token rows are first gathered into permuted order (x_perm) so that every
@@ -40,6 +40,7 @@ using namespace tc;
 
 constexpr int kRows = 128;                 // weight rows per tile (MMA M)
 constexpr int kMaxN = 128;                 // tokens per gate/up tile (MMA N, multiple of 16)
+constexpr int kWideN = 256;                // tokens per gate/up tile of large batches
 constexpr int kMaxDownN = 256;             // tokens per down tile
 constexpr int kSlab = 64;                  // k elements per stage (one 128-byte swizzle row)
 constexpr int kNBox = 16;                  // token rows per activation TMA box (small tiles)
@@ -48,14 +49,15 @@ constexpr int kBigBox = 128;               // token rows per box for large tiles
                                            // the issuer, so large tiles take few, large boxes
 constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
 constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
-constexpr int kEpiWarps = 8;               // two per TMEM lane quadrant, splitting the columns
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+// Epilogue warps: four per TMEM lane quadrant, splitting the columns (two with LoRA, whose
+// epilogue needs more registers per thread).
+__host__ __device__ constexpr int epi_warps(bool lora) { return lora ? 8 : 16; }
+__host__ __device__ constexpr int kernel_threads(bool lora) { return (2 + epi_warps(lora)) * 32; }
 constexpr int kMetaRing = 8;
 constexpr int kCtrlBytes = 1024;
 // Pipeline shape: token rows held per stage (BCap, a bound on N) and stage count.  Small
 // batches need little room for token rows, so they get more stages (more weight bytes in
-// flight).  (256-token tiles with a single TMEM buffer and 3 stages measured slower
-// at prefill than 128-token tiles with double buffering and 4 stages.)
+// flight).
 template <int BCap, int Stages>
 struct Cfg {
     static constexpr int kBBytes = BCap * 128;
@@ -118,17 +120,18 @@ __device__ __forceinline__ TileInfo read_tile(uint4 rec, const Params &p, int ca
 }
 
 template <int BCap, int kStages, bool kLora>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kernel_threads(kLora), 1)
 tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                  const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_xb,
                  const __grid_constant__ CUtensorMap tm_hb, const Params p) {
     constexpr int kBBytes = Cfg<BCap, kStages>::kBBytes;
     constexpr int kStageBytes = Cfg<BCap, kStages>::kStageBytes;
-    // TMEM: gate accumulators at column 0, up at kUpCol, of one of kNBuf buffers
-    constexpr int kUpCol = BCap > 128 ? 256 : 128;
-    constexpr int kBufCols = 2 * kUpCol;
-    constexpr int kNBuf = kTmemCols / kBufCols;
+    constexpr int kEpiWarps = epi_warps(kLora);
+    // TMEM: two halves of 256 columns.  A tile of at most 128 tokens (and every down or
+    // router tile) takes one half, alternating, with gate at its column 0 and up at 128;
+    // a gate/up tile of more than 128 tokens takes both (gate in half 0, up in half 1).
+    // Each half has its own full/free barrier pair, so one-half tiles double-buffer.
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ctrl = smem + kStages * kStageBytes;
@@ -139,7 +142,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     uint64_t *tmf = acce + 2;                                      // [kMetaRing]
     uint64_t *tme = tmf + kMetaRing;                               // [kMetaRing]
     uint64_t *drain = tme + kMetaRing;                             // [1]
-    int *smeta = reinterpret_cast<int *>(drain + 1);               // [kStages][4]: down|two<<1, ks, nstage, N
+    int *smeta = reinterpret_cast<int *>(drain + 1);               // [kStages][4]: kind, first, nstage, N
     int *tmeta = smeta + 4 * kStages;                              // [kMetaRing][8]
     volatile int *abort = tmeta + 8 * kMetaRing;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmeta + 8 * kMetaRing + 4);
@@ -197,6 +200,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         int next = router ? int(blockIdx.x) : lo + atomicAdd(ctr, 1);
         uint4 next_rec = (!router && next < hi) ? __ldg(p.tiles + next) : make_uint4(0, 0, 0, 0);
         const int cap_dn = min(p.dmax, (kABytes + kBBytes) / 128);
+        int hnext = 0;  // TMEM half of the next one-half tile
         bool live = true;
         while (live) {
             const int t = next;
@@ -222,6 +226,13 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 wait_count(p.done + d.e, d.need, p.err, abort);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
+            int hmask;  // TMEM halves of this tile (bit h = half h)
+            if (d.down == kGateUp && d.N > 128) {
+                hmask = 3;
+            } else {
+                hmask = 1 << hnext;
+                hnext ^= 1;
+            }
             // hand the tile to the epilogue
             mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, p.err, abort);
             int *tm = tmeta + 8 * slot;
@@ -231,6 +242,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             tm[3] = d.r0;
             tm[4] = d.m;
             tm[5] = d.N;
+            tm[6] = hmask;
             mbar_arrive(smem_u32(&tmf[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
 
@@ -259,7 +271,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 }
                 if (ks == 0) {  // the tile's shape, read by the MMA issuer at its first stage
                     int *sm = smeta + 4 * stage;
-                    sm[0] = d.down | (two << 2);
+                    sm[0] = d.down | (two << 2) | (hmask << 4);
                     sm[1] = 0;
                     sm[2] = nstage;
                     sm[3] = d.N;
@@ -305,18 +317,22 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         // wait for their data, so the issue stream is not broken up by shared-memory loads.
         int stage = 0;
         uint32_t phase = 0;
-        int tile_count = 0;
+        int uses[2] = {0, 0};  // tiles that have taken each TMEM half so far
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, p.err, abort))) break;
             const int *sm = smeta + 4 * stage;
             const int kind = sm[0], first = sm[1], nstage = sm[2], N = sm[3];
             if (__any_sync(0xffffffffu, first < 0 || *abort)) break;
-            const int down = (kind & 3) != kGateUp, two = kind >> 2;
-            const int b = tile_count % kNBuf;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce[b]), ((tile_count / kNBuf) & 1) ^ 1, p.err, abort)))
-                break;
+            const int down = (kind & 3) != kGateUp, two = (kind >> 2) & 1, hmask = (kind >> 4) & 3;
+            bool freed = true;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                if ((hmask >> hh) & 1)
+                    freed = freed && __all_sync(0xffffffffu, mbar_wait(smem_u32(&acce[hh]), (uses[hh] & 1) ^ 1, p.err, abort));
+            if (!freed) break;
             tc_fence_after();
-            const uint32_t d = tmem_base + uint32_t(b * kBufCols);
+            const uint32_t d = tmem_base + (hmask == 2 ? 256u : 0u);
+            const uint32_t up_col = hmask == 3 ? 256u : 128u;
             const uint32_t idesc = instr_desc(kRows, N);
             bool live = true;
             for (int ks = 0;;) {
@@ -335,7 +351,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                         const uint32_t acc = (ks | kk) != 0;
                         const uint64_t bdesc = smem_desc((down ? a0 + kABytes : bb) + kk * 32);
                         mma_bf16_warp(d, smem_desc(a0 + kk * 32), bdesc, idesc, acc);
-                        if (!down) mma_bf16_warp(d + kUpCol, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, acc);
+                        if (!down) mma_bf16_warp(d + up_col, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, acc);
                     }
                 }
                 mma_commit_warp(smem_u32(&empty[stage]));  // the stage's smem is free once these MMAs are done
@@ -347,8 +363,13 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 }
             }
             if (!live) break;
-            mma_commit_warp(smem_u32(&accf[b]));  // accumulator complete: hand to the epilogue
-            ++tile_count;
+            // accumulators complete: hand them to the epilogue
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                if ((hmask >> hh) & 1) {
+                    mma_commit_warp(smem_u32(&accf[hh]));
+                    ++uses[hh];
+                }
         }
         // every MMA this warp issued has completed before TMEM is released
         mma_commit_warp(smem_u32(drain));
@@ -357,21 +378,25 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         // ------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         const int row = 32 * q + lane;
-        const int half = (warp - 2) >> 2;  // which of the quadrant's two warps: alternate 32-column groups
-        int slot = 0, tile_count = 0;
+        const int part = (warp - 2) >> 2;  // which of the quadrant's warps: they alternate over column groups
+        constexpr int kParts = kEpiWarps / 4;
+        int slot = 0;
+        int uses[2] = {0, 0};
         uint32_t mphase = 0;
         for (;;) {
             mbar_wait(smem_u32(&tmf[slot]), mphase, p.err, abort);
             const int *tm = tmeta + 8 * slot;
-            const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], N = tm[5];
+            const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], N = tm[5], hmask = tm[6];
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tme[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
             if (down < 0 || *abort) break;
-            const int b = tile_count % kNBuf;
-            mbar_wait(smem_u32(&accf[b]), (tile_count / kNBuf) & 1, p.err, abort);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                if ((hmask >> hh) & 1) mbar_wait(smem_u32(&accf[hh]), uses[hh] & 1, p.err, abort);
             tc_fence_after();
-            const uint32_t taddr = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(b * kBufCols);
+            const uint32_t taddr = tmem_base + (uint32_t(32 * q) << 16) + (hmask == 2 ? 256u : 0u);
+            const uint32_t up_col = hmask == 3 ? 256u : 128u;
             const size_t col = (size_t)rb * kRows + row;
             // LoRA: this row's B vectors (the A-side products xa / ha were computed per token)
             const LoraDev &lr = p.lora;
@@ -388,7 +413,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             // TMEM is read 32 columns at a time (gate and up together: one wait per 32
             // tokens); columns past N are read and ignored (they stay inside the buffer)
             if (down == kRouter) {
-                for (int c0 = 16 * half; c0 < N; c0 += 32) {
+                for (int c0 = 16 * part; c0 < N; c0 += 16 * kParts) {
                     float v[16];
                     tmem_ld16(taddr + c0, v);
                     if (col < (size_t)p.E) {
@@ -399,7 +424,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     }
                 }
             } else if (down) {
-                for (int c0 = 32 * half; c0 < N; c0 += 64) {
+                for (int c0 = 32 * part; c0 < N; c0 += 32 * kParts) {
                     uint32_t v[32];
                     tmem_ld32(taddr + c0, v);
 #pragma unroll
@@ -412,9 +437,9 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                         }
                 }
             } else {
-                for (int c0 = 32 * half; c0 < N; c0 += 64) {
+                for (int c0 = 32 * part; c0 < N; c0 += 32 * kParts) {
                     uint32_t gu[64];
-                    tmem_ld32x2(taddr + c0, taddr + kUpCol + c0, gu);
+                    tmem_ld32x2(taddr + c0, taddr + up_col + c0, gu);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (c0 + j < m) {
@@ -430,7 +455,12 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&acce[b]));
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                if ((hmask >> hh) & 1) {
+                    if (lane == 0) mbar_arrive(smem_u32(&acce[hh]));
+                    ++uses[hh];
+                }
             if (down == kGateUp && e < p.E) {
                 // publish this warp's h rows (read back through TMA by down tiles)
                 asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -440,7 +470,6 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done + e) : "memory");
                 }
             }
-            ++tile_count;
         }
     }
 
@@ -483,7 +512,7 @@ cudaError_t launch_tc(dim3 grid, cudaStream_t st, const CUtensorMap &mg, const C
                       const CUtensorMap &mx, const CUtensorMap &mh, const CUtensorMap &mxb, const CUtensorMap &mhb,
                       const Params &prm) {
     if (!set_smem_attr<BCap, Stages, Lora>()) return cudaErrorInvalidValue;
-    return launch_pdl(tc_swiglu_kernel<BCap, Stages, Lora>, grid, dim3(kThreads), Cfg<BCap, Stages>::kSmemBytes, st, mg,
+    return launch_pdl(tc_swiglu_kernel<BCap, Stages, Lora>, grid, dim3(kernel_threads(Lora)), Cfg<BCap, Stages>::kSmemBytes, st, mg,
                       mu, md, mx, mh, mxb, mhb, prm);
 }
 
@@ -554,9 +583,16 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     if (!tc::make_map(&mxb, x_perm, A, s.H, kBigBox) || !tc::make_map(&mhb, h, A, s.I, kBigBox))
         return cudaErrorInvalidValue;
 
-    const int cmax = kMaxN;
+    // Large batches (at least 128 assignments per expert on average) take gate/up tiles of
+    // up to 256 tokens (both TMEM halves, three 64 KB stages): an MMA of N = 256 reads
+    // 12 KB of shared memory per 128 cycles against 8 KB per 64 for N = 128, and shared
+    // memory bandwidth is what bounds the tensor pipe here.  Smaller batches keep tiles of
+    // at most 128 tokens and a deeper pipeline for the weight stream.
+    const bool wide = (size_t)A >= (size_t)kMaxN * s.E;
+    const int cmax = wide ? kWideN : kMaxN;
     const int dmax = kMaxDownN;
-    const TileListArgs ta{cmax, 0, dmax, 1, s.I / kRows, s.H / kRows, kEpiWarps, (int)max_tiles(s)};
+    const TileListArgs ta{cmax, wide ? 1 : 0, dmax, 1, s.I / kRows, s.H / kRows, epi_warps(lora != nullptr),
+                          (int)max_tiles(s)};
     cudaError_t e = launch_pdl(prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
                                offsets, s.T, s.k, s.H, s.E, ta, x_perm, tiles, sched, done, err);
     if (e != cudaSuccess) return e;
@@ -579,11 +615,13 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (!lora)
-        return s.T <= 32 ? launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, mxb, mhb, prm)
-                         : launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, mxb, mhb, prm);
+        return wide        ? launch_tc<kWideN, 3>(grid, st, mg, mu, md, mx, mh, mxb, mhb, prm)
+               : s.T <= 32 ? launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, mxb, mhb, prm)
+                           : launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, mxb, mhb, prm);
     auto run = [&](const Params &pr) {
-        return s.T <= 32 ? launch_tc<32, 6, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, pr)
-                         : launch_tc<kMaxN, 4, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, pr);
+        return wide        ? launch_tc<kWideN, 3, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, pr)
+               : s.T <= 32 ? launch_tc<32, 6, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, pr)
+                           : launch_tc<kMaxN, 4, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, pr);
     };
     prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
     if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, lpart, st)) != cudaSuccess) return e;
