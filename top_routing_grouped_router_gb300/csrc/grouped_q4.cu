@@ -490,21 +490,32 @@ q4_prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order
     griddep_launch_dependents();
     griddep_wait();
     if (blockIdx.x > 0) {
-        const int pr = blockIdx.x - 1;
+        // one warp per permuted row, four 16-byte loads in flight per lane
+        const int pr = (blockIdx.x - 1) * kPrepRowsPerBlock + int(threadIdx.x >> 5);
+        const int lane = threadIdx.x & 31;
+        if (pr >= T * k) return;
         const int a = __ldg(order + pr);
         uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
         const bool bad = a < 0 || a >= T * k;
-        if (bad && threadIdx.x == 0) record_error(err, MOE_ERR_DEVICE);
+        if (bad && lane == 0) record_error(err, MOE_ERR_DEVICE);
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(bad ? 0 : a / k) * H);
-        for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
-            const uint4 v = bad ? make_uint4(0, 0, 0, 0) : __ldg(src + i);
-            // elements e0..e7 in (v.x lo, v.x hi, v.y lo, ...): output (e0,e4),(e1,e5),(e2,e6),(e3,e7)
-            uint4 o;
-            o.x = __byte_perm(v.x, v.z, 0x5410);
-            o.y = __byte_perm(v.x, v.z, 0x7632);
-            o.z = __byte_perm(v.y, v.w, 0x5410);
-            o.w = __byte_perm(v.y, v.w, 0x7632);
-            dst[i] = o;
+        const int n = H / 8;
+        for (int i = lane; i < n; i += 32 * 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = (!bad && i + 32 * u < n) ? __ldg(src + i + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (i + 32 * u >= n) continue;
+                // elements e0..e7 in (v.x lo, v.x hi, v.y lo, ...): output (e0,e4),(e1,e5),(e2,e6),(e3,e7)
+                uint4 o;
+                o.x = __byte_perm(v[u].x, v[u].z, 0x5410);
+                o.y = __byte_perm(v[u].x, v[u].z, 0x7632);
+                o.z = __byte_perm(v[u].y, v[u].w, 0x5410);
+                o.w = __byte_perm(v[u].y, v[u].w, 0x7632);
+                dst[i + 32 * u] = o;
+            }
         }
         return;
     }
@@ -613,7 +624,7 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
 
     const bool decode = s.T <= kDecodeMaxN;
     const int cmax = decode ? kDecodeMaxN : kChunkN;
-    cudaError_t e = launch_pdl(q4_prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
+    cudaError_t e = launch_pdl(q4_prep_kernel, dim3(prep_blocks(A)), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
                                offsets, s.T, s.k, s.H, s.I, s.E, cmax, (int)q4_max_tiles(s), x_perm, tiles, sched,
                                done, err);
     if (e != cudaSuccess) return e;

@@ -593,7 +593,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     const int dmax = kMaxDownN;
     const TileListArgs ta{cmax, wide ? 1 : 0, dmax, 1, s.I / kRows, s.H / kRows, epi_warps(lora != nullptr),
                           (int)max_tiles(s)};
-    cudaError_t e = launch_pdl(prep_kernel, dim3(A + 1), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
+    cudaError_t e = launch_pdl(prep_kernel, dim3(prep_blocks(A)), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
                                offsets, s.T, s.k, s.H, s.E, ta, x_perm, tiles, sched, done, err);
     if (e != cudaSuccess) return e;
 

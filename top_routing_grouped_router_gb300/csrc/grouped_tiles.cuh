@@ -95,7 +95,10 @@ struct TileListArgs {
 enum : int { kSchedClaim = 0, kSchedTiles = 1, kSchedGateUp = 2, kSchedClaimDown = 3 };
 
 // Block 0: the tile list from the offsets, the scheduling words (zeroed claim counters)
-// and zeroed per-expert completion counters.  Blocks 1..A: x_perm row blockIdx.x - 1.
+// and zeroed per-expert completion counters.  Blocks 1..: x_perm rows, one per warp
+// (kPrepRowsPerBlock per block).
+constexpr int kPrepRowsPerBlock = 8;
+__host__ __device__ constexpr int prep_blocks(int A) { return 1 + (A + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock; }
 __global__ void __launch_bounds__(256)
 prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
             int T, int k, int H, int E, TileListArgs ta, uint16_t *__restrict__ x_perm, uint4 *tiles,
@@ -103,15 +106,24 @@ prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, c
     griddep_launch_dependents();
     griddep_wait();
     if (blockIdx.x > 0) {
-        const int pr = blockIdx.x - 1;
+        // one warp per permuted row, four 16-byte loads in flight per lane
+        const int pr = (blockIdx.x - 1) * kPrepRowsPerBlock + int(threadIdx.x >> 5);
+        const int lane = threadIdx.x & 31;
+        if (pr >= T * k) return;
         const int a = __ldg(order + pr);
+        const bool bad = a < 0 || a >= T * k;
+        if (bad && lane == 0) record_error(err, MOE_ERR_DEVICE);
         uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
-        if (a < 0 || a >= T * k) {
-            if (threadIdx.x == 0) record_error(err, MOE_ERR_DEVICE);
-            for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
-        } else {
-            const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(a / k) * H);
-            for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(bad ? 0 : a / k) * H);
+        const int n = H / 8;
+        for (int i = lane; i < n; i += 32 * 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = (!bad && i + 32 * u < n) ? __ldg(src + i + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (i + 32 * u < n) dst[i + 32 * u] = v[u];
         }
         return;
     }
