@@ -50,11 +50,18 @@ permute_scan_kernel(int nchunks, int E, int32_t *hist, int32_t *counts, int32_t 
     griddep_wait();
     const int tid = threadIdx.x;
     if (tid < E) {
+        // 16 chunk counts are loaded before any is overwritten, so the loads overlap
         int run = 0;
-        for (int c = 0; c < nchunks; ++c) {
-            const int v = hist[(size_t)c * E + tid];
-            hist[(size_t)c * E + tid] = run;
-            run += v;
+        for (int c0 = 0; c0 < nchunks; c0 += 16) {
+            int v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = c0 + j < nchunks ? hist[(size_t)(c0 + j) * E + tid] : 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (c0 + j < nchunks) {
+                    hist[(size_t)(c0 + j) * E + tid] = run;
+                    run += v[j];
+                }
         }
         s.cnt[tid] = run;
     }
