@@ -44,9 +44,8 @@ constexpr int kWideN = 256;                // tokens per gate/up tile of large b
 constexpr int kMaxDownN = 256;             // tokens per down tile
 constexpr int kSlab = 64;                  // k elements per stage (one 128-byte swizzle row)
 constexpr int kNBox = 16;                  // token rows per activation TMA box (small tiles)
-constexpr int kBigBox = 128;               // token rows per box for large tiles: a TMA instruction
-                                           // costs the producer thread about as much as an MMA does
-                                           // the issuer, so large tiles take few, large boxes
+constexpr int kMidBox = 64;                // token rows per box for tiles of 33-64 tokens
+constexpr int kBigBox = 128;               // token rows per box for larger tiles
 constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
 constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
 // Epilogue warps: four per TMEM lane quadrant, splitting the columns (two with LoRA, whose
@@ -124,7 +123,8 @@ __global__ void __launch_bounds__(kernel_threads(kLora), 1)
 tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                  const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_xb,
-                 const __grid_constant__ CUtensorMap tm_hb, const Params p) {
+                 const __grid_constant__ CUtensorMap tm_hb, const __grid_constant__ CUtensorMap tm_xm,
+                 const __grid_constant__ CUtensorMap tm_hm, const Params p) {
     constexpr int kBBytes = Cfg<BCap, kStages>::kBBytes;
     constexpr int kStageBytes = Cfg<BCap, kStages>::kStageBytes;
     constexpr int kEpiWarps = epi_warps(kLora);
@@ -253,17 +253,21 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const int two = d.down != kGateUp && d.N <= BCap / 2 && (kdim / kSlab) % 2 == 0;
             const int nslab = kdim / kSlab;
             const int nstage = two ? nslab / 2 : nslab;
-            // token rows: 16-row boxes for small tiles, 128-row boxes (rows past the tile are
-            // loaded and ignored) once the tile holds more than half a box and the box fits
-            // its region of the stage
-            const bool big = BCap >= kBigBox && d.down != kRouter && d.N > kBigBox / 2 && (!two || BCap >= 2 * kBigBox);
-            const int box = big ? kBigBox : kNBox;
+            // token rows: the largest box (128, 64 or 16 rows) that the tile fills more than
+            // half of and that fits the rows its region of the stage holds (rows past the tile
+            // are loaded and ignored): a TMA instruction costs the producer thread about as
+            // much as an MMA costs the issuer, so few, large boxes
+            const int cap_rows = two ? BCap / 2 : BCap;
+            const int box = (cap_rows >= kBigBox && d.N > kBigBox / 2)   ? kBigBox
+                            : (cap_rows >= kMidBox && d.N > kMidBox / 2) ? kMidBox
+                                                                         : kNBox;
             const int nbox = (d.N + box - 1) / box;
             const uint32_t bytes =
                 (d.down != kGateUp && !two ? kABytes : 2 * kABytes) + (two ? 2 : 1) * nbox * box * 128;
             const int wrow = d.down == kRouter ? d.rb * kRows : d.e * (d.down ? p.H : p.I) + d.rb * kRows;
             const CUtensorMap *wmap = d.down == kDown ? &tm_down : &tm_gate;
-            const CUtensorMap *bmap = d.down == kDown ? (big ? &tm_hb : &tm_h) : (big ? &tm_xb : &tm_x);
+            const CUtensorMap *bmap = d.down == kDown ? (box == kBigBox ? &tm_hb : box == kMidBox ? &tm_hm : &tm_h)
+                                                      : (box == kBigBox ? &tm_xb : box == kMidBox ? &tm_xm : &tm_x);
             for (int ks = 0; ks < nstage; ++ks) {
                 if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort)) {
                     live = false;
@@ -510,10 +514,10 @@ bool set_smem_attr() {
 template <int BCap, int Stages, bool Lora = false>
 cudaError_t launch_tc(dim3 grid, cudaStream_t st, const CUtensorMap &mg, const CUtensorMap &mu, const CUtensorMap &md,
                       const CUtensorMap &mx, const CUtensorMap &mh, const CUtensorMap &mxb, const CUtensorMap &mhb,
-                      const Params &prm) {
+                      const CUtensorMap &mxm, const CUtensorMap &mhm, const Params &prm) {
     if (!set_smem_attr<BCap, Stages, Lora>()) return cudaErrorInvalidValue;
     return launch_pdl(tc_swiglu_kernel<BCap, Stages, Lora>, grid, dim3(kernel_threads(Lora)), Cfg<BCap, Stages>::kSmemBytes, st, mg,
-                      mu, md, mx, mh, mxb, mhb, prm);
+                      mu, md, mx, mh, mxb, mhb, mxm, mhm, prm);
 }
 
 }  // namespace
@@ -525,8 +529,10 @@ bool router_tc_supported(const moe_shape &s) {
 
 cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
                              int32_t *err, cudaStream_t st) {
-    CUtensorMap mw, mx;
-    if (!tc::make_map(&mw, wr, s.E, s.H, kRows) || !tc::make_map(&mx, x, s.T, s.H, kNBox)) return cudaErrorInvalidValue;
+    CUtensorMap mw, mx, mxm;
+    if (!tc::make_map(&mw, wr, s.E, s.H, kRows) || !tc::make_map(&mx, x, s.T, s.H, kNBox) ||
+        !tc::make_map(&mxm, x, s.T, s.H, kMidBox))
+        return cudaErrorInvalidValue;
     const int tiles = ((s.E + kRows - 1) / kRows) * ((s.T + kRouterN - 1) / kRouterN);
     Params prm{};
     prm.err = err;
@@ -537,7 +543,7 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
     prm.T = s.T;
     prm.logits = logits;
     prm.bias = bias;
-    return launch_tc<kMaxN, 4>(dim3(std::min(tiles, tc::sm_count())), st, mw, mw, mw, mx, mx, mx, mx, prm);
+    return launch_tc<kMaxN, 4>(dim3(std::min(tiles, tc::sm_count())), st, mw, mw, mw, mx, mx, mxm, mxm, mxm, mxm, prm);
 }
 
 // 0 = the per-output-element kernels of grouped_simple.cu; 1 = the bf16 tensor-core
@@ -579,8 +585,9 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
         !tc::make_map(&md, wd, (uint64_t)s.E * s.H, s.I, kRows) || !tc::make_map(&mx, x_perm, A, s.H, kNBox) ||
         !tc::make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
-    CUtensorMap mxb, mhb;
-    if (!tc::make_map(&mxb, x_perm, A, s.H, kBigBox) || !tc::make_map(&mhb, h, A, s.I, kBigBox))
+    CUtensorMap mxb, mhb, mxm, mhm;
+    if (!tc::make_map(&mxb, x_perm, A, s.H, kBigBox) || !tc::make_map(&mhb, h, A, s.I, kBigBox) ||
+        !tc::make_map(&mxm, x_perm, A, s.H, kMidBox) || !tc::make_map(&mhm, h, A, s.I, kMidBox))
         return cudaErrorInvalidValue;
 
     // Large batches (at least 128 assignments per expert on average) take gate/up tiles of
@@ -615,13 +622,13 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (!lora)
-        return wide        ? launch_tc<kWideN, 3>(grid, st, mg, mu, md, mx, mh, mxb, mhb, prm)
-               : s.T <= 32 ? launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, mxb, mhb, prm)
-                           : launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, mxb, mhb, prm);
+        return wide        ? launch_tc<kWideN, 3>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, prm)
+               : s.T <= 32 ? launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, prm)
+                           : launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, prm);
     auto run = [&](const Params &pr) {
-        return wide        ? launch_tc<kWideN, 3, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, pr)
-               : s.T <= 32 ? launch_tc<32, 6, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, pr)
-                           : launch_tc<kMaxN, 4, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, pr);
+        return wide        ? launch_tc<kWideN, 3, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, pr)
+               : s.T <= 32 ? launch_tc<32, 6, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, pr)
+                           : launch_tc<kMaxN, 4, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, pr);
     };
     prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
     if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, lpart, st)) != cudaSuccess) return e;
