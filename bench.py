@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--copies", type=int, default=0, help="weight copies to rotate (0 = automatic)")
     ap.add_argument("--layers", type=int, default=0, help="use only the first N layers (profiling; 0 = all)")
+    ap.add_argument("--lora-unpacked", action="store_true",
+                    help="with --entry lora: pass the fp32 adapters without a pack (CUDA-core adapter products)")
     ap.add_argument("--entry", choices=["forward", "rmsnorm", "lora"], default="forward",
                     help="moe_forward, moe_forward_rmsnorm (pre-router RMSNorm and residual fused in) or "
                          "moe_forward_lora (synthetic rank-16 fp32 adapters on the expert projections)")
@@ -259,8 +261,13 @@ def run_ours(args, rank, world, local):
         for i, l in enumerate(layers):
             ad = synth.make_lora(l.E, l.H, l.I, rank=16, seed=l.T, layer=i)
             t = [to_device(ad[n], dev) for n in names]
+            lo = moe.make_lora(ad["rank"], ad["scale"], *t)
+            if l.w == "bf16" and not args.lora_unpacked:
+                # adapters are static: packed once, before timing, like the weights
+                lo = moe.pack_lora(dl[0][i].shape, lo, device=dev)
+                t.append(lo.pack_tensor)
             lora_keep.append(t)
-            loras.append(moe.make_lora(ad["rank"], ad["scale"], *t))
+            loras.append(lo)
 
     def forward(c, st=None):
         for l, L in enumerate(dl[c]):
@@ -415,7 +422,9 @@ def run_ours(args, rank, world, local):
         "data": "synthetic: seeded N(0,1) tokens, N(0,1/fan_in) random-init weights of the model's shapes",
         "config": {"workload": DESCR[args.workload],
                    "entry": {"forward": "moe_forward", "rmsnorm": "moe_forward_rmsnorm (pre-router RMSNorm + residual)",
-                             "lora": "moe_forward_lora (rank-16 fp32 adapters on the expert projections)"}[args.entry], "T": T, "H": H, "E": E, "k": k, "I": I,
+                             "lora": "moe_forward_lora (rank-16 fp32 adapters on the expert projections"
+                                      + (", packed: tensor-core adapter products)" if inp0.w == "bf16" and not args.lora_unpacked
+                                         else ", CUDA-core adapter products)")}[args.entry], "T": T, "H": H, "E": E, "k": k, "I": I,
                    "layers": len(layers), "weights": inp0.w, "active_experts": n_active,
                    "l2": f"inputs larger than L2: {n_copies} rotating weight cop{'y' if n_copies == 1 else 'ies'} "
                          f"({n_copies * per_copy / 1e9:.1f} GB), one moe_forward graph per copy",

@@ -113,6 +113,12 @@ typedef struct {
  *   a_gate, a_up [E][r][H]     b_gate, b_up [E][I][r]
  *   a_down       [E][r][I]     b_down       [E][H][r]
  * Device pointers, row-major, 16-byte aligned.
+ *
+ * packed: NULL, or the output of moe_lora_pack for these adapters (device,
+ * 256-byte aligned).  With a pack, the bf16 tensor-core path runs the adapter
+ * products on the tensor cores: bf16 operands (the adapters and scale * x . A^T
+ * rounded to nearest even), fp32 accumulation, as for the base weights.  Without
+ * one, and on every other path, they run in fp32 on CUDA cores.
  */
 typedef struct {
     int32_t rank;
@@ -120,6 +126,7 @@ typedef struct {
     const float *a_gate, *b_gate;
     const float *a_up, *b_up;
     const float *a_down, *b_down;
+    const void *packed;
 } moe_lora;
 
 /*
@@ -229,9 +236,10 @@ MOE_API int moe_forward_rmsnorm(const moe_shape *shape, const void *hs, const vo
 
 /*
  * moe_forward with LoRA adapters on the three expert projections (see
- * moe_lora).  The rank-r products x . A^T and h . A_down^T are computed in fp32
- * by separate launches; the B side is added in the grouped kernels' epilogues
- * before SiLU (gate/up) and before y is rounded (down).  Same arguments, results,
+ * moe_lora).  The rank-r products x . A^T and h . A_down^T are computed by
+ * separate launches and the B side is added before SiLU (gate/up) and before y
+ * is rounded (down): in fp32 on CUDA cores, or, with a pack on the bf16
+ * tensor-core path, as tensor-core tiles and one more MMA stage per tile.  Same arguments, results,
  * workspace and errors as moe_forward, plus MOE_ERR_NULLPTR for a NULL lora or
  * adapter pointer and MOE_ERR_SHAPE for a rank outside [1, 16] or a non-finite
  * scale.
@@ -240,6 +248,27 @@ MOE_API int moe_forward_lora(const moe_shape *shape, const void *x, const void *
                              const void *w_gate, const void *w_up, const void *w_down, const moe_q4 *q4,
                              const moe_lora *lora, void *out, int32_t *expert_ids_out, float *weights_out,
                              void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Bytes of the adapter pack for this shape (host only, no CUDA call): the four
+ * bf16 arrays the tensor-core LoRA path reads, zero-padded, each 256-byte aligned:
+ *   [E][32][H]  A_gate rows 0..r-1, A_up rows 16..16+r-1
+ *   [E][16][I]  A_down rows 0..r-1
+ *   [E*I][64]   B_gate columns 0..r-1, B_up columns 16..16+r-1
+ *   [E*H][64]   B_down columns 0..r-1
+ */
+MOE_API int moe_lora_pack_size(const moe_shape *shape, size_t *bytes);
+
+/*
+ * Writes that pack from the fp32 adapters (lora->packed is ignored) into
+ * `packed` (device, 256-byte aligned, at least moe_lora_pack_size bytes), on
+ * `stream`.  Adapters are static across calls, so a caller packs once and
+ * passes the pack in moe_lora.packed; after changing the adapters it packs
+ * again.  Errors: MOE_ERR_NULLPTR, MOE_ERR_SHAPE (rank, scale or shape),
+ * MOE_ERR_ALIGN, MOE_ERR_WORKSPACE (packed_bytes too small), MOE_ERR_LAUNCH.
+ */
+MOE_API int moe_lora_pack(const moe_shape *shape, const moe_lora *lora, void *packed, size_t packed_bytes,
+                          moe_stream_t stream);
 
 /* Size of the library's fixed device scratch array used by moe_forward_static_scratch. */
 #define MOE_STATIC_SCRATCH_BYTES (32u << 20)

@@ -1,7 +1,9 @@
 """GPU parity of moe_forward_lora (LoRA adapters on the expert projections) against the
 oracle, on the bf16 and 4-bit tensor-core paths (decode and large batches) and the
-generic fp32 path; with B = 0 the result must equal moe_forward bit for bit, which also
-checks the split gate/up and down launches the adapters need."""
+generic fp32 path; on the bf16 path both with the fp32 adapters as given (CUDA-core
+adapter products) and with a pack (tensor-core adapter products).  With B = 0 the result
+must equal moe_forward bit for bit, which also checks the split launches the adapters
+need."""
 import numpy as np
 import pytest
 
@@ -29,9 +31,13 @@ def _built():
 _NAMES = ("a_gate", "b_gate", "a_up", "b_up", "a_down", "b_down")
 
 
-def _dev_lora(lora):
+def _dev_lora(lora, shape=None):
     t = {n: to_device(np.ascontiguousarray(lora[n], dtype=np.float32), "cuda") for n in _NAMES}
-    return moe.make_lora(lora["rank"], lora["scale"], *[t[n] for n in _NAMES]), t
+    s = moe.make_lora(lora["rank"], lora["scale"], *[t[n] for n in _NAMES])
+    if shape is not None:
+        s = moe.pack_lora(shape, s)
+        t["pack"] = s.pack_tensor
+    return s, t
 
 
 def _run_lora(L, lora_s):
@@ -45,10 +51,10 @@ def _run_lora(L, lora_s):
     return out, ids
 
 
-def _check(inp, rank, n_tok):
+def _check(inp, rank, n_tok, packed=False):
     lora = synth.make_lora(inp.E, inp.H, inp.I, rank=rank, seed=inp.T + rank)
     L = upload(inp)
-    lora_s, keep_alive = _dev_lora(lora)
+    lora_s, keep_alive = _dev_lora(lora, L.shape if packed else None)
     out, ids = _run_lora(L, lora_s)
     toks = np.arange(inp.T) if n_tok is None else sample_tokens(inp.T, n_tok)
     ref = oracle.forward_lora(inp, lora, toks)
@@ -66,7 +72,7 @@ def _check(inp, rank, n_tok):
     zero = dict(lora)
     for n in ("b_gate", "b_up", "b_down"):
         zero[n] = np.zeros_like(lora[n])
-    zs, keep_alive2 = _dev_lora(zero)
+    zs, keep_alive2 = _dev_lora(zero, L.shape if packed else None)
     out0, ids0 = _run_lora(L, zs)
     ref0 = torch.empty_like(out0)
     ids_ref = torch.empty_like(ids0)
@@ -82,6 +88,20 @@ def test_lora_decode_bf16_rank16():
     _check(synth.make_inputs("decode8"), 16, None)
 
 
+def test_lora_packed_decode_bf16_rank16():
+    _check(synth.make_inputs("decode8"), 16, None, packed=True)
+
+
+def test_lora_packed_mid_batch_bf16_rank7():
+    # 64 tokens: 128-token tiles, two-slab down tiles, A-side tiles of partial chunks
+    _check(synth.make_custom(64, 1024, 32, 4, 256, seed=45, name="lora64"), 7, 16, packed=True)
+
+
+def test_lora_packed_large_batch_bf16_rank16():
+    # 2048 assignments over 16 experts (128 per expert on average): 256-token gate/up tiles
+    _check(synth.make_custom(512, 1024, 16, 4, 384, seed=51, name="lora512"), 16, 16, packed=True)
+
+
 def test_lora_decode_q4_rank16():
     _check(synth.make_inputs("decode48q"), 16, 12)
 
@@ -92,6 +112,10 @@ def test_lora_fp32_generic_path_rank4():
 
 def test_lora_large_batch_bf16_rank8():
     _check(synth.make_custom(300, 512, 16, 4, 256, seed=41, name="lora300"), 8, 16)
+
+
+def test_lora_packed_large_batch_bf16_rank8():
+    _check(synth.make_custom(300, 512, 16, 4, 256, seed=41, name="lora300"), 8, 16, packed=True)
 
 
 def test_lora_large_batch_q4_rank16():

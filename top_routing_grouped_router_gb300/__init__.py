@@ -19,7 +19,7 @@ __all__ = [
     "make_shape", "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string", "EXPORTED_SYMBOLS",
     "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_forward_lora", "moe_graph_buckets", "moe_graphs_arena_size",
-    "DecodeGraphs",
+    "DecodeGraphs", "moe_lora_pack_size", "moe_lora_pack", "pack_lora",
 ]
 
 MOE_DT_F32, MOE_DT_BF16, MOE_DT_Q4 = 0, 1, 2
@@ -31,7 +31,7 @@ library_path = os.path.join(_HERE, "libmoe_gb300.so")
 EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
                     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string",
                     "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_forward_lora", "moe_graph_buckets", "moe_graphs_arena_size", "moe_graphs_create",
-                    "moe_graphs_bucket", "moe_graphs_run", "moe_graphs_destroy")
+                    "moe_graphs_bucket", "moe_graphs_run", "moe_graphs_destroy", "moe_lora_pack_size", "moe_lora_pack")
 
 
 class MoEError(RuntimeError):
@@ -49,7 +49,7 @@ class MoEShape(ctypes.Structure):
 class MoELora(ctypes.Structure):
     _fields_ = [("rank", ctypes.c_int32), ("scale", ctypes.c_float), ("a_gate", ctypes.c_void_p),
                 ("b_gate", ctypes.c_void_p), ("a_up", ctypes.c_void_p), ("b_up", ctypes.c_void_p),
-                ("a_down", ctypes.c_void_p), ("b_down", ctypes.c_void_p)]
+                ("a_down", ctypes.c_void_p), ("b_down", ctypes.c_void_p), ("packed", ctypes.c_void_p)]
 
 
 class MoEQ4(ctypes.Structure):
@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
             "moe_graphs_bucket": [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)],
             "moe_graphs_run": [vp, ctypes.c_int, vp, vp, i32p, vp],
             "moe_graphs_destroy": [vp],
+            "moe_lora_pack_size": [sp, ctypes.POINTER(ctypes.c_size_t)],
+            "moe_lora_pack": [sp, ctypes.POINTER(MoELora), vp, sz, vp],
         }
         for name, argtypes in sig.items():
             f = getattr(L, name)
@@ -195,10 +197,35 @@ def moe_forward_rmsnorm(shape, hs, gamma, eps, w_router, b_router, w_gate, w_up,
                                      _stream(stream)), "moe_forward_rmsnorm")
 
 
-def make_lora(rank, scale, a_gate, b_gate, a_up, b_up, a_down, b_down) -> MoELora:
-    """The moe_lora struct over device tensors (fp32, row-major; see moe.h for the shapes)."""
+def make_lora(rank, scale, a_gate, b_gate, a_up, b_up, a_down, b_down, packed=None) -> MoELora:
+    """The moe_lora struct over device tensors (fp32, row-major; see moe.h for the shapes);
+    `packed` is a buffer written by moe_lora_pack / pack_lora, or None."""
     return MoELora(int(rank), float(scale), _ptr(a_gate), _ptr(b_gate), _ptr(a_up), _ptr(b_up), _ptr(a_down),
-                   _ptr(b_down))
+                   _ptr(b_down), _ptr(packed))
+
+
+def moe_lora_pack_size(shape: MoEShape) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_lora_pack_size(ctypes.byref(shape), ctypes.byref(n)), "moe_lora_pack_size")
+    return n.value
+
+
+def moe_lora_pack(shape: MoEShape, lora: MoELora, packed, stream=None):
+    """Packs the adapters of `lora` into the device buffer `packed` (moe_lora_pack_size bytes)."""
+    _check(lib().moe_lora_pack(ctypes.byref(shape), ctypes.byref(lora), _ptr(packed), _nbytes(packed),
+                               _stream(stream)), "moe_lora_pack")
+
+
+def pack_lora(shape: MoEShape, lora: MoELora, device=None, stream=None) -> MoELora:
+    """A copy of `lora` that carries a freshly written pack.  The pack is a uint8 tensor on
+    `device`, kept alive as the returned struct's `pack_tensor` attribute."""
+    import torch
+    buf = torch.empty(moe_lora_pack_size(shape), dtype=torch.uint8, device=device or "cuda")
+    moe_lora_pack(shape, lora, buf, stream)
+    out = MoELora(lora.rank, lora.scale, lora.a_gate, lora.b_gate, lora.a_up, lora.b_up, lora.a_down, lora.b_down,
+                  _ptr(buf))
+    out.pack_tensor = buf
+    return out
 
 
 def moe_forward_lora(shape, x, w_router, b_router, w_gate, w_up, w_down, q4, lora: MoELora, out, expert_ids_out=None,

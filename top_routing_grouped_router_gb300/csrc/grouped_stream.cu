@@ -48,10 +48,14 @@ constexpr int kMidBox = 64;                // token rows per box for tiles of 33
 constexpr int kBigBox = 128;               // token rows per box for larger tiles
 constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
 constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
-// Epilogue warps: four per TMEM lane quadrant, splitting the columns (two with LoRA, whose
-// epilogue needs more registers per thread).
-__host__ __device__ constexpr int epi_warps(bool lora) { return lora ? 8 : 16; }
-__host__ __device__ constexpr int kernel_threads(bool lora) { return (2 + epi_warps(lora)) * 32; }
+// LoRA modes of the kernel: none; B side in the epilogue on CUDA cores (fp32 adapters as
+// given); or packed bf16 adapters on the tensor cores (A-side tiles of their own, and the
+// B side as one more MMA stage of each gate/up and down tile).
+enum : int { kLoraNone = 0, kLoraEpi = 1, kLoraPacked = 2 };
+// Epilogue warps: four per TMEM lane quadrant, splitting the columns (two with the
+// epilogue-side LoRA, whose epilogue needs more registers per thread).
+__host__ __device__ constexpr int epi_warps(int lora) { return lora == kLoraEpi ? 8 : 16; }
+__host__ __device__ constexpr int kernel_threads(int lora) { return (2 + epi_warps(lora)) * 32; }
 constexpr int kMetaRing = 8;
 constexpr int kCtrlBytes = 1024;
 // Pipeline shape: token rows held per stage (BCap, a bound on N) and stage count.  Small
@@ -67,8 +71,10 @@ struct Cfg {
 constexpr int kRouterN = 64;               // tokens per router tile: twice the tiles, two k-slabs per stage
 
 // Tile kinds.  The router GEMM (logits[t][e] = x_t . W_r[e]) reuses the kernel as one
-// 128-expert x 128-token tile per CTA.
-enum : int { kGateUp = 0, kDown = 1, kRouter = 2 };
+// 128-expert x 64-token tile per CTA.  LoRA A-side tiles (packed adapters) take 128 token
+// rows as the MMA's M side and the expert's 32 (x) or 16 (h) adapter rows as N.
+enum : int { kGateUp = 0, kDown = 1, kRouter = 2, kLoraX = 3, kLoraH = 4 };
+static_assert(kGateUp == kRecGateUp && kDown == kRecDown && kLoraX == kRecLoraX && kLoraH == kRecLoraH, "kinds");
 
 struct Params {
     const int32_t *offsets;     // [E+1]
@@ -76,7 +82,12 @@ struct Params {
     int *sched;                 // scheduling words (grouped_tiles.cuh)
     int phase;                  // kPhaseAll / kPhaseGateUp / kPhaseDown
     LoraDev lora;               // LoRA B-side terms of the epilogue (rank 0: none)
-    int *done;                  // [E] published gate/up tiles (per epilogue warp)
+    int lora_packed;            // packed adapters: A-side tiles and a B-side stage per tile
+    float lora_scale;
+    uint16_t *xab;              // [A][64] bf16: scale * x . A^T (gate 0..15, up 16..31), rest zero
+    uint16_t *hab;              // [A][64] bf16: scale * h . A_down^T (0..15), rest zero
+    int *done;                  // [3][kMaxE] publications: h (per epilogue warp of a gate/up tile),
+                                // then x . A^T and h . A_down^T (per quadrant warp of an A-side tile)
     int32_t *err;
     uint16_t *h;                // [A][I] bf16
     uint16_t *y;                // [A][H] bf16
@@ -91,7 +102,7 @@ struct Params {
 };
 
 struct TileInfo {
-    int down, e, rb, r0, m, N, need;
+    int down, e, rb, r0, m, N, need, need_l;
 };
 
 // A tile record checked against the shapes: rows within the permuted range and within
@@ -105,26 +116,43 @@ __device__ __forceinline__ TileInfo read_tile(uint4 rec, const Params &p, int ca
     d.r0 = r.r0;
     d.m = r.m;
     d.need = r.need;
-    ok = d.e < p.E && d.rb < (d.down ? p.H : p.I) / kRows && d.r0 >= 0 && d.m > 0 && d.m <= p.A - d.r0 &&
-         d.m <= (d.down ? cap_dn : cap_gu);
+    d.need_l = r.need_l;
+    const bool lora_tile = d.down == kLoraX || d.down == kLoraH;
+    const int rbmax = d.down == kGateUp ? p.I / kRows : d.down == kDown ? p.H / kRows : 1;
+    const int mcap = d.down == kGateUp ? cap_gu : d.down == kDown ? cap_dn : kLoraChunk;
+    ok = (d.down == kGateUp || d.down == kDown || (lora_tile && p.lora_packed)) && d.e < p.E && d.rb < rbmax &&
+         d.r0 >= 0 && d.m > 0 && d.m <= p.A - d.r0 && d.m <= mcap;
     if (!ok) {  // inconsistent record: load in-range rows, store nothing
         d.m = 0;
         d.r0 = 0;
         d.rb = 0;
         d.e = min(d.e, p.E - 1);
         d.need = 0;
+        d.need_l = 0;
+        if (lora_tile) d.down = kDown;  // an empty down tile: loads in range, stores nothing
     }
     d.N = d.m > 0 ? (d.m + 15) & ~15 : 16;
     return d;
 }
 
-template <int BCap, int kStages, bool kLora>
+// Tensor maps of the packed LoRA adapters and of the scaled A-side products; kernels
+// without packed adapters take an empty struct instead (their parameter block stays
+// small: 8 more maps in every instantiation measurably slowed the plain kernel).
+struct LoraMaps {
+    CUtensorMap lax, lah, lbg, lbd, xa16, xa128, ha16, ha128;
+};
+struct NoLoraMaps {};
+template <int kLora> struct LoraMapsOf { using type = NoLoraMaps; };
+template <> struct LoraMapsOf<kLoraPacked> { using type = LoraMaps; };
+
+template <int BCap, int kStages, int kLora>
 __global__ void __launch_bounds__(kernel_threads(kLora), 1)
 tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                  const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_xb,
                  const __grid_constant__ CUtensorMap tm_hb, const __grid_constant__ CUtensorMap tm_xm,
-                 const __grid_constant__ CUtensorMap tm_hm, const Params p) {
+                 const __grid_constant__ CUtensorMap tm_hm,
+                 const __grid_constant__ typename LoraMapsOf<kLora>::type lm, const Params p) {
     constexpr int kBBytes = Cfg<BCap, kStages>::kBBytes;
     constexpr int kStageBytes = Cfg<BCap, kStages>::kStageBytes;
     constexpr int kEpiWarps = epi_warps(kLora);
@@ -186,12 +214,14 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         int stage = 0, slot = 0;
         uint32_t phase = 0, mphase = 0;
         // this launch's tile range [lo, hi) and its claim counter
-        int lo = 0, hi = router ? p.router_tiles : p.sched[kSchedTiles];
-        int *ctr = router ? nullptr : p.sched + kSchedClaim;
-        if (!router && p.phase == kPhaseGateUp) hi = p.sched[kSchedGateUp];
-        if (!router && p.phase == kPhaseDown) {
-            lo = p.sched[kSchedGateUp];
-            ctr = p.sched + kSchedClaimDown;
+        int lo = 0, hi = router ? p.router_tiles : 0;
+        int *ctr = nullptr;
+        if (!router) {
+            const int r = p.phase == kPhaseLoraX ? 0 : p.phase == kPhaseGateUp ? 1 : p.phase == kPhaseLoraH ? 2 : 3;
+            const bool all = p.phase == kPhaseAll;
+            lo = p.sched[kSchedBound + (all ? 0 : r)];
+            hi = p.sched[kSchedBound + (all ? 4 : r + 1)];
+            ctr = p.sched + kSchedRangeClaim + (all ? 0 : r);
         }
         // the next tile is claimed when this one starts, and its record is loaded a few
         // stages into this one (when the claim has returned), so neither latency falls
@@ -217,15 +247,18 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 d.m = min(kRouterN, p.T - d.r0);
                 d.N = (d.m + 15) & ~15;
                 d.need = 0;
+                d.need_l = 0;
             } else {
                 d = read_tile(rec, p, BCap, cap_dn, ok);
             }
             if (!ok) record_error(p.err, MOE_ERR_DEVICE);
-            if (d.down == kDown) {
+            if (d.down == kDown || d.down == kLoraH) {
                 // the expert's h must be complete: every epilogue warp of every gate/up tile
                 wait_count(p.done + d.e, d.need, p.err, abort);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
+            const bool lora_a = d.down == kLoraX || d.down == kLoraH;
+            const int nl = d.down == kLoraX ? 32 : 16;  // adapter rows of an A-side tile (its MMA's N)
             int hmask;  // TMEM halves of this tile (bit h = half h)
             if (d.down == kGateUp && d.N > 128) {
                 hmask = 3;
@@ -241,7 +274,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             tm[2] = d.rb;
             tm[3] = d.r0;
             tm[4] = d.m;
-            tm[5] = d.N;
+            tm[5] = lora_a ? nl : d.N;
             tm[6] = hmask;
             mbar_arrive(smem_u32(&tmf[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
@@ -249,10 +282,13 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             // a one-matrix tile (down, router) with at most 64 tokens takes two k-slabs per
             // stage (weights in both A regions, token rows in the two halves of B), so every
             // stage carries 32 KB of weights whatever the tile kind
-            const int kdim = d.down == kDown ? p.I : p.H;
-            const int two = d.down != kGateUp && d.N <= BCap / 2 && (kdim / kSlab) % 2 == 0;
+            const int kdim = (d.down == kDown || d.down == kLoraH) ? p.I : p.H;
+            const int two = !lora_a && d.down != kGateUp && d.N <= BCap / 2 && (kdim / kSlab) % 2 == 0;
             const int nslab = kdim / kSlab;
-            const int nstage = two ? nslab / 2 : nslab;
+            // with packed LoRA adapters a gate/up or down tile takes one more stage: the B
+            // adapter rows of its weight rows against scale * x . A^T (or h . A_down^T)
+            const int lst = kLora == kLoraPacked && p.lora_packed && (d.down == kGateUp || d.down == kDown);
+            const int nstage = (two ? nslab / 2 : nslab) + lst;
             // token rows: the largest box (128, 64 or 16 rows) that the tile fills more than
             // half of and that fits the rows its region of the stage holds (rows past the tile
             // are loaded and ignored): a TMA instruction costs the producer thread about as
@@ -263,7 +299,14 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                                                                          : kNBox;
             const int nbox = (d.N + box - 1) / box;
             const uint32_t bytes =
-                (d.down != kGateUp && !two ? kABytes : 2 * kABytes) + (two ? 2 : 1) * nbox * box * 128;
+                lora_a ? kABytes + nl * 128
+                       : (d.down != kGateUp && !two ? kABytes : 2 * kABytes) + (two ? 2 : 1) * nbox * box * 128;
+            // the LoRA stage's token rows: scale * x . A^T (or h . A_down^T) rows, 128-row boxes
+            // when they fit the region and the tile fills more than half of one
+            const int lcap = d.down == kGateUp ? BCap : two ? BCap / 2 : BCap + kRows;
+            const int lbox = (lcap >= kBigBox && d.N > kBigBox / 2) ? kBigBox : kNBox;
+            const int lnbox = (d.N + lbox - 1) / lbox;
+            const uint32_t lbytes = kABytes + lnbox * lbox * 128;
             const int wrow = d.down == kRouter ? d.rb * kRows : d.e * (d.down ? p.H : p.I) + d.rb * kRows;
             const CUtensorMap *wmap = d.down == kDown ? &tm_down : &tm_gate;
             const CUtensorMap *bmap = d.down == kDown ? (box == kBigBox ? &tm_hb : box == kMidBox ? &tm_hm : &tm_h)
@@ -275,18 +318,42 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 }
                 if (ks == 0) {  // the tile's shape, read by the MMA issuer at its first stage
                     int *sm = smeta + 4 * stage;
-                    sm[0] = d.down | (two << 2) | (hmask << 4);
+                    sm[0] = d.down | (two << 3) | (hmask << 4) | (lst << 6);
                     sm[1] = 0;
                     sm[2] = nstage;
-                    sm[3] = d.N;
+                    sm[3] = lora_a ? nl : d.N;
                 }
                 if (!router && ks == min(2, nstage - 1))
                     next_rec = next < hi ? __ldg(p.tiles + next) : make_uint4(0, 0, 0, 0);
                 const uint32_t fb = smem_u32(&full[stage]);
-                mbar_arrive_expect_tx(fb, bytes);
+                const bool lstage = lst && ks == nstage - 1;
+                mbar_arrive_expect_tx(fb, lstage ? lbytes : bytes);
                 const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
                 const uint32_t bb = a0 + 2 * kABytes;
-                if (two) {
+                bool issued = false;
+                if constexpr (kLora == kLoraPacked) {
+                    issued = lstage || lora_a;
+                    if (lstage) {
+                    // B adapter rows of the tile's 128 weight rows (rank columns, zero-padded to
+                    // 64) and the tokens' scaled A-side products, in the token region of the kind;
+                    // those products must be complete (the expert's A-side tiles published)
+                        const bool gu = d.down == kGateUp;
+                        wait_count(p.done + (gu ? 1 : 2) * kMaxE + d.e, d.need_l, p.err, abort);
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        tma_load_2d(a0, gu ? &lm.lbg : &lm.lbd, 0, d.e * (gu ? p.I : p.H) + d.rb * kRows, fb);
+                        const uint32_t tb = gu || two ? bb : a0 + kABytes;
+                        const CUtensorMap *tm2 = gu ? (lbox == kBigBox ? &lm.xa128 : &lm.xa16)
+                                                    : (lbox == kBigBox ? &lm.ha128 : &lm.ha16);
+                        for (int q = 0; q < lnbox; ++q) tma_load_2d(tb + q * lbox * 128, tm2, 0, d.r0 + q * lbox, fb);
+                    } else if (lora_a) {
+                        // 128 token rows (the MMA's M side) and the expert's adapter rows (N)
+                        const bool lx = d.down == kLoraX;
+                        tma_load_2d(a0, lx ? &tm_xb : &tm_hb, ks * kSlab, d.r0, fb);
+                        tma_load_2d(a0 + kABytes, lx ? &lm.lax : &lm.lah, ks * kSlab, d.e * nl, fb);
+                    }
+                }
+                if (issued) {
+                } else if (two) {
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int k0 = (2 * ks + h2) * kSlab;
                         tma_load_2d(a0 + h2 * kABytes, wmap, k0, wrow, fb);
@@ -327,7 +394,9 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const int *sm = smeta + 4 * stage;
             const int kind = sm[0], first = sm[1], nstage = sm[2], N = sm[3];
             if (__any_sync(0xffffffffu, first < 0 || *abort)) break;
-            const int down = (kind & 3) != kGateUp, two = (kind >> 2) & 1, hmask = (kind >> 4) & 3;
+            // A-side LoRA tiles run like a down tile: A at the slot's start, B after 16 KB
+            const int down = (kind & 7) != kGateUp, two = (kind >> 3) & 1, hmask = (kind >> 4) & 3;
+            const int lst = (kind >> 6) & 1;
             bool freed = true;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
@@ -342,7 +411,15 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             for (int ks = 0;;) {
                 const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
                 const uint32_t bb = a0 + 2 * kABytes;
-                if (two) {
+                if (kLora == kLoraPacked && lst && ks == nstage - 1) {
+                    // the LoRA stage: k = 0..15 of the slab against gate (or down), 16..31 against up
+                    if (!down) {
+                        mma_bf16_warp(d, smem_desc(a0), smem_desc(bb), idesc, 1u);
+                        mma_bf16_warp(d + up_col, smem_desc(a0 + 32), smem_desc(bb + 32), idesc, 1u);
+                    } else {
+                        mma_bf16_warp(d, smem_desc(a0), smem_desc(two ? bb : a0 + kABytes), idesc, 1u);
+                    }
+                } else if (two) {
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
@@ -404,7 +481,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const size_t col = (size_t)rb * kRows + row;
             // LoRA: this row's B vectors (the A-side products xa / ha were computed per token)
             const LoraDev &lr = p.lora;
-            const bool lora = kLora && lr.rank > 0 && down != kRouter && e < p.E;
+            const bool lora = kLora == kLoraEpi && lr.rank > 0 && (down == kGateUp || down == kDown) && e < p.E;
             float lb0[16], lb1[16];
             if (lora) {
                 if (down) {
@@ -425,6 +502,36 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             if (c0 + j < m) p.logits[(size_t)(r0 + c0 + j) * p.E + col] = v[j] + b;
+                    }
+                }
+            } else if (kLora == kLoraPacked && (down == kLoraX || down == kLoraH)) {
+                // tokens are the TMEM lanes here: row r0 + row gets its N adapter products,
+                // scaled, as one 64-column bf16 row (the columns past N zero)
+                if (part == 0) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr, v);
+                    if (row < m) {
+                        uint4 *dst = reinterpret_cast<uint4 *>((down == kLoraX ? p.xab : p.hab) + (size_t)(r0 + row) * 64);
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int c = 8 * g + 2 * i;
+                                const float lo = c < N ? p.lora_scale * __uint_as_float(v[c & 31]) : 0.f;
+                                const float hi = c + 1 < N ? p.lora_scale * __uint_as_float(v[(c + 1) & 31]) : 0.f;
+                                w[i] = uint32_t(f32_to_bf16_bits(lo)) | (uint32_t(f32_to_bf16_bits(hi)) << 16);
+                            }
+                            dst[g] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                    // publish (read back through TMA by the expert's gate/up or down tiles)
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0 && e < p.E) {
+                        __threadfence();
+                        int *ctr = p.done + (down == kLoraX ? 1 : 2) * kMaxE + e;
+                        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ctr) : "memory");
                     }
                 }
             } else if (down) {
@@ -492,12 +599,22 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
 constexpr int kMaxT = 8192;
 
 size_t xperm_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * s.H * 2 + 255) / 256 * 256; }
+// Tiles: at most E + A / 128 token chunks, each with I / 128 gate/up and H / 128 down
+// tiles, plus with packed LoRA adapters two A-side tiles per 128-token chunk.
 size_t max_tiles(const moe_shape &s) {
     const size_t chunks = (size_t)s.E + ((size_t)s.T * s.k + kMaxN - 1) / kMaxN;
-    return chunks * (size_t)(s.I / kRows + s.H / kRows);
+    return chunks * (size_t)(s.I / kRows + s.H / kRows) + 2 * chunks;
 }
 
-template <int BCap, int Stages, bool Lora>
+// Every tensor map the kernel takes (the LoRA ones only with packed adapters).
+struct Maps {
+    CUtensorMap g, u, d, x, h, xb, hb, xm, hm;
+    LoraMaps l;
+};
+inline const LoraMaps &lora_maps(const Maps &m, LoraMaps *) { return m.l; }
+inline NoLoraMaps lora_maps(const Maps &, NoLoraMaps *) { return NoLoraMaps{}; }
+
+template <int BCap, int Stages, int Lora>
 bool set_smem_attr() {
     static bool attr_set[64] = {};
     int dev = 0;
@@ -511,13 +628,21 @@ bool set_smem_attr() {
     return true;
 }
 
-template <int BCap, int Stages, bool Lora = false>
-cudaError_t launch_tc(dim3 grid, cudaStream_t st, const CUtensorMap &mg, const CUtensorMap &mu, const CUtensorMap &md,
-                      const CUtensorMap &mx, const CUtensorMap &mh, const CUtensorMap &mxb, const CUtensorMap &mhb,
-                      const CUtensorMap &mxm, const CUtensorMap &mhm, const Params &prm) {
+template <int BCap, int Stages, int Lora = kLoraNone>
+cudaError_t launch_tc(dim3 grid, cudaStream_t st, const Maps &m, const Params &prm) {
     if (!set_smem_attr<BCap, Stages, Lora>()) return cudaErrorInvalidValue;
-    return launch_pdl(tc_swiglu_kernel<BCap, Stages, Lora>, grid, dim3(kernel_threads(Lora)), Cfg<BCap, Stages>::kSmemBytes, st, mg,
-                      mu, md, mx, mh, mxb, mhb, mxm, mhm, prm);
+    using LM = typename LoraMapsOf<Lora>::type;
+    const LM lm = lora_maps(m, static_cast<LM *>(nullptr));
+    return launch_pdl(tc_swiglu_kernel<BCap, Stages, Lora>, grid, dim3(kernel_threads(Lora)),
+                      Cfg<BCap, Stages>::kSmemBytes, st, m.g, m.u, m.d, m.x, m.h, m.xb, m.hb, m.xm, m.hm, lm, prm);
+}
+
+// The pipeline shape for this batch (see launch_grouped_fast) in LoRA mode Lora.
+template <int Lora>
+cudaError_t launch_tc_for(const moe_shape &s, bool wide, dim3 grid, cudaStream_t st, const Maps &m, const Params &prm) {
+    return wide        ? launch_tc<kWideN, 3, Lora>(grid, st, m, prm)
+           : s.T <= 32 ? launch_tc<32, 6, Lora>(grid, st, m, prm)
+                       : launch_tc<kMaxN, 4, Lora>(grid, st, m, prm);
 }
 
 }  // namespace
@@ -533,6 +658,7 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
     if (!tc::make_map(&mw, wr, s.E, s.H, kRows) || !tc::make_map(&mx, x, s.T, s.H, kNBox) ||
         !tc::make_map(&mxm, x, s.T, s.H, kMidBox))
         return cudaErrorInvalidValue;
+    Maps m{mw, mw, mw, mx, mx, mxm, mxm, mxm, mxm, {}};
     const int tiles = ((s.E + kRows - 1) / kRows) * ((s.T + kRouterN - 1) / kRouterN);
     Params prm{};
     prm.err = err;
@@ -543,7 +669,7 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
     prm.T = s.T;
     prm.logits = logits;
     prm.bias = bias;
-    return launch_tc<kMaxN, 4>(dim3(std::min(tiles, tc::sm_count())), st, mw, mw, mw, mx, mx, mxm, mxm, mxm, mxm, prm);
+    return launch_tc<kMaxN, 4>(dim3(std::min(tiles, tc::sm_count())), st, m, prm);
 }
 
 // 0 = the per-output-element kernels of grouped_simple.cu; 1 = the bf16 tensor-core
@@ -560,13 +686,17 @@ int select_grouped_path(const moe_shape &s) {
 size_t grouped_fast_part_bytes(int path, const moe_shape &s) {
     if (path == 2) return q4_part_bytes(s);
     if (path != 1) return 0;
-    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (max_tiles(s) * 16 + 255) / 256 * 256;
+    return xperm_bytes(s) + 256 + (size_t)kCountersPerExpert * kMaxE * 4 + (max_tiles(s) * 16 + 255) / 256 * 256;
 }
 
 int grouped_fast_launches(int path, const moe_shape &) { return path == 1 || path == 2 ? 2 : 0; }
 
-// Without adapters: prep + one launch over all tiles.  With LoRA: prep, x . A^T, the
-// gate/up tiles, h . A_down^T, the down tiles (five launches).
+// Without adapters: prep + one launch over all tiles.  With packed LoRA adapters also one
+// launch: the A-side products are tiles of the same kernel (tensor cores, first in the
+// list: x . A^T, then after the gate/up tiles h . A_down^T) and the B side is one more MMA
+// stage of each gate/up and down tile, which waits for its expert's A-side tiles.  With
+// unpacked adapters: prep, x . A^T, the gate/up tiles, h . A_down^T, the down tiles (five
+// launches; CUDA-core A side, B side in the epilogue).
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
                                 const moe_q4 *q4, const int32_t *, float *part, void *h, void *y, int32_t *err,
@@ -578,17 +708,28 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     uint16_t *x_perm = reinterpret_cast<uint16_t *>(base);
     int *sched = reinterpret_cast<int *>(base + xperm_bytes(s));
     int *done = sched + 64;
-    uint4 *tiles = reinterpret_cast<uint4 *>(base + xperm_bytes(s) + 256 + (size_t)kMaxE * 4);
+    uint4 *tiles = reinterpret_cast<uint4 *>(base + xperm_bytes(s) + 256 + (size_t)kCountersPerExpert * kMaxE * 4);
 
-    CUtensorMap mg, mu, md, mx, mh;
-    if (!tc::make_map(&mg, wg, (uint64_t)s.E * s.I, s.H, kRows) || !tc::make_map(&mu, wu, (uint64_t)s.E * s.I, s.H, kRows) ||
-        !tc::make_map(&md, wd, (uint64_t)s.E * s.H, s.I, kRows) || !tc::make_map(&mx, x_perm, A, s.H, kNBox) ||
-        !tc::make_map(&mh, h, A, s.I, kNBox))
+    Maps m;
+    if (!tc::make_map(&m.g, wg, (uint64_t)s.E * s.I, s.H, kRows) ||
+        !tc::make_map(&m.u, wu, (uint64_t)s.E * s.I, s.H, kRows) ||
+        !tc::make_map(&m.d, wd, (uint64_t)s.E * s.H, s.I, kRows) || !tc::make_map(&m.x, x_perm, A, s.H, kNBox) ||
+        !tc::make_map(&m.h, h, A, s.I, kNBox) || !tc::make_map(&m.xb, x_perm, A, s.H, kBigBox) ||
+        !tc::make_map(&m.hb, h, A, s.I, kBigBox) || !tc::make_map(&m.xm, x_perm, A, s.H, kMidBox) ||
+        !tc::make_map(&m.hm, h, A, s.I, kMidBox))
         return cudaErrorInvalidValue;
-    CUtensorMap mxb, mhb, mxm, mhm;
-    if (!tc::make_map(&mxb, x_perm, A, s.H, kBigBox) || !tc::make_map(&mhb, h, A, s.I, kBigBox) ||
-        !tc::make_map(&mxm, x_perm, A, s.H, kMidBox) || !tc::make_map(&mhm, h, A, s.I, kMidBox))
-        return cudaErrorInvalidValue;
+    const bool packed = lora && lora->packed;
+    if (packed) {
+        const LoraPack L = lora_pack_layout(s);
+        const char *pk = static_cast<const char *>(lora->packed);
+        if (!tc::make_map(&m.l.lax, pk + L.ax, (uint64_t)s.E * 32, s.H, 32) ||
+            !tc::make_map(&m.l.lah, pk + L.ah, (uint64_t)s.E * 16, s.I, 16) ||
+            !tc::make_map(&m.l.lbg, pk + L.bgu, (uint64_t)s.E * s.I, 64, kRows) ||
+            !tc::make_map(&m.l.lbd, pk + L.bd, (uint64_t)s.E * s.H, 64, kRows) ||
+            !tc::make_map(&m.l.xa16, xa, A, 64, kNBox) || !tc::make_map(&m.l.xa128, xa, A, 64, kBigBox) ||
+            !tc::make_map(&m.l.ha16, ha, A, 64, kNBox) || !tc::make_map(&m.l.ha128, ha, A, 64, kBigBox))
+            return cudaErrorInvalidValue;
+    }
 
     // Large batches (at least 128 assignments per expert on average) take gate/up tiles of
     // up to 256 tokens (both TMEM halves, three 64 KB stages): an MMA of N = 256 reads
@@ -598,8 +739,9 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     const bool wide = (size_t)A >= (size_t)kMaxN * s.E;
     const int cmax = wide ? kWideN : kMaxN;
     const int dmax = kMaxDownN;
-    const TileListArgs ta{cmax, wide ? 1 : 0, dmax, 1, s.I / kRows, s.H / kRows, epi_warps(lora != nullptr),
-                          (int)max_tiles(s)};
+    const int mode = !lora ? kLoraNone : packed ? kLoraPacked : kLoraEpi;
+    const TileListArgs ta{cmax, wide ? 1 : 0, dmax, 1, s.I / kRows, s.H / kRows, epi_warps(mode), (int)max_tiles(s),
+                          packed ? 1 : 0};
     cudaError_t e = launch_pdl(prep_kernel, dim3(prep_blocks(A)), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
                                offsets, s.T, s.k, s.H, s.E, ta, x_perm, tiles, sched, done, err);
     if (e != cudaSuccess) return e;
@@ -621,15 +763,16 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.dmax = dmax;
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
-    if (!lora)
-        return wide        ? launch_tc<kWideN, 3>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, prm)
-               : s.T <= 32 ? launch_tc<32, 6>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, prm)
-                           : launch_tc<kMaxN, 4>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, prm);
-    auto run = [&](const Params &pr) {
-        return wide        ? launch_tc<kWideN, 3, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, pr)
-               : s.T <= 32 ? launch_tc<32, 6, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, pr)
-                           : launch_tc<kMaxN, 4, true>(grid, st, mg, mu, md, mx, mh, mxb, mhb, mxm, mhm, pr);
-    };
+    if (!lora) return launch_tc_for<kLoraNone>(s, wide, grid, st, m, prm);
+    if (packed) {
+        prm.lora_packed = 1;
+        prm.lora_scale = lora->scale;
+        prm.xab = reinterpret_cast<uint16_t *>(xa);
+        prm.hab = reinterpret_cast<uint16_t *>(ha);
+        // one launch: A-side tiles first in the list, every wait on the per-expert counters
+        return launch_tc_for<kLoraPacked>(s, wide, grid, st, m, prm);
+    }
+    auto run = [&](const Params &pr) { return launch_tc_for<kLoraEpi>(s, wide, grid, st, m, pr); };
     prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
     if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, lpart, st)) != cudaSuccess) return e;
     prm.phase = kPhaseGateUp;

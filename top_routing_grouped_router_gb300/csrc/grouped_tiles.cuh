@@ -35,19 +35,28 @@ __host__ __device__ constexpr uint32_t pack_tile(int down, int e, int rb, int nc
     return (uint32_t(down) << 31) | (uint32_t(e) << 16) | (uint32_t(rb) << 8) | uint32_t(nc);
 }
 
-// Tile record of the bf16 kernels: x = packed word, y = first permuted row, z = rows,
-// w = h publications (gate/up epilogue arrivals) a down tile waits for (0 for gate/up).
+// Tile kinds of the bf16 kernel's records (the 4-bit kernel's list uses pack_tile).
+enum : int { kRecGateUp = 0, kRecDown = 1, kRecLoraX = 3, kRecLoraH = 4 };
+// Tile record of the bf16 kernels: x = kind (bits 28-30), expert (16-23), row block (8-15),
+// token chunk (0-7); y = first permuted row, z = rows; w = the publications the tile waits
+// for: bits 0-15 h publications (gate/up epilogue warps; down and LoRA-h tiles), bits
+// 16-31 LoRA A-side publications of its expert (x . A^T for a gate/up tile, h . A_down^T
+// for a down tile; packed adapters only).
+__host__ __device__ constexpr uint32_t pack_rec(int kind, int e, int rb, int nc) {
+    return (uint32_t(kind) << 28) | (uint32_t(e) << 16) | (uint32_t(rb) << 8) | uint32_t(nc);
+}
 struct TileRec {
-    int down, e, rb, r0, m, need;
+    int down, e, rb, r0, m, need, need_l;  // down: the kind
 };
 __device__ __forceinline__ TileRec unpack_rec(uint4 r) {
     TileRec t;
-    t.down = int(r.x >> 31);
+    t.down = int((r.x >> 28) & 7);
     t.e = int((r.x >> 16) & 0xFF);
     t.rb = int((r.x >> 8) & 0xFF);
     t.r0 = int(r.y);
     t.m = int(r.z);
-    t.need = int(r.w);
+    t.need = int(r.w & 0xFFFFu);
+    t.need_l = int(r.w >> 16);
     return t;
 }
 
@@ -87,15 +96,25 @@ struct TileListArgs {
     int dn_per;            // down tiles per chunk (row blocks of H)
     int pub;               // h publications per gate/up tile (epilogue warps that write h)
     int max_tiles;         // capacity of `tiles`
+    int lora;              // also LoRA A-side tiles: x . A^T before the gate/up tiles, h . A_down^T
+                           // before the down tiles, one per 128-token chunk of an expert
 };
 
 // Scheduling words next to the tile list: [0] claim counter of the gate/up (or all) tiles,
 // [1] number of tiles, [2] number of gate/up tiles (they come first), [3] claim counter
-// of the down tiles when those run in a launch of their own.
+// of the down tiles when those run in a launch of their own (the 4-bit kernel's list).
+// The bf16 kernel's list has up to four ranges, [bound[i], bound[i+1]) for i = LoRA-x,
+// gate/up, LoRA-h, down, each with its own claim counter.
 enum : int { kSchedClaim = 0, kSchedTiles = 1, kSchedGateUp = 2, kSchedClaimDown = 3 };
+enum : int { kSchedRangeClaim = 8, kSchedBound = 12 };  // 4 claim counters, 5 bounds
+constexpr int kLoraChunk = 128;  // tokens per LoRA A-side tile (the MMA's M)
+constexpr int kLoraPub = 4;      // publications per LoRA A-side tile (one epilogue warp per lane quadrant)
+// Per-expert completion counters after the scheduling words: h publications, then the
+// LoRA A-side publications of x . A^T and of h . A_down^T.
+constexpr int kCountersPerExpert = 3;
 
 // Block 0: the tile list from the offsets, the scheduling words (zeroed claim counters)
-// and zeroed per-expert completion counters.  Blocks 1..: x_perm rows, one per warp
+// and zeroed per-expert completion counters (done[e], done[kMaxE + e], done[2 kMaxE + e]).  Blocks 1..: x_perm rows, one per warp
 // (kPrepRowsPerBlock per block).
 constexpr int kPrepRowsPerBlock = 8;
 __host__ __device__ constexpr int prep_blocks(int A) { return 1 + (A + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock; }
@@ -139,33 +158,52 @@ prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, c
             off = me = 0;
         }
         done[e] = 0;
+        done[kMaxE + e] = 0;
+        done[2 * kMaxE + e] = 0;
     }
     const int bgu = chunk_base(me, ta.gu_cmax, ta.gu_even != 0);
     const int bdn = chunk_base(me, ta.dn_cmax, ta.dn_even != 0);
     const int nch_gu = n_chunks(me, ta.gu_cmax, ta.gu_even != 0);
     const int nch_dn = n_chunks(me, ta.dn_cmax, ta.dn_even != 0);
-    int n_gu, n_dn;
+    const int nch_l = ta.lora ? (me + kLoraChunk - 1) / kLoraChunk : 0;
+    int n_gu, n_dn, n_l;
     const int gu_off = scan256(nch_gu * ta.gu_per, s_warp, n_gu);
     const int dn_off = scan256(nch_dn * ta.dn_per, s_warp, n_dn);
+    const int l_off = scan256(nch_l, s_warp, n_l);
+    // ranges: [0, n_l) LoRA-x, then gate/up, then [.., + n_l) LoRA-h, then down
+    const int b1 = n_l, b2 = b1 + n_gu, b3 = b2 + n_l, b4 = b3 + n_dn;
+    auto put = [&](int i, uint4 rec) {
+        if (i < ta.max_tiles) tiles[i] = rec;
+    };
+    const uint32_t need = uint32_t(nch_gu * ta.gu_per * ta.pub);          // h publications
+    const uint32_t need_l = uint32_t(nch_l * kLoraPub) << 16;             // A-side publications
+    for (int c = 0; c < nch_l; ++c) {
+        const uint32_t r0 = uint32_t(off + c * kLoraChunk), m = uint32_t(min(kLoraChunk, me - c * kLoraChunk));
+        put(l_off + c, make_uint4(pack_rec(kRecLoraX, e, 0, c), r0, m, 0u));
+        put(b2 + l_off + c, make_uint4(pack_rec(kRecLoraH, e, 0, c), r0, m, need));
+    }
     for (int c = 0; c < nch_gu; ++c)
-        for (int r = 0; r < ta.gu_per; ++r) {
-            const int i = gu_off + c * ta.gu_per + r;
-            if (i < ta.max_tiles)
-                tiles[i] = make_uint4(pack_tile(0, e, r, c), uint32_t(off + c * bgu), uint32_t(min(bgu, me - c * bgu)), 0u);
-        }
-    const uint32_t need = uint32_t(nch_gu * ta.gu_per * ta.pub);
+        for (int r = 0; r < ta.gu_per; ++r)
+            put(b1 + gu_off + c * ta.gu_per + r,
+                make_uint4(pack_rec(kRecGateUp, e, r, c), uint32_t(off + c * bgu), uint32_t(min(bgu, me - c * bgu)),
+                           need_l));
     for (int c = 0; c < nch_dn; ++c)
-        for (int r = 0; r < ta.dn_per; ++r) {
-            const int i = n_gu + dn_off + c * ta.dn_per + r;
-            if (i < ta.max_tiles)
-                tiles[i] = make_uint4(pack_tile(1, e, r, c), uint32_t(off + c * bdn), uint32_t(min(bdn, me - c * bdn)), need);
-        }
+        for (int r = 0; r < ta.dn_per; ++r)
+            put(b3 + dn_off + c * ta.dn_per + r,
+                make_uint4(pack_rec(kRecDown, e, r, c), uint32_t(off + c * bdn), uint32_t(min(bdn, me - c * bdn)),
+                           need | need_l));
     if (threadIdx.x == 0) {
-        if (n_gu + n_dn > ta.max_tiles) record_error(err, MOE_ERR_DEVICE);  // inconsistent offsets
+        if (b4 > ta.max_tiles) record_error(err, MOE_ERR_DEVICE);  // inconsistent offsets
         sched[kSchedClaim] = 0;
-        sched[kSchedTiles] = min(n_gu + n_dn, ta.max_tiles);
-        sched[kSchedGateUp] = min(n_gu, ta.max_tiles);
+        sched[kSchedTiles] = min(b4, ta.max_tiles);
+        sched[kSchedGateUp] = min(b2, ta.max_tiles);
         sched[kSchedClaimDown] = 0;
+        for (int i = 0; i < 4; ++i) sched[kSchedRangeClaim + i] = 0;
+        sched[kSchedBound + 0] = 0;
+        sched[kSchedBound + 1] = min(b1, ta.max_tiles);
+        sched[kSchedBound + 2] = min(b2, ta.max_tiles);
+        sched[kSchedBound + 3] = min(b3, ta.max_tiles);
+        sched[kSchedBound + 4] = min(b4, ta.max_tiles);
     }
 }
 

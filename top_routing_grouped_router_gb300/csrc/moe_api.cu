@@ -66,7 +66,7 @@ WsLayout ws_layout(const moe_shape &s) {
     L.h = take(A * s.I * 4);
     L.y = take(A * s.H * act_bytes(s));
     L.xa = take(A * 32 * 4);
-    L.ha = take(A * 16 * 4);
+    L.ha = take(A * 32 * 4);  // fp32 [A][16], or bf16 [A][64] with packed adapters
     L.lpart = take(lora_part_floats(s) * 4);
     L.part = take(grouped_fast_part_bytes(select_grouped_path(s), s));
     L.total = off;
@@ -246,6 +246,35 @@ int moe_forward(const moe_shape *shape, const void *x, const void *w_router, con
                         workspace, reinterpret_cast<cudaStream_t>(stream), nullptr, 0.f, nullptr, nullptr);
 }
 
+static int check_lora(const moe_lora *lora) {
+    if (!lora) return MOE_ERR_NULLPTR;
+    if (!lora->a_gate || !lora->b_gate || !lora->a_up || !lora->b_up || !lora->a_down || !lora->b_down)
+        return MOE_ERR_NULLPTR;
+    if (lora->rank < 1 || lora->rank > 16 || !std::isfinite(lora->scale)) return MOE_ERR_SHAPE;
+    if (misaligned(lora->a_gate) || misaligned(lora->b_gate) || misaligned(lora->a_up) || misaligned(lora->b_up) ||
+        misaligned(lora->a_down) || misaligned(lora->b_down))
+        return MOE_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(lora->packed) & 255u) return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
+int moe_lora_pack_size(const moe_shape *shape, size_t *bytes) {
+    MOE_TRY(validate_shape(shape));
+    if (!bytes) return MOE_ERR_NULLPTR;
+    *bytes = lora_pack_layout(*shape).total;
+    return MOE_OK;
+}
+
+int moe_lora_pack(const moe_shape *shape, const moe_lora *lora, void *packed, size_t packed_bytes,
+                  moe_stream_t stream) {
+    MOE_TRY(validate_shape(shape));
+    MOE_TRY(check_lora(lora));
+    if (!packed) return MOE_ERR_NULLPTR;
+    if (reinterpret_cast<uintptr_t>(packed) & 255u) return MOE_ERR_ALIGN;
+    if (packed_bytes < lora_pack_layout(*shape).total) return MOE_ERR_WORKSPACE;
+    return launch_rc(launch_lora_pack(*shape, *lora, packed, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_forward_lora(const moe_shape *shape, const void *x, const void *w_router, const float *b_router,
                      const void *w_gate, const void *w_up, const void *w_down, const moe_q4 *q4, const moe_lora *lora,
                      void *out, int32_t *expert_ids_out, float *weights_out, void *workspace, size_t workspace_bytes,
@@ -253,12 +282,7 @@ int moe_forward_lora(const moe_shape *shape, const void *x, const void *w_router
     MOE_TRY(validate_shape(shape));
     const moe_shape &s = *shape;
     if (!x || !w_router || !out || !lora) return MOE_ERR_NULLPTR;
-    if (!lora->a_gate || !lora->b_gate || !lora->a_up || !lora->b_up || !lora->a_down || !lora->b_down)
-        return MOE_ERR_NULLPTR;
-    if (lora->rank < 1 || lora->rank > 16 || !std::isfinite(lora->scale)) return MOE_ERR_SHAPE;
-    if (misaligned(lora->a_gate) || misaligned(lora->b_gate) || misaligned(lora->a_up) || misaligned(lora->b_up) ||
-        misaligned(lora->a_down) || misaligned(lora->b_down))
-        return MOE_ERR_ALIGN;
+    MOE_TRY(check_lora(lora));
     MOE_TRY(check_weights(s, w_gate, w_up, w_down, q4));
     MOE_TRY(check_ws(s, workspace, workspace_bytes));
     if (misaligned(x) || misaligned(w_router) || misaligned(out)) return MOE_ERR_ALIGN;

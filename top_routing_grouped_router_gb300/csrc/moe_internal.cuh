@@ -133,8 +133,22 @@ __device__ __forceinline__ void lora_row16(const float *B, size_t row, int rank,
     for (int q = 0; q < 16; ++q) b[q] = q < rank ? __ldg(B + row * rank + q) : 0.f;
 }
 
-// Grouped kernels run all tiles (0), only the gate/up tiles (1) or only the down tiles (2).
-enum : int { kPhaseAll = 0, kPhaseGateUp = 1, kPhaseDown = 2 };
+// Grouped kernels run all tiles (0), only the gate/up tiles (1) or only the down tiles (2);
+// the bf16 kernel with packed LoRA adapters also runs the A-side tiles on their own: x . A^T
+// (3) before the gate/up tiles, h . A_down^T (4) before the down tiles.
+enum : int { kPhaseAll = 0, kPhaseGateUp = 1, kPhaseDown = 2, kPhaseLoraX = 3, kPhaseLoraH = 4 };
+
+// Packed adapters of the bf16 tensor-core LoRA path (moe_lora_pack): bf16, zero-padded,
+// each region 256-byte aligned.
+//   ax  [E][32][H]  rows 0..15 A_gate, 16..31 A_up (rows past the rank zero)
+//   ah  [E][16][I]  A_down
+//   bgu [E*I][64]   columns 0..15 B_gate, 16..31 B_up, the rest zero
+//   bd  [E*H][64]   columns 0..15 B_down, the rest zero
+struct LoraPack {
+    size_t ax, ah, bgu, bd, total;  // byte offsets and size
+};
+LoraPack lora_pack_layout(const moe_shape &s);
+cudaError_t launch_lora_pack(const moe_shape &s, const moe_lora &l, void *dst, cudaStream_t st);
 
 // A-side LoRA products (lora.cu); `part` holds lora_part_floats() floats of slice sums.
 size_t lora_part_floats(const moe_shape &s);
