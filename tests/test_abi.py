@@ -120,3 +120,28 @@ def test_graph_arena_covers_every_bucket_workspace():
     static = 2 * 64 * 2048 * 2 + 64 * 8 * 4
     assert arena >= ws64 + static
     assert arena <= ws64 + static + 4 * 256
+
+
+def test_lora_pack_size_is_the_four_padded_bf16_arrays():
+    # [E][32][H] + [E][16][I] + [E*I][64] + [E*H][64] bf16, each region rounded up to 256 bytes
+    E, H, I = 128, 2048, 768
+    shape = moe.make_shape(8, H, E, 8, I)
+    al = lambda b: (b + 255) // 256 * 256
+    want = al(E * 32 * H * 2) + al(E * 16 * I * 2) + al(E * I * 64 * 2) + al(E * H * 64 * 2)
+    assert moe.moe_lora_pack_size(shape) == want
+    odd = moe.make_shape(3, 24, 5, 2, 40)
+    assert moe.moe_lora_pack_size(odd) == al(5 * 32 * 24 * 2) + al(5 * 16 * 40 * 2) + al(5 * 40 * 128) + al(5 * 24 * 128)
+
+
+def test_lora_pack_rejects_bad_arguments_without_a_gpu_call(L):
+    st = None
+    shape = moe.make_shape(8, 128, 8, 2, 64)
+    fake = ctypes.c_void_p(1 << 20)
+    lo = moe.MoELora(16, 2.0, fake, fake, fake, fake, fake, fake, None)
+    need = moe.moe_lora_pack_size(shape)
+    # NULL pack, misaligned pack, too small, rank out of range: all refused before any launch
+    assert L.moe_lora_pack(ctypes.byref(shape), ctypes.byref(lo), None, need, st) == -1
+    assert L.moe_lora_pack(ctypes.byref(shape), ctypes.byref(lo), ctypes.c_void_p((1 << 20) + 16), need, st) == -5
+    assert L.moe_lora_pack(ctypes.byref(shape), ctypes.byref(lo), fake, need - 1, st) == -4
+    bad = moe.MoELora(17, 2.0, fake, fake, fake, fake, fake, fake, None)
+    assert L.moe_lora_pack(ctypes.byref(shape), ctypes.byref(bad), fake, need, st) == -2
