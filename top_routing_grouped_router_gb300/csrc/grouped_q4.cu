@@ -19,7 +19,7 @@
 //    in the mantissa of a bf16 pair with one shift + LOP3: bits 0x4300 | (j << 1) are
 //    exactly 128 + 2j, so one bf16x2 subtraction gives the exact integers 2j - 2j0,
 //    and one bf16x2 multiply by s*b/2 gives the weights (one rounding);
-//  * warp 1 lane 0: tcgen05.mma from the A ring and the token rows still in the raw
+//  * warp 1 (converged, one elected lane): tcgen05.mma from the A ring and the token rows still in the raw
 //    ring, accumulators in TMEM (gate and up in separate column ranges);
 //  * warps 2-5: epilogue as in the bf16 kernel.
 // The shift + LOP3 pairs nibbles m and m+4 of a 32-bit word, so each 8-element group
@@ -348,19 +348,23 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             if (++a == kAStages) { a = 0; ap ^= 1; }
             if (ks < 0 || *abort) break;
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
+        // The whole warp runs this loop, converged (the waits' outcomes are voted), and one
+        // elected lane issues each MMA and commit: far fewer issue cycles per MMA than a lone
+        // lane, which matters for the small-N MMAs of decode.
         int r = 0, a = 0, tile_count = 0;
         uint32_t ap = 0;
         for (;;) {
-            mbar_wait(smem_u32(&afull[a]), ap, p.err, abort);
+            const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&afull[a]), ap, p.err, abort));
             const int *mt = rmeta + 8 * r;
             const int kind = mt[0], ks = mt[1], nstage = mt[2], N = mt[3];
-            if (ks < 0 || *abort) break;
+            if (__any_sync(0xffffffffu, !got || ks < 0 || *abort)) break;
             const int down = kind & 3, two = kind >> 2;
             const int b = tile_count & 1;
             if (ks == 0) {
-                mbar_wait(smem_u32(&acce[b]), ((tile_count >> 1) & 1) ^ 1, p.err, abort);
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce[b]), ((tile_count >> 1) & 1) ^ 1, p.err, abort)))
+                    break;
                 tc_fence_after();
             }
             tc_fence_after();
@@ -372,26 +376,26 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 #pragma unroll
                 for (int kk = 0; kk < kSlab / 16; ++kk) {
                     const uint64_t bdesc = smem_desc(bb + kk * 32);
-                    mma_bf16(d, smem_desc(a0 + kk * 32), bdesc, idesc, (ks | kk) != 0);
-                    mma_bf16(d + kUpCol, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, (ks | kk) != 0);
+                    mma_bf16_warp(d, smem_desc(a0 + kk * 32), bdesc, idesc, (ks | kk) != 0);
+                    mma_bf16_warp(d + kUpCol, smem_desc(a0 + kABytes + kk * 32), bdesc, idesc, (ks | kk) != 0);
                 }
             } else {
                 for (int h2 = 0; h2 < 1 + two; ++h2)
 #pragma unroll
                     for (int kk = 0; kk < kSlab / 16; ++kk)
-                        mma_bf16(d, smem_desc(a0 + h2 * kABytes + kk * 32), smem_desc(bb + h2 * kHalfTok + kk * 32), idesc,
-                                 (ks | h2 | kk) != 0);
+                        mma_bf16_warp(d, smem_desc(a0 + h2 * kABytes + kk * 32), smem_desc(bb + h2 * kHalfTok + kk * 32),
+                                      idesc, (ks | h2 | kk) != 0);
             }
-            mma_commit(smem_u32(&aempty[a]));
-            mma_commit(smem_u32(&rempty[r]));
+            mma_commit_warp(smem_u32(&aempty[a]));
+            mma_commit_warp(smem_u32(&rempty[r]));
             if (ks == nstage - 1) {
-                mma_commit(smem_u32(&accf[b]));
+                mma_commit_warp(smem_u32(&accf[b]));
                 ++tile_count;
             }
             if (++r == kRawStages) r = 0;
             if (++a == kAStages) { a = 0; ap ^= 1; }
         }
-        mma_commit(smem_u32(drain));
+        mma_commit_warp(smem_u32(drain));
         mbar_wait(smem_u32(drain), 0, p.err, abort);
     } else if (warp >= 2 && warp < 2 + kEpiWarps) {
         // ------------------------------------------------ epilogue
