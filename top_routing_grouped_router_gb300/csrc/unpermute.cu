@@ -12,7 +12,7 @@ namespace {
 constexpr int kThreads = 64;
 constexpr int kCols = 8;
 
-template <typename T>
+template <int kBatch, typename T>
 __global__ void __launch_bounds__(kThreads)
 unpermute_kernel(const T *__restrict__ y, const float *__restrict__ w, const int32_t *__restrict__ pos,
                  T *__restrict__ out, int k, int H, int A, int col_blocks, const T *__restrict__ resid) {
@@ -20,8 +20,10 @@ unpermute_kernel(const T *__restrict__ y, const float *__restrict__ w, const int
     griddep_wait();
     const int t = blockIdx.x / col_blocks;
     const int c0 = ((blockIdx.x % col_blocks) * kThreads + threadIdx.x) * kCols;
-    if (c0 < H) unpermute8(y, w, pos, out, t, c0, k, H, A, resid);
+    if (c0 < H) unpermute8<kBatch>(y, w, pos, out, t, c0, k, H, A, resid);
 }
+
+constexpr int kBatchMaxT = 64;  // up to this many tokens the slots are read 8 at a time
 
 }  // namespace
 
@@ -30,12 +32,14 @@ cudaError_t launch_unpermute(const moe_shape &s, const void *y, const float *w, 
     if (s.T == 0) return cudaSuccess;
     const int cb = (s.H / kCols + kThreads - 1) / kThreads;
     const unsigned grid = unsigned(cb) * unsigned(s.T);
+    const bool small = s.T <= kBatchMaxT;
     if (s.act_dtype == MOE_DT_F32)
-        return launch_pdl(unpermute_kernel<float>, dim3(grid), dim3(kThreads), 0, st, static_cast<const float *>(y), w,
-                          pos, static_cast<float *>(out), s.k, s.H, s.T * s.k, cb, static_cast<const float *>(resid));
-    return launch_pdl(unpermute_kernel<uint16_t>, dim3(grid), dim3(kThreads), 0, st, static_cast<const uint16_t *>(y),
-                      w, pos, static_cast<uint16_t *>(out), s.k, s.H, s.T * s.k, cb,
-                      static_cast<const uint16_t *>(resid));
+        return launch_pdl(small ? unpermute_kernel<8, float> : unpermute_kernel<1, float>, dim3(grid), dim3(kThreads),
+                          0, st, static_cast<const float *>(y), w, pos, static_cast<float *>(out), s.k, s.H, s.T * s.k,
+                          cb, static_cast<const float *>(resid));
+    return launch_pdl(small ? unpermute_kernel<8, uint16_t> : unpermute_kernel<1, uint16_t>, dim3(grid),
+                      dim3(kThreads), 0, st, static_cast<const uint16_t *>(y), w, pos, static_cast<uint16_t *>(out),
+                      s.k, s.H, s.T * s.k, cb, static_cast<const uint16_t *>(resid));
 }
 
 }  // namespace moe

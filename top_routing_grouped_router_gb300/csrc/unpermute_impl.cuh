@@ -37,20 +37,33 @@ __device__ __forceinline__ void unp_store8(uint16_t *p, const float *v) {
 // Columns [c0, c0 + 8) of token t.  A slot whose pos is outside [0, A) contributes nothing.
 // With a residual stream `resid` ([T][H], may be null) the sum is added to it before the
 // single rounding: out = resid + sum_j w_j y_j.
-template <typename T>
+// kBatch slots at a time: every position and weight of a batch, then every row, is
+// requested before the first is used (the sum stays in slot order).  Small batches are
+// latency-bound and take kBatch = 8; large ones need the occupancy of kBatch = 1.
+template <int kBatch, typename T>
 __device__ __forceinline__ void unpermute8(const T *y, const float *w, const int32_t *pos, T *out, int t, int c0,
                                            int k, int H, int A, const T *resid = nullptr) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-        const int p = __ldg(pos + (size_t)t * k + j);
-        if (p < 0 || p >= A) continue;
-        const float wt = __ldg(w + (size_t)t * k + j);
-        float v[8];
-        unp_load8(y + (size_t)p * H + c0, v);
+    for (int j0 = 0; j0 < k; j0 += kBatch) {
+        int pp[kBatch];
+        float ww[kBatch];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wt, v[i], acc[i]);
+        for (int j = 0; j < kBatch; ++j) {
+            pp[j] = j0 + j < k ? __ldg(pos + (size_t)t * k + j0 + j) : -1;
+            ww[j] = j0 + j < k ? __ldg(w + (size_t)t * k + j0 + j) : 0.f;
+        }
+        float v[kBatch][8];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (pp[j] >= 0 && pp[j] < A) unp_load8(y + (size_t)pp[j] * H + c0, v[j]);
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (pp[j] >= 0 && pp[j] < A) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(ww[j], v[j][i], acc[i]);
+            }
     }
     if (resid) {
         float r[8];
