@@ -116,9 +116,11 @@ typedef struct {
  *
  * packed: NULL, or the output of moe_lora_pack for these adapters (device,
  * 256-byte aligned).  With a pack, the bf16 tensor-core path runs the adapter
- * products on the tensor cores: bf16 operands (the adapters and scale * x . A^T
- * rounded to nearest even), fp32 accumulation, as for the base weights.  Without
- * one, and on every other path, they run in fp32 on CUDA cores.
+ * products on the tensor cores.  Each fp32 operand (the adapters, and
+ * scale * x . A^T) is split as hi = bf16(v), lo = bf16(v - hi), and the products
+ * are hi.hi + hi.lo + lo.hi with fp32 accumulation (x is bf16 already, so
+ * x . A^T takes x.hi + x.lo): close to fp32 accuracy.  Without a pack, and on
+ * every other path, the products run in fp32 on CUDA cores.
  */
 typedef struct {
     int32_t rank;
@@ -251,11 +253,12 @@ MOE_API int moe_forward_lora(const moe_shape *shape, const void *x, const void *
 
 /*
  * Bytes of the adapter pack for this shape (host only, no CUDA call): the four
- * bf16 arrays the tensor-core LoRA path reads, zero-padded, each 256-byte aligned:
- *   [E][32][H]  A_gate rows 0..r-1, A_up rows 16..16+r-1
- *   [E][16][I]  A_down rows 0..r-1
- *   [E*I][64]   B_gate columns 0..r-1, B_up columns 16..16+r-1
- *   [E*H][64]   B_down columns 0..r-1
+ * bf16 arrays the tensor-core LoRA path reads, zero-padded, each 256-byte aligned
+ * (hi = bf16(v), lo = bf16(v - hi); rank rows or columns past r are zero):
+ *   [E][64][H]   A_gate hi, A_up hi, A_gate lo, A_up lo  (16 rows each)
+ *   [E][32][I]   A_down hi, A_down lo                    (16 rows each)
+ *   [E*I][128]   B_gate then B_up, each as 64 columns (hi, hi, lo, 0) x 16
+ *   [E*H][64]    B_down as (hi, hi, lo, 0) x 16 columns
  */
 MOE_API int moe_lora_pack_size(const moe_shape *shape, size_t *bytes);
 

@@ -123,14 +123,14 @@ def test_graph_arena_covers_every_bucket_workspace():
 
 
 def test_lora_pack_size_is_the_four_padded_bf16_arrays():
-    # [E][32][H] + [E][16][I] + [E*I][64] + [E*H][64] bf16, each region rounded up to 256 bytes
+    # [E][64][H] + [E][32][I] + [E*I][128] + [E*H][64] bf16, each region rounded up to 256 bytes
     E, H, I = 128, 2048, 768
     shape = moe.make_shape(8, H, E, 8, I)
     al = lambda b: (b + 255) // 256 * 256
-    want = al(E * 32 * H * 2) + al(E * 16 * I * 2) + al(E * I * 64 * 2) + al(E * H * 64 * 2)
+    want = al(E * 64 * H * 2) + al(E * 32 * I * 2) + al(E * I * 128 * 2) + al(E * H * 64 * 2)
     assert moe.moe_lora_pack_size(shape) == want
     odd = moe.make_shape(3, 24, 5, 2, 40)
-    assert moe.moe_lora_pack_size(odd) == al(5 * 32 * 24 * 2) + al(5 * 16 * 40 * 2) + al(5 * 40 * 128) + al(5 * 24 * 128)
+    assert moe.moe_lora_pack_size(odd) == al(5 * 64 * 24 * 2) + al(5 * 32 * 40 * 2) + al(5 * 40 * 256) + al(5 * 24 * 128)
 
 
 def test_lora_pack_rejects_bad_arguments_without_a_gpu_call(L):

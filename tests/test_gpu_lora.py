@@ -97,6 +97,23 @@ def test_lora_packed_mid_batch_bf16_rank7():
     _check(synth.make_custom(64, 1024, 32, 4, 256, seed=45, name="lora64"), 7, 16, packed=True)
 
 
+def test_lora_packed_single_token_rank1():
+    # one token, rank 1: A-side tiles of a single row, the rest of each tile padding
+    _check(synth.make_custom(1, 256, 8, 2, 128, seed=53, name="lora1"), 1, None, packed=True)
+
+
+def test_lora_pack_is_ignored_off_the_bf16_path():
+    # a pack passed with fp32 weights changes nothing: the fp32 path keeps fp32 adapters
+    inp = synth.make_inputs("tiny")
+    lora = synth.make_lora(inp.E, inp.H, inp.I, rank=4, seed=7)
+    L = upload(inp)
+    plain, keep = _dev_lora(lora)
+    packed, keep2 = _dev_lora(lora, L.shape)
+    a, _ = _run_lora(L, plain)
+    b, _ = _run_lora(L, packed)
+    assert torch.equal(a, b)
+
+
 def test_lora_packed_large_batch_bf16_rank16():
     # 2048 assignments over 16 experts (128 per expert on average): 256-token gate/up tiles
     _check(synth.make_custom(512, 1024, 16, 4, 384, seed=51, name="lora512"), 16, 16, packed=True)

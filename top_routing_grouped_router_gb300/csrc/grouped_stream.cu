@@ -84,8 +84,8 @@ struct Params {
     LoraDev lora;               // LoRA B-side terms of the epilogue (rank 0: none)
     int lora_packed;            // packed adapters: A-side tiles and a B-side stage per tile
     float lora_scale;
-    uint16_t *xab;              // [A][64] bf16: scale * x . A^T (gate 0..15, up 16..31), rest zero
-    uint16_t *hab;              // [A][64] bf16: scale * h . A_down^T (0..15), rest zero
+    uint16_t *xab;              // [A][128] bf16: scale * x . A^T, split (see the LoRA stage)
+    uint16_t *hab;              // [A][64] bf16: scale * h . A_down^T, split
     int *done;                  // [3][kMaxE] publications: h (per epilogue warp of a gate/up tile),
                                 // then x . A^T and h . A_down^T (per quadrant warp of an A-side tile)
     int32_t *err;
@@ -258,7 +258,9 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             const bool lora_a = d.down == kLoraX || d.down == kLoraH;
-            const int nl = d.down == kLoraX ? 32 : 16;  // adapter rows of an A-side tile (its MMA's N)
+            // adapter rows of an A-side tile (its MMA's N): hi and lo parts of A_gate and A_up
+            // (x side) or of A_down (h side)
+            const int nl = d.down == kLoraX ? 64 : 32;
             int hmask;  // TMEM halves of this tile (bit h = half h)
             if (d.down == kGateUp && d.N > 128) {
                 hmask = 3;
@@ -285,9 +287,12 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const int kdim = (d.down == kDown || d.down == kLoraH) ? p.I : p.H;
             const int two = !lora_a && d.down != kGateUp && d.N <= BCap / 2 && (kdim / kSlab) % 2 == 0;
             const int nslab = kdim / kSlab;
-            // with packed LoRA adapters a gate/up or down tile takes one more stage: the B
-            // adapter rows of its weight rows against scale * x . A^T (or h . A_down^T)
-            const int lst = kLora == kLoraPacked && p.lora_packed && (d.down == kGateUp || d.down == kDown);
+            // with packed LoRA adapters a gate/up tile takes two more stages (gate, up) and a down
+            // tile one: the B adapter rows of its weight rows against scale * x . A^T (or
+            // h . A_down^T), both split into bf16 hi + lo parts (see the LoRA stage)
+            const int lst = kLora == kLoraPacked && p.lora_packed && (d.down == kGateUp || d.down == kDown)
+                                ? (d.down == kGateUp ? 2 : 1)
+                                : 0;
             const int nstage = (two ? nslab / 2 : nslab) + lst;
             // token rows: the largest box (128, 64 or 16 rows) that the tile fills more than
             // half of and that fits the rows its region of the stage holds (rows past the tile
@@ -326,7 +331,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 if (!router && ks == min(2, nstage - 1))
                     next_rec = next < hi ? __ldg(p.tiles + next) : make_uint4(0, 0, 0, 0);
                 const uint32_t fb = smem_u32(&full[stage]);
-                const bool lstage = lst && ks == nstage - 1;
+                const bool lstage = lst && ks >= nstage - lst;
                 mbar_arrive_expect_tx(fb, lstage ? lbytes : bytes);
                 const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
                 const uint32_t bb = a0 + 2 * kABytes;
@@ -334,17 +339,21 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 if constexpr (kLora == kLoraPacked) {
                     issued = lstage || lora_a;
                     if (lstage) {
-                    // B adapter rows of the tile's 128 weight rows (rank columns, zero-padded to
-                    // 64) and the tokens' scaled A-side products, in the token region of the kind;
-                    // those products must be complete (the expert's A-side tiles published)
+                        // B adapter rows of the tile's 128 weight rows and the tokens' scaled A-side
+                        // products (64-column slab li: gate, up, or down), in the token region of the
+                        // kind; those products must be complete (the expert's A-side tiles published)
                         const bool gu = d.down == kGateUp;
-                        wait_count(p.done + (gu ? 1 : 2) * kMaxE + d.e, d.need_l, p.err, abort);
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        tma_load_2d(a0, gu ? &lm.lbg : &lm.lbd, 0, d.e * (gu ? p.I : p.H) + d.rb * kRows, fb);
+                        const int li = ks - (nstage - lst);
+                        if (li == 0) {
+                            wait_count(p.done + (gu ? 1 : 2) * kMaxE + d.e, d.need_l, p.err, abort);
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                        }
+                        tma_load_2d(a0, gu ? &lm.lbg : &lm.lbd, li * kSlab, d.e * (gu ? p.I : p.H) + d.rb * kRows, fb);
                         const uint32_t tb = gu || two ? bb : a0 + kABytes;
                         const CUtensorMap *tm2 = gu ? (lbox == kBigBox ? &lm.xa128 : &lm.xa16)
                                                     : (lbox == kBigBox ? &lm.ha128 : &lm.ha16);
-                        for (int q = 0; q < lnbox; ++q) tma_load_2d(tb + q * lbox * 128, tm2, 0, d.r0 + q * lbox, fb);
+                        for (int q = 0; q < lnbox; ++q)
+                            tma_load_2d(tb + q * lbox * 128, tm2, li * kSlab, d.r0 + q * lbox, fb);
                     } else if (lora_a) {
                         // 128 token rows (the MMA's M side) and the expert's adapter rows (N)
                         const bool lx = d.down == kLoraX;
@@ -396,7 +405,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             if (__any_sync(0xffffffffu, first < 0 || *abort)) break;
             // A-side LoRA tiles run like a down tile: A at the slot's start, B after 16 KB
             const int down = (kind & 7) != kGateUp, two = (kind >> 3) & 1, hmask = (kind >> 4) & 3;
-            const int lst = (kind >> 6) & 1;
+            const int lst = (kind >> 6) & 3;  // LoRA stages at the end of the tile
             bool freed = true;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
@@ -411,14 +420,16 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             for (int ks = 0;;) {
                 const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
                 const uint32_t bb = a0 + 2 * kABytes;
-                if (kLora == kLoraPacked && lst && ks == nstage - 1) {
-                    // the LoRA stage: k = 0..15 of the slab against gate (or down), 16..31 against up
-                    if (!down) {
-                        mma_bf16_warp(d, smem_desc(a0), smem_desc(bb), idesc, 1u);
-                        mma_bf16_warp(d + up_col, smem_desc(a0 + 32), smem_desc(bb + 32), idesc, 1u);
-                    } else {
-                        mma_bf16_warp(d, smem_desc(a0), smem_desc(two ? bb : a0 + kABytes), idesc, 1u);
-                    }
+                if (kLora == kLoraPacked && lst && ks >= nstage - lst) {
+                    // a LoRA stage: the slab's k = 0..47 hold (B_hi, B_hi, B_lo) against the tokens'
+                    // (v_hi, v_lo, v_hi), so three K = 16 MMAs add B . v to within fp32-like error
+                    // (the bf16 products B_lo . v_lo are dropped); into gate or up (first or second
+                    // stage of a gate/up tile) or the down accumulator
+                    const uint32_t dst = (!down && ks == nstage - 1) ? d + up_col : d;
+                    const uint32_t tb = (!down || two) ? bb : a0 + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < 3; ++kk)
+                        mma_bf16_warp(dst, smem_desc(a0 + kk * 32), smem_desc(tb + kk * 32), idesc, 1u);
                 } else if (two) {
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2)
@@ -505,24 +516,43 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     }
                 }
             } else if (kLora == kLoraPacked && (down == kLoraX || down == kLoraH)) {
-                // tokens are the TMEM lanes here: row r0 + row gets its N adapter products,
-                // scaled, as one 64-column bf16 row (the columns past N zero)
+                // tokens are the TMEM lanes here: row r0 + row has x . A_hi^T in columns [0, N/2)
+                // and x . A_lo^T in [N/2, N); their sums v (16 per projection), scaled, go out as
+                // v_hi = bf16(v) and v_lo = bf16(v - v_hi), one 64-column slab per projection laid
+                // out (v_hi, v_lo, v_hi, 0): gate then up for x, down alone for h
                 if (part == 0) {
-                    uint32_t v[32];
-                    tmem_ld32(taddr, v);
+                    uint32_t v[64];
+                    tmem_ld32x2(taddr, taddr + 32, v);
                     if (row < m) {
-                        uint4 *dst = reinterpret_cast<uint4 *>((down == kLoraX ? p.xab : p.hab) + (size_t)(r0 + row) * 64);
+                        const int half = N / 2, nproj = half / 16;
+                        uint4 *dst = reinterpret_cast<uint4 *>((down == kLoraX ? p.xab : p.hab) +
+                                                               (size_t)(r0 + row) * 64 * nproj);
+                        for (int pj = 0; pj < nproj; ++pj) {
+                            uint32_t hi2[8], lo2[8];
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            uint32_t w[4];
+                            for (int i = 0; i < 8; ++i) {
+                                uint32_t hb[2], lb[2];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int c = 8 * g + 2 * i;
-                                const float lo = c < N ? p.lora_scale * __uint_as_float(v[c & 31]) : 0.f;
-                                const float hi = c + 1 < N ? p.lora_scale * __uint_as_float(v[(c + 1) & 31]) : 0.f;
-                                w[i] = uint32_t(f32_to_bf16_bits(lo)) | (uint32_t(f32_to_bf16_bits(hi)) << 16);
+                                for (int h = 0; h < 2; ++h) {
+                                    const int c = 16 * pj + 2 * i + h;
+                                    const float x = p.lora_scale * (__uint_as_float(v[c & 63]) +
+                                                                    __uint_as_float(v[(half + c) & 63]));
+                                    const uint16_t xh = f32_to_bf16_bits(x);
+                                    hb[h] = xh;
+                                    lb[h] = f32_to_bf16_bits(x - __uint_as_float(uint32_t(xh) << 16));
+                                }
+                                hi2[i] = hb[0] | (hb[1] << 16);
+                                lo2[i] = lb[0] | (lb[1] << 16);
                             }
-                            dst[g] = make_uint4(w[0], w[1], w[2], w[3]);
+                            uint4 *row64 = dst + pj * 8;  // 64 bf16 = 8 x 16 bytes
+                            row64[0] = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
+                            row64[1] = make_uint4(hi2[4], hi2[5], hi2[6], hi2[7]);
+                            row64[2] = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+                            row64[3] = make_uint4(lo2[4], lo2[5], lo2[6], lo2[7]);
+                            row64[4] = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
+                            row64[5] = make_uint4(hi2[4], hi2[5], hi2[6], hi2[7]);
+                            row64[6] = make_uint4(0u, 0u, 0u, 0u);
+                            row64[7] = make_uint4(0u, 0u, 0u, 0u);
                         }
                     }
                     // publish (read back through TMA by the expert's gate/up or down tiles)
@@ -722,11 +752,11 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     if (packed) {
         const LoraPack L = lora_pack_layout(s);
         const char *pk = static_cast<const char *>(lora->packed);
-        if (!tc::make_map(&m.l.lax, pk + L.ax, (uint64_t)s.E * 32, s.H, 32) ||
-            !tc::make_map(&m.l.lah, pk + L.ah, (uint64_t)s.E * 16, s.I, 16) ||
-            !tc::make_map(&m.l.lbg, pk + L.bgu, (uint64_t)s.E * s.I, 64, kRows) ||
+        if (!tc::make_map(&m.l.lax, pk + L.ax, (uint64_t)s.E * 64, s.H, 64) ||
+            !tc::make_map(&m.l.lah, pk + L.ah, (uint64_t)s.E * 32, s.I, 32) ||
+            !tc::make_map(&m.l.lbg, pk + L.bgu, (uint64_t)s.E * s.I, 128, kRows) ||
             !tc::make_map(&m.l.lbd, pk + L.bd, (uint64_t)s.E * s.H, 64, kRows) ||
-            !tc::make_map(&m.l.xa16, xa, A, 64, kNBox) || !tc::make_map(&m.l.xa128, xa, A, 64, kBigBox) ||
+            !tc::make_map(&m.l.xa16, xa, A, 128, kNBox) || !tc::make_map(&m.l.xa128, xa, A, 128, kBigBox) ||
             !tc::make_map(&m.l.ha16, ha, A, 64, kNBox) || !tc::make_map(&m.l.ha128, ha, A, 64, kBigBox))
             return cudaErrorInvalidValue;
     }

@@ -161,56 +161,73 @@ cudaError_t launch_a(const moe_shape &s, const SrcT *src, const int32_t *order, 
                       static_cast<const float *>(part), A, slices, out);
 }
 
+// 8 bf16 values (16 bytes): bf16(v), or with lo the remainder bf16(v - bf16(v)).
+__device__ __forceinline__ void write_split(uint16_t *dst, const float *v, bool lo) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t h[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float x = v[2 * j + k];
+            const uint16_t xh = f32_to_bf16_bits(x);
+            h[k] = lo ? f32_to_bf16_bits(x - __uint_as_float(uint32_t(xh) << 16)) : xh;
+        }
+        w[j] = h[0] | (h[1] << 16);
+    }
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // The packed adapters of the tensor-core path, 8 bf16 outputs (16 bytes) per thread; see
 // LoraPack for the layout.  Values are rounded to nearest even; rows / columns past the rank
-// are zero.
+// are zero.  Each B slab holds (B_hi, B_hi, B_lo, 0) in its four 16-column groups.
 __global__ void __launch_bounds__(256)
 lora_pack_kernel(moe_lora l, int E, int H, int I, size_t n_ax, size_t n_ah, size_t n_bgu, size_t n_bd,
                  uint16_t *ax, uint16_t *ah, uint16_t *bgu, uint16_t *bd) {
     const size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x;  // group of 8 outputs
     const int r = l.rank;
     float v[8];
-    uint16_t *dst;
     size_t i = g * 8;
-    if (i < n_ax) {  // [E][32][H]
+    if (i < n_ax) {  // [E][64][H]: A_gate hi, A_up hi, A_gate lo, A_up lo
         const size_t c = i % H, row = i / H;
-        const int e = int(row / 32), q = int(row % 32);
-        const float *src = q < 16 ? l.a_gate : l.a_up;
+        const int e = int(row / 64), q = int(row % 64);
+        const float *src = (q & 16) ? l.a_up : l.a_gate;
         const int qq = q & 15;
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] = qq < r ? src[((size_t)e * r + qq) * H + c + j] : 0.f;
-        dst = ax + i;
-    } else if ((i -= n_ax) < n_ah) {  // [E][16][I]
+        write_split(ax + i, v, q >= 32);
+        return;
+    } else if ((i -= n_ax) < n_ah) {  // [E][32][I]: A_down hi, A_down lo
         const size_t c = i % I, row = i / I;
-        const int e = int(row / 16), q = int(row % 16);
+        const int e = int(row / 32), q = int(row % 32);
+        const int qq = q & 15;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = q < r ? l.a_down[((size_t)e * r + q) * I + c + j] : 0.f;
-        dst = ah + i;
-    } else if ((i -= n_ah) < n_bgu) {  // [E*I][64]
-        const size_t row = i / 64;
-        const int c0 = int(i % 64);
+        for (int j = 0; j < 8; ++j) v[j] = qq < r ? l.a_down[((size_t)e * r + qq) * I + c + j] : 0.f;
+        write_split(ah + i, v, q >= 16);
+        return;
+    } else if ((i -= n_ah) < n_bgu) {  // [E*I][128]: gate slab, up slab
+        const size_t row = i / 128;
+        const int c0 = int(i % 128);
+        const float *b = c0 < 64 ? l.b_gate : l.b_up;
+        const int part = (c0 % 64) / 16;  // 0: hi, 1: hi, 2: lo, 3: zero
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int c = c0 + j;
-            v[j] = c < 16 ? (c < r ? l.b_gate[row * r + c] : 0.f)
-                 : c < 32 ? (c - 16 < r ? l.b_up[row * r + c - 16] : 0.f)
-                          : 0.f;
+            const int q = (c0 + j) % 16;
+            v[j] = part < 3 && q < r ? b[row * r + q] : 0.f;
         }
-        dst = bgu + i;
+        write_split(bgu + i, v, part == 2);
+        return;
     } else if ((i -= n_bgu) < n_bd) {  // [E*H][64]
         const size_t row = i / 64;
         const int c0 = int(i % 64);
+        const int part = c0 / 16;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = c0 + j < r ? l.b_down[row * r + c0 + j] : 0.f;
-        dst = bd + i;
-    } else {
-        return;
+        for (int j = 0; j < 8; ++j) {
+            const int q = (c0 + j) % 16;
+            v[j] = part < 3 && q < r ? l.b_down[row * r + q] : 0.f;
+        }
+        write_split(bd + i, v, part == 2);
     }
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        w[j] = uint32_t(f32_to_bf16_bits(v[2 * j])) | (uint32_t(f32_to_bf16_bits(v[2 * j + 1])) << 16);
-    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 }  // namespace
@@ -219,9 +236,9 @@ LoraPack lora_pack_layout(const moe_shape &s) {
     auto al = [](size_t b) { return (b + 255) / 256 * 256; };
     LoraPack L;
     L.ax = 0;
-    L.ah = L.ax + al((size_t)s.E * 32 * s.H * 2);
-    L.bgu = L.ah + al((size_t)s.E * 16 * s.I * 2);
-    L.bd = L.bgu + al((size_t)s.E * s.I * 64 * 2);
+    L.ah = L.ax + al((size_t)s.E * 64 * s.H * 2);
+    L.bgu = L.ah + al((size_t)s.E * 32 * s.I * 2);
+    L.bd = L.bgu + al((size_t)s.E * s.I * 128 * 2);
     L.total = L.bd + al((size_t)s.E * s.H * 64 * 2);
     return L;
 }
@@ -229,7 +246,7 @@ LoraPack lora_pack_layout(const moe_shape &s) {
 cudaError_t launch_lora_pack(const moe_shape &s, const moe_lora &l, void *dst, cudaStream_t st) {
     const LoraPack L = lora_pack_layout(s);
     char *b = static_cast<char *>(dst);
-    const size_t n_ax = (size_t)s.E * 32 * s.H, n_ah = (size_t)s.E * 16 * s.I, n_bgu = (size_t)s.E * s.I * 64,
+    const size_t n_ax = (size_t)s.E * 64 * s.H, n_ah = (size_t)s.E * 32 * s.I, n_bgu = (size_t)s.E * s.I * 128,
                  n_bd = (size_t)s.E * s.H * 64;
     const size_t groups = (n_ax + n_ah + n_bgu + n_bd) / 8;
     lora_pack_kernel<<<dim3((unsigned)((groups + 255) / 256)), dim3(256), 0, st>>>(

@@ -65,7 +65,7 @@ WsLayout ws_layout(const moe_shape &s) {
     L.hist = take((size_t)permute_chunks((int)A) * E * 4);
     L.h = take(A * s.I * 4);
     L.y = take(A * s.H * act_bytes(s));
-    L.xa = take(A * 32 * 4);
+    L.xa = take(A * 64 * 4);  // fp32 [A][32], or bf16 [A][128] with packed adapters
     L.ha = take(A * 32 * 4);  // fp32 [A][16], or bf16 [A][64] with packed adapters
     L.lpart = take(lora_part_floats(s) * 4);
     L.part = take(grouped_fast_part_bytes(select_grouped_path(s), s));

@@ -140,10 +140,12 @@ enum : int { kPhaseAll = 0, kPhaseGateUp = 1, kPhaseDown = 2, kPhaseLoraX = 3, k
 
 // Packed adapters of the bf16 tensor-core LoRA path (moe_lora_pack): bf16, zero-padded,
 // each region 256-byte aligned.
-//   ax  [E][32][H]  rows 0..15 A_gate, 16..31 A_up (rows past the rank zero)
-//   ah  [E][16][I]  A_down
-//   bgu [E*I][64]   columns 0..15 B_gate, 16..31 B_up, the rest zero
-//   bd  [E*H][64]   columns 0..15 B_down, the rest zero
+//   ax  [E][64][H]  rows 0..15 A_gate hi, 16..31 A_up hi, 32..47 A_gate lo, 48..63 A_up lo
+//                   (hi = bf16(A), lo = bf16(A - hi); rows past the rank zero)
+//   ah  [E][32][I]  A_down hi, A_down lo
+//   bgu [E*I][128]  a gate slab then an up slab of 64 columns: (B_hi, B_hi, B_lo, 0) in
+//                   16-column groups, B_hi = bf16(B), B_lo = bf16(B - B_hi)
+//   bd  [E*H][64]   one such slab of B_down
 struct LoraPack {
     size_t ax, ah, bgu, bd, total;  // byte offsets and size
 };
