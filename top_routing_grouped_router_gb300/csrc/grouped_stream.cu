@@ -3,7 +3,7 @@
 // mbarrier pipeline into tcgen05.mma, with fp32 accumulators in tensor memory.
 //
 // Orientation ("swap AB"): the weights are the MMA's M side (128 weight rows per
-// tile) and the expert's tokens the N side (up to 128 per tile, padded to 16), so a
+// tile) and the expert's tokens the N side (up to 256 per tile, padded to 16), so a
 // decode step with 1-64 tokens per expert still fills the 128-row MMA and its cost is
 // the weight stream alone.  Both operands are K-major, loaded by TMA as 64-element
 // (128-byte) slabs with the 128-byte swizzle.
@@ -16,14 +16,15 @@
 // stage's room after the weight slab, so a down stage carries as many MMA cycles as a
 // gate/up stage.  All gate/up tiles precede all down tiles in one list that CTAs
 // claim with an atomic counter; a down tile waits (bounded) until every epilogue warp
-// of every gate/up tile of its expert has published h.
+// of every gate/up tile of its expert has published h.  With packed LoRA adapters the
+// list also holds the A-side tiles (x . A^T first, h . A_down^T before the down tiles).
 //
-// Roles per CTA (one CTA per SM): warp 0 lane 0 issues TMA loads into a 4-6 stage ring;
+// Roles per CTA (one CTA per SM): warp 0 lane 0 issues TMA loads into a 3-6 stage ring;
 // warp 1 owns the TMEM allocation and issues the MMAs, converged, through one elected
 // lane (tcgen05.commit frees a stage when its MMAs are done, and hands a finished
 // accumulator to the epilogue); warps 2-17 are the epilogue (warp w reads TMEM lanes
 // 32*(w%4)..+31, the four warps of a lane quadrant alternating over 32-column groups),
-// with two accumulator buffers so the epilogue of one tile overlaps the MMAs of the next.
+// with TMEM in two halves so the epilogue of one tile overlaps the MMAs of the next.
 //
 // The token rows are first gathered into permuted order (x_perm) so that every
 // expert's rows are contiguous for TMA; the same prep kernel builds the tile list.
@@ -47,7 +48,7 @@ constexpr int kNBox = 16;                  // token rows per activation TMA box 
 constexpr int kMidBox = 64;                // token rows per box for tiles of 33-64 tokens
 constexpr int kBigBox = 128;               // token rows per box for larger tiles
 constexpr int kABytes = kRows * 128;       // 16 KB per weight slab
-constexpr int kTmemCols = 512;             // two accumulator buffers of 256 columns
+constexpr int kTmemCols = 512;             // two halves of 256 columns
 // LoRA modes of the kernel: none; B side in the epilogue on CUDA cores (fp32 adapters as
 // given); or packed bf16 adapters on the tensor cores (A-side tiles of their own, and the
 // B side as one more MMA stage of each gate/up and down tile).
@@ -77,7 +78,6 @@ enum : int { kGateUp = 0, kDown = 1, kRouter = 2, kLoraX = 3, kLoraH = 4 };
 static_assert(kGateUp == kRecGateUp && kDown == kRecDown && kLoraX == kRecLoraX && kLoraH == kRecLoraH, "kinds");
 
 struct Params {
-    const int32_t *offsets;     // [E+1]
     const uint4 *tiles;         // tile records (grouped_tiles.cuh)
     int *sched;                 // scheduling words (grouped_tiles.cuh)
     int phase;                  // kPhaseAll / kPhaseGateUp / kPhaseDown
@@ -92,7 +92,6 @@ struct Params {
     uint16_t *h;                // [A][I] bf16
     uint16_t *y;                // [A][H] bf16
     int E, H, I, A;
-    int cmax;                   // token chunk of the gate/up tiles (fixed chunks)
     int dmax;                   // token chunk bound of the down tiles (even chunks)
     // router mode: tiles are (row block of experts, 128-token chunk), one static sweep
     int router_tiles;           // > 0 selects router mode
@@ -777,7 +776,6 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     if (e != cudaSuccess) return e;
 
     Params prm{};
-    prm.offsets = offsets;
     prm.tiles = tiles;
     prm.sched = sched;
     prm.phase = kPhaseAll;
@@ -789,7 +787,6 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.H = s.H;
     prm.I = s.I;
     prm.A = A;
-    prm.cmax = cmax;
     prm.dmax = dmax;
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());

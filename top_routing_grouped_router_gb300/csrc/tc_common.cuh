@@ -126,25 +126,13 @@ __device__ __forceinline__ uint32_t instr_desc(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// Warp-converged forms: the whole warp executes them (all 32 lanes, converged) and one
-// elected lane issues.  The election is deterministic, so every MMA and commit of the
-// warp comes from the same lane, as tcgen05.commit requires (it tracks the operations of
-// its own thread).  Keeping the issuing loop converged lets the operands stay warp-uniform,
-// which costs the issue stream markedly fewer cycles per MMA than a lone lane does.
+// MMA (kind::f16: bf16 operands from shared memory, fp32 accumulator in TMEM; acc = 0
+// overwrites) and commit, in warp-converged form: the whole warp executes them (all 32
+// lanes, converged) and one elected lane issues.  The election is deterministic, so every
+// MMA and commit of the warp comes from the same lane, as tcgen05.commit requires (it
+// tracks the operations of its own thread).  Keeping the issuing loop converged lets the
+// operands stay warp-uniform, which costs the issue stream markedly fewer cycles per MMA
+// than a lone lane does.
 __device__ __forceinline__ void mma_bf16_warp(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p, e;\n\t"
