@@ -137,3 +137,48 @@ def test_lora_packed_large_batch_bf16_rank8():
 
 def test_lora_large_batch_q4_rank16():
     _check(synth.make_custom(200, 256, 16, 4, 128, w="q4", seed=43, name="lora200q"), 16, 16)
+
+
+def test_pack_layout_is_the_documented_hi_lo_split():
+    # the pack's bytes against the layout moe.h documents, built here from the fp32 adapters:
+    # hi = bf16(v), lo = bf16(v - hi) (nearest even), rows / columns past the rank zero
+    E, H, I, r = 4, 128, 128, 5
+    shape = moe.make_shape(8, H, E, 2, I)
+    lora = synth.make_lora(E, H, I, rank=r, seed=3)
+    s, keep = _dev_lora(lora, shape)
+    got = s.pack_tensor.cpu().numpy().view(np.uint16)
+
+    def split(v):
+        v = np.asarray(v, dtype=np.float32)
+        hi = synth.bf16_bits(v)
+        lo = synth.bf16_bits(v - synth.bf16_bits_to_f32(hi))
+        return hi, lo
+
+    al = lambda b: (b + 255) // 256 * 256
+    off_ah = al(E * 64 * H * 2) // 2
+    off_bgu = off_ah + al(E * 32 * I * 2) // 2
+    off_bd = off_bgu + al(E * I * 128 * 2) // 2
+    ax = np.zeros((E, 64, H), np.uint16)
+    ah = np.zeros((E, 32, I), np.uint16)
+    bgu = np.zeros((E * I, 128), np.uint16)
+    bd = np.zeros((E * H, 64), np.uint16)
+    for name, base in (("a_gate", 0), ("a_up", 16)):
+        hi, lo = split(lora[name])  # [E][r][H]
+        ax[:, base:base + r] = hi
+        ax[:, 32 + base:32 + base + r] = lo
+    hi, lo = split(lora["a_down"])
+    ah[:, :r] = hi
+    ah[:, 16:16 + r] = lo
+    for name, col in (("b_gate", 0), ("b_up", 64)):
+        hi, lo = split(lora[name].reshape(E * I, r))
+        bgu[:, col:col + r] = hi
+        bgu[:, col + 16:col + 16 + r] = hi
+        bgu[:, col + 32:col + 32 + r] = lo
+    hi, lo = split(lora["b_down"].reshape(E * H, r))
+    bd[:, :r] = hi
+    bd[:, 16:16 + r] = hi
+    bd[:, 32:32 + r] = lo
+    np.testing.assert_array_equal(got[:E * 64 * H].reshape(ax.shape), ax)
+    np.testing.assert_array_equal(got[off_ah:off_ah + E * 32 * I].reshape(ah.shape), ah)
+    np.testing.assert_array_equal(got[off_bgu:off_bgu + E * I * 128].reshape(bgu.shape), bgu)
+    np.testing.assert_array_equal(got[off_bd:off_bd + E * H * 64].reshape(bd.shape), bd)
