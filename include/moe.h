@@ -8,9 +8,10 @@
  * backend) names for the MoE block: expert histogram (bincount, replaced by a
  * capture-safe scatter_add_), cumsum, argsort, torch._grouped_mm, index_add_.
  * Here each op is a hand-written CUDA kernel; the whole block runs without a
- * host synchronisation, so every call below can be captured in a CUDA graph
- * (the capture failure that page describes came from a host round trip inside
- * bincount).
+ * host synchronisation, so moe_route, moe_permute, moe_grouped_swiglu,
+ * moe_unpermute and the moe_forward* calls that take a caller workspace can be
+ * captured in a CUDA graph (the capture failure that page describes came from
+ * a host round trip inside bincount).
  *
  * Notation: T tokens, H hidden size, E experts, k experts per token, I expert
  * intermediate size, A = T*k assignments.  Assignment a = t*k + j is token t's
@@ -143,7 +144,11 @@ typedef struct {
 MOE_API int moe_workspace_size(const moe_shape *shape, size_t *bytes);
 
 /*
- * Router GEMM, softmax, top-k and renormalisation (steps A-B).
+ * Router GEMM, softmax, top-k and renormalisation (steps A-B).  Defined by
+ * the Qwen3-MoE gate whose "router pointwise ops" the unsloth commit page
+ * a1bc5cbd73 (compile_walker paragraph) fuses; the tie rule below answers the
+ * "tie-break logit boundary" that page 80aaf1121b (flex_moe_parity paragraph)
+ * names as its only divergence.
  *   x           [T][H]   act dtype
  *   w_router    [E][H]   act dtype
  *   b_router    [E] fp32 or NULL (added to the logits before softmax/top-k)
@@ -161,7 +166,10 @@ MOE_API int moe_route(const moe_shape *shape, const void *x, const void *w_route
               void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
- * Expert histogram, exclusive scan and stable permutation (steps C-D).
+ * Expert histogram, exclusive scan and stable permutation (steps C-D): the
+ * bincount (capture-safe scatter_add_) + cumsum + argsort of the grouped_mm
+ * path on the unsloth commit page 80aaf1121b (grouped_mm paragraph and the
+ * closing paragraph on the capture-safe histogram).
  *   expert_ids [A] int32 in
  *   counts     [E] int32 out: assignments per expert
  *   offsets    [E+1] int32 out: offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]
@@ -174,7 +182,10 @@ MOE_API int moe_permute(const moe_shape *shape, const int32_t *expert_ids, int32
                 int32_t *order, int32_t *pos, void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
- * Grouped SwiGLU experts (steps E-F) over the permuted rows.  For permuted row
+ * Grouped SwiGLU experts (steps E-F) over the permuted rows: the
+ * torch._grouped_mm step of the grouped_mm path on the unsloth commit page
+ * 80aaf1121b (grouped_mm paragraph), with the Qwen3-MoE SwiGLU expert MLP.
+ * For permuted row
  * p of expert e (offsets[e] <= p < offsets[e+1]) and source token
  * t = order[p] / k:
  *   h = SiLU(x[t] . W_gate[e]^T) * (x[t] . W_up[e]^T),  SiLU(z) = z / (1 + e^-z)
@@ -192,7 +203,9 @@ MOE_API int moe_grouped_swiglu(const moe_shape *shape, const void *x, const int3
                        void *y, void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
- * Weighted un-permute (step G): out[t] = sum_{j<k} weights[t][j] * y[pos[t*k+j]],
+ * Weighted un-permute (step G), the index_add_ step of the grouped_mm path on
+ * the unsloth commit page 80aaf1121b (grouped_mm paragraph), done as a gather:
+ * out[t] = sum_{j<k} weights[t][j] * y[pos[t*k+j]],
  * summed in j order in fp32 and rounded once to the act dtype.  No atomics;
  * bitwise deterministic.
  *   y [A][H] (dtype as produced by moe_grouped_swiglu), weights [T][k] fp32,
@@ -202,7 +215,9 @@ MOE_API int moe_unpermute(const moe_shape *shape, const void *y, const float *we
                   void *out, moe_stream_t stream);
 
 /*
- * The whole block (steps A-G) in one call, intermediates in the workspace.
+ * The whole block (steps A-G) in one call, intermediates in the workspace: the
+ * sparse MoE block that the unsloth commit page 80aaf1121b captures per batch
+ * bucket (capture_decode_cudagraph and grouped_mm paragraphs).
  *   out            [T][H] act dtype
  *   expert_ids_out [T][k] int32 or NULL, weights_out [T][k] fp32 or NULL:
  *                  optional copies of the routing decision.
@@ -287,22 +302,35 @@ MOE_API int moe_lora_pack(const moe_shape *shape, const moe_lora *lora, void *pa
  * Same arguments and results as moe_forward, minus the workspace.  The scratch
  * is one fixed MOE_STATIC_SCRATCH_BYTES (32 MiB) array in the library's device
  * image; every GPU that loads the library holds it until the process exits.
- *   - Allocates nothing and calls no allocating routine.
+ *   - Calls no allocating routine.  The array's module is loaded lazily: the
+ *     first call on each device looks up the array's device address (with that
+ *     device current), and that lookup is when the driver reserves the 32 MiB
+ *     on the device and may synchronise.  Make that first call before any
+ *     stream capture.
  *   - Shapes whose moe_workspace_size() exceeds 32 MiB are rejected with
  *     MOE_ERR_WORKSPACE before anything is enqueued (the decode shapes fit:
- *     the Qwen3-30B-A3B layer up to a few hundred tokens).
- *   - The first call on each device looks up the array's device address
- *     (with that device current); make that first call outside any stream
- *     capture.
+ *     the Qwen3-30B-A3B layer up to a few hundred tokens).  Every other argument
+ *     error is also returned before anything is enqueued.
  *   - Every call shares the one array and leaves its contents behind; each call
- *     clears the array's 2 KB header (error word and counters) itself.  Calls whose executions overlap on the GPU
- *     (different streams, or graphs replayed concurrently) race on the array:
- *     serialise them.
+ *     clears the array's scheduling counters itself.  Calls whose executions
+ *     overlap on the GPU (different streams, or concurrent replays) race on the
+ *     array: serialise them.
+ *   - A device-detected error (MOE_ERR_DEVICE) is recorded in the array's error
+ *     word and stays there, across later calls, until
+ *     moe_static_scratch_read_error reads and clears it.
  */
 MOE_API int moe_forward_static_scratch(const moe_shape *shape, const void *x, const void *w_router,
                                        const float *b_router, const void *w_gate, const void *w_up,
                                        const void *w_down, const moe_q4 *q4, void *out,
                                        int32_t *expert_ids_out, float *weights_out, moe_stream_t stream);
+
+/*
+ * moe_read_device_error for the static scratch array of the current device:
+ * reads and clears its error word after the work enqueued on `stream`.
+ * Synchronises `stream`.  *code receives MOE_OK or MOE_ERR_DEVICE.  Returns
+ * MOE_ERR_NULLPTR for a NULL code, MOE_ERR_LAUNCH if the copy failed.
+ */
+MOE_API int moe_static_scratch_read_error(int32_t *code, moe_stream_t stream);
 
 /*
  * Number of kernel launches one moe_forward call with this shape enqueues

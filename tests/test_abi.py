@@ -145,3 +145,18 @@ def test_lora_pack_rejects_bad_arguments_without_a_gpu_call(L):
     assert L.moe_lora_pack(ctypes.byref(shape), ctypes.byref(lo), fake, need - 1, st) == -4
     bad = moe.MoELora(17, 2.0, fake, fake, fake, fake, fake, fake, None)
     assert L.moe_lora_pack(ctypes.byref(shape), ctypes.byref(bad), fake, need, st) == -2
+
+
+def test_static_scratch_rejects_misaligned_q4_scales_before_any_cuda_call(L):
+    # every check of moe_forward_static_scratch runs before its first CUDA call, so on a
+    # host without a GPU a misaligned 4-bit scale pointer must come back as MOE_ERR_ALIGN
+    s = moe.make_shape(8, 256, 8, 2, 128, "bf16", "q4")
+    fake = 1 << 20  # never dereferenced
+    q4 = moe.MoEQ4(fake, fake + 8, fake, (ctypes.c_float * 16)(*[-1 + 2 * j / 15 for j in range(16)]))
+    rc = L.moe_forward_static_scratch(ctypes.byref(s), fake, fake, None, fake, fake, fake, ctypes.byref(q4), fake,
+                                      None, None, None)
+    assert rc == -5  # MOE_ERR_ALIGN
+    q4.up_scales = None
+    rc = L.moe_forward_static_scratch(ctypes.byref(s), fake, fake, None, fake, fake, fake, ctypes.byref(q4), fake,
+                                      None, None, None)
+    assert rc == -1  # MOE_ERR_NULLPTR

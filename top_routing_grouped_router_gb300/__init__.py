@@ -19,7 +19,7 @@ __all__ = [
     "make_shape", "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string", "EXPORTED_SYMBOLS",
     "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_forward_lora", "moe_graph_buckets", "moe_graphs_arena_size",
-    "DecodeGraphs", "moe_lora_pack_size", "moe_lora_pack", "pack_lora",
+    "DecodeGraphs", "moe_lora_pack_size", "moe_lora_pack", "pack_lora", "moe_static_scratch_read_error",
 ]
 
 MOE_DT_F32, MOE_DT_BF16, MOE_DT_Q4 = 0, 1, 2
@@ -31,7 +31,8 @@ library_path = os.path.join(_HERE, "libmoe_gb300.so")
 EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_swiglu", "moe_unpermute",
                     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string",
                     "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_forward_lora", "moe_graph_buckets", "moe_graphs_arena_size", "moe_graphs_create",
-                    "moe_graphs_bucket", "moe_graphs_run", "moe_graphs_destroy", "moe_lora_pack_size", "moe_lora_pack")
+                    "moe_graphs_bucket", "moe_graphs_run", "moe_graphs_destroy", "moe_lora_pack_size", "moe_lora_pack",
+                    "moe_static_scratch_read_error")
 
 
 class MoEError(RuntimeError):
@@ -81,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "moe_read_device_error": [vp, ctypes.POINTER(ctypes.c_int32), vp],
             "moe_forward_launches": [sp, ctypes.POINTER(ctypes.c_int32)],
             "moe_forward_static_scratch": [sp, vp, vp, vp, vp, vp, vp, q4p, vp, i32p, vp, vp],
+            "moe_static_scratch_read_error": [ctypes.POINTER(ctypes.c_int32), vp],
             "moe_forward_rmsnorm": [sp, vp, vp, ctypes.c_float, ctypes.c_int, vp, vp, vp, vp, vp, q4p, vp, vp, i32p,
                                     vp, vp, sz, vp],
             "moe_forward_lora": [sp, vp, vp, vp, vp, vp, vp, q4p, ctypes.POINTER(MoELora), vp, i32p, vp, vp, sz, vp],
@@ -185,6 +187,14 @@ def moe_forward_static_scratch(shape, x, w_router, b_router, w_gate, w_up, w_dow
                                             ctypes.byref(q4) if q4 is not None else None, _ptr(out),
                                             _ptr(expert_ids_out), _ptr(weights_out), _stream(stream)),
            "moe_forward_static_scratch")
+
+
+def moe_static_scratch_read_error(stream=None) -> int:
+    """Reads and clears the device error word of the static scratch array (synchronises the stream)."""
+    code = ctypes.c_int32(0)
+    _check(lib().moe_static_scratch_read_error(ctypes.byref(code), _stream(stream)),
+           "moe_static_scratch_read_error")
+    return code.value
 
 
 def moe_forward_rmsnorm(shape, hs, gamma, eps, w_router, b_router, w_gate, w_up, w_down, q4, out, add_residual=True,

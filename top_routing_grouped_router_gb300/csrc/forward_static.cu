@@ -7,8 +7,10 @@
 // cudaMalloc's implicit device synchronisation.  This entry point runs the same
 // kernels as moe_forward, with the scratch in a fixed array that lives in the
 // library's device image: every GPU that loads the library holds these
-// MOE_STATIC_SCRATCH_BYTES until the process exits.  It allocates nothing and
-// calls no allocating routine.
+// MOE_STATIC_SCRATCH_BYTES until the process exits.  It calls no allocating
+// routine.  The array's module is loaded lazily: the driver reserves the 32 MiB on
+// a device the first time the array's address is looked up there, which is the
+// one moment this entry point can allocate and synchronise implicitly.
 #include "moe_internal.cuh"
 
 #include <mutex>
@@ -58,13 +60,27 @@ extern "C" int moe_forward_static_scratch(const moe_shape *shape, const void *x,
     if (misaligned(x) || misaligned(w_router) || misaligned(out) || misaligned(w_gate) || misaligned(w_up) ||
         misaligned(w_down))
         return MOE_ERR_ALIGN;
+    if (shape->w_dtype == MOE_DT_Q4 &&
+        (misaligned(q4->gate_scales) || misaligned(q4->up_scales) || misaligned(q4->down_scales)))
+        return MOE_ERR_ALIGN;
     void *scratch = nullptr;
     const int ra = scratch_address(&scratch);
     if (ra != MOE_OK) return ra;
-    // the array keeps the previous call's contents: the header (error word and scheduling
-    // counters) must start at zero
-    if (cudaMemsetAsync(scratch, 0, moe::kHdrBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // the array keeps the previous call's contents: the scheduling counters of the header
+    // must start at zero.  The error word (its first 4 bytes) is left alone, so that a
+    // device error stays recorded until moe_static_scratch_read_error reads and clears it.
+    if (cudaMemsetAsync(static_cast<char *>(scratch) + 4, 0, moe::kHdrBytes - 4,
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MOE_ERR_LAUNCH;
     return moe_forward(shape, x, w_router, b_router, w_gate, w_up, w_down, q4, out, expert_ids_out, weights_out,
                        scratch, kStaticScratchBytes, stream);
+}
+
+extern "C" int moe_static_scratch_read_error(int32_t *code, moe_stream_t stream) {
+    if (!code) return MOE_ERR_NULLPTR;
+    void *scratch = nullptr;
+    const int ra = scratch_address(&scratch);
+    if (ra != MOE_OK) return ra;
+    // the error word sits at the start of the array's header, as in a caller workspace
+    return moe_read_device_error(scratch, code, stream);
 }

@@ -53,7 +53,6 @@ constexpr int kBufCols = 256;
 constexpr int kUpCol = 128;
 constexpr int kEpiWarps = 4;
 constexpr int kDeqWarps = 8;
-constexpr int kDeqThreads = kDeqWarps * 32;
 constexpr int kThreads = (2 + kEpiWarps + kDeqWarps) * 32;
 constexpr int kMetaRing = 8;
 constexpr int kScaleBytes = 2 * 8192;          // one tile's block scales: 2 matrices x 128 rows x <= 32 blocks

@@ -75,7 +75,9 @@ constexpr int kRouterN = 64;               // tokens per router tile: twice the 
 // 128-expert x 64-token tile per CTA.  LoRA A-side tiles (packed adapters) take 128 token
 // rows as the MMA's M side and the expert's 32 (x) or 16 (h) adapter rows as N.
 enum : int { kGateUp = 0, kDown = 1, kRouter = 2, kLoraX = 3, kLoraH = 4 };
-static_assert(kGateUp == kRecGateUp && kDown == kRecDown && kLoraX == kRecLoraX && kLoraH == kRecLoraH, "kinds");
+static_assert(int(kGateUp) == int(kRecGateUp) && int(kDown) == int(kRecDown) && int(kLoraX) == int(kRecLoraX) &&
+                  int(kLoraH) == int(kRecLoraH),
+              "kinds");
 
 struct Params {
     const uint4 *tiles;         // tile records (grouped_tiles.cuh)

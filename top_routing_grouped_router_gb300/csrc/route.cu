@@ -31,7 +31,6 @@ constexpr int kEPB = 4;      // experts per block
 constexpr int kTG = 8;       // tokens per accumulation group
 constexpr int kTPB = 8;      // tokens per block
 constexpr int kFuseMaxT = 64;
-constexpr int kMaxGroups = kFuseMaxT / kTPB;
 
 template <typename T> struct Vec;
 template <> struct Vec<float> {
