@@ -7,17 +7,22 @@ experts, weighted un-permute) over one batch of seeded synthetic tokens, as one
 ``moe_forward`` call captured in a CUDA graph.  Weights are random-init with the
 model's shapes (no checkpoint); inputs are resident in HBM when timing starts.
 
+The headline line is the decode workload (T=8, bf16).  In the same process, at one
+GPU, every other workload (Zipf decode, 4-bit decode, the 4-layer prefill stack and
+4-bit prefill) is measured the same way and reported under ``configs``, each with its
+own roofline, clock record and per-op breakdown.
+
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle (plain C
-loops in double) on the same workload instead.
+loops in double, on every host core) on the same workload instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode8|...] [--impl ours|reference]
 """
 from __future__ import annotations
 
 import argparse
+import concurrent.futures as cf
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -30,7 +35,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/sec at Qwen3-30B-A3B shape; achieved HBM GB/s vs roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-L2_BYTES = 129 * 1024 * 1024
+FALLBACK_L2_BYTES = 129 * 1024 * 1024
 
 DESCR = {
     "tiny": "tiny MoE block fp32: T=16 H=64 E=8 k=2 I=32",
@@ -40,17 +45,20 @@ DESCR = {
     "prefill": "Qwen3-30B-A3B MoE layer prefill, bf16: 4 independent layers x T=4096 H=2048 E=128 k=8 I=768",
     "prefill4q": "Qwen3-30B-A3B MoE layer prefill, 4-bit codebook expert weights: T=4096 H=2048 E=128 k=8 I=768",
 }
+EXTRA_WORKLOADS = ("decode64z", "decode48q", "prefill", "prefill4q")
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode8", choices=sorted(DESCR))
+    ap.add_argument("--extras", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated workloads also measured at one GPU ('none' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--copies", type=int, default=0, help="weight copies to rotate (0 = automatic)")
     ap.add_argument("--layers", type=int, default=0, help="use only the first N layers (profiling; 0 = all)")
     ap.add_argument("--lora-unpacked", action="store_true",
@@ -159,92 +167,130 @@ def expert_bytes_per_expert(inp):
     return 3 * inp.I * inp.H * (4 if inp.w == "f32" else 2)
 
 
-def cpu_baseline(layers, seconds: float):
-    """The oracle as it stands (single-threaded C, double) on a bounded sample of the workload."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_throughput(inp, seconds: float, threads: int):
+    """Tokens/s of the oracle as it stands on `threads` host threads: every thread evaluates
+    single tokens of the batch (token i, i + threads, ... cycling) through
+    oracle.forward_tokens until the time is up.  The oracle's C call releases the GIL, so
+    the threads run on separate cores.  Returns (tokens/s, tokens done, seconds)."""
     import numpy as np
     import oracle
     oracle.build()
-    inp = layers[0]
-    # one step of the sample: the whole batch if it is small, else a slice of tokens
-    toks = np.arange(inp.T, dtype=np.int32)
+    deadline = time.perf_counter() + seconds
+    T = inp.T
+
+    def worker(i):
+        done, j = 0, i
+        while True:
+            oracle.forward_tokens(inp, np.array([j % T], dtype=np.int32))
+            done += 1
+            j += threads
+            if time.perf_counter() >= deadline:
+                return done
+
     t0 = time.perf_counter()
-    oracle.forward_tokens(inp, toks[:1])
-    per_tok = max(time.perf_counter() - t0, 1e-4)
-    n = int(max(1, min(inp.T, seconds / per_tok)))
-    reps, done, t0 = 0, 0, time.perf_counter()
-    while True:
-        oracle.forward_tokens(inp, toks[:n])
-        reps += 1
-        done += n
-        if time.perf_counter() - t0 >= seconds:
-            break
+    with cf.ThreadPoolExecutor(threads) as pool:
+        n = sum(pool.map(worker, range(threads)))
     dt = time.perf_counter() - t0
-    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"oracle.forward_tokens on {n} of the {inp.T} tokens of layer 0, {reps} repetition(s), "
-                      f"{dt:.1f} s single-threaded"}
+    return n / dt, n, dt
+
+
+def cpu_baseline(layers, seconds: float):
+    """The oracle as it stands (plain C, double) on a bounded sample of the workload: single
+    tokens of layer 0, on every host core, plus a single-thread figure."""
+    inp = layers[0]
+    cores = host_cores()
+    v1, n1, d1 = oracle_throughput(inp, seconds / 4, 1)
+    vn, nn, dn = oracle_throughput(inp, seconds, cores)
+    return {"value": vn, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"oracle.forward_tokens on single tokens of layer 0 ({inp.T}-token batch, cycled), "
+                      f"{nn} tokens in {dn:.1f} s on {cores} threads",
+            "single_thread": {"value": v1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"{n1} tokens in {d1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    layers = layer_inputs(args.workload)
     import numpy as np
     import oracle
+    layers = layer_inputs(args.workload)
     oracle.build()
     inp = layers[0]
-    toks = np.arange(inp.T, dtype=np.int32)
+    cores = host_cores()
     t0 = time.perf_counter()
-    oracle.forward_tokens(inp, toks[:1])
+    oracle.forward_tokens(inp, np.array([0], dtype=np.int32))
     per_tok = max(time.perf_counter() - t0, 1e-4)
+    # each step: n single-token evaluations spread over the host cores, bounded so that the
+    # whole run stays within about two minutes
     budget = 120.0 / max(1, args.steps + args.warmup)
-    n = int(max(1, min(inp.T, budget / per_tok)))
-    for _ in range(args.warmup):
-        oracle.forward_tokens(inp, toks[:n])
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.forward_tokens(inp, toks[:n])
-    dt = time.perf_counter() - t0
+    n = int(max(1, min(inp.T * 8, budget * cores / per_tok)))
+    toks = [np.array([i % inp.T], dtype=np.int32) for i in range(n)]
+
+    def step(pool):
+        list(pool.map(lambda t: oracle.forward_tokens(inp, t), toks))
+
+    with cf.ThreadPoolExecutor(cores) as pool:
+        for _ in range(args.warmup):
+            step(pool)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step(pool)
+        dt = time.perf_counter() - t0
     value = args.steps * n / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": DESCR[args.workload], "tokens_per_step": n},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n} of {inp.T} tokens per step through oracle.forward_tokens (C, double, "
-                                   f"single-threaded)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} single-token evaluations per step (tokens of the {inp.T}-token batch, "
+                                   f"cycled) through oracle.forward_tokens (C, double) on {cores} threads"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def run_ours(args, rank, world, local):
-    import numpy as np
-    import torch
-    import top_routing_grouped_router_gb300 as moe
-    from top_routing_grouped_router_gb300 import build as moe_build
-    from top_routing_grouped_router_gb300.device import upload, to_device
+class Ctx:
+    """What every measurement shares: device, stream, peaks, the library."""
+
+    def __init__(self, args, world, local):
+        import torch
+        import top_routing_grouped_router_gb300 as moe
+        from top_routing_grouped_router_gb300 import build as moe_build
+        self.torch, self.moe = torch, moe
+        self.args, self.world, self.local = args, world, local
+        self.dev = torch.device("cuda", local)
+        moe_build.build()
+        self.peaks, self.peak_kind = load_peaks()
+        props = torch.cuda.get_device_properties(self.dev)
+        self.l2_bytes = int(getattr(props, "L2_cache_size", 0) or FALLBACK_L2_BYTES)
+        self.l2_source = "device property" if getattr(props, "L2_cache_size", 0) else "fallback"
+        self.stream = torch.cuda.Stream(device=self.dev)
+
+
+def measure(ctx: Ctx, workload: str, steps: int, warmup: int, *, headline: bool):
+    """One workload: graph-replayed steps (timed), then each entry point timed alone, the
+    roofline of the grouped expert op, and (headline only) the end-to-end C-ABI run."""
+    torch, moe, args, dev, stream = ctx.torch, ctx.moe, ctx.args, ctx.dev, ctx.stream
     import synth
+    from top_routing_grouped_router_gb300.device import upload, to_device
 
-    if not torch.cuda.is_available():
-        raise RuntimeError("bench.py needs a CUDA GPU")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    moe_build.build()
-    peaks, peak_kind = load_peaks()
-
-    layers = layer_inputs(args.workload)
-    if args.layers > 0:
+    layers = layer_inputs(workload)
+    if headline and args.layers > 0:
         layers = layers[:args.layers]
     inp0 = layers[0]
     T, H, E, k, I = inp0.T, inp0.H, inp0.E, inp0.k, inp0.I
     # enough weight copies that a replay never finds the previous replay's weights in L2
     per_copy = sum(expert_bytes_per_expert(l) * E for l in layers)
-    n_copies = args.copies if args.copies > 0 else (1 if per_copy > 32 * L2_BYTES else 3)
+    n_copies = args.copies if (headline and args.copies > 0) else (1 if per_copy > 32 * ctx.l2_bytes else 3)
     dl = [[upload(l, dev) for l in layers] for _ in range(n_copies)]
     for c in range(1, n_copies):  # copies share x / router / bias with copy 0 (the same tokens each step)
         for l in range(len(layers)):
@@ -252,11 +298,11 @@ def run_ours(args, rank, world, local):
     out_dt = dl[0][0].out_dtype()
     outs = [torch.empty((T, H), dtype=out_dt, device=dev) for _ in layers]
     wss = [d.new_workspace() for d in dl[0]]
-    stream = torch.cuda.Stream(device=dev)
+    entry = args.entry if headline else "forward"
 
     gammas = [to_device(synth.make_norm_weight(l.H, l.act, seed=l.T, layer=i), dev) for i, l in enumerate(layers)]
     loras, lora_keep = [], []
-    if args.entry == "lora":
+    if entry == "lora":
         names = ("a_gate", "b_gate", "a_up", "b_up", "a_down", "b_down")
         for i, l in enumerate(layers):
             ad = synth.make_lora(l.E, l.H, l.I, rank=16, seed=l.T, layer=i)
@@ -271,10 +317,10 @@ def run_ours(args, rank, world, local):
 
     def forward(c, st=None):
         for l, L in enumerate(dl[c]):
-            if args.entry == "lora":
+            if entry == "lora":
                 moe.moe_forward_lora(L.shape, L.x, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4,
                                      loras[l], outs[l], workspace=wss[l], stream=st)
-            elif args.entry == "rmsnorm":
+            elif entry == "rmsnorm":
                 moe.moe_forward_rmsnorm(L.shape, L.x, gammas[l], 1e-6, L.w_router, L.b_router, L.w_gate, L.w_up,
                                         L.w_down, L.q4, outs[l], workspace=wss[l], stream=st)
             else:
@@ -305,12 +351,13 @@ def run_ours(args, rank, world, local):
     grouped_bytes = sum(na * expert_bytes_per_expert(l) + T * H * act_b + T * k * H * act_b
                         for na, l in zip(n_active, layers))
     step_bytes = grouped_bytes + sum(E * H * act_b + T * H * act_b for _ in layers)
-    flops = sum(2 * T * H * E + 2 * T * k * 3 * I * H for _ in layers)
+    expert_flops = sum(2 * T * k * 3 * I * H for _ in layers)
+    flops = expert_flops + sum(2 * T * H * E for _ in layers)
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(ctx.local)
     clocks.start()
     with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
+        for i in range(max(3, warmup)):
             graphs[i % n_copies].replay()
         # bring the GPU under load before the timed region so the clock samples mean something
         t_end = time.perf_counter() + 0.5
@@ -318,26 +365,26 @@ def run_ours(args, rank, world, local):
             for g in graphs:
                 g.replay()
             stream.synchronize()
-    if world > 1:
+    if ctx.world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             graphs[i % n_copies].replay()
         ev1.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
+    if ctx.world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-    ms_step = ms_total / args.steps
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), ctx.world, dev)
+    ms_step = ms_total / steps
     tokens_per_step = T * len(layers)
-    value = job_throughput(world, tokens_per_step, args.steps, ms_total)
+    value = job_throughput(ctx.world, tokens_per_step, steps, ms_total)
 
-    # the dominant kernel (grouped SwiGLU experts) timed alone with events on its stream
-    kt_steps = min(args.steps, 200)
+    # each entry point timed alone with events on its stream, eager launches back to back
+    kt_steps = max(20, min(steps, 200))
     ids_b = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in layers]
     w_b = [torch.empty((T, k), dtype=torch.float32, device=dev) for _ in layers]
     cnt_b = [torch.empty(E, dtype=torch.int32, device=dev) for _ in layers]
@@ -345,7 +392,6 @@ def run_ours(args, rank, world, local):
     ord_b = [torch.empty(T * k, dtype=torch.int32, device=dev) for _ in layers]
     pos_b = [torch.empty(T * k, dtype=torch.int32, device=dev) for _ in layers]
     y_b = [torch.empty((T * k, H), dtype=out_dt, device=dev) for _ in layers]
-    # per entry point: events around each op of the step, ops launched eagerly back to back
     ops = ("route", "permute", "grouped_swiglu", "unpermute")
     kev = {o: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(kt_steps)] for o in ops}
@@ -375,68 +421,157 @@ def run_ours(args, rank, world, local):
     breakdown = {o: statistics.mean(a.elapsed_time(b) for a, b in kev[o]) * 1e3 for o in ops}
     k_ms = breakdown["grouped_swiglu"] / 1e3
 
-    # end to end through the public API: pinned host tokens in, host result out, every step
-    x_host = [to_device(l.x, "cpu", pin=True) for l in layers]
-    out_host = [torch.empty((T, H), dtype=out_dt, pin_memory=True) for _ in layers]
-    e2e_steps = min(args.steps, 500)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(e2e_steps):
-            for l in range(len(layers)):
-                dl[0][l].x.copy_(x_host[l], non_blocking=True)
-            graphs[i % n_copies].replay()
-            for l in range(len(layers)):
-                out_host[l].copy_(outs[l], non_blocking=True)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    bi = sum(x.numel() * x.element_size() for x in x_host)
-    bo = sum(o.numel() * o.element_size() for o in out_host)
-
-    launches = sum(moe.moe_forward_launches(L.shape) for L in dl[0])
-    tensor_bound = args.workload.startswith("prefill")
+    peaks = ctx.peaks
+    tensor_bound = workload.startswith("prefill")
+    peak_src = "measured (MEASURED_PEAKS.json)" if ctx.peak_kind == "measured" else "fallback"
     if tensor_bound:
-        peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-        achieved = flops / (k_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
+        # the grouped op is timed on its own (eager launches of a few hundred microseconds):
+        # the burst bf16 peak applies, and only the expert flops count (the op does no router GEMM)
+        peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        achieved = expert_flops / (k_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src}, bf16 burst", "algorithmic_flops": expert_flops}
     else:
         peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         achieved = grouped_bytes / (k_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
-    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": peak_src}
     roof["kernel"] = "moe_grouped_swiglu (grouped SwiGLU expert kernels)"
     roof["kernel_ms"] = k_ms
     roof["algorithmic_bytes"] = grouped_bytes
     roof["traffic"] = None
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr_path):
-        tr = json.load(open(tr_path)).get(args.workload)
+        tr = json.load(open(tr_path)).get(workload)
         if tr and tr.get("src_digest") == src_digest(tr["sources"]):
             roof["traffic"] = tr["dram_bytes_per_launch"]
 
+    res = {
+        "workload": DESCR[workload], "value": value, "unit": "tokens/s", "steps": steps, "ms_per_step": ms_step,
+        "roofline": roof, "clocks": clk, "active_experts": n_active, "layers": len(layers),
+        "weights": inp0.w, "T": T, "H": H, "E": E, "k": k, "I": I,
+        "step_hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
+        "step_tflops": flops / (ms_step / 1e3) / 1e12,
+        "l2": f"inputs larger than L2 ({ctx.l2_bytes / 2**20:.0f} MiB, {ctx.l2_source}): {n_copies} rotating "
+              f"weight cop{'y' if n_copies == 1 else 'ies'} ({n_copies * per_copy / 1e9:.1f} GB), "
+              f"one moe_forward graph per copy",
+        "breakdown_us": {**breakdown, "note": "each entry point timed alone (eager launches, CUDA events)"},
+        "gpu_launches_per_step": sum(moe.moe_forward_launches(L.shape) for L in dl[0]),
+    }
+    if tensor_bound:
+        peak_s = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        res["step_frac_of_sustained_bf16"] = res["step_tflops"] / peak_s
+
+    if headline:
+        res["e2e"] = end_to_end(ctx, layers, dl, outs, graphs, n_copies, steps)
+        res["entry"] = entry
+        res["n_copies"] = n_copies
+        res["per_copy"] = per_copy
+    del graphs, dl, wss, outs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res, layers
+
+
+def end_to_end(ctx, layers, dl, outs, graphs, n_copies, steps):
+    """The same metric through the C ABI with HOST buffers: each step copies the step's tokens
+    from pinned host memory, runs the block and copies the result back to pinned host memory.
+    Decode batches use moe_graphs_run (the library's bucketed decode graphs: zero-fill of the
+    padded rows, host->device copy, graph launch, device->host copy, all enqueued by the
+    library); larger batches copy around the block's graph replay."""
+    torch, moe, dev, stream = ctx.torch, ctx.moe, ctx.dev, ctx.stream
+    from top_routing_grouped_router_gb300.device import to_device
+    T, H = layers[0].T, layers[0].H
+    out_dt = outs[0].dtype
+    x_host = [to_device(l.x, "cpu", pin=True) for l in layers]
+    out_host = [torch.empty((T, H), dtype=out_dt, pin_memory=True) for _ in layers]
+    e2e_steps = min(steps, 500)
+    use_graph_api = len(layers) == 1 and T <= 64 and ctx.args.entry == "forward"
+    if use_graph_api:
+        dgs = [moe.DecodeGraphs(dl[c][0].shape, T, dl[c][0].w_router, dl[c][0].b_router, dl[c][0].w_gate,
+                                dl[c][0].w_up, dl[c][0].w_down, dl[c][0].q4, device=dev, stream=stream)
+               for c in range(n_copies)]
+        run = lambda i: dgs[i % n_copies].run(T, x_host[0], out_host[0], stream=stream)
+        how = "moe_graphs_run (C ABI) with pinned host x and out"
+    else:
+        def run(i):
+            for l in range(len(layers)):
+                dl[0][l].x.copy_(x_host[l], non_blocking=True)
+            graphs[i % n_copies].replay()
+            for l in range(len(layers)):
+                out_host[l].copy_(outs[l], non_blocking=True)
+        how = "pinned host copies around the moe_forward graph replay"
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            run(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e2e_steps):
+            run(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    # the host result equals the device path's result on the same tokens
+    with torch.cuda.stream(stream):
+        graphs[(e2e_steps - 1) % n_copies].replay()
+    torch.cuda.synchronize()
+    same = all(torch.equal(out_host[l], outs[l].cpu()) for l in range(len(layers)))
+    if use_graph_api:
+        for g in dgs:
+            g.close()
+    bi = sum(x.numel() * x.element_size() for x in x_host)
+    bo = sum(o.numel() * o.element_size() for o in out_host)
+    return {"value": ctx.world * T * len(layers) / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms, "steps": e2e_steps, "how": how,
+            "host_result_equals_device_result": bool(same)}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ctx = Ctx(args, world, local)
+    head, layers = measure(ctx, args.workload, args.steps, args.warmup, headline=True)
+    inp0 = layers[0]
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if inp0.act == "bf16" else "f32",
         "data": "synthetic: seeded N(0,1) tokens, N(0,1/fan_in) random-init weights of the model's shapes",
-        "config": {"workload": DESCR[args.workload],
+        "config": {"workload": head["workload"],
                    "entry": {"forward": "moe_forward", "rmsnorm": "moe_forward_rmsnorm (pre-router RMSNorm + residual)",
                              "lora": "moe_forward_lora (rank-16 fp32 adapters on the expert projections"
                                       + (", packed: tensor-core adapter products)" if inp0.w == "bf16" and not args.lora_unpacked
-                                         else ", CUDA-core adapter products)")}[args.entry], "T": T, "H": H, "E": E, "k": k, "I": I,
-                   "layers": len(layers), "weights": inp0.w, "active_experts": n_active,
-                   "l2": f"inputs larger than L2: {n_copies} rotating weight cop{'y' if n_copies == 1 else 'ies'} "
-                         f"({n_copies * per_copy / 1e9:.1f} GB), one moe_forward graph per copy",
-                   "step_hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
-                   "step_tflops": flops / (ms_step / 1e3) / 1e12, "parallelism": f"replicas x{world}"},
-        "roofline": roof,
-        "e2e": {"value": world * tokens_per_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
-        "gpu_launches": launches * args.steps,
-        "breakdown_us": {**breakdown, "note": "each entry point timed alone (eager launches, CUDA events)"},
-        "clocks": clk,
+                                         else ", CUDA-core adapter products)")}[head["entry"]],
+                   "T": head["T"], "H": head["H"], "E": head["E"], "k": head["k"], "I": head["I"],
+                   "layers": head["layers"], "weights": head["weights"], "active_experts": head["active_experts"],
+                   "l2": head["l2"], "l2_bytes": ctx.l2_bytes,
+                   "step_hbm_gbs": head["step_hbm_gbs"], "step_tflops": head["step_tflops"],
+                   "parallelism": f"replicas x{world}"},
+        "roofline": head["roofline"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches_per_step"] * args.steps,
+        "breakdown_us": head["breakdown_us"],
+        "clocks": head["clocks"],
     }
+    extras = [] if args.extras.strip().lower() in ("", "none") else [w.strip() for w in args.extras.split(",")]
+    if world == 1 and args.entry == "forward":
+        configs = {}
+        for wl in extras:
+            if wl == args.workload:
+                continue
+            # a few hundred microseconds (decode) to 1.6 ms (prefill) per step
+            st = max(50, min(args.steps, 500)) if not wl.startswith("prefill") else max(20, min(args.steps, 100))
+            r, _ = measure(ctx, wl, st, max(3, args.warmup), headline=False)
+            configs[wl] = r
+        if configs:
+            line["configs"] = configs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(layers, args.cpu_seconds)
     if rank == 0:
