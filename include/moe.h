@@ -345,6 +345,21 @@ MOE_API int moe_forward_launches(const moe_shape *shape, int32_t *launches);
  */
 MOE_API int moe_read_device_error(void *workspace, int32_t *code, moe_stream_t stream);
 
+/*
+ * Failure-path test hook (process-wide; not for production use).  Every wait
+ * inside the tensor-core expert kernels (a pipeline barrier, or a down tile
+ * waiting for its expert's h) is bounded: after limit_ns of wall time
+ * (default 2e9 = 2 s) it records MOE_ERR_DEVICE in the error word, and the CTA
+ * stops starting new work, waits for the copies and MMAs it already issued,
+ * frees its tensor memory and exits.  extra_need > 0 raises the count every
+ * down tile waits for by that much, so those waits can never be met and must
+ * run out: a test sets a short limit and extra_need, checks that the call
+ * returns with MOE_ERR_DEVICE recorded, restores (2e9, 0), and checks that the
+ * next ordinary call is correct.  Read at each launch; calls already enqueued
+ * keep their values.  MOE_ERR_SHAPE for limit_ns == 0 or extra_need < 0.
+ */
+MOE_API int moe_debug_set_waits(uint64_t limit_ns, int32_t extra_need);
+
 /* ------------------------------------------------------------------------
  * Bucketed CUDA-graph decode (the capture pattern of the unsloth commit page
  * 80aaf1121b, paragraph on FlexMoEInference.capture_decode_cudagraph): one

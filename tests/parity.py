@@ -2,6 +2,9 @@
 and compare every step with the CPU oracle on the same seeded inputs."""
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import torch
 
@@ -14,6 +17,52 @@ from top_routing_grouped_router_gb300.device import DeviceLayer, bf16_tensor_bit
 # its expert choice may legitimately differ between fp32 and double, so it is excluded
 # from the bit-exact comparison and reported.
 NEAR_TIE = 1e-5
+
+# Every excluded near-tie token and every slot-order swap between near-equal selected
+# logits, per checked layer: printed in the pytest terminal summary (tests/conftest.py).
+EXCLUSIONS: list = []
+
+
+def exclusion_bound(T: int) -> int:
+    """Largest number of near-tie tokens (and, separately, of slot-order swaps) a batch of T
+    tokens may show.  With N(0,1)-like logits over 128 experts the gap between two
+    neighbouring order statistics falls below 1e-5 for roughly one token in 10^4, so a
+    count above this bound means a routing bug, not rounding."""
+    return 3 + T // 500
+
+
+def _pool():
+    return cf.ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1)))
+
+
+def oracle_y_rows(inp, offsets: np.ndarray, order: np.ndarray, rows) -> np.ndarray:
+    """The oracle's y for the given permuted rows (steps E-F), one oracle call per row on
+    host threads (the oracle's C calls release the GIL)."""
+    k = inp.k
+
+    def one(p):
+        e = int(np.searchsorted(offsets, p, side="right") - 1)
+        t = int(order[p]) // k
+        xrow = (synth.bf16_bits_to_f32(inp.x[t]).astype(np.float64) if inp.act == "bf16"
+                else inp.x[t].astype(np.float64))
+        return oracle.expert_mlp(inp, xrow, e)[1]
+
+    rows = [int(r) for r in rows]
+    if not rows:
+        return np.zeros((0, inp.H))
+    with _pool() as pool:
+        return np.array(list(pool.map(one, rows)))
+
+
+def oracle_tokens(inp, toks) -> dict:
+    """oracle.forward_tokens over `toks`, split into chunks evaluated on host threads."""
+    toks = np.asarray(toks, dtype=np.int32)
+    if toks.size == 0:
+        return dict(out=np.zeros((0, inp.H)), ids=np.zeros((0, inp.k), np.int32))
+    chunks = np.array_split(toks, min(toks.size, 64))
+    with _pool() as pool:
+        parts = list(pool.map(lambda c: oracle.forward_tokens(inp, c), chunks))
+    return dict(out=np.concatenate([r["out"] for r in parts]), ids=np.concatenate([r["ids"] for r in parts]))
 
 
 def tolerance(inp) -> float:
@@ -110,8 +159,16 @@ def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
     return np.array(sorted(pick), dtype=np.int32)
 
 
-def check_layer(inp, *, full_oracle: bool, n_sample_tokens: int = 16, n_sample_rows: int = 24, report=None):
-    """Every step of the CUDA path against the oracle; returns a summary dict."""
+def check_layer(inp, *, full_oracle: bool, n_sample_tokens: int = 16, n_sample_rows: int = 24, report=None,
+                target_experts: bool = False, token_slice: int = 0):
+    """Every step of the CUDA path against the oracle; returns a summary dict.
+
+    full_oracle: every y row and every output token against the oracle.  Otherwise a
+    sample of rows and tokens, plus (target_experts) every y row of three experts -- the
+    one with the most rows (several token chunks), the one with the fewest, and the last
+    active one (it ends the tile list) -- and (token_slice) every output row of a
+    contiguous slice of that many tokens from the middle of the batch.
+    """
     L = upload(inp)
     g = run_steps(L)
     T, k, E = inp.T, inp.k, inp.E
@@ -130,6 +187,11 @@ def check_layer(inp, *, full_oracle: bool, n_sample_tokens: int = 16, n_sample_r
                                atol=4e-4 * max(1.0, np.abs(o_logits).max()))
     np.testing.assert_array_equal(g["ids_forward"], g["ids"])
     np.testing.assert_array_equal(g["weights_forward"], g["weights"])
+    record = dict(name=f"{inp.name} (T={T}, layer {inp.layer})", T=T, near_ties=near.tolist(),
+                  order_ties=order_ties, bound=exclusion_bound(T))
+    EXCLUSIONS.append(record)
+    assert near.size <= record["bound"], f"{near.size} near-tie tokens, more than rounding explains"
+    assert len(order_ties) <= record["bound"], f"{len(order_ties)} slot-order swaps, more than rounding explains"
 
     # steps C-D on the GPU's own routing decision: integer-exact
     c, off, order, pos = oracle.permute(g["ids"], E)
@@ -141,17 +203,18 @@ def check_layer(inp, *, full_oracle: bool, n_sample_tokens: int = 16, n_sample_r
     # steps E-F on the GPU's permutation
     A = T * k
     if full_oracle:
-        _, o_y = oracle.grouped_swiglu(inp, off, order)
-        y_err = rel_err(g["y"], o_y)
+        rows = np.arange(A)
     else:
-        rows = sample_tokens(A, n_sample_rows, seed=1) if A else np.zeros(0, np.int32)
-        ref = []
-        for p in rows:
-            e = int(np.searchsorted(off, p, side="right") - 1)
-            t = order[p] // k
-            xrow = synth.bf16_bits_to_f32(inp.x[t]).astype(np.float64) if inp.act == "bf16" else inp.x[t].astype(np.float64)
-            ref.append(oracle.expert_mlp(inp, xrow, e)[1])
-        y_err = rel_err(g["y"][rows], np.array(ref)) if len(rows) else 0.0
+        rows = set(sample_tokens(A, n_sample_rows, seed=1).tolist()) if A else set()
+        if target_experts and A:
+            nz = np.nonzero(c)[0]
+            picks = {int(np.argmax(c)), int(nz[np.argmin(c[nz])]), int(nz[-1])}
+            for e in picks:
+                rows |= set(range(int(off[e]), int(off[e + 1])))
+            record["experts_compared_fully"] = sorted(picks)
+            record["expert_rows"] = {int(e): int(c[e]) for e in sorted(picks)}
+        rows = np.array(sorted(rows), dtype=np.int64)
+    y_err = rel_err(g["y"][rows], oracle_y_rows(inp, off, order, rows)) if len(rows) else 0.0
     assert y_err <= tol, f"grouped SwiGLU rel err {y_err}"
 
     # step G on the GPU's own y, weights and pos
@@ -163,18 +226,23 @@ def check_layer(inp, *, full_oracle: bool, n_sample_tokens: int = 16, n_sample_r
     # whole block vs the oracle's own routing, near-tie tokens excluded
     np.testing.assert_array_equal(g["out_forward"], g["out"])
     if full_oracle:
-        ref = oracle.forward(inp)
         toks = ok
-        o_out = ref["out"][toks]
     else:
-        toks = np.setdiff1d(sample_tokens(T, n_sample_tokens), near)
-        o_out = oracle.forward_tokens(inp, toks)["out"]
-    out_err = rel_err(g["out"][toks], o_out) if len(toks) else 0.0
+        pick = set(sample_tokens(T, n_sample_tokens).tolist())
+        if token_slice:
+            t0 = max(0, T // 2 - token_slice // 2)
+            pick |= set(range(t0, min(T, t0 + token_slice)))
+        toks = np.setdiff1d(np.array(sorted(pick), dtype=np.int32), near)
+    o_tok = oracle_tokens(inp, toks)
+    # the oracle's own per-token routing agrees with its full routing
+    np.testing.assert_array_equal(o_tok["ids"], o_ids[toks])
+    out_err = rel_err(g["out"][toks], o_tok["out"]) if len(toks) else 0.0
     assert out_err <= tol, f"block output rel err {out_err}"
     summary = dict(name=inp.name, T=T, near_ties=near.tolist(), order_ties=order_ties, y_rel_err=y_err,
-                   out_rel_err=out_err, active_experts=int((g["counts"] > 0).sum()))
-    if near.size or order_ties:
-        print(f"{inp.name}: near-tie tokens excluded {near.tolist()}, slot-order near ties {order_ties}")
+                   out_rel_err=out_err, active_experts=int((g["counts"] > 0).sum()), y_rows_compared=int(len(rows)),
+                   tokens_compared=int(len(toks)))
+    record.update(y_rows_compared=int(len(rows)), tokens_compared=int(len(toks)), y_rel_err=y_err,
+                  out_rel_err=out_err)
     if report is not None:
         report.append(summary)
     return summary, g

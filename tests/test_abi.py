@@ -160,3 +160,9 @@ def test_static_scratch_rejects_misaligned_q4_scales_before_any_cuda_call(L):
     rc = L.moe_forward_static_scratch(ctypes.byref(s), fake, fake, None, fake, fake, fake, ctypes.byref(q4), fake,
                                       None, None, None)
     assert rc == -1  # MOE_ERR_NULLPTR
+
+
+def test_debug_wait_hook_validates_and_restores(L):
+    assert L.moe_debug_set_waits(0, 0) == -2          # a zero limit is refused
+    assert L.moe_debug_set_waits(1000, -1) == -2      # so is a negative count
+    assert L.moe_debug_set_waits(2_000_000_000, 0) == 0

@@ -32,24 +32,25 @@ def test_decode8_full_size():
 
 
 def test_decode64_zipf_full_size_has_empty_experts():
-    s, g = check_layer(synth.make_inputs("decode64z"), full_oracle=False, n_sample_tokens=16, n_sample_rows=32)
+    s, g = check_layer(synth.make_inputs("decode64z"), full_oracle=True)
     assert (g["counts"] == 0).sum() >= 1
     assert g["counts"].max() >= 32
 
 
 def test_decode48_q4_full_size():
-    check_layer(synth.make_inputs("decode48q"), full_oracle=False, n_sample_tokens=12, n_sample_rows=24)
+    check_layer(synth.make_inputs("decode48q"), full_oracle=True)
 
 
 def test_prefill_q4_full_size():
-    s, g = check_layer(synth.make_inputs("prefill4q"), full_oracle=False, n_sample_tokens=10, n_sample_rows=16)
+    s, g = check_layer(synth.make_inputs("prefill4q"), full_oracle=False, n_sample_tokens=16, n_sample_rows=32,
+                       target_experts=True, token_slice=64)
     assert g["counts"].sum() == 4096 * 8
 
 
 @pytest.mark.parametrize("layer", [0, 1, 2, 3])
 def test_prefill_full_size_layer(layer):
-    s, g = check_layer(synth.make_inputs("prefill", layer=layer), full_oracle=False, n_sample_tokens=12,
-                       n_sample_rows=16)
+    s, g = check_layer(synth.make_inputs("prefill", layer=layer), full_oracle=False, n_sample_tokens=16,
+                       n_sample_rows=32, target_experts=True, token_slice=64)
     assert g["counts"].sum() == 4096 * 8
 
 
@@ -69,7 +70,9 @@ def test_prefill_full_size_layer(layer):
 ])
 def test_reduced_and_ragged_cases(T, H, E, k, I, act, w, zipf):
     inp = synth.make_custom(T, H, E, k, I, act=act, w=w, zipf=zipf, seed=T + E, name=f"custom{T}")
-    check_layer(inp, full_oracle=T * k <= 256, n_sample_tokens=16, n_sample_rows=32)
+    # every y row and every token against the oracle: the second token chunk of an expert
+    # with more than 256 rows, the split down chunks and the ragged last tiles included
+    check_layer(inp, full_oracle=True)
 
 
 def test_q4_non_affine_codebook_uses_generic_kernels():
@@ -93,7 +96,7 @@ def test_all_tokens_to_the_same_experts():
     bias = np.zeros(32, np.float32)
     bias[[3, 17, 22, 30]] = 40.0
     inp.b_router = bias
-    s, g = check_layer(inp, full_oracle=False, n_sample_tokens=12, n_sample_rows=24)
+    s, g = check_layer(inp, full_oracle=True)
     assert sorted(np.nonzero(g["counts"])[0].tolist()) == [3, 17, 22, 30]
     assert (g["counts"][[3, 17, 22, 30]] == 40).all()
 
@@ -103,7 +106,7 @@ def test_two_experts_take_every_token_of_a_large_batch():
     bias = np.zeros(16, np.float32)
     bias[[2, 11]] = 40.0
     inp.b_router = bias
-    s, g = check_layer(inp, full_oracle=False, n_sample_tokens=12, n_sample_rows=32)
+    s, g = check_layer(inp, full_oracle=True)
     assert (g["counts"][[2, 11]] == 777).all()
 
 

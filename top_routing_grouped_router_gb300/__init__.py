@@ -20,6 +20,7 @@ __all__ = [
     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string", "EXPORTED_SYMBOLS",
     "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_forward_lora", "moe_graph_buckets", "moe_graphs_arena_size",
     "DecodeGraphs", "moe_lora_pack_size", "moe_lora_pack", "pack_lora", "moe_static_scratch_read_error",
+    "moe_debug_set_waits",
 ]
 
 MOE_DT_F32, MOE_DT_BF16, MOE_DT_Q4 = 0, 1, 2
@@ -32,7 +33,7 @@ EXPORTED_SYMBOLS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_group
                     "moe_forward", "moe_forward_launches", "moe_read_device_error", "moe_status_string",
                     "moe_forward_static_scratch", "moe_forward_rmsnorm", "moe_forward_lora", "moe_graph_buckets", "moe_graphs_arena_size", "moe_graphs_create",
                     "moe_graphs_bucket", "moe_graphs_run", "moe_graphs_destroy", "moe_lora_pack_size", "moe_lora_pack",
-                    "moe_static_scratch_read_error")
+                    "moe_static_scratch_read_error", "moe_debug_set_waits")
 
 
 class MoEError(RuntimeError):
@@ -83,6 +84,7 @@ def lib() -> ctypes.CDLL:
             "moe_forward_launches": [sp, ctypes.POINTER(ctypes.c_int32)],
             "moe_forward_static_scratch": [sp, vp, vp, vp, vp, vp, vp, q4p, vp, i32p, vp, vp],
             "moe_static_scratch_read_error": [ctypes.POINTER(ctypes.c_int32), vp],
+            "moe_debug_set_waits": [ctypes.c_uint64, ctypes.c_int32],
             "moe_forward_rmsnorm": [sp, vp, vp, ctypes.c_float, ctypes.c_int, vp, vp, vp, vp, vp, q4p, vp, vp, i32p,
                                     vp, vp, sz, vp],
             "moe_forward_lora": [sp, vp, vp, vp, vp, vp, vp, q4p, ctypes.POINTER(MoELora), vp, i32p, vp, vp, sz, vp],
@@ -187,6 +189,12 @@ def moe_forward_static_scratch(shape, x, w_router, b_router, w_gate, w_up, w_dow
                                             ctypes.byref(q4) if q4 is not None else None, _ptr(out),
                                             _ptr(expert_ids_out), _ptr(weights_out), _stream(stream)),
            "moe_forward_static_scratch")
+
+
+def moe_debug_set_waits(limit_ns: int = 2_000_000_000, extra_need: int = 0):
+    """Failure-path test hook: the bounded device waits' limit and an unreachable extra count
+    for the down tiles' h wait (see moe.h).  Call with no arguments to restore the defaults."""
+    _check(lib().moe_debug_set_waits(int(limit_ns), int(extra_need)), "moe_debug_set_waits")
 
 
 def moe_static_scratch_read_error(stream=None) -> int:

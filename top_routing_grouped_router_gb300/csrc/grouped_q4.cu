@@ -83,6 +83,9 @@ struct Params {
     uint32_t centre2;               // bf16x2 of 128 + 2*j0
     int E, H, I, A;
     int cmax;                       // token chunk (fixed chunks of cmax, see chunk_base)
+    unsigned long long wait_ns;     // limit of every bounded wait
+    int extra_need;                 // added to the h publications a down tile waits for (failure-path
+                                    // test: a count nothing reaches, so those waits must run out)
 };
 
 // The 8-element group order of the weights: position q holds element kSigma[q].
@@ -152,6 +155,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
     int *rmeta = reinterpret_cast<int *>(drain + 1);        // [kRawStages][8]
     int *tmeta = rmeta + 8 * kRawStages;                    // [kMetaRing][8]
     volatile int *abort = tmeta + 8 * kMetaRing;
+    const Waits wt{p.err, abort, p.wait_ns};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmeta + 8 * kMetaRing + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -196,7 +200,9 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         int r = 0, slot = 0, tiles_done = 0;
+        int rfills = 0;  // raw-ring fills issued so far (tiles_done counts the scale fills)
         uint32_t rp = 0, mphase = 0;
+        bool live = true;
         // this launch's tile range [lo, hi) and its claim counter
         int lo = 0, hi = p.sched[kSchedTiles];
         int *ctr = p.sched + kSchedClaim;
@@ -206,7 +212,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             ctr = p.sched + kSchedClaimDown;
         }
         int next = lo + atomicAdd(ctr, 1);
-        for (;;) {
+        while (live) {
             const int t = next;
             if (t >= hi || *abort) break;
             next = lo + atomicAdd(ctr, 1);
@@ -226,10 +232,10 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const int N = m > 0 ? (m + 15) & ~15 : 16;
             if (down) {
                 const int need = (p.I / kRows) * n_chunks(me, p.cmax, false) * kEpiWarps;
-                wait_count(p.done + e, need, p.err, abort);
+                if (!wait_count(p.done + e, need + p.extra_need, wt)) break;
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
-            mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, p.err, abort);
+            if (!mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, wt)) break;
             int *tm = tmeta + 8 * slot;
             tm[0] = down;
             tm[1] = e;
@@ -245,7 +251,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             {
                 // the tile's block scales: 128 consecutive rows x nslab bf16, contiguous in memory
                 const int sb = tiles_done & 1;
-                mbar_wait(smem_u32(&sempty[sb]), ((tiles_done >> 1) & 1) ^ 1, p.err, abort);
+                if (!mbar_wait(smem_u32(&sempty[sb]), ((tiles_done >> 1) & 1) ^ 1, wt)) break;
                 const uint32_t sfb = smem_u32(&sfull[sb]);
                 const uint32_t sbytes = uint32_t(kRows * nslab * 2);
                 const size_t row0 = (size_t)e * (down ? p.H : p.I) + (size_t)rb * kRows;
@@ -265,7 +271,10 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const uint32_t bytes = (down && !two ? kCodeBytes : 2 * kCodeBytes) + (two ? 2 : 1) * nbox * kNBox * 128;
             const int wrow = e * (down ? p.H : p.I) + rb * kRows;
             for (int ks = 0; ks < nstage; ++ks) {
-                mbar_wait(smem_u32(&rempty[r]), rp ^ 1, p.err, abort);
+                if (!mbar_wait(smem_u32(&rempty[r]), rp ^ 1, wt)) {
+                    live = false;
+                    break;
+                }
                 int *mt = rmeta + 8 * r;
                 mt[0] = down | (two << 2);
                 mt[1] = ks;
@@ -275,6 +284,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 mt[5] = rb;
                 const uint32_t fb = smem_u32(&rfull[r]);
                 mbar_arrive_expect_tx(fb, bytes);
+                ++rfills;
                 const uint32_t base = smem_u32(raw + r * kRawBytes);
                 if (!down) {
                     tma_load_2d(base, &tm_gc, ks * (kSlab / 2), wrow, fb);
@@ -297,12 +307,22 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 if (++r == kRawStages) { r = 0; rp ^= 1; }
             }
         }
-        mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, p.err, abort);
-        tmeta[8 * slot] = -1;
-        mbar_arrive(smem_u32(&tmf[slot]));
-        mbar_wait(smem_u32(&rempty[r]), rp ^ 1, p.err, abort);
-        rmeta[8 * r + 1] = -1;
-        mbar_arrive(smem_u32(&rfull[r]));
+        // no TMA or bulk write may still be landing in this CTA's shared memory when it
+        // exits: wait for the last fills of the raw ring and of the scale buffers (all
+        // consumed already unless the CTA is aborting)
+        for (int i = max(0, rfills - kRawStages); i < rfills; ++i)
+            mbar_wait_drain(smem_u32(&rfull[i % kRawStages]), uint32_t((i / kRawStages) & 1), wt);
+        for (int i = max(0, tiles_done - 2); i < tiles_done; ++i)
+            mbar_wait_drain(smem_u32(&sfull[i & 1]), uint32_t((i >> 1) & 1), wt);
+        // sentinels (an aborting CTA's roles leave on the abort flag instead)
+        if (mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, wt)) {
+            tmeta[8 * slot] = -1;
+            mbar_arrive(smem_u32(&tmf[slot]));
+        }
+        if (mbar_wait(smem_u32(&rempty[r]), rp ^ 1, wt)) {
+            rmeta[8 * r + 1] = -1;
+            mbar_arrive(smem_u32(&rfull[r]));
+        }
     } else if (warp >= 2 + kEpiWarps) {
         // ------------------------------------------------ dequant
         const int u = (warp - 2 - kEpiWarps) * 32 + lane;   // 0..255
@@ -310,12 +330,12 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         int r = 0, a = 0, tiles_done = 0;
         uint32_t rp = 0, ap = 0;
         for (;;) {
-            mbar_wait(smem_u32(&rfull[r]), rp, p.err, abort);
+            if (!mbar_wait(smem_u32(&rfull[r]), rp, wt)) break;
             const uint32_t mt = smem_u32(rmeta + 8 * r);
             const int kind = int(lds_u32(mt)), ks = int(lds_u32(mt + 4)), nstage = int(lds_u32(mt + 8));
-            mbar_wait(smem_u32(&aempty[a]), ap ^ 1, p.err, abort);
+            mbar_wait(smem_u32(&aempty[a]), ap ^ 1, wt);
             const int sb = tiles_done & 1;
-            if (ks == 0) mbar_wait(smem_u32(&sfull[sb]), (tiles_done >> 1) & 1, p.err, abort);
+            if (ks == 0) mbar_wait(smem_u32(&sfull[sb]), (tiles_done >> 1) & 1, wt);
             if (ks >= 0 && !*abort) {
                 const int down = kind & 3, two = kind >> 2;
                 const uint32_t rbase = smem_u32(raw + r * kRawBytes) + uint32_t(row * 32 + half * 16);
@@ -355,14 +375,14 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         int r = 0, a = 0, tile_count = 0;
         uint32_t ap = 0;
         for (;;) {
-            const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&afull[a]), ap, p.err, abort));
+            const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&afull[a]), ap, wt));
             const int *mt = rmeta + 8 * r;
             const int kind = mt[0], ks = mt[1], nstage = mt[2], N = mt[3];
             if (__any_sync(0xffffffffu, !got || ks < 0 || *abort)) break;
             const int down = kind & 3, two = kind >> 2;
             const int b = tile_count & 1;
             if (ks == 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce[b]), ((tile_count >> 1) & 1) ^ 1, p.err, abort)))
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce[b]), ((tile_count >> 1) & 1) ^ 1, wt)))
                     break;
                 tc_fence_after();
             }
@@ -394,8 +414,10 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             if (++r == kRawStages) r = 0;
             if (++a == kAStages) { a = 0; ap ^= 1; }
         }
+        // every MMA this warp issued has completed before TMEM is released (an aborting CTA
+        // waits for them too)
         mma_commit_warp(smem_u32(drain));
-        mbar_wait(smem_u32(drain), 0, p.err, abort);
+        mbar_wait_drain(smem_u32(drain), 0, wt);
     } else if (warp >= 2 && warp < 2 + kEpiWarps) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;
@@ -403,7 +425,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         int slot = 0, tile_count = 0;
         uint32_t mphase = 0;
         for (;;) {
-            mbar_wait(smem_u32(&tmf[slot]), mphase, p.err, abort);
+            if (!mbar_wait(smem_u32(&tmf[slot]), mphase, wt)) break;
             const int *tm = tmeta + 8 * slot;
             const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], N = tm[5];
             __syncwarp();
@@ -411,7 +433,8 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
             if (down < 0 || *abort) break;
             const int b = tile_count & 1;
-            mbar_wait(smem_u32(&accf[b]), (tile_count >> 1) & 1, p.err, abort);
+            // the accumulator must be complete before TMEM is read (an aborting CTA leaves)
+            if (!mbar_wait(smem_u32(&accf[b]), (tile_count >> 1) & 1, wt)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(b * kBufCols);
             const int col = rb * kRows + row;
@@ -657,6 +680,8 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     prm.I = s.I;
     prm.A = A;
     prm.cmax = cmax;
+    prm.wait_ns = wait_limit_ns();
+    prm.extra_need = debug_extra_need();
     auto run = [&](const Params &pr, auto lora_tag) {
         constexpr bool L = decltype(lora_tag)::value;
         if (decode)

@@ -95,6 +95,9 @@ struct Params {
     uint16_t *y;                // [A][H] bf16
     int E, H, I, A;
     int dmax;                   // token chunk bound of the down tiles (even chunks)
+    unsigned long long wait_ns; // limit of every bounded wait
+    int extra_need;             // added to the h publications a down tile waits for (failure-path
+                                // test: a count nothing reaches, so those waits must run out)
     // router mode: tiles are (row block of experts, 128-token chunk), one static sweep
     int router_tiles;           // > 0 selects router mode
     int T;
@@ -174,6 +177,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     int *smeta = reinterpret_cast<int *>(drain + 1);               // [kStages][4]: kind, first, nstage, N
     int *tmeta = smeta + 4 * kStages;                              // [kMetaRing][8]
     volatile int *abort = tmeta + 8 * kMetaRing;
+    const Waits wt{p.err, abort, p.wait_ns};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmeta + 8 * kMetaRing + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -232,6 +236,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         uint4 next_rec = (!router && next < hi) ? __ldg(p.tiles + next) : make_uint4(0, 0, 0, 0);
         const int cap_dn = min(p.dmax, (kABytes + kBBytes) / 128);
         int hnext = 0;  // TMEM half of the next one-half tile
+        int fills = 0;  // stage fills issued (arrive.expect_tx + TMA) so far
         bool live = true;
         while (live) {
             const int t = next;
@@ -255,7 +260,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             if (!ok) record_error(p.err, MOE_ERR_DEVICE);
             if (d.down == kDown || d.down == kLoraH) {
                 // the expert's h must be complete: every epilogue warp of every gate/up tile
-                wait_count(p.done + d.e, d.need, p.err, abort);
+                if (!wait_count(p.done + d.e, d.need + p.extra_need, wt)) break;
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             const bool lora_a = d.down == kLoraX || d.down == kLoraH;
@@ -270,7 +275,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 hnext ^= 1;
             }
             // hand the tile to the epilogue
-            mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, p.err, abort);
+            if (!mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, wt)) break;
             int *tm = tmeta + 8 * slot;
             tm[0] = d.down;
             tm[1] = d.e;
@@ -318,9 +323,19 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             const CUtensorMap *bmap = d.down == kDown ? (box == kBigBox ? &tm_hb : box == kMidBox ? &tm_hm : &tm_h)
                                                       : (box == kBigBox ? &tm_xb : box == kMidBox ? &tm_xm : &tm_x);
             for (int ks = 0; ks < nstage; ++ks) {
-                if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort)) {
+                if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wt)) {
                     live = false;
                     break;
+                }
+                const bool lstage = lst && ks >= nstage - lst;
+                if (kLora == kLoraPacked && lstage && ks == nstage - lst) {
+                    // the tokens' scaled A-side products must be complete (the expert's A-side
+                    // tiles published) before this stage's loads are armed
+                    if (!wait_count(p.done + (d.down == kGateUp ? 1 : 2) * kMaxE + d.e, d.need_l, wt)) {
+                        live = false;
+                        break;
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
                 }
                 if (ks == 0) {  // the tile's shape, read by the MMA issuer at its first stage
                     int *sm = smeta + 4 * stage;
@@ -332,8 +347,8 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 if (!router && ks == min(2, nstage - 1))
                     next_rec = next < hi ? __ldg(p.tiles + next) : make_uint4(0, 0, 0, 0);
                 const uint32_t fb = smem_u32(&full[stage]);
-                const bool lstage = lst && ks >= nstage - lst;
                 mbar_arrive_expect_tx(fb, lstage ? lbytes : bytes);
+                ++fills;
                 const uint32_t a0 = smem_u32(smem + stage * kStageBytes);
                 const uint32_t bb = a0 + 2 * kABytes;
                 bool issued = false;
@@ -342,13 +357,9 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     if (lstage) {
                         // B adapter rows of the tile's 128 weight rows and the tokens' scaled A-side
                         // products (64-column slab li: gate, up, or down), in the token region of the
-                        // kind; those products must be complete (the expert's A-side tiles published)
+                        // kind (the products were waited for above)
                         const bool gu = d.down == kGateUp;
                         const int li = ks - (nstage - lst);
-                        if (li == 0) {
-                            wait_count(p.done + (gu ? 1 : 2) * kMaxE + d.e, d.need_l, p.err, abort);
-                            asm volatile("fence.proxy.async.global;" ::: "memory");
-                        }
                         tma_load_2d(a0, gu ? &lm.lbg : &lm.lbd, li * kSlab, d.e * (gu ? p.I : p.H) + d.rb * kRows, fb);
                         const uint32_t tb = gu || two ? bb : a0 + kABytes;
                         const CUtensorMap *tm2 = gu ? (lbox == kBigBox ? &lm.xa128 : &lm.xa16)
@@ -383,13 +394,20 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
         }
-        // sentinels for the MMA issuer and the epilogue
-        mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, p.err, abort);
-        tmeta[8 * slot] = -1;
-        mbar_arrive(smem_u32(&tmf[slot]));
-        mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, abort);
-        smeta[4 * stage + 1] = -1;
-        mbar_arrive(smem_u32(&full[stage]));
+        // no TMA write may still be landing in this CTA's shared memory when it exits: wait
+        // for the last fills of the ring (all consumed already unless the CTA is aborting)
+        for (int i = max(0, fills - kStages); i < fills; ++i)
+            mbar_wait_drain(smem_u32(&full[i % kStages]), uint32_t((i / kStages) & 1), wt);
+        // sentinels for the MMA issuer and the epilogue (an aborting CTA's roles leave on
+        // the abort flag instead)
+        if (mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, wt)) {
+            tmeta[8 * slot] = -1;
+            mbar_arrive(smem_u32(&tmf[slot]));
+        }
+        if (mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wt)) {
+            smeta[4 * stage + 1] = -1;
+            mbar_arrive(smem_u32(&full[stage]));
+        }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         // The whole warp runs this loop, converged (every branch below is warp-uniform, and
@@ -400,7 +418,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         uint32_t phase = 0;
         int uses[2] = {0, 0};  // tiles that have taken each TMEM half so far
         for (;;) {
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, p.err, abort))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, wt))) break;
             const int *sm = smeta + 4 * stage;
             const int kind = sm[0], first = sm[1], nstage = sm[2], N = sm[3];
             if (__any_sync(0xffffffffu, first < 0 || *abort)) break;
@@ -411,7 +429,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
                 if ((hmask >> hh) & 1)
-                    freed = freed && __all_sync(0xffffffffu, mbar_wait(smem_u32(&acce[hh]), (uses[hh] & 1) ^ 1, p.err, abort));
+                    freed = freed && __all_sync(0xffffffffu, mbar_wait(smem_u32(&acce[hh]), (uses[hh] & 1) ^ 1, wt));
             if (!freed) break;
             tc_fence_after();
             const uint32_t d = tmem_base + (hmask == 2 ? 256u : 0u);
@@ -450,7 +468,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 mma_commit_warp(smem_u32(&empty[stage]));  // the stage's smem is free once these MMAs are done
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
                 if (++ks == nstage) break;
-                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, p.err, abort))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[stage]), phase, wt))) {
                     live = false;
                     break;
                 }
@@ -464,9 +482,10 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     ++uses[hh];
                 }
         }
-        // every MMA this warp issued has completed before TMEM is released
+        // every MMA this warp issued has completed before TMEM is released (an aborting CTA
+        // waits for them too)
         mma_commit_warp(smem_u32(drain));
-        mbar_wait(smem_u32(drain), 0, p.err, abort);
+        mbar_wait_drain(smem_u32(drain), 0, wt);
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
@@ -477,16 +496,19 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         int uses[2] = {0, 0};
         uint32_t mphase = 0;
         for (;;) {
-            mbar_wait(smem_u32(&tmf[slot]), mphase, p.err, abort);
+            if (!mbar_wait(smem_u32(&tmf[slot]), mphase, wt)) break;
             const int *tm = tmeta + 8 * slot;
             const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], N = tm[5], hmask = tm[6];
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tme[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
             if (down < 0 || *abort) break;
+            // the accumulators must be complete before TMEM is read (an aborting CTA leaves)
+            bool got = true;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
-                if ((hmask >> hh) & 1) mbar_wait(smem_u32(&accf[hh]), uses[hh] & 1, p.err, abort);
+                if ((hmask >> hh) & 1) got = mbar_wait(smem_u32(&accf[hh]), uses[hh] & 1, wt) && got;
+            if (!got) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t(32 * q) << 16) + (hmask == 2 ? 256u : 0u);
             const uint32_t up_col = hmask == 3 ? 256u : 128u;
@@ -697,6 +719,7 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
     prm.H = s.H;
     prm.I = s.I;
     prm.router_tiles = tiles;
+    prm.wait_ns = tc::wait_limit_ns();
     prm.T = s.T;
     prm.logits = logits;
     prm.bias = bias;
@@ -790,6 +813,8 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.I = s.I;
     prm.A = A;
     prm.dmax = dmax;
+    prm.wait_ns = tc::wait_limit_ns();
+    prm.extra_need = tc::debug_extra_need();
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (!lora) return launch_tc_for<kLoraNone>(s, wide, grid, st, m, prm);

@@ -3,6 +3,7 @@
 // count per device.
 #include "tc_common.cuh"
 
+#include <atomic>
 #include <mutex>
 
 namespace moe {
@@ -57,5 +58,20 @@ int sm_count() {
 }
 
 
+namespace {
+std::atomic<unsigned long long> g_wait_ns{kWaitNs};
+std::atomic<int> g_extra_need{0};
+}  // namespace
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int debug_extra_need() { return g_extra_need.load(std::memory_order_relaxed); }
+
 }  // namespace tc
 }  // namespace moe
+
+extern "C" int moe_debug_set_waits(uint64_t limit_ns, int32_t extra_need) {
+    if (limit_ns == 0 || extra_need < 0) return MOE_ERR_SHAPE;
+    moe::tc::g_wait_ns.store(limit_ns, std::memory_order_relaxed);
+    moe::tc::g_extra_need.store(extra_need, std::memory_order_relaxed);
+    return MOE_OK;
+}

@@ -9,10 +9,11 @@
 namespace moe {
 namespace tc {
 
-// Every wait of the tensor-core kernels gives up after kWaitNs of wall time (read from
-// %globaltimer): it then records MOE_ERR_DEVICE, raises the CTA's abort flag and returns,
-// so that a lost arrival ends the kernel with an error instead of a hang.  Healthy waits
-// last microseconds; the limit only has to be far above any legitimate stall.
+// Every wait of the tensor-core kernels gives up after a wall-time limit (read from
+// %globaltimer; 2 s unless moe_debug_set_waits changed it): it then records
+// MOE_ERR_DEVICE, raises the CTA's abort flag and returns, so that a lost arrival ends the
+// kernel with an error instead of a hang.  Healthy waits last microseconds; the limit only
+// has to be far above any legitimate stall.
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
@@ -21,6 +22,13 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
+// What a bounded wait needs: where to record a timeout, the CTA's abort flag (shared
+// memory) and the limit.
+struct Waits {
+    int32_t *err;
+    volatile int *abort;
+    unsigned long long limit_ns;
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -63,38 +71,57 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     return v;
 }
 
-// Bounded wait: after kWaitNs record the error and raise the CTA's abort flag, so that
+// Bounded wait: after the limit record the error and raise the CTA's abort flag, so that
 // every later wait of the CTA gives up at once and the kernel drains.  The flag and the
 // clock are checked every 16 polls.  Returns false when it gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *err, volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Waits &w) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 15) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitNs) {
-                record_error(err, MOE_ERR_DEVICE);
-                *abort = 1;
+            if (*w.abort) return false;
+            if (globaltimer_ns() - t0 > w.limit_ns) {
+                record_error(w.err, MOE_ERR_DEVICE);
+                *w.abort = 1;
                 return false;
             }
         }
     }
 }
 
-// Bounded wait until the global counter *p reaches `need` (acquire); same limit.
-__device__ __forceinline__ void wait_count(const int *p, int need, int32_t *err, volatile int *abort) {
+// The drain wait of an aborting CTA: waits for the completion of asynchronous work the
+// CTA itself issued (a TMA fill landing in its shared memory, its MMAs finishing), which
+// needs no other CTA and so always ends; it ignores the abort flag and gives up only
+// after the limit (recording the error).  Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, const Waits &w) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 15) == 0 && globaltimer_ns() - t0 > w.limit_ns) {
+            record_error(w.err, MOE_ERR_DEVICE);
+            *w.abort = 1;
+            return false;
+        }
+    }
+}
+
+// Bounded wait until the global counter *p reaches `need` (acquire); same limit.  Returns
+// false when it gave up (or the CTA is aborting).
+__device__ __forceinline__ bool wait_count(const int *p, int need, const Waits &w) {
     unsigned long long t0 = 0;
     for (uint32_t n = 0;; ++n) {
         int v;
         asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-        if (v >= need || *abort) return;
+        if (v >= need) return true;
+        if (*w.abort) return false;
         if (n == 0) {
             t0 = globaltimer_ns();
-        } else if (globaltimer_ns() - t0 > kWaitNs) {
-            record_error(err, MOE_ERR_DEVICE);
-            *abort = 1;
-            return;
+        } else if (globaltimer_ns() - t0 > w.limit_ns) {
+            record_error(w.err, MOE_ERR_DEVICE);
+            *w.abort = 1;
+            return false;
         }
         __nanosleep(64);
     }
@@ -208,6 +235,10 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t *r) {
 bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
               uint32_t box_cols = 64, bool bytes = false);
 int sm_count();
+// The bounded waits' limit and the failure-path test's extra publication count
+// (moe_debug_set_waits), read at each launch.
+unsigned long long wait_limit_ns();
+int debug_extra_need();
 
 }  // namespace tc
 }  // namespace moe
