@@ -42,9 +42,9 @@ def _forward(moe, L, ws):
     return out, ids
 
 
-# bf16 decode (tensor-core kernel), 4-bit decode (4-bit kernel) and a large bf16 batch
-# (256-token tiles, several chunks per expert)
-@pytest.mark.parametrize("name,T", [("decode8", None), ("decode48q", None), ("decode8", 600)])
+# bf16 decode (tensor-core kernel), 4-bit decode and a large 4-bit batch (the 4-bit kernel's
+# two tile shapes) and a large bf16 batch (several token chunks per expert)
+@pytest.mark.parametrize("name,T", [("decode8", None), ("decode48q", None), ("decode48q", 200), ("decode8", 600)])
 def test_bounded_wait_runs_out_and_the_next_call_is_correct(moe, name, T):
     from top_routing_grouped_router_gb300.device import upload
     inp = synth.make_inputs(name, T=T)

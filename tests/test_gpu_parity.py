@@ -67,6 +67,8 @@ def test_prefill_full_size_layer(layer):
     (1030, 512, 8, 2, 384, "bf16", "bf16", True),    # large batch, skewed load: ragged chunks
     (200, 256, 16, 4, 128, "bf16", "q4", False),     # 4-bit large batch: several 128-token chunks per expert
     (300, 512, 8, 2, 256, "bf16", "q4", True),       # 4-bit large batch, skewed load
+    (37, 512, 16, 4, 256, "bf16", "q4", False),      # 4-bit decode on CUDA cores: 8 and 4 scale blocks per row
+    (64, 64, 4, 2, 64, "bf16", "q4", True),          # 4-bit decode, one scale block per row, up to 64 tokens per expert
 ])
 def test_reduced_and_ragged_cases(T, H, E, k, I, act, w, zipf):
     inp = synth.make_custom(T, H, E, k, I, act=act, w=w, zipf=zipf, seed=T + E, name=f"custom{T}")
@@ -172,3 +174,44 @@ def test_out_of_range_expert_id_is_recorded_not_trapped():
     assert moe.moe_read_device_error(ws) == -7  # MOE_ERR_DEVICE
     assert moe.moe_read_device_error(ws) == 0
     assert counts.sum().item() == 7
+
+
+@pytest.mark.parametrize("name,entry", [("decode8", "forward"), ("decode48q", "forward"), ("decode8", "rmsnorm"),
+                                        ("decode48q", "rmsnorm")])
+def test_chained_layers_read_the_previous_layers_output(name, entry):
+    """Each call's kernels overlap the previous call's tail (programmatic dependent launch),
+    so a kernel that read its inputs before waiting would see the previous layer's output
+    half-written.  Layer l + 1 reads layer l's output as its tokens: the chain enqueued
+    back to back must equal, bit for bit, the same chain with a synchronisation between
+    calls."""
+    import top_routing_grouped_router_gb300 as moe
+    from top_routing_grouped_router_gb300.device import upload, to_device
+    inp = synth.make_inputs(name)
+    L = upload(inp)
+    ws = L.new_workspace()
+    gamma = to_device(synth.make_norm_weight(inp.H, inp.act, seed=7), "cuda")
+
+    def chain(sync):
+        x = L.x.clone()
+        outs = []
+        for _ in range(4):
+            out = torch.empty_like(x)
+            if entry == "rmsnorm":
+                moe.moe_forward_rmsnorm(L.shape, x, gamma, 1e-6, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down,
+                                        L.q4, out, workspace=ws)
+            else:
+                moe.moe_forward(L.shape, x, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4, out,
+                                workspace=ws)
+            if sync:
+                torch.cuda.synchronize()
+            outs.append(out)
+            x = out
+        torch.cuda.synchronize()
+        return outs
+
+    ref = chain(True)
+    for _ in range(3):
+        got = chain(False)
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
+    assert moe.moe_read_device_error(ws) == 0

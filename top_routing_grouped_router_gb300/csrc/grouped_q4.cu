@@ -204,11 +204,11 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         uint32_t rp = 0, mphase = 0;
         bool live = true;
         // this launch's tile range [lo, hi) and its claim counter
-        int lo = 0, hi = p.sched[kSchedTiles];
+        int lo = 0, hi = ldp(p.sched + kSchedTiles);
         int *ctr = p.sched + kSchedClaim;
-        if (p.phase == kPhaseGateUp) hi = p.sched[kSchedGateUp];
+        if (p.phase == kPhaseGateUp) hi = ldp(p.sched + kSchedGateUp);
         if (p.phase == kPhaseDown) {
-            lo = p.sched[kSchedGateUp];
+            lo = ldp(p.sched + kSchedGateUp);
             ctr = p.sched + kSchedClaimDown;
         }
         int next = lo + atomicAdd(ctr, 1);
@@ -216,12 +216,12 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const int t = next;
             if (t >= hi || *abort) break;
             next = lo + atomicAdd(ctr, 1);
-            const uint32_t entry = __ldg(p.tiles + t);
+            const uint32_t entry = ldp(p.tiles + t);
             const int down = int(entry >> 31), e0 = int((entry >> 16) & 0xFF), rb = int((entry >> 8) & 0xFF);
             const int nc = int(entry & 0xFF);
             const int e = min(e0, p.E - 1);
-            const int off = __ldg(p.offsets + e);
-            const int me = __ldg(p.offsets + e + 1) - off;
+            const int off = ldp(p.offsets + e);
+            const int me = ldp(p.offsets + e + 1) - off;
             const int base = chunk_base(me, p.cmax, false);
             int m = min(base, me - nc * base);
             if (e0 >= p.E || off < 0 || me <= 0 || off + me > p.A || m <= 0 || m > MaxN) {
@@ -510,8 +510,8 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 // (0,4,1,5,2,6,3,7).  Block 0 builds the tile list (an expert's tokens in fixed chunks of
 // cmax; all gate/up tiles before all down tiles) and clears the scheduling counters.
 __global__ void __launch_bounds__(256)
-q4_prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
-               int T, int k, int H, int I, int E, int cmax, int max_tiles, uint16_t *__restrict__ x_perm,
+q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, int T, int k, int H, int I, int E,
+               int cmax, int max_tiles, uint16_t *__restrict__ x_perm,
                uint32_t *tiles, int *sched, int *done, int32_t *err) {
     griddep_launch_dependents();
     griddep_wait();
@@ -520,7 +520,7 @@ q4_prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order
         const int pr = (blockIdx.x - 1) * kPrepRowsPerBlock + int(threadIdx.x >> 5);
         const int lane = threadIdx.x & 31;
         if (pr >= T * k) return;
-        const int a = __ldg(order + pr);
+        const int a = ldp(order + pr);
         uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
         const bool bad = a < 0 || a >= T * k;
         if (bad && lane == 0) record_error(err, MOE_ERR_DEVICE);
@@ -530,7 +530,7 @@ q4_prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order
             uint4 v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                v[u] = (!bad && i + 32 * u < n) ? __ldg(src + i + 32 * u) : make_uint4(0, 0, 0, 0);
+                v[u] = (!bad && i + 32 * u < n) ? ldp16(src + i + 32 * u) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 if (i + 32 * u >= n) continue;
@@ -549,7 +549,7 @@ q4_prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order
     const int e = threadIdx.x;
     int me = 0;
     if (e < E) {
-        me = min(max(offsets[e + 1] - offsets[e], 0), T * k);
+        me = min(max(ldp(offsets + e + 1) - ldp(offsets + e), 0), T * k);
         done[e] = 0;
     }
     const int nch = n_chunks(me, cmax, false);

@@ -37,10 +37,11 @@ __device__ __forceinline__ float weight_at(const WeightRef &w, const Codebook &c
     }
 }
 
+// token rows: produced-data loads (they may be an earlier kernel's output)
 template <typename ActT>
 __device__ __forceinline__ float act_at(const ActT *p, size_t i) {
-    if constexpr (sizeof(ActT) == 4) return __ldg(reinterpret_cast<const float *>(p) + i);
-    else return bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t *>(p) + i));
+    if constexpr (sizeof(ActT) == 4) return ldp(reinterpret_cast<const float *>(p) + i);
+    else return bf16_bits_to_f32(ldp(reinterpret_cast<const uint16_t *>(p) + i));
 }
 
 // Largest e with offsets[e] <= p, i.e. the expert whose segment holds row p.
@@ -48,15 +49,14 @@ __device__ __forceinline__ int expert_of_row(const int32_t *offsets, int E, int 
     int lo = 0, hi = E;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(offsets + mid) <= p) lo = mid; else hi = mid - 1;
+        if (ldp(offsets + mid) <= p) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
 
 template <typename ActT, int WFMT>
 __global__ void __launch_bounds__(kWarps * 32)
-gate_up_simple_kernel(const ActT *__restrict__ x, const int32_t *__restrict__ offsets,
-                      const int32_t *__restrict__ order, int E, int k, int H, int I, int A, WeightRef wg,
+gate_up_simple_kernel(const ActT *x, const int32_t *offsets, const int32_t *order, int E, int k, int H, int I, int A, WeightRef wg,
                       WeightRef wu, Codebook cb, float *__restrict__ h, int p0, LoraDev lr) {
     griddep_launch_dependents();
     griddep_wait();
@@ -65,7 +65,7 @@ gate_up_simple_kernel(const ActT *__restrict__ x, const int32_t *__restrict__ of
     const int p = p0 + blockIdx.y;
     if (i >= I) return;
     const int e = expert_of_row(offsets, E, p);
-    const int a = __ldg(order + p);
+    const int a = ldp(order + p);
     if (e >= E) return;
     if (a < 0 || a >= A) return;  // inconsistent permutation: leave the row alone
     const int t = a / k;
@@ -93,7 +93,7 @@ gate_up_simple_kernel(const ActT *__restrict__ x, const int32_t *__restrict__ of
 
 template <typename OutT, int WFMT>
 __global__ void __launch_bounds__(kWarps * 32)
-down_simple_kernel(const float *__restrict__ h, const int32_t *__restrict__ offsets, int E, int H, int I,
+down_simple_kernel(const float *h, const int32_t *offsets, int E, int H, int I,
                    WeightRef wd, Codebook cb, OutT *__restrict__ y, int p0, LoraDev lr) {
     griddep_launch_dependents();
     griddep_wait();
@@ -104,7 +104,7 @@ down_simple_kernel(const float *__restrict__ h, const int32_t *__restrict__ offs
     const int e = expert_of_row(offsets, E, p);
     if (e >= E) return;  // inconsistent offsets: leave the row alone
     float s = 0.f;
-    for (int c = lane; c < I; c += 32) s = fmaf(__ldg(h + (size_t)p * I + c), weight_at<WFMT>(wd, cb, e, r, c), s);
+    for (int c = lane; c < I; c += 32) s = fmaf(ldp(h + (size_t)p * I + c), weight_at<WFMT>(wd, cb, e, r, c), s);
     s = warp_sum(s);
     if (lane == 0) {
         if (lr.rank) {

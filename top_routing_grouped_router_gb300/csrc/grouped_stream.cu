@@ -224,8 +224,8 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         if (!router) {
             const int r = p.phase == kPhaseLoraX ? 0 : p.phase == kPhaseGateUp ? 1 : p.phase == kPhaseLoraH ? 2 : 3;
             const bool all = p.phase == kPhaseAll;
-            lo = p.sched[kSchedBound + (all ? 0 : r)];
-            hi = p.sched[kSchedBound + (all ? 4 : r + 1)];
+            lo = ldp(p.sched + kSchedBound + (all ? 0 : r));
+            hi = ldp(p.sched + kSchedBound + (all ? 4 : r + 1));
             ctr = p.sched + kSchedRangeClaim + (all ? 0 : r);
         }
         // the next tile is claimed when this one starts, and its record is loaded a few
@@ -233,7 +233,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         // between two tiles; claiming only one ahead keeps the tail balanced when tiles are
         // long (a decode gate/up tile streams 1 MB of weights)
         int next = router ? int(blockIdx.x) : lo + atomicAdd(ctr, 1);
-        uint4 next_rec = (!router && next < hi) ? __ldg(p.tiles + next) : make_uint4(0, 0, 0, 0);
+        uint4 next_rec = (!router && next < hi) ? ldp16(p.tiles + next) : make_uint4(0, 0, 0, 0);
         const int cap_dn = min(p.dmax, (kABytes + kBBytes) / 128);
         int hnext = 0;  // TMEM half of the next one-half tile
         int fills = 0;  // stage fills issued (arrive.expect_tx + TMA) so far
@@ -345,7 +345,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     sm[3] = lora_a ? nl : d.N;
                 }
                 if (!router && ks == min(2, nstage - 1))
-                    next_rec = next < hi ? __ldg(p.tiles + next) : make_uint4(0, 0, 0, 0);
+                    next_rec = next < hi ? ldp16(p.tiles + next) : make_uint4(0, 0, 0, 0);
                 const uint32_t fb = smem_u32(&full[stage]);
                 mbar_arrive_expect_tx(fb, lstage ? lbytes : bytes);
                 ++fills;

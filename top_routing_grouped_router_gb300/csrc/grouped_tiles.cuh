@@ -119,8 +119,8 @@ constexpr int kCountersPerExpert = 3;
 constexpr int kPrepRowsPerBlock = 8;
 __host__ __device__ constexpr int prep_blocks(int A) { return 1 + (A + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock; }
 __global__ void __launch_bounds__(256)
-prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, const int32_t *__restrict__ offsets,
-            int T, int k, int H, int E, TileListArgs ta, uint16_t *__restrict__ x_perm, uint4 *tiles,
+prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, int T, int k, int H, int E,
+            TileListArgs ta, uint16_t *__restrict__ x_perm, uint4 *tiles,
             int *sched, int *done, int32_t *err) {
     griddep_launch_dependents();
     griddep_wait();
@@ -129,7 +129,7 @@ prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, c
         const int pr = (blockIdx.x - 1) * kPrepRowsPerBlock + int(threadIdx.x >> 5);
         const int lane = threadIdx.x & 31;
         if (pr >= T * k) return;
-        const int a = __ldg(order + pr);
+        const int a = ldp(order + pr);
         const bool bad = a < 0 || a >= T * k;
         if (bad && lane == 0) record_error(err, MOE_ERR_DEVICE);
         uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
@@ -139,7 +139,7 @@ prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, c
             uint4 v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                v[u] = (!bad && i + 32 * u < n) ? __ldg(src + i + 32 * u) : make_uint4(0, 0, 0, 0);
+                v[u] = (!bad && i + 32 * u < n) ? ldp16(src + i + 32 * u) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 if (i + 32 * u < n) dst[i + 32 * u] = v[u];
@@ -151,8 +151,8 @@ prep_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ order, c
     const int A = T * k;
     int me = 0, off = 0;
     if (e < E) {
-        off = offsets[e];
-        me = offsets[e + 1] - off;
+        off = ldp(offsets + e);
+        me = ldp(offsets + e + 1) - off;
         if (off < 0 || me < 0 || off > A || me > A - off) {  // inconsistent offsets: no tiles
             record_error(err, MOE_ERR_DEVICE);
             off = me = 0;

@@ -27,22 +27,23 @@ __device__ __forceinline__ int expert_of_row(const int32_t *offsets, int E, int 
     int lo = 0, hi = E;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(offsets + mid) <= p) lo = mid; else hi = mid - 1;
+        if (ldp(offsets + mid) <= p) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
 
-// 8 consecutive source values from column c (a multiple of 8) of a row.  The 4-bit path
-// stores each 8-element group of h in the order (0,4,1,5,2,6,3,7) (grouped = 1).
+// 8 consecutive source values from column c (a multiple of 8) of a row (token rows or h:
+// produced-data loads).  The 4-bit tensor-core path stores each 8-element group of h in the
+// order (0,4,1,5,2,6,3,7) (grouped = 1).
 __device__ __forceinline__ void load8(const float *row, int c, int grouped, float *v) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(row + c));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(row + c) + 1);
+    const float4 a = ldp16f(row + c);
+    const float4 b = ldp16f(row + c + 4);
     const float t[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = grouped ? t[((i & 3) << 1) | (i >> 2)] : t[i];
 }
 __device__ __forceinline__ void load8(const uint16_t *row, int c, int grouped, float *v) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(row + c));
+    const uint4 a = ldp16(row + c);
     const uint32_t w[4] = {a.x, a.y, a.z, a.w};
     float t[8];
 #pragma unroll
@@ -58,8 +59,7 @@ __device__ __forceinline__ void load8(const uint16_t *row, int c, int grouped, f
 // out[(p * slices + slice) * kNV + v] = sum over this slice's columns of src_row(p)[c] * Amat(e, v)[c].
 template <typename SrcT, int kNV>
 __global__ void __launch_bounds__(kLWarps * 32)
-lora_a_kernel(const SrcT *__restrict__ src, const int32_t *__restrict__ order, int k, int by_token, int grouped,
-              const int32_t *__restrict__ offsets, int E, int A, int len, int slice_cols,
+lora_a_kernel(const SrcT *src, const int32_t *order, int k, int by_token, int grouped, const int32_t *offsets, int E, int A, int len, int slice_cols,
               const float *__restrict__ a0, const float *__restrict__ a1, int rank, float *__restrict__ out) {
     constexpr int kVPW = kNV / kLWarps;  // rank vectors per warp
     griddep_launch_dependents();
@@ -77,7 +77,7 @@ lora_a_kernel(const SrcT *__restrict__ src, const int32_t *__restrict__ order, i
             e = expert_of_row(offsets, E, p);
             row = p;
             if (by_token) {
-                const int a = __ldg(order + p);
+                const int a = ldp(order + p);
                 row = (a >= 0 && a < A) ? a / k : -1;
             }
             if (e >= E) row = -1;
@@ -134,14 +134,14 @@ lora_a_kernel(const SrcT *__restrict__ src, const int32_t *__restrict__ order, i
 // out[p][v] = sum_{s < slices} part[p][s][v], in slice order.
 template <int kNV>
 __global__ void __launch_bounds__(256)
-lora_reduce_kernel(const float *__restrict__ part, int A, int slices, float *__restrict__ out) {
+lora_reduce_kernel(const float *part, int A, int slices, float *__restrict__ out) {
     griddep_launch_dependents();
     griddep_wait();
     const int i = blockIdx.x * 256 + threadIdx.x;
     if (i >= A * kNV) return;
     const int p = i / kNV, v = i % kNV;
     float s = 0.f;
-    for (int sl = 0; sl < slices; ++sl) s += part[((size_t)p * slices + sl) * kNV + v];
+    for (int sl = 0; sl < slices; ++sl) s += ldp(part + ((size_t)p * slices + sl) * kNV + v);
     out[i] = s;
 }
 

@@ -67,6 +67,46 @@ __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + e
 // instruction count decides how long an accumulator stays busy.
 __device__ __forceinline__ float swiglu_fast(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
+// Loads of data that an earlier kernel of the stream may have written: token rows (the
+// previous layer's output may be this layer's input), routing results, offsets, orders,
+// tile lists, intermediates.  With programmatic dependent launch a kernel starts before
+// the kernel before it has finished, so such data may be read only after griddep_wait:
+// these loads are volatile asm, which the compiler keeps after the wait (it may move a
+// read-only __ldg load above it), and read L2 (.cg), the point of coherence, never a
+// cached line that predates the writer.  Weights, scales, biases and adapters, which no
+// kernel of the library writes, are read with __ldg.
+__device__ __forceinline__ int32_t ldp(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldp(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ldp(const float *p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint16_t ldp(const uint16_t *p) {
+    unsigned short v;
+    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+// 16 bytes (16-byte aligned).
+__device__ __forceinline__ uint4 ldp16(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float4 ldp16f(const void *p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
 // Programmatic dependent launch: let the next kernel of the stream be scheduled now,
 // and wait until the previous kernel has completed and its writes are visible.
 __device__ __forceinline__ void griddep_launch_dependents() {
@@ -115,11 +155,10 @@ struct LoraDev {
 
 // scale * sum_q b[q] v[q] over a 16-float rank vector (b zero beyond the rank).
 __device__ __forceinline__ float lora_dot16(const float *b, const float *v) {
-    const float4 *v4 = reinterpret_cast<const float4 *>(v);
     float s = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const float4 a = __ldg(v4 + q);
+        const float4 a = ldp16f(v + 4 * q);  // xa / ha: written by the adapter kernels
         s = fmaf(b[4 * q], a.x, s);
         s = fmaf(b[4 * q + 1], a.y, s);
         s = fmaf(b[4 * q + 2], a.z, s);

@@ -17,7 +17,7 @@ constexpr int kThreads = 1024;
 constexpr int kSmallA = 4 * kPermuteChunk;
 
 __global__ void __launch_bounds__(kThreads)
-permute_small_kernel(const int32_t *__restrict__ ids, int A, int E, int32_t *counts, int32_t *offsets,
+permute_small_kernel(const int32_t *ids, int A, int E, int32_t *counts, int32_t *offsets,
                      int32_t *order, int32_t *pos, int32_t *active, int32_t *err) {
     __shared__ PermuteSmem<kThreads> s;
     griddep_launch_dependents();
@@ -26,7 +26,7 @@ permute_small_kernel(const int32_t *__restrict__ ids, int A, int E, int32_t *cou
 }
 
 __global__ void __launch_bounds__(kThreads)
-permute_hist_kernel(const int32_t *__restrict__ ids, int A, int E, int32_t *hist) {
+permute_hist_kernel(const int32_t *ids, int A, int E, int32_t *hist) {
     __shared__ int s_cnt[kMaxE];
     griddep_launch_dependents();
     griddep_wait();
@@ -35,7 +35,7 @@ permute_hist_kernel(const int32_t *__restrict__ ids, int A, int E, int32_t *hist
     __syncthreads();
     const int a = blockIdx.x * kThreads + tid;
     if (a < A) {
-        const int e = ids[a];
+        const int e = ldp(ids + a);
         if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
     }
     __syncthreads();
@@ -55,7 +55,7 @@ permute_scan_kernel(int nchunks, int E, int32_t *hist, int32_t *counts, int32_t 
         for (int c0 = 0; c0 < nchunks; c0 += 16) {
             int v[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = c0 + j < nchunks ? hist[(size_t)(c0 + j) * E + tid] : 0;
+            for (int j = 0; j < 16; ++j) v[j] = c0 + j < nchunks ? ldp(hist + (size_t)(c0 + j) * E + tid) : 0;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
                 if (c0 + j < nchunks) {
@@ -71,12 +71,12 @@ permute_scan_kernel(int nchunks, int E, int32_t *hist, int32_t *counts, int32_t 
 }
 
 __global__ void __launch_bounds__(kThreads)
-permute_scatter_kernel(const int32_t *__restrict__ ids, int A, int E, const int32_t *hist, int32_t *order,
+permute_scatter_kernel(const int32_t *ids, int A, int E, const int32_t *hist, int32_t *order,
                        int32_t *pos, int32_t *err) {
     __shared__ PermuteSmem<kThreads> s;
     griddep_launch_dependents();
     griddep_wait();
-    for (int i = threadIdx.x; i < E; i += kThreads) s.base[i] = hist[(size_t)blockIdx.x * E + i];
+    for (int i = threadIdx.x; i < E; i += kThreads) s.base[i] = ldp(hist + (size_t)blockIdx.x * E + i);
     __syncthreads();
     scatter_chunk<kThreads>(ids, blockIdx.x * kThreads, A, E, s, order, pos, err);
 }

@@ -77,7 +77,7 @@ __device__ void scatter_chunk(const int32_t *ids, int a0, int A, int E, PermuteS
                               int32_t *pos, int32_t *err) {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int a = a0 + tid;
-    int e = (a < A) ? __ldcg(ids + a) : -1;
+    int e = (a < A) ? ldp(ids + a) : -1;
     if (a < A && (e < 0 || e >= E)) {
         record_error(err, MOE_ERR_DEVICE);
         e = -1;
@@ -112,7 +112,7 @@ __device__ void permute_block(const int32_t *ids, int A, int E, int32_t *counts,
     for (int i = tid; i < E; i += NT) s.cnt[i] = 0;
     __syncthreads();
     for (int a = tid; a < A; a += NT) {
-        const int e = __ldcg(ids + a);
+        const int e = ldp(ids + a);
         if (e >= 0 && e < E) atomicAdd(&s.cnt[e], 1);
     }
     __syncthreads();

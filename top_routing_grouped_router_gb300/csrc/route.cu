@@ -35,8 +35,14 @@ constexpr int kFuseMaxT = 64;
 template <typename T> struct Vec;
 template <> struct Vec<float> {
     static constexpr int N = 4;
+    // weights (never written by the library)
     __device__ static void load(const float *p, float *out) {
         float4 v = __ldg(reinterpret_cast<const float4 *>(p));
+        out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+    }
+    // token rows (may be an earlier kernel's output)
+    __device__ static void load_p(const float *p, float *out) {
+        float4 v = ldp16f(p);
         out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
     }
     __device__ static void store(float *p, const float *v) {
@@ -46,8 +52,7 @@ template <> struct Vec<float> {
 };
 template <> struct Vec<uint16_t> {
     static constexpr int N = 8;
-    __device__ static void load(const uint16_t *p, float *out) {
-        uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+    __device__ static void widen(uint4 v, float *out) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -55,6 +60,8 @@ template <> struct Vec<uint16_t> {
             out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
         }
     }
+    __device__ static void load(const uint16_t *p, float *out) { widen(__ldg(reinterpret_cast<const uint4 *>(p)), out); }
+    __device__ static void load_p(const uint16_t *p, float *out) { widen(ldp16(p), out); }
     // v already bf16-representable (see round)
     __device__ static void store(uint16_t *p, const float *v) {
         uint32_t w[4];
@@ -90,7 +97,7 @@ __device__ void group_rms(const ActT *__restrict__ x, int H, float eps, int tg, 
         for (int tt = 0; tt < kTG; ++tt)
             if (tt < nt) {
                 float xv[V];
-                Vec<ActT>::load(x + (size_t)(tg + tt) * H + (size_t)c * V, xv);
+                Vec<ActT>::load_p(x + (size_t)(tg + tt) * H + (size_t)c * V, xv);
 #pragma unroll
                 for (int v = 0; v < V; ++v) ss[tt] = fmaf(xv[v], xv[v], ss[tt]);
             }
@@ -145,7 +152,7 @@ __device__ void router_block(const ActT *__restrict__ x, const ActT *__restrict_
             for (int tt = 0; tt < kTG; ++tt) {
                 if (tt < nt) {
                     float xv[V];
-                    Vec<ActT>::load(x + (size_t)(tg + tt) * H + (size_t)c * V, xv);
+                    Vec<ActT>::load_p(x + (size_t)(tg + tt) * H + (size_t)c * V, xv);
                     if (kNorm) {
                         const float rms = s_rms[tt];
 #pragma unroll
@@ -201,7 +208,7 @@ __device__ void topk_token(const float *logits, int t, int E, int k, int norm, i
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
         const int e = lane + 32 * i;
-        v[i] = (e < E) ? __ldcg(l + e) : -INFINITY;
+        v[i] = (e < E) ? ldp(l + e) : -INFINITY;
     }
     uint32_t taken = 0;
     float lmax = 0.f, my_l = 0.f, last = 0.f;
@@ -314,7 +321,7 @@ rmsnorm_kernel(const ActT *__restrict__ x, const ActT *__restrict__ gamma, float
     float ss = 0.f;
     for (int c = tid; c < H / V; c += kRThreads) {
         float xv[V];
-        Vec<ActT>::load(row + (size_t)c * V, xv);
+        Vec<ActT>::load_p(row + (size_t)c * V, xv);
 #pragma unroll
         for (int v = 0; v < V; ++v) ss = fmaf(xv[v], xv[v], ss);
     }
@@ -327,7 +334,7 @@ rmsnorm_kernel(const ActT *__restrict__ x, const ActT *__restrict__ gamma, float
     const float rms = sqrtf(tot / float(H) + eps);
     for (int c = tid; c < H / V; c += kRThreads) {
         float xv[V], gv[V];
-        Vec<ActT>::load(row + (size_t)c * V, xv);
+        Vec<ActT>::load_p(row + (size_t)c * V, xv);
         Vec<ActT>::load(gamma + (size_t)c * V, gv);
 #pragma unroll
         for (int v = 0; v < V; ++v) xv[v] = Vec<ActT>::round(__fdiv_rn(xv[v], rms) * gv[v]);

@@ -14,8 +14,8 @@ constexpr int kCols = 8;
 
 template <int kBatch, typename T>
 __global__ void __launch_bounds__(kThreads)
-unpermute_kernel(const T *__restrict__ y, const float *__restrict__ w, const int32_t *__restrict__ pos,
-                 T *__restrict__ out, int k, int H, int A, int col_blocks, const T *__restrict__ resid) {
+unpermute_kernel(const T *y, const float *w, const int32_t *pos, T *out, int k, int H, int A, int col_blocks,
+                 const T *resid) {
     griddep_launch_dependents();
     griddep_wait();
     const int t = blockIdx.x / col_blocks;

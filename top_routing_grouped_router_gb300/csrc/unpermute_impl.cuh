@@ -8,13 +8,14 @@
 
 namespace moe {
 
+// y (and the residual stream) were written by earlier kernels: produced-data loads.
 __device__ __forceinline__ void unp_load8(const float *p, float *v) {
-    const float4 a = __ldcg(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldcg(reinterpret_cast<const float4 *>(p) + 1);
+    const float4 a = ldp16f(p);
+    const float4 b = ldp16f(p + 4);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 __device__ __forceinline__ void unp_load8(const uint16_t *p, float *v) {
-    const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(p));
+    const uint4 a = ldp16(p);
     const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -51,8 +52,8 @@ __device__ __forceinline__ void unpermute8(const T *y, const float *w, const int
         float ww[kBatch];
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-            pp[j] = j0 + j < k ? __ldg(pos + (size_t)t * k + j0 + j) : -1;
-            ww[j] = j0 + j < k ? __ldg(w + (size_t)t * k + j0 + j) : 0.f;
+            pp[j] = j0 + j < k ? ldp(pos + (size_t)t * k + j0 + j) : -1;
+            ww[j] = j0 + j < k ? ldp(w + (size_t)t * k + j0 + j) : 0.f;
         }
         float v[kBatch][8];
 #pragma unroll
