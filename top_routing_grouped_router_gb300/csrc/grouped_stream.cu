@@ -98,6 +98,14 @@ struct Params {
     unsigned long long wait_ns; // limit of every bounded wait
     int extra_need;             // added to the h publications a down tile waits for (failure-path
                                 // test: a count nothing reaches, so those waits must run out)
+    // gather mode (decode batches whose tile list the routing kernel built): the epilogue
+    // warps first copy the token rows into permuted order, x_perm[p] = xsrc[order[p] / k],
+    // and the producer waits for all of them before its first token-row load
+    int gather;
+    const uint16_t *xsrc;
+    const int32_t *order;
+    uint16_t *xperm;
+    int k;
     // router mode: tiles are (row block of experts, 128-token chunk), one static sweep
     int router_tiles;           // > 0 selects router mode
     int T;
@@ -237,6 +245,32 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         const int cap_dn = min(p.dmax, (kABytes + kBBytes) / 128);
         int hnext = 0;  // TMEM half of the next one-half tile
         int fills = 0;  // stage fills issued (arrive.expect_tx + TMA) so far
+        // gather mode: until every CTA has published its share of the token rows, a gate/up
+        // stage is armed and its weight slabs loaded at once, but its token-row loads are
+        // deferred (dq); they are issued as soon as the rows are complete, or when the ring is
+        // full of deferred stages (then waiting for the rows)
+        bool xready = !p.gather;
+        const int xtarget = p.A * (p.H / 8);
+        struct Deferred {
+            uint32_t dst, bar;
+            int k0, r0, nbox, box;
+            const CUtensorMap *map;
+        } dq[kStages];
+        int ndq = 0;
+        auto rows_ready = [&]() {
+            int v;
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p.sched + kSchedXDone) : "memory");
+            return v >= xtarget;
+        };
+        auto flush = [&]() {
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // the rows' generic writes -> TMA
+            for (int i = 0; i < ndq; ++i)
+                for (int q = 0; q < dq[i].nbox; ++q)
+                    tma_load_2d(dq[i].dst + q * dq[i].box * 128, dq[i].map, dq[i].k0, dq[i].r0 + q * dq[i].box,
+                                dq[i].bar);
+            ndq = 0;
+            xready = true;
+        };
         bool live = true;
         while (live) {
             const int t = next;
@@ -259,6 +293,12 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
             }
             if (!ok) record_error(p.err, MOE_ERR_DEVICE);
             if (d.down == kDown || d.down == kLoraH) {
+                // this CTA's own deferred gate/up stages may be among those the h waits for:
+                // issue them first (the rows' gather never waits on anything)
+                if (ndq > 0) {
+                    wait_count(p.sched + kSchedXDone, xtarget, wt);
+                    flush();
+                }
                 // the expert's h must be complete: every epilogue warp of every gate/up tile
                 if (!wait_count(p.done + d.e, d.need + p.extra_need, wt)) break;
                 asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -389,10 +429,28 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 } else {
                     tma_load_2d(a0, &tm_gate, ks * kSlab, wrow, fb);
                     tma_load_2d(a0 + kABytes, &tm_up, ks * kSlab, wrow, fb);
-                    for (int q = 0; q < nbox; ++q) tma_load_2d(bb + q * box * 128, bmap, ks * kSlab, d.r0 + q * box, fb);
+                    if (xready) {
+                        for (int q = 0; q < nbox; ++q)
+                            tma_load_2d(bb + q * box * 128, bmap, ks * kSlab, d.r0 + q * box, fb);
+                    } else {
+                        dq[ndq++] = Deferred{bb, fb, ks * kSlab, d.r0, nbox, box, bmap};
+                        if (rows_ready()) {
+                            flush();
+                        } else if (ndq == kStages) {
+                            // the ring is full of stages waiting for rows; on a timeout the loads
+                            // are still issued (in bounds), so the drain below completes
+                            if (!wait_count(p.sched + kSchedXDone, xtarget, wt)) live = false;
+                            flush();
+                        }
+                    }
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
+                if (!live) break;
             }
+        }
+        if (ndq > 0) {  // deferred token rows of the last stages
+            wait_count(p.sched + kSchedXDone, xtarget, wt);
+            flush();
         }
         // no TMA write may still be landing in this CTA's shared memory when it exits: wait
         // for the last fills of the ring (all consumed already unless the CTA is aborting)
@@ -492,6 +550,30 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         const int row = 32 * q + lane;
         const int part = (warp - 2) >> 2;  // which of the quadrant's warps: they alternate over column groups
         constexpr int kParts = kEpiWarps / 4;
+        if (p.gather) {
+            // this CTA's share of the token rows (rows blockIdx.x, + gridDim.x, ...), 16 bytes
+            // per thread and step; each warp publishes the chunks it copied
+            const int et = threadIdx.x - 64, cpr = p.H / 8;
+            int copied = 0;
+            for (int pr = blockIdx.x; pr < p.A; pr += gridDim.x) {
+                const int a = ldp(p.order + pr);
+                const bool bad = a < 0 || a >= p.A;
+                if (bad && et == 0) record_error(p.err, MOE_ERR_DEVICE);
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.xsrc + (size_t)(bad ? 0 : a / p.k) * p.H);
+                uint4 *dst = reinterpret_cast<uint4 *>(p.xperm + (size_t)pr * p.H);
+                for (int c = et; c < cpr; c += kEpiWarps * 32) {
+                    dst[c] = bad ? make_uint4(0, 0, 0, 0) : ldp16(src + c);
+                    ++copied;
+                }
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const int wsum = __reduce_add_sync(0xffffffffu, copied);
+            if (lane == 0 && wsum > 0) {
+                __threadfence();
+                asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p.sched + kSchedXDone), "r"(wsum)
+                             : "memory");
+            }
+        }
         int slot = 0;
         int uses[2] = {0, 0};
         uint32_t mphase = 0;
@@ -743,6 +825,8 @@ size_t grouped_fast_part_bytes(int path, const moe_shape &s) {
     return xperm_bytes(s) + 256 + (size_t)kCountersPerExpert * kMaxE * 4 + (max_tiles(s) * 16 + 255) / 256 * 256;
 }
 
+// prep + the expert kernel (the decode path of moe_forward builds its tile list in the routing
+// kernel and skips the prep launch: see moe_forward_launches)
 int grouped_fast_launches(int path, const moe_shape &) { return path == 1 || path == 2 ? 2 : 0; }
 
 // Without adapters: prep + one launch over all tiles.  With packed LoRA adapters also one
@@ -751,18 +835,56 @@ int grouped_fast_launches(int path, const moe_shape &) { return path == 1 || pat
 // stage of each gate/up and down tile, which waits for its expert's A-side tiles.  With
 // unpacked adapters: prep, x . A^T, the gate/up tiles, h . A_down^T, the down tiles (five
 // launches; CUDA-core A side, B side in the epilogue).
+namespace {
+// The part region of the bf16 tensor-core path: x_perm, the scheduling words, the
+// per-expert counters, the tile list.
+struct TcPart {
+    uint16_t *x_perm;
+    int *sched, *done;
+    uint4 *tiles;
+};
+TcPart tc_part(const moe_shape &s, float *part) {
+    char *base = reinterpret_cast<char *>(part);
+    TcPart t;
+    t.x_perm = reinterpret_cast<uint16_t *>(base);
+    t.sched = reinterpret_cast<int *>(base + xperm_bytes(s));
+    t.done = t.sched + 64;
+    t.tiles = reinterpret_cast<uint4 *>(base + xperm_bytes(s) + 256 + (size_t)kCountersPerExpert * kMaxE * 4);
+    return t;
+}
+// Large batches (at least 128 assignments per expert on average) take gate/up tiles of up
+// to 256 tokens (both TMEM halves, three 64 KB stages): an MMA of N = 256 reads 12 KB of
+// shared memory per 128 cycles against 8 KB per 64 for N = 128, and shared memory
+// bandwidth is what bounds the tensor pipe here.  Smaller batches keep tiles of at most
+// 128 tokens and a deeper pipeline for the weight stream.
+bool tc_wide(const moe_shape &s) { return (size_t)s.T * s.k >= (size_t)kMaxN * s.E; }
+TileListArgs tc_tile_args(const moe_shape &s, int mode) {
+    const bool wide = tc_wide(s);
+    return TileListArgs{wide ? kWideN : kMaxN, wide ? 1 : 0, kMaxDownN, 1, s.I / kRows, s.H / kRows,
+                        epi_warps(mode), (int)max_tiles(s), mode == kLoraPacked ? 1 : 0};
+}
+}  // namespace
+
+bool tc_tile_build(const moe_shape &s, float *part, TileBuild *tb) {
+    if (select_grouped_path(s) != 1) return false;
+    const TcPart t = tc_part(s, part);
+    *tb = TileBuild{tc_tile_args(s, kLoraNone), t.tiles, t.sched, t.done};
+    return true;
+}
+
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
                                 const moe_q4 *q4, const int32_t *, float *part, void *h, void *y, int32_t *err,
-                                cudaStream_t st, const moe_lora *lora, float *xa, float *ha, float *lpart) {
+                                cudaStream_t st, const moe_lora *lora, float *xa, float *ha, float *lpart,
+                                bool prebuilt) {
     if (path == 2) return launch_q4(s, x, offsets, order, wg, wu, wd, q4, part, h, y, err, st, lora, xa, ha, lpart);
     if (path != 1) return cudaErrorInvalidValue;
     const int A = s.T * s.k;
-    char *base = reinterpret_cast<char *>(part);
-    uint16_t *x_perm = reinterpret_cast<uint16_t *>(base);
-    int *sched = reinterpret_cast<int *>(base + xperm_bytes(s));
-    int *done = sched + 64;
-    uint4 *tiles = reinterpret_cast<uint4 *>(base + xperm_bytes(s) + 256 + (size_t)kCountersPerExpert * kMaxE * 4);
+    const TcPart tp = tc_part(s, part);
+    uint16_t *x_perm = tp.x_perm;
+    int *sched = tp.sched;
+    int *done = tp.done;
+    uint4 *tiles = tp.tiles;
 
     Maps m;
     if (!tc::make_map(&m.g, wg, (uint64_t)s.E * s.I, s.H, kRows) ||
@@ -785,20 +907,18 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
             return cudaErrorInvalidValue;
     }
 
-    // Large batches (at least 128 assignments per expert on average) take gate/up tiles of
-    // up to 256 tokens (both TMEM halves, three 64 KB stages): an MMA of N = 256 reads
-    // 12 KB of shared memory per 128 cycles against 8 KB per 64 for N = 128, and shared
-    // memory bandwidth is what bounds the tensor pipe here.  Smaller batches keep tiles of
-    // at most 128 tokens and a deeper pipeline for the weight stream.
-    const bool wide = (size_t)A >= (size_t)kMaxN * s.E;
-    const int cmax = wide ? kWideN : kMaxN;
+    const bool wide = tc_wide(s);
     const int dmax = kMaxDownN;
     const int mode = !lora ? kLoraNone : packed ? kLoraPacked : kLoraEpi;
-    const TileListArgs ta{cmax, wide ? 1 : 0, dmax, 1, s.I / kRows, s.H / kRows, epi_warps(mode), (int)max_tiles(s),
-                          packed ? 1 : 0};
-    cudaError_t e = launch_pdl(prep_kernel, dim3(prep_blocks(A)), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
-                               offsets, s.T, s.k, s.H, s.E, ta, x_perm, tiles, sched, done, err);
-    if (e != cudaSuccess) return e;
+    // with the tile list prebuilt by the routing kernel (decode batches, no adapters) the
+    // kernel gathers the token rows itself; otherwise the prep kernel does both
+    prebuilt = prebuilt && !lora;
+    cudaError_t e = cudaSuccess;
+    if (!prebuilt) {
+        e = launch_pdl(prep_kernel, dim3(prep_blocks(A)), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
+                       offsets, s.T, s.k, s.H, s.E, tc_tile_args(s, mode), x_perm, tiles, sched, done, err);
+        if (e != cudaSuccess) return e;
+    }
 
     Params prm{};
     prm.tiles = tiles;
@@ -815,6 +935,11 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.dmax = dmax;
     prm.wait_ns = tc::wait_limit_ns();
     prm.extra_need = tc::debug_extra_need();
+    prm.gather = prebuilt ? 1 : 0;
+    prm.xsrc = static_cast<const uint16_t *>(x);
+    prm.order = order;
+    prm.xperm = x_perm;
+    prm.k = s.k;
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (!lora) return launch_tc_for<kLoraNone>(s, wide, grid, st, m, prm);

@@ -89,16 +89,6 @@ __device__ inline int scan256(int v, int *s_warp, int &total) {
     return excl;
 }
 
-struct TileListArgs {
-    int gu_cmax, gu_even;  // token chunks of the gate/up tiles: bound and policy (see chunk_base)
-    int dn_cmax, dn_even;  // token chunks of the down tiles
-    int gu_per;            // gate/up tiles per chunk (row blocks of I)
-    int dn_per;            // down tiles per chunk (row blocks of H)
-    int pub;               // h publications per gate/up tile (epilogue warps that write h)
-    int max_tiles;         // capacity of `tiles`
-    int lora;              // also LoRA A-side tiles: x . A^T before the gate/up tiles, h . A_down^T
-                           // before the down tiles, one per 128-token chunk of an expert
-};
 
 // Scheduling words next to the tile list: [0] claim counter of the gate/up (or all) tiles,
 // [1] number of tiles, [2] number of gate/up tiles (they come first), [3] claim counter
@@ -107,52 +97,25 @@ struct TileListArgs {
 // gate/up, LoRA-h, down, each with its own claim counter.
 enum : int { kSchedClaim = 0, kSchedTiles = 1, kSchedGateUp = 2, kSchedClaimDown = 3 };
 enum : int { kSchedRangeClaim = 8, kSchedBound = 12 };  // 4 claim counters, 5 bounds
+// Token-row chunks (16 bytes) of x_perm gathered so far, when the tensor-core kernel gathers
+// them itself (decode batches routed by the fused routing kernel).
+enum : int { kSchedXDone = 20 };
 constexpr int kLoraChunk = 128;  // tokens per LoRA A-side tile (the MMA's M)
 constexpr int kLoraPub = 4;      // publications per LoRA A-side tile (one epilogue warp per lane quadrant)
 // Per-expert completion counters after the scheduling words: h publications, then the
 // LoRA A-side publications of x . A^T and of h . A_down^T.
 constexpr int kCountersPerExpert = 3;
 
-// Block 0: the tile list from the offsets, the scheduling words (zeroed claim counters)
-// and zeroed per-expert completion counters (done[e], done[kMaxE + e], done[2 kMaxE + e]).  Blocks 1..: x_perm rows, one per warp
-// (kPrepRowsPerBlock per block).
-constexpr int kPrepRowsPerBlock = 8;
-__host__ __device__ constexpr int prep_blocks(int A) { return 1 + (A + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock; }
-__global__ void __launch_bounds__(256)
-prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, int T, int k, int H, int E,
-            TileListArgs ta, uint16_t *__restrict__ x_perm, uint4 *tiles,
-            int *sched, int *done, int32_t *err) {
-    griddep_launch_dependents();
-    griddep_wait();
-    if (blockIdx.x > 0) {
-        // one warp per permuted row, four 16-byte loads in flight per lane
-        const int pr = (blockIdx.x - 1) * kPrepRowsPerBlock + int(threadIdx.x >> 5);
-        const int lane = threadIdx.x & 31;
-        if (pr >= T * k) return;
-        const int a = ldp(order + pr);
-        const bool bad = a < 0 || a >= T * k;
-        if (bad && lane == 0) record_error(err, MOE_ERR_DEVICE);
-        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(bad ? 0 : a / k) * H);
-        const int n = H / 8;
-        for (int i = lane; i < n; i += 32 * 4) {
-            uint4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                v[u] = (!bad && i + 32 * u < n) ? ldp16(src + i + 32 * u) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (i + 32 * u < n) dst[i + 32 * u] = v[u];
-        }
-        return;
-    }
+// The tile list, the scheduling words (zeroed claim counters) and zeroed per-expert
+// completion counters (done[e], done[kMaxE + e], done[2 kMaxE + e]), by one block of 256
+// threads, thread e holding expert e's segment [off, off + me) of the permuted rows (off =
+// me = 0 beyond E).
+__device__ inline void build_tile_list_from(int off, int me, int T, int k, int E, const TileListArgs &ta,
+                                            uint4 *tiles, int *sched, int *done, int32_t *err) {
     __shared__ int s_warp[9];
     const int e = threadIdx.x;
     const int A = T * k;
-    int me = 0, off = 0;
     if (e < E) {
-        off = ldp(offsets + e);
-        me = ldp(offsets + e + 1) - off;
         if (off < 0 || me < 0 || off > A || me > A - off) {  // inconsistent offsets: no tiles
             record_error(err, MOE_ERR_DEVICE);
             off = me = 0;
@@ -166,10 +129,20 @@ prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, int
     const int nch_gu = n_chunks(me, ta.gu_cmax, ta.gu_even != 0);
     const int nch_dn = n_chunks(me, ta.dn_cmax, ta.dn_even != 0);
     const int nch_l = ta.lora ? (me + kLoraChunk - 1) / kLoraChunk : 0;
-    int n_gu, n_dn, n_l;
-    const int gu_off = scan256(nch_gu * ta.gu_per, s_warp, n_gu);
-    const int dn_off = scan256(nch_dn * ta.dn_per, s_warp, n_dn);
-    const int l_off = scan256(nch_l, s_warp, n_l);
+    int n_gu, n_dn, n_l = 0, l_off = 0, gu_off, dn_off;
+    if (!ta.lora && ta.max_tiles < 32768) {
+        // both counts in one scan: gate/up tiles in the low 16 bits, down tiles above
+        int tot;
+        const int x = scan256((nch_gu * ta.gu_per) | ((nch_dn * ta.dn_per) << 16), s_warp, tot);
+        gu_off = x & 0xFFFF;
+        dn_off = x >> 16;
+        n_gu = tot & 0xFFFF;
+        n_dn = tot >> 16;
+    } else {
+        gu_off = scan256(nch_gu * ta.gu_per, s_warp, n_gu);
+        dn_off = scan256(nch_dn * ta.dn_per, s_warp, n_dn);
+        l_off = scan256(nch_l, s_warp, n_l);
+    }
     // ranges: [0, n_l) LoRA-x, then gate/up, then [.., + n_l) LoRA-h, then down
     const int b1 = n_l, b2 = b1 + n_gu, b3 = b2 + n_l, b4 = b3 + n_dn;
     auto put = [&](int i, uint4 rec) {
@@ -204,7 +177,55 @@ prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, int
         sched[kSchedBound + 2] = min(b2, ta.max_tiles);
         sched[kSchedBound + 3] = min(b3, ta.max_tiles);
         sched[kSchedBound + 4] = min(b4, ta.max_tiles);
+        sched[kSchedXDone] = 0;
     }
+}
+
+// The same from the offsets in global memory (written by an earlier kernel).
+__device__ inline void build_tile_list(const int32_t *offsets, int T, int k, int E, const TileListArgs &ta,
+                                       uint4 *tiles, int *sched, int *done, int32_t *err) {
+    const int e = threadIdx.x;
+    int off = 0, me = 0;
+    if (e < E) {
+        off = ldp(offsets + e);
+        me = ldp(offsets + e + 1) - off;
+    }
+    build_tile_list_from(off, me, T, k, E, ta, tiles, sched, done, err);
+}
+
+// Block 0: the tile list (build_tile_list).  Blocks 1..: x_perm rows, one per warp
+// (kPrepRowsPerBlock per block).
+constexpr int kPrepRowsPerBlock = 8;
+__host__ __device__ constexpr int prep_blocks(int A) { return 1 + (A + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock; }
+__global__ void __launch_bounds__(256)
+prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, int T, int k, int H, int E,
+            TileListArgs ta, uint16_t *__restrict__ x_perm, uint4 *tiles, int *sched, int *done, int32_t *err) {
+    griddep_launch_dependents();
+    griddep_wait();
+    if (blockIdx.x > 0) {
+        // one warp per permuted row, eight 16-byte loads in flight per lane (a 4 KB row in
+        // one round trip)
+        const int pr = (blockIdx.x - 1) * kPrepRowsPerBlock + int(threadIdx.x >> 5);
+        const int lane = threadIdx.x & 31;
+        if (pr >= T * k) return;
+        const int a = ldp(order + pr);
+        const bool bad = a < 0 || a >= T * k;
+        if (bad && lane == 0) record_error(err, MOE_ERR_DEVICE);
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)pr * H);
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(bad ? 0 : a / k) * H);
+        const int n = H / 8;
+        for (int i = lane; i < n; i += 32 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                v[u] = (!bad && i + 32 * u < n) ? ldp16(src + i + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i + 32 * u < n) dst[i + 32 * u] = v[u];
+        }
+        return;
+    }
+    build_tile_list(offsets, T, k, E, ta, tiles, sched, done, err);
 }
 
 }  // namespace

@@ -15,7 +15,7 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
                                 const moe_q4 *q4, const int32_t *active, float *part, void *h, void *y,
                                 int32_t *err, cudaStream_t st, const moe_lora *lora = nullptr, float *xa = nullptr,
-                                float *ha = nullptr, float *lpart = nullptr);
+                                float *ha = nullptr, float *lpart = nullptr, bool prebuilt = false);
 size_t grouped_fast_part_bytes(int path, const moe_shape &s);
 int grouped_fast_launches(int path, const moe_shape &s);
 int route_launches(const moe_shape &s);
@@ -125,7 +125,7 @@ int do_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t 
 
 int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order, const void *wg,
                const void *wu, const void *wd, const moe_q4 *q4, void *y, void *ws, cudaStream_t st,
-               const moe_lora *lora = nullptr) {
+               const moe_lora *lora = nullptr, bool prebuilt = false) {
     const WsLayout L = ws_layout(s);
     float *xa = at<float>(ws, L.xa), *ha = at<float>(ws, L.ha), *lpart = at<float>(ws, L.lpart);
     int path = select_grouped_path(s);
@@ -135,7 +135,7 @@ int do_grouped(const moe_shape &s, const void *x, const int32_t *offsets, const 
     if (path > 0)
         return launch_rc(launch_grouped_fast(path, s, x, offsets, order, wg, wu, wd, q4,
                                              at<int32_t>(ws, L.active), at<float>(ws, L.part), at<void>(ws, L.h),
-                                             y, at<int32_t>(ws, L.err), st, lora, xa, ha, lpart));
+                                             y, at<int32_t>(ws, L.err), st, lora, xa, ha, lpart, prebuilt));
     return launch_rc(launch_grouped_simple(s, x, offsets, order, wg, wu, wd, q4, at<void>(ws, L.h), y, st, lora, xa,
                                            ha, lpart));
 }
@@ -212,17 +212,22 @@ int forward_impl(const moe_shape &s, const void *x, const void *w_router, const 
             *pos = at<int32_t>(workspace, L.pos);
     void *y = at<void>(workspace, L.y);
     const void *xe = gamma ? xn_dst : x;  // the experts' input
+    // decode batches on the bf16 tensor-core path: the routing kernel also builds the expert
+    // kernel's tile list, and the expert kernel gathers the token rows (no prep launch)
+    TileBuild tb{};
+    const bool prebuilt = route_fuses(s) && !lora && tc_tile_build(s, at<float>(workspace, L.part), &tb);
     if (route_fuses(s)) {
         MOE_TRY(launch_rc(launch_route_permute(s, x, w_router, b_router, at<float>(workspace, L.logits), ids, w,
                                                at<int>(workspace, kHdrArrivals), at<int32_t>(workspace, L.counts),
                                                offsets, order, pos, at<int32_t>(workspace, L.active),
-                                               at<int32_t>(workspace, L.err), st, gamma, eps, xn_dst)));
+                                               at<int32_t>(workspace, L.err), st, gamma, eps, xn_dst,
+                                               prebuilt ? &tb : nullptr)));
     } else {
         if (gamma) MOE_TRY(launch_rc(launch_rmsnorm(s, x, gamma, eps, xn_dst, st)));
         MOE_TRY(do_route(s, xe, w_router, b_router, ids, w, nullptr, nullptr, workspace, st));
         MOE_TRY(do_permute(s, ids, at<int32_t>(workspace, L.counts), offsets, order, pos, workspace, st));
     }
-    MOE_TRY(do_grouped(s, xe, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st, lora));
+    MOE_TRY(do_grouped(s, xe, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st, lora, prebuilt));
     return launch_rc(launch_unpermute(s, y, w, pos, out, st, resid));
 }
 
@@ -322,6 +327,7 @@ int moe_forward_launches(const moe_shape *shape, int32_t *launches) {
     const int path = select_grouped_path(s);  // a non-affine 4-bit codebook takes path 0 (also 2 launches)
     *launches = (route_fuses(s) ? 1 : route_launches(s) + permute_launches(s)) +
                 (path > 0 ? grouped_fast_launches(path, s) : grouped_simple_launches(s)) + 1;
+    if (route_fuses(s) && path == 1) --*launches;  // the routing kernel builds the tile list: no prep launch
     return MOE_OK;
 }
 

@@ -198,6 +198,29 @@ cudaError_t launch_lora_xa(const moe_shape &s, const void *x, const int32_t *ord
 cudaError_t launch_lora_ha(const moe_shape &s, const void *h, bool h_fp32, bool h_grouped, const int32_t *offsets,
                            const moe_lora &l, float *ha, float *part, cudaStream_t st);
 
+// Shape of the bf16 tensor-core kernel's tile list (grouped_tiles.cuh).
+struct TileListArgs {
+    int gu_cmax, gu_even;  // token chunks of the gate/up tiles: bound and policy (see chunk_base)
+    int dn_cmax, dn_even;  // token chunks of the down tiles
+    int gu_per;            // gate/up tiles per chunk (row blocks of I)
+    int dn_per;            // down tiles per chunk (row blocks of H)
+    int pub;               // h publications per gate/up tile (epilogue warps that write h)
+    int max_tiles;         // capacity of `tiles`
+    int lora;              // also LoRA A-side tiles: x . A^T before the gate/up tiles, h . A_down^T
+                           // before the down tiles, one per 128-token chunk of an expert
+};
+
+// The tile list when the fused routing kernel builds it (decode batches on the bf16
+// tensor-core path): its shape and where it goes (the grouped op's part region).
+struct TileBuild {
+    TileListArgs ta;
+    uint4 *tiles;
+    int *sched;
+    int *done;
+};
+// Fills tb for this shape (bf16 tensor-core path, no adapters); false if the path differs.
+bool tc_tile_build(const moe_shape &s, float *part, TileBuild *tb);
+
 bool route_fuses(const moe_shape &s);
 cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, const float *bias, float *logits,
                          int32_t *ids, float *w, float *margin, int *arrivals, int32_t *err, cudaStream_t st);
@@ -207,7 +230,8 @@ cudaError_t launch_router_tc(const moe_shape &s, const void *x, const void *wr, 
 cudaError_t launch_route_permute(const moe_shape &s, const void *x, const void *wr, const float *bias,
                                  float *logits, int32_t *ids, float *w, int *arrivals, int32_t *counts,
                                  int32_t *offsets, int32_t *order, int32_t *pos, int32_t *active, int32_t *err,
-                                 cudaStream_t st, const void *gamma = nullptr, float eps = 0.f, void *xn = nullptr);
+                                 cudaStream_t st, const void *gamma = nullptr, float eps = 0.f, void *xn = nullptr,
+                                 const TileBuild *tb = nullptr);
 cudaError_t launch_rmsnorm(const moe_shape &s, const void *x, const void *gamma, float eps, void *xn,
                            cudaStream_t st);
 cudaError_t launch_permute(const moe_shape &s, const int32_t *ids, int32_t *counts, int32_t *offsets,

@@ -66,7 +66,7 @@ permute_scan_kernel(int nchunks, int E, int32_t *hist, int32_t *counts, int32_t 
         s.cnt[tid] = run;
     }
     __syncthreads();
-    write_counts(s, E, counts, offsets, active);
+    write_counts(s, E, 1 << 30, counts, offsets, active);
     for (int i = tid; i < nchunks * E; i += kThreads) hist[i] += s.base[i % E];
 }
 

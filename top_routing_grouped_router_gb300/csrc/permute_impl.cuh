@@ -54,9 +54,31 @@ struct PermuteSmem {
 };
 
 // counts / offsets / active-expert list from the block's histogram s.cnt (s.base = offsets).
+// Counts below 2^16 (at most kMaxPackedA assignments) are scanned together with the
+// active flags in one pass (count in the low 16 bits, flag in the high bits).
+constexpr int kMaxPackedA = 65535;
 template <int NT>
-__device__ void write_counts(PermuteSmem<NT> &s, int E, int32_t *counts, int32_t *offsets, int32_t *active) {
+__device__ void write_counts(PermuteSmem<NT> &s, int E, int A, int32_t *counts, int32_t *offsets, int32_t *active) {
     const int tid = threadIdx.x;
+    int *slot = s.flag + kMaxE;
+    if (A <= kMaxPackedA) {
+        if (tid < E) s.flag[tid] = s.cnt[tid] | ((s.cnt[tid] > 0) << 16);
+        __syncthreads();
+        const int tot = block_excl_scan(s.flag, slot, E, s.warp);
+        if (tid < E) {
+            const int c = s.cnt[tid], x = slot[tid];
+            s.base[tid] = x & 0xFFFF;
+            counts[tid] = c;
+            offsets[tid] = x & 0xFFFF;
+            if (c > 0) active[1 + (x >> 16)] = tid;
+        }
+        if (tid == 0) {
+            offsets[E] = tot & 0xFFFF;
+            active[0] = tot >> 16;
+        }
+        __syncthreads();
+        return;
+    }
     const int total = block_excl_scan(s.cnt, s.base, E, s.warp);
     if (tid < E) {
         counts[tid] = s.cnt[tid];
@@ -65,19 +87,20 @@ __device__ void write_counts(PermuteSmem<NT> &s, int E, int32_t *counts, int32_t
     }
     if (tid == 0) offsets[E] = total;
     __syncthreads();
-    int *slot = s.flag + kMaxE;
     const int n_active = block_excl_scan(s.flag, slot, E, s.warp);
     if (tid < E && s.flag[tid]) active[1 + slot[tid]] = tid;
     if (tid == 0) active[0] = n_active;
 }
 
-// Scatter the chunk [a0, a0 + NT) given per-expert bases s.base (advanced in place).
+// Scatter the chunk [a0, a0 + NT) given per-expert bases s.base (advanced in place); e_in is
+// this thread's id (ids[a0 + tid]), or kLoadId to load it here.
+constexpr int kLoadId = -2;
 template <int NT>
 __device__ void scatter_chunk(const int32_t *ids, int a0, int A, int E, PermuteSmem<NT> &s, int32_t *order,
-                              int32_t *pos, int32_t *err) {
+                              int32_t *pos, int32_t *err, int e_in = kLoadId) {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int a = a0 + tid;
-    int e = (a < A) ? ldp(ids + a) : -1;
+    int e = (a < A) ? (e_in == kLoadId ? ldp(ids + a) : e_in) : -1;
     if (a < A && (e < 0 || e >= E)) {
         record_error(err, MOE_ERR_DEVICE);
         e = -1;
@@ -110,14 +133,17 @@ __device__ void permute_block(const int32_t *ids, int A, int E, int32_t *counts,
                               int32_t *pos, int32_t *active, int32_t *err, PermuteSmem<NT> &s) {
     const int tid = threadIdx.x;
     for (int i = tid; i < E; i += NT) s.cnt[i] = 0;
+    // the ids of the first two chunks stay in registers for the scatter
+    const int e0 = tid < A ? ldp(ids + tid) : -1, e1 = NT + tid < A ? ldp(ids + NT + tid) : -1;
     __syncthreads();
     for (int a = tid; a < A; a += NT) {
-        const int e = ldp(ids + a);
+        const int e = a < NT ? e0 : a < 2 * NT ? e1 : ldp(ids + a);
         if (e >= 0 && e < E) atomicAdd(&s.cnt[e], 1);
     }
     __syncthreads();
-    write_counts(s, E, counts, offsets, active);
-    for (int a0 = 0; a0 < A; a0 += NT) scatter_chunk(ids, a0, A, E, s, order, pos, err);
+    write_counts(s, E, A, counts, offsets, active);
+    for (int a0 = 0; a0 < A; a0 += NT)
+        scatter_chunk(ids, a0, A, E, s, order, pos, err, a0 == 0 ? e0 : a0 == NT ? e1 : kLoadId);
 }
 
 }  // namespace moe

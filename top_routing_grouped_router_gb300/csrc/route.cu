@@ -20,6 +20,7 @@
 // group to finish -- atomic arrival counters in the workspace header, reset by the
 // blocks that consume them -- saving two launches.
 #include "moe_internal.cuh"
+#include "grouped_tiles.cuh"
 #include "permute_impl.cuh"
 
 namespace moe {
@@ -166,13 +167,26 @@ __device__ void router_block(const ActT *__restrict__ x, const ActT *__restrict_
                 }
             }
         }
+        // reduce-scatter of the 32 sums over the warp: at each halving step a lane keeps one
+        // half of the values (by its lane bit) and adds the partner's copy of that half, so
+        // lane l ends with the warp's sum of value l (31 shuffles instead of 32 x 5)
+        static_assert(kEPB * kTG == 32, "one value per lane");
+        float v[32];
 #pragma unroll
         for (int ee = 0; ee < kEPB; ++ee)
 #pragma unroll
-            for (int tt = 0; tt < kTG; ++tt) {
-                const float s = warp_sum(acc[ee][tt]);
-                if (lane == 0) s_part[w][ee * kTG + tt] = s;
+            for (int tt = 0; tt < kTG; ++tt) v[ee * kTG + tt] = acc[ee][tt];
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < m; ++i) {
+                const float send = upper ? v[i] : v[i + m];
+                const float keep = upper ? v[i + m] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
             }
+        }
+        s_part[w][lane] = v[0];
         __syncthreads();
         if (tid < kEPB * kTG) {
             const int ee = tid / kTG, tt = tid % kTG;
@@ -260,6 +274,8 @@ struct RouteArgs {
     int fuse;                 // 0: logits only, 1: + top-k, 2: + top-k + permutation
     int32_t *counts, *offsets, *order, *pos, *active, *err;
     NormArgs norm_in;         // optional pre-router RMSNorm of x
+    int build;                // with fuse 2: also the expert kernel's tile list (tb)
+    TileBuild tb;
 };
 
 template <typename ActT, bool kNorm>
@@ -269,6 +285,19 @@ route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const floa
     __shared__ float s_rms[kTG];
     __shared__ int s_last;
     griddep_launch_dependents();
+    {
+        // bring this thread's router-weight and token chunks into L2 while the previous
+        // kernel finishes (a prefetch is safe even for data that kernel is still writing:
+        // L2 is the point of coherence, and the loads come after the wait)
+        constexpr int V = Vec<ActT>::N;
+        const int e0 = blockIdx.x * kEPB, t0 = blockIdx.y * kTPB;
+        for (int c = threadIdx.x; c < a.H / V; c += kRThreads) {
+            for (int ee = 0; ee < kEPB && e0 + ee < a.E; ++ee)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(wr + (size_t)(e0 + ee) * a.H + (size_t)c * V));
+            for (int tt = 0; tt < kTPB && t0 + tt < a.T; ++tt)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(x + (size_t)(t0 + tt) * a.H + (size_t)c * V));
+        }
+    }
     griddep_wait();  // the previous kernel in the stream may still read this workspace
     router_block<ActT, kNorm>(x, wr, bias, a.logits, a.T, a.H, a.E, blockIdx.x * kEPB, blockIdx.y * kTPB, s_part,
                               a.norm_in, s_rms);
@@ -297,6 +326,12 @@ route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const floa
     if (threadIdx.x == 0) *a.arrivals = 0;
     __shared__ PermuteSmem<kRThreads> ps;
     permute_block<kRThreads>(a.ids, a.T * a.k, a.E, a.counts, a.offsets, a.order, a.pos, a.active, a.err, ps);
+    if (!a.build) return;
+    // the tensor-core expert kernel's tile list from this block's counts (after the scatter
+    // ps.base[e] = offsets[e] + counts[e])
+    const int e = threadIdx.x;
+    const int me = e < a.E ? ps.cnt[e] : 0, off = e < a.E ? ps.base[e] - me : 0;
+    build_tile_list_from(off, me, a.T, a.k, a.E, a.tb.ta, a.tb.tiles, a.tb.sched, a.tb.done, a.err);
 }
 
 __global__ void __launch_bounds__(128)
@@ -367,7 +402,8 @@ cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, cons
                          int32_t *ids, float *w, float *margin, int *arrivals, int32_t *err, cudaStream_t st) {
     if (s.T == 0) return cudaSuccess;
     RouteArgs a{logits, s.T, s.H, s.E, s.k, s.norm_topk, ids, w, margin, arrivals, route_fuses(s) ? 1 : 0,
-                nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, NormArgs{nullptr, 0.f, nullptr}};
+                nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, NormArgs{nullptr, 0.f, nullptr}, 0,
+                TileBuild{}};
     // large bf16 batches: the router GEMM on the tensor cores, then a top-k launch
     cudaError_t e = (!a.fuse && router_tc_supported(s)) ? launch_router_tc(s, x, wr, bias, logits, err, st)
                                                        : launch_route_kernel(s, x, wr, bias, a, st);
@@ -380,9 +416,10 @@ cudaError_t launch_route(const moe_shape &s, const void *x, const void *wr, cons
 cudaError_t launch_route_permute(const moe_shape &s, const void *x, const void *wr, const float *bias,
                                  float *logits, int32_t *ids, float *w, int *arrivals, int32_t *counts,
                                  int32_t *offsets, int32_t *order, int32_t *pos, int32_t *active, int32_t *err,
-                                 cudaStream_t st, const void *gamma, float eps, void *xn) {
+                                 cudaStream_t st, const void *gamma, float eps, void *xn, const TileBuild *tb) {
     RouteArgs a{logits, s.T, s.H, s.E, s.k, s.norm_topk, ids, w, nullptr, arrivals, 2,
-                counts, offsets, order, pos, active, err, NormArgs{gamma, eps, xn}};
+                counts, offsets, order, pos, active, err, NormArgs{gamma, eps, xn}, tb ? 1 : 0,
+                tb ? *tb : TileBuild{}};
     return launch_route_kernel(s, x, wr, bias, a, st);
 }
 
