@@ -1,6 +1,7 @@
 // grouped_q4.cu -- grouped SwiGLU experts with 4-bit codebook weights on the tensor
-// cores, for decode batches (an expert's tokens in one tile of <= 64) and large batches
-// (an expert's tokens in chunks of 128).
+// cores: q4_decode_kernel for decode batches (an expert's tokens in chunks of <= 32; see
+// its own comment below) and q4_swiglu_kernel for large batches (chunks of 128), which the
+// rest of this header describes.
 //
 // Weight format: element (e, r, c) of a [rows][in] matrix is codebook[code] * scale,
 // code = nibble c of row r (element 2i low, 2i+1 high nibble of byte i), one bf16
@@ -81,6 +82,9 @@ struct Params {
     const uint16_t *gs, *us, *ds;   // bf16 block scales
     float half_b;                   // b / 2
     uint32_t centre2;               // bf16x2 of 128 + 2*j0
+    float b, cc;                    // decode kernel: codebook step b and 128 + j0
+    const float *sx;                // decode kernel: block sums of the token rows [A][sx_stride(H)]
+    float *sh;                      // decode kernel: block sums of h, two halves [A][sh_stride(I)]
     int E, H, I, A;
     int cmax;                       // token chunk (fixed chunks of cmax, see chunk_base)
     unsigned long long wait_ns;     // limit of every bounded wait
@@ -136,7 +140,9 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
     constexpr int kRawBytes = QCfg<MaxN, kRawStages>::kRawBytes;
     constexpr int kHalfTok = (MaxN / 2) * 128;  // second token half of a two-slab down stage
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned by pointer arithmetic on the shared array, so that the compiler keeps
+    // the shared address space (and emits shared, not generic, loads) for everything derived
+    uint8_t *smem = smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
     uint8_t *raw = smem;
     uint8_t *aring = smem + kRawStages * kRawBytes;
     uint8_t *sbuf = aring + kAStages * kAStageBytes;        // [2][kScaleBytes] per-tile block scales
@@ -155,7 +161,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
     int *rmeta = reinterpret_cast<int *>(drain + 1);        // [kRawStages][8]
     int *tmeta = rmeta + 8 * kRawStages;                    // [kMetaRing][8]
     volatile int *abort = tmeta + 8 * kMetaRing;
-    const Waits wt{p.err, abort, p.wait_ns};
+    const Waits wt{p.err, abort, p.wait_ns, smem_u32(const_cast<int *>(abort))};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmeta + 8 * kMetaRing + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -506,13 +512,508 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
     }
 }
 
+// ---------------------------------------------------------------- decode kernel
+// Decode batches (an expert's tokens in chunks of at most kDN): the codes reach the tensor
+// core through TMEM, and the block scales are applied after the MMA.
+//  * The dequant warps turn each code j into the integer 128 + j, exact in bf16 and one
+//    LOP3 per pair of codes (after a shift for three of the four nibble positions), and
+//    store the stage's slabs into a TMEM ring (tcgen05.st).
+//  * The MMA (A from TMEM, B = the token rows in shared memory) forms each 64-element
+//    block's partial P[row][t] = sum_k (128 + j_k) x[t][k] in a fresh accumulator of a
+//    TMEM ring.
+//  * The consumer warps add the block's term s[row][blk] b (P[row][t] - (128 + j0) S[t][blk])
+//    -- which is sum_k c_{j_k} s x[t][k], since c_j = b (j - j0) -- to fp32 registers, with
+//    S[t][blk] the sum of the block's token values: formed for the token rows by the prep
+//    kernel and, for h, from the rounded h values the gate/up consumers store (two
+//    32-row halves per block, added in a fixed order).
+// Per 8 weights the dequant costs 7 integer operations instead of 16, and the scales cost
+// two fp32 operations per (row, token, block) instead of one bf16 multiply per weight.
+// A stage is 128 input elements (two blocks) of a tile's 128 rows, of both gate and up on a
+// gate/up tile: every role synchronises once per stage, so the longer stage halves that
+// cost per code byte.
+constexpr int kDN = 32;                              // token chunk (MMA N <= 32)
+constexpr int kDK = 2 * kSlab;                       // input elements per stage
+constexpr int kDCodeBytes = kRows * kDK / 2;         // 8 KB: one matrix's codes of a stage
+constexpr int kDTok = 2 * kDCodeBytes;               // token rows after the gate and up codes
+constexpr int kDTokSlab = kDN * 128;                 // token rows of one 64-element slab (SW128)
+constexpr int kDRawBytes = kDTok + 2 * kDTokSlab;    // 24 KB
+constexpr int kDRawStages = 7;
+constexpr int kDAS = 2;                              // TMEM A-ring stages
+constexpr int kDPS = 2;                              // TMEM partial-ring entries
+constexpr int kDPartCols = 128;                      // a stage's partials: block h at 64 h (gate +0, up +32)
+constexpr int kDACol = kDPS * kDPartCols;            // first A-ring column
+constexpr int kDAStageCols = 128;                    // gate slabs +0, +32; up slabs +64, +96
+constexpr int kDCons = 4;                            // consumer warps: one per lane quadrant
+constexpr int kDDeq = 4;                             // dequant warps: one per lane quadrant
+constexpr int kDThreads = (2 + kDCons + kDDeq) * 32;
+constexpr int kDSBytes = 8192;                       // a tile's block sums: <= 32 rows x 256 B
+constexpr int kDSide = kScaleBytes + kDSBytes;       // per-tile side buffer: scales, then block sums
+constexpr int kDSmemBytes = kDRawStages * kDRawBytes + 2 * kDSide + 1024 + 2048;
+static_assert(kDSmemBytes <= 232448, "shared memory");
+static_assert(kDACol + kDAS * kDAStageCols <= kTmemCols, "TMEM columns");
+// Row strides (floats) of the block-sum arrays, padded to 16 bytes so that every bulk copy of
+// consecutive rows starts and ends on a 16-byte boundary: token rows H/64 sums, h rows
+// I/64 blocks x 2 halves.
+__host__ __device__ constexpr int sx_stride(int H) { return (H / kSlab + 3) & ~3; }
+__host__ __device__ constexpr int sh_stride(int I) { return (2 * (I / kSlab) + 3) & ~3; }
+
+// 32 codes (16 bytes) -> the 16 bf16 pairs (128 + j) in the MMA's K order (per 8-element
+// group: (0,4), (1,5), (2,6), (3,7)).
+__device__ __forceinline__ void codes_to_ints(const uint4 cw, uint32_t *v) {
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w = words[i];
+        v[4 * i + 0] = (w & 0x000F000Fu) | 0x43004300u;
+        v[4 * i + 1] = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
+        v[4 * i + 2] = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
+        v[4 * i + 3] = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
+    }
+}
+
+// One 64-element slab of this thread's row: 32 bytes of codes at `cb` -> 32 TMEM columns.
+__device__ __forceinline__ void slab_to_tmem(uint32_t cb, uint32_t taddr) {
+    const uint4 c0 = lds_v4(cb), c1 = lds_v4(cb + 16);
+    uint32_t v[32];
+    codes_to_ints(c0, v);
+    codes_to_ints(c1, v + 16);
+    tmem_st32(taddr, v);
+}
+
+// Two loads of 16 fp32 columns of this thread's lane, one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float *a, float *b) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta), "r"(tb)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        a[i] = __uint_as_float(r[i]);
+        b[i] = __uint_as_float(r[16 + i]);
+    }
+}
+
+template <bool kLora>
+__global__ void __launch_bounds__(kDThreads, 1)
+q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constant__ CUtensorMap tm_uc,
+                 const __grid_constant__ CUtensorMap tm_dc, const __grid_constant__ CUtensorMap tm_x,
+                 const __grid_constant__ CUtensorMap tm_h, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned by pointer arithmetic on the shared array, so that the compiler keeps
+    // the shared address space (and emits shared, not generic, loads) for everything derived
+    uint8_t *smem = smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
+    uint8_t *raw = smem;
+    uint8_t *side = smem + kDRawStages * kDRawBytes;        // [2][kDSide]
+    uint8_t *ctrl = side + 2 * kDSide;
+    uint64_t *rfull = reinterpret_cast<uint64_t *>(ctrl);   // [kDRawStages]
+    uint64_t *rempty = rfull + kDRawStages;                 // [kDRawStages]
+    uint64_t *afull = rempty + kDRawStages;                 // [kDAS]
+    uint64_t *aempty = afull + kDAS;                        // [kDAS]
+    uint64_t *pfull = aempty + kDAS;                        // [kDPS]
+    uint64_t *pempty = pfull + kDPS;                        // [kDPS]
+    uint64_t *tmf = pempty + kDPS;                          // [kMetaRing]
+    uint64_t *tme = tmf + kMetaRing;                        // [kMetaRing]
+    uint64_t *sfull = tme + kMetaRing;                      // [2]
+    uint64_t *sempty = sfull + 2;                           // [2]
+    uint64_t *drain = sempty + 2;                           // [1]
+    int *rmeta = reinterpret_cast<int *>(drain + 1);        // [kDRawStages][4]
+    int *tmeta = rmeta + 4 * kDRawStages;                   // [kMetaRing][8]
+    volatile int *abort = tmeta + 8 * kMetaRing;
+    const Waits wt{p.err, abort, p.wait_ns, smem_u32(const_cast<int *>(abort))};
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmeta + 8 * kMetaRing + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kDRawStages; ++s) {
+            mbar_init(smem_u32(&rfull[s]), 1);
+            mbar_init(smem_u32(&rempty[s]), 1);
+        }
+        for (int s = 0; s < kDAS; ++s) {
+            mbar_init(smem_u32(&afull[s]), kDDeq);
+            mbar_init(smem_u32(&aempty[s]), 1);
+        }
+        for (int s = 0; s < kDPS; ++s) {
+            mbar_init(smem_u32(&pfull[s]), 1);
+            mbar_init(smem_u32(&pempty[s]), kDCons);
+        }
+        for (int s = 0; s < kMetaRing; ++s) {
+            mbar_init(smem_u32(&tmf[s]), 1);
+            mbar_init(smem_u32(&tme[s]), kDCons);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&sfull[b]), 1);
+            mbar_init(smem_u32(&sempty[b]), kDCons);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "n"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    griddep_launch_dependents();
+    griddep_wait();
+    const uint32_t tmem_base = *tmem_slot;
+    const int nblk_h = p.H / kSlab, nblk_i = p.I / kSlab;
+    const int sxs = sx_stride(p.H), shs = sh_stride(p.I);
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int r = 0, slot = 0, tiles_done = 0, rfills = 0;
+        uint32_t rp = 0, mphase = 0;
+        bool live = true;
+        int lo = 0, hi = ldp(p.sched + kSchedTiles);
+        int *ctr = p.sched + kSchedClaim;
+        if (p.phase == kPhaseGateUp) hi = ldp(p.sched + kSchedGateUp);
+        if (p.phase == kPhaseDown) {
+            lo = ldp(p.sched + kSchedGateUp);
+            ctr = p.sched + kSchedClaimDown;
+        }
+        int next = lo + atomicAdd(ctr, 1);
+        while (live) {
+            const int t = next;
+            if (t >= hi || abort_raised(wt)) break;
+            next = lo + atomicAdd(ctr, 1);
+            const uint32_t entry = ldp(p.tiles + t);
+            const int down = int(entry >> 31), e0 = int((entry >> 16) & 0xFF), rb = int((entry >> 8) & 0xFF);
+            const int nc = int(entry & 0xFF);
+            const int e = min(e0, p.E - 1);
+            const int off = ldp(p.offsets + e);
+            const int me = ldp(p.offsets + e + 1) - off;
+            const int base = chunk_base(me, kDN, false);
+            int m = min(base, me - nc * base);
+            if (e0 >= p.E || off < 0 || me <= 0 || off + me > p.A || m <= 0 || m > kDN) {
+                record_error(p.err, MOE_ERR_DEVICE);
+                m = 0;
+            }
+            const int r0 = m > 0 ? off + nc * base : 0;
+            const int N = m > 0 ? (m + 15) & ~15 : 16;
+            if (down) {
+                const int need = (p.I / kRows) * n_chunks(me, kDN, false) * kDCons;
+                if (!wait_count(p.done + e, need + p.extra_need, wt)) break;
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            const int nblk = down ? nblk_i : nblk_h;
+            const int nstage = nblk / 2;
+            if (!mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, wt)) break;
+            int *tm = tmeta + 8 * slot;
+            tm[0] = down;
+            tm[1] = e;
+            tm[2] = rb;
+            tm[3] = r0;
+            tm[4] = m;
+            tm[5] = N;
+            tm[6] = nstage;
+            mbar_arrive(smem_u32(&tmf[slot]));
+            if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
+            {
+                // the tile's block scales (128 consecutive rows x nblk bf16, contiguous) and its
+                // tokens' block sums (m consecutive rows)
+                const int sb = tiles_done & 1;
+                if (!mbar_wait(smem_u32(&sempty[sb]), ((tiles_done >> 1) & 1) ^ 1, wt)) break;
+                const uint32_t sfb = smem_u32(&sfull[sb]);
+                const uint32_t sbytes = uint32_t(kRows * nblk * 2);
+                const uint32_t ssum = uint32_t(m * (down ? shs : sxs) * 4);  // <= kDSBytes
+                const size_t row0 = (size_t)e * (down ? p.H : p.I) + (size_t)rb * kRows;
+                const uint32_t dst = smem_u32(side + sb * kDSide);
+                mbar_arrive_expect_tx(sfb, (down ? sbytes : 2 * sbytes) + ssum);
+                if (down) {
+                    bulk_load(dst, p.ds + row0 * nblk, sbytes, sfb);
+                } else {
+                    bulk_load(dst, p.gs + row0 * nblk, sbytes, sfb);
+                    bulk_load(dst + kScaleBytes / 2, p.us + row0 * nblk, sbytes, sfb);
+                }
+                if (ssum > 0)
+                    bulk_load(dst + kScaleBytes, down ? p.sh + (size_t)r0 * shs : p.sx + (size_t)r0 * sxs, ssum, sfb);
+                ++tiles_done;
+            }
+            const int nbox = N / kNBox;
+            const uint32_t bytes = (down ? 1 : 2) * kDCodeBytes + 2 * nbox * kNBox * 128;
+            const int wrow = e * (down ? p.H : p.I) + rb * kRows;
+            const CUtensorMap *tokmap = down ? &tm_h : &tm_x;
+            for (int ks = 0; ks < nstage; ++ks) {
+                if (!mbar_wait(smem_u32(&rempty[r]), rp ^ 1, wt)) {
+                    live = false;
+                    break;
+                }
+                int *mt = rmeta + 4 * r;
+                mt[0] = down;
+                mt[1] = ks;
+                mt[2] = N;
+                const uint32_t fb = smem_u32(&rfull[r]);
+                mbar_arrive_expect_tx(fb, bytes);
+                ++rfills;
+                const uint32_t base = smem_u32(raw + r * kDRawBytes);
+                tma_load_2d(base, down ? &tm_dc : &tm_gc, ks * (kDK / 2), wrow, fb);
+                if (!down) tma_load_2d(base + kDCodeBytes, &tm_uc, ks * (kDK / 2), wrow, fb);
+                for (int h2 = 0; h2 < 2; ++h2)
+                    for (int q = 0; q < nbox; ++q)
+                        tma_load_2d(base + kDTok + h2 * kDTokSlab + q * 2048, tokmap, (2 * ks + h2) * kSlab,
+                                    r0 + q * kNBox, fb);
+                if (++r == kDRawStages) { r = 0; rp ^= 1; }
+            }
+        }
+        // no TMA or bulk write may still be landing in this CTA's shared memory when it exits
+        for (int i = max(0, rfills - kDRawStages); i < rfills; ++i)
+            mbar_wait_drain(smem_u32(&rfull[i % kDRawStages]), uint32_t((i / kDRawStages) & 1), wt);
+        for (int i = max(0, tiles_done - 2); i < tiles_done; ++i)
+            mbar_wait_drain(smem_u32(&sfull[i & 1]), uint32_t((i >> 1) & 1), wt);
+        // sentinels (an aborting CTA's roles leave on the abort flag instead)
+        if (mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, wt)) {
+            tmeta[8 * slot] = -1;
+            mbar_arrive(smem_u32(&tmf[slot]));
+        }
+        if (mbar_wait(smem_u32(&rempty[r]), rp ^ 1, wt)) {
+            rmeta[4 * r + 1] = -1;
+            mbar_arrive(smem_u32(&rfull[r]));
+        }
+    } else if (warp >= 2 + kDCons) {
+        // ------------------------------------------------ dequant into TMEM
+        // Warp w writes TMEM lanes 32 (w % 4) .. + 31: the 32 rows of its lane quadrant.
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const uint32_t tlane = tmem_base + (uint32_t(32 * q) << 16);
+        int r = 0, a = 0;
+        uint32_t rp = 0, ap = 0;
+        for (;;) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&rfull[r]), rp, wt))) break;
+            const uint32_t mt = smem_u32(rmeta + 4 * r);
+            const int down = int(lds_u32(mt)), ks = int(lds_u32(mt + 4));
+            const bool ok = mbar_wait(smem_u32(&aempty[a]), ap ^ 1, wt);
+            tc_fence_after();
+            if (__all_sync(0xffffffffu, ok && ks >= 0 && !abort_raised(wt))) {
+                // a row's codes of a stage are 64 bytes: two slabs of 32
+                const uint32_t cb = smem_u32(raw + r * kDRawBytes) + uint32_t(row * (kDK / 2));
+                const uint32_t ta = tlane + uint32_t(kDACol + a * kDAStageCols);
+                slab_to_tmem(cb, ta);
+                slab_to_tmem(cb + 32, ta + 32);
+                if (!down) {
+                    slab_to_tmem(cb + kDCodeBytes, ta + 64);
+                    slab_to_tmem(cb + kDCodeBytes + 32, ta + 96);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&afull[a]));
+            if (++r == kDRawStages) { r = 0; rp ^= 1; }
+            if (++a == kDAS) { a = 0; ap ^= 1; }
+            if (ks < 0 || abort_raised(wt)) break;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (converged warp, elected lane)
+        int r = 0, a = 0, pb = 0;
+        uint32_t ap = 0, pp = 0;
+        for (;;) {
+            const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&afull[a]), ap, wt));
+            const int *mt = rmeta + 4 * r;
+            const int down = mt[0], ks = mt[1], N = mt[2];
+            if (__any_sync(0xffffffffu, !got || ks < 0 || abort_raised(wt))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&pempty[pb]), pp ^ 1, wt))) break;
+            tc_fence_after();
+            const uint32_t d = tmem_base + uint32_t(pb * kDPartCols);
+            const uint32_t ta = tmem_base + uint32_t(kDACol + a * kDAStageCols);
+            const uint32_t idesc = instr_desc(kRows, N);
+            // the stage's B descriptors differ from the first only in the start-address field
+            // (address / 16, 14 bits: shared memory stays below 256 KB, so adding cannot carry)
+            const uint64_t b0 = smem_desc(smem_u32(raw + r * kDRawBytes) + kDTok);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                for (int kk = 0; kk < kSlab / 16; ++kk) {
+                    const uint64_t bdesc = b0 + uint64_t((h2 * kDTokSlab + kk * 32) >> 4);
+                    mma_bf16_tmem_warp(d + h2 * 64, ta + h2 * 32 + kk * 8, bdesc, idesc, kk != 0);
+                    if (!down) mma_bf16_tmem_warp(d + h2 * 64 + 32, ta + 64 + h2 * 32 + kk * 8, bdesc, idesc, kk != 0);
+                }
+            mma_commit_warp(smem_u32(&aempty[a]));
+            mma_commit_warp(smem_u32(&rempty[r]));
+            mma_commit_warp(smem_u32(&pfull[pb]));
+            if (++r == kDRawStages) r = 0;
+            if (++a == kDAS) { a = 0; ap ^= 1; }
+            if (++pb == kDPS) { pb = 0; pp ^= 1; }
+        }
+        // every MMA this warp issued has completed before TMEM is released
+        mma_commit_warp(smem_u32(drain));
+        mbar_wait_drain(smem_u32(drain), 0, wt);
+    } else if (warp >= 2) {
+        // ------------------------------------------------ consumers
+        // One warp per lane quadrant (its 32 rows), the tile's tokens in two halves of 16.
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const float cc = p.cc, bstep = p.b;
+        int slot = 0, tiles = 0, pb = 0;
+        uint32_t mphase = 0, pp = 0;
+        bool live = true;
+        while (live) {
+            if (!mbar_wait(smem_u32(&tmf[slot]), mphase, wt)) break;
+            const int *tm = tmeta + 8 * slot;
+            const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], N = tm[5], nstage = tm[6];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tme[slot]));
+            if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
+            if (down < 0 || abort_raised(wt)) break;
+            const int sb = tiles & 1;
+            if (!mbar_wait(smem_u32(&sfull[sb]), (tiles >> 1) & 1, wt)) break;
+            const uint8_t *sd = side + sb * kDSide;
+            const uint16_t *sc_a = reinterpret_cast<const uint16_t *>(sd);                    // gate / down
+            const uint16_t *sc_u = reinterpret_cast<const uint16_t *>(sd + kScaleBytes / 2);  // up
+            const float *bs = reinterpret_cast<const float *>(sd + kScaleBytes);              // block sums
+            const int nblk = down ? nblk_i : nblk_h;
+            float acc0[32], acc1[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) acc0[t] = acc1[t] = 0.f;
+            for (int ks = 0; ks < nstage; ++ks) {
+                if (!mbar_wait(smem_u32(&pfull[pb]), pp, wt)) {
+                    live = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ta = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(pb * kDPartCols);
+                if (!down) {
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int blk = 2 * ks + h2;
+                        const float gg = bf16_bits_to_f32(sc_a[row * nblk + blk]) * bstep;
+                        const float gu = bf16_bits_to_f32(sc_u[row * nblk + blk]) * bstep;
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            if (hf * 16 >= N) break;  // warp-uniform
+                            float v0[16], v1[16];
+                            tmem_ld16x2(ta + h2 * 64 + hf * 16, ta + h2 * 64 + 32 + hf * 16, v0, v1);
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) {
+                                const float cs = cc * bs[(hf * 16 + t) * sxs + blk];
+                                acc0[hf * 16 + t] = fmaf(gg, v0[t] - cs, acc0[hf * 16 + t]);
+                                acc1[hf * 16 + t] = fmaf(gu, v1[t] - cs, acc1[hf * 16 + t]);
+                            }
+                        }
+                    }
+                } else {
+                    const int blk = 2 * ks;
+                    const float g0 = bf16_bits_to_f32(sc_a[row * nblk + blk]) * bstep;
+                    const float g1 = bf16_bits_to_f32(sc_a[row * nblk + blk + 1]) * bstep;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        if (hf * 16 >= N) break;  // warp-uniform
+                        float v0[16], v1[16];
+                        tmem_ld16x2(ta + hf * 16, ta + 64 + hf * 16, v0, v1);  // blocks 2 ks and 2 ks + 1
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const float *s2 = bs + (hf * 16 + t) * shs + blk * 2;
+                            float a0 = fmaf(g0, v0[t] - cc * (s2[0] + s2[1]), acc0[hf * 16 + t]);
+                            acc0[hf * 16 + t] = fmaf(g1, v1[t] - cc * (s2[2] + s2[3]), a0);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&pempty[pb]));
+                if (++pb == kDPS) { pb = 0; pp ^= 1; }
+            }
+            if (!live) break;
+            // the tile's scales and block sums are no longer needed
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sempty[sb]));
+            ++tiles;
+            const int col = rb * kRows + row;
+            const LoraDev &lr = p.lora;
+            const bool lora = kLora && lr.rank > 0;
+            float lb0[16], lb1[16];
+            if (lora) {
+                if (down) {
+                    lora_row16(lr.bd, (size_t)e * p.H + col, lr.rank, lb0);
+                } else {
+                    lora_row16(lr.bg, (size_t)e * p.I + col, lr.rank, lb0);
+                    lora_row16(lr.bu, (size_t)e * p.I + col, lr.rank, lb1);
+                }
+            }
+            if (down) {
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    if (t < m) {
+                        const size_t pr = (size_t)(r0 + t);
+                        float val = acc0[t];
+                        if (lora) val += lr.scale * lora_dot16(lb0, lr.ha + pr * 16);
+                        p.y[pr * p.H + col] = f32_to_bf16_bits(val);
+                    }
+            } else {
+                // h is stored in the weights' 8-element group order (see the file comment); its
+                // sums over this warp's 32 rows (half of a 64-row block) go to sh[token][block][half]
+                const int hcol = (col & ~7) | sigma_inv(col & 7);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    float hv = 0.f;
+                    if (t < m) {
+                        const size_t pr = (size_t)(r0 + t);
+                        float gv = acc0[t], uv = acc1[t];
+                        if (lora) {
+                            gv += lr.scale * lora_dot16(lb0, lr.xa + pr * 32);
+                            uv += lr.scale * lora_dot16(lb1, lr.xa + pr * 32 + 16);
+                        }
+                        const uint16_t hb = f32_to_bf16_bits(swiglu(gv, uv));
+                        p.h[pr * p.I + hcol] = hb;
+                        hv = bf16_bits_to_f32(hb);
+                    }
+                    acc0[t] = hv;
+                }
+                // reduce-scatter over the warp: lane l ends with the sum over the 32 rows of token l
+#pragma unroll
+                for (int w2 = 16; w2 >= 1; w2 >>= 1) {
+                    const bool upper = (lane & w2) != 0;
+#pragma unroll
+                    for (int i = 0; i < w2; ++i) {
+                        const float send = upper ? acc0[i] : acc0[i + w2];
+                        const float keep = upper ? acc0[i + w2] : acc0[i];
+                        acc0[i] = keep + __shfl_xor_sync(0xffffffffu, send, w2);
+                    }
+                }
+                if (lane < m) {
+                    const int blk_h = (rb * kRows + 32 * q) / kSlab;
+                    p.sh[(size_t)(r0 + lane) * shs + blk_h * 2 + (q & 1)] = acc0[0];
+                }
+                // publish this warp's h rows and block sums (read back by down tiles: h through TMA)
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done + e) : "memory");
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kTmemCols)
+                     : "memory");
+    }
+}
+
 // x_perm[p] = x[order[p] / k] with every 8-element group in the weights' order
-// (0,4,1,5,2,6,3,7).  Block 0 builds the tile list (an expert's tokens in fixed chunks of
-// cmax; all gate/up tiles before all down tiles) and clears the scheduling counters.
+// (0,4,1,5,2,6,3,7), and with sx the row's sums over its 64-element blocks (fp32, a fixed
+// order: 8 elements per lane, then three shuffle steps).  Block 0 builds the tile list (an
+// expert's tokens in fixed chunks of cmax; all gate/up tiles before all down tiles) and
+// clears the scheduling counters.
 __global__ void __launch_bounds__(256)
 q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, int T, int k, int H, int I, int E,
                int cmax, int max_tiles, uint16_t *__restrict__ x_perm,
-               uint32_t *tiles, int *sched, int *done, int32_t *err) {
+               uint32_t *tiles, int *sched, int *done, int32_t *err, float *sx) {
     griddep_launch_dependents();
     griddep_wait();
     if (blockIdx.x > 0) {
@@ -526,11 +1027,29 @@ q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, 
         if (bad && lane == 0) record_error(err, MOE_ERR_DEVICE);
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(bad ? 0 : a / k) * H);
         const int n = H / 8;
-        for (int i = lane; i < n; i += 32 * 4) {
+        // the loop runs the same number of times in every lane (the block sums shuffle)
+        for (int i0 = 0; i0 < n; i0 += 32 * 4) {
+            const int i = i0 + lane;
             uint4 v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 v[u] = (!bad && i + 32 * u < n) ? ldp16(src + i + 32 * u) : make_uint4(0, 0, 0, 0);
+            if (sx) {
+                // 8 lanes hold a 64-element block (n is a multiple of 8, so a group's lanes are all
+                // in range or all out of it; out-of-range lanes hold zeros and write nothing)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                    float sum = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        sum += __uint_as_float(w[c] << 16) + __uint_as_float(w[c] & 0xffff0000u);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                    if ((lane & 7) == 0 && i + 32 * u < n) sx[(size_t)pr * sx_stride(H) + (i + 32 * u) / 8] = sum;
+                }
+            }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 if (i + 32 * u >= n) continue;
@@ -592,8 +1111,22 @@ bool set_attr() {
     return true;
 }
 
+template <bool Lora>
+bool set_decode_attr() {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(q4_decode_kernel<Lora>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDSmemBytes) !=
+            cudaSuccess)
+            return false;
+        attr_set[dev] = true;
+    }
+    return true;
+}
+
 size_t q4_max_tiles(const moe_shape &s) {
-    const size_t chunks = (size_t)s.E + ((size_t)s.T * s.k + kDecodeMaxN - 1) / kDecodeMaxN;
+    const size_t chunks = (size_t)s.E + ((size_t)s.T * s.k + kDN - 1) / kDN;
     return chunks * (size_t)(s.I / kRows + s.H / kRows);
 }
 
@@ -624,8 +1157,14 @@ bool q4_path_supported(const moe_shape &s) {
            s.T <= kQ4MaxT && s.H % kRows == 0 && s.I % kRows == 0 && s.H <= 32 * kSlab && s.I <= 32 * kSlab;
 }
 
+// Block sums of the decode kernel, fp32: token rows [A][sx_stride(H)] and h
+// [A][sh_stride(I)] (block, half).
+size_t q4_sx_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * sx_stride(s.H) * 4 + 255) / 256 * 256; }
+size_t q4_sh_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * sh_stride(s.I) * 4 + 255) / 256 * 256; }
+
 size_t q4_part_bytes(const moe_shape &s) {
-    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (q4_max_tiles(s) * 4 + 255) / 256 * 256;
+    return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (q4_max_tiles(s) * 4 + 255) / 256 * 256 + q4_sx_bytes(s) +
+           q4_sh_bytes(s);
 }
 
 cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
@@ -640,21 +1179,26 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     int *sched = reinterpret_cast<int *>(base + xperm_bytes(s));
     int *done = sched + 64;
     uint32_t *tiles = reinterpret_cast<uint32_t *>(base + xperm_bytes(s) + 256 + (size_t)kMaxE * 4);
+    char *sums = reinterpret_cast<char *>(tiles) + (q4_max_tiles(s) * 4 + 255) / 256 * 256;
+    float *sx = reinterpret_cast<float *>(sums);
+    float *sh = reinterpret_cast<float *>(sums + q4_sx_bytes(s));
 
+    // code boxes: 128 rows x one stage's codes (32 bytes; the decode kernel's stages are 64)
+    const bool decode = s.T <= kDecodeMaxN;
+    const uint32_t cbox = decode ? kDK / 2 : kSlab / 2;
     CUtensorMap mg, mu, md, mx, mh;
-    if (!make_map(&mg, wg, (uint64_t)s.E * s.I, s.H / 2, kRows, kSlab / 2, true) ||
-        !make_map(&mu, wu, (uint64_t)s.E * s.I, s.H / 2, kRows, kSlab / 2, true) ||
-        !make_map(&md, wd, (uint64_t)s.E * s.H, s.I / 2, kRows, kSlab / 2, true) ||
+    if (!make_map(&mg, wg, (uint64_t)s.E * s.I, s.H / 2, kRows, cbox, true) ||
+        !make_map(&mu, wu, (uint64_t)s.E * s.I, s.H / 2, kRows, cbox, true) ||
+        !make_map(&md, wd, (uint64_t)s.E * s.H, s.I / 2, kRows, cbox, true) ||
         !make_map(&mx, x_perm, A, s.H, kNBox) || !make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
 
-    const bool decode = s.T <= kDecodeMaxN;
-    const int cmax = decode ? kDecodeMaxN : kChunkN;
+    const int cmax = decode ? kDN : kChunkN;
     cudaError_t e = launch_pdl(q4_prep_kernel, dim3(prep_blocks(A)), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
                                offsets, s.T, s.k, s.H, s.I, s.E, cmax, (int)q4_max_tiles(s), x_perm, tiles, sched,
-                               done, err);
+                               done, err, decode ? sx : nullptr);
     if (e != cudaSuccess) return e;
-    if (!(decode ? set_attr<kDecodeMaxN, 6, false>() && set_attr<kDecodeMaxN, 6, true>()
+    if (!(decode ? set_decode_attr<false>() && set_decode_attr<true>()
                  : set_attr<kChunkN, 4, false>() && set_attr<kChunkN, 4, true>()))
         return cudaErrorInvalidValue;
     Params prm{};
@@ -675,6 +1219,10 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     memcpy(&cbits, &centre, 4);
     const uint32_t c16 = cbits >> 16;  // 128 + 2 j0 is exact in bf16
     prm.centre2 = c16 | (c16 << 16);
+    prm.b = b;
+    prm.cc = 128.0f + 0.5f * float(t2);  // exact
+    prm.sx = sx;
+    prm.sh = sh;
     prm.E = s.E;
     prm.H = s.H;
     prm.I = s.I;
@@ -685,8 +1233,8 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     auto run = [&](const Params &pr, auto lora_tag) {
         constexpr bool L = decltype(lora_tag)::value;
         if (decode)
-            return launch_pdl(q4_swiglu_kernel<kDecodeMaxN, 6, L>, dim3(sm_count()), dim3(kThreads),
-                              QCfg<kDecodeMaxN, 6>::kSmemBytes, st, mg, mu, md, mx, mh, pr);
+            return launch_pdl(q4_decode_kernel<L>, dim3(sm_count()), dim3(kDThreads), kDSmemBytes, st, mg, mu, md, mx,
+                              mh, pr);
         return launch_pdl(q4_swiglu_kernel<kChunkN, 4, L>, dim3(sm_count()), dim3(kThreads),
                           QCfg<kChunkN, 4>::kSmemBytes, st, mg, mu, md, mx, mh, pr);
     };

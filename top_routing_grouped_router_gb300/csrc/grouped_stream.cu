@@ -173,7 +173,9 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     // a gate/up tile of more than 128 tokens takes both (gate in half 0, up in half 1).
     // Each half has its own full/free barrier pair, so one-half tiles double-buffer.
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned by pointer arithmetic on the shared array, so that the compiler keeps
+    // the shared address space (and emits shared, not generic, loads) for everything derived
+    uint8_t *smem = smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
     uint8_t *ctrl = smem + kStages * kStageBytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(ctrl);           // [kStages]
     uint64_t *empty = full + kStages;                              // [kStages]
@@ -185,7 +187,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     int *smeta = reinterpret_cast<int *>(drain + 1);               // [kStages][4]: kind, first, nstage, N
     int *tmeta = smeta + 4 * kStages;                              // [kMetaRing][8]
     volatile int *abort = tmeta + 8 * kMetaRing;
-    const Waits wt{p.err, abort, p.wait_ns};
+    const Waits wt{p.err, abort, p.wait_ns, smem_u32(const_cast<int *>(abort))};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tmeta + 8 * kMetaRing + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -127,14 +127,17 @@ __device__ void scatter_chunk(const int32_t *ids, int a0, int A, int E, PermuteS
     __syncthreads();
 }
 
-// The whole permutation of A assignments by one block of NT threads.
+// The whole permutation of A assignments by one block of NT threads.  s_ids, when given,
+// holds the ids in shared memory (A <= NT, filled before the call's first barrier).
 template <int NT>
 __device__ void permute_block(const int32_t *ids, int A, int E, int32_t *counts, int32_t *offsets, int32_t *order,
-                              int32_t *pos, int32_t *active, int32_t *err, PermuteSmem<NT> &s) {
+                              int32_t *pos, int32_t *active, int32_t *err, PermuteSmem<NT> &s,
+                              const int *s_ids = nullptr) {
     const int tid = threadIdx.x;
     for (int i = tid; i < E; i += NT) s.cnt[i] = 0;
     // the ids of the first two chunks stay in registers for the scatter
-    const int e0 = tid < A ? ldp(ids + tid) : -1, e1 = NT + tid < A ? ldp(ids + NT + tid) : -1;
+    const int e0 = tid < A ? (s_ids ? s_ids[tid] : ldp(ids + tid)) : -1;
+    const int e1 = NT + tid < A ? ldp(ids + NT + tid) : -1;
     __syncthreads();
     for (int a = tid; a < A; a += NT) {
         const int e = a < NT ? e0 : a < 2 * NT ? e1 : ldp(ids + a);

@@ -10,8 +10,10 @@
 // the grid, so every path below produces bit-identical logits.
 //
 // Top-k: one warp per token.  Lane l holds the logits of experts l, l+32, ...;
-// k rounds of a shuffle arg-max (ties -> lower expert index) pick the experts in
-// descending order, a (k+1)-th round gives the tie margin.  The weights are
+// k rounds of a warp arg-max (ties -> lower expert index) pick the experts in
+// descending order, a (k+1)-th round gives the tie margin.  A round is two warp
+// reductions (redux.sync): the maximum of an order-preserving 32-bit key of the logits,
+// then the minimum expert index among the lanes that hold it.  The weights are
 // exp(l_j - l_max) / sum over the chosen experts (norm_topk) or over all experts,
 // which equals softmax followed by renormalisation of the chosen probabilities.
 //
@@ -203,45 +205,53 @@ __device__ void router_block(const ActT *__restrict__ x, const ActT *__restrict_
 
 constexpr int kMaxPerLane = kMaxE / 32;
 
-// Warp arg-max over (value, index) pairs; equal values -> lower index.
-__device__ __forceinline__ void warp_argmax(float &v, int &i) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, v, o);
-        int oi = __shfl_xor_sync(0xffffffffu, i, o);
-        if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
-    }
+// Order-preserving key of a logit: a > b (as floats) <=> key(a) > key(b), and key(-0) =
+// key(+0).  Key 0 marks an expert that cannot be chosen (taken, or beyond E); NaN takes
+// key 1, below every number, so NaN logits are chosen last, in index order.
+__device__ __forceinline__ uint32_t logit_key(float f) {
+    if (f != f) return 1u;
+    const uint32_t b = f == 0.f ? 0u : __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Softmax / top-k / renormalisation of token t by one warp.
+// Softmax / top-k / renormalisation of token t by one warp; with s_ids, the chosen ids
+// also go to shared memory (s_ids[j] for slot j).
 __device__ void topk_token(const float *logits, int t, int E, int k, int norm, int32_t *ids, float *w,
-                           float *margin) {
+                           float *margin, int *s_ids = nullptr) {
     const int lane = threadIdx.x & 31;
     const float *l = logits + (size_t)t * E;
     float v[kMaxPerLane];
+    uint32_t key[kMaxPerLane];
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
         const int e = lane + 32 * i;
         v[i] = (e < E) ? ldp(l + e) : -INFINITY;
+        key[i] = (e < E) ? logit_key(v[i]) : 0u;
     }
-    uint32_t taken = 0;
     float lmax = 0.f, my_l = 0.f, last = 0.f;
     int my_id = 0;
     for (int j = 0; j <= k; ++j) {
         if (j == k && k == E) break;
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+        // this lane's best candidate: ascending e within a lane, strict '>' keeps the lower index
+        uint32_t bk = 0u;
+        int bi = 0;
 #pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i) {
-            const int e = lane + 32 * i;
-            // ascending e within a lane: strict '>' keeps the lower index on ties
-            if (e < E && !(taken >> i & 1u) && (v[i] > bv || bi == 0x7fffffff)) { bv = v[i]; bi = e; }
-        }
-        warp_argmax(bv, bi);
+        for (int i = 0; i < kMaxPerLane; ++i)
+            if (key[i] > bk) { bk = key[i]; bi = lane + 32 * i; }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const int win = int(__reduce_min_sync(0xffffffffu, bk == mk ? uint32_t(bi) : 0xffffffffu));
+        const float bv = key_logit(mk);
         if (j == 0) lmax = bv;
         if (j < k) {
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            if (lane == j) { my_id = bi; my_l = bv; }
+            if ((win & 31) == lane) {
+#pragma unroll
+                for (int i = 0; i < kMaxPerLane; ++i)
+                    if (i == (win >> 5)) key[i] = 0u;
+            }
+            if (lane == j) { my_id = win; my_l = bv; }
             last = bv;
         } else if (lane == 0 && margin) {
             margin[t] = last - bv;
@@ -262,6 +272,7 @@ __device__ void topk_token(const float *logits, int t, int E, int k, int norm, i
     if (lane < k) {
         ids[(size_t)t * k + lane] = my_id;
         w[(size_t)t * k + lane] = ex / denom;
+        if (s_ids) s_ids[lane] = my_id;
     }
 }
 
@@ -311,21 +322,31 @@ route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const floa
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    // with a single token group this block also permutes, from the ids in shared memory
+    const bool one_group = gridDim.y == 1;
+    __shared__ int s_ids[kTPB * kMaxK];
     const int w = threadIdx.x >> 5;
     const int t = blockIdx.y * kTPB + w;
-    if (w < kTPB && t < a.T) topk_token(a.logits, t, a.E, a.k, a.norm, a.ids, a.w, a.margin);
+    if (w < kTPB && t < a.T)
+        topk_token(a.logits, t, a.E, a.k, a.norm, a.ids, a.w, a.margin,
+                   one_group && a.fuse >= 2 ? s_ids + w * a.k : nullptr);
     if (threadIdx.x == 0) *group_arrivals = 0;
     if (a.fuse < 2) return;
-    // the last token group to finish permutes the whole batch
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(a.arrivals, 1) == int(gridDim.y) - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (threadIdx.x == 0) *a.arrivals = 0;
+    if (!one_group) {
+        // the last token group to finish permutes the whole batch
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) s_last = atomicAdd(a.arrivals, 1) == int(gridDim.y) - 1;
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        if (threadIdx.x == 0) *a.arrivals = 0;
+    } else {
+        __syncthreads();
+    }
     __shared__ PermuteSmem<kRThreads> ps;
-    permute_block<kRThreads>(a.ids, a.T * a.k, a.E, a.counts, a.offsets, a.order, a.pos, a.active, a.err, ps);
+    permute_block<kRThreads>(a.ids, a.T * a.k, a.E, a.counts, a.offsets, a.order, a.pos, a.active, a.err, ps,
+                             one_group ? s_ids : nullptr);
     if (!a.build) return;
     // the tensor-core expert kernel's tile list from this block's counts (after the scatter
     // ps.base[e] = offsets[e] + counts[e])

@@ -28,7 +28,13 @@ struct Waits {
     int32_t *err;
     volatile int *abort;
     unsigned long long limit_ns;
+    uint32_t abort_addr;  // the flag's shared-memory address (read with an explicit shared load)
 };
+__device__ __forceinline__ bool abort_raised(const Waits &w) {
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(w.abort_addr) : "memory");
+    return v != 0;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -55,6 +61,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, but a thread whose phase is not complete is suspended until it completes or
+// `ns` nanoseconds pass, instead of returning at once: a waiting warp then takes no issue slots
+// from the warps that work on the same scheduler.
+constexpr uint32_t kSuspendNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -72,20 +94,19 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
 }
 
 // Bounded wait: after the limit record the error and raise the CTA's abort flag, so that
-// every later wait of the CTA gives up at once and the kernel drains.  The flag and the
-// clock are checked every 16 polls.  Returns false when it gave up.
+// every later wait of the CTA gives up at once and the kernel drains.  Between tests the
+// thread sleeps in the barrier (at most kSuspendNs); the flag and the clock are checked
+// after each.  Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Waits &w) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 15) == 0) {
-            if (*w.abort) return false;
-            if (globaltimer_ns() - t0 > w.limit_ns) {
-                record_error(w.err, MOE_ERR_DEVICE);
-                *w.abort = 1;
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity)) return true;
+        if (abort_raised(w)) return false;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+            record_error(w.err, MOE_ERR_DEVICE);
+            *w.abort = 1;
+            return false;
         }
     }
 }
@@ -97,9 +118,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, const Waits &w) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 15) == 0 && globaltimer_ns() - t0 > w.limit_ns) {
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
             record_error(w.err, MOE_ERR_DEVICE);
             *w.abort = 1;
             return false;
@@ -115,7 +136,7 @@ __device__ __forceinline__ bool wait_count(const int *p, int need, const Waits &
         int v;
         asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
         if (v >= need) return true;
-        if (*w.abort) return false;
+        if (abort_raised(w)) return false;
         if (n == 0) {
             t0 = globaltimer_ns();
         } else if (globaltimer_ns() - t0 > w.limit_ns) {
@@ -177,6 +198,41 @@ __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
         ::"r"(bar)
         : "memory");
 }
+
+// The same MMA with A read from TMEM (a_tmem: the column of A's first K element, lane 0):
+// M rows in M lanes, K elements packed two per 32-bit column (the lower K in the low half).
+__device__ __forceinline__ void mma_bf16_tmem_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                   uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// 16 / 32 consecutive 32-bit columns of this thread's TMEM lane from registers (warp-wide;
+// completion is awaited with tmem_st_wait).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+          "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+          "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
