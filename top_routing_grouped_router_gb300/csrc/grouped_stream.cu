@@ -106,6 +106,12 @@ struct Params {
     const int32_t *order;
     uint16_t *xperm;
     int k;
+    // implicit tile list (same batches: every expert's tokens are one chunk): the tiles are
+    // derived from the active-expert list and the offsets instead of read from records
+    const int32_t *active;      // [1 + E]: count, then the active experts in ascending order; or null
+    const int32_t *offsets;     // [E + 1]
+    int gu_per, dn_per;         // row blocks of I and of H
+    int need1;                  // h publications of an expert (its gate/up tiles' epilogue warps)
     // router mode: tiles are (row block of experts, 128-token chunk), one static sweep
     int router_tiles;           // > 0 selects router mode
     int T;
@@ -145,6 +151,21 @@ __device__ __forceinline__ TileInfo read_tile(uint4 rec, const Params &p, int ca
     }
     d.N = d.m > 0 ? (d.m + 15) & ~15 : 16;
     return d;
+}
+
+// Tile t of the implicit list -- the record the list builder writes when every expert holds
+// one token chunk: the gate/up tiles (row block t % gu_per of the (t / gu_per)-th active
+// expert) and after them, in the same expert order, the down tiles.
+__device__ __forceinline__ uint4 implicit_rec(const Params &p, int n_act, int t) {
+    const int n_gu = n_act * p.gu_per;
+    const bool dn = t >= n_gu;
+    const int u = dn ? t - n_gu : t;
+    const int per = dn ? p.dn_per : p.gu_per;
+    const int i = u / per, rb = u - i * per;
+    const int e = ldp(p.active + 1 + i);
+    const int off = ldp(p.offsets + e), me = ldp(p.offsets + e + 1) - off;
+    return make_uint4(pack_rec(dn ? kRecDown : kRecGateUp, e, rb, 0), uint32_t(off), uint32_t(me),
+                      dn ? uint32_t(p.need1) : 0u);
 }
 
 // Tensor maps of the packed LoRA adapters and of the scaled A-side products; kernels
@@ -231,7 +252,11 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         // this launch's tile range [lo, hi) and its claim counter
         int lo = 0, hi = router ? p.router_tiles : 0;
         int *ctr = nullptr;
-        if (!router) {
+        const int n_act = (!router && p.active) ? ldp(p.active) : 0;
+        if (!router && p.active) {
+            hi = n_act * (p.gu_per + p.dn_per);
+            ctr = p.sched + kSchedRangeClaim;
+        } else if (!router) {
             const int r = p.phase == kPhaseLoraX ? 0 : p.phase == kPhaseGateUp ? 1 : p.phase == kPhaseLoraH ? 2 : 3;
             const bool all = p.phase == kPhaseAll;
             lo = ldp(p.sched + kSchedBound + (all ? 0 : r));
@@ -243,7 +268,10 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
         // between two tiles; claiming only one ahead keeps the tail balanced when tiles are
         // long (a decode gate/up tile streams 1 MB of weights)
         int next = router ? int(blockIdx.x) : lo + atomicAdd(ctr, 1);
-        uint4 next_rec = (!router && next < hi) ? ldp16(p.tiles + next) : make_uint4(0, 0, 0, 0);
+        auto fetch = [&](int t) {
+            return p.active ? implicit_rec(p, n_act, t) : ldp16(p.tiles + t);
+        };
+        uint4 next_rec = (!router && next < hi) ? fetch(next) : make_uint4(0, 0, 0, 0);
         const int cap_dn = min(p.dmax, (kABytes + kBBytes) / 128);
         int hnext = 0;  // TMEM half of the next one-half tile
         int fills = 0;  // stage fills issued (arrive.expect_tx + TMA) so far
@@ -387,7 +415,7 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                     sm[3] = lora_a ? nl : d.N;
                 }
                 if (!router && ks == min(2, nstage - 1))
-                    next_rec = next < hi ? ldp16(p.tiles + next) : make_uint4(0, 0, 0, 0);
+                    next_rec = next < hi ? fetch(next) : make_uint4(0, 0, 0, 0);
                 const uint32_t fb = smem_u32(&full[stage]);
                 mbar_arrive_expect_tx(fb, lstage ? lbytes : bytes);
                 ++fills;
@@ -868,7 +896,8 @@ TileListArgs tc_tile_args(const moe_shape &s, int mode) {
 }  // namespace
 
 bool tc_tile_build(const moe_shape &s, float *part, TileBuild *tb) {
-    if (select_grouped_path(s) != 1) return false;
+    // the implicit list needs every expert's tokens (at most T) in one gate/up and one down tile
+    if (select_grouped_path(s) != 1 || tc_wide(s) || s.T > kMaxN || s.T > kMaxDownN) return false;
     const TcPart t = tc_part(s, part);
     *tb = TileBuild{tc_tile_args(s, kLoraNone), t.tiles, t.sched, t.done};
     return true;
@@ -876,7 +905,7 @@ bool tc_tile_build(const moe_shape &s, float *part, TileBuild *tb) {
 
 cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, const int32_t *offsets,
                                 const int32_t *order, const void *wg, const void *wu, const void *wd,
-                                const moe_q4 *q4, const int32_t *, float *part, void *h, void *y, int32_t *err,
+                                const moe_q4 *q4, const int32_t *active, float *part, void *h, void *y, int32_t *err,
                                 cudaStream_t st, const moe_lora *lora, float *xa, float *ha, float *lpart,
                                 bool prebuilt) {
     if (path == 2) return launch_q4(s, x, offsets, order, wg, wu, wd, q4, part, h, y, err, st, lora, xa, ha, lpart);
@@ -942,6 +971,13 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     prm.order = order;
     prm.xperm = x_perm;
     prm.k = s.k;
+    if (prebuilt) {
+        prm.active = active;
+        prm.offsets = offsets;
+        prm.gu_per = s.I / kRows;
+        prm.dn_per = s.H / kRows;
+        prm.need1 = prm.gu_per * epi_warps(kLoraNone);
+    }
     // every expert has at most T tokens: small batches take the deeper pipeline
     const dim3 grid(tc::sm_count());
     if (!lora) return launch_tc_for<kLoraNone>(s, wide, grid, st, m, prm);

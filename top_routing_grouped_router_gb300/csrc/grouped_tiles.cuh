@@ -181,6 +181,18 @@ __device__ inline void build_tile_list_from(int off, int me, int T, int k, int E
     }
 }
 
+// With the implicit list (every expert one token chunk, no adapters) the expert kernel
+// derives its tiles from the active-expert list; only its counters start at zero: the
+// claim counter, the gathered-rows count and the experts' h publications.  By a block whose
+// threads cover the E experts.
+__device__ inline void reset_implicit_list(int E, int *sched, int *done) {
+    if (int(threadIdx.x) < E) done[threadIdx.x] = 0;
+    if (threadIdx.x == 0) {
+        sched[kSchedRangeClaim] = 0;
+        sched[kSchedXDone] = 0;
+    }
+}
+
 // The same from the offsets in global memory (written by an earlier kernel).
 __device__ inline void build_tile_list(const int32_t *offsets, int T, int k, int E, const TileListArgs &ta,
                                        uint4 *tiles, int *sched, int *done, int32_t *err) {

@@ -285,7 +285,7 @@ struct RouteArgs {
     int fuse;                 // 0: logits only, 1: + top-k, 2: + top-k + permutation
     int32_t *counts, *offsets, *order, *pos, *active, *err;
     NormArgs norm_in;         // optional pre-router RMSNorm of x
-    int build;                // with fuse 2: also the expert kernel's tile list (tb)
+    int build;                // with fuse 2: also reset the expert kernel's counters (tb)
     TileBuild tb;
 };
 
@@ -348,11 +348,9 @@ route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const floa
     permute_block<kRThreads>(a.ids, a.T * a.k, a.E, a.counts, a.offsets, a.order, a.pos, a.active, a.err, ps,
                              one_group ? s_ids : nullptr);
     if (!a.build) return;
-    // the tensor-core expert kernel's tile list from this block's counts (after the scatter
-    // ps.base[e] = offsets[e] + counts[e])
-    const int e = threadIdx.x;
-    const int me = e < a.E ? ps.cnt[e] : 0, off = e < a.E ? ps.base[e] - me : 0;
-    build_tile_list_from(off, me, a.T, a.k, a.E, a.tb.ta, a.tb.tiles, a.tb.sched, a.tb.done, a.err);
+    // the tensor-core expert kernel derives its tiles from the active list this block just
+    // wrote (every expert's tokens are one chunk at these batch sizes): only its counters
+    reset_implicit_list(a.E, a.tb.sched, a.tb.done);
 }
 
 __global__ void __launch_bounds__(128)
