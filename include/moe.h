@@ -305,8 +305,8 @@ MOE_API int moe_lora_pack(const moe_shape *shape, const moe_lora *lora, void *pa
  *   - Calls no allocating routine.  The array's module is loaded lazily: the
  *     first call on each device looks up the array's device address (with that
  *     device current), and that lookup is when the driver reserves the 32 MiB
- *     on the device and may synchronise.  Make that first call before any
- *     stream capture.
+ *     on the device and may synchronise.  Make that first call where a
+ *     synchronisation is harmless.
  *   - Shapes whose moe_workspace_size() exceeds 32 MiB are rejected with
  *     MOE_ERR_WORKSPACE before anything is enqueued (the decode shapes fit:
  *     the Qwen3-30B-A3B layer up to a few hundred tokens).  Every other argument
