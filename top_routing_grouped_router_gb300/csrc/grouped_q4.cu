@@ -571,15 +571,6 @@ __device__ __forceinline__ void codes_to_ints(const uint4 cw, uint32_t *v) {
     }
 }
 
-// One 64-element slab of this thread's row: 32 bytes of codes at `cb` -> 32 TMEM columns.
-__device__ __forceinline__ void slab_to_tmem(uint32_t cb, uint32_t taddr) {
-    const uint4 c0 = lds_v4(cb), c1 = lds_v4(cb + 16);
-    uint32_t v[32];
-    codes_to_ints(c0, v);
-    codes_to_ints(c1, v + 16);
-    tmem_st32(taddr, v);
-}
-
 // Two loads of 16 fp32 columns of this thread's lane, one wait.
 __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float *a, float *b) {
     uint32_t r[32];
@@ -599,6 +590,73 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float *a, 
         b[i] = __uint_as_float(r[16 + i]);
     }
 }
+
+// Four loads of 16 fp32 columns of this thread's lane, one wait.
+__device__ __forceinline__ void tmem_ld16x4(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3, float (*v)[16]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%65];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47}, [%66];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%67];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(t0), "r"(t1), "r"(t2), "r"(t3)
+        : "memory");
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[g][i] = __uint_as_float(r[16 * g + i]);
+}
+
+// A stage's MMAs and its three commits in one block, issued by one elected lane of the converged
+// warp: the partials of the stage's two blocks (gate and up, or the two blocks of a down tile)
+// from the A ring (TMEM, 8 columns per K = 16) and the stage's token rows (B descriptors one add
+// apart: the start address is bits 0-13 in 16-byte units).  The first MMA of each accumulator
+// overwrites it.
+#define Q4D_MMA(DOFF, AOFF, BOFF, P)                                                                      \
+    "add.u32 dd, %0, " #DOFF ";\n\tadd.u32 aa, %1, " #AOFF ";\n\tadd.s64 bd, %2, " #BOFF ";\n\t"        \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [dd], [aa], bd, %3, " #P ";\n\t"
+#define Q4D_COMMITS                                                                                        \
+    "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t"                 \
+    "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"                 \
+    "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+static_assert(kDTokSlab / 16 == 256 && kDPartCols == 128 && kDAStageCols == 128, "offsets in the MMA blocks");
+__device__ __forceinline__ void q4d_stage_gate_up(uint32_t d, uint32_t ta, uint64_t b0, uint32_t idesc, uint32_t c0,
+                                                  uint32_t c1, uint32_t c2) {
+    asm volatile(
+        "{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 dd, aa;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        Q4D_MMA(0, 0, 0, pf) Q4D_MMA(32, 64, 0, pf) Q4D_MMA(0, 8, 2, pt) Q4D_MMA(32, 72, 2, pt)
+        Q4D_MMA(0, 16, 4, pt) Q4D_MMA(32, 80, 4, pt) Q4D_MMA(0, 24, 6, pt) Q4D_MMA(32, 88, 6, pt)
+        Q4D_MMA(64, 32, 256, pf) Q4D_MMA(96, 96, 256, pf) Q4D_MMA(64, 40, 258, pt) Q4D_MMA(96, 104, 258, pt)
+        Q4D_MMA(64, 48, 260, pt) Q4D_MMA(96, 112, 260, pt) Q4D_MMA(64, 56, 262, pt) Q4D_MMA(96, 120, 262, pt)
+        Q4D_COMMITS "}"
+        ::"r"(d), "r"(ta), "l"(b0), "r"(idesc), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void q4d_stage_down(uint32_t d, uint32_t ta, uint64_t b0, uint32_t idesc, uint32_t c0,
+                                               uint32_t c1, uint32_t c2) {
+    asm volatile(
+        "{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 dd, aa;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        Q4D_MMA(0, 0, 0, pf) Q4D_MMA(0, 8, 2, pt) Q4D_MMA(0, 16, 4, pt) Q4D_MMA(0, 24, 6, pt)
+        Q4D_MMA(64, 32, 256, pf) Q4D_MMA(64, 40, 258, pt) Q4D_MMA(64, 48, 260, pt) Q4D_MMA(64, 56, 262, pt)
+        Q4D_COMMITS "}"
+        ::"r"(d), "r"(ta), "l"(b0), "r"(idesc), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+#undef Q4D_MMA
+#undef Q4D_COMMITS
 
 template <bool kLora>
 __global__ void __launch_bounds__(kDThreads, 1)
@@ -795,14 +853,31 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const bool ok = mbar_wait(smem_u32(&aempty[a]), ap ^ 1, wt);
             tc_fence_after();
             if (__all_sync(0xffffffffu, ok && ks >= 0 && !abort_raised(wt))) {
-                // a row's codes of a stage are 64 bytes: two slabs of 32
+                // a row's codes of a stage are 64 bytes: two slabs of 32.  Every load is issued
+                // before the first conversion (the asm statements keep their order).
                 const uint32_t cb = smem_u32(raw + r * kDRawBytes) + uint32_t(row * (kDK / 2));
                 const uint32_t ta = tlane + uint32_t(kDACol + a * kDAStageCols);
-                slab_to_tmem(cb, ta);
-                slab_to_tmem(cb + 32, ta + 32);
+                uint4 c[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) c[i] = lds_v4(cb + 16 * i);
                 if (!down) {
-                    slab_to_tmem(cb + kDCodeBytes, ta + 64);
-                    slab_to_tmem(cb + kDCodeBytes + 32, ta + 96);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) c[4 + i] = lds_v4(cb + kDCodeBytes + 16 * i);
+                }
+                uint32_t v[32];
+                codes_to_ints(c[0], v);
+                codes_to_ints(c[1], v + 16);
+                tmem_st32(ta, v);
+                codes_to_ints(c[2], v);
+                codes_to_ints(c[3], v + 16);
+                tmem_st32(ta + 32, v);
+                if (!down) {
+                    codes_to_ints(c[4], v);
+                    codes_to_ints(c[5], v + 16);
+                    tmem_st32(ta + 64, v);
+                    codes_to_ints(c[6], v);
+                    codes_to_ints(c[7], v + 16);
+                    tmem_st32(ta + 96, v);
                 }
                 tmem_st_wait();
             }
@@ -830,17 +905,11 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             // the stage's B descriptors differ from the first only in the start-address field
             // (address / 16, 14 bits: shared memory stays below 256 KB, so adding cannot carry)
             const uint64_t b0 = smem_desc(smem_u32(raw + r * kDRawBytes) + kDTok);
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-                for (int kk = 0; kk < kSlab / 16; ++kk) {
-                    const uint64_t bdesc = b0 + uint64_t((h2 * kDTokSlab + kk * 32) >> 4);
-                    mma_bf16_tmem_warp(d + h2 * 64, ta + h2 * 32 + kk * 8, bdesc, idesc, kk != 0);
-                    if (!down) mma_bf16_tmem_warp(d + h2 * 64 + 32, ta + 64 + h2 * 32 + kk * 8, bdesc, idesc, kk != 0);
-                }
-            mma_commit_warp(smem_u32(&aempty[a]));
-            mma_commit_warp(smem_u32(&rempty[r]));
-            mma_commit_warp(smem_u32(&pfull[pb]));
+            const uint32_t c0 = smem_u32(&aempty[a]), c1 = smem_u32(&rempty[r]), c2 = smem_u32(&pfull[pb]);
+            if (!down)
+                q4d_stage_gate_up(d, ta, b0, idesc, c0, c1, c2);
+            else
+                q4d_stage_down(d, ta, b0, idesc, c0, c1, c2);
             if (++r == kDRawStages) r = 0;
             if (++a == kDAS) { a = 0; ap ^= 1; }
             if (++pb == kDPS) { pb = 0; pp ^= 1; }
@@ -883,21 +952,26 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 tc_fence_after();
                 const uint32_t ta = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(pb * kDPartCols);
                 if (!down) {
+                    float g[4];  // gate and up scale x b of the stage's two blocks
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
-                        const int blk = 2 * ks + h2;
-                        const float gg = bf16_bits_to_f32(sc_a[row * nblk + blk]) * bstep;
-                        const float gu = bf16_bits_to_f32(sc_u[row * nblk + blk]) * bstep;
+                        g[2 * h2] = bf16_bits_to_f32(sc_a[row * nblk + 2 * ks + h2]) * bstep;
+                        g[2 * h2 + 1] = bf16_bits_to_f32(sc_u[row * nblk + 2 * ks + h2]) * bstep;
+                    }
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            if (hf * 16 >= N) break;  // warp-uniform
-                            float v0[16], v1[16];
-                            tmem_ld16x2(ta + h2 * 64 + hf * 16, ta + h2 * 64 + 32 + hf * 16, v0, v1);
+                    for (int hf = 0; hf < 2; ++hf) {
+                        if (hf * 16 >= N) break;  // warp-uniform
+                        // gate and up partials of both blocks for these 16 tokens, one wait
+                        float v[4][16];
+                        tmem_ld16x4(ta + hf * 16, ta + 32 + hf * 16, ta + 64 + hf * 16, ta + 96 + hf * 16, v);
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int blk = 2 * ks + h2;
 #pragma unroll
                             for (int t = 0; t < 16; ++t) {
                                 const float cs = cc * bs[(hf * 16 + t) * sxs + blk];
-                                acc0[hf * 16 + t] = fmaf(gg, v0[t] - cs, acc0[hf * 16 + t]);
-                                acc1[hf * 16 + t] = fmaf(gu, v1[t] - cs, acc1[hf * 16 + t]);
+                                acc0[hf * 16 + t] = fmaf(g[2 * h2], v[2 * h2][t] - cs, acc0[hf * 16 + t]);
+                                acc1[hf * 16 + t] = fmaf(g[2 * h2 + 1], v[2 * h2 + 1][t] - cs, acc1[hf * 16 + t]);
                             }
                         }
                     }
