@@ -83,6 +83,7 @@ struct Params {
     float half_b;                   // b / 2
     uint32_t centre2;               // bf16x2 of 128 + 2*j0
     float b, cc;                    // decode kernel: codebook step b and 128 + j0
+    uint32_t nib_mask, nib_bias;    // decode kernel: 0x000F000F and bf16x2 128.0 (operands of its LOP3s)
     const float *sx;                // decode kernel: block sums of the token rows [A][sx_stride(H)]
     float *sh;                      // decode kernel: block sums of h, two halves [A][sh_stride(I)]
     int E, H, I, A;
@@ -557,17 +558,26 @@ static_assert(kDACol + kDAS * kDAStageCols <= kTmemCols, "TMEM columns");
 __host__ __device__ constexpr int sx_stride(int H) { return (H / kSlab + 3) & ~3; }
 __host__ __device__ constexpr int sh_stride(int I) { return (2 * (I / kSlab) + 3) & ~3; }
 
+// (a & m) | c as one LOP3: m and c in registers (written as C, `(a & m) | c` with two
+// immediates takes two instructions)
+__device__ __forceinline__ uint32_t lop3_andor(uint32_t a, uint32_t m, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(m), "r"(c));
+    return d;
+}
+
 // 32 codes (16 bytes) -> the 16 bf16 pairs (128 + j) in the MMA's K order (per 8-element
-// group: (0,4), (1,5), (2,6), (3,7)).
-__device__ __forceinline__ void codes_to_ints(const uint4 cw, uint32_t *v) {
+// group: (0,4), (1,5), (2,6), (3,7)); m = 0x000F000F, c = bf16x2 128.0 = 0x43004300 (kernel
+// parameters, so that they stay register operands).  7 integer operations per 8 codes.
+__device__ __forceinline__ void codes_to_ints(const uint4 cw, uint32_t *v, uint32_t m, uint32_t c) {
     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t w = words[i];
-        v[4 * i + 0] = (w & 0x000F000Fu) | 0x43004300u;
-        v[4 * i + 1] = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
-        v[4 * i + 2] = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
-        v[4 * i + 3] = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
+        v[4 * i + 0] = lop3_andor(w, m, c);
+        v[4 * i + 1] = lop3_andor(w >> 4, m, c);
+        v[4 * i + 2] = lop3_andor(w >> 8, m, c);
+        v[4 * i + 3] = lop3_andor(w >> 12, m, c);
     }
 }
 
@@ -864,20 +874,15 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 #pragma unroll
                     for (int i = 0; i < 4; ++i) c[4 + i] = lds_v4(cb + kDCodeBytes + 16 * i);
                 }
-                uint32_t v[32];
-                codes_to_ints(c[0], v);
-                codes_to_ints(c[1], v + 16);
-                tmem_st32(ta, v);
-                codes_to_ints(c[2], v);
-                codes_to_ints(c[3], v + 16);
-                tmem_st32(ta + 32, v);
+                const uint32_t km = p.nib_mask, kc = p.nib_bias;
+                uint32_t v[64];  // one matrix's two slabs: 64 columns, one store
+#pragma unroll
+                for (int i = 0; i < 4; ++i) codes_to_ints(c[i], v + 16 * i, km, kc);
+                tmem_st64(ta, v);
                 if (!down) {
-                    codes_to_ints(c[4], v);
-                    codes_to_ints(c[5], v + 16);
-                    tmem_st32(ta + 64, v);
-                    codes_to_ints(c[6], v);
-                    codes_to_ints(c[7], v + 16);
-                    tmem_st32(ta + 96, v);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) codes_to_ints(c[4 + i], v + 16 * i, km, kc);
+                    tmem_st64(ta + 64, v);
                 }
                 tmem_st_wait();
             }
@@ -1295,6 +1300,8 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     prm.centre2 = c16 | (c16 << 16);
     prm.b = b;
     prm.cc = 128.0f + 0.5f * float(t2);  // exact
+    prm.nib_mask = 0x000F000Fu;
+    prm.nib_bias = 0x43004300u;
     prm.sx = sx;
     prm.sh = sh;
     prm.E = s.E;
