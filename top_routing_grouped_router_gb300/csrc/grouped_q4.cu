@@ -83,7 +83,8 @@ struct Params {
     float half_b;                   // b / 2
     uint32_t centre2;               // bf16x2 of 128 + 2*j0
     float b, cc;                    // decode kernel: codebook step b and 128 + j0
-    uint32_t nib_mask, nib_bias;    // decode kernel: 0x000F000F and bf16x2 128.0 (operands of its LOP3s)
+    uint32_t nib_mask, nib_bias;    // 0x000F000F and bf16x2 128.0: operands of the dequant LOP3s
+    uint32_t nib_mask2;             // 0x001E001E (large-batch kernel: codes doubled)
     const float *sx;                // decode kernel: block sums of the token rows [A][sx_stride(H)]
     float *sh;                      // decode kernel: block sums of h, two halves [A][sh_stride(I)]
     int E, H, I, A;
@@ -105,19 +106,28 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
+// (a & m) | c as one LOP3: m and c in registers (written as C, `(a & m) | c` with two
+// immediates takes two instructions)
+__device__ __forceinline__ uint32_t lop3_andor(uint32_t a, uint32_t m, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(m), "r"(c));
+    return d;
+}
+
 // 32 codes (16 bytes) -> 32 bf16 weights written as four swizzled 16-byte chunks of row
 // `row`, chunks 4*half .. 4*half+3 of the 64-element slab.
+// m2 = 0x001E001E and c = bf16x2 128.0 (register operands of the LOP3s).
 __device__ __forceinline__ void dequant_unit(const uint4 cw, uint32_t a_base, int row, int half, uint32_t gamma2,
-                                             uint32_t centre2) {
+                                             uint32_t centre2, uint32_t m2, uint32_t c) {
     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t w = words[i];
         uint32_t p[4];
-        p[0] = ((w << 1) & 0x001E001Eu) | 0x43004300u;   // elements 0, 4
-        p[1] = ((w >> 3) & 0x001E001Eu) | 0x43004300u;   // 1, 5
-        p[2] = ((w >> 7) & 0x001E001Eu) | 0x43004300u;   // 2, 6
-        p[3] = ((w >> 11) & 0x001E001Eu) | 0x43004300u;  // 3, 7
+        p[0] = lop3_andor(w << 1, m2, c);   // elements 0, 4
+        p[1] = lop3_andor(w >> 3, m2, c);   // 1, 5
+        p[2] = lop3_andor(w >> 7, m2, c);   // 2, 6
+        p[3] = lop3_andor(w >> 11, m2, c);  // 3, 7
 #pragma unroll
         for (int q = 0; q < 4; ++q) p[q] = bf16x2_mul(bf16x2_sub(p[q], centre2), gamma2);
         const int j = 4 * half + i;
@@ -358,8 +368,8 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 const uint4 c1 = second ? lds_v4(rbase + kCodeBytes) : c0;
                 const uint32_t g0 = gamma_pair(uint16_t(lds_u16(si0)), p.half_b);
                 const uint32_t g1 = second ? gamma_pair(uint16_t(lds_u16(si1)), p.half_b) : g0;
-                dequant_unit(c0, abase, row, half, g0, p.centre2);
-                if (second) dequant_unit(c1, abase + kABytes, row, half, g1, p.centre2);
+                dequant_unit(c0, abase, row, half, g0, p.centre2, p.nib_mask2, p.nib_bias);
+                if (second) dequant_unit(c1, abase + kABytes, row, half, g1, p.centre2, p.nib_mask2, p.nib_bias);
                 // generic-proxy smem writes -> visible to the tensor core
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
@@ -557,14 +567,6 @@ static_assert(kDACol + kDAS * kDAStageCols <= kTmemCols, "TMEM columns");
 // I/64 blocks x 2 halves.
 __host__ __device__ constexpr int sx_stride(int H) { return (H / kSlab + 3) & ~3; }
 __host__ __device__ constexpr int sh_stride(int I) { return (2 * (I / kSlab) + 3) & ~3; }
-
-// (a & m) | c as one LOP3: m and c in registers (written as C, `(a & m) | c` with two
-// immediates takes two instructions)
-__device__ __forceinline__ uint32_t lop3_andor(uint32_t a, uint32_t m, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(m), "r"(c));
-    return d;
-}
 
 // 32 codes (16 bytes) -> the 16 bf16 pairs (128 + j) in the MMA's K order (per 8-element
 // group: (0,4), (1,5), (2,6), (3,7)); m = 0x000F000F, c = bf16x2 128.0 = 0x43004300 (kernel
@@ -1301,6 +1303,7 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     prm.b = b;
     prm.cc = 128.0f + 0.5f * float(t2);  // exact
     prm.nib_mask = 0x000F000Fu;
+    prm.nib_mask2 = 0x001E001Eu;
     prm.nib_bias = 0x43004300u;
     prm.sx = sx;
     prm.sh = sh;
