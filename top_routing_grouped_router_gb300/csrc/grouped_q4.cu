@@ -524,7 +524,8 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 }
 
 // ---------------------------------------------------------------- decode kernel
-// Decode batches (an expert's tokens in chunks of at most kDN): the codes reach the tensor
+// Decode batches (an expert's tokens in chunks of at most kDN = 16; an expert with more tokens
+// streams its weights once per chunk): the codes reach the tensor
 // core through TMEM, and the block scales are applied after the MMA.
 //  * The dequant warps turn each code j into the integer 128 + j, exact in bf16 and one
 //    LOP3 per pair of codes (after a shift for three of the four nibble positions), and
@@ -542,22 +543,22 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 // A stage is 128 input elements (two blocks) of a tile's 128 rows, of both gate and up on a
 // gate/up tile: every role synchronises once per stage, so the longer stage halves that
 // cost per code byte.
-constexpr int kDN = 32;                              // token chunk (MMA N <= 32)
+constexpr int kDN = 16;                              // token chunk (MMA N = 16)
 constexpr int kDK = 2 * kSlab;                       // input elements per stage
 constexpr int kDCodeBytes = kRows * kDK / 2;         // 8 KB: one matrix's codes of a stage
 constexpr int kDTok = 2 * kDCodeBytes;               // token rows after the gate and up codes
 constexpr int kDTokSlab = kDN * 128;                 // token rows of one 64-element slab (SW128)
 constexpr int kDRawBytes = kDTok + 2 * kDTokSlab;    // 24 KB
-constexpr int kDRawStages = 7;
+constexpr int kDRawStages = 8;
 constexpr int kDAS = 2;                              // TMEM A-ring stages
-constexpr int kDPS = 2;                              // TMEM partial-ring entries
-constexpr int kDPartCols = 128;                      // a stage's partials: block h at 64 h (gate +0, up +32)
+constexpr int kDPS = 4;                              // TMEM partial-ring entries
+constexpr int kDPartCols = 64;                       // a stage's partials: block h at 32 h (gate +0, up +16)
 constexpr int kDACol = kDPS * kDPartCols;            // first A-ring column
 constexpr int kDAStageCols = 128;                    // gate slabs +0, +32; up slabs +64, +96
 constexpr int kDCons = 4;                            // consumer warps: one per lane quadrant
 constexpr int kDDeq = 4;                             // dequant warps: one per lane quadrant
 constexpr int kDThreads = (2 + kDCons + kDDeq) * 32;
-constexpr int kDSBytes = 8192;                       // a tile's block sums: <= 32 rows x 256 B
+constexpr int kDSBytes = 4096;                       // a tile's block sums: <= 16 rows x 256 B
 constexpr int kDSide = kScaleBytes + kDSBytes;       // per-tile side buffer: scales, then block sums
 constexpr int kDSmemBytes = kDRawStages * kDRawBytes + 2 * kDSide + 1024 + 2048;
 static_assert(kDSmemBytes <= 232448, "shared memory");
@@ -640,17 +641,17 @@ __device__ __forceinline__ void tmem_ld16x4(uint32_t t0, uint32_t t1, uint32_t t
     "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t"                 \
     "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"                 \
     "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
-static_assert(kDTokSlab / 16 == 256 && kDPartCols == 128 && kDAStageCols == 128, "offsets in the MMA blocks");
+static_assert(kDTokSlab / 16 == 128 && kDPartCols == 64 && kDAStageCols == 128, "offsets in the MMA blocks");
 __device__ __forceinline__ void q4d_stage_gate_up(uint32_t d, uint32_t ta, uint64_t b0, uint32_t idesc, uint32_t c0,
                                                   uint32_t c1, uint32_t c2) {
     asm volatile(
         "{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 dd, aa;\n\t.reg .b64 bd;\n\t"
         "setp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
-        Q4D_MMA(0, 0, 0, pf) Q4D_MMA(32, 64, 0, pf) Q4D_MMA(0, 8, 2, pt) Q4D_MMA(32, 72, 2, pt)
-        Q4D_MMA(0, 16, 4, pt) Q4D_MMA(32, 80, 4, pt) Q4D_MMA(0, 24, 6, pt) Q4D_MMA(32, 88, 6, pt)
-        Q4D_MMA(64, 32, 256, pf) Q4D_MMA(96, 96, 256, pf) Q4D_MMA(64, 40, 258, pt) Q4D_MMA(96, 104, 258, pt)
-        Q4D_MMA(64, 48, 260, pt) Q4D_MMA(96, 112, 260, pt) Q4D_MMA(64, 56, 262, pt) Q4D_MMA(96, 120, 262, pt)
+        Q4D_MMA(0, 0, 0, pf) Q4D_MMA(16, 64, 0, pf) Q4D_MMA(0, 8, 2, pt) Q4D_MMA(16, 72, 2, pt)
+        Q4D_MMA(0, 16, 4, pt) Q4D_MMA(16, 80, 4, pt) Q4D_MMA(0, 24, 6, pt) Q4D_MMA(16, 88, 6, pt)
+        Q4D_MMA(32, 32, 128, pf) Q4D_MMA(48, 96, 128, pf) Q4D_MMA(32, 40, 130, pt) Q4D_MMA(48, 104, 130, pt)
+        Q4D_MMA(32, 48, 132, pt) Q4D_MMA(48, 112, 132, pt) Q4D_MMA(32, 56, 134, pt) Q4D_MMA(48, 120, 134, pt)
         Q4D_COMMITS "}"
         ::"r"(d), "r"(ta), "l"(b0), "r"(idesc), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
@@ -662,7 +663,7 @@ __device__ __forceinline__ void q4d_stage_down(uint32_t d, uint32_t ta, uint64_t
         "setp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         Q4D_MMA(0, 0, 0, pf) Q4D_MMA(0, 8, 2, pt) Q4D_MMA(0, 16, 4, pt) Q4D_MMA(0, 24, 6, pt)
-        Q4D_MMA(64, 32, 256, pf) Q4D_MMA(64, 40, 258, pt) Q4D_MMA(64, 48, 260, pt) Q4D_MMA(64, 56, 262, pt)
+        Q4D_MMA(32, 32, 128, pf) Q4D_MMA(32, 40, 130, pt) Q4D_MMA(32, 48, 132, pt) Q4D_MMA(32, 56, 134, pt)
         Q4D_COMMITS "}"
         ::"r"(d), "r"(ta), "l"(b0), "r"(idesc), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
@@ -926,7 +927,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         mbar_wait_drain(smem_u32(drain), 0, wt);
     } else if (warp >= 2) {
         // ------------------------------------------------ consumers
-        // One warp per lane quadrant (its 32 rows), the tile's tokens in two halves of 16.
+        // One warp per lane quadrant (its 32 rows), the tile's tokens (at most 16) in registers.
         const int q = warp & 3;
         const int row = 32 * q + lane;
         const float cc = p.cc, bstep = p.b;
@@ -936,7 +937,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         while (live) {
             if (!mbar_wait(smem_u32(&tmf[slot]), mphase, wt)) break;
             const int *tm = tmeta + 8 * slot;
-            const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], N = tm[5], nstage = tm[6];
+            const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], nstage = tm[6];
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tme[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
@@ -948,9 +949,9 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const uint16_t *sc_u = reinterpret_cast<const uint16_t *>(sd + kScaleBytes / 2);  // up
             const float *bs = reinterpret_cast<const float *>(sd + kScaleBytes);              // block sums
             const int nblk = down ? nblk_i : nblk_h;
-            float acc0[32], acc1[32];
+            float acc0[kDN], acc1[kDN];
 #pragma unroll
-            for (int t = 0; t < 32; ++t) acc0[t] = acc1[t] = 0.f;
+            for (int t = 0; t < kDN; ++t) acc0[t] = acc1[t] = 0.f;
             for (int ks = 0; ks < nstage; ++ks) {
                 if (!mbar_wait(smem_u32(&pfull[pb]), pp, wt)) {
                     live = false;
@@ -965,38 +966,30 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                         g[2 * h2] = bf16_bits_to_f32(sc_a[row * nblk + 2 * ks + h2]) * bstep;
                         g[2 * h2 + 1] = bf16_bits_to_f32(sc_u[row * nblk + 2 * ks + h2]) * bstep;
                     }
+                    // gate and up partials of both blocks (gate 0, up 0, gate 1, up 1), one wait
+                    float v[4][16];
+                    tmem_ld16x4(ta, ta + 16, ta + 32, ta + 48, v);
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        if (hf * 16 >= N) break;  // warp-uniform
-                        // gate and up partials of both blocks for these 16 tokens, one wait
-                        float v[4][16];
-                        tmem_ld16x4(ta + hf * 16, ta + 32 + hf * 16, ta + 64 + hf * 16, ta + 96 + hf * 16, v);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int blk = 2 * ks + h2;
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const int blk = 2 * ks + h2;
-#pragma unroll
-                            for (int t = 0; t < 16; ++t) {
-                                const float cs = cc * bs[(hf * 16 + t) * sxs + blk];
-                                acc0[hf * 16 + t] = fmaf(g[2 * h2], v[2 * h2][t] - cs, acc0[hf * 16 + t]);
-                                acc1[hf * 16 + t] = fmaf(g[2 * h2 + 1], v[2 * h2 + 1][t] - cs, acc1[hf * 16 + t]);
-                            }
+                        for (int t = 0; t < kDN; ++t) {
+                            const float cs = cc * bs[t * sxs + blk];
+                            acc0[t] = fmaf(g[2 * h2], v[2 * h2][t] - cs, acc0[t]);
+                            acc1[t] = fmaf(g[2 * h2 + 1], v[2 * h2 + 1][t] - cs, acc1[t]);
                         }
                     }
                 } else {
                     const int blk = 2 * ks;
                     const float g0 = bf16_bits_to_f32(sc_a[row * nblk + blk]) * bstep;
                     const float g1 = bf16_bits_to_f32(sc_a[row * nblk + blk + 1]) * bstep;
+                    float v0[16], v1[16];
+                    tmem_ld16x2(ta, ta + 32, v0, v1);  // blocks 2 ks and 2 ks + 1
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        if (hf * 16 >= N) break;  // warp-uniform
-                        float v0[16], v1[16];
-                        tmem_ld16x2(ta + hf * 16, ta + 64 + hf * 16, v0, v1);  // blocks 2 ks and 2 ks + 1
-#pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            const float *s2 = bs + (hf * 16 + t) * shs + blk * 2;
-                            float a0 = fmaf(g0, v0[t] - cc * (s2[0] + s2[1]), acc0[hf * 16 + t]);
-                            acc0[hf * 16 + t] = fmaf(g1, v1[t] - cc * (s2[2] + s2[3]), a0);
-                        }
+                    for (int t = 0; t < kDN; ++t) {
+                        const float *s2 = bs + t * shs + blk * 2;
+                        const float a0 = fmaf(g0, v0[t] - cc * (s2[0] + s2[1]), acc0[t]);
+                        acc0[t] = fmaf(g1, v1[t] - cc * (s2[2] + s2[3]), a0);
                     }
                 }
                 tc_fence_before();
@@ -1023,7 +1016,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             }
             if (down) {
 #pragma unroll
-                for (int t = 0; t < 32; ++t)
+                for (int t = 0; t < kDN; ++t)
                     if (t < m) {
                         const size_t pr = (size_t)(r0 + t);
                         float val = acc0[t];
@@ -1035,7 +1028,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 // sums over this warp's 32 rows (half of a 64-row block) go to sh[token][block][half]
                 const int hcol = (col & ~7) | sigma_inv(col & 7);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
+                for (int t = 0; t < kDN; ++t) {
                     float hv = 0.f;
                     if (t < m) {
                         const size_t pr = (size_t)(r0 + t);
@@ -1050,9 +1043,13 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                     }
                     acc0[t] = hv;
                 }
-                // reduce-scatter over the warp: lane l ends with the sum over the 32 rows of token l
+                // sum over the 32 rows: fold the upper 16 lanes in, then a reduce-scatter leaves
+                // lane l (l < 16) with the sum of token l
+                static_assert(kDN == 16, "the reduction below covers 16 tokens");
 #pragma unroll
-                for (int w2 = 16; w2 >= 1; w2 >>= 1) {
+                for (int t = 0; t < kDN; ++t) acc0[t] += __shfl_xor_sync(0xffffffffu, acc0[t], 16);
+#pragma unroll
+                for (int w2 = 8; w2 >= 1; w2 >>= 1) {
                     const bool upper = (lane & w2) != 0;
 #pragma unroll
                     for (int i = 0; i < w2; ++i) {
@@ -1061,7 +1058,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                         acc0[i] = keep + __shfl_xor_sync(0xffffffffu, send, w2);
                     }
                 }
-                if (lane < m) {
+                if (lane < 16 && lane < m) {
                     const int blk_h = (rb * kRows + 32 * q) / kSlab;
                     p.sh[(size_t)(r0 + lane) * shs + blk_h * 2 + (q & 1)] = acc0[0];
                 }
