@@ -85,8 +85,8 @@ struct Params {
     float b, cc;                    // decode kernel: codebook step b and 128 + j0
     uint32_t nib_mask, nib_bias;    // 0x000F000F and bf16x2 128.0: operands of the dequant LOP3s
     uint32_t nib_mask2;             // 0x001E001E (large-batch kernel: codes doubled)
-    const float *sx;                // decode kernel: block sums of the token rows [A][sx_stride(H)]
-    float *sh;                      // decode kernel: block sums of h, two halves [A][sh_stride(I)]
+    const float *sx;                // decode kernel: (128 + j0) x the token rows' block sums [A][sx_stride(H)]
+    float *sh;                      // decode kernel: the same for h, two halves [A][sh_stride(I)]
     int E, H, I, A;
     int cmax;                       // token chunk (fixed chunks of cmax, see chunk_base)
     unsigned long long wait_ns;     // limit of every bounded wait
@@ -535,9 +535,9 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 //    TMEM ring.
 //  * The consumer warps add the block's term s[row][blk] b (P[row][t] - (128 + j0) S[t][blk])
 //    -- which is sum_k c_{j_k} s x[t][k], since c_j = b (j - j0) -- to fp32 registers, with
-//    S[t][blk] the sum of the block's token values: formed for the token rows by the prep
-//    kernel and, for h, from the rounded h values the gate/up consumers store (two
-//    32-row halves per block, added in a fixed order).
+//    S[t][blk] the sum of the block's token values.  (128 + j0) S is stored ready-made: for
+//    the token rows by the prep kernel, for h by the gate/up consumers from the rounded h
+//    values they store (two 32-row halves per block, added in a fixed order).
 // Per 8 weights the dequant costs 7 integer operations instead of 16, and the scales cost
 // two fp32 operations per (row, token, block) instead of one bf16 multiply per weight.
 // A stage is 128 input elements (two blocks) of a tile's 128 rows, of both gate and up on a
@@ -974,7 +974,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                         const int blk = 2 * ks + h2;
 #pragma unroll
                         for (int t = 0; t < kDN; ++t) {
-                            const float cs = cc * bs[t * sxs + blk];
+                            const float cs = bs[t * sxs + blk];  // (128 + j0) S
                             acc0[t] = fmaf(g[2 * h2], v[2 * h2][t] - cs, acc0[t]);
                             acc1[t] = fmaf(g[2 * h2 + 1], v[2 * h2 + 1][t] - cs, acc1[t]);
                         }
@@ -988,8 +988,8 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 #pragma unroll
                     for (int t = 0; t < kDN; ++t) {
                         const float *s2 = bs + t * shs + blk * 2;
-                        const float a0 = fmaf(g0, v0[t] - cc * (s2[0] + s2[1]), acc0[t]);
-                        acc0[t] = fmaf(g1, v1[t] - cc * (s2[2] + s2[3]), a0);
+                        const float a0 = fmaf(g0, v0[t] - (s2[0] + s2[1]), acc0[t]);  // halves hold (128 + j0) S / 2
+                        acc0[t] = fmaf(g1, v1[t] - (s2[2] + s2[3]), a0);
                     }
                 }
                 tc_fence_before();
@@ -1060,7 +1060,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 }
                 if (lane < 16 && lane < m) {
                     const int blk_h = (rb * kRows + 32 * q) / kSlab;
-                    p.sh[(size_t)(r0 + lane) * shs + blk_h * 2 + (q & 1)] = acc0[0];
+                    p.sh[(size_t)(r0 + lane) * shs + blk_h * 2 + (q & 1)] = cc * acc0[0];
                 }
                 // publish this warp's h rows and block sums (read back by down tiles: h through TMA)
                 asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -1084,14 +1084,14 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 }
 
 // x_perm[p] = x[order[p] / k] with every 8-element group in the weights' order
-// (0,4,1,5,2,6,3,7), and with sx the row's sums over its 64-element blocks (fp32, a fixed
-// order: 8 elements per lane, then three shuffle steps).  Block 0 builds the tile list (an
+// (0,4,1,5,2,6,3,7), and with sx the row's sums over its 64-element blocks times cc = 128 + j0
+// (fp32, a fixed order: 8 elements per lane, then three shuffle steps, then the product).  Block 0 builds the tile list (an
 // expert's tokens in fixed chunks of cmax; all gate/up tiles before all down tiles) and
 // clears the scheduling counters.
 __global__ void __launch_bounds__(256)
 q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, int T, int k, int H, int I, int E,
                int cmax, int max_tiles, uint16_t *__restrict__ x_perm,
-               uint32_t *tiles, int *sched, int *done, int32_t *err, float *sx) {
+               uint32_t *tiles, int *sched, int *done, int32_t *err, float *sx, float cc) {
     griddep_launch_dependents();
     griddep_wait();
     if (blockIdx.x > 0) {
@@ -1125,7 +1125,7 @@ q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, 
                     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
                     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
                     sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                    if ((lane & 7) == 0 && i + 32 * u < n) sx[(size_t)pr * sx_stride(H) + (i + 32 * u) / 8] = sum;
+                    if ((lane & 7) == 0 && i + 32 * u < n) sx[(size_t)pr * sx_stride(H) + (i + 32 * u) / 8] = cc * sum;
                 }
             }
 #pragma unroll
@@ -1274,7 +1274,7 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     const int cmax = decode ? kDN : kChunkN;
     cudaError_t e = launch_pdl(q4_prep_kernel, dim3(prep_blocks(A)), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
                                offsets, s.T, s.k, s.H, s.I, s.E, cmax, (int)q4_max_tiles(s), x_perm, tiles, sched,
-                               done, err, decode ? sx : nullptr);
+                               done, err, decode ? sx : nullptr, 128.0f + 0.5f * float(t2));
     if (e != cudaSuccess) return e;
     if (!(decode ? set_decode_attr<false>() && set_decode_attr<true>()
                  : set_attr<kChunkN, 4, false>() && set_attr<kChunkN, 4, true>()))
