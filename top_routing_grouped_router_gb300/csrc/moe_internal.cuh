@@ -133,6 +133,16 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Arrival on a global counter with acquire-release semantics at GPU scope: after a barrier of
+// the arriving block (so that its threads' writes happen before the arrival), the block that
+// sees the last count also sees every other block's writes, with no separate fences.  Returns
+// the previous count.
+__device__ __forceinline__ int arrive_acq_rel(int *p) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
+}
+
 // Records the first device-side error in the workspace error word.
 __device__ __forceinline__ void record_error(int32_t *err, int code) { atomicCAS(err, 0, code); }
 

@@ -315,13 +315,11 @@ route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const floa
     if (!a.fuse) return;
     // the last expert block of this token group to finish sees all its logits: top-k,
     // one warp per token
-    __threadfence();
     __syncthreads();
     int *group_arrivals = a.arrivals + 1 + blockIdx.y;
-    if (threadIdx.x == 0) s_last = atomicAdd(group_arrivals, 1) == int(gridDim.x) - 1;
+    if (threadIdx.x == 0) s_last = arrive_acq_rel(group_arrivals) == int(gridDim.x) - 1;
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     // with a single token group this block also permutes, from the ids in shared memory
     const bool one_group = gridDim.y == 1;
     __shared__ int s_ids[kTPB * kMaxK];
@@ -334,12 +332,10 @@ route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const floa
     if (a.fuse < 2) return;
     if (!one_group) {
         // the last token group to finish permutes the whole batch
-        __threadfence();
         __syncthreads();
-        if (threadIdx.x == 0) s_last = atomicAdd(a.arrivals, 1) == int(gridDim.y) - 1;
+        if (threadIdx.x == 0) s_last = arrive_acq_rel(a.arrivals) == int(gridDim.y) - 1;
         __syncthreads();
         if (!s_last) return;
-        __threadfence();
         if (threadIdx.x == 0) *a.arrivals = 0;
     } else {
         __syncthreads();
