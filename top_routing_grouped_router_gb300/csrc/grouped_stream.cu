@@ -239,8 +239,11 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
     __syncthreads();
     tc_fence_after();
     // everything above overlaps the previous kernel; from here on its outputs are read
-    griddep_launch_dependents();
+    // dependents are released only after this grid's own wait: a kernel launched after this one
+    // then finds every kernel before this one complete, and may read their results before its
+    // own wait (the un-permute of the fused decode path does)
     griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
     const bool router = p.router_tiles > 0;
     const int erb = (p.E + kRows - 1) / kRows;  // expert row blocks in router mode

@@ -228,7 +228,9 @@ int forward_impl(const moe_shape &s, const void *x, const void *w_router, const 
         MOE_TRY(do_permute(s, ids, at<int32_t>(workspace, L.counts), offsets, order, pos, workspace, st));
     }
     MOE_TRY(do_grouped(s, xe, offsets, order, w_gate, w_up, w_down, q4, y, workspace, st, lora, prebuilt));
-    return launch_rc(launch_unpermute(s, y, w, pos, out, st, resid));
+    // after the bf16 expert kernel of the fused decode path (it releases its dependents only
+    // after its own wait), w and pos may be read before the un-permute's wait
+    return launch_rc(launch_unpermute(s, y, w, pos, out, st, resid, prebuilt));
 }
 
 }  // namespace

@@ -260,6 +260,6 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
                       int32_t *err, cudaStream_t st, const moe_lora *lora = nullptr, float *xa = nullptr,
                       float *ha = nullptr, float *lpart = nullptr);
 cudaError_t launch_unpermute(const moe_shape &s, const void *y, const float *w, const int32_t *pos, void *out,
-                             cudaStream_t st, const void *resid = nullptr);
+                             cudaStream_t st, const void *resid = nullptr, bool early = false);
 
 }  // namespace moe

@@ -41,19 +41,36 @@ __device__ __forceinline__ void unp_store8(uint16_t *p, const float *v) {
 // kBatch slots at a time: every position and weight of a batch, then every row, is
 // requested before the first is used (the sum stays in slot order).  Small batches are
 // latency-bound and take kBatch = 8; large ones need the occupancy of kBatch = 1.
+// Slots [j0, j0 + kBatch) of token t: positions (-1 past k) and weights.
+template <int kBatch>
+__device__ __forceinline__ void unp_slots(const float *w, const int32_t *pos, int t, int j0, int k, int *pp,
+                                          float *ww) {
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+        pp[j] = j0 + j < k ? ldp(pos + (size_t)t * k + j0 + j) : -1;
+        ww[j] = j0 + j < k ? ldp(w + (size_t)t * k + j0 + j) : 0.f;
+    }
+}
+
+// pp0 / ww0, when given, are the first batch of slots, already read.
 template <int kBatch, typename T>
 __device__ __forceinline__ void unpermute8(const T *y, const float *w, const int32_t *pos, T *out, int t, int c0,
-                                           int k, int H, int A, const T *resid = nullptr) {
+                                           int k, int H, int A, const T *resid = nullptr, const int *pp0 = nullptr,
+                                           const float *ww0 = nullptr) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
     for (int j0 = 0; j0 < k; j0 += kBatch) {
         int pp[kBatch];
         float ww[kBatch];
+        if (j0 == 0 && pp0) {
 #pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            pp[j] = j0 + j < k ? ldp(pos + (size_t)t * k + j0 + j) : -1;
-            ww[j] = j0 + j < k ? ldp(w + (size_t)t * k + j0 + j) : 0.f;
+            for (int j = 0; j < kBatch; ++j) {
+                pp[j] = pp0[j];
+                ww[j] = ww0[j];
+            }
+        } else {
+            unp_slots<kBatch>(w, pos, t, j0, k, pp, ww);
         }
         float v[kBatch][8];
 #pragma unroll
