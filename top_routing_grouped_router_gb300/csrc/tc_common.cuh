@@ -129,7 +129,8 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, c
 }
 
 // Bounded wait until the global counter *p reaches `need` (acquire); same limit.  Returns
-// false when it gave up (or the CTA is aborting).
+// false when it gave up (or the CTA is aborting).  Each test is an L2 round trip, which paces
+// the loop; a sleep between tests only delayed the waiter (by microseconds).
 __device__ __forceinline__ bool wait_count(const int *p, int need, const Waits &w) {
     unsigned long long t0 = 0;
     for (uint32_t n = 0;; ++n) {
@@ -144,7 +145,6 @@ __device__ __forceinline__ bool wait_count(const int *p, int need, const Waits &
             *w.abort = 1;
             return false;
         }
-        __nanosleep(64);
     }
 }
 
