@@ -584,8 +584,85 @@ __device__ __forceinline__ void codes_to_ints(const uint4 cw, uint32_t *v, uint3
     }
 }
 
-// Two loads of 16 fp32 columns of this thread's lane, one wait.
-__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float *a, float *b) {
+// G loads of NT fp32 columns (4, 8 or 16) of this thread's TMEM lane, one wait.
+template <int NT, int G>
+__device__ __forceinline__ void tmem_ld_cols(const uint32_t (&t)[G], float (&v)[G][NT]);
+
+template <>
+__device__ __forceinline__ void tmem_ld_cols<4, 2>(const uint32_t (&t)[2], float (&v)[2][4]) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%8];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%4, %5, %6, %7}, [%9];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(t[0]), "r"(t[1])
+        : "memory");
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[k][i] = __uint_as_float(r[4 * k + i]);
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld_cols<4, 4>(const uint32_t (&t)[4], float (&v)[4][4]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%4, %5, %6, %7}, [%17];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%8, %9, %10, %11}, [%18];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%12, %13, %14, %15}, [%19];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(t[0]), "r"(t[1]), "r"(t[2]), "r"(t[3])
+        : "memory");
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[k][i] = __uint_as_float(r[4 * k + i]);
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld_cols<8, 2>(const uint32_t (&t)[2], float (&v)[2][8]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(t[0]), "r"(t[1])
+        : "memory");
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[k][i] = __uint_as_float(r[8 * k + i]);
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld_cols<8, 4>(const uint32_t (&t)[4], float (&v)[4][8]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%33];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16, %17, %18, %19, %20, %21, %22, %23}, [%34];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24, %25, %26, %27, %28, %29, %30, %31}, [%35];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(t[0]), "r"(t[1]), "r"(t[2]), "r"(t[3])
+        : "memory");
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[k][i] = __uint_as_float(r[8 * k + i]);
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld_cols<16, 2>(const uint32_t (&t)[2], float (&v)[2][16]) {
     uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
@@ -595,17 +672,16 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float *a, 
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(ta), "r"(tb)
+        : "r"(t[0]), "r"(t[1])
         : "memory");
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        a[i] = __uint_as_float(r[i]);
-        b[i] = __uint_as_float(r[16 + i]);
-    }
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[k][i] = __uint_as_float(r[16 * k + i]);
 }
 
-// Four loads of 16 fp32 columns of this thread's lane, one wait.
-__device__ __forceinline__ void tmem_ld16x4(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3, float (*v)[16]) {
+template <>
+__device__ __forceinline__ void tmem_ld_cols<16, 4>(const uint32_t (&t)[4], float (&v)[4][16]) {
     uint32_t r[64];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%64];\n\t"
@@ -621,12 +697,12 @@ __device__ __forceinline__ void tmem_ld16x4(uint32_t t0, uint32_t t1, uint32_t t
           "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
           "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
           "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(t0), "r"(t1), "r"(t2), "r"(t3)
+        : "r"(t[0]), "r"(t[1]), "r"(t[2]), "r"(t[3])
         : "memory");
 #pragma unroll
-    for (int g = 0; g < 4; ++g)
+    for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[g][i] = __uint_as_float(r[16 * g + i]);
+        for (int i = 0; i < 16; ++i) v[k][i] = __uint_as_float(r[16 * k + i]);
 }
 
 // A stage's MMAs and its three commits in one block, issued by one elected lane of the converged
@@ -670,6 +746,178 @@ __device__ __forceinline__ void q4d_stage_down(uint32_t d, uint32_t ta, uint64_t
 }
 #undef Q4D_MMA
 #undef Q4D_COMMITS
+
+// A consumer warp's fixed state: its TMEM lane quadrant, row, block-sum strides, block
+// counts and the partial ring (barrier addresses, entry and phase).
+struct Q4DCons {
+    uint32_t tq;  // TMEM address of lane 32 q, column 0
+    int row, lane, q, sxs, shs, nblk_h, nblk_i;
+    uint32_t pfull, pempty;  // shared addresses of the partial ring's barriers
+    int pb;
+    uint32_t pp;
+};
+// One tile as a consumer sees it: its side buffer (scales, then the tokens' block sums) and
+// the barrier that frees it.
+struct Q4DTile {
+    int down, e, rb, r0, m, nstage;
+    uint32_t side, sempty;
+};
+
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// A consumer's whole tile: per stage, the partials of the first NT token columns (NT >= the
+// chunk's m) are corrected by the block sums, scaled and accumulated; then SwiGLU and the h
+// store (gate/up) or the y store (down).  Returns false when a wait gave up.
+template <int NT, bool kLora>
+__device__ __forceinline__ bool q4d_consume_tile(const Params &p, const Waits &wt, Q4DCons &c, const Q4DTile &t) {
+    const bool down = t.down != 0;
+    const int nblk = down ? c.nblk_i : c.nblk_h;
+    // this row's block scales (bf16, blocks consecutive) of gate (or down) and up, and the block sums
+    const uint32_t sg = t.side + uint32_t(c.row * nblk) * 2u;
+    const uint32_t su = sg + kScaleBytes / 2;
+    const uint32_t bsa = t.side + kScaleBytes;
+    const float bstep = p.b;
+    // gate/up rows hold a multiple of 8 blocks: one 16-byte load covers four stages
+    const bool vec8 = nblk % 8 == 0;
+    uint4 g4 = make_uint4(0, 0, 0, 0), u4 = g4;
+    float acc0[NT], acc1[NT];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) acc0[i] = acc1[i] = 0.f;
+    for (int ks = 0; ks < t.nstage; ++ks) {
+        if (!mbar_wait(c.pfull + 8u * c.pb, c.pp, wt)) return false;
+        tc_fence_after();
+        const uint32_t ta = c.tq + uint32_t(c.pb * kDPartCols);
+        if (!down) {
+            uint32_t gw, uw;  // the scales of blocks 2 ks (low half) and 2 ks + 1 (high half)
+            if (vec8) {
+                if ((ks & 3) == 0) {
+                    g4 = lds_v4(sg + 16u * uint32_t(ks >> 2));
+                    u4 = lds_v4(su + 16u * uint32_t(ks >> 2));
+                }
+                gw = g4.x;
+                uw = u4.x;
+                g4 = make_uint4(g4.y, g4.z, g4.w, 0u);
+                u4 = make_uint4(u4.y, u4.z, u4.w, 0u);
+            } else {
+                gw = lds_u32(sg + 4u * uint32_t(ks));
+                uw = lds_u32(su + 4u * uint32_t(ks));
+            }
+            const float g0 = __uint_as_float(gw << 16) * bstep, g1 = __uint_as_float(gw & 0xffff0000u) * bstep;
+            const float u0 = __uint_as_float(uw << 16) * bstep, u1 = __uint_as_float(uw & 0xffff0000u) * bstep;
+            // gate and up partials of both blocks (gate 0, up 0, gate 1, up 1), one wait
+            float v[4][NT];
+            const uint32_t tt[4] = {ta, ta + 16, ta + 32, ta + 48};
+            tmem_ld_cols<NT, 4>(tt, v);
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                const float2 cs = lds_f2(bsa + uint32_t(i * c.sxs + 2 * ks) * 4u);  // (128 + j0) S of both blocks
+                acc0[i] = fmaf(g0, v[0][i] - cs.x, acc0[i]);
+                acc1[i] = fmaf(u0, v[1][i] - cs.x, acc1[i]);
+                acc0[i] = fmaf(g1, v[2][i] - cs.y, acc0[i]);
+                acc1[i] = fmaf(u1, v[3][i] - cs.y, acc1[i]);
+            }
+        } else {
+            const uint32_t dw = lds_u32(sg + 4u * uint32_t(ks));  // blocks 2 ks, 2 ks + 1
+            const float g0 = __uint_as_float(dw << 16) * bstep, g1 = __uint_as_float(dw & 0xffff0000u) * bstep;
+            float v[2][NT];
+            const uint32_t tt[2] = {ta, ta + 32};
+            tmem_ld_cols<NT, 2>(tt, v);
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                const float4 s2 = lds_f4(bsa + uint32_t(i * c.shs + 4 * ks) * 4u);  // halves hold (128 + j0) S / 2
+                const float a0 = fmaf(g0, v[0][i] - (s2.x + s2.y), acc0[i]);
+                acc0[i] = fmaf(g1, v[1][i] - (s2.z + s2.w), a0);
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (c.lane == 0) mbar_arrive(c.pempty + 8u * c.pb);
+        if (++c.pb == kDPS) { c.pb = 0; c.pp ^= 1; }
+    }
+    // the tile's scales and block sums are no longer needed
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(t.sempty);
+    const int col = t.rb * kRows + c.row;
+    const LoraDev &lr = p.lora;
+    const bool lora = kLora && lr.rank > 0;
+    float lb0[16], lb1[16];
+    if (lora) {
+        if (down) {
+            lora_row16(lr.bd, (size_t)t.e * p.H + col, lr.rank, lb0);
+        } else {
+            lora_row16(lr.bg, (size_t)t.e * p.I + col, lr.rank, lb0);
+            lora_row16(lr.bu, (size_t)t.e * p.I + col, lr.rank, lb1);
+        }
+    }
+    if (down) {
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+            if (i < t.m) {
+                const size_t pr = (size_t)(t.r0 + i);
+                float val = acc0[i];
+                if (lora) val += lr.scale * lora_dot16(lb0, lr.ha + pr * 16);
+                p.y[pr * p.H + col] = f32_to_bf16_bits(val);
+            }
+        return true;
+    }
+    // h is stored in the weights' 8-element group order (see the file comment); its sums over
+    // this warp's 32 rows (half of a 64-row block) go to sh[token][block][half]
+    const int hcol = (col & ~7) | sigma_inv(col & 7);
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+        float hv = 0.f;
+        if (i < t.m) {
+            const size_t pr = (size_t)(t.r0 + i);
+            float gv = acc0[i], uv = acc1[i];
+            if (lora) {
+                gv += lr.scale * lora_dot16(lb0, lr.xa + pr * 32);
+                uv += lr.scale * lora_dot16(lb1, lr.xa + pr * 32 + 16);
+            }
+            const uint16_t hb = f32_to_bf16_bits(swiglu(gv, uv));
+            p.h[pr * p.I + hcol] = hb;
+            hv = bf16_bits_to_f32(hb);
+        }
+        acc0[i] = hv;
+    }
+    // sum over the 32 rows: fold the lanes down to NT groups, then a reduce-scatter leaves
+    // lane l (l < NT) with the sum of token l
+#pragma unroll
+    for (int o = 16; o >= NT; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < NT; ++i) acc0[i] += __shfl_xor_sync(0xffffffffu, acc0[i], o);
+#pragma unroll
+    for (int w2 = NT / 2; w2 >= 1; w2 >>= 1) {
+        const bool upper = (c.lane & w2) != 0;
+#pragma unroll
+        for (int i = 0; i < w2; ++i) {
+            const float send = upper ? acc0[i] : acc0[i + w2];
+            const float keep = upper ? acc0[i + w2] : acc0[i];
+            acc0[i] = keep + __shfl_xor_sync(0xffffffffu, send, w2);
+        }
+    }
+    if (c.lane < NT && c.lane < t.m) {
+        const int blk_h = (t.rb * kRows + 32 * c.q) / kSlab;
+        p.sh[(size_t)(t.r0 + c.lane) * c.shs + blk_h * 2 + (c.q & 1)] = p.cc * acc0[0];
+    }
+    // publish this warp's h rows and block sums (read back by down tiles: h through TMA)
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (c.lane == 0) {
+        __threadfence();
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done + t.e) : "memory");
+    }
+    return true;
+}
 
 template <bool kLora>
 __global__ void __launch_bounds__(kDThreads, 1)
@@ -870,12 +1118,14 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 // before the first conversion (the asm statements keep their order).
                 const uint32_t cb = smem_u32(raw + r * kDRawBytes) + uint32_t(row * (kDK / 2));
                 const uint32_t ta = tlane + uint32_t(kDACol + a * kDAStageCols);
+                // (64-byte swizzle: the row's 16-byte chunk i sits at chunk i ^ ((row >> 1) & 3))
+                const int sw = (row >> 1) & 3;
                 uint4 c[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) c[i] = lds_v4(cb + 16 * i);
+                for (int i = 0; i < 4; ++i) c[i] = lds_v4(cb + 16 * (i ^ sw));
                 if (!down) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) c[4 + i] = lds_v4(cb + kDCodeBytes + 16 * i);
+                    for (int i = 0; i < 4; ++i) c[4 + i] = lds_v4(cb + kDCodeBytes + 16 * (i ^ sw));
                 }
                 const uint32_t km = p.nib_mask, kc = p.nib_bias;
                 uint32_t v[64];  // one matrix's two slabs: 64 columns, one store
@@ -927,14 +1177,15 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         mbar_wait_drain(smem_u32(drain), 0, wt);
     } else if (warp >= 2) {
         // ------------------------------------------------ consumers
-        // One warp per lane quadrant (its 32 rows), the tile's tokens (at most 16) in registers.
+        // One warp per lane quadrant (its 32 rows); a tile's tokens (at most 16) in registers,
+        // only as many token columns as the chunk needs (4, 8 or 16) read and accumulated.
         const int q = warp & 3;
         const int row = 32 * q + lane;
-        const float cc = p.cc, bstep = p.b;
-        int slot = 0, tiles = 0, pb = 0;
-        uint32_t mphase = 0, pp = 0;
-        bool live = true;
-        while (live) {
+        Q4DCons c{tmem_base + (uint32_t(32 * q) << 16), row, lane, q, sxs, shs, nblk_h, nblk_i,
+                  smem_u32(pfull), smem_u32(pempty), 0, 0u};
+        int slot = 0, tiles = 0;
+        uint32_t mphase = 0;
+        for (;;) {
             if (!mbar_wait(smem_u32(&tmf[slot]), mphase, wt)) break;
             const int *tm = tmeta + 8 * slot;
             const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], nstage = tm[6];
@@ -944,132 +1195,14 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             if (down < 0 || abort_raised(wt)) break;
             const int sb = tiles & 1;
             if (!mbar_wait(smem_u32(&sfull[sb]), (tiles >> 1) & 1, wt)) break;
-            const uint8_t *sd = side + sb * kDSide;
-            const uint16_t *sc_a = reinterpret_cast<const uint16_t *>(sd);                    // gate / down
-            const uint16_t *sc_u = reinterpret_cast<const uint16_t *>(sd + kScaleBytes / 2);  // up
-            const float *bs = reinterpret_cast<const float *>(sd + kScaleBytes);              // block sums
-            const int nblk = down ? nblk_i : nblk_h;
-            float acc0[kDN], acc1[kDN];
-#pragma unroll
-            for (int t = 0; t < kDN; ++t) acc0[t] = acc1[t] = 0.f;
-            for (int ks = 0; ks < nstage; ++ks) {
-                if (!mbar_wait(smem_u32(&pfull[pb]), pp, wt)) {
-                    live = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t ta = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(pb * kDPartCols);
-                if (!down) {
-                    float g[4];  // gate and up scale x b of the stage's two blocks
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        g[2 * h2] = bf16_bits_to_f32(sc_a[row * nblk + 2 * ks + h2]) * bstep;
-                        g[2 * h2 + 1] = bf16_bits_to_f32(sc_u[row * nblk + 2 * ks + h2]) * bstep;
-                    }
-                    // gate and up partials of both blocks (gate 0, up 0, gate 1, up 1), one wait
-                    float v[4][16];
-                    tmem_ld16x4(ta, ta + 16, ta + 32, ta + 48, v);
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int blk = 2 * ks + h2;
-#pragma unroll
-                        for (int t = 0; t < kDN; ++t) {
-                            const float cs = bs[t * sxs + blk];  // (128 + j0) S
-                            acc0[t] = fmaf(g[2 * h2], v[2 * h2][t] - cs, acc0[t]);
-                            acc1[t] = fmaf(g[2 * h2 + 1], v[2 * h2 + 1][t] - cs, acc1[t]);
-                        }
-                    }
-                } else {
-                    const int blk = 2 * ks;
-                    const float g0 = bf16_bits_to_f32(sc_a[row * nblk + blk]) * bstep;
-                    const float g1 = bf16_bits_to_f32(sc_a[row * nblk + blk + 1]) * bstep;
-                    float v0[16], v1[16];
-                    tmem_ld16x2(ta, ta + 32, v0, v1);  // blocks 2 ks and 2 ks + 1
-#pragma unroll
-                    for (int t = 0; t < kDN; ++t) {
-                        const float *s2 = bs + t * shs + blk * 2;
-                        const float a0 = fmaf(g0, v0[t] - (s2[0] + s2[1]), acc0[t]);  // halves hold (128 + j0) S / 2
-                        acc0[t] = fmaf(g1, v1[t] - (s2[2] + s2[3]), a0);
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&pempty[pb]));
-                if (++pb == kDPS) { pb = 0; pp ^= 1; }
-            }
-            if (!live) break;
-            // the tile's scales and block sums are no longer needed
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sempty[sb]));
+            const Q4DTile t{down, e, rb, r0, m, nstage, smem_u32(side + sb * kDSide), smem_u32(&sempty[sb])};
+            // (the adapter variant keeps one width: three inlined copies of its epilogue spill)
+            const bool ok = kLora     ? q4d_consume_tile<16, kLora>(p, wt, c, t)
+                            : m <= 4 ? q4d_consume_tile<4, kLora>(p, wt, c, t)
+                            : m <= 8 ? q4d_consume_tile<8, kLora>(p, wt, c, t)
+                                     : q4d_consume_tile<16, kLora>(p, wt, c, t);
+            if (!ok) break;
             ++tiles;
-            const int col = rb * kRows + row;
-            const LoraDev &lr = p.lora;
-            const bool lora = kLora && lr.rank > 0;
-            float lb0[16], lb1[16];
-            if (lora) {
-                if (down) {
-                    lora_row16(lr.bd, (size_t)e * p.H + col, lr.rank, lb0);
-                } else {
-                    lora_row16(lr.bg, (size_t)e * p.I + col, lr.rank, lb0);
-                    lora_row16(lr.bu, (size_t)e * p.I + col, lr.rank, lb1);
-                }
-            }
-            if (down) {
-#pragma unroll
-                for (int t = 0; t < kDN; ++t)
-                    if (t < m) {
-                        const size_t pr = (size_t)(r0 + t);
-                        float val = acc0[t];
-                        if (lora) val += lr.scale * lora_dot16(lb0, lr.ha + pr * 16);
-                        p.y[pr * p.H + col] = f32_to_bf16_bits(val);
-                    }
-            } else {
-                // h is stored in the weights' 8-element group order (see the file comment); its
-                // sums over this warp's 32 rows (half of a 64-row block) go to sh[token][block][half]
-                const int hcol = (col & ~7) | sigma_inv(col & 7);
-#pragma unroll
-                for (int t = 0; t < kDN; ++t) {
-                    float hv = 0.f;
-                    if (t < m) {
-                        const size_t pr = (size_t)(r0 + t);
-                        float gv = acc0[t], uv = acc1[t];
-                        if (lora) {
-                            gv += lr.scale * lora_dot16(lb0, lr.xa + pr * 32);
-                            uv += lr.scale * lora_dot16(lb1, lr.xa + pr * 32 + 16);
-                        }
-                        const uint16_t hb = f32_to_bf16_bits(swiglu(gv, uv));
-                        p.h[pr * p.I + hcol] = hb;
-                        hv = bf16_bits_to_f32(hb);
-                    }
-                    acc0[t] = hv;
-                }
-                // sum over the 32 rows: fold the upper 16 lanes in, then a reduce-scatter leaves
-                // lane l (l < 16) with the sum of token l
-                static_assert(kDN == 16, "the reduction below covers 16 tokens");
-#pragma unroll
-                for (int t = 0; t < kDN; ++t) acc0[t] += __shfl_xor_sync(0xffffffffu, acc0[t], 16);
-#pragma unroll
-                for (int w2 = 8; w2 >= 1; w2 >>= 1) {
-                    const bool upper = (lane & w2) != 0;
-#pragma unroll
-                    for (int i = 0; i < w2; ++i) {
-                        const float send = upper ? acc0[i] : acc0[i + w2];
-                        const float keep = upper ? acc0[i + w2] : acc0[i];
-                        acc0[i] = keep + __shfl_xor_sync(0xffffffffu, send, w2);
-                    }
-                }
-                if (lane < 16 && lane < m) {
-                    const int blk_h = (rb * kRows + 32 * q) / kSlab;
-                    p.sh[(size_t)(r0 + lane) * shs + blk_h * 2 + (q & 1)] = cc * acc0[0];
-                }
-                // publish this warp's h rows and block sums (read back by down tiles: h through TMA)
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) {
-                    __threadfence();
-                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done + e) : "memory");
-                }
-            }
         }
     }
 
@@ -1265,9 +1398,9 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     const bool decode = s.T <= kDecodeMaxN;
     const uint32_t cbox = decode ? kDK / 2 : kSlab / 2;
     CUtensorMap mg, mu, md, mx, mh;
-    if (!make_map(&mg, wg, (uint64_t)s.E * s.I, s.H / 2, kRows, cbox, true) ||
-        !make_map(&mu, wu, (uint64_t)s.E * s.I, s.H / 2, kRows, cbox, true) ||
-        !make_map(&md, wd, (uint64_t)s.E * s.H, s.I / 2, kRows, cbox, true) ||
+    if (!make_map(&mg, wg, (uint64_t)s.E * s.I, s.H / 2, kRows, cbox, true, decode) ||
+        !make_map(&mu, wu, (uint64_t)s.E * s.I, s.H / 2, kRows, cbox, true, decode) ||
+        !make_map(&md, wd, (uint64_t)s.E * s.H, s.I / 2, kRows, cbox, true, decode) ||
         !make_map(&mx, x_perm, A, s.H, kNBox) || !make_map(&mh, h, A, s.I, kNBox))
         return cudaErrorInvalidValue;
 

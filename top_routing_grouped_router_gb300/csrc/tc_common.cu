@@ -30,7 +30,8 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,
-              bool bytes) {
+              bool bytes, bool swz64) {
+    if (swz64 && (!bytes || box_cols != 64)) return false;
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const uint64_t esz = bytes ? 1 : 2;
@@ -40,7 +41,8 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
     cuuint32_t estr[2] = {1, 1};
     return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swz64 ? CU_TENSOR_MAP_SWIZZLE_64B : bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -303,9 +303,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t *r) {
 
 // 2-D tensor map over a row-major [rows][cols] matrix of `elem_bytes`-byte elements;
 // box = box_cols x box_rows.  bf16 maps use the 128-byte swizzle the MMA descriptors
-// expect; byte maps (4-bit codes) are unswizzled.
+// expect; byte maps (4-bit codes) are unswizzled, or with swz64 (64-byte boxes) take the
+// 64-byte swizzle: 16-byte chunk c of row r lands at chunk c ^ ((r >> 1) & 3), so that
+// eight consecutive rows read by eight lanes fall in distinct banks.
 bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-              uint32_t box_cols = 64, bool bytes = false);
+              uint32_t box_cols = 64, bool bytes = false, bool swz64 = false);
 int sm_count();
 // The bounded waits' limit and the failure-path test's extra publication count
 // (moe_debug_set_waits), read at each launch.
