@@ -548,8 +548,8 @@ constexpr int kDK = 2 * kSlab;                       // input elements per stage
 constexpr int kDCodeBytes = kRows * kDK / 2;         // 8 KB: one matrix's codes of a stage
 constexpr int kDTok = 2 * kDCodeBytes;               // token rows after the gate and up codes
 constexpr int kDTokSlab = kDN * 128;                 // token rows of one 64-element slab (SW128)
-constexpr int kDRawBytes = kDTok + 2 * kDTokSlab;    // 24 KB
-constexpr int kDRawStages = 8;
+constexpr int kDRawBytes = kDTok + 2 * kDTokSlab;    // 20 KB
+constexpr int kDRawStages = 9;
 constexpr int kDAS = 2;                              // TMEM A-ring stages
 constexpr int kDPS = 4;                              // TMEM partial-ring entries
 constexpr int kDPartCols = 64;                       // a stage's partials: block h at 32 h (gate +0, up +16)
@@ -563,6 +563,7 @@ constexpr int kDSide = kScaleBytes + kDSBytes;       // per-tile side buffer: sc
 constexpr int kDSmemBytes = kDRawStages * kDRawBytes + 2 * kDSide + 1024 + 2048;
 static_assert(kDSmemBytes <= 232448, "shared memory");
 static_assert(kDACol + kDAS * kDAStageCols <= kTmemCols, "TMEM columns");
+static_assert(kDN == kNBox && kDTokSlab == kNBox * 128, "a stage's token rows: one 16-row box per slab");
 // Row strides (floats) of the block-sum arrays, padded to 16 bytes so that every bulk copy of
 // consecutive rows starts and ends on a 16-byte boundary: token rows H/64 sums, h rows
 // I/64 blocks x 2 halves.
@@ -1001,17 +1002,27 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             lo = ldp(p.sched + kSchedGateUp);
             ctr = p.sched + kSchedClaimDown;
         }
+        // the next tile's record (entry and its expert's offsets) is fetched while the current
+        // tile streams, so that no tile starts with a chain of L2 round trips
         int next = lo + atomicAdd(ctr, 1);
+        uint32_t nentry = 0;
+        int noff = 0, nme = 0;
+        auto fetch = [&](int t) {
+            nentry = ldp(p.tiles + t);
+            const int ne = min(int((nentry >> 16) & 0xFF), p.E - 1);
+            noff = ldp(p.offsets + ne);
+            nme = ldp(p.offsets + ne + 1) - noff;
+        };
+        if (next < hi) fetch(next);
         while (live) {
             const int t = next;
             if (t >= hi || abort_raised(wt)) break;
+            const uint32_t entry = nentry;
+            const int off = noff, me = nme;
             next = lo + atomicAdd(ctr, 1);
-            const uint32_t entry = ldp(p.tiles + t);
             const int down = int(entry >> 31), e0 = int((entry >> 16) & 0xFF), rb = int((entry >> 8) & 0xFF);
             const int nc = int(entry & 0xFF);
             const int e = min(e0, p.E - 1);
-            const int off = ldp(p.offsets + e);
-            const int me = ldp(p.offsets + e + 1) - off;
             const int base = chunk_base(me, kDN, false);
             int m = min(base, me - nc * base);
             if (e0 >= p.E || off < 0 || me <= 0 || off + me > p.A || m <= 0 || m > kDN) {
@@ -1059,10 +1070,11 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                     bulk_load(dst + kScaleBytes, down ? p.sh + (size_t)r0 * shs : p.sx + (size_t)r0 * sxs, ssum, sfb);
                 ++tiles_done;
             }
-            const int nbox = N / kNBox;
-            const uint32_t bytes = (down ? 1 : 2) * kDCodeBytes + 2 * nbox * kNBox * 128;
+            // (N <= kDN = kNBox: the token rows of a stage are one box of both slabs)
+            const uint32_t bytes = (down ? 1 : 2) * kDCodeBytes + 2 * kDTokSlab;
             const int wrow = e * (down ? p.H : p.I) + rb * kRows;
             const CUtensorMap *tokmap = down ? &tm_h : &tm_x;
+            const int kfetch = min(2, nstage - 1);
             for (int ks = 0; ks < nstage; ++ks) {
                 if (!mbar_wait(smem_u32(&rempty[r]), rp ^ 1, wt)) {
                     live = false;
@@ -1078,11 +1090,9 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 const uint32_t base = smem_u32(raw + r * kDRawBytes);
                 tma_load_2d(base, down ? &tm_dc : &tm_gc, ks * (kDK / 2), wrow, fb);
                 if (!down) tma_load_2d(base + kDCodeBytes, &tm_uc, ks * (kDK / 2), wrow, fb);
-                for (int h2 = 0; h2 < 2; ++h2)
-                    for (int q = 0; q < nbox; ++q)
-                        tma_load_2d(base + kDTok + h2 * kDTokSlab + q * 2048, tokmap, (2 * ks + h2) * kSlab,
-                                    r0 + q * kNBox, fb);
+                tma_load_3d(base + kDTok, tokmap, 0, r0, 2 * ks, fb);  // slabs 2 ks and 2 ks + 1
                 if (++r == kDRawStages) { r = 0; rp ^= 1; }
+                if (ks == kfetch && next < hi) fetch(next);
             }
         }
         // no TMA or bulk write may still be landing in this CTA's shared memory when it exits
@@ -1107,13 +1117,16 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         const uint32_t tlane = tmem_base + (uint32_t(32 * q) << 16);
         int r = 0, a = 0;
         uint32_t rp = 0, ap = 0;
+        // An aborting CTA's dequant warps leave at their next wait that does not complete at once
+        // (every wait tests the abort flag then): no flag test per stage.
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&rfull[r]), rp, wt))) break;
-            const uint32_t mt = smem_u32(rmeta + 4 * r);
-            const int down = int(lds_u32(mt)), ks = int(lds_u32(mt + 4));
-            const bool ok = mbar_wait(smem_u32(&aempty[a]), ap ^ 1, wt);
+            const uint2 md = lds_v2(smem_u32(rmeta + 4 * r));
+            const int down = int(md.x), ks = int(md.y);
+            // the sentinel (ks < 0) is passed on to the MMA warp through the A ring
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&aempty[a]), ap ^ 1, wt))) break;
             tc_fence_after();
-            if (__all_sync(0xffffffffu, ok && ks >= 0 && !abort_raised(wt))) {
+            if (ks >= 0) {
                 // a row's codes of a stage are 64 bytes: two slabs of 32.  Every load is issued
                 // before the first conversion (the asm statements keep their order).
                 const uint32_t cb = smem_u32(raw + r * kDRawBytes) + uint32_t(row * (kDK / 2));
@@ -1144,7 +1157,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             if (lane == 0) mbar_arrive(smem_u32(&afull[a]));
             if (++r == kDRawStages) { r = 0; rp ^= 1; }
             if (++a == kDAS) { a = 0; ap ^= 1; }
-            if (ks < 0 || abort_raised(wt)) break;
+            if (ks < 0) break;
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (converged warp, elected lane)
@@ -1401,7 +1414,8 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     if (!make_map(&mg, wg, (uint64_t)s.E * s.I, s.H / 2, kRows, cbox, true, decode) ||
         !make_map(&mu, wu, (uint64_t)s.E * s.I, s.H / 2, kRows, cbox, true, decode) ||
         !make_map(&md, wd, (uint64_t)s.E * s.H, s.I / 2, kRows, cbox, true, decode) ||
-        !make_map(&mx, x_perm, A, s.H, kNBox) || !make_map(&mh, h, A, s.I, kNBox))
+        !(decode ? make_map_slabs(&mx, x_perm, A, s.H, kNBox, 2) : make_map(&mx, x_perm, A, s.H, kNBox)) ||
+        !(decode ? make_map_slabs(&mh, h, A, s.I, kNBox, 2) : make_map(&mh, h, A, s.I, kNBox)))
         return cudaErrorInvalidValue;
 
     const int cmax = decode ? kDN : kChunkN;

@@ -87,6 +87,11 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
     return v;
 }
+__device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -146,6 +151,13 @@ __device__ __forceinline__ bool wait_count(const int *p, int need, const Waits &
             return false;
         }
     }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
@@ -308,6 +320,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t *r) {
 // eight consecutive rows read by eight lanes fall in distinct banks.
 bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
               uint32_t box_cols = 64, bool bytes = false, bool swz64 = false);
+// 3-D view of a row-major bf16 [rows][cols] matrix as 64-element slabs: coordinates
+// (element in slab, row, slab), box = 64 x box_rows x nslab, 128-byte swizzle.  One load
+// then fills nslab consecutive slab regions of box_rows rows each, the layout of nslab
+// separate 2-D loads.
+bool make_map_slabs(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    uint32_t nslab);
 int sm_count();
 // The bounded waits' limit and the failure-path test's extra publication count
 // (moe_debug_set_waits), read at each launch.
