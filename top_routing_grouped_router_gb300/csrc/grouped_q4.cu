@@ -560,7 +560,8 @@ constexpr int kDDeq = 4;                             // dequant warps: one per l
 constexpr int kDThreads = (2 + kDCons + kDDeq) * 32;
 constexpr int kDSBytes = 4096;                       // a tile's block sums: <= 16 rows x 256 B
 constexpr int kDSide = kScaleBytes + kDSBytes;       // per-tile side buffer: scales, then block sums
-constexpr int kDSmemBytes = kDRawStages * kDRawBytes + 2 * kDSide + 1024 + 2048;
+constexpr int kDSideBufs = 2;                        // side buffers (tiles in flight between producer and consumers)
+constexpr int kDSmemBytes = kDRawStages * kDRawBytes + kDSideBufs * kDSide + 1024 + 2048;
 static_assert(kDSmemBytes <= 232448, "shared memory");
 static_assert(kDACol + kDAS * kDAStageCols <= kTmemCols, "TMEM columns");
 static_assert(kDN == kNBox && kDTokSlab == kNBox * 128, "a stage's token rows: one 16-row box per slab");
@@ -572,7 +573,8 @@ __host__ __device__ constexpr int sh_stride(int I) { return (2 * (I / kSlab) + 3
 
 // 32 codes (16 bytes) -> the 16 bf16 pairs (128 + j) in the MMA's K order (per 8-element
 // group: (0,4), (1,5), (2,6), (3,7)); m = 0x000F000F, c = bf16x2 128.0 = 0x43004300 (kernel
-// parameters, so that they stay register operands).  7 integer operations per 8 codes.
+// parameters, so that they stay register operands).  7 integer operations per 8 codes (the
+// shifts as high-half multiplies, off the logic pipe, ran slower).
 __device__ __forceinline__ void codes_to_ints(const uint4 cw, uint32_t *v, uint32_t m, uint32_t c) {
     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
@@ -757,10 +759,15 @@ struct Q4DCons {
     int pb;
     uint32_t pp;
 };
+// Decode tile kinds: gate/up (128 rows of both), down over 128 rows, and down over 256 rows
+// (two row halves that share the token rows: the stage layout, MMAs and partials of a gate/up
+// tile, with the lower half in the gate position and the upper half in the up position).
+enum : int { kQ4GateUp = 0, kQ4Down = 1, kQ4DownPair = 2 };
+
 // One tile as a consumer sees it: its side buffer (scales, then the tokens' block sums) and
 // the barrier that frees it.
 struct Q4DTile {
-    int down, e, rb, r0, m, nstage;
+    int kind, e, rb, r0, m, nstage;
     uint32_t side, sempty;
 };
 
@@ -781,11 +788,13 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
 // store (gate/up) or the y store (down).  Returns false when a wait gave up.
 template <int NT, bool kLora>
 __device__ __forceinline__ bool q4d_consume_tile(const Params &p, const Waits &wt, Q4DCons &c, const Q4DTile &t) {
-    const bool down = t.down != 0;
+    const bool down = t.kind != kQ4GateUp;
+    const bool pair = t.kind == kQ4DownPair;
     const int nblk = down ? c.nblk_i : c.nblk_h;
-    // this row's block scales (bf16, blocks consecutive) of gate (or down) and up, and the block sums
+    // this row's block scales (bf16, blocks consecutive) of gate (or down) and of up (or of the
+    // upper row half: its scales follow the lower half's 128 rows), and the block sums
     const uint32_t sg = t.side + uint32_t(c.row * nblk) * 2u;
-    const uint32_t su = sg + kScaleBytes / 2;
+    const uint32_t su = pair ? sg + uint32_t(kRows * nblk) * 2u : sg + kScaleBytes / 2;
     const uint32_t bsa = t.side + kScaleBytes;
     const float bstep = p.b;
     // gate/up rows hold a multiple of 8 blocks: one 16-byte load covers four stages
@@ -798,7 +807,7 @@ __device__ __forceinline__ bool q4d_consume_tile(const Params &p, const Waits &w
         if (!mbar_wait(c.pfull + 8u * c.pb, c.pp, wt)) return false;
         tc_fence_after();
         const uint32_t ta = c.tq + uint32_t(c.pb * kDPartCols);
-        if (!down) {
+        if (t.kind != kQ4Down) {
             uint32_t gw, uw;  // the scales of blocks 2 ks (low half) and 2 ks + 1 (high half)
             if (vec8) {
                 if ((ks & 3) == 0) {
@@ -815,13 +824,20 @@ __device__ __forceinline__ bool q4d_consume_tile(const Params &p, const Waits &w
             }
             const float g0 = __uint_as_float(gw << 16) * bstep, g1 = __uint_as_float(gw & 0xffff0000u) * bstep;
             const float u0 = __uint_as_float(uw << 16) * bstep, u1 = __uint_as_float(uw & 0xffff0000u) * bstep;
-            // gate and up partials of both blocks (gate 0, up 0, gate 1, up 1), one wait
+            // gate and up (lower and upper row half) partials of both blocks (gate 0, up 0,
+            // gate 1, up 1), one wait
             float v[4][NT];
             const uint32_t tt[4] = {ta, ta + 16, ta + 32, ta + 48};
             tmem_ld_cols<NT, 4>(tt, v);
 #pragma unroll
             for (int i = 0; i < NT; ++i) {
-                const float2 cs = lds_f2(bsa + uint32_t(i * c.sxs + 2 * ks) * 4u);  // (128 + j0) S of both blocks
+                float2 cs;  // (128 + j0) S of both blocks (h rows: two halves per block, added in order)
+                if (pair) {
+                    const float4 s2 = lds_f4(bsa + uint32_t(i * c.shs + 4 * ks) * 4u);
+                    cs = make_float2(s2.x + s2.y, s2.z + s2.w);
+                } else {
+                    cs = lds_f2(bsa + uint32_t(i * c.sxs + 2 * ks) * 4u);
+                }
                 acc0[i] = fmaf(g0, v[0][i] - cs.x, acc0[i]);
                 acc1[i] = fmaf(u0, v[1][i] - cs.x, acc1[i]);
                 acc0[i] = fmaf(g1, v[2][i] - cs.y, acc0[i]);
@@ -848,28 +864,31 @@ __device__ __forceinline__ bool q4d_consume_tile(const Params &p, const Waits &w
     // the tile's scales and block sums are no longer needed
     __syncwarp();
     if (c.lane == 0) mbar_arrive(t.sempty);
-    const int col = t.rb * kRows + c.row;
+    const int col = t.rb * (down ? 2 * kRows : kRows) + c.row;  // (down tiles: 256-row steps)
     const LoraDev &lr = p.lora;
     const bool lora = kLora && lr.rank > 0;
     float lb0[16], lb1[16];
-    if (lora) {
-        if (down) {
-            lora_row16(lr.bd, (size_t)t.e * p.H + col, lr.rank, lb0);
-        } else {
-            lora_row16(lr.bg, (size_t)t.e * p.I + col, lr.rank, lb0);
-            lora_row16(lr.bu, (size_t)t.e * p.I + col, lr.rank, lb1);
-        }
-    }
     if (down) {
+        // y rows of the lower half (acc0), then of the upper half (acc1), one adapter row at a time
 #pragma unroll
-        for (int i = 0; i < NT; ++i)
-            if (i < t.m) {
-                const size_t pr = (size_t)(t.r0 + i);
-                float val = acc0[i];
-                if (lora) val += lr.scale * lora_dot16(lb0, lr.ha + pr * 16);
-                p.y[pr * p.H + col] = f32_to_bf16_bits(val);
-            }
+        for (int half = 0; half < 2; ++half) {
+            if (half == 1 && !pair) break;
+            const int ycol = col + half * kRows;
+            if (lora) lora_row16(lr.bd, (size_t)t.e * p.H + ycol, lr.rank, lb0);
+#pragma unroll
+            for (int i = 0; i < NT; ++i)
+                if (i < t.m) {
+                    const size_t pr = (size_t)(t.r0 + i);
+                    float val = half ? acc1[i] : acc0[i];
+                    if (lora) val += lr.scale * lora_dot16(lb0, lr.ha + pr * 16);
+                    p.y[pr * p.H + ycol] = f32_to_bf16_bits(val);
+                }
+        }
         return true;
+    }
+    if (lora) {
+        lora_row16(lr.bg, (size_t)t.e * p.I + col, lr.rank, lb0);
+        lora_row16(lr.bu, (size_t)t.e * p.I + col, lr.rank, lb1);
     }
     // h is stored in the weights' 8-element group order (see the file comment); its sums over
     // this warp's 32 rows (half of a 64-row block) go to sh[token][block][half]
@@ -930,8 +949,8 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
     // the shared address space (and emits shared, not generic, loads) for everything derived
     uint8_t *smem = smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
     uint8_t *raw = smem;
-    uint8_t *side = smem + kDRawStages * kDRawBytes;        // [2][kDSide]
-    uint8_t *ctrl = side + 2 * kDSide;
+    uint8_t *side = smem + kDRawStages * kDRawBytes;        // [kDSideBufs][kDSide]
+    uint8_t *ctrl = side + kDSideBufs * kDSide;
     uint64_t *rfull = reinterpret_cast<uint64_t *>(ctrl);   // [kDRawStages]
     uint64_t *rempty = rfull + kDRawStages;                 // [kDRawStages]
     uint64_t *afull = rempty + kDRawStages;                 // [kDAS]
@@ -940,9 +959,9 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
     uint64_t *pempty = pfull + kDPS;                        // [kDPS]
     uint64_t *tmf = pempty + kDPS;                          // [kMetaRing]
     uint64_t *tme = tmf + kMetaRing;                        // [kMetaRing]
-    uint64_t *sfull = tme + kMetaRing;                      // [2]
-    uint64_t *sempty = sfull + 2;                           // [2]
-    uint64_t *drain = sempty + 2;                           // [1]
+    uint64_t *sfull = tme + kMetaRing;                      // [kDSideBufs]
+    uint64_t *sempty = sfull + kDSideBufs;                  // [kDSideBufs]
+    uint64_t *drain = sempty + kDSideBufs;                  // [1]
     int *rmeta = reinterpret_cast<int *>(drain + 1);        // [kDRawStages][4]
     int *tmeta = rmeta + 4 * kDRawStages;                   // [kMetaRing][8]
     volatile int *abort = tmeta + 8 * kMetaRing;
@@ -967,7 +986,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             mbar_init(smem_u32(&tmf[s]), 1);
             mbar_init(smem_u32(&tme[s]), kDCons);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kDSideBufs; ++b) {
             mbar_init(smem_u32(&sfull[b]), 1);
             mbar_init(smem_u32(&sempty[b]), kDCons);
         }
@@ -1020,12 +1039,17 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const uint32_t entry = nentry;
             const int off = noff, me = nme;
             next = lo + atomicAdd(ctr, 1);
-            const int down = int(entry >> 31), e0 = int((entry >> 16) & 0xFF), rb = int((entry >> 8) & 0xFF);
+            const int down = int(entry >> 31), e0 = int((entry >> 16) & 0xFF), rb0 = int((entry >> 8) & 0xFF);
             const int nc = int(entry & 0xFF);
             const int e = min(e0, p.E - 1);
+            const bool rb_ok = down ? rb0 * 2 * kRows < p.H : rb0 * kRows < p.I;
+            const int rb = rb_ok ? rb0 : 0;
+            // a down tile covers 256 rows (the last one of an odd count of 128-row blocks: 128)
+            const int drows = down ? min(2 * kRows, p.H - rb * 2 * kRows) : kRows;
+            const int kind = !down ? kQ4GateUp : drows == 2 * kRows ? kQ4DownPair : kQ4Down;
             const int base = chunk_base(me, kDN, false);
             int m = min(base, me - nc * base);
-            if (e0 >= p.E || off < 0 || me <= 0 || off + me > p.A || m <= 0 || m > kDN) {
+            if (e0 >= p.E || !rb_ok || off < 0 || me <= 0 || off + me > p.A || m <= 0 || m > kDN) {
                 record_error(p.err, MOE_ERR_DEVICE);
                 m = 0;
             }
@@ -1040,7 +1064,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const int nstage = nblk / 2;
             if (!mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, wt)) break;
             int *tm = tmeta + 8 * slot;
-            tm[0] = down;
+            tm[0] = kind;
             tm[1] = e;
             tm[2] = rb;
             tm[3] = r0;
@@ -1050,14 +1074,14 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             mbar_arrive(smem_u32(&tmf[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
             {
-                // the tile's block scales (128 consecutive rows x nblk bf16, contiguous) and its
-                // tokens' block sums (m consecutive rows)
-                const int sb = tiles_done & 1;
-                if (!mbar_wait(smem_u32(&sempty[sb]), ((tiles_done >> 1) & 1) ^ 1, wt)) break;
+                // the tile's block scales (its 128 or 256 consecutive rows x nblk bf16, contiguous)
+                // and its tokens' block sums (m consecutive rows)
+                const int sb = tiles_done % kDSideBufs;
+                if (!mbar_wait(smem_u32(&sempty[sb]), ((tiles_done / kDSideBufs) & 1) ^ 1, wt)) break;
                 const uint32_t sfb = smem_u32(&sfull[sb]);
-                const uint32_t sbytes = uint32_t(kRows * nblk * 2);
+                const uint32_t sbytes = uint32_t(drows * nblk * 2);  // <= kScaleBytes
                 const uint32_t ssum = uint32_t(m * (down ? shs : sxs) * 4);  // <= kDSBytes
-                const size_t row0 = (size_t)e * (down ? p.H : p.I) + (size_t)rb * kRows;
+                const size_t row0 = down ? (size_t)e * p.H + (size_t)rb * 2 * kRows : (size_t)e * p.I + (size_t)rb * kRows;
                 const uint32_t dst = smem_u32(side + sb * kDSide);
                 mbar_arrive_expect_tx(sfb, (down ? sbytes : 2 * sbytes) + ssum);
                 if (down) {
@@ -1071,8 +1095,8 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 ++tiles_done;
             }
             // (N <= kDN = kNBox: the token rows of a stage are one box of both slabs)
-            const uint32_t bytes = (down ? 1 : 2) * kDCodeBytes + 2 * kDTokSlab;
-            const int wrow = e * (down ? p.H : p.I) + rb * kRows;
+            const uint32_t bytes = (kind == kQ4Down ? 1 : 2) * kDCodeBytes + 2 * kDTokSlab;
+            const int wrow = down ? e * p.H + rb * 2 * kRows : e * p.I + rb * kRows;
             const CUtensorMap *tokmap = down ? &tm_h : &tm_x;
             const int kfetch = min(2, nstage - 1);
             for (int ks = 0; ks < nstage; ++ks) {
@@ -1081,7 +1105,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                     break;
                 }
                 int *mt = rmeta + 4 * r;
-                mt[0] = down;
+                mt[0] = kind;
                 mt[1] = ks;
                 mt[2] = N;
                 const uint32_t fb = smem_u32(&rfull[r]);
@@ -1089,7 +1113,8 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 ++rfills;
                 const uint32_t base = smem_u32(raw + r * kDRawBytes);
                 tma_load_2d(base, down ? &tm_dc : &tm_gc, ks * (kDK / 2), wrow, fb);
-                if (!down) tma_load_2d(base + kDCodeBytes, &tm_uc, ks * (kDK / 2), wrow, fb);
+                if (kind == kQ4GateUp) tma_load_2d(base + kDCodeBytes, &tm_uc, ks * (kDK / 2), wrow, fb);
+                if (kind == kQ4DownPair) tma_load_2d(base + kDCodeBytes, &tm_dc, ks * (kDK / 2), wrow + kRows, fb);
                 tma_load_3d(base + kDTok, tokmap, 0, r0, 2 * ks, fb);  // slabs 2 ks and 2 ks + 1
                 if (++r == kDRawStages) { r = 0; rp ^= 1; }
                 if (ks == kfetch && next < hi) fetch(next);
@@ -1098,8 +1123,8 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         // no TMA or bulk write may still be landing in this CTA's shared memory when it exits
         for (int i = max(0, rfills - kDRawStages); i < rfills; ++i)
             mbar_wait_drain(smem_u32(&rfull[i % kDRawStages]), uint32_t((i / kDRawStages) & 1), wt);
-        for (int i = max(0, tiles_done - 2); i < tiles_done; ++i)
-            mbar_wait_drain(smem_u32(&sfull[i & 1]), uint32_t((i >> 1) & 1), wt);
+        for (int i = max(0, tiles_done - kDSideBufs); i < tiles_done; ++i)
+            mbar_wait_drain(smem_u32(&sfull[i % kDSideBufs]), uint32_t((i / kDSideBufs) & 1), wt);
         // sentinels (an aborting CTA's roles leave on the abort flag instead)
         if (mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, wt)) {
             tmeta[8 * slot] = -1;
@@ -1122,7 +1147,8 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&rfull[r]), rp, wt))) break;
             const uint2 md = lds_v2(smem_u32(rmeta + 4 * r));
-            const int down = int(md.x), ks = int(md.y);
+            const bool two = int(md.x) != kQ4Down;  // two code slabs: gate and up, or two row halves
+            const int ks = int(md.y);
             // the sentinel (ks < 0) is passed on to the MMA warp through the A ring
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&aempty[a]), ap ^ 1, wt))) break;
             tc_fence_after();
@@ -1136,7 +1162,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 uint4 c[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) c[i] = lds_v4(cb + 16 * (i ^ sw));
-                if (!down) {
+                if (two) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) c[4 + i] = lds_v4(cb + kDCodeBytes + 16 * (i ^ sw));
                 }
@@ -1145,7 +1171,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 #pragma unroll
                 for (int i = 0; i < 4; ++i) codes_to_ints(c[i], v + 16 * i, km, kc);
                 tmem_st64(ta, v);
-                if (!down) {
+                if (two) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) codes_to_ints(c[4 + i], v + 16 * i, km, kc);
                     tmem_st64(ta + 64, v);
@@ -1166,7 +1192,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         for (;;) {
             const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&afull[a]), ap, wt));
             const int *mt = rmeta + 4 * r;
-            const int down = mt[0], ks = mt[1], N = mt[2];
+            const int kind = mt[0], ks = mt[1], N = mt[2];
             if (__any_sync(0xffffffffu, !got || ks < 0 || abort_raised(wt))) break;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&pempty[pb]), pp ^ 1, wt))) break;
             tc_fence_after();
@@ -1177,7 +1203,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             // (address / 16, 14 bits: shared memory stays below 256 KB, so adding cannot carry)
             const uint64_t b0 = smem_desc(smem_u32(raw + r * kDRawBytes) + kDTok);
             const uint32_t c0 = smem_u32(&aempty[a]), c1 = smem_u32(&rempty[r]), c2 = smem_u32(&pfull[pb]);
-            if (!down)
+            if (kind != kQ4Down)
                 q4d_stage_gate_up(d, ta, b0, idesc, c0, c1, c2);
             else
                 q4d_stage_down(d, ta, b0, idesc, c0, c1, c2);
@@ -1201,14 +1227,14 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         for (;;) {
             if (!mbar_wait(smem_u32(&tmf[slot]), mphase, wt)) break;
             const int *tm = tmeta + 8 * slot;
-            const int down = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], nstage = tm[6];
+            const int kind = tm[0], e = tm[1], rb = tm[2], r0 = tm[3], m = tm[4], nstage = tm[6];
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tme[slot]));
             if (++slot == kMetaRing) { slot = 0; mphase ^= 1; }
-            if (down < 0 || abort_raised(wt)) break;
-            const int sb = tiles & 1;
-            if (!mbar_wait(smem_u32(&sfull[sb]), (tiles >> 1) & 1, wt)) break;
-            const Q4DTile t{down, e, rb, r0, m, nstage, smem_u32(side + sb * kDSide), smem_u32(&sempty[sb])};
+            if (kind < 0 || abort_raised(wt)) break;
+            const int sb = tiles % kDSideBufs;
+            if (!mbar_wait(smem_u32(&sfull[sb]), (tiles / kDSideBufs) & 1, wt)) break;
+            const Q4DTile t{kind, e, rb, r0, m, nstage, smem_u32(side + sb * kDSide), smem_u32(&sempty[sb])};
             // (the adapter variant keeps one width: three inlined copies of its epilogue spill)
             const bool ok = kLora     ? q4d_consume_tile<16, kLora>(p, wt, c, t)
                             : m <= 4 ? q4d_consume_tile<4, kLora>(p, wt, c, t)
@@ -1236,7 +1262,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
 // clears the scheduling counters.
 __global__ void __launch_bounds__(256)
 q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, int T, int k, int H, int I, int E,
-               int cmax, int max_tiles, uint16_t *__restrict__ x_perm,
+               int cmax, int dn_rows, int max_tiles, uint16_t *__restrict__ x_perm,
                uint32_t *tiles, int *sched, int *done, int32_t *err, float *sx, float cc) {
     griddep_launch_dependents();
     griddep_wait();
@@ -1296,7 +1322,7 @@ q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, 
         done[e] = 0;
     }
     const int nch = n_chunks(me, cmax, false);
-    const int gu_per = I / kRows, dn_per = H / kRows;
+    const int gu_per = I / kRows, dn_per = (H + dn_rows - 1) / dn_rows;
     int n_gu, n_dn;
     const int gu_off = scan256(nch * gu_per, s_warp, n_gu);
     const int dn_off = scan256(nch * dn_per, s_warp, n_dn);
@@ -1420,7 +1446,8 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
 
     const int cmax = decode ? kDN : kChunkN;
     cudaError_t e = launch_pdl(q4_prep_kernel, dim3(prep_blocks(A)), dim3(256), 0, st, static_cast<const uint16_t *>(x), order,
-                               offsets, s.T, s.k, s.H, s.I, s.E, cmax, (int)q4_max_tiles(s), x_perm, tiles, sched,
+                               offsets, s.T, s.k, s.H, s.I, s.E, cmax, decode ? 2 * kRows : kRows,
+                               (int)q4_max_tiles(s), x_perm, tiles, sched,
                                done, err, decode ? sx : nullptr, 128.0f + 0.5f * float(t2));
     if (e != cudaSuccess) return e;
     if (!(decode ? set_decode_attr<false>() && set_decode_attr<true>()
