@@ -308,7 +308,7 @@ def measure(ctx: Ctx, workload: str, steps: int, warmup: int, *, headline: bool)
             ad = synth.make_lora(l.E, l.H, l.I, rank=16, seed=l.T, layer=i)
             t = [to_device(ad[n], dev) for n in names]
             lo = moe.make_lora(ad["rank"], ad["scale"], *t)
-            if l.w == "bf16" and not args.lora_unpacked:
+            if l.w in ("bf16", "q4") and not args.lora_unpacked:
                 # adapters are static: packed once, before timing, like the weights
                 lo = moe.pack_lora(dl[0][i].shape, lo, device=dev)
                 t.append(lo.pack_tensor)
@@ -568,6 +568,8 @@ def run_ours(args, rank, world, local):
                    "entry": {"forward": "moe_forward", "rmsnorm": "moe_forward_rmsnorm (pre-router RMSNorm + residual)",
                              "lora": "moe_forward_lora (rank-16 fp32 adapters on the expert projections"
                                       + (", packed: tensor-core adapter products)" if inp0.w == "bf16" and not args.lora_unpacked
+                                         else ", packed: tensor-core A-side products, B side in the epilogue)"
+                                         if inp0.w == "q4" and not args.lora_unpacked
                                          else ", CUDA-core adapter products)")}[head["entry"]],
                    "T": head["T"], "H": head["H"], "E": head["E"], "k": head["k"], "I": head["I"],
                    "layers": head["layers"], "weights": head["weights"], "active_experts": head["active_experts"],

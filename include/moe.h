@@ -115,13 +115,15 @@ typedef struct {
  *   a_down       [E][r][I]     b_down       [E][H][r]
  * Device pointers, row-major, 16-byte aligned.
  *
- * packed: NULL, or the output of moe_lora_pack for these adapters (device,
- * 256-byte aligned).  With a pack, the bf16 tensor-core path runs the adapter
- * products on the tensor cores.  Each fp32 operand (the adapters, and
+ * packed: NULL, or the output of moe_lora_pack for these adapters and this
+ * shape (device, 256-byte aligned).  With a pack, the bf16 tensor-core path runs
+ * the adapter products on the tensor cores.  Each fp32 operand (the adapters, and
  * scale * x . A^T) is split as hi = bf16(v), lo = bf16(v - hi), and the products
  * are hi.hi + hi.lo + lo.hi with fp32 accumulation (x is bf16 already, so
- * x . A^T takes x.hi + x.lo): close to fp32 accuracy.  Without a pack, and on
- * every other path, the products run in fp32 on CUDA cores.
+ * x . A^T takes x.hi + x.lo): close to fp32 accuracy.  The 4-bit tensor-core
+ * path takes the A-side products (x . A^T, h . A_down^T) from the tensor cores
+ * the same way and adds the B side in fp32 in its epilogues.  Without a pack,
+ * and on every other path, the products run in fp32 on CUDA cores.
  */
 typedef struct {
     int32_t rank;
@@ -274,6 +276,10 @@ MOE_API int moe_forward_lora(const moe_shape *shape, const void *x, const void *
  *   [E][32][I]   A_down hi, A_down lo                    (16 rows each)
  *   [E*I][128]   B_gate then B_up, each as 64 columns (hi, hi, lo, 0) x 16
  *   [E*H][64]    B_down as (hi, hi, lo, 0) x 16 columns
+ * With 4-bit weights (shape->w_dtype MOE_DT_Q4) the A columns of every
+ * 8-column group are stored in the order (0,4,1,5,2,6,3,7), the order in which
+ * the 4-bit path keeps its token rows and h; a pack is therefore specific to the
+ * weight type of the shape it was written for.
  */
 MOE_API int moe_lora_pack_size(const moe_shape *shape, size_t *bytes);
 

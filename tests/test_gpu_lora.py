@@ -1,7 +1,7 @@
 """GPU parity of moe_forward_lora (LoRA adapters on the expert projections) against the
 oracle, on the bf16 and 4-bit tensor-core paths (decode and large batches) and the
-generic fp32 path; on the bf16 path both with the fp32 adapters as given (CUDA-core
-adapter products) and with a pack (tensor-core adapter products).  With B = 0 the result
+generic fp32 path; on the bf16 and 4-bit paths both with the fp32 adapters as given
+(CUDA-core adapter products) and with a pack (tensor-core adapter products).  With B = 0 the result
 must equal moe_forward bit for bit, which also checks the split launches the adapters
 need."""
 import numpy as np
@@ -123,6 +123,20 @@ def test_lora_decode_q4_rank16():
     _check(synth.make_inputs("decode48q"), 16, 12)
 
 
+def test_lora_packed_decode_q4_rank16():
+    # 4-bit decode with a pack: A-side products on the tensor cores from the grouped-order rows
+    _check(synth.make_inputs("decode48q"), 16, 12, packed=True)
+
+
+def test_lora_packed_q4_odd_row_blocks_rank5():
+    # H = 384: an odd count of 128-row blocks (a 128-row down tile at the end of each expert)
+    _check(synth.make_custom(40, 384, 16, 4, 256, w="q4", seed=47, name="lora40q"), 5, 16, packed=True)
+
+
+def test_lora_packed_large_batch_q4_rank16():
+    _check(synth.make_custom(200, 256, 16, 4, 128, w="q4", seed=43, name="lora200q"), 16, 16, packed=True)
+
+
 def test_lora_fp32_generic_path_rank4():
     _check(synth.make_inputs("tiny"), 4, None)
 
@@ -182,3 +196,26 @@ def test_pack_layout_is_the_documented_hi_lo_split():
     np.testing.assert_array_equal(got[off_ah:off_ah + E * 32 * I].reshape(ah.shape), ah)
     np.testing.assert_array_equal(got[off_bgu:off_bgu + E * I * 128].reshape(bgu.shape), bgu)
     np.testing.assert_array_equal(got[off_bd:off_bd + E * H * 64].reshape(bd.shape), bd)
+
+
+def test_pack_for_4bit_weights_keeps_the_grouped_column_order():
+    # with 4-bit weights the pack's A columns follow the 4-bit path's order of x and h: stored
+    # position p of every 8-column group holds column (0,4,1,5,2,6,3,7)[p]; the B slabs are
+    # those of the bf16 pack
+    E, H, I, r = 4, 128, 128, 5
+    lora = synth.make_lora(E, H, I, rank=r, seed=3)
+    plain, keep = _dev_lora(lora, moe.make_shape(8, H, E, 2, I))
+    grouped, keep2 = _dev_lora(lora, moe.make_shape(8, H, E, 2, I, w="q4", q_block=64))
+    a = plain.pack_tensor.cpu().numpy().view(np.uint16)
+    b = grouped.pack_tensor.cpu().numpy().view(np.uint16)
+    assert a.shape == b.shape
+    al = lambda n: (n + 255) // 256 * 256
+    n_ax, n_ah = E * 64 * H, E * 32 * I
+    off_ah = al(n_ax * 2) // 2
+    order = np.array([0, 4, 1, 5, 2, 6, 3, 7])
+    perm = lambda n: (np.arange(n).reshape(-1, 8)[:, order]).reshape(-1)
+    np.testing.assert_array_equal(b[:n_ax].reshape(E * 64, H), a[:n_ax].reshape(E * 64, H)[:, perm(H)])
+    np.testing.assert_array_equal(b[off_ah:off_ah + n_ah].reshape(E * 32, I),
+                                  a[off_ah:off_ah + n_ah].reshape(E * 32, I)[:, perm(I)])
+    off_bgu = off_ah + al(n_ah * 2) // 2
+    np.testing.assert_array_equal(b[off_bgu:], a[off_bgu:])

@@ -1412,9 +1412,11 @@ bool q4_path_supported(const moe_shape &s) {
 size_t q4_sx_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * sx_stride(s.H) * 4 + 255) / 256 * 256; }
 size_t q4_sh_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * sh_stride(s.I) * 4 + 255) / 256 * 256; }
 
+// x_perm, the scheduling words, the per-expert counters, the tile list, the block sums of the
+// token rows and of h, and the scratch of the tensor-core A-side launches (packed adapters)
 size_t q4_part_bytes(const moe_shape &s) {
     return xperm_bytes(s) + 256 + (size_t)kMaxE * 4 + (q4_max_tiles(s) * 4 + 255) / 256 * 256 + q4_sx_bytes(s) +
-           q4_sh_bytes(s);
+           q4_sh_bytes(s) + lora_aside_bytes(s);
 }
 
 cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
@@ -1432,6 +1434,7 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     char *sums = reinterpret_cast<char *>(tiles) + (q4_max_tiles(s) * 4 + 255) / 256 * 256;
     float *sx = reinterpret_cast<float *>(sums);
     float *sh = reinterpret_cast<float *>(sums + q4_sx_bytes(s));
+    char *aside = sums + q4_sx_bytes(s) + q4_sh_bytes(s);
 
     // code boxes: 128 rows x one stage's codes (32 bytes; the decode kernel's stages are 64)
     const bool decode = s.T <= kDecodeMaxN;
@@ -1494,12 +1497,24 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
                           QCfg<kChunkN, 4>::kSmemBytes, st, mg, mu, md, mx, mh, pr);
     };
     if (!lora) return run(prm, std::false_type{});
-    // with adapters: x . A^T, the gate/up tiles, h . A_down^T (h in the grouped column order), the down tiles
+    // with adapters: x . A^T, the gate/up tiles, h . A_down^T (h in the grouped column order), the
+    // down tiles.  With a pack the A-side products run on the tensor cores (from x_perm and h in
+    // the grouped order, which the pack's A columns follow) and come out scaled, in fp32; without
+    // one, on CUDA cores in fp32.  Either way the epilogues add the B side.
     prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
-    if ((e = launch_lora_xa(s, x, order, offsets, *lora, xa, lpart, st)) != cudaSuccess) return e;
+    const bool packed = lora->packed != nullptr;
+    if (packed) {
+        prm.lora.scale = 1.f;  // the tensor-core products come out scaled (fp32)
+        e = launch_lora_aside_tc(s, false, x_perm, offsets, *lora, xa, aside, err, st);
+    } else {
+        e = launch_lora_xa(s, x, order, offsets, *lora, xa, lpart, st);
+    }
+    if (e != cudaSuccess) return e;
     prm.phase = kPhaseGateUp;
     if ((e = run(prm, std::true_type{})) != cudaSuccess) return e;
-    if ((e = launch_lora_ha(s, h, false, true, offsets, *lora, ha, lpart, st)) != cudaSuccess) return e;
+    e = packed ? launch_lora_aside_tc(s, true, h, offsets, *lora, ha, aside, err, st)
+               : launch_lora_ha(s, h, false, true, offsets, *lora, ha, lpart, st);
+    if (e != cudaSuccess) return e;
     prm.phase = kPhaseDown;
     return run(prm, std::true_type{});
 }

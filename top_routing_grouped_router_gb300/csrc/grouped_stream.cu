@@ -88,6 +88,8 @@ struct Params {
     float lora_scale;
     uint16_t *xab;              // [A][128] bf16: scale * x . A^T, split (see the LoRA stage)
     uint16_t *hab;              // [A][64] bf16: scale * h . A_down^T, split
+    int lora_f32;               // A-side tiles write scale * x . A^T as fp32 [A][32] (h: [A][16])
+                                // into xab / hab instead (the 4-bit path's epilogues read them)
     int *done;                  // [3][kMaxE] publications: h (per epilogue warp of a gate/up tile),
                                 // then x . A^T and h . A_down^T (per quadrant warp of an A-side tile)
     int32_t *err;
@@ -661,7 +663,22 @@ tc_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gate, const __grid_const
                 if (part == 0) {
                     uint32_t v[64];
                     tmem_ld32x2(taddr, taddr + 32, v);
-                    if (row < m) {
+                    if (row < m && p.lora_f32) {
+                        const int half = N / 2, nproj = half / 16;
+                        float4 *dst = reinterpret_cast<float4 *>(
+                            reinterpret_cast<float *>(down == kLoraX ? p.xab : p.hab) + (size_t)(r0 + row) * 16 * nproj);
+                        for (int pj = 0; pj < nproj; ++pj)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                float x4[4];
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const int c = 16 * pj + 4 * i + h;
+                                    x4[h] = p.lora_scale * (__uint_as_float(v[c & 63]) + __uint_as_float(v[(half + c) & 63]));
+                                }
+                                dst[4 * pj + i] = make_float4(x4[0], x4[1], x4[2], x4[3]);
+                            }
+                    } else if (row < m) {
                         const int half = N / 2, nproj = half / 16;
                         uint4 *dst = reinterpret_cast<uint4 *>((down == kLoraX ? p.xab : p.hab) +
                                                                (size_t)(r0 + row) * 64 * nproj);
@@ -1000,6 +1017,66 @@ cudaError_t launch_grouped_fast(int path, const moe_shape &s, const void *x, con
     if ((e = launch_lora_ha(s, h, false, false, offsets, *lora, ha, lpart, st)) != cudaSuccess) return e;
     prm.phase = kPhaseDown;
     return run(prm);
+}
+
+size_t lora_aside_bytes(const moe_shape &s) {
+    return 256 + (size_t)kCountersPerExpert * kMaxE * 4 + (max_tiles(s) * 16 + 255) / 256 * 256;
+}
+
+cudaError_t launch_lora_aside_tc(const moe_shape &s, bool h_side, const void *src, const int32_t *offsets,
+                                 const moe_lora &lora, void *out, char *region, int32_t *err, cudaStream_t st) {
+    const int A = s.T * s.k;
+    if (A == 0) return cudaSuccess;
+    int *sched = reinterpret_cast<int *>(region);
+    int *done = sched + 64;
+    uint4 *tiles = reinterpret_cast<uint4 *>(region + 256 + (size_t)kCountersPerExpert * kMaxE * 4);
+    const int len = h_side ? s.I : s.H;
+    // every map the kernel takes must be valid; the A-side phases read only the token rows
+    // (128-row boxes) and the pack's A rows, and write the products with plain stores
+    Maps m;
+    const LoraPack L = lora_pack_layout(s);
+    const char *pk = static_cast<const char *>(lora.packed);
+    if (!tc::make_map(&m.x, src, A, len, kNBox) || !tc::make_map(&m.xb, src, A, len, kBigBox) ||
+        !tc::make_map(&m.xm, src, A, len, kMidBox) || !tc::make_map(&m.l.lax, pk + L.ax, (uint64_t)s.E * 64, s.H, 64) ||
+        !tc::make_map(&m.l.lah, pk + L.ah, (uint64_t)s.E * 32, s.I, 32) ||
+        !tc::make_map(&m.l.lbg, pk + L.bgu, (uint64_t)s.E * s.I, 128, kRows) ||
+        !tc::make_map(&m.l.lbd, pk + L.bd, (uint64_t)s.E * s.H, 64, kRows) ||
+        !tc::make_map(&m.l.xa16, out, A, h_side ? 64 : 128, kNBox) ||
+        !tc::make_map(&m.l.xa128, out, A, h_side ? 64 : 128, kBigBox))
+        return cudaErrorInvalidValue;
+    m.g = m.u = m.d = m.x;
+    m.h = m.x;
+    m.hb = m.xb;
+    m.hm = m.xm;
+    m.l.ha16 = m.l.xa16;
+    m.l.ha128 = m.l.xa128;
+    // the tile list alone (one block of the prep kernel): A-side tiles per 128-token chunk of
+    // an expert; no publication count (h is complete: the gate/up tiles ran in an earlier launch)
+    TileListArgs ta = tc_tile_args(s, kLoraPacked);
+    ta.pub = 0;
+    cudaError_t e = launch_pdl(prep_kernel, dim3(1), dim3(256), 0, st, static_cast<const uint16_t *>(nullptr),
+                               static_cast<const int32_t *>(nullptr), offsets, s.T, s.k, s.H, s.E, ta,
+                               static_cast<uint16_t *>(nullptr), tiles, sched, done, err);
+    if (e != cudaSuccess) return e;
+    Params prm{};
+    prm.tiles = tiles;
+    prm.sched = sched;
+    prm.phase = h_side ? kPhaseLoraH : kPhaseLoraX;
+    prm.done = done;
+    prm.err = err;
+    prm.E = s.E;
+    prm.H = s.H;
+    prm.I = s.I;
+    prm.A = A;
+    prm.dmax = kMaxDownN;
+    prm.wait_ns = tc::wait_limit_ns();
+    prm.k = s.k;
+    prm.lora_packed = 1;
+    prm.lora_scale = lora.scale;
+    prm.lora_f32 = 1;
+    prm.xab = h_side ? nullptr : static_cast<uint16_t *>(out);
+    prm.hab = h_side ? static_cast<uint16_t *>(out) : nullptr;
+    return launch_tc_for<kLoraPacked>(s, tc_wide(s), dim3(tc::sm_count()), st, m, prm);
 }
 
 }  // namespace moe

@@ -180,9 +180,11 @@ __device__ __forceinline__ void write_split(uint16_t *dst, const float *v, bool 
 
 // The packed adapters of the tensor-core path, 8 bf16 outputs (16 bytes) per thread; see
 // LoraPack for the layout.  Values are rounded to nearest even; rows / columns past the rank
-// are zero.  Each B slab holds (B_hi, B_hi, B_lo, 0) in its four 16-column groups.
+// are zero.  Each B slab holds (B_hi, B_hi, B_lo, 0) in its four 16-column groups.  With
+// grouped (4-bit weights) the A columns of every 8-element group are stored in the order
+// (0,4,1,5,2,6,3,7), the order in which the 4-bit path keeps its token rows and h.
 __global__ void __launch_bounds__(256)
-lora_pack_kernel(moe_lora l, int E, int H, int I, size_t n_ax, size_t n_ah, size_t n_bgu, size_t n_bd,
+lora_pack_kernel(moe_lora l, int E, int H, int I, int grouped, size_t n_ax, size_t n_ah, size_t n_bgu, size_t n_bd,
                  uint16_t *ax, uint16_t *ah, uint16_t *bgu, uint16_t *bd) {
     const size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x;  // group of 8 outputs
     const int r = l.rank;
@@ -194,7 +196,8 @@ lora_pack_kernel(moe_lora l, int E, int H, int I, size_t n_ax, size_t n_ah, size
         const float *src = (q & 16) ? l.a_up : l.a_gate;
         const int qq = q & 15;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = qq < r ? src[((size_t)e * r + qq) * H + c + j] : 0.f;
+        for (int j = 0; j < 8; ++j)
+            v[j] = qq < r ? src[((size_t)e * r + qq) * H + c + (grouped ? ((j & 1) << 2) | (j >> 1) : j)] : 0.f;
         write_split(ax + i, v, q >= 32);
         return;
     } else if ((i -= n_ax) < n_ah) {  // [E][32][I]: A_down hi, A_down lo
@@ -202,7 +205,8 @@ lora_pack_kernel(moe_lora l, int E, int H, int I, size_t n_ax, size_t n_ah, size
         const int e = int(row / 32), q = int(row % 32);
         const int qq = q & 15;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = qq < r ? l.a_down[((size_t)e * r + qq) * I + c + j] : 0.f;
+        for (int j = 0; j < 8; ++j)
+            v[j] = qq < r ? l.a_down[((size_t)e * r + qq) * I + c + (grouped ? ((j & 1) << 2) | (j >> 1) : j)] : 0.f;
         write_split(ah + i, v, q >= 16);
         return;
     } else if ((i -= n_ah) < n_bgu) {  // [E*I][128]: gate slab, up slab
@@ -250,7 +254,7 @@ cudaError_t launch_lora_pack(const moe_shape &s, const moe_lora &l, void *dst, c
                  n_bd = (size_t)s.E * s.H * 64;
     const size_t groups = (n_ax + n_ah + n_bgu + n_bd) / 8;
     lora_pack_kernel<<<dim3((unsigned)((groups + 255) / 256)), dim3(256), 0, st>>>(
-        l, s.E, s.H, s.I, n_ax, n_ah, n_bgu, n_bd, reinterpret_cast<uint16_t *>(b + L.ax),
+        l, s.E, s.H, s.I, s.w_dtype == MOE_DT_Q4 ? 1 : 0, n_ax, n_ah, n_bgu, n_bd, reinterpret_cast<uint16_t *>(b + L.ax),
         reinterpret_cast<uint16_t *>(b + L.ah), reinterpret_cast<uint16_t *>(b + L.bgu),
         reinterpret_cast<uint16_t *>(b + L.bd));
     return cudaGetLastError();
