@@ -88,6 +88,13 @@ struct Params {
     const float *sx;                // decode kernel: (128 + j0) x the token rows' block sums [A][sx_stride(H)]
     float *sh;                      // decode kernel: the same for h, two halves [A][sh_stride(I)]
     int E, H, I, A;
+    // large-batch kernel with packed adapters: after its K stages a tile takes adapter stages
+    // (gate/up: two, down: one) whose A operand is the tile's packed B-adapter rows (copied by
+    // the dequant warps into the A ring) and whose B operand is the tokens' packed, scaled
+    // A-side products (v_hi, v_lo, v_hi, 0); three K = 16 MMAs add B_hi.v_hi + B_hi.v_lo +
+    // B_lo.v_hi to the projection's accumulator
+    int lora_tc;
+    const uint16_t *lbgu, *lbd;     // packed B adapters [E*I][128] (gate slab, up slab), [E*H][64]
     int cmax;                       // token chunk (fixed chunks of cmax, see chunk_base)
     unsigned long long wait_ns;     // limit of every bounded wait
     int extra_need;                 // added to the h publications a down tile waits for (failure-path
@@ -147,7 +154,8 @@ template <int MaxN, int kRawStages, bool kLora>
 __global__ void __launch_bounds__(kThreads, 1)
 q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constant__ CUtensorMap tm_uc,
                  const __grid_constant__ CUtensorMap tm_dc, const __grid_constant__ CUtensorMap tm_x,
-                 const __grid_constant__ CUtensorMap tm_h, const Params p) {
+                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_va,
+                 const __grid_constant__ CUtensorMap tm_vh, const Params p) {
     constexpr int kRawBytes = QCfg<MaxN, kRawStages>::kRawBytes;
     constexpr int kHalfTok = (MaxN / 2) * 128;  // second token half of a two-slab down stage
     extern __shared__ uint8_t smem_raw[];
@@ -283,7 +291,9 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 ++tiles_done;
             }
             const int two = down && N <= MaxN / 2 && nslab % 2 == 0;
-            const int nstage = two ? nslab / 2 : nslab;
+            const int nk = two ? nslab / 2 : nslab;                 // K stages
+            const int nl = p.lora_tc ? (down ? 1 : 2) : 0;          // adapter stages
+            const int nstage = nk + nl;
             const int nbox = N / kNBox;
             const uint32_t bytes = (down && !two ? kCodeBytes : 2 * kCodeBytes) + (two ? 2 : 1) * nbox * kNBox * 128;
             const int wrow = e * (down ? p.H : p.I) + rb * kRows;
@@ -292,18 +302,23 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                     live = false;
                     break;
                 }
+                const int li = ks - nk;  // adapter stage li (>= 0): gate (or down), then up
                 int *mt = rmeta + 8 * r;
-                mt[0] = down | (two << 2);
+                mt[0] = li >= 0 ? down | 8 | (li << 4) : down | (two << 2);
                 mt[1] = ks;
                 mt[2] = nstage;
                 mt[3] = N;
                 mt[4] = e;
                 mt[5] = rb;
                 const uint32_t fb = smem_u32(&rfull[r]);
-                mbar_arrive_expect_tx(fb, bytes);
+                mbar_arrive_expect_tx(fb, li >= 0 ? uint32_t(nbox * kNBox * 128) : bytes);
                 ++rfills;
                 const uint32_t base = smem_u32(raw + r * kRawBytes);
-                if (!down) {
+                if (li >= 0) {
+                    // the tokens' packed products of this projection (64 columns) in the token slot
+                    for (int q = 0; q < nbox; ++q)
+                        tma_load_2d(base + kRawTok + q * 2048, down ? &tm_vh : &tm_va, li * kSlab, r0 + q * kNBox, fb);
+                } else if (!down) {
                     tma_load_2d(base, &tm_gc, ks * (kSlab / 2), wrow, fb);
                     tma_load_2d(base + kCodeBytes, &tm_uc, ks * (kSlab / 2), wrow, fb);
                     for (int q = 0; q < nbox; ++q)
@@ -353,8 +368,23 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             mbar_wait(smem_u32(&aempty[a]), ap ^ 1, wt);
             const int sb = tiles_done & 1;
             if (ks == 0) mbar_wait(smem_u32(&sfull[sb]), (tiles_done >> 1) & 1, wt);
-            if (ks >= 0 && !*abort) {
-                const int down = kind & 3, two = kind >> 2;
+            if (ks >= 0 && !*abort && (kind & 8)) {
+                // adapter stage: this row's 64 bytes (half) of the tile's packed B-adapter row,
+                // into the A slot with the 128-byte swizzle of the rebuilt weights
+                const int down = kind & 3, up = (kind >> 4) & 1;
+                const int e = int(lds_u32(mt + 16)), rb = int(lds_u32(mt + 20));
+                const uint16_t *src = down ? p.lbd + ((size_t)e * p.H + (size_t)rb * kRows + row) * 64
+                                           : p.lbgu + ((size_t)e * p.I + (size_t)rb * kRows + row) * 128 + up * 64;
+                const uint4 *s4 = reinterpret_cast<const uint4 *>(src) + 4 * half;
+                const uint32_t abase = smem_u32(aring + a * kAStageBytes);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int j = 4 * half + i;
+                    sts_v4(abase + uint32_t(row * 128 + ((j ^ (row & 7)) << 4)), __ldg(s4 + i));
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            } else if (ks >= 0 && !*abort) {
+                const int down = kind & 3, two = (kind >> 2) & 1;
                 const uint32_t rbase = smem_u32(raw + r * kRawBytes) + uint32_t(row * 32 + half * 16);
                 const uint32_t abase = smem_u32(aring + a * kAStageBytes);
                 const uint32_t sc = smem_u32(sbuf + sb * kScaleBytes);
@@ -396,7 +426,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const int *mt = rmeta + 8 * r;
             const int kind = mt[0], ks = mt[1], nstage = mt[2], N = mt[3];
             if (__any_sync(0xffffffffu, !got || ks < 0 || *abort)) break;
-            const int down = kind & 3, two = kind >> 2;
+            const int down = kind & 3, two = (kind >> 2) & 1;
             const int b = tile_count & 1;
             if (ks == 0) {
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce[b]), ((tile_count >> 1) & 1) ^ 1, wt)))
@@ -408,7 +438,13 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const uint32_t idesc = instr_desc(kRows, N);
             const uint32_t a0 = smem_u32(aring + a * kAStageBytes);
             const uint32_t bb = smem_u32(raw + r * kRawBytes) + kRawTok;
-            if (!down) {
+            if (kind & 8) {
+                // adapter stage: K = 48 of the 64 columns (the last 16-column group is zero)
+                const uint32_t dd = d + ((kind >> 4) & 1 ? uint32_t(kUpCol) : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 3; ++kk)
+                    mma_bf16_warp(dd, smem_desc(a0 + kk * 32), smem_desc(bb + kk * 32), idesc, true);
+            } else if (!down) {
 #pragma unroll
                 for (int kk = 0; kk < kSlab / 16; ++kk) {
                     const uint64_t bdesc = smem_desc(bb + kk * 32);
@@ -1488,13 +1524,18 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     prm.cmax = cmax;
     prm.wait_ns = wait_limit_ns();
     prm.extra_need = debug_extra_need();
+    // the tokens' packed adapter products (large batches with a pack: adapter stages)
+    CUtensorMap mva = mx, mvh = mh;
+    const bool lora_tc = lora && lora->packed && !decode;
+    if (lora_tc && (!make_map(&mva, xa, A, 128, kNBox) || !make_map(&mvh, ha, A, 64, kNBox)))
+        return cudaErrorInvalidValue;
     auto run = [&](const Params &pr, auto lora_tag) {
         constexpr bool L = decltype(lora_tag)::value;
         if (decode)
             return launch_pdl(q4_decode_kernel<L>, dim3(sm_count()), dim3(kDThreads), kDSmemBytes, st, mg, mu, md, mx,
                               mh, pr);
         return launch_pdl(q4_swiglu_kernel<kChunkN, 4, L>, dim3(sm_count()), dim3(kThreads),
-                          QCfg<kChunkN, 4>::kSmemBytes, st, mg, mu, md, mx, mh, pr);
+                          QCfg<kChunkN, 4>::kSmemBytes, st, mg, mu, md, mx, mh, mva, mvh, pr);
     };
     if (!lora) return run(prm, std::false_type{});
     // with adapters: x . A^T, the gate/up tiles, h . A_down^T (h in the grouped column order), the
@@ -1503,16 +1544,31 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     // one, on CUDA cores in fp32.  Either way the epilogues add the B side.
     prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
     const bool packed = lora->packed != nullptr;
+    if (lora_tc) {
+        // large batches: adapter stages on the tensor cores, the plain epilogue
+        const LoraPack L = lora_pack_layout(s);
+        prm.lora_tc = 1;
+        prm.lbgu = reinterpret_cast<const uint16_t *>(static_cast<const char *>(lora->packed) + L.bgu);
+        prm.lbd = reinterpret_cast<const uint16_t *>(static_cast<const char *>(lora->packed) + L.bd);
+        prm.lora = LoraDev{};
+        if ((e = launch_lora_aside_tc(s, false, x_perm, offsets, *lora, xa, aside, false, err, st)) != cudaSuccess)
+            return e;
+        prm.phase = kPhaseGateUp;
+        if ((e = run(prm, std::false_type{})) != cudaSuccess) return e;
+        if ((e = launch_lora_aside_tc(s, true, h, offsets, *lora, ha, aside, false, err, st)) != cudaSuccess) return e;
+        prm.phase = kPhaseDown;
+        return run(prm, std::false_type{});
+    }
     if (packed) {
         prm.lora.scale = 1.f;  // the tensor-core products come out scaled (fp32)
-        e = launch_lora_aside_tc(s, false, x_perm, offsets, *lora, xa, aside, err, st);
+        e = launch_lora_aside_tc(s, false, x_perm, offsets, *lora, xa, aside, true, err, st);
     } else {
         e = launch_lora_xa(s, x, order, offsets, *lora, xa, lpart, st);
     }
     if (e != cudaSuccess) return e;
     prm.phase = kPhaseGateUp;
     if ((e = run(prm, std::true_type{})) != cudaSuccess) return e;
-    e = packed ? launch_lora_aside_tc(s, true, h, offsets, *lora, ha, aside, err, st)
+    e = packed ? launch_lora_aside_tc(s, true, h, offsets, *lora, ha, aside, true, err, st)
                : launch_lora_ha(s, h, false, true, offsets, *lora, ha, lpart, st);
     if (e != cudaSuccess) return e;
     prm.phase = kPhaseDown;

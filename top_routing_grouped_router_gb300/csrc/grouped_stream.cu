@@ -1024,7 +1024,8 @@ size_t lora_aside_bytes(const moe_shape &s) {
 }
 
 cudaError_t launch_lora_aside_tc(const moe_shape &s, bool h_side, const void *src, const int32_t *offsets,
-                                 const moe_lora &lora, void *out, char *region, int32_t *err, cudaStream_t st) {
+                                 const moe_lora &lora, void *out, char *region, bool f32, int32_t *err,
+                                 cudaStream_t st) {
     const int A = s.T * s.k;
     if (A == 0) return cudaSuccess;
     int *sched = reinterpret_cast<int *>(region);
@@ -1073,7 +1074,7 @@ cudaError_t launch_lora_aside_tc(const moe_shape &s, bool h_side, const void *sr
     prm.k = s.k;
     prm.lora_packed = 1;
     prm.lora_scale = lora.scale;
-    prm.lora_f32 = 1;
+    prm.lora_f32 = f32 ? 1 : 0;
     prm.xab = h_side ? nullptr : static_cast<uint16_t *>(out);
     prm.hab = h_side ? static_cast<uint16_t *>(out) : nullptr;
     return launch_tc_for<kLoraPacked>(s, tc_wide(s), dim3(tc::sm_count()), st, m, prm);

@@ -259,11 +259,14 @@ size_t q4_part_bytes(const moe_shape &s);
 // bf16 tensor-core kernel's A-side tiles, in a launch of their own (after the 4-bit prep has
 // put the token rows into expert order, or after the gate/up tiles for h).  src: bf16
 // [A][H] or [A][I] rows in the 4-bit path's 8-element group order (the pack's A columns
-// follow it); out: scale * src . A^T in fp32, [A][32] (gate, up) or [A][16]; region:
-// lora_aside_bytes() bytes of scratch (tile list and counters).
+// follow it); out: scale * src . A^T, in fp32 ([A][32] gate and up, or [A][16]) with f32, else
+// packed as the bf16 path's B-side stages read it ([A][128] or [A][64] bf16, each 64-column
+// projection slab (v_hi, v_lo, v_hi, 0)); region: lora_aside_bytes() bytes of scratch (tile
+// list and counters).
 size_t lora_aside_bytes(const moe_shape &s);
 cudaError_t launch_lora_aside_tc(const moe_shape &s, bool h_side, const void *src, const int32_t *offsets,
-                                 const moe_lora &lora, void *out, char *region, int32_t *err, cudaStream_t st);
+                                 const moe_lora &lora, void *out, char *region, bool f32, int32_t *err,
+                                 cudaStream_t st);
 cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets, const int32_t *order,
                       const void *wg, const void *wu, const void *wd, const moe_q4 *q4, float *part, void *h, void *y,
                       int32_t *err, cudaStream_t st, const moe_lora *lora = nullptr, float *xa = nullptr,
