@@ -568,8 +568,7 @@ def run_ours(args, rank, world, local):
                    "entry": {"forward": "moe_forward", "rmsnorm": "moe_forward_rmsnorm (pre-router RMSNorm + residual)",
                              "lora": "moe_forward_lora (rank-16 fp32 adapters on the expert projections"
                                       + (", packed: tensor-core adapter products)" if inp0.w == "bf16" and not args.lora_unpacked
-                                         else (", packed: tensor-core adapter products)" if inp0.T > 64 else
-                                               ", packed: tensor-core A-side products, B side in the epilogue)")
+                                         else ", packed: tensor-core adapter products)"
                                          if inp0.w == "q4" and not args.lora_unpacked
                                          else ", CUDA-core adapter products)")}[head["entry"]],
                    "T": head["T"], "H": head["H"], "E": head["E"], "k": head["k"], "I": head["I"],

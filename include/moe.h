@@ -121,10 +121,9 @@ typedef struct {
  * scale * x . A^T) is split as hi = bf16(v), lo = bf16(v - hi), and the products
  * are hi.hi + hi.lo + lo.hi with fp32 accumulation (x is bf16 already, so
  * x . A^T takes x.hi + x.lo): close to fp32 accuracy.  The 4-bit tensor-core
- * path takes the A-side products (x . A^T, h . A_down^T) from the tensor cores
- * the same way; for large batches (T > 64) its B side runs there too, and for
- * decode batches it is added in fp32 in the epilogues.  Without a pack, and on
- * every other path, the products run in fp32 on CUDA cores.
+ * path does the same: the A-side products in launches of their own, the B side
+ * as one more MMA stage of each tile.  Without a pack, and on every other path,
+ * the products run in fp32 on CUDA cores.
  */
 typedef struct {
     int32_t rank;

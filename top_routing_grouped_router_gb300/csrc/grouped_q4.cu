@@ -783,6 +783,37 @@ __device__ __forceinline__ void q4d_stage_down(uint32_t d, uint32_t ta, uint64_t
         ::"r"(d), "r"(ta), "l"(b0), "r"(idesc), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// Adapter stage (packed adapters): K = 48 of each 64-column adapter slab in the A stage (the
+// last 16 columns are zero).  Gate and up (or a down pair's two row halves) go to the partial's
+// first and second 16 columns; B is the tokens' packed products, b1 for the second slab (the up
+// products, or the same products for a down pair).
+#define Q4D_MMA1(DOFF, AOFF, BOFF, P)                                                                     \
+    "add.u32 dd, %0, " #DOFF ";\n\tadd.u32 aa, %1, " #AOFF ";\n\tadd.s64 bd, %7, " #BOFF ";\n\t"        \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [dd], [aa], bd, %3, " #P ";\n\t"
+__device__ __forceinline__ void q4d_stage_adapter(uint32_t d, uint32_t ta, uint64_t b0, uint32_t idesc, uint32_t c0,
+                                                  uint32_t c1, uint32_t c2, uint64_t b1) {
+    asm volatile(
+        "{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 dd, aa;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        Q4D_MMA(0, 0, 0, pf) Q4D_MMA(0, 8, 2, pt) Q4D_MMA(0, 16, 4, pt)
+        Q4D_MMA1(16, 64, 0, pf) Q4D_MMA1(16, 72, 2, pt) Q4D_MMA1(16, 80, 4, pt)
+        Q4D_COMMITS "}"
+        ::"r"(d), "r"(ta), "l"(b0), "r"(idesc), "r"(c0), "r"(c1), "r"(c2), "l"(b1)
+        : "memory");
+}
+__device__ __forceinline__ void q4d_stage_adapter1(uint32_t d, uint32_t ta, uint64_t b0, uint32_t idesc, uint32_t c0,
+                                                   uint32_t c1, uint32_t c2) {
+    asm volatile(
+        "{\n\t.reg .pred e, pf, pt;\n\t.reg .b32 dd, aa;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 pf, %0, %0;\n\tsetp.eq.b32 pt, %0, %0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        Q4D_MMA(0, 0, 0, pf) Q4D_MMA(0, 8, 2, pt) Q4D_MMA(0, 16, 4, pt)
+        Q4D_COMMITS "}"
+        ::"r"(d), "r"(ta), "l"(b0), "r"(idesc), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+#undef Q4D_MMA1
 #undef Q4D_MMA
 #undef Q4D_COMMITS
 
@@ -839,11 +870,22 @@ __device__ __forceinline__ bool q4d_consume_tile(const Params &p, const Waits &w
     float acc0[NT], acc1[NT];
 #pragma unroll
     for (int i = 0; i < NT; ++i) acc0[i] = acc1[i] = 0.f;
+    const int nk = t.nstage - (p.lora_tc ? 1 : 0);  // K stages; then the adapter stage
     for (int ks = 0; ks < t.nstage; ++ks) {
         if (!mbar_wait(c.pfull + 8u * c.pb, c.pp, wt)) return false;
         tc_fence_after();
         const uint32_t ta = c.tq + uint32_t(c.pb * kDPartCols);
-        if (t.kind != kQ4Down) {
+        if (ks >= nk) {
+            // adapter stage: its products are already scaled, added as they are
+            float v[2][NT];
+            const uint32_t tt[2] = {ta, ta + 16};
+            tmem_ld_cols<NT, 2>(tt, v);
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                acc0[i] += v[0][i];
+                if (t.kind != kQ4Down) acc1[i] += v[1][i];
+            }
+        } else if (t.kind != kQ4Down) {
             uint32_t gw, uw;  // the scales of blocks 2 ks (low half) and 2 ks + 1 (high half)
             if (vec8) {
                 if ((ks & 3) == 0) {
@@ -979,7 +1021,8 @@ template <bool kLora>
 __global__ void __launch_bounds__(kDThreads, 1)
 q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constant__ CUtensorMap tm_uc,
                  const __grid_constant__ CUtensorMap tm_dc, const __grid_constant__ CUtensorMap tm_x,
-                 const __grid_constant__ CUtensorMap tm_h, const Params p) {
+                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_va,
+                 const __grid_constant__ CUtensorMap tm_vh, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned by pointer arithmetic on the shared array, so that the compiler keeps
     // the shared address space (and emits shared, not generic, loads) for everything derived
@@ -1097,7 +1140,8 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             const int nblk = down ? nblk_i : nblk_h;
-            const int nstage = nblk / 2;
+            const int nk = nblk / 2;                     // K stages
+            const int nstage = nk + (p.lora_tc ? 1 : 0);  // and the adapter stage
             if (!mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, wt)) break;
             int *tm = tmeta + 8 * slot;
             tm[0] = kind;
@@ -1140,14 +1184,28 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                     live = false;
                     break;
                 }
+                const bool adapter = ks >= nk;
                 int *mt = rmeta + 4 * r;
-                mt[0] = kind;
+                mt[0] = kind | (adapter ? 8 : 0);
                 mt[1] = ks;
                 mt[2] = N;
+                mt[3] = (e << 16) | rb;
                 const uint32_t fb = smem_u32(&rfull[r]);
-                mbar_arrive_expect_tx(fb, bytes);
                 ++rfills;
                 const uint32_t base = smem_u32(raw + r * kDRawBytes);
+                if (adapter) {
+                    // the tokens' packed adapter products in the token slot: gate and up slabs, or
+                    // the down products (one slab, both row halves read it)
+                    mbar_arrive_expect_tx(fb, kind == kQ4GateUp ? 2 * kDTokSlab : kDTokSlab);
+                    if (kind == kQ4GateUp)
+                        tma_load_3d(base + kDTok, &tm_va, 0, r0, 0, fb);
+                    else
+                        tma_load_2d(base + kDTok, &tm_vh, 0, r0, fb);
+                    if (++r == kDRawStages) { r = 0; rp ^= 1; }
+                    if (ks == kfetch && next < hi) fetch(next);
+                    continue;
+                }
+                mbar_arrive_expect_tx(fb, bytes);
                 tma_load_2d(base, down ? &tm_dc : &tm_gc, ks * (kDK / 2), wrow, fb);
                 if (kind == kQ4GateUp) tma_load_2d(base + kDCodeBytes, &tm_uc, ks * (kDK / 2), wrow, fb);
                 if (kind == kQ4DownPair) tma_load_2d(base + kDCodeBytes, &tm_dc, ks * (kDK / 2), wrow + kRows, fb);
@@ -1183,12 +1241,43 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&rfull[r]), rp, wt))) break;
             const uint2 md = lds_v2(smem_u32(rmeta + 4 * r));
-            const bool two = int(md.x) != kQ4Down;  // two code slabs: gate and up, or two row halves
+            const bool adapter = (md.x & 8u) != 0;
+            const bool two = int(md.x & 7u) != kQ4Down;  // two slabs: gate and up, or two row halves
             const int ks = int(md.y);
             // the sentinel (ks < 0) is passed on to the MMA warp through the A ring
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&aempty[a]), ap ^ 1, wt))) break;
             tc_fence_after();
-            if (ks >= 0) {
+            if (ks >= 0 && adapter) {
+                // adapter stage: this row's packed adapter rows (64 bf16 each) into the A stage,
+                // gate (lower half) at column 0, up (upper half) at column 64
+                const uint32_t er = lds_u32(smem_u32(rmeta + 4 * r + 3));
+                const int e = int(er >> 16), rb = int(er & 0xFFFF);
+                const uint32_t ta = tlane + uint32_t(kDACol + a * kDAStageCols);
+                const uint16_t *s0, *s1;
+                if (int(md.x & 7u) == kQ4GateUp) {
+                    s0 = p.lbgu + ((size_t)e * p.I + (size_t)rb * kRows + row) * 128;
+                    s1 = s0 + 64;
+                } else {
+                    s0 = p.lbd + ((size_t)e * p.H + (size_t)rb * 2 * kRows + row) * 64;
+                    s1 = s0 + (size_t)kRows * 64;
+                }
+                uint32_t v[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(s0) + i);
+                    v[4 * i] = w.x; v[4 * i + 1] = w.y; v[4 * i + 2] = w.z; v[4 * i + 3] = w.w;
+                }
+                tmem_st32(ta, v);
+                if (two) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(s1) + i);
+                        v[4 * i] = w.x; v[4 * i + 1] = w.y; v[4 * i + 2] = w.z; v[4 * i + 3] = w.w;
+                    }
+                    tmem_st32(ta + 64, v);
+                }
+                tmem_st_wait();
+            } else if (ks >= 0) {
                 // a row's codes of a stage are 64 bytes: two slabs of 32.  Every load is issued
                 // before the first conversion (the asm statements keep their order).
                 const uint32_t cb = smem_u32(raw + r * kDRawBytes) + uint32_t(row * (kDK / 2));
@@ -1228,7 +1317,8 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         for (;;) {
             const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&afull[a]), ap, wt));
             const int *mt = rmeta + 4 * r;
-            const int kind = mt[0], ks = mt[1], N = mt[2];
+            const int kindw = mt[0], ks = mt[1], N = mt[2];
+            const int kind = kindw & 7;
             if (__any_sync(0xffffffffu, !got || ks < 0 || abort_raised(wt))) break;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&pempty[pb]), pp ^ 1, wt))) break;
             tc_fence_after();
@@ -1239,10 +1329,16 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             // (address / 16, 14 bits: shared memory stays below 256 KB, so adding cannot carry)
             const uint64_t b0 = smem_desc(smem_u32(raw + r * kDRawBytes) + kDTok);
             const uint32_t c0 = smem_u32(&aempty[a]), c1 = smem_u32(&rempty[r]), c2 = smem_u32(&pfull[pb]);
-            if (kind != kQ4Down)
+            if (kindw & 8) {
+                if (kind == kQ4Down)
+                    q4d_stage_adapter1(d, ta, b0, idesc, c0, c1, c2);
+                else  // the up products in the second token slab; a down pair's halves share one
+                    q4d_stage_adapter(d, ta, b0, idesc, c0, c1, c2, b0 + (kind == kQ4GateUp ? 128u : 0u));
+            } else if (kind != kQ4Down) {
                 q4d_stage_gate_up(d, ta, b0, idesc, c0, c1, c2);
-            else
+            } else {
                 q4d_stage_down(d, ta, b0, idesc, c0, c1, c2);
+            }
             if (++r == kDRawStages) r = 0;
             if (++a == kDAS) { a = 0; ap ^= 1; }
             if (++pb == kDPS) { pb = 0; pp ^= 1; }
@@ -1526,14 +1622,15 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     prm.extra_need = debug_extra_need();
     // the tokens' packed adapter products (large batches with a pack: adapter stages)
     CUtensorMap mva = mx, mvh = mh;
-    const bool lora_tc = lora && lora->packed && !decode;
-    if (lora_tc && (!make_map(&mva, xa, A, 128, kNBox) || !make_map(&mvh, ha, A, 64, kNBox)))
+    const bool lora_tc = lora && lora->packed;
+    if (lora_tc && (!(decode ? make_map_slabs(&mva, xa, A, 128, kNBox, 2) : make_map(&mva, xa, A, 128, kNBox)) ||
+                    !make_map(&mvh, ha, A, 64, kNBox)))
         return cudaErrorInvalidValue;
     auto run = [&](const Params &pr, auto lora_tag) {
         constexpr bool L = decltype(lora_tag)::value;
         if (decode)
             return launch_pdl(q4_decode_kernel<L>, dim3(sm_count()), dim3(kDThreads), kDSmemBytes, st, mg, mu, md, mx,
-                              mh, pr);
+                              mh, mva, mvh, pr);
         return launch_pdl(q4_swiglu_kernel<kChunkN, 4, L>, dim3(sm_count()), dim3(kThreads),
                           QCfg<kChunkN, 4>::kSmemBytes, st, mg, mu, md, mx, mh, mva, mvh, pr);
     };
@@ -1545,7 +1642,7 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     prm.lora = LoraDev{lora->b_gate, lora->b_up, lora->b_down, xa, ha, lora->rank, lora->scale};
     const bool packed = lora->packed != nullptr;
     if (lora_tc) {
-        // large batches: adapter stages on the tensor cores, the plain epilogue
+        // adapter stages on the tensor cores, the plain epilogue
         const LoraPack L = lora_pack_layout(s);
         prm.lora_tc = 1;
         prm.lbgu = reinterpret_cast<const uint16_t *>(static_cast<const char *>(lora->packed) + L.bgu);
