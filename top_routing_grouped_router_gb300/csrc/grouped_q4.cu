@@ -93,13 +93,24 @@ struct Params {
     // the dequant warps into the A ring) and whose B operand is the tokens' packed, scaled
     // A-side products (v_hi, v_lo, v_hi, 0); three K = 16 MMAs add B_hi.v_hi + B_hi.v_lo +
     // B_lo.v_hi to the projection's accumulator
-    int lora_tc;
     const uint16_t *lbgu, *lbd;     // packed B adapters [E*I][128] (gate slab, up slab), [E*H][64]
     int cmax;                       // token chunk (fixed chunks of cmax, see chunk_base)
     unsigned long long wait_ns;     // limit of every bounded wait
     int extra_need;                 // added to the h publications a down tile waits for (failure-path
                                     // test: a count nothing reaches, so those waits must run out)
 };
+
+// Kernel modes: no adapters; adapters with the B side added in the epilogues (fp32, CUDA
+// cores); adapter stages (packed adapters, tensor cores).  Only the last takes the maps of the
+// tokens' packed adapter products: two more tensor maps in every instantiation's parameter
+// block slowed the plain 4-bit kernels by about 4%.
+enum : int { kQ4Plain = 0, kQ4LoraEpi = 1, kQ4LoraTc = 2 };
+struct Q4VMaps {
+    CUtensorMap va, vh;  // packed products of x (gate, up slabs) and of h
+};
+struct Q4NoVMaps {};
+template <int M> struct Q4VMapsOf { using type = Q4NoVMaps; };
+template <> struct Q4VMapsOf<kQ4LoraTc> { using type = Q4VMaps; };
 
 // The 8-element group order of the weights: position q holds element kSigma[q].
 __device__ __forceinline__ int sigma_inv(int i) { return ((i & 3) << 1) | (i >> 2); }
@@ -150,12 +161,14 @@ __device__ __forceinline__ uint32_t gamma_pair(uint16_t scale, float half_b) {
     return g | (g << 16);
 }
 
-template <int MaxN, int kRawStages, bool kLora>
+template <int MaxN, int kRawStages, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constant__ CUtensorMap tm_uc,
                  const __grid_constant__ CUtensorMap tm_dc, const __grid_constant__ CUtensorMap tm_x,
-                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_va,
-                 const __grid_constant__ CUtensorMap tm_vh, const Params p) {
+                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ typename Q4VMapsOf<kMode>::type vm,
+                 const Params p) {
+    constexpr bool kLora = kMode == kQ4LoraEpi;
+    constexpr bool kAdapt = kMode == kQ4LoraTc;
     constexpr int kRawBytes = QCfg<MaxN, kRawStages>::kRawBytes;
     constexpr int kHalfTok = (MaxN / 2) * 128;  // second token half of a two-slab down stage
     extern __shared__ uint8_t smem_raw[];
@@ -292,7 +305,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             }
             const int two = down && N <= MaxN / 2 && nslab % 2 == 0;
             const int nk = two ? nslab / 2 : nslab;                 // K stages
-            const int nl = p.lora_tc ? (down ? 1 : 2) : 0;          // adapter stages
+            const int nl = kAdapt ? (down ? 1 : 2) : 0;             // adapter stages
             const int nstage = nk + nl;
             const int nbox = N / kNBox;
             const uint32_t bytes = (down && !two ? kCodeBytes : 2 * kCodeBytes) + (two ? 2 : 1) * nbox * kNBox * 128;
@@ -316,8 +329,10 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 const uint32_t base = smem_u32(raw + r * kRawBytes);
                 if (li >= 0) {
                     // the tokens' packed products of this projection (64 columns) in the token slot
-                    for (int q = 0; q < nbox; ++q)
-                        tma_load_2d(base + kRawTok + q * 2048, down ? &tm_vh : &tm_va, li * kSlab, r0 + q * kNBox, fb);
+                    if constexpr (kAdapt)
+                        for (int q = 0; q < nbox; ++q)
+                            tma_load_2d(base + kRawTok + q * 2048, down ? &vm.vh : &vm.va, li * kSlab, r0 + q * kNBox,
+                                        fb);
                 } else if (!down) {
                     tma_load_2d(base, &tm_gc, ks * (kSlab / 2), wrow, fb);
                     tma_load_2d(base + kCodeBytes, &tm_uc, ks * (kSlab / 2), wrow, fb);
@@ -368,7 +383,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             mbar_wait(smem_u32(&aempty[a]), ap ^ 1, wt);
             const int sb = tiles_done & 1;
             if (ks == 0) mbar_wait(smem_u32(&sfull[sb]), (tiles_done >> 1) & 1, wt);
-            if (ks >= 0 && !*abort && (kind & 8)) {
+            if (kAdapt && ks >= 0 && !*abort && (kind & 8)) {
                 // adapter stage: this row's 64 bytes (half) of the tile's packed B-adapter row,
                 // into the A slot with the 128-byte swizzle of the rebuilt weights
                 const int down = kind & 3, up = (kind >> 4) & 1;
@@ -438,7 +453,7 @@ q4_swiglu_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             const uint32_t idesc = instr_desc(kRows, N);
             const uint32_t a0 = smem_u32(aring + a * kAStageBytes);
             const uint32_t bb = smem_u32(raw + r * kRawBytes) + kRawTok;
-            if (kind & 8) {
+            if (kAdapt && (kind & 8)) {
                 // adapter stage: K = 48 of the 64 columns (the last 16-column group is zero)
                 const uint32_t dd = d + ((kind >> 4) & 1 ? uint32_t(kUpCol) : 0u);
 #pragma unroll
@@ -853,7 +868,7 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
 // A consumer's whole tile: per stage, the partials of the first NT token columns (NT >= the
 // chunk's m) are corrected by the block sums, scaled and accumulated; then SwiGLU and the h
 // store (gate/up) or the y store (down).  Returns false when a wait gave up.
-template <int NT, bool kLora>
+template <int NT, bool kLora, bool kAdapt>
 __device__ __forceinline__ bool q4d_consume_tile(const Params &p, const Waits &wt, Q4DCons &c, const Q4DTile &t) {
     const bool down = t.kind != kQ4GateUp;
     const bool pair = t.kind == kQ4DownPair;
@@ -870,7 +885,7 @@ __device__ __forceinline__ bool q4d_consume_tile(const Params &p, const Waits &w
     float acc0[NT], acc1[NT];
 #pragma unroll
     for (int i = 0; i < NT; ++i) acc0[i] = acc1[i] = 0.f;
-    const int nk = t.nstage - (p.lora_tc ? 1 : 0);  // K stages; then the adapter stage
+    const int nk = t.nstage - (kAdapt ? 1 : 0);  // K stages; then the adapter stage
     for (int ks = 0; ks < t.nstage; ++ks) {
         if (!mbar_wait(c.pfull + 8u * c.pb, c.pp, wt)) return false;
         tc_fence_after();
@@ -1017,12 +1032,14 @@ __device__ __forceinline__ bool q4d_consume_tile(const Params &p, const Waits &w
     return true;
 }
 
-template <bool kLora>
+template <int kMode>
 __global__ void __launch_bounds__(kDThreads, 1)
 q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constant__ CUtensorMap tm_uc,
                  const __grid_constant__ CUtensorMap tm_dc, const __grid_constant__ CUtensorMap tm_x,
-                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_va,
-                 const __grid_constant__ CUtensorMap tm_vh, const Params p) {
+                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ typename Q4VMapsOf<kMode>::type vm,
+                 const Params p) {
+    constexpr bool kLora = kMode == kQ4LoraEpi;
+    constexpr bool kAdapt = kMode == kQ4LoraTc;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned by pointer arithmetic on the shared array, so that the compiler keeps
     // the shared address space (and emits shared, not generic, loads) for everything derived
@@ -1141,7 +1158,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             }
             const int nblk = down ? nblk_i : nblk_h;
             const int nk = nblk / 2;                     // K stages
-            const int nstage = nk + (p.lora_tc ? 1 : 0);  // and the adapter stage
+            const int nstage = nk + (kAdapt ? 1 : 0);     // and the adapter stage
             if (!mbar_wait(smem_u32(&tme[slot]), mphase ^ 1, wt)) break;
             int *tm = tmeta + 8 * slot;
             tm[0] = kind;
@@ -1197,10 +1214,12 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                     // the tokens' packed adapter products in the token slot: gate and up slabs, or
                     // the down products (one slab, both row halves read it)
                     mbar_arrive_expect_tx(fb, kind == kQ4GateUp ? 2 * kDTokSlab : kDTokSlab);
-                    if (kind == kQ4GateUp)
-                        tma_load_3d(base + kDTok, &tm_va, 0, r0, 0, fb);
-                    else
-                        tma_load_2d(base + kDTok, &tm_vh, 0, r0, fb);
+                    if constexpr (kAdapt) {
+                        if (kind == kQ4GateUp)
+                            tma_load_3d(base + kDTok, &vm.va, 0, r0, 0, fb);
+                        else
+                            tma_load_2d(base + kDTok, &vm.vh, 0, r0, fb);
+                    }
                     if (++r == kDRawStages) { r = 0; rp ^= 1; }
                     if (ks == kfetch && next < hi) fetch(next);
                     continue;
@@ -1241,7 +1260,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         for (;;) {
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&rfull[r]), rp, wt))) break;
             const uint2 md = lds_v2(smem_u32(rmeta + 4 * r));
-            const bool adapter = (md.x & 8u) != 0;
+            const bool adapter = kAdapt && (md.x & 8u) != 0;
             const bool two = int(md.x & 7u) != kQ4Down;  // two slabs: gate and up, or two row halves
             const int ks = int(md.y);
             // the sentinel (ks < 0) is passed on to the MMA warp through the A ring
@@ -1329,7 +1348,7 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             // (address / 16, 14 bits: shared memory stays below 256 KB, so adding cannot carry)
             const uint64_t b0 = smem_desc(smem_u32(raw + r * kDRawBytes) + kDTok);
             const uint32_t c0 = smem_u32(&aempty[a]), c1 = smem_u32(&rempty[r]), c2 = smem_u32(&pfull[pb]);
-            if (kindw & 8) {
+            if (kAdapt && (kindw & 8)) {
                 if (kind == kQ4Down)
                     q4d_stage_adapter1(d, ta, b0, idesc, c0, c1, c2);
                 else  // the up products in the second token slab; a down pair's halves share one
@@ -1368,10 +1387,10 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             if (!mbar_wait(smem_u32(&sfull[sb]), (tiles / kDSideBufs) & 1, wt)) break;
             const Q4DTile t{kind, e, rb, r0, m, nstage, smem_u32(side + sb * kDSide), smem_u32(&sempty[sb])};
             // (the adapter variant keeps one width: three inlined copies of its epilogue spill)
-            const bool ok = kLora     ? q4d_consume_tile<16, kLora>(p, wt, c, t)
-                            : m <= 4 ? q4d_consume_tile<4, kLora>(p, wt, c, t)
-                            : m <= 8 ? q4d_consume_tile<8, kLora>(p, wt, c, t)
-                                     : q4d_consume_tile<16, kLora>(p, wt, c, t);
+            const bool ok = kLora     ? q4d_consume_tile<16, kLora, kAdapt>(p, wt, c, t)
+                            : m <= 4 ? q4d_consume_tile<4, kLora, kAdapt>(p, wt, c, t)
+                            : m <= 8 ? q4d_consume_tile<8, kLora, kAdapt>(p, wt, c, t)
+                                     : q4d_consume_tile<16, kLora, kAdapt>(p, wt, c, t);
             if (!ok) break;
             ++tiles;
         }
@@ -1479,7 +1498,7 @@ q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, 
 
 size_t xperm_bytes(const moe_shape &s) { return ((size_t)s.T * s.k * s.H * 2 + 255) / 256 * 256; }
 
-template <int MaxN, int RawStages, bool Lora>
+template <int MaxN, int RawStages, int Lora>
 bool set_attr() {
     static bool attr_set[64] = {};
     int dev = 0;
@@ -1493,7 +1512,7 @@ bool set_attr() {
     return true;
 }
 
-template <bool Lora>
+template <int Lora>
 bool set_decode_attr() {
     static bool attr_set[64] = {};
     int dev = 0;
@@ -1585,8 +1604,9 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
                                (int)q4_max_tiles(s), x_perm, tiles, sched,
                                done, err, decode ? sx : nullptr, 128.0f + 0.5f * float(t2));
     if (e != cudaSuccess) return e;
-    if (!(decode ? set_decode_attr<false>() && set_decode_attr<true>()
-                 : set_attr<kChunkN, 4, false>() && set_attr<kChunkN, 4, true>()))
+    if (!(decode ? set_decode_attr<kQ4Plain>() && set_decode_attr<kQ4LoraEpi>() && set_decode_attr<kQ4LoraTc>()
+                 : set_attr<kChunkN, 4, kQ4Plain>() && set_attr<kChunkN, 4, kQ4LoraEpi>() &&
+                       set_attr<kChunkN, 4, kQ4LoraTc>()))
         return cudaErrorInvalidValue;
     Params prm{};
     prm.offsets = offsets;
@@ -1626,15 +1646,21 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     if (lora_tc && (!(decode ? make_map_slabs(&mva, xa, A, 128, kNBox, 2) : make_map(&mva, xa, A, 128, kNBox)) ||
                     !make_map(&mvh, ha, A, 64, kNBox)))
         return cudaErrorInvalidValue;
-    auto run = [&](const Params &pr, auto lora_tag) {
-        constexpr bool L = decltype(lora_tag)::value;
+    auto run = [&](const Params &pr, auto mode_tag) {
+        constexpr int M = decltype(mode_tag)::value;
+        using VM = typename Q4VMapsOf<M>::type;
+        VM vm{};
+        if constexpr (M == kQ4LoraTc) vm = Q4VMaps{mva, mvh};
         if (decode)
-            return launch_pdl(q4_decode_kernel<L>, dim3(sm_count()), dim3(kDThreads), kDSmemBytes, st, mg, mu, md, mx,
-                              mh, mva, mvh, pr);
-        return launch_pdl(q4_swiglu_kernel<kChunkN, 4, L>, dim3(sm_count()), dim3(kThreads),
-                          QCfg<kChunkN, 4>::kSmemBytes, st, mg, mu, md, mx, mh, mva, mvh, pr);
+            return launch_pdl(q4_decode_kernel<M>, dim3(sm_count()), dim3(kDThreads), kDSmemBytes, st, mg, mu, md, mx,
+                              mh, vm, pr);
+        return launch_pdl(q4_swiglu_kernel<kChunkN, 4, M>, dim3(sm_count()), dim3(kThreads),
+                          QCfg<kChunkN, 4>::kSmemBytes, st, mg, mu, md, mx, mh, vm, pr);
     };
-    if (!lora) return run(prm, std::false_type{});
+    using Plain = std::integral_constant<int, kQ4Plain>;
+    using Epi = std::integral_constant<int, kQ4LoraEpi>;
+    using Tc = std::integral_constant<int, kQ4LoraTc>;
+    if (!lora) return run(prm, Plain{});
     // with adapters: x . A^T, the gate/up tiles, h . A_down^T (h in the grouped column order), the
     // down tiles.  With a pack the A-side products run on the tensor cores (from x_perm and h in
     // the grouped order, which the pack's A columns follow) and come out scaled, in fp32; without
@@ -1644,17 +1670,16 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     if (lora_tc) {
         // adapter stages on the tensor cores, the plain epilogue
         const LoraPack L = lora_pack_layout(s);
-        prm.lora_tc = 1;
         prm.lbgu = reinterpret_cast<const uint16_t *>(static_cast<const char *>(lora->packed) + L.bgu);
         prm.lbd = reinterpret_cast<const uint16_t *>(static_cast<const char *>(lora->packed) + L.bd);
         prm.lora = LoraDev{};
         if ((e = launch_lora_aside_tc(s, false, x_perm, offsets, *lora, xa, aside, false, err, st)) != cudaSuccess)
             return e;
         prm.phase = kPhaseGateUp;
-        if ((e = run(prm, std::false_type{})) != cudaSuccess) return e;
+        if ((e = run(prm, Tc{})) != cudaSuccess) return e;
         if ((e = launch_lora_aside_tc(s, true, h, offsets, *lora, ha, aside, false, err, st)) != cudaSuccess) return e;
         prm.phase = kPhaseDown;
-        return run(prm, std::false_type{});
+        return run(prm, Tc{});
     }
     if (packed) {
         prm.lora.scale = 1.f;  // the tensor-core products come out scaled (fp32)
@@ -1664,12 +1689,12 @@ cudaError_t launch_q4(const moe_shape &s, const void *x, const int32_t *offsets,
     }
     if (e != cudaSuccess) return e;
     prm.phase = kPhaseGateUp;
-    if ((e = run(prm, std::true_type{})) != cudaSuccess) return e;
+    if ((e = run(prm, Epi{})) != cudaSuccess) return e;
     e = packed ? launch_lora_aside_tc(s, true, h, offsets, *lora, ha, aside, true, err, st)
                : launch_lora_ha(s, h, false, true, offsets, *lora, ha, lpart, st);
     if (e != cudaSuccess) return e;
     prm.phase = kPhaseDown;
-    return run(prm, std::true_type{});
+    return run(prm, Epi{});
 }
 
 }  // namespace moe
