@@ -1051,14 +1051,18 @@ cudaError_t launch_lora_aside_tc(const moe_shape &s, bool h_side, const void *sr
     m.hm = m.xm;
     m.l.ha16 = m.l.xa16;
     m.l.ha128 = m.l.xa128;
-    // the tile list alone (one block of the prep kernel): A-side tiles per 128-token chunk of
-    // an expert; no publication count (h is complete: the gate/up tiles ran in an earlier launch)
-    TileListArgs ta = tc_tile_args(s, kLoraPacked);
-    ta.pub = 0;
-    cudaError_t e = launch_pdl(prep_kernel, dim3(1), dim3(256), 0, st, static_cast<const uint16_t *>(nullptr),
-                               static_cast<const int32_t *>(nullptr), offsets, s.T, s.k, s.H, s.E, ta,
-                               static_cast<uint16_t *>(nullptr), tiles, sched, done, err);
-    if (e != cudaSuccess) return e;
+    // the tile list alone (one block of the prep kernel), built for the x side: A-side tiles per
+    // 128-token chunk of an expert, both the x and the h section (each phase claims from its own
+    // counter, so the h side reuses the list); no publication count (h is complete: the gate/up
+    // tiles ran in an earlier launch)
+    if (!h_side) {
+        TileListArgs ta = tc_tile_args(s, kLoraPacked);
+        ta.pub = 0;
+        cudaError_t e = launch_pdl(prep_kernel, dim3(1), dim3(256), 0, st, static_cast<const uint16_t *>(nullptr),
+                                   static_cast<const int32_t *>(nullptr), offsets, s.T, s.k, s.H, s.E, ta,
+                                   static_cast<uint16_t *>(nullptr), tiles, sched, done, err);
+        if (e != cudaSuccess) return e;
+    }
     Params prm{};
     prm.tiles = tiles;
     prm.sched = sched;

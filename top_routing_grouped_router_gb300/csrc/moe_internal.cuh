@@ -262,7 +262,8 @@ size_t q4_part_bytes(const moe_shape &s);
 // follow it); out: scale * src . A^T, in fp32 ([A][32] gate and up, or [A][16]) with f32, else
 // packed as the bf16 path's B-side stages read it ([A][128] or [A][64] bf16, each 64-column
 // projection slab (v_hi, v_lo, v_hi, 0)); region: lora_aside_bytes() bytes of scratch (tile
-// list and counters).
+// list and counters).  The x side builds the tile list, and the h side (same region, same
+// offsets, later in the stream) uses it.
 size_t lora_aside_bytes(const moe_shape &s);
 cudaError_t launch_lora_aside_tc(const moe_shape &s, bool h_side, const void *src, const int32_t *offsets,
                                  const moe_lora &lora, void *out, char *region, bool f32, int32_t *err,
