@@ -103,6 +103,30 @@ def test_all_tokens_to_the_same_experts():
     assert (g["counts"][[3, 17, 22, 30]] == 40).all()
 
 
+def test_exact_logit_ties_pick_the_lower_expert_first():
+    # experts 5, 9 and 12 get expert 2's router row and bias, so their logits equal expert 2's
+    # bit for bit on every token (same rows, same arithmetic); with k = 3 the tie straddles the
+    # selection boundary, and the slots must hold 2, 5, 9 in that order, as in the oracle (a
+    # tie goes to the lower expert index)
+    import top_routing_grouped_router_gb300 as moe
+    from top_routing_grouped_router_gb300.device import upload
+    inp = synth.make_custom(16, 256, 32, 3, 128, act="bf16", w="bf16", seed=21)
+    for e in (5, 9, 12):
+        inp.w_router[e] = inp.w_router[2]
+    bias = np.zeros(32, np.float32)
+    bias[[2, 5, 9, 12]] = 8.0
+    inp.b_router = bias
+    L = upload(inp)
+    out = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((inp.T, inp.k), dtype=torch.int32, device="cuda")
+    moe.moe_forward(L.shape, L.x, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, None, out, ids,
+                    workspace=L.new_workspace())
+    torch.cuda.synchronize()
+    ref = oracle.forward_tokens(inp, np.arange(inp.T))["ids"]
+    assert (ref == np.array([2, 5, 9])).all()
+    np.testing.assert_array_equal(ids.cpu().numpy(), ref)
+
+
 def test_two_experts_take_every_token_of_a_large_batch():
     inp = synth.make_custom(777, 256, 16, 2, 128, act="bf16", w="bf16", seed=9)
     bias = np.zeros(16, np.float32)
