@@ -1,7 +1,8 @@
 // grouped_q4.cu -- grouped SwiGLU experts with 4-bit codebook weights on the tensor
-// cores: q4_decode_kernel for decode batches (an expert's tokens in chunks of <= 32; see
+// cores: q4_decode_kernel for decode batches (an expert's tokens in chunks of <= 16; see
 // its own comment below) and q4_swiglu_kernel for large batches (chunks of 128), which the
-// rest of this header describes.
+// rest of this header describes.  With packed LoRA adapters both take adapter stages after
+// a tile's K stages (see Params::lbgu).
 //
 // Weight format: element (e, r, c) of a [rows][in] matrix is codebook[code] * scale,
 // code = nibble c of row r (element 2i low, 2i+1 high nibble of byte i), one bf16
@@ -11,8 +12,8 @@
 //
 // Pipeline per CTA (one per SM):
 //  * warp 0 lane 0: TMA loads of the packed codes (128 rows x 32 bytes per matrix and
-//    64-element slab, unswizzled) and of the token rows into a "raw" ring (6 stages
-//    with room for 64 token rows, or 4 with room for 128), and
+//    64-element slab, unswizzled) and of the token rows into a "raw" ring (4 stages with
+//    room for 128 token rows), and
 //    a bulk copy of each tile's block scales (contiguous for 128 consecutive rows) into
 //    one of two per-tile scale buffers;
 //  * warps 6-13 (dequant): turn one slab of codes into bf16 weights in the 128-byte
