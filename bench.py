@@ -496,9 +496,10 @@ def measure(ctx: Ctx, workload: str, steps: int, warmup: int, *, headline: bool)
 def end_to_end(ctx, layers, dl, outs, graphs, n_copies, steps):
     """The same metric through the C ABI with HOST buffers: each step copies the step's tokens
     from pinned host memory, runs the block and copies the result back to pinned host memory.
-    Decode batches use moe_graphs_run (the library's bucketed decode graphs: zero-fill of the
-    padded rows, host->device copy, graph launch, device->host copy, all enqueued by the
-    library); larger batches copy around the block's graph replay."""
+    Decode batches use moe_graphs_run (the library's bucketed decode graphs: with pinned
+    buffers one graph launch whose first kernel reads the step's rows from pinned host memory
+    and whose last kernel writes the result there); larger batches copy around the block's
+    graph replay."""
     torch, moe, dev, stream = ctx.torch, ctx.moe, ctx.dev, ctx.stream
     from top_routing_grouped_router_gb300.device import to_device
     T, H = layers[0].T, layers[0].H

@@ -398,6 +398,10 @@ MOE_API int moe_graphs_arena_size(const moe_shape *shape, int max_bs, size_t *by
 /*
  * Captures the bucket graphs on `stream` (a non-default stream; thread-local
  * capture mode) after one eager moe_forward per bucket (outside capture).
+ * Each bucket gets two graphs: the forward alone, and the forward between a
+ * copy-in kernel (the step's rows, then zero padding rows, into the arena) and
+ * a copy-out kernel.  Should the second one fail to capture, that bucket's
+ * steps take the first route of moe_graphs_run (nothing is reported).
  *   arena          caller-owned device memory of moe_graphs_arena_size() bytes,
  *                  256-byte aligned; the graphs own it until moe_graphs_destroy.
  *   weights, q4    captured by address (their contents may change between
@@ -420,6 +424,12 @@ MOE_API int moe_graphs_bucket(const moe_graphs *graphs, int T, int32_t *bucket);
  *   x    [T][H] activations, device or host memory (cudaMemcpyDefault).
  *   out  [T][H] output, device or host memory.
  *   expert_ids_out [T][k] int32 or NULL.
+ * When x and out are both device-addressable (device memory, or pinned or
+ * registered host memory through its device address) at 16-byte aligned
+ * addresses, the step is one launch of the bucket's copy graph, its copy nodes
+ * pointed at x and out first; otherwise a zero-fill of the padding rows, a
+ * copy of x, the forward graph and a copy of out are enqueued one by one.
+ * Both routes give the same bits.  expert_ids_out is copied after either.
  * Steps on different streams must be serialised: the graphs share one arena.
  */
 MOE_API int moe_graphs_run(moe_graphs *graphs, int T, const void *x, void *out, int32_t *expert_ids_out,

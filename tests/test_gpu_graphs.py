@@ -82,3 +82,35 @@ def test_graph_step_from_pinned_host_buffers_and_replay_is_deterministic():
     with pytest.raises(moe.MoEError):
         g.run(17, xh, oh)  # larger than every bucket
     g.close()
+
+
+def test_graph_step_from_pageable_and_unaligned_buffers_equals_the_aligned_step():
+    """Buffers the device cannot address (pageable host memory) or whose address is not a
+    multiple of 16 bytes take the copy-engine route around the bucket's graph; both must give
+    the same bits as device buffers."""
+    inp = synth.make_inputs("decode8", T=16)
+    L = upload(inp)
+    g = moe.DecodeGraphs(L.shape, 16, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down)
+    T, H = 13, inp.H
+    ref = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    ref_ids = torch.empty((T, inp.k), dtype=torch.int32, device="cuda")
+    g.run(T, L.x[:T], ref, ref_ids)
+    # pageable host memory
+    xh = L.x[:T].cpu()
+    oh = torch.empty((T, H), dtype=torch.bfloat16)
+    g.run(T, xh, oh)
+    g._stream.synchronize()
+    # device buffers 2 bytes past a 16-byte boundary
+    xb = torch.empty(T * H + 1, dtype=torch.bfloat16, device="cuda")
+    ob = torch.empty(T * H + 1, dtype=torch.bfloat16, device="cuda")
+    xu, ou = xb[1:].view(T, H), ob[1:].view(T, H)
+    assert xu.data_ptr() % 16 and ou.data_ptr() % 16
+    xu.copy_(L.x[:T])
+    torch.cuda.synchronize()
+    ids = torch.empty((T, inp.k), dtype=torch.int32, device="cuda")
+    g.run(T, xu, ou, ids)
+    g._stream.synchronize()
+    assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
+    assert torch.equal(ou.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(ids, ref_ids)
+    g.close()

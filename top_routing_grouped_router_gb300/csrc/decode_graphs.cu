@@ -19,6 +19,7 @@
 #include <new>
 
 #include "moe.h"
+#include "moe_internal.cuh"
 
 namespace {
 
@@ -37,6 +38,32 @@ int bucket_list(int max_bs, int32_t *out) {
 }
 
 size_t act_bytes(const moe_shape &s) { return s.act_dtype == MOE_DT_F32 ? 4 : 2; }
+
+// A step's rows between memory the device addresses (device memory, or pinned host memory
+// seen through its device view) and the arena, 16 bytes per thread and loop step: n_copy
+// chunks from src, then n_zero zero chunks (the bucket's padding rows).  Captured at both
+// ends of a bucket's graph, with the step's buffers patched into the nodes before each
+// launch, so that a step is one graph launch instead of a copy, a launch and a copy.
+__global__ void __launch_bounds__(256) rows_copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                        size_t n_copy, size_t n_zero) {
+    moe::griddep_launch_dependents();  // the forward's first kernel may start its prologue
+    moe::griddep_wait();               // the forward's last kernel has written the output rows
+    const size_t n = n_copy + n_zero;
+    for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256)
+        dst[i] = i < n_copy ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// The device address of p (device memory, or pinned / registered host memory), or null.
+const void *device_view(const void *p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged || a.type == cudaMemoryTypeHost)
+        return a.devicePointer;
+    return nullptr;
+}
 
 struct ArenaLayout {
     size_t x, out, ids, ws, ws_bytes, total;
@@ -74,9 +101,55 @@ struct moe_graphs {
     int n;
     int32_t buckets[kMaxBuckets];
     cudaGraphExec_t exec[kMaxBuckets];
+    // per bucket, the same forward between a copy-in and a copy-out kernel node (the graph is
+    // kept: its nodes address the executable's nodes when a step patches their buffers)
+    cudaGraph_t io_graph[kMaxBuckets];
+    cudaGraphExec_t io_exec[kMaxBuckets];
+    cudaGraphNode_t io_in[kMaxBuckets], io_out[kMaxBuckets];
+    unsigned io_blocks[kMaxBuckets];
     char *arena;
     ArenaLayout L;
 };
+
+namespace {
+
+// The copy nodes of a captured io graph: the kernel nodes of rows_copy_kernel, told apart by
+// their destination (the arena's input rows for the copy-in node).
+bool find_copy_nodes(cudaGraph_t graph, const void *x_arena, cudaGraphNode_t *in, cudaGraphNode_t *out) {
+    size_t n = 0;
+    if (cudaGraphGetNodes(graph, nullptr, &n) != cudaSuccess || n == 0) return false;
+    cudaGraphNode_t *nodes = new (std::nothrow) cudaGraphNode_t[n];
+    if (!nodes) return false;
+    bool ok = cudaGraphGetNodes(graph, nodes, &n) == cudaSuccess;
+    *in = *out = nullptr;
+    for (size_t i = 0; ok && i < n; ++i) {
+        cudaGraphNodeType t;
+        if (cudaGraphNodeGetType(nodes[i], &t) != cudaSuccess || t != cudaGraphNodeTypeKernel) continue;
+        cudaKernelNodeParams kp{};
+        if (cudaGraphKernelNodeGetParams(nodes[i], &kp) != cudaSuccess || !kp.kernelParams) continue;
+        if (kp.func != reinterpret_cast<void *>(rows_copy_kernel)) continue;
+        void *dst = *static_cast<void **>(kp.kernelParams[1]);
+        (dst == x_arena ? *in : *out) = nodes[i];
+    }
+    delete[] nodes;
+    return ok && *in && *out;
+}
+
+// Points a copy node at this step's buffers.
+cudaError_t patch_copy(cudaGraphExec_t exec, cudaGraphNode_t node, unsigned blocks, const void *src, void *dst,
+                       size_t n_copy, size_t n_zero) {
+    void *args[4] = {&src, &dst, &n_copy, &n_zero};
+    cudaKernelNodeParams kp{};
+    kp.func = reinterpret_cast<void *>(rows_copy_kernel);
+    kp.gridDim = dim3(blocks);
+    kp.blockDim = dim3(256);
+    kp.sharedMemBytes = 0;
+    kp.kernelParams = args;
+    kp.extra = nullptr;
+    return cudaGraphExecKernelNodeSetParams(exec, node, &kp);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -151,9 +224,47 @@ int moe_graphs_create(const moe_shape *shape, int max_bs, const void *w_router, 
         if (rc == MOE_OK && cudaGraphInstantiate(&g->exec[made], graph, 0) != cudaSuccess) rc = MOE_ERR_LAUNCH;
         if (graph) cudaGraphDestroy(graph);
         if (rc != MOE_OK) break;
+        // the same forward between the copy kernels (each region onto itself as captured; a
+        // step patches its own buffers in before every launch)
+        const size_t row = (size_t)shape->H * act_bytes(*shape);
+        const size_t n16 = (size_t)sb.T * row / 16;
+        g->io_blocks[made] = unsigned(std::min<size_t>((n16 + 255) / 256, 64));
+        g->io_graph[made] = nullptr;
+        g->io_exec[made] = nullptr;
+        if (row % 16 == 0) {
+            cudaGraph_t io = nullptr;
+            bool ok = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+            if (ok) {
+                ok = moe::launch_pdl(rows_copy_kernel, dim3(g->io_blocks[made]), dim3(256), 0, st,
+                                reinterpret_cast<const uint4 *>(g->arena + g->L.x),
+                                reinterpret_cast<uint4 *>(g->arena + g->L.x), n16, size_t(0)) == cudaSuccess;
+                const int rf = moe_forward(&sb, g->arena + g->L.x, w_router, b_router, w_gate, w_up, w_down, q4,
+                                           g->arena + g->L.out, reinterpret_cast<int32_t *>(g->arena + g->L.ids),
+                                           nullptr, g->arena + g->L.ws, g->L.ws_bytes, stream);
+                ok = ok && moe::launch_pdl(rows_copy_kernel, dim3(g->io_blocks[made]), dim3(256), 0, st,
+                                      reinterpret_cast<const uint4 *>(g->arena + g->L.out),
+                                      reinterpret_cast<uint4 *>(g->arena + g->L.out), n16, size_t(0)) == cudaSuccess;
+                const cudaError_t e2 = cudaStreamEndCapture(st, &io);
+                ok = ok && rf == MOE_OK && e2 == cudaSuccess && io &&
+                     find_copy_nodes(io, g->arena + g->L.x, &g->io_in[made], &g->io_out[made]) &&
+                     cudaGraphInstantiate(&g->io_exec[made], io, 0) == cudaSuccess;
+            }
+            if (ok) {
+                g->io_graph[made] = io;
+            } else {
+                // steps of this bucket take the copy engine around the plain graph
+                cudaGetLastError();
+                if (io) cudaGraphDestroy(io);
+                g->io_exec[made] = nullptr;
+            }
+        }
     }
     if (rc != MOE_OK) {
-        for (int i = 0; i < made; ++i) cudaGraphExecDestroy(g->exec[i]);
+        for (int i = 0; i < made; ++i) {
+            cudaGraphExecDestroy(g->exec[i]);
+            if (g->io_exec[i]) cudaGraphExecDestroy(g->io_exec[i]);
+            if (g->io_graph[i]) cudaGraphDestroy(g->io_graph[i]);
+        }
         delete g;
         return rc;
     }
@@ -182,6 +293,23 @@ int moe_graphs_run(moe_graphs *graphs, int T, const void *x, void *out, int32_t 
     const size_t row = (size_t)s.H * act_bytes(s);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char *xs = graphs->arena + graphs->L.x;
+    // one launch when both buffers are addressable by the device and 16-byte aligned: the
+    // bucket's io graph with this step's buffers patched into its copy nodes
+    const void *xd = graphs->io_exec[i] ? device_view(x) : nullptr;
+    void *od = xd ? const_cast<void *>(device_view(out)) : nullptr;
+    if (xd && od && ((reinterpret_cast<uintptr_t>(xd) | reinterpret_cast<uintptr_t>(od)) & 15) == 0 && row % 16 == 0) {
+        const size_t n16 = (size_t)T * row / 16, pad16 = (size_t)(B - T) * row / 16;
+        if (patch_copy(graphs->io_exec[i], graphs->io_in[i], graphs->io_blocks[i], xd, xs, n16, pad16) != cudaSuccess ||
+            patch_copy(graphs->io_exec[i], graphs->io_out[i], graphs->io_blocks[i], graphs->arena + graphs->L.out, od,
+                       n16, 0) != cudaSuccess ||
+            cudaGraphLaunch(graphs->io_exec[i], st) != cudaSuccess)
+            return MOE_ERR_LAUNCH;
+        if (expert_ids_out &&
+            cudaMemcpyAsync(expert_ids_out, graphs->arena + graphs->L.ids, (size_t)T * s.k * 4, cudaMemcpyDefault,
+                            st) != cudaSuccess)
+            return MOE_ERR_LAUNCH;
+        return MOE_OK;
+    }
     if (B > T && cudaMemsetAsync(xs + (size_t)T * row, 0, (size_t)(B - T) * row, st) != cudaSuccess)
         return MOE_ERR_LAUNCH;
     if (cudaMemcpyAsync(xs, x, (size_t)T * row, cudaMemcpyDefault, st) != cudaSuccess) return MOE_ERR_LAUNCH;
@@ -197,7 +325,11 @@ int moe_graphs_run(moe_graphs *graphs, int T, const void *x, void *out, int32_t 
 
 int moe_graphs_destroy(moe_graphs *graphs) {
     if (!graphs) return MOE_ERR_NULLPTR;
-    for (int i = 0; i < graphs->n; ++i) cudaGraphExecDestroy(graphs->exec[i]);
+    for (int i = 0; i < graphs->n; ++i) {
+        cudaGraphExecDestroy(graphs->exec[i]);
+        if (graphs->io_exec[i]) cudaGraphExecDestroy(graphs->io_exec[i]);
+        if (graphs->io_graph[i]) cudaGraphDestroy(graphs->io_graph[i]);
+    }
     delete graphs;
     return MOE_OK;
 }
