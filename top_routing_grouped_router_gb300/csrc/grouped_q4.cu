@@ -1120,6 +1120,10 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
         }
         // the next tile's record (entry and its expert's offsets) is fetched while the current
         // tile streams, so that no tile starts with a chain of L2 round trips
+        // the codes are streamed (an expert's chunks of at most 16 tokens run at about the same
+        // time): marked first to evict, so that they do not push the token rows, h, their block
+        // sums and y out of L2
+        const uint64_t cpol = l2_evict_first_policy();
         int next = lo + atomicAdd(ctr, 1);
         uint32_t nentry = 0;
         int noff = 0, nme = 0;
@@ -1183,10 +1187,10 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                 const uint32_t dst = smem_u32(side + sb * kDSide);
                 mbar_arrive_expect_tx(sfb, (down ? sbytes : 2 * sbytes) + ssum);
                 if (down) {
-                    bulk_load(dst, p.ds + row0 * nblk, sbytes, sfb);
+                    bulk_load_hint(dst, p.ds + row0 * nblk, sbytes, sfb, cpol);
                 } else {
-                    bulk_load(dst, p.gs + row0 * nblk, sbytes, sfb);
-                    bulk_load(dst + kScaleBytes / 2, p.us + row0 * nblk, sbytes, sfb);
+                    bulk_load_hint(dst, p.gs + row0 * nblk, sbytes, sfb, cpol);
+                    bulk_load_hint(dst + kScaleBytes / 2, p.us + row0 * nblk, sbytes, sfb, cpol);
                 }
                 if (ssum > 0)
                     bulk_load(dst + kScaleBytes, down ? p.sh + (size_t)r0 * shs : p.sx + (size_t)r0 * sxs, ssum, sfb);
@@ -1226,9 +1230,10 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
                     continue;
                 }
                 mbar_arrive_expect_tx(fb, bytes);
-                tma_load_2d(base, down ? &tm_dc : &tm_gc, ks * (kDK / 2), wrow, fb);
-                if (kind == kQ4GateUp) tma_load_2d(base + kDCodeBytes, &tm_uc, ks * (kDK / 2), wrow, fb);
-                if (kind == kQ4DownPair) tma_load_2d(base + kDCodeBytes, &tm_dc, ks * (kDK / 2), wrow + kRows, fb);
+                tma_load_2d_hint(base, down ? &tm_dc : &tm_gc, ks * (kDK / 2), wrow, fb, cpol);
+                if (kind == kQ4GateUp) tma_load_2d_hint(base + kDCodeBytes, &tm_uc, ks * (kDK / 2), wrow, fb, cpol);
+                if (kind == kQ4DownPair)
+                    tma_load_2d_hint(base + kDCodeBytes, &tm_dc, ks * (kDK / 2), wrow + kRows, fb, cpol);
                 tma_load_3d(base + kDTok, tokmap, 0, r0, 2 * ks, fb);  // slabs 2 ks and 2 ks + 1
                 if (++r == kDRawStages) { r = 0; rp ^= 1; }
                 if (ks == kfetch && next < hi) fetch(next);
