@@ -149,4 +149,77 @@ __device__ void permute_block(const int32_t *ids, int A, int E, int32_t *counts,
         scatter_chunk(ids, a0, A, E, s, order, pos, err, a0 == 0 ? e0 : a0 == NT ? e1 : kLoadId);
 }
 
+// The same permutation of A <= 64 assignments by one warp (no block barrier), from ids in
+// shared memory; cnt and base: shared scratch of kMaxE ints each.  Lane l holds assignments
+// l and 32 + l; an assignment's rank among the earlier ones of its expert is the popcount of
+// the lower lanes with the same expert (__match_any_sync), plus, for the second half, that
+// expert's count in the first half.  Outputs are bit-identical to permute_block's.
+__device__ inline void permute_warp64(const int *s_ids, int A, int E, int32_t *counts, int32_t *offsets, int32_t *order,
+                               int32_t *pos, int32_t *active, int32_t *err, int *cnt, int *base) {
+    const int lane = threadIdx.x & 31;
+    constexpr int kPer = kMaxE / 32;  // experts per lane: lane * kPer + j
+    for (int i = lane; i < E; i += 32) cnt[i] = 0;
+    int e0 = lane < A ? s_ids[lane] : -1;
+    int e1 = 32 + lane < A ? s_ids[32 + lane] : -1;
+    if (lane < A && (e0 < 0 || e0 >= E)) {
+        record_error(err, MOE_ERR_DEVICE);
+        e0 = -1;
+    }
+    if (32 + lane < A && (e1 < 0 || e1 >= E)) {
+        record_error(err, MOE_ERR_DEVICE);
+        e1 = -1;
+    }
+    __syncwarp();
+    if (e0 >= 0) atomicAdd(&cnt[e0], 1);
+    __syncwarp();
+    const int h0 = e1 >= 0 ? cnt[e1] : 0;  // e1's assignments among the first 32
+    __syncwarp();
+    if (e1 >= 0) atomicAdd(&cnt[e1], 1);
+    __syncwarp();
+    // counts (low 16 bits) and active flags (high bits) of this lane's experts, scanned together
+    int c[kPer], mine = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int e = lane * kPer + j;
+        c[j] = e < E ? cnt[e] : 0;
+        mine += c[j] | ((c[j] > 0) << 16);
+    }
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    int x = incl - mine;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int e = lane * kPer + j;
+        if (e < E) {
+            base[e] = x & 0xFFFF;
+            counts[e] = c[j];
+            offsets[e] = x & 0xFFFF;
+            if (c[j] > 0) active[1 + (x >> 16)] = e;
+        }
+        x += c[j] | ((c[j] > 0) << 16);
+    }
+    if (lane == 0) {
+        offsets[E] = tot & 0xFFFF;
+        active[0] = tot >> 16;
+    }
+    __syncwarp();
+    const unsigned lower = (1u << lane) - 1u;
+    const unsigned p0 = __match_any_sync(0xffffffffu, e0), p1 = __match_any_sync(0xffffffffu, e1);
+    if (e0 >= 0) {
+        const int p = base[e0] + __popc(p0 & lower);
+        order[p] = lane;
+        pos[lane] = p;
+    }
+    if (e1 >= 0) {
+        const int p = base[e1] + h0 + __popc(p1 & lower);
+        order[p] = 32 + lane;
+        pos[32 + lane] = p;
+    }
+}
+
 }  // namespace moe

@@ -341,6 +341,16 @@ route_kernel(const ActT *__restrict__ x, const ActT *__restrict__ wr, const floa
         __syncthreads();
     }
     __shared__ PermuteSmem<kRThreads> ps;
+    if (one_group && a.T * a.k <= 64) {
+        // one warp permutes (no block barriers), from the ids in shared memory
+        if (w != 0) return;
+        permute_warp64(s_ids, a.T * a.k, a.E, a.counts, a.offsets, a.order, a.pos, a.active, a.err, ps.cnt,
+                       ps.base);
+        if (!a.build) return;
+        for (int i = threadIdx.x; i < a.E; i += 32) a.tb.done[i] = 0;
+        if (threadIdx.x == 0) reset_implicit_list(0, a.tb.sched, a.tb.done);
+        return;
+    }
     permute_block<kRThreads>(a.ids, a.T * a.k, a.E, a.counts, a.offsets, a.order, a.pos, a.active, a.err, ps,
                              one_group ? s_ids : nullptr);
     if (!a.build) return;
