@@ -11,9 +11,9 @@
 //
 // Top-k: one warp per token.  Lane l holds the logits of experts l, l+32, ...;
 // k rounds of a warp arg-max (ties -> lower expert index) pick the experts in
-// descending order, a (k+1)-th round gives the tie margin.  A round is two warp
-// reductions (redux.sync): the maximum of an order-preserving 32-bit key of the logits,
-// then the minimum expert index among the lanes that hold it.  The weights are
+// descending order, a (k+1)-th round gives the tie margin when the caller asks for it.  A
+// round is two warp reductions (redux.sync): the maximum of an order-preserving 32-bit key
+// of the logits, then the minimum expert index among the lanes that hold it.  The weights are
 // exp(l_j - l_max) / sum over the chosen experts (norm_topk) or over all experts,
 // which equals softmax followed by renormalisation of the chosen probabilities.
 //
@@ -217,16 +217,18 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Softmax / top-k / renormalisation of token t by one warp; with s_ids, the chosen ids
-// also go to shared memory (s_ids[j] for slot j).
-__device__ void topk_token(const float *logits, int t, int E, int k, int norm, int32_t *ids, float *w,
-                           float *margin, int *s_ids = nullptr) {
+// Softmax / top-k / renormalisation of token t by one warp, kPer logits per lane (E <= 32
+// kPer); with s_ids, the chosen ids also go to shared memory (s_ids[j] for slot j).  The
+// (k+1)-th round only measures the tie margin: it runs when the margin is asked for.
+template <int kPer>
+__device__ void topk_token_t(const float *logits, int t, int E, int k, int norm, int32_t *ids, float *w,
+                             float *margin, int *s_ids) {
     const int lane = threadIdx.x & 31;
     const float *l = logits + (size_t)t * E;
-    float v[kMaxPerLane];
-    uint32_t key[kMaxPerLane];
+    float v[kPer];
+    uint32_t key[kPer];
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < kPer; ++i) {
         const int e = lane + 32 * i;
         v[i] = (e < E) ? ldp(l + e) : -INFINITY;
         key[i] = (e < E) ? logit_key(v[i]) : 0u;
@@ -234,12 +236,12 @@ __device__ void topk_token(const float *logits, int t, int E, int k, int norm, i
     float lmax = 0.f, my_l = 0.f, last = 0.f;
     int my_id = 0;
     for (int j = 0; j <= k; ++j) {
-        if (j == k && k == E) break;
+        if (j == k && (k == E || !margin)) break;
         // this lane's best candidate: ascending e within a lane, strict '>' keeps the lower index
         uint32_t bk = 0u;
         int bi = 0;
 #pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i)
+        for (int i = 0; i < kPer; ++i)
             if (key[i] > bk) { bk = key[i]; bi = lane + 32 * i; }
         const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
         const int win = int(__reduce_min_sync(0xffffffffu, bk == mk ? uint32_t(bi) : 0xffffffffu));
@@ -248,7 +250,7 @@ __device__ void topk_token(const float *logits, int t, int E, int k, int norm, i
         if (j < k) {
             if ((win & 31) == lane) {
 #pragma unroll
-                for (int i = 0; i < kMaxPerLane; ++i)
+                for (int i = 0; i < kPer; ++i)
                     if (i == (win >> 5)) key[i] = 0u;
             }
             if (lane == j) { my_id = win; my_l = bv; }
@@ -265,7 +267,7 @@ __device__ void topk_token(const float *logits, int t, int E, int k, int norm, i
     } else {
         float z = 0.f;
 #pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i)
+        for (int i = 0; i < kPer; ++i)
             if (lane + 32 * i < E) z += expf(v[i] - lmax);
         denom = warp_sum(z);
     }
@@ -274,6 +276,13 @@ __device__ void topk_token(const float *logits, int t, int E, int k, int norm, i
         w[(size_t)t * k + lane] = ex / denom;
         if (s_ids) s_ids[lane] = my_id;
     }
+}
+__device__ void topk_token(const float *logits, int t, int E, int k, int norm, int32_t *ids, float *w,
+                           float *margin, int *s_ids = nullptr) {
+    if (E <= 128)
+        topk_token_t<4>(logits, t, E, k, norm, ids, w, margin, s_ids);
+    else
+        topk_token_t<kMaxPerLane>(logits, t, E, k, norm, ids, w, margin, s_ids);
 }
 
 struct RouteArgs {
