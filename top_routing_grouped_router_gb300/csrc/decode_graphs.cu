@@ -236,14 +236,15 @@ int moe_graphs_create(const moe_shape *shape, int max_bs, const void *w_router, 
             bool ok = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
             if (ok) {
                 ok = moe::launch_pdl(rows_copy_kernel, dim3(g->io_blocks[made]), dim3(256), 0, st,
-                                reinterpret_cast<const uint4 *>(g->arena + g->L.x),
-                                reinterpret_cast<uint4 *>(g->arena + g->L.x), n16, size_t(0)) == cudaSuccess;
+                                     reinterpret_cast<const uint4 *>(g->arena + g->L.x),
+                                     reinterpret_cast<uint4 *>(g->arena + g->L.x), n16, size_t(0)) == cudaSuccess;
                 const int rf = moe_forward(&sb, g->arena + g->L.x, w_router, b_router, w_gate, w_up, w_down, q4,
                                            g->arena + g->L.out, reinterpret_cast<int32_t *>(g->arena + g->L.ids),
                                            nullptr, g->arena + g->L.ws, g->L.ws_bytes, stream);
                 ok = ok && moe::launch_pdl(rows_copy_kernel, dim3(g->io_blocks[made]), dim3(256), 0, st,
-                                      reinterpret_cast<const uint4 *>(g->arena + g->L.out),
-                                      reinterpret_cast<uint4 *>(g->arena + g->L.out), n16, size_t(0)) == cudaSuccess;
+                                           reinterpret_cast<const uint4 *>(g->arena + g->L.out),
+                                           reinterpret_cast<uint4 *>(g->arena + g->L.out), n16,
+                                           size_t(0)) == cudaSuccess;
                 const cudaError_t e2 = cudaStreamEndCapture(st, &io);
                 ok = ok && rf == MOE_OK && e2 == cudaSuccess && io &&
                      find_copy_nodes(io, g->arena + g->L.x, &g->io_in[made], &g->io_out[made]) &&

@@ -1118,12 +1118,12 @@ q4_decode_kernel(const __grid_constant__ CUtensorMap tm_gc, const __grid_constan
             lo = ldp(p.sched + kSchedGateUp);
             ctr = p.sched + kSchedClaimDown;
         }
-        // the next tile's record (entry and its expert's offsets) is fetched while the current
-        // tile streams, so that no tile starts with a chain of L2 round trips
         // the codes are streamed (an expert's chunks of at most 16 tokens run at about the same
         // time): marked first to evict, so that they do not push the token rows, h, their block
         // sums and y out of L2
         const uint64_t cpol = l2_evict_first_policy();
+        // the next tile's record (entry and its expert's offsets) is fetched while the current
+        // tile streams, so that no tile starts with a chain of L2 round trips
         int next = lo + atomicAdd(ctr, 1);
         uint32_t nentry = 0;
         int noff = 0, nme = 0;

@@ -154,8 +154,9 @@ __device__ void permute_block(const int32_t *ids, int A, int E, int32_t *counts,
 // l and 32 + l; an assignment's rank among the earlier ones of its expert is the popcount of
 // the lower lanes with the same expert (__match_any_sync), plus, for the second half, that
 // expert's count in the first half.  Outputs are bit-identical to permute_block's.
-__device__ inline void permute_warp64(const int *s_ids, int A, int E, int32_t *counts, int32_t *offsets, int32_t *order,
-                               int32_t *pos, int32_t *active, int32_t *err, int *cnt, int *base) {
+__device__ inline void permute_warp64(const int *s_ids, int A, int E, int32_t *counts, int32_t *offsets,
+                                      int32_t *order, int32_t *pos, int32_t *active, int32_t *err, int *cnt,
+                                      int *base) {
     const int lane = threadIdx.x & 31;
     constexpr int kPer = kMaxE / 32;  // experts per lane: lane * kPer + j
     for (int i = lane; i < E; i += 32) cnt[i] = 0;
