@@ -1424,7 +1424,8 @@ q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, 
     griddep_launch_dependents();
     griddep_wait();
     if (blockIdx.x > 0) {
-        // one warp per permuted row, four 16-byte loads in flight per lane
+        // one warp per permuted row, eight 16-byte loads in flight per lane (a 4 KB row in one
+        // round trip)
         const int pr = (blockIdx.x - 1) * kPrepRowsPerBlock + int(threadIdx.x >> 5);
         const int lane = threadIdx.x & 31;
         if (pr >= T * k) return;
@@ -1435,17 +1436,17 @@ q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, 
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(bad ? 0 : a / k) * H);
         const int n = H / 8;
         // the loop runs the same number of times in every lane (the block sums shuffle)
-        for (int i0 = 0; i0 < n; i0 += 32 * 4) {
+        for (int i0 = 0; i0 < n; i0 += 32 * 8) {
             const int i = i0 + lane;
-            uint4 v[4];
+            uint4 v[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 8; ++u)
                 v[u] = (!bad && i + 32 * u < n) ? ldp16(src + i + 32 * u) : make_uint4(0, 0, 0, 0);
             if (sx) {
                 // 8 lanes hold a 64-element block (n is a multiple of 8, so a group's lanes are all
                 // in range or all out of it; out-of-range lanes hold zeros and write nothing)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 8; ++u) {
                     const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
                     float sum = 0.f;
 #pragma unroll
@@ -1458,7 +1459,7 @@ q4_prep_kernel(const uint16_t *x, const int32_t *order, const int32_t *offsets, 
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 if (i + 32 * u >= n) continue;
                 // elements e0..e7 in (v.x lo, v.x hi, v.y lo, ...): output (e0,e4),(e1,e5),(e2,e6),(e3,e7)
                 uint4 o;
