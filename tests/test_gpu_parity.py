@@ -69,6 +69,9 @@ def test_prefill_full_size_layer(layer):
     (300, 512, 8, 2, 256, "bf16", "q4", True),       # 4-bit large batch, skewed load
     (37, 512, 16, 4, 256, "bf16", "q4", False),      # 4-bit decode on CUDA cores: 8 and 4 scale blocks per row
     (64, 64, 4, 2, 64, "bf16", "q4", True),          # 4-bit decode, one scale block per row, up to 64 tokens per expert
+    (8, 256, 256, 8, 128, "bf16", "bf16", False),    # E = 256, the largest: 8 logits per lane, one-warp permutation
+    (40, 256, 160, 6, 128, "bf16", "bf16", True),    # E = 160 (ragged over the lanes), five token groups
+    (16, 256, 256, 4, 128, "bf16", "q4", False),     # 4-bit decode at E = 256
 ])
 def test_reduced_and_ragged_cases(T, H, E, k, I, act, w, zipf):
     inp = synth.make_custom(T, H, E, k, I, act=act, w=w, zipf=zipf, seed=T + E, name=f"custom{T}")
