@@ -72,6 +72,9 @@ def test_prefill_full_size_layer(layer):
     (8, 256, 256, 8, 128, "bf16", "bf16", False),    # E = 256, the largest: 8 logits per lane, one-warp permutation
     (40, 256, 160, 6, 128, "bf16", "bf16", True),    # E = 160 (ragged over the lanes), five token groups
     (16, 256, 256, 4, 128, "bf16", "q4", False),     # 4-bit decode at E = 256
+    (8, 4096, 32, 4, 256, "bf16", "bf16", False),    # H = 4096: two hidden-dim chunks per router thread, 32 down row blocks
+    (8, 256, 16, 1, 128, "bf16", "bf16", False),     # top-1 routing at decode
+    (12, 4096, 16, 2, 128, "bf16", "q4", False),     # 4-bit with 64 scale blocks per row: the generic kernels
 ])
 def test_reduced_and_ragged_cases(T, H, E, k, I, act, w, zipf):
     inp = synth.make_custom(T, H, E, k, I, act=act, w=w, zipf=zipf, seed=T + E, name=f"custom{T}")
