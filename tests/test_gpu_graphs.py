@@ -114,3 +114,26 @@ def test_graph_step_from_pageable_and_unaligned_buffers_equals_the_aligned_step(
     assert torch.equal(ou.view(torch.int16), ref.view(torch.int16))
     assert torch.equal(ids, ref_ids)
     g.close()
+
+
+def test_graph_steps_with_4bit_weights_equal_padded_forward():
+    """The bucket graphs of a 4-bit layer (prep, 4-bit decode kernel) from pinned host buffers:
+    every step equals the live rows of moe_forward on the zero-padded batch."""
+    inp = synth.make_inputs("decode48q", T=48)
+    L = upload(inp)
+    g = moe.DecodeGraphs(L.shape, 48, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4)
+    for T in (48, 5, 20):
+        B = g.bucket(T)
+        xh = L.x[:T].cpu().pin_memory()
+        oh = torch.empty((T, inp.H), dtype=torch.bfloat16).pin_memory()
+        g.run(T, xh, oh)
+        g._stream.synchronize()
+        s = moe.make_shape(B, inp.H, inp.E, inp.k, inp.I, w=L.shape.w_dtype, q_block=L.shape.q_block)
+        xp = torch.zeros((B, inp.H), dtype=torch.bfloat16, device="cuda")
+        xp[:T] = L.x[:T]
+        ref = torch.empty_like(xp)
+        ws = torch.zeros(moe.moe_workspace_size(s), dtype=torch.uint8, device="cuda")
+        moe.moe_forward(s, xp, L.w_router, L.b_router, L.w_gate, L.w_up, L.w_down, L.q4, ref, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(oh.view(torch.int16), ref[:T].cpu().view(torch.int16)), T
+    g.close()
